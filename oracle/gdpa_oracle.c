@@ -1,0 +1,365 @@
+/*
+ * gdpa_oracle.c -- plain fp64 CPU oracle for jagged attention (JFA / GDPA).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link or call
+ * this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline do.  It shares no code, header or constant with the CUDA library.
+ *
+ * What it computes (restated from "GEM Training: How Meta Doubled the
+ * Efficiency of Its LLM-Scale Ads Foundation Model", the JFA and GDPA
+ * paragraphs): attention over jagged (variable-length, unpadded) samples,
+ * written as two matrix products with an elementwise activation between
+ * them.  Softmax as the activation gives jagged flash attention (JFA);
+ * SiLU or GELU in place of softmax gives generalized dot-product attention
+ * (GDPA).  Rec-specific features: an additive attention bias, query and
+ * key/value lengths that differ per sample, and backward passes.
+ *
+ * The pages give no formula, so each step below is the plain definition:
+ *
+ *   s_ij = scale * <q_i, k_j> + bias_h(i - j)        (i < Lq_b, j < Lkv_b)
+ *   mask_ij = (j <= i) if causal else 1
+ *   softmax: p_ij = exp(s_ij - M_i) / sum_{j' masked-in} exp(s_ij' - M_i)
+ *            lse_i = M_i + log sum_j exp(s_ij - M_i)   (natural log)
+ *   GDPA:    p_ij = act(s_ij)   (no row normalisation)
+ *   masked pairs have p_ij = 0.
+ *   o_i = sum_j p_ij v_j
+ *
+ * Backward (the chain rule applied to the lines above):
+ *   dv_j  = sum_i p_ij dO_i
+ *   dp_ij = <dO_i, v_j>
+ *   softmax: ds_ij = p_ij (dp_ij - sum_j' p_ij' dp_ij')
+ *   GDPA:    ds_ij = act'(s_ij) dp_ij
+ *   dq_i  = scale * sum_j ds_ij k_j,   dk_j = scale * sum_i ds_ij q_i
+ *
+ * Readings taken where the pages are silent:
+ *   - SiLU(x) = x * sigmoid(x); GELU is the tanh form
+ *     0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+ *   - The bias is a per-head relative-position table of 2*max_rel-1 entries,
+ *     indexed by (i - j) + (max_rel - 1) with per-sample local positions; an
+ *     index outside the table is clamped to its first or last entry.
+ *   - Causal is top-left (j <= i) and needs Lq_b == Lkv_b.
+ *   - A softmax row with no masked-in key gets o = 0 and lse = -inf.
+ *
+ * Layouts: q/out/dq [Tq][H][d], k/v/dk/dv [Tkv][H][d], lse [H][Tq], bias
+ * table [H][2*max_rel-1]; offsets int32 [B+1] with o[0] = 0, non-decreasing.
+ *
+ * MXFP8 (the low-precision paragraph: "end-to-end MXFP8 blockscaled MMA"):
+ * the element format is OCP FP8 E4M3 (bias 7, max normal 448, no infinity),
+ * rounded to nearest even and saturated at +-448; each block of 32 elements
+ * shares an E8M0 scale 2^(floor(log2(amax)) - 8) as in the OCP Microscaling
+ * Formats spec v1.0 (8 = exponent of E4M3's largest normal).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_ACT_SOFTMAX = 0, ORC_ACT_SILU = 1, ORC_ACT_GELU_TANH = 2, ORC_ACT_IDENTITY = 3 };
+
+static double act_value(int act, double x) {
+  switch (act) {
+    case ORC_ACT_SILU:
+      return x / (1.0 + exp(-x));
+    case ORC_ACT_GELU_TANH: {
+      const double c = sqrt(2.0 / M_PI);
+      return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+    }
+    default:
+      return x;
+  }
+}
+
+static double act_deriv(int act, double x) {
+  switch (act) {
+    case ORC_ACT_SILU: {
+      const double sg = 1.0 / (1.0 + exp(-x));
+      return sg * (1.0 + x * (1.0 - sg));
+    }
+    case ORC_ACT_GELU_TANH: {
+      const double c = sqrt(2.0 / M_PI);
+      const double u = c * (x + 0.044715 * x * x * x);
+      const double t = tanh(u);
+      return 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * c * (1.0 + 3.0 * 0.044715 * x * x);
+    }
+    default:
+      return 1.0;
+  }
+}
+
+static double bias_at(const double* table, int max_rel, int h, long i, long j) {
+  if (table == NULL) return 0.0;
+  const long width = 2L * max_rel - 1;
+  long idx = (i - j) + (max_rel - 1);
+  if (idx < 0) idx = 0;
+  if (idx > width - 1) idx = width - 1;
+  return table[(long)h * width + idx];
+}
+
+static double dot(const double* a, const double* b, int d) {
+  double s = 0.0;
+  for (int c = 0; c < d; ++c) s += a[c] * b[c];
+  return s;
+}
+
+/* Row i of sample b, head h: fills s[j] and p[j] for j < Lkv (p = 0 when
+ * masked) and returns the row's lse (softmax) or 0.  `live[j]` marks
+ * masked-in pairs. */
+static double row_probs(const double* q, const double* k, long qrow, long kbase, long Lkv, int H,
+                        int d, int h, long i, const double* bias, int max_rel, int act, int causal,
+                        double scale, double* s, double* p, unsigned char* live) {
+  const double* qi = q + (qrow * H + h) * (long)d;
+  long n_live = 0;
+  for (long j = 0; j < Lkv; ++j) {
+    live[j] = (unsigned char)(causal ? (j <= i) : 1);
+    if (!live[j]) { s[j] = 0.0; p[j] = 0.0; continue; }
+    ++n_live;
+    const double* kj = k + ((kbase + j) * H + h) * (long)d;
+    s[j] = scale * dot(qi, kj, d) + bias_at(bias, max_rel, h, i, j);
+  }
+  if (act != ORC_ACT_SOFTMAX) {
+    for (long j = 0; j < Lkv; ++j) p[j] = live[j] ? act_value(act, s[j]) : 0.0;
+    return 0.0;
+  }
+  if (n_live == 0) {
+    for (long j = 0; j < Lkv; ++j) p[j] = 0.0;
+    return -INFINITY;
+  }
+  double m = -INFINITY;
+  for (long j = 0; j < Lkv; ++j)
+    if (live[j] && s[j] > m) m = s[j];
+  double l = 0.0;
+  for (long j = 0; j < Lkv; ++j) {
+    p[j] = live[j] ? exp(s[j] - m) : 0.0;
+    l += p[j];
+  }
+  for (long j = 0; j < Lkv; ++j) p[j] /= l;
+  return m + log(l);
+}
+
+static int check_offsets(const int32_t* o, int B) {
+  if (o[0] != 0) return 0;
+  for (int b = 0; b < B; ++b)
+    if (o[b + 1] < o[b]) return 0;
+  return 1;
+}
+
+/* Forward.  Returns 0 on success, -1 on bad arguments. */
+int oracle_fwd(const double* q, const int32_t* qo, const double* k, const double* v,
+               const int32_t* ko, int B, int H, int d, const double* bias, int max_rel, int act,
+               int causal, double scale, double* out, double* lse) {
+  if (B < 0 || H <= 0 || d <= 0 || act < 0 || act > 3) return -1;
+  if (!check_offsets(qo, B) || !check_offsets(ko, B)) return -1;
+  if (causal)
+    for (int b = 0; b < B; ++b)
+      if (qo[b + 1] - qo[b] != ko[b + 1] - ko[b]) return -1;
+  const long Tq = qo[B];
+  const long nwork = (long)B * H;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long w = 0; w < nwork; ++w) {
+    const int b = (int)(w / H), h = (int)(w % H);
+    const long Lq = qo[b + 1] - qo[b], Lkv = ko[b + 1] - ko[b];
+    const long q0 = qo[b], k0 = ko[b];
+    double* s = (double*)malloc(sizeof(double) * (size_t)(Lkv > 0 ? Lkv : 1));
+    double* p = (double*)malloc(sizeof(double) * (size_t)(Lkv > 0 ? Lkv : 1));
+    unsigned char* live = (unsigned char*)malloc((size_t)(Lkv > 0 ? Lkv : 1));
+    for (long i = 0; i < Lq; ++i) {
+      const double l = row_probs(q, k, q0 + i, k0, Lkv, H, d, h, i, bias, max_rel, act, causal,
+                                 scale, s, p, live);
+      double* oi = out + ((q0 + i) * H + h) * (long)d;
+      for (int c = 0; c < d; ++c) oi[c] = 0.0;
+      for (long j = 0; j < Lkv; ++j) {
+        if (p[j] == 0.0) continue;
+        const double* vj = v + ((k0 + j) * H + h) * (long)d;
+        for (int c = 0; c < d; ++c) oi[c] += p[j] * vj[c];
+      }
+      if (lse != NULL) lse[(long)h * Tq + q0 + i] = (act == ORC_ACT_SOFTMAX) ? l : 0.0;
+    }
+    free(s);
+    free(p);
+    free(live);
+  }
+  return 0;
+}
+
+/* Backward.  dq must be [Tq][H][d]; dk, dv [Tkv][H][d].  All three are
+ * overwritten.  Returns 0 on success, -1 on bad arguments. */
+int oracle_bwd(const double* q, const int32_t* qo, const double* k, const double* v,
+               const int32_t* ko, int B, int H, int d, const double* bias, int max_rel, int act,
+               int causal, double scale, const double* dout, double* dq, double* dk, double* dv) {
+  if (B < 0 || H <= 0 || d <= 0 || act < 0 || act > 3) return -1;
+  if (!check_offsets(qo, B) || !check_offsets(ko, B)) return -1;
+  if (causal)
+    for (int b = 0; b < B; ++b)
+      if (qo[b + 1] - qo[b] != ko[b + 1] - ko[b]) return -1;
+  const long nwork = (long)B * H;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long w = 0; w < nwork; ++w) {
+    const int b = (int)(w / H), h = (int)(w % H);
+    const long Lq = qo[b + 1] - qo[b], Lkv = ko[b + 1] - ko[b];
+    const long q0 = qo[b], k0 = ko[b];
+    const size_t n = (size_t)(Lkv > 0 ? Lkv : 1);
+    double* s = (double*)malloc(sizeof(double) * n);
+    double* p = (double*)malloc(sizeof(double) * n);
+    double* dp = (double*)malloc(sizeof(double) * n);
+    unsigned char* live = (unsigned char*)malloc(n);
+    for (long j = 0; j < Lkv; ++j) {
+      double* dkj = dk + ((k0 + j) * H + h) * (long)d;
+      double* dvj = dv + ((k0 + j) * H + h) * (long)d;
+      for (int c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
+    }
+    for (long i = 0; i < Lq; ++i) {
+      const double* qi = q + ((q0 + i) * H + h) * (long)d;
+      const double* doi = dout + ((q0 + i) * H + h) * (long)d;
+      double* dqi = dq + ((q0 + i) * H + h) * (long)d;
+      for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+      row_probs(q, k, q0 + i, k0, Lkv, H, d, h, i, bias, max_rel, act, causal, scale, s, p, live);
+      double row_dot = 0.0; /* sum_j p_ij dp_ij (softmax only) */
+      for (long j = 0; j < Lkv; ++j) {
+        const double* vj = v + ((k0 + j) * H + h) * (long)d;
+        dp[j] = live[j] ? dot(doi, vj, d) : 0.0;
+        row_dot += p[j] * dp[j];
+      }
+      for (long j = 0; j < Lkv; ++j) {
+        if (!live[j]) continue;
+        double ds;
+        if (act == ORC_ACT_SOFTMAX)
+          ds = p[j] * (dp[j] - row_dot);
+        else
+          ds = act_deriv(act, s[j]) * dp[j];
+        const double* kj = k + ((k0 + j) * H + h) * (long)d;
+        double* dkj = dk + ((k0 + j) * H + h) * (long)d;
+        double* dvj = dv + ((k0 + j) * H + h) * (long)d;
+        for (int c = 0; c < d; ++c) {
+          dqi[c] += scale * ds * kj[c];
+          dkj[c] += scale * ds * qi[c];
+          dvj[c] += p[j] * doi[c];
+        }
+      }
+    }
+    free(s);
+    free(p);
+    free(dp);
+    free(live);
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------ MXFP8 (OCP) */
+
+/* E4M3 code for x, rounded to nearest even, saturated at +-448.  NaN input
+ * gives the NaN code 0x7F.  Written from the E4M3 definition: value =
+ * (-1)^s 2^(e-7) (1 + m/8) for e in 1..15 (except e=15,m=7 which is NaN),
+ * and (-1)^s 2^-6 (m/8) for e = 0. */
+uint8_t oracle_e4m3_encode(double x) {
+  if (isnan(x)) return 0x7F;
+  const uint8_t sign = (x < 0.0 || (x == 0.0 && signbit(x))) ? 0x80 : 0x00;
+  double a = fabs(x);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+  /* find the binade: step between neighbours is 2^(e-10) for normals with
+   * unbiased exponent e >= -6, and 2^-9 in the subnormal range. */
+  int e;
+  if (a < ldexp(1.0, -6)) {
+    e = -6;
+  } else {
+    e = (int)floor(log2(a));
+    /* guard against log2 rounding near powers of two */
+    if (ldexp(1.0, e) > a) --e;
+    if (ldexp(1.0, e + 1) <= a) ++e;
+  }
+  const double step = ldexp(1.0, e - 3);
+  double n = a / step; /* exact: a and step are binary; quotient fits a double */
+  double fl = floor(n);
+  double frac = n - fl;
+  double r;
+  if (frac > 0.5)
+    r = fl + 1.0;
+  else if (frac < 0.5)
+    r = fl;
+  else
+    r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+  double val = r * step;
+  if (val > 448.0) val = 448.0;
+  /* encode val */
+  if (val == 0.0) return sign;
+  int ev;
+  if (val < ldexp(1.0, -6)) {
+    const int m = (int)(val / ldexp(1.0, -9));
+    return (uint8_t)(sign | (uint8_t)m);
+  }
+  ev = (int)floor(log2(val));
+  if (ldexp(1.0, ev) > val) --ev;
+  if (ldexp(1.0, ev + 1) <= val) ++ev;
+  const int m = (int)(val / ldexp(1.0, ev - 3)) - 8;
+  return (uint8_t)(sign | (uint8_t)((ev + 7) << 3) | (uint8_t)m);
+}
+
+double oracle_e4m3_decode(uint8_t c) {
+  const int s = c >> 7, e = (c >> 3) & 0xF, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  double v = (e == 0) ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* E8M0 code of the shared scale for a block whose largest magnitude is
+ * amax: 2^(floor(log2 amax) - 8), biased by 127, clamped to [0, 254]. */
+uint8_t oracle_e8m0_scale(double amax) {
+  if (!(amax > 0.0)) return 0;
+  int e = (int)floor(log2(amax));
+  if (ldexp(1.0, e) > amax) --e;
+  if (ldexp(1.0, e + 1) <= amax) ++e;
+  int code = e - 8 + 127;
+  if (code < 0) code = 0;
+  if (code > 254) code = 254;
+  return (uint8_t)code;
+}
+
+static void quant_block(const double* x, long stride, int n, uint8_t* codes, long cstride,
+                        uint8_t* scale) {
+  double amax = 0.0;
+  for (int t = 0; t < n; ++t) {
+    const double a = fabs(x[t * stride]);
+    if (a > amax) amax = a;
+  }
+  const uint8_t sc = oracle_e8m0_scale(amax);
+  *scale = sc;
+  const double inv = ldexp(1.0, -(sc - 127));
+  for (int t = 0; t < n; ++t) codes[t * cstride] = oracle_e4m3_encode(x[t * stride] * inv);
+}
+
+/* Q or K: blocks of 32 consecutive channels of each (token, head) row.
+ * x [T][H][d] -> codes [T][H][d], scales [T][H][d/32].  d % 32 == 0. */
+void oracle_quant_rows(const double* x, long T, int H, int d, uint8_t* codes, uint8_t* scales) {
+  const int nb = d / 32;
+#pragma omp parallel for schedule(static)
+  for (long t = 0; t < T; ++t)
+    for (int h = 0; h < H; ++h)
+      for (int g = 0; g < nb; ++g) {
+        const long base = (t * H + h) * (long)d + 32L * g;
+        quant_block(x + base, 1, 32, codes + base, 1, scales + (t * H + h) * (long)nb + g);
+      }
+}
+
+/* V: blocks of 32 consecutive tokens of one sample (the first block starts
+ * at the sample's first token; the last may be partial), per head and
+ * channel.  x [T][H][d] -> codes [T][H][d]; scales [NB][H][d] where block
+ * row r of sample b is NB-row blk_off[b] + r and blk_off[b] = sum over
+ * b' < b of ceil(L_b' / 32). */
+void oracle_quant_cols(const double* x, const int32_t* offs, int B, int H, int d, uint8_t* codes,
+                       uint8_t* scales) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int b = 0; b < B; ++b) {
+    long blk = 0;
+    for (int bb = 0; bb < b; ++bb) blk += (offs[bb + 1] - offs[bb] + 31) / 32;
+    const long L = offs[b + 1] - offs[b];
+    for (long r = 0; 32 * r < L; ++r) {
+      const long t0 = offs[b] + 32 * r;
+      const int n = (int)((L - 32 * r) < 32 ? (L - 32 * r) : 32);
+      for (int h = 0; h < H; ++h)
+        for (int c = 0; c < d; ++c) {
+          const long base = (t0 * H + h) * (long)d + c;
+          quant_block(x + base, (long)H * d, n, codes + base, (long)H * d,
+                      scales + ((blk + r) * H + h) * (long)d + c);
+        }
+    }
+  }
+}

@@ -1,0 +1,178 @@
+"""ctypes front end of the fp64 oracle (test infrastructure only).
+
+All inputs are converted to float64 numpy arrays before the call; the bf16
+values the GPU sees convert to float64 exactly, so the oracle works on the
+same numbers.  Layouts: q/out [Tq, H, d], k/v [Tkv, H, d], lse [H, Tq],
+bias table [H, 2*max_rel-1], offsets int32 [B+1].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH, ACT_IDENTITY = 0, 1, 2, 3
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdpa_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_SO = os.path.join(_OUT_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile gdpa_oracle.c into a shared object (gcc, OpenMP, no fast-math)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-D_DEFAULT_SOURCE",
+               _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int32)
+        up = ctypes.POINTER(ctypes.c_uint8)
+        I, D = ctypes.c_int, ctypes.c_double
+        lib.oracle_fwd.argtypes = [dp, ip, dp, dp, ip, I, I, I, dp, I, I, I, D, dp, dp]
+        lib.oracle_fwd.restype = I
+        lib.oracle_bwd.argtypes = [dp, ip, dp, dp, ip, I, I, I, dp, I, I, I, D, dp, dp, dp, dp]
+        lib.oracle_bwd.restype = I
+        lib.oracle_e4m3_encode.argtypes = [D]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = D
+        lib.oracle_e8m0_scale.argtypes = [D]
+        lib.oracle_e8m0_scale.restype = ctypes.c_uint8
+        lib.oracle_quant_rows.argtypes = [dp, ctypes.c_long, I, I, up, up]
+        lib.oracle_quant_rows.restype = None
+        lib.oracle_quant_cols.argtypes = [dp, ip, I, I, I, up, up]
+        lib.oracle_quant_cols.restype = None
+        _lib = lib
+        return lib
+
+
+def _f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # torch tensor
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _i32(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _p(a: np.ndarray, ct):
+    return a.ctypes.data_as(ctypes.POINTER(ct))
+
+
+def _bias_arg(bias, H, max_rel):
+    if bias is None:
+        return None, ctypes.POINTER(ctypes.c_double)()
+    b = _f64(bias)
+    assert b.shape == (H, 2 * max_rel - 1), b.shape
+    return b, _p(b, ctypes.c_double)
+
+
+def fwd(q, q_offsets, k, v, kv_offsets, *, act: int, causal: bool = False, scale: float,
+        bias=None, max_rel: int = 0):
+    """Forward pass.  Returns (out [Tq,H,d] float64, lse [H,Tq] float64).
+
+    lse is the natural-log row logsumexp for softmax (-inf for a row with no
+    key) and 0 for the GDPA activations."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    qo, ko = _i32(q_offsets), _i32(kv_offsets)
+    Tq, H, d = q.shape
+    B = len(qo) - 1
+    assert k.shape[1:] == (H, d) and v.shape == k.shape
+    assert qo[-1] == Tq and ko[-1] == k.shape[0]
+    out = np.zeros((Tq, H, d), dtype=np.float64)
+    lse = np.zeros((H, Tq), dtype=np.float64)
+    keep, bp = _bias_arg(bias, H, max_rel)
+    rc = _load().oracle_fwd(_p(q, ctypes.c_double), _p(qo, ctypes.c_int32),
+                            _p(k, ctypes.c_double), _p(v, ctypes.c_double),
+                            _p(ko, ctypes.c_int32), B, H, d, bp, int(max_rel), int(act),
+                            int(bool(causal)), float(scale), _p(out, ctypes.c_double),
+                            _p(lse, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle_fwd rejected its arguments")
+    del keep
+    return out, lse
+
+
+def bwd(q, q_offsets, k, v, kv_offsets, dout, *, act: int, causal: bool = False, scale: float,
+        bias=None, max_rel: int = 0):
+    """Backward pass.  Returns (dq, dk, dv) as float64 arrays."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
+    qo, ko = _i32(q_offsets), _i32(kv_offsets)
+    Tq, H, d = q.shape
+    B = len(qo) - 1
+    assert do.shape == q.shape
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    keep, bp = _bias_arg(bias, H, max_rel)
+    rc = _load().oracle_bwd(_p(q, ctypes.c_double), _p(qo, ctypes.c_int32),
+                            _p(k, ctypes.c_double), _p(v, ctypes.c_double),
+                            _p(ko, ctypes.c_int32), B, H, d, bp, int(max_rel), int(act),
+                            int(bool(causal)), float(scale), _p(do, ctypes.c_double),
+                            _p(dq, ctypes.c_double), _p(dk, ctypes.c_double),
+                            _p(dv, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle_bwd rejected its arguments")
+    del keep
+    return dq, dk, dv
+
+
+def e4m3_encode(x: float) -> int:
+    return int(_load().oracle_e4m3_encode(float(x)))
+
+
+def e4m3_decode(c: int) -> float:
+    return float(_load().oracle_e4m3_decode(int(c) & 0xFF))
+
+
+def e8m0_scale(amax: float) -> int:
+    return int(_load().oracle_e8m0_scale(float(amax)))
+
+
+def quant_rows(x):
+    """MXFP8 along the channel axis: x [T,H,d] -> (codes u8 [T,H,d], scales u8 [T,H,d/32])."""
+    x = _f64(x)
+    T, H, d = x.shape
+    assert d % 32 == 0
+    codes = np.zeros((T, H, d), dtype=np.uint8)
+    scales = np.zeros((T, H, d // 32), dtype=np.uint8)
+    _load().oracle_quant_rows(_p(x, ctypes.c_double), T, H, d, _p(codes, ctypes.c_uint8),
+                              _p(scales, ctypes.c_uint8))
+    return codes, scales
+
+
+def quant_cols(x, offsets):
+    """MXFP8 along tokens, in 32-token blocks aligned to each sample's start.
+
+    x [T,H,d] -> (codes u8 [T,H,d], scales u8 [NB,H,d]) with NB = sum ceil(L_b/32)."""
+    x = _f64(x)
+    o = _i32(offsets)
+    T, H, d = x.shape
+    B = len(o) - 1
+    nb = int(sum((int(o[b + 1]) - int(o[b]) + 31) // 32 for b in range(B)))
+    codes = np.zeros((T, H, d), dtype=np.uint8)
+    scales = np.zeros((max(nb, 0), H, d), dtype=np.uint8)
+    _load().oracle_quant_cols(_p(x, ctypes.c_double), _p(o, ctypes.c_int32), B, H, d,
+                              _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_uint8))
+    return codes, scales

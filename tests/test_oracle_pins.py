@@ -1,0 +1,420 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+Each pin checks the oracle against an independent fact: a hand-derived worked
+example, a closed form, a library routine (torch's fp64 SDPA, logsumexp,
+SiLU/GELU, float8 conversion), an algebraic identity evaluated in a different
+order, an invariant, or central finite differences of the oracle's own
+forward (which pins every backward formula).  They are chosen so that a
+dropped term, a wrong sign or index, or a transposed operand in the oracle
+fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import ACT_GELU_TANH, ACT_IDENTITY, ACT_SILU, ACT_SOFTMAX
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+ACT_NAMES = {ACT_SOFTMAX: "softmax", ACT_SILU: "silu", ACT_GELU_TANH: "gelu", ACT_IDENTITY: "identity"}
+
+
+def _bf16_randn(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(*shape, generator=g) * scale).to(torch.bfloat16).double().numpy()
+
+
+def _offsets(lengths):
+    o = np.zeros(len(lengths) + 1, dtype=np.int32)
+    o[1:] = np.cumsum(lengths)
+    return o
+
+
+def _relpos_mask(table_h, Lq, Lkv, max_rel):
+    i = np.arange(Lq)[:, None]
+    j = np.arange(Lkv)[None, :]
+    idx = np.clip(i - j + max_rel - 1, 0, 2 * max_rel - 2)
+    return table_h[idx]
+
+
+# --------------------------------------------------------------- golden cases
+def _expr(s):
+    return eval(s, {"log": math.log, "sqrt": math.sqrt})  # literal arithmetic from the fixture
+
+
+def _golden_cases():
+    with open(os.path.join(GOLDEN, "hand_examples.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c["name"])
+def test_hand_worked_examples(oracle_mod, case):
+    q = np.array(case["q"], dtype=np.float64)
+    k = np.array(_expr(case["k_expr"]) if "k_expr" in case else case["k"], dtype=np.float64)
+    v = np.array(case["v"], dtype=np.float64)
+    qo, ko = _offsets(case["lq"]), _offsets(case["lkv"])
+    bias = np.array(case["bias_table"]) if "bias_table" in case else None
+    out, lse = oracle_mod.fwd(q, qo, k, v, ko, act=case["act"], causal=case["causal"],
+                              scale=_expr(case["scale_expr"]), bias=bias,
+                              max_rel=case.get("max_rel", 0))
+    exp_out = np.array(_expr(case["out_expr"]) if "out_expr" in case else case["out"])
+    np.testing.assert_allclose(out, exp_out, rtol=1e-13, atol=1e-13)
+    if "lse" in case:
+        exp_lse = np.array([[float(x) for x in row] for row in case["lse"]])
+        np.testing.assert_allclose(lse, exp_lse, rtol=1e-13, atol=1e-13)
+
+
+# --------------------------------------------------------------- library pins
+@pytest.mark.parametrize("with_bias", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+def test_softmax_matches_torch_sdpa(oracle_mod, with_bias, causal):
+    H, d, max_rel = 2, 16, 8
+    lq = [5, 0, 17, 1, 12]
+    lkv = lq if causal else [9, 3, 12, 0, 20]
+    q = _bf16_randn((sum(lq), H, d), 1)
+    k = _bf16_randn((sum(lkv), H, d), 2)
+    v = _bf16_randn((sum(lkv), H, d), 3)
+    table = np.random.default_rng(4).normal(0, 0.5, size=(H, 2 * max_rel - 1)) if with_bias else None
+    qo, ko = _offsets(lq), _offsets(lkv)
+    scale = 1 / math.sqrt(d)
+    out, lse = oracle_mod.fwd(q, qo, k, v, ko, act=ACT_SOFTMAX, causal=causal, scale=scale,
+                              bias=table, max_rel=max_rel)
+    for b in range(len(lq)):
+        Lq, Lkv = lq[b], lkv[b]
+        if Lq == 0:
+            continue
+        qb = torch.from_numpy(q[qo[b]:qo[b + 1]]).permute(1, 0, 2)[None]
+        kb = torch.from_numpy(k[ko[b]:ko[b + 1]]).permute(1, 0, 2)[None]
+        vb = torch.from_numpy(v[ko[b]:ko[b + 1]]).permute(1, 0, 2)[None]
+        if Lkv == 0:
+            np.testing.assert_array_equal(out[qo[b]:qo[b + 1]], 0.0)
+            assert np.all(np.isneginf(lse[:, qo[b]:qo[b + 1]]))
+            continue
+        mask = np.zeros((H, Lq, Lkv))
+        if with_bias:
+            mask += np.stack([_relpos_mask(table[h], Lq, Lkv, max_rel) for h in range(H)])
+        if causal:
+            mask += np.where(np.arange(Lkv)[None, :] > np.arange(Lq)[:, None], -np.inf, 0.0)[None]
+        m = torch.from_numpy(mask)[None]
+        ref = F.scaled_dot_product_attention(qb, kb, vb, attn_mask=m, scale=scale)
+        ref = ref[0].permute(1, 0, 2).numpy()
+        np.testing.assert_allclose(out[qo[b]:qo[b + 1]], ref, rtol=1e-11, atol=1e-12)
+        logits = scale * torch.einsum("bhqd,bhkd->bhqk", qb, kb) + m
+        ref_lse = torch.logsumexp(logits, dim=-1)[0].numpy()
+        np.testing.assert_allclose(lse[:, qo[b]:qo[b + 1]], ref_lse, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("act", [ACT_SILU, ACT_GELU_TANH, ACT_IDENTITY])
+@pytest.mark.parametrize("with_bias", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+def test_gdpa_activation_via_onehot_values(oracle_mod, act, with_bias, causal):
+    """With v_j = e_j (one-hot rows) the output row is the activated score row,
+    so the oracle's activation and masking meet torch's fp64 SiLU/GELU."""
+    H, d, max_rel = 2, 32, 6
+    lq = [7, 3, 20] if not causal else [7, 3, 20]
+    lkv = [11, 1, 32] if not causal else lq
+    q = _bf16_randn((sum(lq), H, d), 5)
+    k = _bf16_randn((sum(lkv), H, d), 6, scale=0.7)
+    v = np.zeros((sum(lkv), H, d))
+    qo, ko = _offsets(lq), _offsets(lkv)
+    for b in range(len(lq)):
+        for j in range(lkv[b]):
+            v[ko[b] + j, :, j] = 1.0
+    table = np.random.default_rng(7).normal(0, 0.3, size=(H, 2 * max_rel - 1)) if with_bias else None
+    scale = 0.37
+    out, _ = oracle_mod.fwd(q, qo, k, v, ko, act=act, causal=causal, scale=scale, bias=table,
+                            max_rel=max_rel)
+    tact = {ACT_SILU: F.silu, ACT_GELU_TANH: lambda x: F.gelu(x, approximate="tanh"),
+            ACT_IDENTITY: lambda x: x}[act]
+    for b in range(len(lq)):
+        qb = torch.from_numpy(q[qo[b]:qo[b + 1]])
+        kb = torch.from_numpy(k[ko[b]:ko[b + 1]])
+        s = scale * torch.einsum("qhd,khd->hqk", qb, kb)
+        if with_bias:
+            s = s + torch.from_numpy(np.stack([_relpos_mask(table[h], lq[b], lkv[b], max_rel)
+                                               for h in range(H)]))
+        p = tact(s)
+        if causal:
+            p = p * (torch.arange(lkv[b])[None, :] <= torch.arange(lq[b])[:, None])
+        got = out[qo[b]:qo[b + 1], :, :lkv[b]].transpose(1, 0, 2)
+        np.testing.assert_allclose(got, p.numpy(), rtol=1e-12, atol=1e-13)
+        np.testing.assert_array_equal(out[qo[b]:qo[b + 1], :, lkv[b]:], 0.0)
+
+
+def test_identity_activation_associativity(oracle_mod):
+    """Identity activation: O = (scale Q K^T) V must equal scale Q (K^T V)."""
+    H, d = 3, 24
+    lq, lkv = [9, 4, 30], [14, 25, 6]
+    q = _bf16_randn((sum(lq), H, d), 8)
+    k = _bf16_randn((sum(lkv), H, d), 9)
+    v = _bf16_randn((sum(lkv), H, d), 10)
+    qo, ko = _offsets(lq), _offsets(lkv)
+    out, _ = oracle_mod.fwd(q, qo, k, v, ko, act=ACT_IDENTITY, scale=0.125)
+    for b in range(3):
+        for h in range(H):
+            Q = q[qo[b]:qo[b + 1], h]
+            K = k[ko[b]:ko[b + 1], h]
+            V = v[ko[b]:ko[b + 1], h]
+            ref = 0.125 * (Q @ (K.T @ V))
+            np.testing.assert_allclose(out[qo[b]:qo[b + 1], h], ref, rtol=1e-12, atol=1e-11)
+
+
+# --------------------------------------------------------------- closed forms
+@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH])
+def test_zero_keys(oracle_mod, act):
+    """K = 0, no bias: softmax gives the mean of V; SiLU/GELU give act(0) = 0."""
+    H, d = 2, 8
+    lq, lkv = [3, 5], [4, 7]
+    q = _bf16_randn((8, H, d), 11)
+    k = np.zeros((11, H, d))
+    v = _bf16_randn((11, H, d), 12)
+    qo, ko = _offsets(lq), _offsets(lkv)
+    out, lse = oracle_mod.fwd(q, qo, k, v, ko, act=act, scale=0.3)
+    for b in range(2):
+        if act == ACT_SOFTMAX:
+            mean = v[ko[b]:ko[b + 1]].mean(axis=0)
+            np.testing.assert_allclose(out[qo[b]:qo[b + 1]], np.broadcast_to(mean, (lq[b], H, d)),
+                                       rtol=1e-13, atol=1e-14)
+            np.testing.assert_allclose(lse[:, qo[b]:qo[b + 1]], math.log(lkv[b]), rtol=1e-14)
+        else:
+            np.testing.assert_array_equal(out[qo[b]:qo[b + 1]], 0.0)
+
+
+def test_single_key_and_constant_values(oracle_mod):
+    H, d = 2, 8
+    q = _bf16_randn((6, H, d), 13)
+    k = _bf16_randn((6, H, d), 14)
+    v = _bf16_randn((6, H, d), 15)
+    # one key per sample: softmax output is that key's value row exactly
+    out, _ = oracle_mod.fwd(q, _offsets([4, 2]), k[:2], v[:2], _offsets([1, 1]), act=ACT_SOFTMAX,
+                            scale=1.0)
+    np.testing.assert_array_equal(out[:4], np.broadcast_to(v[0], (4, H, d)))
+    np.testing.assert_array_equal(out[4:], np.broadcast_to(v[1], (2, H, d)))
+    # constant value rows: softmax output equals that row for any scores
+    vc = np.broadcast_to(v[3], (6, H, d)).copy()
+    out, _ = oracle_mod.fwd(q, _offsets([6]), k, vc, _offsets([6]), act=ACT_SOFTMAX, scale=2.0)
+    np.testing.assert_allclose(out, vc, rtol=1e-13, atol=1e-14)
+    # scale 0: uniform weights
+    out, lse = oracle_mod.fwd(q, _offsets([6]), k, v, _offsets([6]), act=ACT_SOFTMAX, scale=0.0)
+    np.testing.assert_allclose(out, np.broadcast_to(v.mean(0), (6, H, d)), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(lse, math.log(6), rtol=1e-14)
+
+
+def test_causal_closed_form(oracle_mod):
+    """K = 0 and one-hot V under the causal mask: o_ij = 1/(i+1) for j <= i."""
+    L, H, d = 9, 1, 16
+    q = _bf16_randn((L, H, d), 16)
+    k = np.zeros((L, H, d))
+    v = np.zeros((L, H, d))
+    for j in range(L):
+        v[j, 0, j] = 1.0
+    out, lse = oracle_mod.fwd(q, _offsets([L]), k, v, _offsets([L]), act=ACT_SOFTMAX, causal=True,
+                              scale=1.0)
+    ref = np.tril(np.ones((L, L))) / np.arange(1, L + 1)[:, None]
+    np.testing.assert_allclose(out[:, 0, :L], ref, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(lse[0], np.log(np.arange(1, L + 1)), rtol=1e-14, atol=1e-15)
+
+
+def test_relpos_index_closed_form(oracle_mod):
+    """q = k = 0, identity act, one-hot V: o_ij = table[clamp(i - j + max_rel - 1)]."""
+    max_rel, L = 5, 12
+    table = np.arange(2 * max_rel - 1, dtype=np.float64)[None, :] * 10.0 + 1.0
+    q = np.zeros((L, 1, L))
+    k = np.zeros((L, 1, L))
+    v = np.eye(L)[:, None, :]
+    out, _ = oracle_mod.fwd(q, _offsets([L]), k, v, _offsets([L]), act=ACT_IDENTITY, scale=1.0,
+                            bias=table, max_rel=max_rel)
+    for i in range(L):
+        for j in range(L):
+            idx = min(max(i - j + max_rel - 1, 0), 2 * max_rel - 2)
+            assert out[i, 0, j] == 10.0 * idx + 1.0
+
+
+def test_softmax_rows_sum_to_one(oracle_mod):
+    H, d = 2, 8
+    lq, lkv = [5, 9, 2], [7, 3, 16]
+    q = _bf16_randn((sum(lq), H, d), 17, scale=3.0)
+    k = _bf16_randn((sum(lkv), H, d), 18, scale=3.0)
+    v = np.ones((sum(lkv), H, d))
+    table = np.random.default_rng(0).normal(size=(H, 15))
+    out, _ = oracle_mod.fwd(q, _offsets(lq), k, v, _offsets(lkv), act=ACT_SOFTMAX, scale=0.5,
+                            bias=table, max_rel=8)
+    np.testing.assert_allclose(out, 1.0, rtol=1e-13)
+
+
+# --------------------------------------------------------------- invariants
+@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_SILU])
+def test_sample_permutation_and_per_sample_equality(oracle_mod, act):
+    H, d = 2, 16
+    lq, lkv = [6, 0, 13, 3], [4, 9, 0, 11]
+    q = _bf16_randn((sum(lq), H, d), 19)
+    k = _bf16_randn((sum(lkv), H, d), 20)
+    v = _bf16_randn((sum(lkv), H, d), 21)
+    qo, ko = _offsets(lq), _offsets(lkv)
+    out, lse = oracle_mod.fwd(q, qo, k, v, ko, act=act, scale=0.25)
+    # each sample alone equals its slice of the jagged result
+    for b in range(4):
+        ob, lb = oracle_mod.fwd(q[qo[b]:qo[b + 1]], _offsets([lq[b]]), k[ko[b]:ko[b + 1]],
+                                v[ko[b]:ko[b + 1]], _offsets([lkv[b]]), act=act, scale=0.25)
+        np.testing.assert_array_equal(out[qo[b]:qo[b + 1]], ob)
+        np.testing.assert_array_equal(lse[:, qo[b]:qo[b + 1]], lb)
+    # permuting samples permutes the outputs
+    perm = [2, 0, 3, 1]
+    qp = np.concatenate([q[qo[b]:qo[b + 1]] for b in perm])
+    kp = np.concatenate([k[ko[b]:ko[b + 1]] for b in perm])
+    vp = np.concatenate([v[ko[b]:ko[b + 1]] for b in perm])
+    op, _ = oracle_mod.fwd(qp, _offsets([lq[b] for b in perm]), kp, vp,
+                           _offsets([lkv[b] for b in perm]), act=act, scale=0.25)
+    np.testing.assert_array_equal(op, np.concatenate([out[qo[b]:qo[b + 1]] for b in perm]))
+
+
+def test_zero_length_writes_nothing(oracle_mod):
+    """A sample with no keys (GDPA) gives zero rows; samples with no queries
+    leave every other row untouched."""
+    H, d = 1, 8
+    lq, lkv = [3, 0, 2], [0, 5, 4]
+    q = _bf16_randn((5, H, d), 22)
+    k = _bf16_randn((9, H, d), 23)
+    v = _bf16_randn((9, H, d), 24)
+    out, _ = oracle_mod.fwd(q, _offsets(lq), k, v, _offsets(lkv), act=ACT_SILU, scale=0.3)
+    np.testing.assert_array_equal(out[:3], 0.0)
+    o2, _ = oracle_mod.fwd(q[3:], _offsets([2]), k[5:], v[5:], _offsets([4]), act=ACT_SILU,
+                           scale=0.3)
+    np.testing.assert_array_equal(out[3:], o2)
+
+
+def test_rejects_bad_offsets(oracle_mod):
+    q = np.zeros((3, 1, 4))
+    with pytest.raises(ValueError):
+        oracle_mod.fwd(q, np.array([0, 2, 1, 3], dtype=np.int32), q, q,
+                       np.array([0, 1, 2, 3], dtype=np.int32), act=0, scale=1.0)
+    with pytest.raises(ValueError):  # causal needs equal lengths
+        oracle_mod.fwd(q, np.array([0, 1, 3], dtype=np.int32), q, q,
+                       np.array([0, 2, 3], dtype=np.int32), act=0, causal=True, scale=1.0)
+
+
+# --------------------------------------------------------------- backward (finite differences)
+@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH, ACT_IDENTITY])
+@pytest.mark.parametrize("variant", ["plain", "bias", "causal_bias"])
+def test_backward_matches_central_differences(oracle_mod, act, variant):
+    H, d, max_rel = 2, 6, 3
+    causal = variant == "causal_bias"
+    lq = [3, 4, 0]
+    lkv = lq if causal else [5, 2, 3]
+    rng = np.random.default_rng(100 + act)
+    q = rng.normal(size=(sum(lq), H, d))
+    k = rng.normal(size=(sum(lkv), H, d))
+    v = rng.normal(size=(sum(lkv), H, d))
+    do = rng.normal(size=(sum(lq), H, d))
+    table = rng.normal(0, 0.5, size=(H, 2 * max_rel - 1)) if variant != "plain" else None
+    qo, ko = _offsets(lq), _offsets(lkv)
+    kw = dict(act=act, causal=causal, scale=0.45, bias=table, max_rel=max_rel)
+    dq, dk, dv = oracle_mod.bwd(q, qo, k, v, ko, do, **kw)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle_mod.fwd(qq, qo, kk, vv, ko, **kw)
+        return float(np.sum(o * do))
+
+    h = 1e-5
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp = x.copy(); xp[idx] += h
+            xm = x.copy(); xm[idx] -= h
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        err = np.abs(num - g).max() / max(1.0, np.abs(num).max())
+        assert err < 1e-7, f"d{name}: {err}"
+
+
+# --------------------------------------------------------------- MXFP8 (OCP)
+def test_e4m3_spec_values(oracle_mod):
+    enc = oracle_mod.e4m3_encode
+    assert enc(0.0) == 0x00
+    assert enc(1.0) == 0x38            # exponent field 7, mantissa 0
+    assert enc(448.0) == 0x7E          # largest normal S.1111.110
+    assert enc(-448.0) == 0xFE
+    assert enc(2.0 ** -6) == 0x08      # smallest normal
+    assert enc(2.0 ** -9) == 0x01      # smallest subnormal
+    assert enc(1.0 + 1 / 16) == 0x38   # tie between 1 and 1.125 -> even (1.0)
+    assert enc(1.0 + 3 / 16) == 0x3A   # tie between 1.125 and 1.25 -> even (1.25)
+    assert enc(1000.0) == 0x7E         # saturates
+    assert enc(-1e30) == 0xFE
+    assert enc(float("nan")) == 0x7F
+    assert enc(2.0 ** -11) == 0x00     # below half the smallest subnormal rounds to 0
+    for c in range(256):
+        if (c & 0x7F) == 0x7F:
+            assert math.isnan(oracle_mod.e4m3_decode(c))
+        elif c != 0x80:
+            assert enc(oracle_mod.e4m3_decode(c)) == c
+
+
+def test_e4m3_matches_torch_float8(oracle_mod):
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.normal(0, 50, 4000), rng.normal(0, 0.01, 2000),
+                        rng.uniform(-448, 448, 2000), np.linspace(-448, 448, 4097)])
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle_mod.e4m3_encode(t) for t in x], dtype=np.uint8)
+    # torch keeps the sign of a value that rounds to zero; so does the oracle
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_e8m0_scale_closed_forms(oracle_mod):
+    s = oracle_mod.e8m0_scale
+    assert s(1.0) == 127 - 8
+    assert s(3.0) == 127 + 1 - 8
+    assert s(448.0) == 127
+    assert s(511.9) == 127 + 8 - 8
+    assert s(512.0) == 127 + 9 - 8
+    assert s(2.0 ** -3) == 127 - 3 - 8
+    assert s(0.0) == 0
+    assert s(2.0 ** -140) == 0
+    assert s(2.0 ** 200) == 254
+
+
+def test_quant_rows_roundtrip_and_blocks(oracle_mod):
+    T, H, d = 5, 2, 64
+    x = _bf16_randn((T, H, d), 30) * np.exp2(np.arange(d) // 32)[None, None, :] * 3
+    codes, scales = oracle_mod.quant_rows(x)
+    assert scales.shape == (T, H, 2)
+    dec = np.vectorize(oracle_mod.e4m3_decode)(codes)
+    X = np.exp2(scales.astype(np.float64) - 127).repeat(32, axis=2)
+    xr = dec * X
+    # E4M3 keeps 3 mantissa bits: relative error <= 2^-4 on normals, plus half a
+    # subnormal step.  The scale 2^(floor(log2 amax) - 8) maps a block's largest
+    # magnitude into [256, 512), so scaled values above 448 saturate to 448.
+    sat = np.abs(x) / X > 448.0
+    np.testing.assert_array_equal(np.abs(xr[sat]), 448.0 * X[sat])
+    ok = np.abs(xr - x) <= 2.0 ** -4 * np.abs(x) + 2.0 ** -10 * X
+    assert np.all(ok | sat)
+    amax = np.abs(x).reshape(T, H, 2, 32).max(-1)
+    np.testing.assert_array_equal(scales, np.floor(np.log2(amax)).astype(int) - 8 + 127)
+
+
+def test_quant_cols_sample_aligned_blocks(oracle_mod):
+    """V blocks start at each sample's first token: sample b is filled with
+    +-2^b so every one of its blocks must carry scale code b - 8 + 127, and
+    a block straddling two samples would show the wrong code."""
+    lengths = [5, 40, 33, 0, 64]
+    H, d = 2, 4
+    o = _offsets(lengths)
+    x = np.zeros((sum(lengths), H, d))
+    rng = np.random.default_rng(1)
+    for b, L in enumerate(lengths):
+        x[o[b]:o[b + 1]] = rng.choice([-1.0, 1.0], size=(L, H, d)) * 2.0 ** b
+    codes, scales = oracle_mod.quant_cols(x, o)
+    nb = [(L + 31) // 32 for L in lengths]
+    assert scales.shape[0] == sum(nb)
+    r = 0
+    for b in range(len(lengths)):
+        for _ in range(nb[b]):
+            np.testing.assert_array_equal(scales[r], b - 8 + 127)
+            r += 1
+    dec = np.vectorize(oracle_mod.e4m3_decode)(codes)
+    # every element is +-2^b = +-2^8 * 2^(b-8): code 256 -> 0x78 with sign
+    np.testing.assert_array_equal(np.abs(dec), 256.0)

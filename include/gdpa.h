@@ -1,0 +1,131 @@
+/*
+ * gdpa.h -- C ABI of the GB300 (sm_103a) jagged attention library.
+ *
+ * The operation: attention over jagged (variable-length, unpadded) samples,
+ * i.e. two matrix products with an elementwise activation between them.
+ * Softmax as the activation is jagged flash attention (JFA); SiLU or GELU in
+ * place of softmax is generalized dot-product attention (GDPA), one kernel
+ * for self-attention, PMA and cross-attention.  Source: "GEM Training: How
+ * Meta Doubled the Efficiency of Its LLM-Scale Ads Foundation Model", JFA
+ * paragraph (jagged tensors, custom attention biases, asymmetric query /
+ * key-value lengths, backward passes) and GDPA paragraph ("two matrix
+ * multiplications with an element-wise activation in between").
+ *
+ * For sample b with Lq_b = q_offsets[b+1]-q_offsets[b] query rows and
+ * Lkv_b = kv_offsets[b+1]-kv_offsets[b] key/value rows, head h, local row i
+ * and local key j (mask: j <= i when causal, else all):
+ *     s_ij  = scale * <q_i, k_j> + bias_h(i - j)
+ *     p_ij  = softmax_j(s_ij)       (GDPA_ACT_SOFTMAX, masked entries excluded)
+ *           = act(s_ij)             (SiLU, GELU-tanh, identity; no normalisation)
+ *     out_i = sum_j p_ij v_j
+ * SiLU(x) = x sigmoid(x); GELU-tanh(x) = 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))).
+ * A softmax row with no key gets out = 0 and lse = -inf; GDPA rows with no
+ * key get 0.  Samples with no query rows write nothing.
+ *
+ * Conventions shared by every call:
+ *  - Layouts: q, out, dout, dq: [Tq][H][d] bf16 row-major ("THD"); k, v, dk,
+ *    dv: [Tkv][H][d] bf16; lse: [H][Tq] fp32; offsets: int32 [B+1] with
+ *    offsets[0] = 0, non-decreasing, offsets[B] = Tq (or Tkv).  All tensors
+ *    and offsets live in device memory; B, H, d, Tq, Tkv are host scalars,
+ *    so no call reads anything back from the device.
+ *  - d must be 64 or 128; H <= 256.  Tensor base addresses must be 16-byte
+ *    aligned.
+ *  - Ownership: the caller owns every buffer, including the workspace (size
+ *    from the matching *_workspace_size query).  Calls enqueue work on
+ *    `stream` (a cudaStream_t; NULL = legacy default stream) and return
+ *    without synchronising.  They do not allocate device memory.
+ *  - Errors: argument errors detectable on the host return immediately and
+ *    launch nothing.  Errors only the device can see (malformed offsets,
+ *    causal with Lq_b != Lkv_b, a pipeline wait that timed out) set a device
+ *    status word; gdpa_get_device_status() synchronises the stream, returns
+ *    it and clears it.  After such an error the outputs are undefined, but
+ *    every write stays inside the caller's buffers.
+ */
+#ifndef GDPA_H_
+#define GDPA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDPA_ACT_SOFTMAX = 0,   /* JFA */
+  GDPA_ACT_SILU = 1,      /* GDPA */
+  GDPA_ACT_GELU_TANH = 2, /* GDPA */
+  GDPA_ACT_IDENTITY = 3   /* GDPA, linear attention; useful for testing */
+} gdpa_act;
+
+typedef enum { GDPA_BIAS_NONE = 0, GDPA_BIAS_RELPOS = 1 } gdpa_bias_kind;
+
+/* Additive attention bias ("custom attention biases", JFA paragraph).
+ * GDPA_BIAS_RELPOS: per-head relative-position table, fp32 device memory
+ * [H][2*max_rel-1]; bias_h(i-j) = table[h][clamp(i-j+max_rel-1, 0, 2*max_rel-2)]
+ * with per-sample local positions i, j.  1 <= max_rel <= 65536. */
+typedef struct {
+  int kind;            /* gdpa_bias_kind */
+  const float* table;  /* device pointer, ignored for GDPA_BIAS_NONE */
+  int max_rel;
+} gdpa_bias;
+
+typedef enum {
+  GDPA_OK = 0,
+  GDPA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned tensor */
+  GDPA_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, H > 256, ... */
+  GDPA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than the query says */
+  GDPA_ERR_CUDA = 4,         /* a CUDA runtime call failed */
+  GDPA_ERR_TIMEOUT = 5,      /* device: a pipeline wait ran past its limit */
+  GDPA_ERR_BAD_OFFSETS = 6   /* device: offsets malformed, or causal with Lq_b != Lkv_b */
+} gdpa_status;
+
+/* Bytes of workspace gdpa_fwd needs (the work list of the persistent
+ * scheduler).  Depends only on the host scalars. */
+size_t gdpa_fwd_workspace_size(int B, int H, int d, int64_t Tq, int64_t Tkv);
+
+/* Forward pass.
+ *   q [Tq][H][d] bf16, k/v [Tkv][H][d] bf16, offsets int32 [B+1] (device).
+ *   bias: NULL or kind NONE for no bias.  act: gdpa_act.  causal: 0/1
+ *   (top-left, j <= i; every sample must have Lq_b == Lkv_b).
+ *   out [Tq][H][d] bf16 (written only at rows that belong to a sample).
+ *   lse [H][Tq] fp32: natural-log row logsumexp for softmax (needed by the
+ *   backward); may be NULL for the GDPA activations, where it is not written.
+ *   workspace: device memory of at least gdpa_fwd_workspace_size() bytes. */
+gdpa_status gdpa_fwd(const void* q, const int32_t* q_offsets, const void* k, const void* v,
+                     const int32_t* kv_offsets, int B, int H, int d, int64_t Tq, int64_t Tkv,
+                     const gdpa_bias* bias, int act, int causal, float scale, void* out,
+                     float* lse, void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of workspace gdpa_bwd needs (work list, fp32 dQ accumulator and the
+ * per-row D = rowsum(dO * O) of the softmax backward). */
+size_t gdpa_bwd_workspace_size(int B, int H, int d, int64_t Tq, int64_t Tkv);
+
+/* Backward pass: recomputes the scores per tile and writes dq [Tq][H][d],
+ * dk and dv [Tkv][H][d] (bf16).  out and lse are the forward's outputs
+ * (needed for softmax only; may be NULL for the GDPA activations).  dout
+ * [Tq][H][d] bf16.  Rows of dk/dv of a sample with no query, and rows of dq
+ * of a sample with no key, are written as zeros. */
+gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, const void* v,
+                     const int32_t* kv_offsets, int B, int H, int d, int64_t Tq, int64_t Tkv,
+                     const gdpa_bias* bias, int act, int causal, float scale, const void* out,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/* Reads the device status word set by earlier calls on this device,
+ * synchronising `stream` first, then clears it.  Returns GDPA_OK,
+ * GDPA_ERR_TIMEOUT, GDPA_ERR_BAD_OFFSETS or GDPA_ERR_CUDA. */
+gdpa_status gdpa_get_device_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* gdpa_status_string(int status);
+
+/* Number of kernels the most recent gdpa_* call on this host thread
+ * launched (for accounting in benchmarks). */
+int gdpa_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDPA_H_ */

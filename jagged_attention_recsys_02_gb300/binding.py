@@ -1,0 +1,169 @@
+"""Thin Python binding of libgdpa.so (include/gdpa.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  Tensors are torch CUDA tensors (device memory and
+streams come from PyTorch); their data pointers and the current stream are
+handed to the library.  If the library cannot be loaded the calls raise: no
+other implementation stands in for it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH, ACT_IDENTITY = 0, 1, 2, 3
+ACT_BY_NAME = {"softmax": ACT_SOFTMAX, "silu": ACT_SILU, "gelu_tanh": ACT_GELU_TANH,
+               "identity": ACT_IDENTITY}
+BIAS_NONE, BIAS_RELPOS = 0, 1
+
+STATUS_NAMES = {0: "GDPA_OK", 1: "GDPA_ERR_INVALID_ARG", 2: "GDPA_ERR_UNSUPPORTED",
+                3: "GDPA_ERR_WORKSPACE", 4: "GDPA_ERR_CUDA", 5: "GDPA_ERR_TIMEOUT",
+                6: "GDPA_ERR_BAD_OFFSETS"}
+
+# Every symbol include/gdpa.h declares.
+EXPORTS = ("gdpa_fwd_workspace_size", "gdpa_fwd", "gdpa_bwd_workspace_size", "gdpa_bwd",
+           "gdpa_get_device_status", "gdpa_status_string", "gdpa_last_launch_count")
+
+
+class GdpaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}")
+
+
+class gdpa_bias(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("table", ctypes.c_void_p), ("max_rel", ctypes.c_int)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libgdpa.so (building it first if asked and needed)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise OSError(f"{path} is missing; run jagged_attention_recsys_02_gb300.build.build()")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        vp, i64, I, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+        sz = ctypes.c_size_t
+        lib.gdpa_fwd_workspace_size.argtypes = [I, I, I, i64, i64]
+        lib.gdpa_fwd_workspace_size.restype = sz
+        lib.gdpa_bwd_workspace_size.argtypes = [I, I, I, i64, i64]
+        lib.gdpa_bwd_workspace_size.restype = sz
+        lib.gdpa_fwd.argtypes = [vp, vp, vp, vp, vp, I, I, I, i64, i64,
+                                 ctypes.POINTER(gdpa_bias), I, I, F, vp, vp, vp, sz, vp]
+        lib.gdpa_fwd.restype = I
+        lib.gdpa_bwd.argtypes = [vp, vp, vp, vp, vp, I, I, I, i64, i64,
+                                 ctypes.POINTER(gdpa_bias), I, I, F, vp, vp, vp, vp, vp, vp,
+                                 vp, sz, vp]
+        lib.gdpa_bwd.restype = I
+        lib.gdpa_get_device_status.argtypes = [vp]
+        lib.gdpa_get_device_status.restype = I
+        lib.gdpa_status_string.argtypes = [I]
+        lib.gdpa_status_string.restype = ctypes.c_char_p
+        lib.gdpa_last_launch_count.argtypes = []
+        lib.gdpa_last_launch_count.restype = I
+        _lib = lib
+        return lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _bias(table, max_rel):
+    if table is None:
+        return None
+    return ctypes.byref(gdpa_bias(BIAS_RELPOS, table.data_ptr(), int(max_rel)))
+
+
+def _act(act) -> int:
+    return ACT_BY_NAME[act] if isinstance(act, str) else int(act)
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise GdpaError(code, where)
+
+
+def fwd_workspace_size(B, H, d, Tq, Tkv) -> int:
+    return int(load().gdpa_fwd_workspace_size(B, H, d, Tq, Tkv))
+
+
+def bwd_workspace_size(B, H, d, Tq, Tkv) -> int:
+    return int(load().gdpa_bwd_workspace_size(B, H, d, Tq, Tkv))
+
+
+def gdpa_fwd(q, q_offsets, k, v, kv_offsets, *, act, causal=False, scale, bias=None, max_rel=0,
+             out=None, lse=None, workspace=None, stream=None):
+    """Forward pass through the C ABI.  Returns (out, lse)."""
+    lib = load()
+    Tq, H, d = q.shape
+    Tkv = k.shape[0]
+    B = q_offsets.numel() - 1
+    a = _act(act)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and a == ACT_SOFTMAX:
+        lse = torch.empty((H, Tq), device=q.device, dtype=torch.float32)
+    if workspace is None:
+        workspace = torch.empty(fwd_workspace_size(B, H, d, Tq, Tkv), device=q.device,
+                                dtype=torch.uint8)
+    rc = lib.gdpa_fwd(_ptr(q), _ptr(q_offsets), _ptr(k), _ptr(v), _ptr(kv_offsets), B, H, d, Tq,
+                      Tkv, _bias(bias, max_rel), a, int(bool(causal)), float(scale), _ptr(out),
+                      _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "gdpa_fwd")
+    return out, lse
+
+
+def gdpa_bwd(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, act, causal=False, scale,
+             bias=None, max_rel=0, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward pass through the C ABI.  Returns (dq, dk, dv)."""
+    lib = load()
+    Tq, H, d = q.shape
+    Tkv = k.shape[0]
+    B = q_offsets.numel() - 1
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(bwd_workspace_size(B, H, d, Tq, Tkv), device=q.device,
+                                dtype=torch.uint8)
+    rc = lib.gdpa_bwd(_ptr(q), _ptr(q_offsets), _ptr(k), _ptr(v), _ptr(kv_offsets), B, H, d, Tq,
+                      Tkv, _bias(bias, max_rel), _act(act), int(bool(causal)), float(scale),
+                      _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                      _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "gdpa_bwd")
+    return dq, dk, dv
+
+
+def device_status(stream=None) -> int:
+    return int(load().gdpa_get_device_status(_stream(stream)))
+
+
+def last_launch_count() -> int:
+    return int(load().gdpa_last_launch_count())

@@ -1,0 +1,238 @@
+// C ABI entry points (include/gdpa.h): argument checks, TMA descriptors,
+// workspace carving and kernel launches.  No device memory is allocated
+// here; the caller passes every buffer, including the workspace.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace gdpa {
+namespace {
+
+// Device status word: set by kernels (timeouts, malformed offsets), read and
+// cleared by gdpa_get_device_status().
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool init = false;
+  int sms = 0;
+  int* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+thread_local int t_launches = 0;
+
+cudaError_t device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word);
+    if (e != cudaSuccess) return e;
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q);
+      if (e != cudaSuccess) return e;
+      if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.init = true;
+  }
+  *out = &d;
+  return cudaSuccess;
+}
+
+// 3-D TMA map over a [T][H][d] bf16 tensor: box = 64 channels x 1 head x
+// `box_rows` rows, 128-byte swizzle (the layout the tcgen05 descriptors use).
+bool make_thd_map(CUtensorMap* m, const void* base, int64_t T, int H, int d, int box_rows) {
+  if (T <= 0) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+gdpa_status check_common(const void* q, const int32_t* qo, const void* k, const void* v,
+                         const int32_t* ko, int B, int H, int d, int64_t Tq, int64_t Tkv,
+                         const gdpa_bias* bias, int act, int causal) {
+  if (B < 0 || H <= 0 || Tq < 0 || Tkv < 0) return GDPA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return GDPA_ERR_UNSUPPORTED;
+  if (H > 256) return GDPA_ERR_UNSUPPORTED;
+  if (act < GDPA_ACT_SOFTMAX || act > GDPA_ACT_IDENTITY) return GDPA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return GDPA_ERR_INVALID_ARG;
+  if (qo == nullptr || ko == nullptr) return GDPA_ERR_INVALID_ARG;
+  if (Tq > 0 && q == nullptr) return GDPA_ERR_INVALID_ARG;
+  if (Tkv > 0 && (k == nullptr || v == nullptr)) return GDPA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return GDPA_ERR_INVALID_ARG;
+  if (Tq > (int64_t(1) << 31) - 1 || Tkv > (int64_t(1) << 31) - 1) return GDPA_ERR_UNSUPPORTED;
+  if (bias != nullptr && bias->kind != GDPA_BIAS_NONE) {
+    if (bias->kind != GDPA_BIAS_RELPOS) return GDPA_ERR_INVALID_ARG;
+    if (bias->table == nullptr || bias->max_rel < 1 || bias->max_rel > 65536)
+      return GDPA_ERR_INVALID_ARG;
+  }
+  return GDPA_OK;
+}
+
+const float* bias_table(const gdpa_bias* bias, int* max_rel) {
+  if (bias == nullptr || bias->kind == GDPA_BIAS_NONE) {
+    *max_rel = 1;
+    return nullptr;
+  }
+  *max_rel = bias->max_rel;
+  return bias->table;
+}
+
+}  // namespace
+}  // namespace gdpa
+
+using namespace gdpa;
+
+extern "C" {
+
+size_t gdpa_fwd_workspace_size(int B, int H, int d, int64_t Tq, int64_t Tkv) {
+  (void)d;
+  (void)Tkv;
+  if (B < 0 || H <= 0 || Tq < 0) return 0;
+  return 256 + align_up(static_cast<size_t>(max_fwd_items(B, H, Tq)) * sizeof(int2), 256);
+}
+
+gdpa_status gdpa_fwd(const void* q, const int32_t* q_offsets, const void* k, const void* v,
+                     const int32_t* kv_offsets, int B, int H, int d, int64_t Tq, int64_t Tkv,
+                     const gdpa_bias* bias, int act, int causal, float scale, void* out,
+                     float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  t_launches = 0;
+  gdpa_status st = check_common(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act,
+                                causal);
+  if (st != GDPA_OK) return st;
+  if (Tq > 0 && (out == nullptr || !aligned16(out))) return GDPA_ERR_INVALID_ARG;
+  if (act == GDPA_ACT_SOFTMAX && Tq > 0 && lse == nullptr) return GDPA_ERR_INVALID_ARG;
+  const size_t need = gdpa_fwd_workspace_size(B, H, d, Tq, Tkv);
+  if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return GDPA_ERR_WORKSPACE;
+  if (Tq == 0 || B == 0) return GDPA_OK;
+
+  DeviceInfo* dev = nullptr;
+  if (device_info(&dev) != cudaSuccess) return GDPA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  int max_rel = 1;
+  const float* table = bias_table(bias, &max_rel);
+  CUtensorMap tq, tk, tv;
+  if (!make_thd_map(&tq, q, Tq, H, d, kHalfRows)) return GDPA_ERR_INVALID_ARG;
+  // With no key rows at all there is nothing to load; any valid map will do.
+  const void* kb = Tkv > 0 ? k : q;
+  const void* vb = Tkv > 0 ? v : q;
+  const int64_t Tk = Tkv > 0 ? Tkv : Tq;
+  if (!make_thd_map(&tk, kb, Tk, H, d, kKvRows)) return GDPA_ERR_INVALID_ARG;
+  if (!make_thd_map(&tv, vb, Tk, H, d, kKvRows)) return GDPA_ERR_INVALID_ARG;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* n_items = reinterpret_cast<int*>(ws);
+  int* ticket = reinterpret_cast<int*>(ws + 4);
+  int2* items = reinterpret_cast<int2*>(ws + 256);
+
+  if (launch_build_worklist(q_offsets, kv_offsets, B, H, Tq, Tkv, causal, 0, items, n_items,
+                            ticket, dev->status, s) != cudaSuccess)
+    return GDPA_ERR_CUDA;
+  ++t_launches;
+
+  FwdParams p{};
+  p.qo = q_offsets;
+  p.ko = kv_offsets;
+  p.B = B;
+  p.H = H;
+  p.d = d;
+  p.Tq = Tq;
+  p.Tkv = Tkv;
+  p.bias_table = table;
+  p.max_rel = max_rel;
+  p.causal = causal;
+  p.scale = scale;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.items = items;
+  p.n_items = n_items;
+  p.ticket = ticket;
+  p.status = dev->status;
+  const int64_t max_items = max_fwd_items(B, H, Tq);
+  const int grid = static_cast<int>(max_items < dev->sms ? max_items : dev->sms);
+  if (launch_fwd(p, act, tq, tk, tv, grid, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  ++t_launches;
+  return GDPA_OK;
+}
+
+size_t gdpa_bwd_workspace_size(int B, int H, int d, int64_t Tq, int64_t Tkv) {
+  if (B < 0 || H <= 0 || Tq < 0 || Tkv < 0) return 0;
+  size_t sz = 256;
+  sz += align_up(static_cast<size_t>(max_bwd_items(B, H, Tkv)) * sizeof(int2), 256);
+  sz += align_up(static_cast<size_t>(Tq) * H * d * sizeof(float), 256);  // dQ accumulator
+  sz += align_up(static_cast<size_t>(Tq) * H * sizeof(float), 256);      // D = rowsum(dO*O)
+  return sz;
+}
+
+gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, const void* v,
+                     const int32_t* kv_offsets, int B, int H, int d, int64_t Tq, int64_t Tkv,
+                     const gdpa_bias* bias, int act, int causal, float scale, const void* out,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                     void* workspace, size_t ws_bytes, void* stream) {
+  t_launches = 0;
+  gdpa_status st = check_common(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act,
+                                causal);
+  if (st != GDPA_OK) return st;
+  (void)scale; (void)out; (void)lse; (void)dout; (void)dq; (void)dk; (void)dv;
+  (void)workspace; (void)ws_bytes; (void)stream;
+  return GDPA_ERR_UNSUPPORTED;
+}
+
+gdpa_status gdpa_get_device_status(void* stream) {
+  DeviceInfo* dev = nullptr;
+  if (device_info(&dev) != cudaSuccess) return GDPA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDPA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GDPA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return GDPA_ERR_CUDA;
+  }
+  return static_cast<gdpa_status>(v);
+}
+
+const char* gdpa_status_string(int status) {
+  switch (status) {
+    case GDPA_OK: return "GDPA_OK";
+    case GDPA_ERR_INVALID_ARG: return "GDPA_ERR_INVALID_ARG";
+    case GDPA_ERR_UNSUPPORTED: return "GDPA_ERR_UNSUPPORTED";
+    case GDPA_ERR_WORKSPACE: return "GDPA_ERR_WORKSPACE";
+    case GDPA_ERR_CUDA: return "GDPA_ERR_CUDA";
+    case GDPA_ERR_TIMEOUT: return "GDPA_ERR_TIMEOUT";
+    case GDPA_ERR_BAD_OFFSETS: return "GDPA_ERR_BAD_OFFSETS";
+    default: return "GDPA_ERR_UNKNOWN";
+  }
+}
+
+int gdpa_last_launch_count(void) { return t_launches; }
+
+}  // extern "C"

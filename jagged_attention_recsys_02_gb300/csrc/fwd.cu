@@ -1,0 +1,532 @@
+// Forward kernel of jagged attention with a pluggable activation, sm_103a.
+//
+// "GEM Training ..." GDPA paragraph: two matrix multiplications with an
+// elementwise activation in between (softmax -> JFA, GELU / SiLU -> GDPA).
+// JFA paragraph: operate directly on jagged tensors with no padding, with
+// custom attention biases and asymmetric query / key lengths.
+//
+// Design (one persistent CTA per SM, warp-specialised, 320 threads):
+//   warps 0-3   "softmax group 0": query rows [0,128) of the item
+//   warps 4-7   "softmax group 1": query rows [128,256) of the item
+//   warp  8     TMA producer: pulls work items from the cost-sorted list
+//               (atomic ticket), loads Q once per item and K/V tiles into a
+//               ring of shared-memory stages
+//   warp  9     MMA issuer: tcgen05.mma S_h = Q_h K^T into TMEM, then
+//               O_h += P_h V with P_h read from TMEM
+// TMEM (512 columns): half h owns S/P columns [256h, 256h+128) and O columns
+// [256h+128, 256h+128+d).  The activation group reads S row by row (TMEM lane
+// = query row), applies scale, bias, mask and the activation in registers
+// and writes P back into the same columns as packed bf16.  Softmax keeps an
+// online row max / sum and rescales O in TMEM only when the max grows by
+// more than 2^8 (stale maxima are exact after the final division).  GDPA
+// activations need no normalisation; their P is split into bf16 hi + lo
+// parts (two MMAs) because a single 16-bit P loses too much precision when
+// thousands of unnormalised terms are summed.
+//
+// Issue order per item (MMA warp):  S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) ...
+// so that while one group runs its activation the tensor core works on the
+// other group's tile.  tcgen05 MMAs from one thread complete in order, which
+// makes S_h(j+1) overwriting P_h(j) safe and guarantees that when S_h(j) is
+// complete, PV_h(j-1) is too (so O may be rescaled then).
+//
+// Every mbarrier wait is bounded; on a timeout the CTA records
+// GDPA_ERR_TIMEOUT in the status word, drains its own copies and MMAs with a
+// short bounded wait, frees TMEM and exits.
+#include "common.cuh"
+
+namespace gdpa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kQHalfBytes = kHalfRows * D * 2;
+  static constexpr int kTileBytes = kKvRows * D * 2;
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kQ0 = 0;
+  static constexpr int kQ1 = kQHalfBytes;
+  static constexpr int kKV = 2 * kQHalfBytes;                          // K[s] = kKV + s*2*tile
+  static constexpr int kBar = kKV + kStages * 2 * kTileBytes;         // barriers after tiles
+  // barrier block layout (8 bytes each)
+  static constexpr int kQFull = 0, kQEmpty = 1;
+  static constexpr int kKFull = 2;                                     // + s
+  static constexpr int kVFull = kKFull + kStages;
+  static constexpr int kKvEmpty = kVFull + kStages;
+  static constexpr int kSFull = kKvEmpty + kStages;                    // + half
+  static constexpr int kPFull = kSFull + 2;
+  static constexpr int kODone = kPFull + 2;
+  static constexpr int kItemFull = kODone + 2;                         // + slot
+  static constexpr int kItemEmpty = kItemFull + 2;
+  static constexpr int kDrain = kItemEmpty + 2;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kItemSlots = kBar + 8 * kNumBars;               // int2[2]
+  static constexpr int kTmemSlot = kItemSlots + 16;
+  static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kUsed = kAbort + 4;
+  static constexpr int kSmemBytes = kUsed + 1024;                      // + alignment slack
+};
+
+__device__ __forceinline__ float act_apply(int act, float x) {
+  if (act == GDPA_ACT_SILU) {
+    const float h = 0.5f * x;
+    return fmaf(h, tanh_approx(h), h);
+  }
+  if (act == GDPA_ACT_GELU_TANH) {
+    // 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
+    const float k0 = 0.7978845608028654f, k1 = 0.7978845608028654f * 0.044715f;
+    const float u = x * fmaf(k1, x * x, k0);
+    const float h = 0.5f * x;
+    return fmaf(h, tanh_approx(u), h);
+  }
+  return x;  // identity
+}
+
+struct ItemInfo {
+  int b, head, blk;
+  int q0, k0, Lq, Lkv;
+  int n0, n1;  // kv tiles visited by half 0 / half 1 (0 = half inactive)
+};
+
+__device__ __forceinline__ ItemInfo decode_item(int2 it, const FwdParams& p) {
+  ItemInfo r;
+  r.b = it.x;
+  r.head = item_head(it);
+  r.blk = item_block(it);
+  r.q0 = p.qo[r.b];
+  r.Lq = p.qo[r.b + 1] - r.q0;
+  r.k0 = p.ko[r.b];
+  r.Lkv = p.ko[r.b + 1] - r.k0;
+  const int nkv = (r.Lkv + kKvRows - 1) / kKvRows;
+  const int r0 = r.blk * kItemRows;
+  const bool h1 = r0 + kHalfRows < r.Lq;
+  if (!p.causal) {
+    r.n0 = nkv;
+    r.n1 = h1 ? nkv : 0;
+  } else {
+    r.n0 = min(nkv, (min(r.Lq, r0 + kHalfRows) + kKvRows - 1) / kKvRows);
+    r.n1 = h1 ? min(nkv, (min(r.Lq, r0 + kItemRows) + kKvRows - 1) / kKvRows) : 0;
+  }
+  return r;
+}
+
+template <int D, int ACT>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+           const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
+  using C = FwdCfg<D>;
+  constexpr bool kSoftmax = (ACT == GDPA_ACT_SOFTMAX);
+  constexpr bool kSplit = !kSoftmax;  // GDPA: P = hi + lo
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kBar + 8u * i; };
+  int2* item_slot = reinterpret_cast<int2*>(gbase + C::kItemSlots);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kAbort);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(C::kQFull), 1);
+    mbar_init(bar(C::kQEmpty), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kKFull + s), 1);
+      mbar_init(bar(C::kVFull + s), 1);
+      mbar_init(bar(C::kKvEmpty + s), 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(C::kSFull + h), 1);
+      mbar_init(bar(C::kPFull + h), kHalfRows);
+      mbar_init(bar(C::kODone + h), 1);
+      mbar_init(bar(C::kItemFull + h), 1);
+      mbar_init(bar(C::kItemEmpty + h), 1 + 2 * kHalfRows);
+    }
+    mbar_init(bar(C::kDrain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    set_status(p.status, GDPA_ERR_TIMEOUT);
+  };
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const int n_items = *p.n_items;
+      uint32_t it = 0, g = 0, qi = 0;
+      uint32_t inflight = 0;  // stages whose K/V load may still be in flight (abort drain)
+      bool q_inflight = false;
+      uint32_t last_g[C::kStages] = {};
+      bool ok = true;
+      while (ok) {
+        const int t = atomicAdd(p.ticket, 1);
+        const int2 item = (t < n_items) ? p.items[t] : make_int2(-1, 0);
+        const uint32_t slot = it & 1u;
+        if (!mbar_wait(bar(C::kItemEmpty + slot), ((it >> 1) & 1u) ^ 1u, abort_flag)) { fail(); break; }
+        item_slot[slot] = item;
+        mbar_arrive(bar(C::kItemFull + slot));
+        ++it;
+        if (item.x < 0) break;
+        const ItemInfo in = decode_item(item, p);
+        const int n = max(in.n0, in.n1);
+        if (n == 0) continue;
+        if (!mbar_wait(bar(C::kQEmpty), (qi & 1u) ^ 1u, abort_flag)) { fail(); break; }
+        const int row0 = in.q0 + in.blk * kItemRows;
+        mbar_arrive_expect_tx(bar(C::kQFull), (in.n1 > 0 ? 2 : 1) * C::kQHalfBytes);
+        for (int half = 0; half < (in.n1 > 0 ? 2 : 1); ++half)
+          for (int x = 0; x < D; x += 64)
+            tma_load_3d(sbase + (half ? C::kQ1 : C::kQ0) + (x / 64) * (kHalfRows * 128),
+                        &tmap_q, bar(C::kQFull), x, in.head, row0 + half * kHalfRows);
+        q_inflight = true;
+        ++qi;
+        for (int j = 0; j < n; ++j, ++g) {
+          const uint32_t s = g % C::kStages;
+          const uint32_t ph = (g / C::kStages) & 1u;
+          if (!mbar_wait(bar(C::kKvEmpty + s), ph ^ 1u, abort_flag)) { ok = false; fail(); break; }
+          const uint32_t kdst = sbase + C::kKV + s * 2 * C::kTileBytes;
+          const int krow = in.k0 + j * kKvRows;
+          mbar_arrive_expect_tx(bar(C::kKFull + s), C::kTileBytes);
+          for (int x = 0; x < D; x += 64)
+            tma_load_3d(kdst + (x / 64) * (kKvRows * 128), &tmap_k, bar(C::kKFull + s), x,
+                        in.head, krow);
+          mbar_arrive_expect_tx(bar(C::kVFull + s), C::kTileBytes);
+          for (int x = 0; x < D; x += 64)
+            tma_load_3d(kdst + C::kTileBytes + (x / 64) * (kKvRows * 128), &tmap_v,
+                        bar(C::kVFull + s), x, in.head, krow);
+          inflight |= 1u << s;
+          last_g[s] = g;
+        }
+      }
+      if (*abort_flag) {
+        // Drain: wait (briefly, bounded) for copies this thread issued.
+        for (int s = 0; s < C::kStages; ++s)
+          if (inflight & (1u << s)) {
+            const uint32_t ph = (last_g[s] / C::kStages) & 1u;
+            mbar_wait(bar(C::kKFull + s), ph, nullptr, 50000000ull);
+            mbar_wait(bar(C::kVFull + s), ph, nullptr, 50000000ull);
+          }
+        if (q_inflight) mbar_wait(bar(C::kQFull), (qi - 1) & 1u, nullptr, 50000000ull);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_f16(128, 128, true, false, false);
+      constexpr uint32_t idesc_pv = idesc_f16(128, D, true, false, true);
+      uint32_t it = 0, g = 0, qi = 0;
+      uint32_t tcount[2] = {0, 0};
+      bool issued_any = false;
+      auto issue_s = [&](int half, uint32_t stage) {
+        const uint32_t qa = sbase + (half ? C::kQ1 : C::kQ0);
+        const uint32_t ka = sbase + C::kKV + stage * 2 * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks / 4) * (kHalfRows * 128) + (ks % 4) * 32;
+          const uint64_t ad = sdesc(qa + off, 0, 1024, kSwizzle128B);
+          const uint64_t bd = sdesc(ka + off, 0, 1024, kSwizzle128B);
+          mma_f16_ss(tmem + half * 256, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kSFull + half));
+        issued_any = true;
+      };
+      auto issue_pv = [&](int half, uint32_t stage, bool first) {
+        const uint32_t va = sbase + C::kKV + stage * 2 * C::kTileBytes + C::kTileBytes;
+        const uint32_t tp = tmem + half * 256;
+        const uint32_t to = tmem + half * 256 + 128;
+#pragma unroll
+        for (int ks = 0; ks < kKvRows / 16; ++ks) {
+          const uint64_t bd = sdesc(va + ks * 2048, kKvRows * 128, 1024, kSwizzle128B);
+          const uint32_t pcol = 32 * (ks / 2) + 8 * (ks % 2);
+          mma_f16_ts(to, tp + pcol, bd, idesc_pv, (first && ks == 0) ? 0u : 1u);
+          if (kSplit) mma_f16_ts(to, tp + pcol + 16, bd, idesc_pv, 1u);
+        }
+        issued_any = true;
+      };
+      bool ok = true;
+      while (ok) {
+        const uint32_t slot = it & 1u;
+        if (!mbar_wait(bar(C::kItemFull + slot), (it >> 1) & 1u, abort_flag)) { fail(); break; }
+        const int2 item = item_slot[slot];
+        mbar_arrive(bar(C::kItemEmpty + slot));
+        ++it;
+        if (item.x < 0) break;
+        const ItemInfo in = decode_item(item, p);
+        const int n = max(in.n0, in.n1);
+        if (n == 0) continue;
+        if (!mbar_wait(bar(C::kQFull), qi & 1u, abort_flag)) { fail(); break; }
+        ++qi;
+        tc_fence_after();
+        // The half that visits the most key tiles issues the item's last S.
+        const int last_s_half = (in.n1 == n) ? 1 : 0;
+        {
+          const uint32_t s = g % C::kStages;
+          if (!mbar_wait(bar(C::kKFull + s), (g / C::kStages) & 1u, abort_flag)) { fail(); break; }
+          tc_fence_after();
+          if (in.n0 > 0) issue_s(0, s);
+          if (in.n1 > 0) issue_s(1, s);
+          if (n == 1) mma_commit(bar(C::kQEmpty));
+        }
+        for (int j = 0; j < n; ++j) {
+          const uint32_t gj = g + j;
+          const uint32_t s = gj % C::kStages;
+          const uint32_t s_next = (gj + 1) % C::kStages;
+          const uint32_t ph_next = ((gj + 1) / C::kStages) & 1u;
+          if (!mbar_wait(bar(C::kVFull + s), (gj / C::kStages) & 1u, abort_flag)) { ok = false; fail(); break; }
+          const int last_half_j = (j < in.n1) ? 1 : 0;  // last user of stage s
+          for (int half = 0; half < 2; ++half) {
+            const int nh = half ? in.n1 : in.n0;
+            if (j >= nh) continue;
+            if (!mbar_wait(bar(C::kPFull + half), tcount[half] & 1u, abort_flag)) { ok = false; fail(); break; }
+            ++tcount[half];
+            tc_fence_after();
+            issue_pv(half, s, j == 0);
+            if (j == nh - 1) mma_commit(bar(C::kODone + half));
+            if (half == last_half_j) mma_commit(bar(C::kKvEmpty + s));
+            if (j + 1 < nh) {
+              if (!mbar_wait(bar(C::kKFull + s_next), ph_next, abort_flag)) { ok = false; fail(); break; }
+              tc_fence_after();
+              issue_s(half, s_next);
+              if (j + 1 == n - 1 && half == last_s_half) mma_commit(bar(C::kQEmpty));
+            }
+          }
+          if (!ok) break;
+        }
+        g += n;
+      }
+      // Make sure every MMA this thread issued has completed before TMEM is freed.
+      if (issued_any) {
+        mma_commit(bar(C::kDrain));
+        mbar_wait(bar(C::kDrain), 0, nullptr, 100000000ull);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ activation groups
+    const int half = warp >> 2;                 // 0 or 1
+    const int wq = warp & 3;                    // TMEM lane quarter
+    const int row_in_half = wq * 32 + lane;     // TMEM lane = query row of the half
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + half * 256;
+    const uint32_t t_o = t_s + 128;
+    const float c_s = kSoftmax ? p.scale * kLog2e : p.scale;   // score multiplier
+    const float c_b = kSoftmax ? kLog2e : 1.0f;                 // bias multiplier
+    const int rel_w = 2 * p.max_rel - 1;
+    uint32_t it = 0, tcount = 0, ocount = 0;
+    while (true) {
+      const uint32_t slot = it & 1u;
+      bool ok = mbar_wait(bar(C::kItemFull + slot), (it >> 1) & 1u, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) { if (lane == 0) fail(); break; }
+      const int2 item = item_slot[slot];
+      mbar_arrive(bar(C::kItemEmpty + slot));
+      ++it;
+      if (item.x < 0) break;
+      const ItemInfo in = decode_item(item, p);
+      const int nh = half ? in.n1 : in.n0;
+      const int r = in.blk * kItemRows + half * kHalfRows + row_in_half;  // local row
+      if (half == 1 && in.n1 == 0 && in.blk * kItemRows + kHalfRows >= in.Lq) continue;
+      const bool row_valid = r < in.Lq;
+      const float* brow = p.bias_table ? p.bias_table + static_cast<long long>(in.head) * rel_w : nullptr;
+      float m = -INFINITY;  // running max (log2 units), possibly stale
+      float l = 0.0f;       // running sum relative to m
+      bool abort_now = false;
+      for (int j = 0; j < nh; ++j) {
+        bool okw = mbar_wait(bar(C::kSFull + half), tcount & 1u, abort_flag);
+        okw = __all_sync(0xffffffffu, okw);
+        if (!okw) { if (lane == 0) fail(); abort_now = true; break; }
+        ++tcount;
+        tc_fence_after();
+        const int c0 = j * kKvRows;
+        const bool need_mask = (c0 + kKvRows > in.Lkv) || (p.causal && c0 + kKvRows - 1 > r);
+        const int col_lim = p.causal ? min(in.Lkv, r + 1) : in.Lkv;  // valid cols: c < col_lim
+        auto load_x = [&](int chunk, float (&x)[32]) {
+          uint32_t sr[32];
+          tmem_ld32(t_s + chunk * 32, sr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(sr[i]) * c_s;
+          if (brow != nullptr) {
+            const int base_idx = r - (c0 + chunk * 32) + p.max_rel - 1;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int idx = min(max(base_idx - i, 0), rel_w - 1);
+              x[i] = fmaf(__ldg(brow + idx), c_b, x[i]);
+            }
+          }
+          if (need_mask) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c0 + chunk * 32 + i >= col_lim) x[i] = kSoftmax ? -INFINITY : 0.0f;
+          }
+        };
+        if (kSoftmax) {
+          float mt = -INFINITY;
+#pragma unroll 1
+          for (int chunk = 0; chunk < 4; ++chunk) {
+            float x[32];
+            load_x(chunk, x);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mt = fmaxf(mt, x[i]);
+          }
+          const float m_new = fmaxf(m, mt);
+          bool rescale = false;
+          float factor = 1.0f;
+          if (m == -INFINITY) {
+            m = m_new;
+          } else if (m_new - m > kRescaleThreshold) {
+            factor = ex2_approx(m - m_new);
+            l *= factor;
+            m = m_new;
+            rescale = true;
+          }
+          if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+            for (int chunk = 0; chunk < D / 32; ++chunk) {
+              uint32_t o[32];
+              tmem_ld32(t_o + chunk * 32, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
+              tmem_st32(t_o + chunk * 32, o);
+            }
+          }
+          const float m_ref = (m == -INFINITY) ? 0.0f : m;
+#pragma unroll 1
+          for (int chunk = 0; chunk < 4; ++chunk) {
+            float x[32];
+            load_x(chunk, x);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float p0 = ex2_approx(x[2 * i] - m_ref);
+              const float p1 = ex2_approx(x[2 * i + 1] - m_ref);
+              l += p0 + p1;
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(t_s + chunk * 32, pk);
+          }
+        } else {
+#pragma unroll 1
+          for (int chunk = 0; chunk < 4; ++chunk) {
+            float x[32];
+            load_x(chunk, x);
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float p0 = act_apply(ACT, x[2 * i]);
+              const float p1 = act_apply(ACT, x[2 * i + 1]);
+              const uint32_t h = pack_bf16x2(p0, p1);
+              const float h0 = __uint_as_float(h << 16);
+              const float h1 = __uint_as_float(h & 0xFFFF0000u);
+              hi[i] = h;
+              lo[i] = pack_bf16x2(p0 - h0, p1 - h1);
+            }
+            tmem_st16(t_s + chunk * 32, hi);
+            tmem_st16(t_s + chunk * 32 + 16, lo);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::kPFull + half));
+      }
+      if (abort_now) break;
+      // ---------------------------------------------------------- epilogue
+      const float inv_l = kSoftmax ? (l > 0.0f ? 1.0f / l : 0.0f) : 1.0f;
+      __nv_bfloat16* orow = p.out + (static_cast<long long>(in.q0 + r) * p.H + in.head) * D;
+      if (nh > 0) {
+        bool okw = mbar_wait(bar(C::kODone + half), ocount & 1u, abort_flag);
+        okw = __all_sync(0xffffffffu, okw);
+        if (!okw) { if (lane == 0) fail(); break; }
+        ++ocount;
+        tc_fence_after();
+#pragma unroll 1
+        for (int chunk = 0; chunk < D / 32; ++chunk) {
+          uint32_t o[32];
+          tmem_ld32(t_o + chunk * 32, o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + chunk * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+        tc_fence_before();
+      } else if (row_valid) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+        for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+      }
+      if (kSoftmax && row_valid && p.lse != nullptr) {
+        const float lse = (l > 0.0f) ? (m * kLn2 + __logf(l)) : -INFINITY;
+        p.lse[static_cast<long long>(in.head) * p.Tq + in.q0 + r] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int ACT>
+cudaError_t launch_one(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, int grid, cudaStream_t stream) {
+  const int smem = FwdCfg<D>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, ACT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  fwd_kernel<D, ACT><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const FwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
+                     const CUtensorMap& tv, int grid, cudaStream_t stream) {
+  switch (act) {
+    case GDPA_ACT_SOFTMAX: return launch_one<D, GDPA_ACT_SOFTMAX>(p, tq, tk, tv, grid, stream);
+    case GDPA_ACT_SILU: return launch_one<D, GDPA_ACT_SILU>(p, tq, tk, tv, grid, stream);
+    case GDPA_ACT_GELU_TANH: return launch_one<D, GDPA_ACT_GELU_TANH>(p, tq, tk, tv, grid, stream);
+    default: return launch_one<D, GDPA_ACT_IDENTITY>(p, tq, tk, tv, grid, stream);
+  }
+}
+
+}  // namespace
+
+int fwd_smem_bytes(int d) { return d == 64 ? FwdCfg<64>::kSmemBytes : FwdCfg<128>::kSmemBytes; }
+
+cudaError_t launch_fwd(const FwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, int grid, cudaStream_t stream) {
+  if (p.d == 64) return launch_d<64>(p, act, tq, tk, tv, grid, stream);
+  return launch_d<128>(p, act, tq, tk, tv, grid, stream);
+}
+
+}  // namespace gdpa

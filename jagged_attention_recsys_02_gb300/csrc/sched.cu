@@ -1,0 +1,128 @@
+// Varlen tile scheduler: turns per-sample offsets into a cost-sorted list of
+// (sample, head, block) work items for the persistent attention kernels.
+//
+// Jagged inputs break the uniform tiling of dense attention: short samples
+// finish early and leave SMs idle ("GEM Training ..." JFA paragraph, and the
+// GDPA paragraph on large batches breaking occupancy assumptions).  The fix
+// here: enumerate every block of every sample, estimate its cost as the
+// number of inner tiles it will visit, counting-sort the blocks by cost in
+// descending order (longest-processing-time first) and let the persistent
+// CTAs pull items in that order from an atomic ticket.
+//
+// One CTA of 1024 threads builds the list; it also validates the offsets and
+// reports malformed ones through the device status word instead of trapping.
+#include "common.cuh"
+
+namespace gdpa {
+namespace {
+
+constexpr int kThreads = 1024;
+
+// mode 0 (forward): outer = queries in 256-row blocks, inner = key tiles of 128.
+// mode 1 (backward): outer = keys in 128-row blocks, inner = query tiles of 64.
+__device__ __forceinline__ int block_cost(int mode, int causal, int Lo, int Li, int blk) {
+  if (mode == 0) {
+    const int nkv = (Li + kKvRows - 1) / kKvRows;
+    if (!causal) return nkv + 1;
+    const int row_end = min(Lo, (blk + 1) * kItemRows);
+    return min(nkv, (row_end + kKvRows - 1) / kKvRows) + 1;
+  }
+  const int first_q = causal ? blk * kBwdKvRows : 0;
+  const int nq = (Li - first_q + kBwdQRows - 1) / kBwdQRows;
+  return max(nq, 0) + 1;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __restrict__ inner_off,
+                      int B, int H, long long T_outer, long long T_inner, int causal, int mode,
+                      int2* __restrict__ items, int* __restrict__ n_items,
+                      int* __restrict__ ticket, int* __restrict__ status) {
+  __shared__ int hist[kCostBuckets];
+  __shared__ int base[kCostBuckets];
+  __shared__ int warp_tot[kThreads / 32];
+  __shared__ int bad;
+  const int tid = threadIdx.x;
+  const int block_rows = (mode == 0) ? kItemRows : kBwdKvRows;
+  for (int i = tid; i < kCostBuckets; i += kThreads) hist[i] = 0;
+  if (tid == 0) {
+    bad = (outer_off[0] != 0 || inner_off[0] != 0 || outer_off[B] != T_outer ||
+           inner_off[B] != T_inner) ? 1 : 0;
+  }
+  __syncthreads();
+  for (int b = tid; b < B; b += kThreads) {
+    const int Lo = outer_off[b + 1] - outer_off[b];
+    const int Li = inner_off[b + 1] - inner_off[b];
+    if (Lo < 0 || Li < 0 || (causal && Lo != Li)) {
+      bad = 1;
+      continue;
+    }
+    const int nblk = (Lo + block_rows - 1) / block_rows;
+    for (int blk = 0; blk < nblk; ++blk)
+      atomicAdd(&hist[min(block_cost(mode, causal, Lo, Li, blk), kCostBuckets - 1)], 1);
+  }
+  __syncthreads();
+  if (bad) {
+    if (tid == 0) {
+      *n_items = 0;
+      *ticket = 0;
+      set_status(status, GDPA_ERR_BAD_OFFSETS);
+    }
+    return;
+  }
+  // Exclusive scan in descending cost order: base[c] = sum of hist[c'] for c' > c.
+  // Thread t owns reversed positions 2t and 2t+1.
+  const int c0 = kCostBuckets - 1 - 2 * tid, c1 = c0 - 1;
+  const int v0 = hist[c0], v1 = hist[c1];
+  int incl = v0 + v1;
+  const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += t;
+    }
+    warp_tot[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? warp_tot[warp - 1] : 0) + incl - (v0 + v1);
+  base[c0] = before;
+  base[c1] = before + v0;
+  __syncthreads();
+  const int total = warp_tot[kThreads / 32 - 1];
+  for (int b = tid; b < B; b += kThreads) {
+    const int Lo = outer_off[b + 1] - outer_off[b];
+    const int Li = inner_off[b + 1] - inner_off[b];
+    const int nblk = (Lo + block_rows - 1) / block_rows;
+    for (int blk = 0; blk < nblk; ++blk) {
+      const int c = min(block_cost(mode, causal, Lo, Li, blk), kCostBuckets - 1);
+      const int pos = atomicAdd(&base[c], 1);
+      for (int h = 0; h < H; ++h)
+        items[static_cast<long long>(pos) * H + h] = make_int2(b, (blk << 8) | h);
+    }
+  }
+  if (tid == 0) {
+    *n_items = total * H;
+    *ticket = 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_build_worklist(const int32_t* outer_off, const int32_t* inner_off, int B, int H,
+                                  int64_t T_outer, int64_t T_inner, int causal, int mode,
+                                  int2* items, int* n_items, int* ticket, int* status,
+                                  cudaStream_t stream) {
+  build_worklist_kernel<<<1, kThreads, 0, stream>>>(outer_off, inner_off, B, H, T_outer, T_inner,
+                                                    causal, mode, items, n_items, ticket, status);
+  return cudaGetLastError();
+}
+
+}  // namespace gdpa

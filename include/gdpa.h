@@ -124,6 +124,18 @@ const char* gdpa_status_string(int status);
  * launched (for accounting in benchmarks). */
 int gdpa_last_launch_count(void);
 
+/* Kernel timing for benchmarks.  While enabled on a host thread, every
+ * gdpa_fwd / gdpa_bwd call on that thread records a pair of CUDA events on
+ * its stream around its main attention kernel (at most 4096 pairs; later
+ * calls are not recorded).  gdpa_timing_enable(1) starts a fresh record,
+ * gdpa_timing_enable(0) stops recording.  gdpa_timing_collect() waits for
+ * the recorded events, writes up to `max` durations in milliseconds to
+ * ms[] and the matching kinds (0 = forward, 1 = backward) to kind[], and
+ * returns how many it wrote (or -1 on a CUDA error).  The events are
+ * created on first use and kept for the life of the thread. */
+gdpa_status gdpa_timing_enable(int enable);
+int gdpa_timing_collect(float* ms, int* kind, int max);
+
 #ifdef __cplusplus
 }
 #endif

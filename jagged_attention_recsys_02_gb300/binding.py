@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "GDPA_OK", 1: "GDPA_ERR_INVALID_ARG", 2: "GDPA_ERR_UNSUPPORTE
 
 # Every symbol include/gdpa.h declares.
 EXPORTS = ("gdpa_fwd_workspace_size", "gdpa_fwd", "gdpa_bwd_workspace_size", "gdpa_bwd",
-           "gdpa_get_device_status", "gdpa_status_string", "gdpa_last_launch_count")
+           "gdpa_get_device_status", "gdpa_status_string", "gdpa_last_launch_count",
+           "gdpa_timing_enable", "gdpa_timing_collect")
 
 
 class GdpaError(RuntimeError):
@@ -79,6 +80,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdpa_status_string.restype = ctypes.c_char_p
         lib.gdpa_last_launch_count.argtypes = []
         lib.gdpa_last_launch_count.restype = I
+        lib.gdpa_timing_enable.argtypes = [I]
+        lib.gdpa_timing_enable.restype = I
+        lib.gdpa_timing_collect.argtypes = [ctypes.POINTER(ctypes.c_float),
+                                            ctypes.POINTER(ctypes.c_int), I]
+        lib.gdpa_timing_collect.restype = I
         _lib = lib
         return lib
 
@@ -167,3 +173,20 @@ def device_status(stream=None) -> int:
 
 def last_launch_count() -> int:
     return int(load().gdpa_last_launch_count())
+
+
+def timing_enable(on: bool = True) -> None:
+    load().gdpa_timing_enable(1 if on else 0)
+
+
+def timing_collect(max_n: int = 4096):
+    """Per-launch durations (ms) of the main kernels recorded while timing was
+    enabled: returns (fwd_ms list, bwd_ms list)."""
+    ms = (ctypes.c_float * max_n)()
+    kind = (ctypes.c_int * max_n)()
+    n = load().gdpa_timing_collect(ms, kind, max_n)
+    if n < 0:
+        raise GdpaError(4, "gdpa_timing_collect")
+    f = [ms[i] for i in range(n) if kind[i] == 0]
+    b = [ms[i] for i in range(n) if kind[i] == 1]
+    return f, b

@@ -25,6 +25,30 @@ std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 thread_local int t_launches = 0;
 
+// Optional timing of the main kernels (gdpa_timing_enable / _collect).
+constexpr int kMaxTimed = 4096;
+struct TimingRing {
+  bool enabled = false;
+  int n = 0;
+  int kind[kMaxTimed];
+  cudaEvent_t ev[2 * kMaxTimed] = {};
+};
+thread_local TimingRing* t_timing = nullptr;
+
+// Returns the event pair to record around the next main kernel, or false.
+bool timing_slot(int kind, cudaEvent_t* a, cudaEvent_t* b) {
+  TimingRing* r = t_timing;
+  if (r == nullptr || !r->enabled || r->n >= kMaxTimed) return false;
+  const int i = r->n;
+  for (int e = 0; e < 2; ++e)
+    if (r->ev[2 * i + e] == nullptr && cudaEventCreate(&r->ev[2 * i + e]) != cudaSuccess) return false;
+  r->kind[i] = kind;
+  *a = r->ev[2 * i];
+  *b = r->ev[2 * i + 1];
+  r->n = i + 1;
+  return true;
+}
+
 cudaError_t device_info(DeviceInfo** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -176,7 +200,11 @@ gdpa_status gdpa_fwd(const void* q, const int32_t* q_offsets, const void* k, con
   p.status = dev->status;
   const int64_t max_items = max_fwd_items(B, H, Tq);
   const int grid = static_cast<int>(max_items < dev->sms ? max_items : dev->sms);
+  cudaEvent_t ea = nullptr, eb = nullptr;
+  const bool timed = timing_slot(0, &ea, &eb);
+  if (timed && cudaEventRecord(ea, s) != cudaSuccess) return GDPA_ERR_CUDA;
   if (launch_fwd(p, act, tq, tk, tv, grid, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (timed && cudaEventRecord(eb, s) != cudaSuccess) return GDPA_ERR_CUDA;
   ++t_launches;
   return GDPA_OK;
 }
@@ -199,9 +227,88 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
   gdpa_status st = check_common(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act,
                                 causal);
   if (st != GDPA_OK) return st;
-  (void)scale; (void)out; (void)lse; (void)dout; (void)dq; (void)dk; (void)dv;
-  (void)workspace; (void)ws_bytes; (void)stream;
-  return GDPA_ERR_UNSUPPORTED;
+  if (Tq > 0 && (dout == nullptr || dq == nullptr || !aligned16(dout) || !aligned16(dq)))
+    return GDPA_ERR_INVALID_ARG;
+  if (Tkv > 0 && (dk == nullptr || dv == nullptr || !aligned16(dk) || !aligned16(dv)))
+    return GDPA_ERR_INVALID_ARG;
+  if (act == GDPA_ACT_SOFTMAX && Tq > 0 && (out == nullptr || lse == nullptr || !aligned16(out)))
+    return GDPA_ERR_INVALID_ARG;
+  const size_t need = gdpa_bwd_workspace_size(B, H, d, Tq, Tkv);
+  if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return GDPA_ERR_WORKSPACE;
+  if (B == 0 || (Tq == 0 && Tkv == 0)) return GDPA_OK;
+
+  DeviceInfo* dev = nullptr;
+  if (device_info(&dev) != cudaSuccess) return GDPA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  int max_rel = 1;
+  const float* table = bias_table(bias, &max_rel);
+  // Maps need at least one row; an empty side is never loaded, so any
+  // valid tensor stands in for it.
+  const void* qb = Tq > 0 ? q : k;
+  const void* dob = Tq > 0 ? dout : k;
+  const int64_t Tqm = Tq > 0 ? Tq : Tkv;
+  const void* kb = Tkv > 0 ? k : q;
+  const void* vb = Tkv > 0 ? v : q;
+  const int64_t Tkm = Tkv > 0 ? Tkv : Tq;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_thd_map(&tq, qb, Tqm, H, d, kBwdQRows) || !make_thd_map(&tdo, dob, Tqm, H, d, kBwdQRows) ||
+      !make_thd_map(&tk, kb, Tkm, H, d, kBwdKvRows) || !make_thd_map(&tv, vb, Tkm, H, d, kBwdKvRows))
+    return GDPA_ERR_INVALID_ARG;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* n_items = reinterpret_cast<int*>(ws);
+  int* ticket = reinterpret_cast<int*>(ws + 4);
+  size_t off = 256;
+  int2* items = reinterpret_cast<int2*>(ws + off);
+  off += align_up(static_cast<size_t>(max_bwd_items(B, H, Tkv)) * sizeof(int2), 256);
+  float* dq_acc = reinterpret_cast<float*>(ws + off);
+  off += align_up(static_cast<size_t>(Tq) * H * d * sizeof(float), 256);
+  float* delta = reinterpret_cast<float*>(ws + off);
+
+  if (launch_build_worklist(kv_offsets, q_offsets, B, H, Tkv, Tq, causal, 1, items, n_items,
+                            ticket, dev->status, s) != cudaSuccess)
+    return GDPA_ERR_CUDA;
+  ++t_launches;
+
+  BwdParams p{};
+  p.qo = q_offsets;
+  p.ko = kv_offsets;
+  p.B = B;
+  p.H = H;
+  p.d = d;
+  p.Tq = Tq;
+  p.Tkv = Tkv;
+  p.bias_table = table;
+  p.max_rel = max_rel;
+  p.causal = causal;
+  p.scale = scale;
+  p.out = static_cast<const __nv_bfloat16*>(out);
+  p.lse = lse;
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.dq_acc = dq_acc;
+  p.delta = delta;
+  p.items = items;
+  p.n_items = n_items;
+  p.ticket = ticket;
+  p.status = dev->status;
+  const int64_t max_items = max_bwd_items(B, H, Tkv);
+  const int grid = static_cast<int>(max_items < dev->sms ? (max_items > 0 ? max_items : 1) : dev->sms);
+  int launches = 0;
+  cudaEvent_t ea = nullptr, eb = nullptr;
+  const bool timed = timing_slot(1, &ea, &eb);
+  cudaError_t e = launch_bwd(p, act, tq, tk, tv, tdo, grid, s, &launches,
+                             timed ? ea : nullptr, timed ? eb : nullptr);
+  t_launches += launches;
+  if (e != cudaSuccess) return GDPA_ERR_CUDA;
+  if (Tq > 0) {
+    if (launch_dq_convert(dq_acc, dq, static_cast<long long>(Tq) * H * d, scale, s) != cudaSuccess)
+      return GDPA_ERR_CUDA;
+    ++t_launches;
+  }
+  return GDPA_OK;
 }
 
 gdpa_status gdpa_get_device_status(void* stream) {
@@ -234,5 +341,26 @@ const char* gdpa_status_string(int status) {
 }
 
 int gdpa_last_launch_count(void) { return t_launches; }
+
+gdpa_status gdpa_timing_enable(int enable) {
+  if (t_timing == nullptr) t_timing = new TimingRing();
+  if (enable) t_timing->n = 0;
+  t_timing->enabled = enable != 0;
+  return GDPA_OK;
+}
+
+int gdpa_timing_collect(float* ms, int* kind, int max) {
+  TimingRing* r = t_timing;
+  if (r == nullptr) return 0;
+  const int n = r->n < max ? r->n : max;
+  for (int i = 0; i < n; ++i) {
+    if (cudaEventSynchronize(r->ev[2 * i + 1]) != cudaSuccess) return -1;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r->ev[2 * i], r->ev[2 * i + 1]) != cudaSuccess) return -1;
+    if (ms != nullptr) ms[i] = t;
+    if (kind != nullptr) kind[i] = r->kind[i];
+  }
+  return n;
+}
 
 }  // extern "C"

@@ -1,0 +1,677 @@
+// Backward kernels of jagged attention with a pluggable activation, sm_103a.
+//
+// "GEM Training ..." JFA paragraph ("efficient backward passes") and GDPA
+// paragraph (1.6x backward speedup).  The gradients follow from the chain
+// rule on s = scale q.k + bias, p = act(s) (or softmax), o = sum p v:
+//   dV = P^T dO,  dP = dO V^T,  dS = P*(dP - D) (softmax, D = rowsum(dO*O))
+//   or act'(S)*dP (GDPA),  dQ = scale dS K,  dK = scale dS^T Q.
+//
+// Main kernel: key/value-major.  A work item is one 128-row key/value block
+// of one (sample, head); the CTA keeps K and V of the block in shared memory
+// and streams the sample's queries past it in 64-row tiles.  Everything is
+// computed transposed so that TMEM lanes are key rows:
+//   S^T = K Q^T, dP^T = V dO^T           (M = 128 keys, N = 64 queries)
+//   dV += P^T dO, dK += dS^T Q           (accumulated in TMEM over the tiles)
+//   dQ^T = K^T dS^T                      (M = d, N = 64) -> fp32 atomics
+// P^T goes back into the S^T columns of TMEM (A operand of dV); dS^T is
+// written to a swizzled shared-memory tile that is both the K-major A
+// operand of dK and the MN-major B operand of dQ^T.
+//
+// Warp roles (320 threads, one CTA per SM, persistent over the cost-sorted
+// work list):
+//   warps 0-3  activation group: P^T, dS^T from S^T, dP^T
+//   warps 4-7  dQ group: dQ^T tile -> fp32 atomics; dK/dV epilogue
+//   warp  8    producer: TMA loads of K/V, Q/dO tiles; lse and D values
+//   warp  9    MMA issuer
+// TMEM columns: S^T/P^T buffers [0,64) [64,128), dP^T [128,192),
+// dQ^T [192,256), dV [256,256+d), dK [384,384+d).
+//
+// Small kernels: preprocess (zero the dQ accumulator, D = rowsum(dO*O)) and
+// the dQ conversion (fp32 accumulator * scale -> bf16).
+#include "common.cuh"
+
+namespace gdpa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D, bool SPLIT>
+struct BwdCfg {
+  static constexpr int kKvTileBytes = kBwdKvRows * D * 2;     // K or V block
+  static constexpr int kQTileBytes = kBwdQRows * D * 2;       // Q or dO tile
+  static constexpr int kDsBytes = kBwdKvRows * kBwdQRows * 2;  // one dS^T tile (16 KB)
+  static constexpr int kDsParts = SPLIT ? 2 : 1;
+  static constexpr int kStages = 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kKvTileBytes;
+  static constexpr int kQ = 2 * kKvTileBytes;                  // + s * 2 * qtile ; dO = Q + qtile
+  static constexpr int kDs = kQ + kStages * 2 * kQTileBytes;   // + buf * parts * ds + part * ds
+  static constexpr int kStats = kDs + 2 * kDsParts * kDsBytes; // float lse2[64], D[64] per stage
+  static constexpr int kBar = kStats + kStages * 2 * kBwdQRows * 4;
+  static constexpr int kKvFull = 0, kKvEmpty = 1;
+  static constexpr int kQdFull = 2;                 // + s
+  static constexpr int kQdEmpty = kQdFull + kStages;
+  static constexpr int kSFull = kQdEmpty + kStages; // + buffer
+  static constexpr int kPFull = kSFull + 2;
+  static constexpr int kDqFull = kPFull + 1;
+  static constexpr int kDqEmpty = kDqFull + 1;
+  static constexpr int kDkvFull = kDqEmpty + 1;
+  static constexpr int kDkvEmpty = kDkvFull + 1;
+  static constexpr int kItemFull = kDkvEmpty + 1;   // + slot
+  static constexpr int kItemEmpty = kItemFull + 2;
+  static constexpr int kDrain = kItemEmpty + 2;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kItemSlots = kBar + 8 * kNumBars;
+  static constexpr int kTmemSlot = kItemSlots + 16;
+  static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kUsed = kAbort + 4;
+  static constexpr int kSmemBytes = kUsed + 1024;
+};
+
+// TMEM column bases
+constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 192, kColDV = 256, kColDK = 384;
+
+struct BwdItem {
+  int b, head, kb;
+  int q0, k0, Lq, Lkv;
+  int qt0;  // first query tile (64 rows) visited
+  int nq;   // number of query tiles visited
+};
+
+__device__ __forceinline__ BwdItem decode_bwd(int2 it, const BwdParams& p) {
+  BwdItem r;
+  r.b = it.x;
+  r.head = item_head(it);
+  r.kb = item_block(it);
+  r.q0 = p.qo[r.b];
+  r.Lq = p.qo[r.b + 1] - r.q0;
+  r.k0 = p.ko[r.b];
+  r.Lkv = p.ko[r.b + 1] - r.k0;
+  r.qt0 = p.causal ? (r.kb * kBwdKvRows) / kBwdQRows : 0;
+  const int rows = r.Lq - r.qt0 * kBwdQRows;
+  r.nq = rows > 0 ? (rows + kBwdQRows - 1) / kBwdQRows : 0;
+  return r;
+}
+
+// act(x) and act'(x) for the GDPA activations (tanh forms).
+template <int ACT>
+__device__ __forceinline__ void act_and_grad(float x, float& a, float& g) {
+  if (ACT == GDPA_ACT_SILU) {
+    const float h = 0.5f * x;
+    const float t = tanh_approx(h);
+    const float sg = fmaf(0.5f, t, 0.5f);           // sigmoid(x)
+    a = x * sg;
+    g = sg * fmaf(x, 1.0f - sg, 1.0f);               // sigmoid * (1 + x (1 - sigmoid))
+  } else if (ACT == GDPA_ACT_GELU_TANH) {
+    const float k0 = 0.7978845608028654f, k1 = 0.7978845608028654f * 0.044715f;
+    const float x2 = x * x;
+    const float t = tanh_approx(x * fmaf(k1, x2, k0));
+    const float h = 0.5f * x;
+    a = fmaf(h, t, h);
+    // 0.5 (1 + t) + 0.5 x (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 x^2)
+    g = fmaf(0.5f, t, 0.5f) + h * (1.0f - t * t) * fmaf(3.0f * k1, x2, k0);
+  } else {
+    a = x;
+    g = 1.0f;
+  }
+}
+
+template <int D, int ACT>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+           const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
+           const BwdParams p) {
+  constexpr bool kSoftmax = (ACT == GDPA_ACT_SOFTMAX);
+  constexpr bool kSplit = !kSoftmax;
+  using C = BwdCfg<D, kSplit>;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kBar + 8u * i; };
+  int2* item_slot = reinterpret_cast<int2*>(gbase + C::kItemSlots);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kAbort);
+  float* stats = reinterpret_cast<float*>(gbase + C::kStats);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(C::kKvFull), 1);
+    mbar_init(bar(C::kKvEmpty), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kQdFull + s), 1);
+      mbar_init(bar(C::kQdEmpty + s), 1);
+    }
+    mbar_init(bar(C::kSFull + 0), 1);
+    mbar_init(bar(C::kSFull + 1), 1);
+    mbar_init(bar(C::kPFull), 128);
+    mbar_init(bar(C::kDqFull), 1);
+    mbar_init(bar(C::kDqEmpty), 128);
+    mbar_init(bar(C::kDkvFull), 1);
+    mbar_init(bar(C::kDkvEmpty), 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::kItemFull + s), 1);
+      mbar_init(bar(C::kItemEmpty + s), 1 + 256);
+    }
+    mbar_init(bar(C::kDrain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_v);
+    prefetch_tmap(&tmap_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    set_status(p.status, GDPA_ERR_TIMEOUT);
+  };
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer (whole warp)
+    const int n_items = *p.n_items;
+    uint32_t it = 0, g = 0, kvi = 0;
+    bool kv_inflight = false;
+    uint32_t inflight = 0, last_g[C::kStages] = {};
+    bool ok = true;
+    while (ok) {
+      int2 item = make_int2(-1, 0);
+      if (lane == 0) {
+        const int t = atomicAdd(p.ticket, 1);
+        if (t < n_items) item = p.items[t];
+      }
+      item.x = __shfl_sync(0xffffffffu, item.x, 0);
+      item.y = __shfl_sync(0xffffffffu, item.y, 0);
+      const uint32_t slot = it & 1u;
+      bool w = mbar_wait(bar(C::kItemEmpty + slot), ((it >> 1) & 1u) ^ 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+      if (lane == 0) {
+        item_slot[slot] = item;
+        mbar_arrive(bar(C::kItemFull + slot));
+      }
+      ++it;
+      if (item.x < 0) break;
+      const BwdItem in = decode_bwd(item, p);
+      if (in.nq == 0) continue;
+      w = mbar_wait(bar(C::kKvEmpty), (kvi & 1u) ^ 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+      ++kvi;
+      const int krow = in.k0 + in.kb * kBwdKvRows;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(C::kKvFull), 2 * C::kKvTileBytes);
+        for (int x = 0; x < D; x += 64) {
+          tma_load_3d(sbase + C::kK + (x / 64) * (kBwdKvRows * 128), &tmap_k, bar(C::kKvFull), x,
+                      in.head, krow);
+          tma_load_3d(sbase + C::kV + (x / 64) * (kBwdKvRows * 128), &tmap_v, bar(C::kKvFull), x,
+                      in.head, krow);
+        }
+        kv_inflight = true;
+      }
+      for (int t = 0; t < in.nq; ++t, ++g) {
+        const uint32_t s = g % C::kStages;
+        const uint32_t ph = (g / C::kStages) & 1u;
+        w = mbar_wait(bar(C::kQdEmpty + s), ph ^ 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; if (lane == 0) fail(); break; }
+        const int qloc = (in.qt0 + t) * kBwdQRows;  // first local query row of the tile
+        float* st = stats + s * 2 * kBwdQRows;
+        for (int c = lane; c < kBwdQRows; c += 32) {
+          const int ql = qloc + c;
+          float l2 = 0.0f, dd = 0.0f;
+          if (ql < in.Lq) {
+            const long long gi = static_cast<long long>(in.head) * p.Tq + in.q0 + ql;
+            if (kSoftmax) {
+              l2 = p.lse[gi] * kLog2e;
+              dd = p.delta[gi];
+            }
+          }
+          st[c] = l2;
+          st[kBwdQRows + c] = dd;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t qd = sbase + C::kQ + s * 2 * C::kQTileBytes;
+          mbar_arrive_expect_tx(bar(C::kQdFull + s), 2 * C::kQTileBytes);
+          for (int x = 0; x < D; x += 64) {
+            tma_load_3d(qd + (x / 64) * (kBwdQRows * 128), &tmap_q, bar(C::kQdFull + s), x,
+                        in.head, in.q0 + qloc);
+            tma_load_3d(qd + C::kQTileBytes + (x / 64) * (kBwdQRows * 128), &tmap_do,
+                        bar(C::kQdFull + s), x, in.head, in.q0 + qloc);
+          }
+          inflight |= 1u << s;
+          last_g[s] = g;
+        }
+      }
+    }
+    if (lane == 0 && *abort_flag) {
+      for (int s = 0; s < C::kStages; ++s)
+        if (inflight & (1u << s))
+          mbar_wait(bar(C::kQdFull + s), (last_g[s] / C::kStages) & 1u, nullptr, 50000000ull);
+      if (kv_inflight) mbar_wait(bar(C::kKvFull), (kvi - 1) & 1u, nullptr, 50000000ull);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_f16(128, kBwdQRows, true, false, false);
+      constexpr uint32_t idesc_acc = idesc_f16(128, D, true, false, true);
+      constexpr uint32_t idesc_dq = idesc_f16(128, kBwdQRows, true, true, true);
+      uint32_t it = 0, g = 0, kvi = 0, pc = 0, dqc = 0, dkvc = 0;
+      uint32_t suse[2] = {0, 0};
+      bool issued_any = false;
+      auto issue_sdp = [&](int t, uint32_t s) {
+        const uint32_t buf = t & 1;
+        const uint32_t qd = sbase + C::kQ + s * 2 * C::kQTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t aoff = (ks / 4) * (kBwdKvRows * 128) + (ks % 4) * 32;
+          const uint32_t boff = (ks / 4) * (kBwdQRows * 128) + (ks % 4) * 32;
+          mma_f16_ss(tmem + kColS + buf * 64, sdesc(sbase + C::kK + aoff, 0, 1024, kSwizzle128B),
+                     sdesc(qd + boff, 0, 1024, kSwizzle128B), idesc_s, ks > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t aoff = (ks / 4) * (kBwdKvRows * 128) + (ks % 4) * 32;
+          const uint32_t boff = (ks / 4) * (kBwdQRows * 128) + (ks % 4) * 32;
+          mma_f16_ss(tmem + kColDP, sdesc(sbase + C::kV + aoff, 0, 1024, kSwizzle128B),
+                     sdesc(qd + C::kQTileBytes + boff, 0, 1024, kSwizzle128B), idesc_s,
+                     ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kSFull + buf));
+        issued_any = true;
+      };
+      bool ok = true;
+      while (ok) {
+        const uint32_t slot = it & 1u;
+        if (!mbar_wait(bar(C::kItemFull + slot), (it >> 1) & 1u, abort_flag)) { fail(); break; }
+        const int2 item = item_slot[slot];
+        mbar_arrive(bar(C::kItemEmpty + slot));
+        ++it;
+        if (item.x < 0) break;
+        const BwdItem in = decode_bwd(item, p);
+        if (in.nq == 0) continue;
+        if (!mbar_wait(bar(C::kKvFull), kvi & 1u, abort_flag)) { fail(); break; }
+        ++kvi;
+        {
+          const uint32_t s = g % C::kStages;
+          if (!mbar_wait(bar(C::kQdFull + s), (g / C::kStages) & 1u, abort_flag)) { fail(); break; }
+          tc_fence_after();
+          issue_sdp(0, s);
+        }
+        for (int t = 0; t < in.nq; ++t) {
+          const uint32_t gt = g + t;
+          const uint32_t s = gt % C::kStages;
+          const uint32_t buf = t & 1;
+          if (!mbar_wait(bar(C::kPFull), pc & 1u, abort_flag)) { ok = false; fail(); break; }
+          ++pc;
+          tc_fence_after();
+          if (t + 1 < in.nq) {
+            const uint32_t s1 = (gt + 1) % C::kStages;
+            if (!mbar_wait(bar(C::kQdFull + s1), ((gt + 1) / C::kStages) & 1u, abort_flag)) { ok = false; fail(); break; }
+            tc_fence_after();
+            issue_sdp(t + 1, s1);
+          }
+          if (t == 0) {
+            // previous item's dK/dV must have been read out before we overwrite them
+            if (!mbar_wait(bar(C::kDkvEmpty), (dkvc & 1u) ^ 1u, abort_flag)) { ok = false; fail(); break; }
+            tc_fence_after();
+          }
+          const uint32_t qd = sbase + C::kQ + s * 2 * C::kQTileBytes;
+          const uint32_t ds = sbase + C::kDs + buf * C::kDsParts * C::kDsBytes;
+          // dV += P^T dO   (A = P^T in TMEM, B = dO tile, MN-major)
+#pragma unroll
+          for (int ks = 0; ks < kBwdQRows / 16; ++ks) {
+            const uint64_t bd = sdesc(qd + C::kQTileBytes + ks * 2048, kBwdQRows * 128, 1024,
+                                      kSwizzle128B);
+            const uint32_t pcol = tmem + kColS + buf * 64 + 32 * (ks / 2) + 8 * (ks % 2);
+            mma_f16_ts(tmem + kColDV, pcol, bd, idesc_acc, (t == 0 && ks == 0) ? 0u : 1u);
+            if (kSplit) mma_f16_ts(tmem + kColDV, pcol + 16, bd, idesc_acc, 1u);
+          }
+          // dK += dS^T Q   (A = dS^T smem K-major, B = Q tile MN-major)
+#pragma unroll
+          for (int ks = 0; ks < kBwdQRows / 16; ++ks) {
+            const uint64_t bd = sdesc(qd + ks * 2048, kBwdQRows * 128, 1024, kSwizzle128B);
+#pragma unroll
+            for (int part = 0; part < C::kDsParts; ++part) {
+              const uint64_t ad = sdesc(ds + part * C::kDsBytes + ks * 32, 0, 1024, kSwizzle128B);
+              mma_f16_ss(tmem + kColDK, ad, bd, idesc_acc, (t == 0 && ks == 0 && part == 0) ? 0u : 1u);
+            }
+          }
+          mma_commit(bar(C::kQdEmpty + s));
+          // dQ^T = K^T dS^T  (A = K block MN-major, B = dS^T MN-major); wait until
+          // the dQ group has drained the previous tile's dQ^T.
+          if (!mbar_wait(bar(C::kDqEmpty), (dqc & 1u) ^ 1u, abort_flag)) { ok = false; fail(); break; }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < kBwdKvRows / 16; ++ks) {
+            // d = 64: the second 64-row half of A repeats the first (LBO 0); its
+            // output lanes 64..127 are ignored.
+            const uint64_t ad = sdesc(sbase + C::kK + ks * 2048, D == 128 ? kBwdKvRows * 128 : 0,
+                                      1024, kSwizzle128B);
+#pragma unroll
+            for (int part = 0; part < C::kDsParts; ++part) {
+              const uint64_t bd = sdesc(ds + part * C::kDsBytes + ks * 2048, 0, 1024, kSwizzle128B);
+              mma_f16_ss(tmem + kColDQ, ad, bd, idesc_dq, (ks == 0 && part == 0) ? 0u : 1u);
+            }
+          }
+          mma_commit(bar(C::kDqFull));
+          ++dqc;
+          suse[buf]++;
+        }
+        if (!ok) break;
+        mma_commit(bar(C::kDkvFull));
+        mma_commit(bar(C::kKvEmpty));
+        ++dkvc;
+        g += in.nq;
+      }
+      if (issued_any) {
+        mma_commit(bar(C::kDrain));
+        mbar_wait(bar(C::kDrain), 0, nullptr, 100000000ull);
+      }
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ activation group
+    const int j = warp * 32 + lane;  // key row within the block = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float c_s = kSoftmax ? p.scale * kLog2e : p.scale;
+    const float c_b = kSoftmax ? kLog2e : 1.0f;
+    const int rel_w = 2 * p.max_rel - 1;
+    uint32_t it = 0, g = 0;
+    uint32_t suse[2] = {0, 0};
+    while (true) {
+      const uint32_t slot = it & 1u;
+      bool w = mbar_wait(bar(C::kItemFull + slot), (it >> 1) & 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+      const int2 item = item_slot[slot];
+      mbar_arrive(bar(C::kItemEmpty + slot));
+      ++it;
+      if (item.x < 0) break;
+      const BwdItem in = decode_bwd(item, p);
+      const int jl = in.kb * kBwdKvRows + j;  // local key row
+      const bool key_ok = jl < in.Lkv;
+      const float* brow = p.bias_table ? p.bias_table + static_cast<long long>(in.head) * rel_w : nullptr;
+      bool abort_now = false;
+      for (int t = 0; t < in.nq; ++t, ++g) {
+        const uint32_t s = g % C::kStages;
+        const uint32_t buf = t & 1;
+        w = mbar_wait(bar(C::kQdFull + s), (g / C::kStages) & 1u, abort_flag);
+        w = w && mbar_wait(bar(C::kSFull + buf), suse[buf] & 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); abort_now = true; break; }
+        suse[buf]++;
+        tc_fence_after();
+        const float* st = stats + s * 2 * kBwdQRows;
+        const int qloc = (in.qt0 + t) * kBwdQRows;
+        const uint32_t t_s = tmem + lane_off + kColS + buf * 64;
+        const uint32_t t_dp = tmem + lane_off + kColDP;
+        uint8_t* dsrow = gbase + C::kDs + buf * C::kDsParts * C::kDsBytes + j * 128;
+#pragma unroll 1
+        for (int chunk = 0; chunk < 2; ++chunk) {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(t_s + chunk * 32, sr);
+          tmem_ld32(t_dp + chunk * 32, dr);
+          uint32_t phi[16], plo[16], dhi[16], dlo[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float pv[2], dv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int c = chunk * 32 + i + e;
+              const int ql = qloc + c;
+              const bool valid = key_ok && ql < in.Lq && (!p.causal || ql >= jl);
+              float x = __uint_as_float(sr[i + e]) * c_s;
+              if (brow != nullptr) {
+                const int idx = min(max(ql - jl + p.max_rel - 1, 0), rel_w - 1);
+                x = fmaf(__ldg(brow + idx), c_b, x);
+              }
+              const float dp = __uint_as_float(dr[i + e]);
+              if (kSoftmax) {
+                const float pp = valid ? ex2_approx(x - st[c]) : 0.0f;
+                pv[e] = pp;
+                dv[e] = pp * (dp - st[kBwdQRows + c]);
+              } else {
+                float a, gr;
+                act_and_grad<ACT>(x, a, gr);
+                pv[e] = valid ? a : 0.0f;
+                dv[e] = valid ? gr * dp : 0.0f;
+              }
+            }
+            const uint32_t ph = pack_bf16x2(pv[0], pv[1]);
+            const uint32_t dh = pack_bf16x2(dv[0], dv[1]);
+            phi[i / 2] = ph;
+            dhi[i / 2] = dh;
+            if (kSplit) {
+              plo[i / 2] = pack_bf16x2(pv[0] - __uint_as_float(ph << 16),
+                                       pv[1] - __uint_as_float(ph & 0xFFFF0000u));
+              dlo[i / 2] = pack_bf16x2(dv[0] - __uint_as_float(dh << 16),
+                                       dv[1] - __uint_as_float(dh & 0xFFFF0000u));
+            }
+          }
+          tmem_st16(t_s + chunk * 32, phi);
+          if (kSplit) tmem_st16(t_s + chunk * 32 + 16, plo);
+          // dS^T row j, 128-byte swizzle: 16-byte chunk c of the row lives at (c ^ (j % 8))
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int cc = chunk * 4 + v;
+            const int phys = (cc ^ (j & 7)) * 16;
+            *reinterpret_cast<uint4*>(dsrow + phys) =
+                make_uint4(dhi[4 * v], dhi[4 * v + 1], dhi[4 * v + 2], dhi[4 * v + 3]);
+            if (kSplit)
+              *reinterpret_cast<uint4*>(dsrow + C::kDsBytes + phys) =
+                  make_uint4(dlo[4 * v], dlo[4 * v + 1], dlo[4 * v + 2], dlo[4 * v + 3]);
+          }
+        }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(C::kPFull));
+      }
+      if (abort_now) break;
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ dQ group + dK/dV epilogue
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // TMEM lane: channel (dQ^T) or key row (dK, dV)
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    uint32_t it = 0, dqc = 0, dkvc = 0;
+    while (true) {
+      const uint32_t slot = it & 1u;
+      bool w = mbar_wait(bar(C::kItemFull + slot), (it >> 1) & 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+      const int2 item = item_slot[slot];
+      mbar_arrive(bar(C::kItemEmpty + slot));
+      ++it;
+      if (item.x < 0) break;
+      const BwdItem in = decode_bwd(item, p);
+      bool abort_now = false;
+      for (int t = 0; t < in.nq; ++t) {
+        w = mbar_wait(bar(C::kDqFull), dqc & 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); abort_now = true; break; }
+        ++dqc;
+        tc_fence_after();
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tmem + lane_off + kColDQ, v0);
+        tmem_ld32(tmem + lane_off + kColDQ + 32, v1);
+        tc_fence_before();
+        mbar_arrive(bar(C::kDqEmpty));
+        if (r < D) {
+          const int qloc = (in.qt0 + t) * kBwdQRows;
+          const int nvalid = min(kBwdQRows, in.Lq - qloc);
+          float* base = p.dq_acc + (static_cast<long long>(in.q0 + qloc) * p.H + in.head) * D + r;
+          const long long rs = static_cast<long long>(p.H) * D;
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c < nvalid) atomicAdd(base + c * rs, __uint_as_float(v0[c]));
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c + 32 < nvalid) atomicAdd(base + (c + 32) * rs, __uint_as_float(v1[c]));
+        }
+      }
+      if (abort_now) break;
+      // epilogue: dV and dK rows of this key block
+      const int jl = in.kb * kBwdKvRows + r;
+      const bool row_ok = jl < in.Lkv;
+      const long long grow = (static_cast<long long>(in.k0 + jl) * p.H + in.head) * D;
+      if (in.nq > 0) {
+        w = mbar_wait(bar(C::kDkvFull), dkvc & 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+        ++dkvc;
+        tc_fence_after();
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t col = which ? kColDK : kColDV;
+          const float mul = which ? p.scale : 1.0f;
+          __nv_bfloat16* dst = (which ? p.dk : p.dv) + grow;
+#pragma unroll 1
+          for (int chunk = 0; chunk < D / 32; ++chunk) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_off + col + chunk * 32, o);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * mul, __uint_as_float(o[2 * i + 1]) * mul);
+            if (row_ok) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + chunk * 32);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(C::kDkvEmpty));
+      } else if (row_ok) {
+        uint4* a4 = reinterpret_cast<uint4*>(p.dv + grow);
+        uint4* b4 = reinterpret_cast<uint4*>(p.dk + grow);
+        for (int v = 0; v < D / 8; ++v) {
+          a4[v] = make_uint4(0, 0, 0, 0);
+          b4[v] = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Zero the fp32 dQ accumulator and (softmax) compute D = rowsum(dO * O).
+// One warp per (row, head); lanes cover the d channels.
+template <int D>
+__global__ void __launch_bounds__(256)
+bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
+                      float* __restrict__ delta, float* __restrict__ dq_acc, long long Tq, int H,
+                      int softmax) {
+  const long long nrows = Tq * H;
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+  for (long long row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; row < nrows; row += warps) {
+    float4* acc = reinterpret_cast<float4*>(dq_acc + row * D);
+    for (int v = lane; v < D / 4; v += 32) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (softmax) {
+      float s = 0.f;
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(out + row * D);
+      const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(dout + row * D);
+      for (int c = lane; c < D / 2; c += 32) {
+        const float2 a = __bfloat1622float2(o2[c]);
+        const float2 b = __bfloat1622float2(d2[c]);
+        s = fmaf(a.x, b.x, fmaf(a.y, b.y, s));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (lane == 0) {
+        const long long t = row / H, h = row % H;
+        delta[h * Tq + t] = s;
+      }
+    }
+  }
+}
+
+// dq = bf16(dq_acc * scale)
+__global__ void __launch_bounds__(256)
+dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, long long n4, float scale) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 a = acc[i];
+    dq[i] = make_uint2(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale));
+  }
+}
+
+template <int D, int ACT>
+cudaError_t launch_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, const CUtensorMap& tdo, int grid, cudaStream_t s) {
+  using C = BwdCfg<D, ACT != GDPA_ACT_SOFTMAX>;
+  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, ACT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  bwd_kernel<D, ACT><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_main_d(const BwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo, int grid, cudaStream_t s) {
+  switch (act) {
+    case GDPA_ACT_SOFTMAX: return launch_main<D, GDPA_ACT_SOFTMAX>(p, tq, tk, tv, tdo, grid, s);
+    case GDPA_ACT_SILU: return launch_main<D, GDPA_ACT_SILU>(p, tq, tk, tv, tdo, grid, s);
+    case GDPA_ACT_GELU_TANH: return launch_main<D, GDPA_ACT_GELU_TANH>(p, tq, tk, tv, tdo, grid, s);
+    default: return launch_main<D, GDPA_ACT_IDENTITY>(p, tq, tk, tv, tdo, grid, s);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, int grid,
+                       cudaStream_t stream, int* launches, cudaEvent_t ev_begin,
+                       cudaEvent_t ev_end) {
+  // 1) zero dQ accumulator, D = rowsum(dO * O)
+  const long long rows = p.Tq * p.H;
+  const int pre_blocks = static_cast<int>(rows / 8 + 1 < 4096 ? rows / 8 + 1 : 4096);
+  if (p.d == 64)
+    bwd_preprocess_kernel<64><<<pre_blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
+                                                              p.Tq, p.H, act == GDPA_ACT_SOFTMAX);
+  else
+    bwd_preprocess_kernel<128><<<pre_blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
+                                                               p.Tq, p.H, act == GDPA_ACT_SOFTMAX);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ++*launches;
+  // 2) main kernel (optionally bracketed by timing events)
+  if (ev_begin != nullptr && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess) return e;
+  e = (p.d == 64) ? launch_main_d<64>(p, act, tq, tk, tv, tdo, grid, stream)
+                  : launch_main_d<128>(p, act, tq, tk, tv, tdo, grid, stream);
+  if (e != cudaSuccess) return e;
+  if (ev_end != nullptr && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess) return e;
+  ++*launches;
+  return cudaSuccess;
+}
+
+cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale,
+                              cudaStream_t stream) {
+  const long long n4 = n / 4;
+  const int blocks = static_cast<int>(n4 / 256 + 1 < 8192 ? n4 / 256 + 1 : 8192);
+  dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(acc),
+                                                reinterpret_cast<uint2*>(dq), n4, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace gdpa

@@ -1,0 +1,484 @@
+#!/usr/bin/env python
+"""Benchmark of the jagged attention hot path on GB300.
+
+A step is one forward plus one backward pass of jagged attention over one
+batch of synthetic input (default workload: causal softmax self-attention
+with a relative-position bias, B=32, lengths ~ U[1,4096] (fill 0.5), H=4,
+d=128), run through the C ABI.  The metric is TFLOPS counted on non-padded
+work only: forward 4*H*d*sum(unmasked query-key pairs), backward 2.5x that.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdpa|reference]
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun, one rank per GPU) each
+rank runs an independent replica on its own seed (the attention has no
+exchange step): value = total FLOPs of all ranks / max time over ranks.
+`--impl reference` times the fp64 CPU oracle instead (rank 0 only), on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "jagged attn fwd/bwd TFLOPS (non-padded FLOPs) & % of GB300 BF16 tensor peak"
+UNIT = "TFLOPS"
+BWD_FLOP_FACTOR = 2.5
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic():
+    """DRAM bytes per launch from the committed ncu summary, keyed
+    "<workload>/<act>/<fwd|bwd>".  An entry is dropped (reported as null) when
+    the kernel's source has changed since the counters were taken."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return {}
+    csrc = os.path.join(ROOT, "jagged_attention_recsys_02_gb300", "csrc")
+    ok = {}
+    for key, src in (("fwd", "fwd.cu"), ("bwd", "bwd.cu")):
+        try:
+            with open(os.path.join(csrc, src), "rb") as f:
+                h = hashlib.sha256(f.read()).hexdigest()[:16]
+        except OSError:
+            h = None
+        ok[key] = h is not None and d.get("sources", {}).get(src) == h
+    return {k: v for k, v in d.items() if "/" in k and ok.get(k.rsplit("/", 1)[1], False)}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            lines = [ln.strip() for ln in f if ln.strip()]
+        os.unlink(self.tmp.name)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": float(np.median(busy)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ ranks
+def reduce_over_ranks(ms, flops, device=None):
+    """Max of the timed duration and sum of the work over all ranks (a no-op
+    without an initialised process group of more than one rank)."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(ms), float(flops)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    f = torch.tensor([float(flops)], dtype=torch.float64, device=device)
+    dist.all_reduce(f, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(f.item())
+
+
+# ------------------------------------------------------------------ workload
+def workload_flops(w):
+    f = w.fwd_flops()
+    return f, BWD_FLOP_FACTOR * f
+
+
+def pick_cpu_sample(w, target_pairs, seed=0):
+    """Deterministic subset of samples whose pair count is close to target_pairs."""
+    order = np.random.default_rng(seed + 12345).permutation(w.B)
+    pairs = (w.lq * (w.lq + 1) // 2) if w.causal else (w.lq * w.lkv)
+    chosen, tot = [], 0
+    for b in order:
+        if pairs[b] == 0:
+            continue
+        if tot > 0 and tot + pairs[b] > target_pairs:
+            continue
+        chosen.append(int(b))
+        tot += int(pairs[b])
+        if tot >= 0.9 * target_pairs:
+            break
+    return sorted(chosen), tot
+
+
+def oracle_step(w, tensors, samples):
+    """One oracle forward + backward over the given samples (host float64)."""
+    import oracle
+
+    qo, ko = w.offsets()
+    a = {"softmax": 0, "silu": 1, "gelu_tanh": 2, "identity": 3}[w.act]
+    bias = tensors.get("bias_np")
+    for b in samples:
+        q0, q1, k0, k1 = int(qo[b]), int(qo[b + 1]), int(ko[b]), int(ko[b + 1])
+        sq = tensors["q_np"][q0:q1]
+        sk = tensors["k_np"][k0:k1]
+        sv = tensors["v_np"][k0:k1]
+        sd = tensors["do_np"][q0:q1]
+        oq = np.array([0, q1 - q0], dtype=np.int32)
+        ok = np.array([0, k1 - k0], dtype=np.int32)
+        oracle.fwd(sq, oq, sk, sv, ok, act=a, causal=w.causal, scale=w.scale, bias=bias,
+                   max_rel=w.max_rel)
+        oracle.bwd(sq, oq, sk, sv, ok, sd, act=a, causal=w.causal, scale=w.scale, bias=bias,
+                   max_rel=w.max_rel)
+
+
+def host_sample_tensors(w, samples, device_tensors=None, seed=0):
+    """float64 host copies of the chosen samples (other rows left zero)."""
+    import torch
+
+    out = {}
+    if device_tensors is not None:
+        src = device_tensors
+    else:
+        from jagged_attention_recsys_02_gb300.workloads import make_tensors
+
+        src = make_tensors(w, device="cpu", seed=seed)
+    qo, ko = w.offsets()
+    for name, key, offs in (("q_np", "q", qo), ("do_np", "dout", qo), ("k_np", "k", ko),
+                            ("v_np", "v", ko)):
+        t = src[key]
+        arr = np.zeros(tuple(t.shape), dtype=np.float64)
+        for b in samples:
+            a0, a1 = int(offs[b]), int(offs[b + 1])
+            arr[a0:a1] = t[a0:a1].float().cpu().double().numpy()
+        out[name] = arr
+    if src.get("bias") is not None:
+        out["bias_np"] = src["bias"].cpu().double().numpy()
+    del torch
+    return out
+
+
+def cpu_cores():
+    n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    env = os.environ.get("OMP_NUM_THREADS")
+    if env and env.isdigit():
+        n = min(n, int(env))
+    return int(n)
+
+
+def measure_oracle(w, seconds, device_tensors=None, seed=0):
+    """Time the oracle on a bounded sample sized to take about `seconds`.
+    Returns (tflops, sample_desc, wall_seconds)."""
+    import oracle
+
+    oracle.build()
+    # calibrate on a small sample
+    cal, cal_pairs = pick_cpu_sample(w, 2e5, seed)
+    t_host = host_sample_tensors(w, cal, device_tensors, seed)
+    t0 = time.perf_counter()
+    oracle_step(w, t_host, cal)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    rate = cal_pairs / dt
+    samples, pairs = pick_cpu_sample(w, max(cal_pairs, rate * seconds), seed)
+    t_host = host_sample_tensors(w, samples, device_tensors, seed)
+    t0 = time.perf_counter()
+    oracle_step(w, t_host, samples)
+    dt = time.perf_counter() - t0
+    flops = (1.0 + BWD_FLOP_FACTOR) * 4.0 * w.H * w.d * pairs
+    desc = (f"{len(samples)} of {w.B} samples ({pairs} of {w.pairs()} non-padded query-key "
+            f"pairs), forward + backward, fp64")
+    return flops / dt / 1e12, desc, dt
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    from jagged_attention_recsys_02_gb300.workloads import make_workload
+
+    if rank != 0:
+        return 0
+    w = make_workload(args.workload, act=args.act)
+    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    import oracle
+
+    oracle.build()
+    cal, cal_pairs = pick_cpu_sample(w, 2e5, 0)
+    t_host = host_sample_tensors(w, cal, None, 0)
+    t0 = time.perf_counter()
+    oracle_step(w, t_host, cal)
+    rate = cal_pairs / max(time.perf_counter() - t0, 1e-3)
+    samples, pairs = pick_cpu_sample(w, max(cal_pairs, rate * budget), 0)
+    t_host = host_sample_tensors(w, samples, None, 0)
+    for _ in range(args.warmup):
+        oracle_step(w, t_host, samples)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, t_host, samples)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    flops = (1.0 + BWD_FLOP_FACTOR) * 4.0 * w.H * w.d * pairs
+    value = flops / dt / 1e12
+    desc = (f"{len(samples)} of {w.B} samples ({pairs} of {w.pairs()} non-padded query-key "
+            f"pairs) per step, forward + backward, fp64")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, "oracle on host cores"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, l2_note):
+    return {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "act": w.act, "causal": w.causal,
+            "bias": (f"relpos table [{w.H},{2 * w.max_rel - 1}]" if w.max_rel else "none"),
+            "Tq": w.Tq, "Tkv": w.Tkv, "pairs_non_padded": w.pairs(),
+            "pairs_full_square": w.full_pairs(), "step": "forward + backward", "l2": l2_note}
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from jagged_attention_recsys_02_gb300 import binding
+    from jagged_attention_recsys_02_gb300.workloads import ACTS, make_tensors, make_workload
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=dev)
+    binding.load()
+    w = make_workload(args.workload, act=args.act)
+    t = make_tensors(w, device=dev, seed=rank)
+    a = ACTS[w.act]
+    H, d, Tq, Tkv = w.H, w.d, w.Tq, w.Tkv
+    out = torch.empty_like(t["q"])
+    lse = torch.empty((H, Tq), device=dev, dtype=torch.float32)
+    dq = torch.empty_like(t["q"])
+    dk = torch.empty_like(t["k"])
+    dv = torch.empty_like(t["v"])
+    ws_f = torch.empty(binding.fwd_workspace_size(w.B, H, d, Tq, Tkv), device=dev, dtype=torch.uint8)
+    ws_b = torch.empty(binding.bwd_workspace_size(w.B, H, d, Tq, Tkv), device=dev, dtype=torch.uint8)
+    kw = dict(act=a, causal=w.causal, scale=w.scale, bias=t["bias"], max_rel=w.max_rel)
+    fwd_flops, bwd_flops = workload_flops(w)
+
+    def step(q, qo, k, v, ko, do):
+        binding.gdpa_fwd(q, qo, k, v, ko, out=out, lse=lse, workspace=ws_f, **kw)
+        n = binding.last_launch_count()
+        binding.gdpa_bwd(q, qo, k, v, ko, out, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws_b, **kw)
+        return n + binding.last_launch_count()
+
+    args_dev = (t["q"], t["qo"], t["k"], t["v"], t["ko"], t["dout"])
+    for _ in range(args.warmup):
+        step(*args_dev)
+    torch.cuda.synchronize()
+    st = binding.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    binding.timing_enable(True)
+    launches = 0
+    e0.record()
+    for _ in range(args.steps):
+        launches += step(*args_dev)
+    e1.record()
+    torch.cuda.synchronize()
+    binding.timing_enable(False)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    fwd_ms, bwd_ms = binding.timing_collect()
+    st = binding.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed region")
+
+    # max time over ranks, total FLOPs over ranks
+    ms, tot_flops = reduce_over_ranks(ms, (fwd_flops + bwd_flops) * args.steps, dev)
+    value = tot_flops / (ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    region_s = ms * 1e-3
+    sustained = region_s > 2.0
+    peak = float(peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"])
+    f_avg = float(np.mean(fwd_ms)) if fwd_ms else float("nan")
+    b_avg = float(np.mean(bwd_ms)) if bwd_ms else float("nan")
+    f_tf = fwd_flops / (f_avg * 1e-3) / 1e12
+    b_tf = bwd_flops / (b_avg * 1e-3) / 1e12
+    dominant = "bwd" if sum(bwd_ms) >= sum(fwd_ms) else "fwd"
+    achieved = b_tf if dominant == "bwd" else f_tf
+    traffic = load_traffic().get(f"{w.name}/{w.act}/{dominant}")
+
+    # ---------------- end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = {k_: t[k_].cpu().pin_memory() for k_ in ("q", "k", "v", "dout", "qo", "ko")}
+        hbias = t["bias"].cpu().pin_memory() if t["bias"] is not None else None
+        host_out = {k_: torch.empty(tuple(x.shape), dtype=x.dtype, pin_memory=True)
+                    for k_, x in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+        dev_in = {k_: torch.empty_like(t[k_]) for k_ in pin}
+        dbias = torch.empty_like(t["bias"]) if hbias is not None else None
+        h2d = sum(x.numel() * x.element_size() for x in pin.values())
+        h2d += hbias.numel() * hbias.element_size() if hbias is not None else 0
+        d2h = sum(x.numel() * x.element_size() for x in host_out.values())
+
+        def e2e_step():
+            for k_, x in pin.items():
+                dev_in[k_].copy_(x, non_blocking=True)
+            if hbias is not None:
+                dbias.copy_(hbias, non_blocking=True)
+            binding.gdpa_fwd(dev_in["q"], dev_in["qo"], dev_in["k"], dev_in["v"], dev_in["ko"],
+                             act=a, causal=w.causal, scale=w.scale, bias=dbias,
+                             max_rel=w.max_rel, out=out, lse=lse, workspace=ws_f)
+            binding.gdpa_bwd(dev_in["q"], dev_in["qo"], dev_in["k"], dev_in["v"], dev_in["ko"],
+                             out, lse, dev_in["dout"], act=a, causal=w.causal, scale=w.scale,
+                             bias=dbias, max_rel=w.max_rel, dq=dq, dk=dk, dv=dv, workspace=ws_b)
+            for k_, x in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+                host_out[k_].copy_(x, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, args.steps // 2)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_e, _ = reduce_over_ranks(e0.elapsed_time(e1), 0.0, dev)
+        e2e = {"value": tot_flops / args.steps * n_e2e / (ms_e * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": ms_e / n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, desc, secs = measure_oracle(w, args.cpu_seconds, device_tensors=t, seed=rank)
+        cpu = {"value": tf, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": desc,
+               "seconds": secs}
+
+    in_bytes = sum(x.numel() * x.element_size() for x in (t["q"], t["k"], t["v"], t["dout"]))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 inputs, lengths per workload recipe)",
+        "config": workload_config(
+            w, f"inputs larger than L2: {in_bytes / 2**20:.0f} MiB of q,k,v,dO per step "
+               f"(no flush)"),
+        "pct_of_peak": {"value": 100.0 * value / peak, "peak_tflops": peak,
+                        "peak": ("bf16_tflops_sustained" if sustained else "bf16_tflops")
+                        + f" of {peak_src}"},
+        "fwd": {"tflops": f_tf, "kernel_ms": f_avg, "flops_per_launch": fwd_flops},
+        "bwd": {"tflops": b_tf, "kernel_ms": b_avg, "flops_per_launch": bwd_flops},
+        "roofline": {"bound": "tensor", "kernel": f"{dominant} main kernel",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": ("bf16_tflops_sustained" if sustained else "bf16_tflops")
+                     + f" of {peak_src}"},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gdpa", choices=["gdpa", "reference"])
+    ap.add_argument("--workload", default="jfa_causal_relpos")
+    ap.add_argument("--act", default=None, help="override the workload's activation")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

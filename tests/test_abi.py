@@ -1,0 +1,125 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+include/gdpa.h declares, and rejects bad arguments on the host before any
+CUDA call (no kernel is launched in this file)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from jagged_attention_recsys_02_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdpa.h")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdpa_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\b(gdpa_[a-z_0-9]+)\b", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    for code, name in binding.STATUS_NAMES.items():
+        assert lib.gdpa_status_string(code).decode() == name
+    assert lib.gdpa_status_string(99).decode() == "GDPA_ERR_UNKNOWN"
+
+
+def test_workspace_sizes(lib):
+    f = lib.gdpa_fwd_workspace_size
+    b = lib.gdpa_bwd_workspace_size
+    assert f(4, 2, 64, 105, 105) >= 256 + 8 * 2 * (105 // 256 + 4)
+    assert f(32, 4, 128, 10**6, 10**6) > f(32, 4, 128, 10**5, 10**6)
+    # backward: work list + fp32 dQ accumulator + D
+    assert b(4, 2, 64, 105, 105) >= 105 * 2 * 64 * 4 + 105 * 2 * 4
+    assert f(-1, 2, 64, 1, 1) == 0 and b(2, 0, 64, 1, 1) == 0
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def _fwd(lib, **kw):
+    a = dict(q=FAKE, qo=FAKE, k=FAKE, v=FAKE, ko=FAKE, B=2, H=2, d=64, Tq=10, Tkv=10, bias=None,
+             act=0, causal=0, scale=0.125, out=FAKE, lse=FAKE, ws=FAKE, ws_bytes=1 << 20,
+             stream=None)
+    a.update(kw)
+    return lib.gdpa_fwd(a["q"], a["qo"], a["k"], a["v"], a["ko"], a["B"], a["H"], a["d"], a["Tq"],
+                        a["Tkv"], a["bias"], a["act"], a["causal"], a["scale"], a["out"],
+                        a["lse"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+def _bwd(lib, **kw):
+    a = dict(q=FAKE, qo=FAKE, k=FAKE, v=FAKE, ko=FAKE, B=2, H=2, d=64, Tq=10, Tkv=10, bias=None,
+             act=0, causal=0, scale=0.125, out=FAKE, lse=FAKE, do=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+             ws=FAKE, ws_bytes=1 << 20, stream=None)
+    a.update(kw)
+    return lib.gdpa_bwd(a["q"], a["qo"], a["k"], a["v"], a["ko"], a["B"], a["H"], a["d"], a["Tq"],
+                        a["Tkv"], a["bias"], a["act"], a["causal"], a["scale"], a["out"],
+                        a["lse"], a["do"], a["dq"], a["dk"], a["dv"], a["ws"], a["ws_bytes"],
+                        a["stream"])
+
+
+@pytest.mark.parametrize("call", [_fwd, _bwd])
+def test_host_rejections(lib, call):
+    assert call(lib, d=96) == UNSUPPORTED
+    assert call(lib, d=256) == UNSUPPORTED
+    assert call(lib, H=300) == UNSUPPORTED
+    assert call(lib, H=0) == INVALID
+    assert call(lib, B=-1) == INVALID
+    assert call(lib, Tq=-5) == INVALID
+    assert call(lib, act=7) == INVALID
+    assert call(lib, causal=2) == INVALID
+    assert call(lib, qo=None) == INVALID
+    assert call(lib, ko=None) == INVALID
+    assert call(lib, q=None) == INVALID
+    assert call(lib, k=FAKE + 8) == INVALID         # not 16-byte aligned
+    assert call(lib, ws=None) == WORKSPACE
+    assert call(lib, ws_bytes=16) == WORKSPACE
+    bad_bias = binding.gdpa_bias(binding.BIAS_RELPOS, None, 16)
+    assert call(lib, bias=ctypes.byref(bad_bias)) == INVALID
+    bad_rel = binding.gdpa_bias(binding.BIAS_RELPOS, FAKE, 0)
+    assert call(lib, bias=ctypes.byref(bad_rel)) == INVALID
+    odd_kind = binding.gdpa_bias(7, FAKE, 4)
+    assert call(lib, bias=ctypes.byref(odd_kind)) == INVALID
+
+
+def test_fwd_specific_rejections(lib):
+    assert _fwd(lib, out=None) == INVALID
+    assert _fwd(lib, lse=None) == INVALID             # softmax needs lse
+    assert _fwd(lib, out=FAKE + 4) == INVALID
+
+
+def test_bwd_specific_rejections(lib):
+    assert _bwd(lib, do=None) == INVALID
+    assert _bwd(lib, dk=None) == INVALID
+    assert _bwd(lib, lse=None) == INVALID             # softmax needs lse
+    assert _bwd(lib, dq=FAKE + 2) == INVALID
+
+
+def test_empty_problem_is_a_no_op(lib):
+    # B = 0 or Tq = 0: nothing to do, returns before touching the device
+    assert _fwd(lib, B=0, Tq=0, Tkv=0) == OK
+    assert _fwd(lib, Tq=0) == OK
+    assert _bwd(lib, B=0, Tq=0, Tkv=0) == OK

@@ -1,0 +1,94 @@
+"""Host-side logic that needs no GPU: the seeded workload recipes and the
+benchmark's aggregation over ranks (world_size 2 over gloo on CPU)."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+from jagged_attention_recsys_02_gb300.workloads import CONFIG_NAMES, make_tensors, make_workload
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_workload_recipes():
+    w = make_workload("tiny_silu")
+    assert list(w.lq) == [1, 7, 33, 64] and (w.H, w.d, w.act) == (2, 64, "silu")
+    w = make_workload("jfa_causal_relpos")
+    assert w.B == 32 and w.causal and w.max_rel == 4096 and np.array_equal(w.lq, w.lkv)
+    assert w.lq.min() >= 1 and w.lq.max() <= 4096
+    assert w.pairs() == int(np.sum(w.lq * (w.lq + 1) // 2))
+    w = make_workload("gdpa_cross_gelu")
+    assert w.lq.min() >= 64 and w.lq.max() <= 8192 and w.lkv.min() >= 32 and w.lkv.max() <= 256
+    w = make_workload("gdpa_pma_silu")
+    assert np.all(w.lq == 32) and w.pma_seeds == 32 and w.H == 8
+    assert w.lkv.min() >= 16 and w.lkv.max() <= 16384
+    w = make_workload("heavy_tail")
+    assert w.B == 1024 and w.lq.min() >= 16 and w.lq.max() <= 16384
+    # log-normal around 1024: the median sits near 1024
+    assert 700 < np.median(w.lq) < 1400
+
+
+def test_workloads_are_seeded():
+    for name in CONFIG_NAMES:
+        a, b = make_workload(name, seed=0), make_workload(name, seed=0)
+        assert np.array_equal(a.lq, b.lq) and np.array_equal(a.lkv, b.lkv)
+    assert not np.array_equal(make_workload("heavy_tail", seed=0).lq,
+                              make_workload("heavy_tail", seed=1).lq)
+
+
+def test_tensors_shapes_and_pma_sharing():
+    w = make_workload("tiny_silu")
+    t = make_tensors(w, device="cpu")
+    assert t["q"].shape == (105, 2, 64) and t["q"].dtype == torch.bfloat16
+    assert t["qo"].tolist() == [0, 1, 8, 41, 105]
+    t2 = make_tensors(w, device="cpu")
+    assert torch.equal(t["q"], t2["q"]) and torch.equal(t["dout"], t2["dout"])
+    w = make_workload("gdpa_pma_silu")
+    w.lkv = np.full(w.B, 16)  # shrink for the test
+    t = make_tensors(w, device="cpu", with_dout=False)
+    q = t["q"].view(w.B, 32, w.H, w.d)
+    assert torch.equal(q[0], q[-1])  # seed queries are shared by every sample
+
+
+_WORKER = r'''
+import os, sys, json
+sys.path.insert(0, sys.argv[1])
+import torch.distributed as dist
+import bench
+rank = int(sys.argv[2])
+dist.init_process_group("gloo", init_method="tcp://127.0.0.1:" + sys.argv[3], rank=rank,
+                        world_size=2)
+ms, flops = bench.reduce_over_ranks(1.5 + rank, 10.0 * (rank + 1))
+print(json.dumps({"rank": rank, "ms": ms, "flops": flops}))
+dist.destroy_process_group()
+'''
+
+
+def test_reduce_over_ranks_gloo_world2(tmp_path):
+    import socket
+
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    script = tmp_path / "worker.py"
+    script.write_text(_WORKER)
+    procs = [subprocess.Popen([sys.executable, str(script), ROOT, str(r), str(port)],
+                              stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+             for r in range(2)]
+    outs = [p.communicate(timeout=120) for p in procs]
+    for p, (o, e) in zip(procs, outs):
+        assert p.returncode == 0, e
+    res = [json.loads(o.strip().splitlines()[-1]) for o, _ in outs]
+    for r in res:
+        assert r["ms"] == 2.5 and r["flops"] == 30.0
+
+
+def test_reduce_over_ranks_single_process():
+    import bench
+
+    assert bench.reduce_over_ranks(3.0, 7.0) == (3.0, 7.0)

@@ -136,6 +136,28 @@ int gdpa_last_launch_count(void);
 gdpa_status gdpa_timing_enable(int enable);
 int gdpa_timing_collect(float* ms, int* kind, int max);
 
+/* Forward pass that allocates nothing and needs no workspace argument.  The
+ * paper has no counterpart: this entry point exists for callers that cannot
+ * allocate device memory -- for example a plugin running inside a framework
+ * that has already reserved the GPU's memory for its own pool, or a service
+ * whose memory plan forbids allocations after start-up -- and so cannot pass
+ * the workspace gdpa_fwd asks for.
+ *
+ * Arguments and results are those of gdpa_fwd without workspace/ws_bytes.
+ * The scratch comes from one 1 MiB array compiled into the library (every
+ * GPU that loads the library holds it until the process exits).  Problems
+ * whose gdpa_fwd_workspace_size() exceeds 1 MiB (about H * (Tq/256 + B) >
+ * 131,000 work items) are refused with GDPA_ERR_WORKSPACE before anything is
+ * launched.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  All calls share the array: calls whose kernels may overlap on the
+ * GPU (different streams or host threads) race and give undefined results,
+ * so serialise them. */
+gdpa_status gdpa_fwd_noalloc(const void* q, const int32_t* q_offsets, const void* k,
+                             const void* v, const int32_t* kv_offsets, int B, int H, int d,
+                             int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
+                             float scale, void* out, float* lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

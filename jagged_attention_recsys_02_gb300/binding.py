@@ -28,7 +28,7 @@ STATUS_NAMES = {0: "GDPA_OK", 1: "GDPA_ERR_INVALID_ARG", 2: "GDPA_ERR_UNSUPPORTE
 # Every symbol include/gdpa.h declares.
 EXPORTS = ("gdpa_fwd_workspace_size", "gdpa_fwd", "gdpa_bwd_workspace_size", "gdpa_bwd",
            "gdpa_get_device_status", "gdpa_status_string", "gdpa_last_launch_count",
-           "gdpa_timing_enable", "gdpa_timing_collect")
+           "gdpa_timing_enable", "gdpa_timing_collect", "gdpa_fwd_noalloc")
 
 
 class GdpaError(RuntimeError):

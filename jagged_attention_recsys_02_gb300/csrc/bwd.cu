@@ -17,12 +17,13 @@
 // written to a swizzled shared-memory tile that is both the K-major A
 // operand of dK and the MN-major B operand of dQ^T.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over the cost-sorted
+// Warp roles (448 threads, one CTA per SM, persistent over the cost-sorted
 // work list):
-//   warps 0-3  activation group: P^T, dS^T from S^T, dP^T
-//   warps 4-7  dQ group: dQ^T tile -> fp32 atomics; dK/dV epilogue
-//   warp  8    producer: TMA loads of K/V, Q/dO tiles; lse and D values
-//   warp  9    MMA issuer
+//   warps 0-3  activation group A: P^T, dS^T for query columns [0,32) of a tile
+//   warps 4-7  activation group B: the same for query columns [32,64)
+//   warps 8-11 dQ group: dQ^T tile -> fp32 atomics; dK/dV epilogue
+//   warp  12   producer: TMA loads of K/V, Q/dO tiles; lse, D and bias values
+//   warp  13   MMA issuer
 // TMEM columns: S^T/P^T buffers [0,64) [64,128), dP^T [128,192),
 // dQ^T [192,256), dV [256,256+d), dK [384,384+d).
 //
@@ -35,9 +36,10 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kThreads = 448;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kActThreads = 256;  // both activation groups
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D, bool SPLIT>
@@ -51,8 +53,10 @@ struct BwdCfg {
   static constexpr int kV = kKvTileBytes;
   static constexpr int kQ = 2 * kKvTileBytes;                  // + s * 2 * qtile ; dO = Q + qtile
   static constexpr int kDs = kQ + kStages * 2 * kQTileBytes;   // + buf * parts * ds + part * ds
-  static constexpr int kStats = kDs + 2 * kDsParts * kDsBytes; // float lse2[64], D[64] per stage
-  static constexpr int kBar = kStats + kStages * 2 * kBwdQRows * 4;
+  // per stage: float lse2[64], D[64], bias window[192]
+  static constexpr int kStatFloats = 2 * kBwdQRows + kBwdQRows + kBwdKvRows;
+  static constexpr int kStats = kDs + 2 * kDsParts * kDsBytes;
+  static constexpr int kBar = kStats + kStages * kStatFloats * 4;
   static constexpr int kKvFull = 0, kKvEmpty = 1;
   static constexpr int kQdFull = 2;                 // + s
   static constexpr int kQdEmpty = kQdFull + kStages;
@@ -153,14 +157,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
     }
     mbar_init(bar(C::kSFull + 0), 1);
     mbar_init(bar(C::kSFull + 1), 1);
-    mbar_init(bar(C::kPFull), 128);
+    mbar_init(bar(C::kPFull), kActThreads);
     mbar_init(bar(C::kDqFull), 1);
     mbar_init(bar(C::kDqEmpty), 128);
     mbar_init(bar(C::kDkvFull), 1);
     mbar_init(bar(C::kDkvEmpty), 128);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kItemFull + s), 1);
-      mbar_init(bar(C::kItemEmpty + s), 1 + 256);
+      mbar_init(bar(C::kItemEmpty + s), 1 + kActThreads + 128);
     }
     mbar_init(bar(C::kDrain), 1);
     fence_mbar_init();
@@ -231,7 +235,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         w = mbar_wait(bar(C::kQdEmpty + s), ph ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, w)) { ok = false; if (lane == 0) fail(); break; }
         const int qloc = (in.qt0 + t) * kBwdQRows;  // first local query row of the tile
-        float* st = stats + s * 2 * kBwdQRows;
+        float* st = stats + s * C::kStatFloats;
         for (int c = lane; c < kBwdQRows; c += 32) {
           const int ql = qloc + c;
           float l2 = 0.0f, dd = 0.0f;
@@ -244,6 +248,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
           }
           st[c] = l2;
           st[kBwdQRows + c] = dd;
+        }
+        if (p.bias_table != nullptr) {
+          // bias(i - j) for query column c and key row jj of the tile is window
+          // entry c - jj + 127 (the tile spans 64 + 127 relative positions)
+          const int rel_w = 2 * p.max_rel - 1;
+          const float* brow = p.bias_table + static_cast<long long>(in.head) * rel_w;
+          const int w0 = qloc - in.kb * kBwdKvRows - (kBwdKvRows - 1) + p.max_rel - 1;
+          for (int e = lane; e < kBwdQRows + kBwdKvRows - 1; e += 32)
+            st[2 * kBwdQRows + e] = __ldg(brow + min(max(w0 + e, 0), rel_w - 1));
         }
         __syncwarp();
         if (lane == 0) {
@@ -385,13 +398,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         mbar_wait(bar(C::kDrain), 0, nullptr, 100000000ull);
       }
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ activation group
-    const int j = warp * 32 + lane;  // key row within the block = TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ activation groups
+    const int wq = warp & 3;
+    const int cbase = (warp >> 2) * 32;  // this group's 32 query columns of the tile
+    const int j = wq * 32 + lane;        // key row within the block = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const float c_s = kSoftmax ? p.scale * kLog2e : p.scale;
     const float c_b = kSoftmax ? kLog2e : 1.0f;
-    const int rel_w = 2 * p.max_rel - 1;
+    const bool has_bias = p.bias_table != nullptr;
     uint32_t it = 0, g = 0;
     uint32_t suse[2] = {0, 0};
     while (true) {
@@ -403,9 +418,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       ++it;
       if (item.x < 0) break;
       const BwdItem in = decode_bwd(item, p);
-      const int jl = in.kb * kBwdKvRows + j;  // local key row
+      const int kb0 = in.kb * kBwdKvRows;   // first local key row of the block
+      const int jl = kb0 + j;               // this thread's local key row
       const bool key_ok = jl < in.Lkv;
-      const float* brow = p.bias_table ? p.bias_table + static_cast<long long>(in.head) * rel_w : nullptr;
+      const bool keys_full = kb0 + kBwdKvRows <= in.Lkv;
       bool abort_now = false;
       for (int t = 0; t < in.nq; ++t, ++g) {
         const uint32_t s = g % C::kStages;
@@ -415,40 +431,50 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); abort_now = true; break; }
         suse[buf]++;
         tc_fence_after();
-        const float* st = stats + s * 2 * kBwdQRows;
+        const float* st = stats + s * C::kStatFloats;
+        const float* bwin = st + 2 * kBwdQRows + (kBwdKvRows - 1) - j;  // bwin[c] = bias(q c, key j)
         const int qloc = (in.qt0 + t) * kBwdQRows;
+        // Tiles strictly inside the sample (and below the causal diagonal) need no mask.
+        const bool full = keys_full && qloc + kBwdQRows <= in.Lq &&
+                          (!p.causal || qloc >= kb0 + kBwdKvRows - 1);
+        int c_lo = 0, c_hi = kBwdQRows;  // valid query columns: c_lo <= c < c_hi
+        if (!full) {
+          c_hi = key_ok ? min(kBwdQRows, in.Lq - qloc) : 0;
+          if (p.causal) c_lo = max(0, jl - qloc);
+        }
         const uint32_t t_s = tmem + lane_off + kColS + buf * 64;
         const uint32_t t_dp = tmem + lane_off + kColDP;
         uint8_t* dsrow = gbase + C::kDs + buf * C::kDsParts * C::kDsBytes + j * 128;
-#pragma unroll 1
-        for (int chunk = 0; chunk < 2; ++chunk) {
-          uint32_t sr[32], dr[32];
-          tmem_ld32(t_s + chunk * 32, sr);
-          tmem_ld32(t_dp + chunk * 32, dr);
-          uint32_t phi[16], plo[16], dhi[16], dlo[16];
+        uint32_t sr[32];
+        tmem_ld32(t_s + cbase, sr);  // all 32 scores first: P overwrites them in place
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
+        for (int half = 0; half < 2; ++half) {
+          const int c0 = cbase + half * 16;
+          uint32_t dr[16];
+          tmem_ld16(t_dp + c0, dr);
+          uint32_t phi[8], plo[8], dhi[8], dlo[8];
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
             float pv[2], dv[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int c = chunk * 32 + i + e;
-              const int ql = qloc + c;
-              const bool valid = key_ok && ql < in.Lq && (!p.causal || ql >= jl);
-              float x = __uint_as_float(sr[i + e]) * c_s;
-              if (brow != nullptr) {
-                const int idx = min(max(ql - jl + p.max_rel - 1, 0), rel_w - 1);
-                x = fmaf(__ldg(brow + idx), c_b, x);
-              }
+              const int c = c0 + i + e;
+              const float sv = __uint_as_float(sr[half * 16 + i + e]);
               const float dp = __uint_as_float(dr[i + e]);
+              const float bv = has_bias ? bwin[c] : 0.0f;
               if (kSoftmax) {
-                const float pp = valid ? ex2_approx(x - st[c]) : 0.0f;
+                const float pp = ex2_approx(fmaf(bv, c_b, fmaf(sv, c_s, -st[c])));
                 pv[e] = pp;
                 dv[e] = pp * (dp - st[kBwdQRows + c]);
               } else {
                 float a, gr;
-                act_and_grad<ACT>(x, a, gr);
-                pv[e] = valid ? a : 0.0f;
-                dv[e] = valid ? gr * dp : 0.0f;
+                act_and_grad<ACT>(fmaf(sv, c_s, bv), a, gr);
+                pv[e] = a;
+                dv[e] = gr * dp;
+              }
+              if (!full && (c < c_lo || c >= c_hi)) {
+                pv[e] = 0.0f;
+                dv[e] = 0.0f;
               }
             }
             const uint32_t ph = pack_bf16x2(pv[0], pv[1]);
@@ -462,12 +488,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
                                        dv[1] - __uint_as_float(dh & 0xFFFF0000u));
             }
           }
-          tmem_st16(t_s + chunk * 32, phi);
-          if (kSplit) tmem_st16(t_s + chunk * 32 + 16, plo);
-          // dS^T row j, 128-byte swizzle: 16-byte chunk c of the row lives at (c ^ (j % 8))
+          // P^T: query pair c/2 of the 32-column chunk lives at column chunk*32 + c/2 (hi)
+          // and chunk*32 + 16 + c/2 (lo), where the dV MMA reads it.
+          const uint32_t pc = t_s + cbase + half * 8;
+          tmem_st8(pc, phi);
+          if (kSplit) tmem_st8(pc + 16, plo);
+          // dS^T row j, 128-byte swizzle: 16-byte chunk cc of the row lives at (cc ^ (j % 8))
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int cc = chunk * 4 + v;
+          for (int v = 0; v < 2; ++v) {
+            const int cc = c0 / 8 + v;
             const int phys = (cc ^ (j & 7)) * 16;
             *reinterpret_cast<uint4*>(dsrow + phys) =
                 make_uint4(dhi[4 * v], dhi[4 * v + 1], dhi[4 * v + 2], dhi[4 * v + 3]);
@@ -483,7 +512,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       }
       if (abort_now) break;
     }
-  } else if (warp < 8) {
+  } else if (warp < 12) {
     // ------------------------------------------------------------ dQ group + dK/dV epilogue
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // TMEM lane: channel (dQ^T) or key row (dK, dV)

@@ -54,7 +54,9 @@ struct FwdCfg {
   static constexpr int kQ0 = 0;
   static constexpr int kQ1 = kQHalfBytes;
   static constexpr int kKV = 2 * kQHalfBytes;                          // K[s] = kKV + s*2*tile
-  static constexpr int kBar = kKV + kStages * 2 * kTileBytes;         // barriers after tiles
+  // per stage and half: bias window of 256 floats (255 relative positions)
+  static constexpr int kBias = kKV + kStages * 2 * kTileBytes;
+  static constexpr int kBar = kBias + kStages * 2 * 256 * 4;          // barriers after tiles
   // barrier block layout (8 bytes each)
   static constexpr int kQFull = 0, kQEmpty = 1;
   static constexpr int kKFull = 2;                                     // + s
@@ -176,39 +178,69 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
   };
 
   if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const int n_items = *p.n_items;
-      uint32_t it = 0, g = 0, qi = 0;
-      uint32_t inflight = 0;  // stages whose K/V load may still be in flight (abort drain)
-      bool q_inflight = false;
-      uint32_t last_g[C::kStages] = {};
-      bool ok = true;
-      while (ok) {
+    // ------------------------------------------------------------ producer (whole warp)
+    // Lane 0 takes tickets and issues the TMA copies; all lanes stage the
+    // bias windows of each key tile (when there is a bias).
+    const int n_items = *p.n_items;
+    const int rel_w = 2 * p.max_rel - 1;
+    float* bias_win = reinterpret_cast<float*>(gbase + C::kBias);
+    uint32_t it = 0, g = 0, qi = 0;
+    uint32_t inflight = 0;  // stages whose K/V load may still be in flight (abort drain)
+    bool q_inflight = false;
+    uint32_t last_g[C::kStages] = {};
+    bool ok = true;
+    while (ok) {
+      int2 item = make_int2(-1, 0);
+      if (lane == 0) {
         const int t = atomicAdd(p.ticket, 1);
-        const int2 item = (t < n_items) ? p.items[t] : make_int2(-1, 0);
-        const uint32_t slot = it & 1u;
-        if (!mbar_wait(bar(C::kItemEmpty + slot), ((it >> 1) & 1u) ^ 1u, abort_flag)) { fail(); break; }
+        if (t < n_items) item = p.items[t];
+      }
+      item.x = __shfl_sync(0xffffffffu, item.x, 0);
+      item.y = __shfl_sync(0xffffffffu, item.y, 0);
+      const uint32_t slot = it & 1u;
+      bool w = mbar_wait(bar(C::kItemEmpty + slot), ((it >> 1) & 1u) ^ 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+      if (lane == 0) {
         item_slot[slot] = item;
         mbar_arrive(bar(C::kItemFull + slot));
-        ++it;
-        if (item.x < 0) break;
-        const ItemInfo in = decode_item(item, p);
-        const int n = max(in.n0, in.n1);
-        if (n == 0) continue;
-        if (!mbar_wait(bar(C::kQEmpty), (qi & 1u) ^ 1u, abort_flag)) { fail(); break; }
-        const int row0 = in.q0 + in.blk * kItemRows;
+      }
+      ++it;
+      if (item.x < 0) break;
+      const ItemInfo in = decode_item(item, p);
+      const int n = max(in.n0, in.n1);
+      if (n == 0) continue;
+      w = mbar_wait(bar(C::kQEmpty), (qi & 1u) ^ 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+      const int row0 = in.q0 + in.blk * kItemRows;
+      if (lane == 0) {
         mbar_arrive_expect_tx(bar(C::kQFull), (in.n1 > 0 ? 2 : 1) * C::kQHalfBytes);
         for (int half = 0; half < (in.n1 > 0 ? 2 : 1); ++half)
           for (int x = 0; x < D; x += 64)
             tma_load_3d(sbase + (half ? C::kQ1 : C::kQ0) + (x / 64) * (kHalfRows * 128),
                         &tmap_q, bar(C::kQFull), x, in.head, row0 + half * kHalfRows);
         q_inflight = true;
-        ++qi;
-        for (int j = 0; j < n; ++j, ++g) {
-          const uint32_t s = g % C::kStages;
-          const uint32_t ph = (g / C::kStages) & 1u;
-          if (!mbar_wait(bar(C::kKvEmpty + s), ph ^ 1u, abort_flag)) { ok = false; fail(); break; }
+      }
+      ++qi;
+      const float* brow =
+          p.bias_table ? p.bias_table + static_cast<long long>(in.head) * rel_w : nullptr;
+      for (int j = 0; j < n; ++j, ++g) {
+        const uint32_t s = g % C::kStages;
+        const uint32_t ph = (g / C::kStages) & 1u;
+        w = mbar_wait(bar(C::kKvEmpty + s), ph ^ 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; if (lane == 0) fail(); break; }
+        if (brow != nullptr) {
+          // Window entry e of half h holds bias(i - j) for (i - r_h) - (j - c0) = e - 127,
+          // where r_h is the half's first local row and c0 the tile's first local column.
+          for (int h = 0; h < 2; ++h) {
+            const int w0 = in.blk * kItemRows + h * kHalfRows - j * kKvRows - (kKvRows - 1) +
+                           p.max_rel - 1;
+            float* win = bias_win + (s * 2 + h) * 256;
+            for (int e = lane; e < 255; e += 32)
+              win[e] = __ldg(brow + min(max(w0 + e, 0), rel_w - 1));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
           const uint32_t kdst = sbase + C::kKV + s * 2 * C::kTileBytes;
           const int krow = in.k0 + j * kKvRows;
           mbar_arrive_expect_tx(bar(C::kKFull + s), C::kTileBytes);
@@ -223,16 +255,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
           last_g[s] = g;
         }
       }
-      if (*abort_flag) {
-        // Drain: wait (briefly, bounded) for copies this thread issued.
-        for (int s = 0; s < C::kStages; ++s)
-          if (inflight & (1u << s)) {
-            const uint32_t ph = (last_g[s] / C::kStages) & 1u;
-            mbar_wait(bar(C::kKFull + s), ph, nullptr, 50000000ull);
-            mbar_wait(bar(C::kVFull + s), ph, nullptr, 50000000ull);
-          }
-        if (q_inflight) mbar_wait(bar(C::kQFull), (qi - 1) & 1u, nullptr, 50000000ull);
-      }
+    }
+    if (lane == 0 && *abort_flag) {
+      // Drain: wait (briefly, bounded) for copies this thread issued.
+      for (int s = 0; s < C::kStages; ++s)
+        if (inflight & (1u << s)) {
+          const uint32_t ph = (last_g[s] / C::kStages) & 1u;
+          mbar_wait(bar(C::kKFull + s), ph, nullptr, 50000000ull);
+          mbar_wait(bar(C::kVFull + s), ph, nullptr, 50000000ull);
+        }
+      if (q_inflight) mbar_wait(bar(C::kQFull), (qi - 1) & 1u, nullptr, 50000000ull);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -335,8 +367,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
     const uint32_t t_o = t_s + 128;
     const float c_s = kSoftmax ? p.scale * kLog2e : p.scale;   // score multiplier
     const float c_b = kSoftmax ? kLog2e : 1.0f;                 // bias multiplier
-    const int rel_w = 2 * p.max_rel - 1;
-    uint32_t it = 0, tcount = 0, ocount = 0;
+    const float* bias_win = reinterpret_cast<const float*>(gbase + C::kBias);
+    uint32_t it = 0, tcount = 0, ocount = 0, g = 0;
     while (true) {
       const uint32_t slot = it & 1u;
       bool ok = mbar_wait(bar(C::kItemFull + slot), (it >> 1) & 1u, abort_flag);
@@ -348,15 +380,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       if (item.x < 0) break;
       const ItemInfo in = decode_item(item, p);
       const int nh = half ? in.n1 : in.n0;
+      const uint32_t g_item = g;  // key-tile counter at this item's first tile
+      g += max(in.n0, in.n1);
       const int r = in.blk * kItemRows + half * kHalfRows + row_in_half;  // local row
       if (half == 1 && in.n1 == 0 && in.blk * kItemRows + kHalfRows >= in.Lq) continue;
       const bool row_valid = r < in.Lq;
-      const float* brow = p.bias_table ? p.bias_table + static_cast<long long>(in.head) * rel_w : nullptr;
+      const bool has_bias = p.bias_table != nullptr;
       float m = -INFINITY;  // running max (log2 units), possibly stale
       float l = 0.0f;       // running sum relative to m
       bool abort_now = false;
       for (int j = 0; j < nh; ++j) {
+        const uint32_t gj = g_item + j;
         bool okw = mbar_wait(bar(C::kSFull + half), tcount & 1u, abort_flag);
+        // the key-tile stage also carries this tile's bias window
+        if (has_bias)
+          okw = okw && mbar_wait(bar(C::kKFull + gj % C::kStages), (gj / C::kStages) & 1u, abort_flag);
         okw = __all_sync(0xffffffffu, okw);
         if (!okw) { if (lane == 0) fail(); abort_now = true; break; }
         ++tcount;
@@ -364,33 +402,46 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         const int c0 = j * kKvRows;
         const bool need_mask = (c0 + kKvRows > in.Lkv) || (p.causal && c0 + kKvRows - 1 > r);
         const int col_lim = p.causal ? min(in.Lkv, r + 1) : in.Lkv;  // valid cols: c < col_lim
-        auto load_x = [&](int chunk, float (&x)[32]) {
+        const bool plain = !need_mask && !has_bias;  // scores need only the scale
+        // bwin[-cc] = bias(row, tile column cc) for this thread's row
+        const float* bwin = bias_win + ((gj % C::kStages) * 2 + half) * 256 + row_in_half + 127;
+        // x = score * c_s + bias * c_b - sub, with masked entries set to `fill`
+        auto load_x = [&](int chunk, float sub, float fill, float (&x)[32]) {
           uint32_t sr[32];
           tmem_ld32(t_s + chunk * 32, sr);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(sr[i]) * c_s;
-          if (brow != nullptr) {
-            const int base_idx = r - (c0 + chunk * 32) + p.max_rel - 1;
+          for (int i = 0; i < 32; ++i) x[i] = fmaf(__uint_as_float(sr[i]), c_s, -sub);
+          if (has_bias) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int idx = min(max(base_idx - i, 0), rel_w - 1);
-              x[i] = fmaf(__ldg(brow + idx), c_b, x[i]);
-            }
+            for (int i = 0; i < 32; ++i) x[i] = fmaf(bwin[-(chunk * 32 + i)], c_b, x[i]);
           }
           if (need_mask) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (c0 + chunk * 32 + i >= col_lim) x[i] = kSoftmax ? -INFINITY : 0.0f;
+              if (c0 + chunk * 32 + i >= col_lim) x[i] = fill;
           }
         };
         if (kSoftmax) {
           float mt = -INFINITY;
+          if (plain) {
+            // max(score * c_s) = c_s * max(score) for c_s > 0: no per-element scaling
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-          for (int chunk = 0; chunk < 4; ++chunk) {
-            float x[32];
-            load_x(chunk, x);
+            for (int chunk = 0; chunk < 4; ++chunk) {
+              uint32_t sr[32];
+              tmem_ld32(t_s + chunk * 32, sr);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) mt = fmaxf(mt, x[i]);
+              for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sr[i]));
+            }
+            mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c_s;
+          } else {
+#pragma unroll 1
+            for (int chunk = 0; chunk < 4; ++chunk) {
+              float x[32];
+              load_x(chunk, 0.0f, -INFINITY, x);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) mt = fmaxf(mt, x[i]);
+            }
           }
           const float m_new = fmaxf(m, mt);
           bool rescale = false;
@@ -414,25 +465,28 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
             }
           }
           const float m_ref = (m == -INFINITY) ? 0.0f : m;
+          float l2[2] = {0.0f, 0.0f};
 #pragma unroll 1
           for (int chunk = 0; chunk < 4; ++chunk) {
             float x[32];
-            load_x(chunk, x);
+            load_x(chunk, m_ref, -INFINITY, x);
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float p0 = ex2_approx(x[2 * i] - m_ref);
-              const float p1 = ex2_approx(x[2 * i + 1] - m_ref);
-              l += p0 + p1;
+              const float p0 = ex2_approx(x[2 * i]);
+              const float p1 = ex2_approx(x[2 * i + 1]);
+              l2[0] += p0;
+              l2[1] += p1;
               pk[i] = pack_bf16x2(p0, p1);
             }
             tmem_st16(t_s + chunk * 32, pk);
           }
+          l += l2[0] + l2[1];
         } else {
 #pragma unroll 1
           for (int chunk = 0; chunk < 4; ++chunk) {
             float x[32];
-            load_x(chunk, x);
+            load_x(chunk, 0.0f, 0.0f, x);
             uint32_t hi[16], lo[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {

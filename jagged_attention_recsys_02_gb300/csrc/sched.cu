@@ -4,10 +4,13 @@
 // Jagged inputs break the uniform tiling of dense attention: short samples
 // finish early and leave SMs idle ("GEM Training ..." JFA paragraph, and the
 // GDPA paragraph on large batches breaking occupancy assumptions).  The fix
-// here: enumerate every block of every sample, estimate its cost as the
-// number of inner tiles it will visit, counting-sort the blocks by cost in
-// descending order (longest-processing-time first) and let the persistent
-// CTAs pull items in that order from an atomic ticket.
+// here: estimate every block's cost as the number of inner tiles it will
+// visit, counting-sort the samples by their total cost in descending order
+// (longest-processing-time first) and let the persistent CTAs pull items in
+// that order from an atomic ticket.  A sample's items stay contiguous
+// (blocks in descending cost, heads innermost), so the CTAs working at the
+// same time share that sample's key/value (forward) or query/dO (backward)
+// tiles through L2 instead of refetching them from DRAM.
 //
 // One CTA of 1024 threads builds the list; it also validates the offsets and
 // reports malformed ones through the device status word instead of trapping.
@@ -30,6 +33,16 @@ __device__ __forceinline__ int block_cost(int mode, int causal, int Lo, int Li, 
   const int first_q = causal ? blk * kBwdKvRows : 0;
   const int nq = (Li - first_q + kBwdQRows - 1) / kBwdQRows;
   return max(nq, 0) + 1;
+}
+
+// Histogram bucket of a sample's total cost: exact below 1024 inner tiles,
+// then 64-tile steps (coarser ordering among very long samples is enough for
+// the longest-first schedule).
+__device__ __forceinline__ int sample_bucket(int mode, int causal, int Lo, int Li, int nblk) {
+  long long total = 0;
+  for (int blk = 0; blk < nblk; ++blk) total += block_cost(mode, causal, Lo, Li, blk);
+  const long long b = total < 1024 ? total : 1024 + (total - 1024) / 64;
+  return static_cast<int>(b < kCostBuckets - 1 ? b : kCostBuckets - 1);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -57,8 +70,7 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
       continue;
     }
     const int nblk = (Lo + block_rows - 1) / block_rows;
-    for (int blk = 0; blk < nblk; ++blk)
-      atomicAdd(&hist[min(block_cost(mode, causal, Lo, Li, blk), kCostBuckets - 1)], 1);
+    if (nblk > 0) atomicAdd(&hist[sample_bucket(mode, causal, Lo, Li, nblk)], nblk);
   }
   __syncthreads();
   if (bad) {
@@ -101,11 +113,14 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
     const int Lo = outer_off[b + 1] - outer_off[b];
     const int Li = inner_off[b + 1] - inner_off[b];
     const int nblk = (Lo + block_rows - 1) / block_rows;
-    for (int blk = 0; blk < nblk; ++blk) {
-      const int c = min(block_cost(mode, causal, Lo, Li, blk), kCostBuckets - 1);
-      const int pos = atomicAdd(&base[c], 1);
+    if (nblk == 0) continue;
+    const int pos = atomicAdd(&base[sample_bucket(mode, causal, Lo, Li, nblk)], nblk);
+    // Blocks in descending cost: under the causal mask the forward's last
+    // query blocks and the backward's first key blocks visit the most tiles.
+    for (int r = 0; r < nblk; ++r) {
+      const int blk = (causal && mode == 0) ? nblk - 1 - r : r;
       for (int h = 0; h < H; ++h)
-        items[static_cast<long long>(pos) * H + h] = make_int2(b, (blk << 8) | h);
+        items[static_cast<long long>(pos + r) * H + h] = make_int2(b, (blk << 8) | h);
     }
   }
   if (tid == 0) {

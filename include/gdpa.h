@@ -112,6 +112,25 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
                      void* workspace, size_t ws_bytes, void* stream);
 
+/* MXFP8 block quantisation (OCP Microscaling Formats v1.0; "GEM Training ..."
+ * low-precision paragraph: attention with MXFP8 block-scaled MMA).  Elements
+ * become E4M3 codes (round to nearest even, saturated at +-448); each block of
+ * 32 elements shares an E8M0 scale 2^(floor(log2 amax) - 8), biased by 127.
+ *   GDPA_MX_ALONG_CHANNELS: blocks of 32 consecutive channels of one (token,
+ *     head) row (for Q and K, whose product contracts over d).
+ *     codes [T][H][d] u8, scales [T][H][d/32] u8.
+ *   GDPA_MX_ALONG_TOKENS: blocks of 32 consecutive tokens of one sample, per
+ *     (head, channel); the first block starts at the sample's first token and
+ *     the last may be partial (for V, whose product contracts over keys).
+ *     codes [T][H][d] u8; scales [B + T/32 + 1][H][d] u8 where block r of
+ *     sample b is scale row b + floor(offsets[b]/32) + r (rows that belong to
+ *     no block are not written).  offsets are needed only in this mode.
+ * x is [T][H][d] bf16, 16-byte aligned; all buffers are device memory. */
+enum { GDPA_MX_ALONG_CHANNELS = 0, GDPA_MX_ALONG_TOKENS = 1 };
+size_t gdpa_mxfp8_scale_bytes(int B, int H, int d, int64_t T, int mode);
+gdpa_status gdpa_quantize_mxfp8(const void* x, const int32_t* offsets, int B, int H, int d,
+                                int64_t T, int mode, void* codes, void* scales, void* stream);
+
 /* Reads the device status word set by earlier calls on this device,
  * synchronising `stream` first, then clears it.  Returns GDPA_OK,
  * GDPA_ERR_TIMEOUT, GDPA_ERR_BAD_OFFSETS or GDPA_ERR_CUDA. */

@@ -28,7 +28,9 @@ STATUS_NAMES = {0: "GDPA_OK", 1: "GDPA_ERR_INVALID_ARG", 2: "GDPA_ERR_UNSUPPORTE
 # Every symbol include/gdpa.h declares.
 EXPORTS = ("gdpa_fwd_workspace_size", "gdpa_fwd", "gdpa_bwd_workspace_size", "gdpa_bwd",
            "gdpa_get_device_status", "gdpa_status_string", "gdpa_last_launch_count",
-           "gdpa_timing_enable", "gdpa_timing_collect", "gdpa_fwd_noalloc")
+           "gdpa_timing_enable", "gdpa_timing_collect", "gdpa_fwd_noalloc",
+           "gdpa_mxfp8_scale_bytes", "gdpa_quantize_mxfp8")
+MX_ALONG_CHANNELS, MX_ALONG_TOKENS = 0, 1
 
 
 class GdpaError(RuntimeError):
@@ -85,6 +87,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdpa_timing_collect.argtypes = [ctypes.POINTER(ctypes.c_float),
                                             ctypes.POINTER(ctypes.c_int), I]
         lib.gdpa_timing_collect.restype = I
+        lib.gdpa_mxfp8_scale_bytes.argtypes = [I, I, I, i64, I]
+        lib.gdpa_mxfp8_scale_bytes.restype = sz
+        lib.gdpa_quantize_mxfp8.argtypes = [vp, vp, I, I, I, i64, I, vp, vp, vp]
+        lib.gdpa_quantize_mxfp8.restype = I
         _lib = lib
         return lib
 
@@ -190,3 +196,20 @@ def timing_collect(max_n: int = 4096):
     f = [ms[i] for i in range(n) if kind[i] == 0]
     b = [ms[i] for i in range(n) if kind[i] == 1]
     return f, b
+
+
+def quantize_mxfp8(x, offsets=None, *, mode, codes=None, scales=None, stream=None):
+    """MXFP8 block quantisation through the C ABI.  Returns (codes u8, scales u8)."""
+    lib = load()
+    T, H, d = x.shape
+    B = offsets.numel() - 1 if offsets is not None else 0
+    if codes is None:
+        codes = torch.empty((T, H, d), device=x.device, dtype=torch.uint8)
+    if scales is None:
+        n = lib.gdpa_mxfp8_scale_bytes(max(B, 0), H, d, T, mode)
+        shape = (T, H, d // 32) if mode == MX_ALONG_CHANNELS else (n // (H * d), H, d)
+        scales = torch.empty(shape, device=x.device, dtype=torch.uint8)
+    rc = lib.gdpa_quantize_mxfp8(_ptr(x), _ptr(offsets), B, H, d, T, int(mode), _ptr(codes),
+                                 _ptr(scales), _stream(stream))
+    _check(rc, "gdpa_quantize_mxfp8")
+    return codes, scales

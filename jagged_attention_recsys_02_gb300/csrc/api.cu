@@ -93,6 +93,22 @@ bool make_thd_map(CUtensorMap* m, const void* base, int64_t T, int H, int d, int
   return r == CUDA_SUCCESS;
 }
 
+// 3-D TMA map over the fp32 dQ accumulator [T][H][d]: box = 64 channels x
+// 1 head x 64 rows, no swizzle (the target of the backward's tile reduce-add).
+bool make_dq_map(CUtensorMap* m, void* base, int64_t T, int H, int d) {
+  if (T <= 0) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                           static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(d) * 4};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBwdQRows)};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -265,6 +281,10 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
   float* dq_acc = reinterpret_cast<float*>(ws + off);
   off += align_up(static_cast<size_t>(Tq) * H * d * sizeof(float), 256);
   float* delta = reinterpret_cast<float*>(ws + off);
+  // Without query rows there is nothing to reduce into; any valid map will do.
+  CUtensorMap tdq;
+  if (!make_dq_map(&tdq, Tq > 0 ? static_cast<void*>(dq_acc) : ws, Tq > 0 ? Tq : 1, H, d))
+    return GDPA_ERR_INVALID_ARG;
 
   if (launch_build_worklist(kv_offsets, q_offsets, B, H, Tkv, Tq, causal, 1, items, n_items,
                             ticket, dev->status, s) != cudaSuccess)
@@ -299,7 +319,7 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
   int launches = 0;
   cudaEvent_t ea = nullptr, eb = nullptr;
   const bool timed = timing_slot(1, &ea, &eb);
-  cudaError_t e = launch_bwd(p, act, tq, tk, tv, tdo, grid, s, &launches,
+  cudaError_t e = launch_bwd(p, act, tq, tk, tv, tdo, tdq, grid, s, &launches,
                              timed ? ea : nullptr, timed ? eb : nullptr);
   t_launches += launches;
   if (e != cudaSuccess) return GDPA_ERR_CUDA;
@@ -308,6 +328,32 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
       return GDPA_ERR_CUDA;
     ++t_launches;
   }
+  return GDPA_OK;
+}
+
+size_t gdpa_mxfp8_scale_bytes(int B, int H, int d, int64_t T, int mode) {
+  if (B < 0 || H <= 0 || T < 0 || (d != 64 && d != 128)) return 0;
+  if (mode == GDPA_MX_ALONG_CHANNELS) return static_cast<size_t>(T) * H * (d / 32);
+  if (mode == GDPA_MX_ALONG_TOKENS) return (static_cast<size_t>(B) + T / 32 + 1) * H * d;
+  return 0;
+}
+
+gdpa_status gdpa_quantize_mxfp8(const void* x, const int32_t* offsets, int B, int H, int d,
+                                int64_t T, int mode, void* codes, void* scales, void* stream) {
+  t_launches = 0;
+  if (B < 0 || H <= 0 || T < 0) return GDPA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return GDPA_ERR_UNSUPPORTED;
+  if (mode != GDPA_MX_ALONG_CHANNELS && mode != GDPA_MX_ALONG_TOKENS) return GDPA_ERR_INVALID_ARG;
+  if (T == 0) return GDPA_OK;
+  if (x == nullptr || codes == nullptr || scales == nullptr || !aligned16(x) || !aligned16(codes))
+    return GDPA_ERR_INVALID_ARG;
+  if (mode == GDPA_MX_ALONG_TOKENS && offsets == nullptr) return GDPA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = (mode == GDPA_MX_ALONG_CHANNELS)
+                      ? launch_quant_rows(x, T * H, d, codes, scales, s)
+                      : launch_quant_tokens(x, offsets, B, H, d, codes, scales, s);
+  if (e != cudaSuccess) return GDPA_ERR_CUDA;
+  ++t_launches;
   return GDPA_OK;
 }
 

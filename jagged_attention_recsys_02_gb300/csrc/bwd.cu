@@ -12,7 +12,7 @@
 // computed transposed so that TMEM lanes are key rows:
 //   S^T = K Q^T, dP^T = V dO^T           (M = 128 keys, N = 64 queries)
 //   dV += P^T dO, dK += dS^T Q           (accumulated in TMEM over the tiles)
-//   dQ^T = K^T dS^T                      (M = d, N = 64) -> fp32 atomics
+//   dQ^T = K^T dS^T                      (M = d, N = 64) -> TMA reduce-add into fp32 dQ
 // P^T goes back into the S^T columns of TMEM (A operand of dV); dS^T is
 // written to a swizzled shared-memory tile that is both the K-major A
 // operand of dK and the MN-major B operand of dQ^T.
@@ -21,7 +21,8 @@
 // work list):
 //   warps 0-3  activation group A: P^T, dS^T for query columns [0,32) of a tile
 //   warps 4-7  activation group B: the same for query columns [32,64)
-//   warps 8-11 dQ group: dQ^T tile -> fp32 atomics; dK/dV epilogue
+//   warps 8-11 dQ group: dQ^T tile -> shared memory -> bulk tensor reduce-add
+//              into the fp32 dQ accumulator; dK/dV epilogue
 //   warp  12   producer: TMA loads of K/V, Q/dO tiles; lse, D and bias values
 //   warp  13   MMA issuer
 // TMEM columns: S^T/P^T buffers [0,64) [64,128), dP^T [128,192),
@@ -56,7 +57,12 @@ struct BwdCfg {
   // per stage: float lse2[64], D[64], bias window[192]
   static constexpr int kStatFloats = 2 * kBwdQRows + kBwdQRows + kBwdKvRows;
   static constexpr int kStats = kDs + 2 * kDsParts * kDsBytes;
-  static constexpr int kBar = kStats + kStages * kStatFloats * 4;
+  // dQ staging: [64 query rows][64 channels] fp32 per buffer (two buffers when
+  // shared memory allows, one for the split-P/dS variants)
+  static constexpr int kDqStageBytes = kBwdQRows * 64 * 4;
+  static constexpr int kDqBufs = SPLIT ? 1 : 2;
+  static constexpr int kDqStage = kStats + kStages * kStatFloats * 4;
+  static constexpr int kBar = kDqStage + kDqBufs * kDqStageBytes;
   static constexpr int kKvFull = 0, kKvEmpty = 1;
   static constexpr int kQdFull = 2;                 // + s
   static constexpr int kQdEmpty = kQdFull + kStages;
@@ -73,7 +79,8 @@ struct BwdCfg {
   static constexpr int kItemSlots = kBar + 8 * kNumBars;
   static constexpr int kTmemSlot = kItemSlots + 16;
   static constexpr int kAbort = kTmemSlot + 4;
-  static constexpr int kUsed = kAbort + 4;
+  static constexpr int kGroupOk = kAbort + 4;   // int[4]: dQ-group vote on a wait's result
+  static constexpr int kUsed = kGroupOk + 16;
   static constexpr int kSmemBytes = kUsed + 1024;
 };
 
@@ -129,7 +136,7 @@ template <int D, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
            const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
-           const BwdParams p) {
+           const __grid_constant__ CUtensorMap tmap_dq, const BwdParams p) {
   constexpr bool kSoftmax = (ACT == GDPA_ACT_SOFTMAX);
   constexpr bool kSplit = !kSoftmax;
   using C = BwdCfg<D, kSplit>;
@@ -178,6 +185,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
     prefetch_tmap(&tmap_do);
+    prefetch_tmap(&tmap_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -517,7 +525,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // TMEM lane: channel (dQ^T) or key row (dK, dV)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    uint32_t it = 0, dqc = 0, dkvc = 0;
+    uint32_t it = 0, dqc = 0, dkvc = 0, dq_issue = 0;
+    volatile int* group_ok = reinterpret_cast<volatile int*>(gbase + C::kGroupOk);
     while (true) {
       const uint32_t slot = it & 1u;
       bool w = mbar_wait(bar(C::kItemFull + slot), (it >> 1) & 1u, abort_flag);
@@ -530,7 +539,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       bool abort_now = false;
       for (int t = 0; t < in.nq; ++t) {
         w = mbar_wait(bar(C::kDqFull), dqc & 1u, abort_flag);
-        if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); abort_now = true; break; }
+        // The group syncs on named barriers below, so its four warps must agree
+        // on whether the wait succeeded before any of them can leave.
+        w = __all_sync(0xffffffffu, w);
+        if (lane == 0) group_ok[wq] = w ? 1 : 0;
+        named_bar_sync(1, 128);
+        const bool all_ok = group_ok[0] && group_ok[1] && group_ok[2] && group_ok[3];
+        if (!all_ok) { if (lane == 0) fail(); abort_now = true; break; }
         ++dqc;
         tc_fence_after();
         uint32_t v0[32], v1[32];
@@ -538,17 +553,32 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         tmem_ld32(tmem + lane_off + kColDQ + 32, v1);
         tc_fence_before();
         mbar_arrive(bar(C::kDqEmpty));
-        if (r < D) {
-          const int qloc = (in.qt0 + t) * kBwdQRows;
-          const int nvalid = min(kBwdQRows, in.Lq - qloc);
-          float* base = p.dq_acc + (static_cast<long long>(in.q0 + qloc) * p.H + in.head) * D + r;
-          const long long rs = static_cast<long long>(p.H) * D;
+        // Stage the tile as [query][channel] and add it into the fp32 dQ rows with
+        // one bulk tensor reduce per 64 channels.  Columns of queries outside the
+        // sample carry exact zeros (their dS is masked to 0), so a box that runs
+        // into the next sample's rows adds nothing; rows past Tq are skipped.
+        const int qrow = in.q0 + (in.qt0 + t) * kBwdQRows;
+#pragma unroll 1
+        for (int hcol = 0; hcol < D / 64; ++hcol) {
+          const int buf = dq_issue % C::kDqBufs;
+          if (r == 0) bulk_wait_group_read<C::kDqBufs - 1>();  // buffer `buf` is free again
+          named_bar_sync(1, 128);
+          if ((r >> 6) == hcol) {
+            float* stg = reinterpret_cast<float*>(gbase + C::kDqStage + buf * C::kDqStageBytes);
+            const int ch = r & 63;
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c < nvalid) atomicAdd(base + c * rs, __uint_as_float(v0[c]));
+            for (int c = 0; c < 32; ++c) stg[c * 64 + ch] = __uint_as_float(v0[c]);
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c + 32 < nvalid) atomicAdd(base + (c + 32) * rs, __uint_as_float(v1[c]));
+            for (int c = 0; c < 32; ++c) stg[(c + 32) * 64 + ch] = __uint_as_float(v1[c]);
+            fence_proxy_async_smem();
+          }
+          named_bar_sync(1, 128);
+          if (r == 0) {
+            tma_reduce_add_3d(&tmap_dq, sbase + C::kDqStage + buf * C::kDqStageBytes, hcol * 64,
+                              in.head, qrow);
+            bulk_commit_group();
+          }
+          ++dq_issue;
         }
       }
       if (abort_now) break;
@@ -592,6 +622,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         }
       }
     }
+    if (r == 0) bulk_wait_group_all();  // every dQ reduce issued by this thread has landed
   }
 
   tc_fence_before();
@@ -646,30 +677,34 @@ dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, long l
 
 template <int D, int ACT>
 cudaError_t launch_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                        const CUtensorMap& tv, const CUtensorMap& tdo, int grid, cudaStream_t s) {
+                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                        int grid, cudaStream_t s) {
   using C = BwdCfg<D, ACT != GDPA_ACT_SOFTMAX>;
   cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, ACT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  bwd_kernel<D, ACT><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, p);
+  bwd_kernel<D, ACT><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_main_d(const BwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& tdo, int grid, cudaStream_t s) {
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                          int grid, cudaStream_t s) {
   switch (act) {
-    case GDPA_ACT_SOFTMAX: return launch_main<D, GDPA_ACT_SOFTMAX>(p, tq, tk, tv, tdo, grid, s);
-    case GDPA_ACT_SILU: return launch_main<D, GDPA_ACT_SILU>(p, tq, tk, tv, tdo, grid, s);
-    case GDPA_ACT_GELU_TANH: return launch_main<D, GDPA_ACT_GELU_TANH>(p, tq, tk, tv, tdo, grid, s);
-    default: return launch_main<D, GDPA_ACT_IDENTITY>(p, tq, tk, tv, tdo, grid, s);
+    case GDPA_ACT_SOFTMAX: return launch_main<D, GDPA_ACT_SOFTMAX>(p, tq, tk, tv, tdo, tdq, grid, s);
+    case GDPA_ACT_SILU: return launch_main<D, GDPA_ACT_SILU>(p, tq, tk, tv, tdo, tdq, grid, s);
+    case GDPA_ACT_GELU_TANH:
+      return launch_main<D, GDPA_ACT_GELU_TANH>(p, tq, tk, tv, tdo, tdq, grid, s);
+    default: return launch_main<D, GDPA_ACT_IDENTITY>(p, tq, tk, tv, tdo, tdq, grid, s);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, int grid,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                       int grid,
                        cudaStream_t stream, int* launches, cudaEvent_t ev_begin,
                        cudaEvent_t ev_end) {
   // 1) zero dQ accumulator, D = rowsum(dO * O)
@@ -686,8 +721,8 @@ cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const
   ++*launches;
   // 2) main kernel (optionally bracketed by timing events)
   if (ev_begin != nullptr && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess) return e;
-  e = (p.d == 64) ? launch_main_d<64>(p, act, tq, tk, tv, tdo, grid, stream)
-                  : launch_main_d<128>(p, act, tq, tk, tv, tdo, grid, stream);
+  e = (p.d == 64) ? launch_main_d<64>(p, act, tq, tk, tv, tdo, tdq, grid, stream)
+                  : launch_main_d<128>(p, act, tq, tk, tv, tdo, tdq, grid, stream);
   if (e != cudaSuccess) return e;
   if (ev_end != nullptr && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess) return e;
   ++*launches;

@@ -80,11 +80,17 @@ cudaError_t launch_fwd(const FwdParams& p, int act, const CUtensorMap& tq, const
                        const CUtensorMap& tv, int grid, cudaStream_t stream);
 int fwd_smem_bytes(int d);
 cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, int grid,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                       int grid,
                        cudaStream_t stream, int* launches, cudaEvent_t ev_begin,
                        cudaEvent_t ev_end);
 cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale,
                               cudaStream_t stream);
+
+cudaError_t launch_quant_rows(const void* x, long long rows, int d, void* codes, void* scales,
+                              cudaStream_t s);
+cudaError_t launch_quant_tokens(const void* x, const int32_t* offsets, int B, int H, int d,
+                                void* codes, void* scales, cudaStream_t s);
 
 // Upper bound on the number of work items (host-side sizing).
 inline int64_t max_fwd_items(int B, int H, int64_t Tq) {

@@ -237,6 +237,39 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         }
         kv_inflight = true;
       }
+      // Per-lane values of one query tile: lse*log2e and D for columns lane and
+      // lane+32, and bias-window entries lane + 32k.  They are fetched one tile
+      // ahead, so the global-load latency overlaps the wait for a free stage.
+      const int rel_w = 2 * p.max_rel - 1;
+      const float* brow =
+          p.bias_table ? p.bias_table + static_cast<long long>(in.head) * rel_w : nullptr;
+      constexpr int kWin = kBwdQRows + kBwdKvRows - 1;  // 191 relative positions
+      auto fetch = [&](int t, float (&v)[10]) {
+        const int qloc = (in.qt0 + t) * kBwdQRows;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int ql = qloc + lane + 32 * k;
+          float l2 = 0.0f, dd = 0.0f;
+          if (kSoftmax && ql < in.Lq) {
+            const long long gi = static_cast<long long>(in.head) * p.Tq + in.q0 + ql;
+            l2 = __ldg(p.lse + gi) * kLog2e;
+            dd = __ldg(p.delta + gi);
+          }
+          v[2 * k] = l2;
+          v[2 * k + 1] = dd;
+        }
+        // bias(i - j) for query column c and key row jj of the tile is window
+        // entry c - jj + 127
+        const int w0 = qloc - in.kb * kBwdKvRows - (kBwdKvRows - 1) + p.max_rel - 1;
+#pragma unroll
+        for (int k = 0; k < 6; ++k) {
+          const int e = lane + 32 * k;
+          v[4 + k] = (brow != nullptr && e < kWin) ? __ldg(brow + min(max(w0 + e, 0), rel_w - 1))
+                                                   : 0.0f;
+        }
+      };
+      float cur[10];
+      fetch(0, cur);
       for (int t = 0; t < in.nq; ++t, ++g) {
         const uint32_t s = g % C::kStages;
         const uint32_t ph = (g / C::kStages) & 1u;
@@ -244,27 +277,22 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         if (!__all_sync(0xffffffffu, w)) { ok = false; if (lane == 0) fail(); break; }
         const int qloc = (in.qt0 + t) * kBwdQRows;  // first local query row of the tile
         float* st = stats + s * C::kStatFloats;
-        for (int c = lane; c < kBwdQRows; c += 32) {
-          const int ql = qloc + c;
-          float l2 = 0.0f, dd = 0.0f;
-          if (ql < in.Lq) {
-            const long long gi = static_cast<long long>(in.head) * p.Tq + in.q0 + ql;
-            if (kSoftmax) {
-              l2 = p.lse[gi] * kLog2e;
-              dd = p.delta[gi];
-            }
-          }
-          st[c] = l2;
-          st[kBwdQRows + c] = dd;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          st[lane + 32 * k] = cur[2 * k];
+          st[kBwdQRows + lane + 32 * k] = cur[2 * k + 1];
         }
-        if (p.bias_table != nullptr) {
-          // bias(i - j) for query column c and key row jj of the tile is window
-          // entry c - jj + 127 (the tile spans 64 + 127 relative positions)
-          const int rel_w = 2 * p.max_rel - 1;
-          const float* brow = p.bias_table + static_cast<long long>(in.head) * rel_w;
-          const int w0 = qloc - in.kb * kBwdKvRows - (kBwdKvRows - 1) + p.max_rel - 1;
-          for (int e = lane; e < kBwdQRows + kBwdKvRows - 1; e += 32)
-            st[2 * kBwdQRows + e] = __ldg(brow + min(max(w0 + e, 0), rel_w - 1));
+        if (brow != nullptr) {
+#pragma unroll
+          for (int k = 0; k < 6; ++k)
+            if (lane + 32 * k < kWin) st[2 * kBwdQRows + lane + 32 * k] = cur[4 + k];
+        }
+        float nxt[10];
+        if (t + 1 < in.nq) {
+          fetch(t + 1, nxt);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 10; ++k) nxt[k] = 0.0f;
         }
         __syncwarp();
         if (lane == 0) {
@@ -279,6 +307,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
           inflight |= 1u << s;
           last_g[s] = g;
         }
+#pragma unroll
+        for (int k = 0; k < 10; ++k) cur[k] = nxt[k];
       }
     }
     if (lane == 0 && *abort_flag) {

@@ -223,21 +223,42 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       ++qi;
       const float* brow =
           p.bias_table ? p.bias_table + static_cast<long long>(in.head) * rel_w : nullptr;
+      // Window entry e of half h for key tile j holds bias(i - j') with
+      // (i - r_h) - (j' - c0) = e - 127 (r_h: the half's first local row, c0: the
+      // tile's first local column).  Each lane holds entries lane + 32k of both
+      // halves, fetched one tile ahead so the load latency overlaps the wait for
+      // a free stage.
+      auto fetch = [&](int j, float (&v)[16]) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int w0 = in.blk * kItemRows + h * kHalfRows - j * kKvRows - (kKvRows - 1) +
+                         p.max_rel - 1;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int e = lane + 32 * k;
+            v[8 * h + k] = (brow != nullptr && e < 255)
+                               ? __ldg(brow + min(max(w0 + e, 0), rel_w - 1))
+                               : 0.0f;
+          }
+        }
+      };
+      float cur[16];
+      if (brow != nullptr) fetch(0, cur);
       for (int j = 0; j < n; ++j, ++g) {
         const uint32_t s = g % C::kStages;
         const uint32_t ph = (g / C::kStages) & 1u;
         w = mbar_wait(bar(C::kKvEmpty + s), ph ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, w)) { ok = false; if (lane == 0) fail(); break; }
+        float nxt[16];
         if (brow != nullptr) {
-          // Window entry e of half h holds bias(i - j) for (i - r_h) - (j - c0) = e - 127,
-          // where r_h is the half's first local row and c0 the tile's first local column.
+#pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int w0 = in.blk * kItemRows + h * kHalfRows - j * kKvRows - (kKvRows - 1) +
-                           p.max_rel - 1;
             float* win = bias_win + (s * 2 + h) * 256;
-            for (int e = lane; e < 255; e += 32)
-              win[e] = __ldg(brow + min(max(w0 + e, 0), rel_w - 1));
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              if (lane + 32 * k < 255) win[lane + 32 * k] = cur[8 * h + k];
           }
+          if (j + 1 < n) fetch(j + 1, nxt);
         }
         __syncwarp();
         if (lane == 0) {
@@ -253,6 +274,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
                         bar(C::kVFull + s), x, in.head, krow);
           inflight |= 1u << s;
           last_g[s] = g;
+        }
+        if (brow != nullptr && j + 1 < n) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) cur[k] = nxt[k];
         }
       }
     }

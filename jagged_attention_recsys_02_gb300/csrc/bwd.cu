@@ -49,7 +49,9 @@ struct BwdCfg {
   static constexpr int kQTileBytes = kBwdQRows * D * 2;       // Q or dO tile
   static constexpr int kDsBytes = kBwdKvRows * kBwdQRows * 2;  // one dS^T tile (16 KB)
   static constexpr int kDsParts = SPLIT ? 2 : 1;
-  static constexpr int kStages = 2;
+  // Q/dO stages: three where shared memory allows (hides the TMA round trip
+  // behind two tiles of work), two for the split-P/dS variants.
+  static constexpr int kStages = SPLIT ? 2 : 3;
   static constexpr int kK = 0;
   static constexpr int kV = kKvTileBytes;
   static constexpr int kQ = 2 * kKvTileBytes;                  // + s * 2 * qtile ; dO = Q + qtile
@@ -57,10 +59,9 @@ struct BwdCfg {
   // per stage: float lse2[64], D[64], bias window[192]
   static constexpr int kStatFloats = 2 * kBwdQRows + kBwdQRows + kBwdKvRows;
   static constexpr int kStats = kDs + 2 * kDsParts * kDsBytes;
-  // dQ staging: [64 query rows][64 channels] fp32 per buffer (two buffers when
-  // shared memory allows, one for the split-P/dS variants)
+  // dQ staging: one [64 query rows][64 channels] fp32 buffer
   static constexpr int kDqStageBytes = kBwdQRows * 64 * 4;
-  static constexpr int kDqBufs = SPLIT ? 1 : 2;
+  static constexpr int kDqBufs = 1;
   static constexpr int kDqStage = kStats + kStages * kStatFloats * 4;
   static constexpr int kBar = kDqStage + kDqBufs * kDqStageBytes;
   static constexpr int kKvFull = 0, kKvEmpty = 1;

@@ -61,8 +61,9 @@ struct FwdCfg {
   static constexpr int kQFull = 0, kQEmpty = 1;
   static constexpr int kKFull = 2;                                     // + s
   static constexpr int kVFull = kKFull + kStages;
-  static constexpr int kKvEmpty = kVFull + kStages;
-  static constexpr int kSFull = kKvEmpty + kStages;                    // + half
+  static constexpr int kKEmpty = kVFull + kStages;                     // K tile consumed
+  static constexpr int kVEmpty = kKEmpty + kStages;                    // V tile (+ bias window) consumed
+  static constexpr int kSFull = kVEmpty + kStages;                     // + half
   static constexpr int kPFull = kSFull + 2;
   static constexpr int kODone = kPFull + 2;
   static constexpr int kItemFull = kODone + 2;                         // + slot
@@ -146,7 +147,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar(C::kKFull + s), 1);
       mbar_init(bar(C::kVFull + s), 1);
-      mbar_init(bar(C::kKvEmpty + s), 1);
+      mbar_init(bar(C::kKEmpty + s), 1);
+      mbar_init(bar(C::kVEmpty + s), 1);
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(bar(C::kSFull + h), 1);
@@ -247,7 +249,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       for (int j = 0; j < n; ++j, ++g) {
         const uint32_t s = g % C::kStages;
         const uint32_t ph = (g / C::kStages) & 1u;
-        w = mbar_wait(bar(C::kKvEmpty + s), ph ^ 1u, abort_flag);
+        const uint32_t kdst = sbase + C::kKV + s * 2 * C::kTileBytes;
+        const int krow = in.k0 + j * kKvRows;
+        w = mbar_wait(bar(C::kKEmpty + s), ph ^ 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; if (lane == 0) fail(); break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(C::kKFull + s), C::kTileBytes);
+          for (int x = 0; x < D; x += 64)
+            tma_load_3d(kdst + (x / 64) * (kKvRows * 128), &tmap_k, bar(C::kKFull + s), x,
+                        in.head, krow);
+          inflight |= 1u << s;
+          last_g[s] = g;
+        }
+        // The V slot (and this tile's bias windows) frees up after the tile's
+        // value products, later than the K slot.
+        w = mbar_wait(bar(C::kVEmpty + s), ph ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, w)) { ok = false; if (lane == 0) fail(); break; }
         float nxt[16];
         if (brow != nullptr) {
@@ -262,18 +278,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         }
         __syncwarp();
         if (lane == 0) {
-          const uint32_t kdst = sbase + C::kKV + s * 2 * C::kTileBytes;
-          const int krow = in.k0 + j * kKvRows;
-          mbar_arrive_expect_tx(bar(C::kKFull + s), C::kTileBytes);
-          for (int x = 0; x < D; x += 64)
-            tma_load_3d(kdst + (x / 64) * (kKvRows * 128), &tmap_k, bar(C::kKFull + s), x,
-                        in.head, krow);
           mbar_arrive_expect_tx(bar(C::kVFull + s), C::kTileBytes);
           for (int x = 0; x < D; x += 64)
             tma_load_3d(kdst + C::kTileBytes + (x / 64) * (kKvRows * 128), &tmap_v,
                         bar(C::kVFull + s), x, in.head, krow);
-          inflight |= 1u << s;
-          last_g[s] = g;
         }
         if (brow != nullptr && j + 1 < n) {
 #pragma unroll
@@ -347,6 +355,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
           tc_fence_after();
           if (in.n0 > 0) issue_s(0, s);
           if (in.n1 > 0) issue_s(1, s);
+          mma_commit(bar(C::kKEmpty + s));  // K tile 0 has all its readers
           if (n == 1) mma_commit(bar(C::kQEmpty));
         }
         for (int j = 0; j < n; ++j) {
@@ -364,11 +373,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
             tc_fence_after();
             issue_pv(half, s, j == 0);
             if (j == nh - 1) mma_commit(bar(C::kODone + half));
-            if (half == last_half_j) mma_commit(bar(C::kKvEmpty + s));
+            if (half == last_half_j) mma_commit(bar(C::kVEmpty + s));
             if (j + 1 < nh) {
               if (!mbar_wait(bar(C::kKFull + s_next), ph_next, abort_flag)) { ok = false; fail(); break; }
               tc_fence_after();
               issue_s(half, s_next);
+              // the last score product that reads K tile j+1
+              if (half == ((j + 1 < in.n1) ? 1 : 0)) mma_commit(bar(C::kKEmpty + s_next));
               if (j + 1 == n - 1 && half == last_s_half) mma_commit(bar(C::kQEmpty));
             }
           }
@@ -417,9 +428,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       for (int j = 0; j < nh; ++j) {
         const uint32_t gj = g_item + j;
         bool okw = mbar_wait(bar(C::kSFull + half), tcount & 1u, abort_flag);
-        // the key-tile stage also carries this tile's bias window
+        // the value-tile stage also carries this tile's bias window
         if (has_bias)
-          okw = okw && mbar_wait(bar(C::kKFull + gj % C::kStages), (gj / C::kStages) & 1u, abort_flag);
+          okw = okw && mbar_wait(bar(C::kVFull + gj % C::kStages), (gj / C::kStages) & 1u, abort_flag);
         okw = __all_sync(0xffffffffu, okw);
         if (!okw) { if (lane == 0) fail(); abort_now = true; break; }
         ++tcount;

@@ -60,6 +60,12 @@ def test_fwd_causal_relpos(act, d):
     _case(L, L, 2, d, act, causal=True, max_rel=200)
 
 
+@pytest.mark.parametrize("act", ["softmax", "silu"])
+def test_fwd_causal_no_bias(act):
+    L = [1, 128, 129, 300, 0, 511, 64, 257, 1000]
+    _case(L, L, 2, 128, act, causal=True)
+
+
 @pytest.mark.parametrize("act", ["softmax", "gelu_tanh"])
 def test_fwd_bias_noncausal(act):
     _case([5, 300, 129], [260, 7, 500], 3, 128, act, max_rel=64)

@@ -458,6 +458,99 @@ def run_gpu(args, rank, world, local_rank):
     return 0
 
 
+# ------------------------------------------------------------------ MXFP8 forward
+def run_gpu_mxfp8(args, rank, world, local_rank):
+    """Forward on MXFP8 operands: a step quantises Q, K, V (E4M3 + E8M0 block
+    scales) and runs the block-scaled forward (softmax).  FLOPs are the forward's
+    non-padded 4*H*d*pairs; the peak is the FP8 one (2x the measured bf16 peak,
+    the nominal FP8 : BF16 ratio of the part)."""
+    import torch
+    import torch.distributed as dist
+
+    from jagged_attention_recsys_02_gb300 import binding
+    from jagged_attention_recsys_02_gb300.workloads import make_tensors, make_workload
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=dev)
+    w = make_workload(args.workload if args.workload != "jfa_causal_relpos" else "heavy_tail",
+                      act="softmax")
+    t = make_tensors(w, device=dev, seed=rank, with_dout=False)
+    H, d, Tq, Tkv = w.H, w.d, w.Tq, w.Tkv
+    out = torch.empty_like(t["q"])
+    lse = torch.empty((H, Tq), device=dev, dtype=torch.float32)
+    ws = torch.empty(binding.fwd_workspace_size(w.B, H, d, Tq, Tkv), device=dev, dtype=torch.uint8)
+    qc, qs = binding.quantize_mxfp8(t["q"], mode=binding.MX_ALONG_CHANNELS)
+    kc, ks = binding.quantize_mxfp8(t["k"], mode=binding.MX_ALONG_CHANNELS)
+    vc, vs = binding.quantize_mxfp8(t["v"], t["ko"], mode=binding.MX_ALONG_TOKENS)
+
+    def step():
+        n = 0
+        binding.quantize_mxfp8(t["q"], mode=binding.MX_ALONG_CHANNELS, codes=qc, scales=qs)
+        n += binding.last_launch_count()
+        binding.quantize_mxfp8(t["k"], mode=binding.MX_ALONG_CHANNELS, codes=kc, scales=ks)
+        n += binding.last_launch_count()
+        binding.quantize_mxfp8(t["v"], t["ko"], mode=binding.MX_ALONG_TOKENS, codes=vc, scales=vs)
+        n += binding.last_launch_count()
+        binding.gdpa_fwd_mxfp8(qc, qs, t["qo"], kc, ks, vc, vs, t["ko"], causal=w.causal,
+                               scale=w.scale, bias=t["bias"], max_rel=w.max_rel, out=out, lse=lse,
+                               workspace=ws)
+        return n + binding.last_launch_count()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if binding.device_status() != 0:
+        raise RuntimeError("device status after warm-up")
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    binding.timing_enable(True)
+    launches = 0
+    e0.record()
+    for _ in range(args.steps):
+        launches += step()
+    e1.record()
+    torch.cuda.synchronize()
+    binding.timing_enable(False)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    fwd_ms, _ = binding.timing_collect()
+    flops = w.fwd_flops()
+    ms, tot = reduce_over_ranks(e0.elapsed_time(e1), flops * args.steps, dev)
+    value = tot / (ms * 1e-3) / 1e12
+    peaks, src = load_peaks()
+    fp8_peak = 2.0 * float(peaks["bf16_tflops"])
+    k_ms = float(np.mean(fwd_ms))
+    achieved = flops / (k_ms * 1e-3) / 1e12
+    line = {
+        "metric": "jagged attn MXFP8 fwd TFLOPS (non-padded FLOPs) & % of GB300 FP8 tensor peak",
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 (E8M0 block scales), fp32 accumulate",
+        "data": "synthetic (seeded N(0,1) bf16 inputs, quantised every step)",
+        "config": dict(workload_config(w, "inputs larger than L2 (no flush)"),
+                       step="MXFP8 quantise Q,K,V + forward"),
+        "roofline": {"bound": "tensor", "kernel": "MXFP8 forward kernel", "achieved": achieved,
+                     "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
+                     "traffic": None,
+                     "peak_source": f"2 x bf16_tflops of {src} (nominal FP8:BF16 = 2)"},
+        "gpu_launches": launches, "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -469,6 +562,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--mxfp8", action="store_true",
+                    help="time the MXFP8 forward path (quantise + block-scaled forward) instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -477,6 +572,8 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.mxfp8:
+        return run_gpu_mxfp8(args, rank, world, local_rank)
     return run_gpu(args, rank, world, local_rank)
 
 

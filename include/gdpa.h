@@ -131,6 +131,26 @@ size_t gdpa_mxfp8_scale_bytes(int B, int H, int d, int64_t T, int mode);
 gdpa_status gdpa_quantize_mxfp8(const void* x, const int32_t* offsets, int B, int H, int d,
                                 int64_t T, int mode, void* codes, void* scales, void* stream);
 
+/* Forward pass on MXFP8 operands: both products run on the block-scaled
+ * tensor cores (E4M3 x E4M3 with E8M0 scales per 32 elements of the
+ * contraction, fp32 accumulation), and P is quantised to E4M3 per 32 keys in
+ * registers.  ("GEM Training ..." low-precision paragraph: attention with
+ * end-to-end MXFP8 block-scaled MMA.)
+ *   q_codes/q_scales, k_codes/k_scales: gdpa_quantize_mxfp8 output along
+ *     channels ([T][H][128] u8, [T][H][4] u8).
+ *   v_codes/v_scales: output along tokens ([Tkv][H][128] u8,
+ *     [B + Tkv/32 + 1][H][128] u8), quantised with the same kv_offsets.
+ * d must be 128 and act GDPA_ACT_SOFTMAX (an unnormalised GDPA sum of
+ * thousands of E4M3-rounded terms would not keep the output's precision);
+ * other values return GDPA_ERR_UNSUPPORTED.  Every other argument, the
+ * outputs and the workspace (gdpa_fwd_workspace_size) are those of gdpa_fwd. */
+gdpa_status gdpa_fwd_mxfp8(const void* q_codes, const void* q_scales, const int32_t* q_offsets,
+                           const void* k_codes, const void* k_scales, const void* v_codes,
+                           const void* v_scales, const int32_t* kv_offsets, int B, int H, int d,
+                           int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
+                           float scale, void* out, float* lse, void* workspace, size_t ws_bytes,
+                           void* stream);
+
 /* Reads the device status word set by earlier calls on this device,
  * synchronising `stream` first, then clears it.  Returns GDPA_OK,
  * GDPA_ERR_TIMEOUT, GDPA_ERR_BAD_OFFSETS or GDPA_ERR_CUDA. */

@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "GDPA_OK", 1: "GDPA_ERR_INVALID_ARG", 2: "GDPA_ERR_UNSUPPORTE
 EXPORTS = ("gdpa_fwd_workspace_size", "gdpa_fwd", "gdpa_bwd_workspace_size", "gdpa_bwd",
            "gdpa_get_device_status", "gdpa_status_string", "gdpa_last_launch_count",
            "gdpa_timing_enable", "gdpa_timing_collect", "gdpa_fwd_noalloc",
-           "gdpa_mxfp8_scale_bytes", "gdpa_quantize_mxfp8")
+           "gdpa_mxfp8_scale_bytes", "gdpa_quantize_mxfp8", "gdpa_fwd_mxfp8")
 MX_ALONG_CHANNELS, MX_ALONG_TOKENS = 0, 1
 
 
@@ -91,6 +91,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdpa_mxfp8_scale_bytes.restype = sz
         lib.gdpa_quantize_mxfp8.argtypes = [vp, vp, I, I, I, i64, I, vp, vp, vp]
         lib.gdpa_quantize_mxfp8.restype = I
+        lib.gdpa_fwd_mxfp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, i64, i64,
+                                       ctypes.POINTER(gdpa_bias), I, I, F, vp, vp, vp, sz, vp]
+        lib.gdpa_fwd_mxfp8.restype = I
         _lib = lib
         return lib
 
@@ -213,3 +216,27 @@ def quantize_mxfp8(x, offsets=None, *, mode, codes=None, scales=None, stream=Non
                                  _ptr(scales), _stream(stream))
     _check(rc, "gdpa_quantize_mxfp8")
     return codes, scales
+
+
+def gdpa_fwd_mxfp8(q_codes, q_scales, q_offsets, k_codes, k_scales, v_codes, v_scales, kv_offsets,
+                   *, causal=False, scale, bias=None, max_rel=0, out=None, lse=None,
+                   workspace=None, stream=None):
+    """MXFP8 forward (softmax) through the C ABI.  Returns (out bf16, lse)."""
+    lib = load()
+    Tq, H, d = q_codes.shape
+    Tkv = k_codes.shape[0]
+    B = q_offsets.numel() - 1
+    if out is None:
+        out = torch.empty((Tq, H, d), device=q_codes.device, dtype=torch.bfloat16)
+    if lse is None:
+        lse = torch.empty((H, Tq), device=q_codes.device, dtype=torch.float32)
+    if workspace is None:
+        workspace = torch.empty(fwd_workspace_size(B, H, d, Tq, Tkv), device=q_codes.device,
+                                dtype=torch.uint8)
+    rc = lib.gdpa_fwd_mxfp8(_ptr(q_codes), _ptr(q_scales), _ptr(q_offsets), _ptr(k_codes),
+                            _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), _ptr(kv_offsets), B,
+                            H, d, Tq, Tkv, _bias(bias, max_rel), ACT_SOFTMAX, int(bool(causal)),
+                            float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                            workspace.numel(), _stream(stream))
+    _check(rc, "gdpa_fwd_mxfp8")
+    return out, lse

@@ -109,6 +109,23 @@ bool make_dq_map(CUtensorMap* m, void* base, int64_t T, int H, int d) {
   return r == CUDA_SUCCESS;
 }
 
+// 3-D TMA map over E4M3 codes [T][H][d] (u8): box = d bytes x 1 head x
+// `box_rows` rows, 128-byte swizzle (d = 128).
+bool make_u8_map(CUtensorMap* m, const void* base, int64_t T, int H, int d, int box_rows) {
+  if (T <= 0) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d),
+                           static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(d)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -353,6 +370,81 @@ gdpa_status gdpa_quantize_mxfp8(const void* x, const int32_t* offsets, int B, in
                       ? launch_quant_rows(x, T * H, d, codes, scales, s)
                       : launch_quant_tokens(x, offsets, B, H, d, codes, scales, s);
   if (e != cudaSuccess) return GDPA_ERR_CUDA;
+  ++t_launches;
+  return GDPA_OK;
+}
+
+gdpa_status gdpa_fwd_mxfp8(const void* q_codes, const void* q_scales, const int32_t* q_offsets,
+                           const void* k_codes, const void* k_scales, const void* v_codes,
+                           const void* v_scales, const int32_t* kv_offsets, int B, int H, int d,
+                           int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
+                           float scale, void* out, float* lse, void* workspace, size_t ws_bytes,
+                           void* stream) {
+  t_launches = 0;
+  gdpa_status st = check_common(q_codes, q_offsets, k_codes, v_codes, kv_offsets, B, H, d, Tq,
+                                Tkv, bias, act, causal);
+  if (st != GDPA_OK) return st;
+  if (d != 128 || act != GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
+  if (Tq > 0 && (q_scales == nullptr || out == nullptr || lse == nullptr || !aligned16(out)))
+    return GDPA_ERR_INVALID_ARG;
+  if (Tkv > 0 && (k_scales == nullptr || v_scales == nullptr)) return GDPA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q_scales) & 3u) || (reinterpret_cast<uintptr_t>(k_scales) & 3u))
+    return GDPA_ERR_INVALID_ARG;  // scale words are read as 32-bit
+  const size_t need = gdpa_fwd_workspace_size(B, H, d, Tq, Tkv);
+  if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return GDPA_ERR_WORKSPACE;
+  if (Tq == 0 || B == 0) return GDPA_OK;
+
+  DeviceInfo* dev = nullptr;
+  if (device_info(&dev) != cudaSuccess) return GDPA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int max_rel = 1;
+  const float* table = bias_table(bias, &max_rel);
+  CUtensorMap tq, tk, tv;
+  if (!make_u8_map(&tq, q_codes, Tq, H, d, kHalfRows)) return GDPA_ERR_INVALID_ARG;
+  const void* kb = Tkv > 0 ? k_codes : q_codes;
+  const void* vb = Tkv > 0 ? v_codes : q_codes;
+  const int64_t Tk = Tkv > 0 ? Tkv : Tq;
+  if (!make_u8_map(&tk, kb, Tk, H, d, fwd_mx_tile_rows()) ||
+      !make_u8_map(&tv, vb, Tk, H, d, fwd_mx_tile_rows()))
+    return GDPA_ERR_INVALID_ARG;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* n_items = reinterpret_cast<int*>(ws);
+  int* ticket = reinterpret_cast<int*>(ws + 4);
+  int2* items = reinterpret_cast<int2*>(ws + 256);
+  if (launch_build_worklist(q_offsets, kv_offsets, B, H, Tq, Tkv, causal, 0, items, n_items,
+                            ticket, dev->status, s) != cudaSuccess)
+    return GDPA_ERR_CUDA;
+  ++t_launches;
+  FwdParams p{};
+  p.qo = q_offsets;
+  p.ko = kv_offsets;
+  p.B = B;
+  p.H = H;
+  p.d = d;
+  p.Tq = Tq;
+  p.Tkv = Tkv;
+  p.bias_table = table;
+  p.max_rel = max_rel;
+  p.causal = causal;
+  p.scale = scale;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.items = items;
+  p.n_items = n_items;
+  p.ticket = ticket;
+  p.status = dev->status;
+  const int64_t max_items = max_fwd_items(B, H, Tq);
+  const int grid = static_cast<int>(max_items < dev->sms ? max_items : dev->sms);
+  const long long v_rows = static_cast<long long>(B) + Tkv / 32 + 1;
+  cudaEvent_t ea = nullptr, eb = nullptr;
+  const bool timed = timing_slot(0, &ea, &eb);
+  if (timed && cudaEventRecord(ea, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (launch_fwd_mx(p, tq, tk, tv, static_cast<const uint8_t*>(q_scales),
+                    static_cast<const uint8_t*>(k_scales), static_cast<const uint8_t*>(v_scales),
+                    v_rows, grid, s) != cudaSuccess)
+    return GDPA_ERR_CUDA;
+  if (timed && cudaEventRecord(eb, s) != cudaSuccess) return GDPA_ERR_CUDA;
   ++t_launches;
   return GDPA_OK;
 }

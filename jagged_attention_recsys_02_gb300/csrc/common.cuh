@@ -92,6 +92,11 @@ cudaError_t launch_quant_rows(const void* x, long long rows, int d, void* codes,
 cudaError_t launch_quant_tokens(const void* x, const int32_t* offsets, int B, int H, int d,
                                 void* codes, void* scales, cudaStream_t s);
 
+int fwd_mx_tile_rows();
+cudaError_t launch_fwd_mx(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
+                          const uint8_t* v_sc, long long v_sc_rows, int grid, cudaStream_t s);
+
 // Upper bound on the number of work items (host-side sizing).
 inline int64_t max_fwd_items(int B, int H, int64_t Tq) {
   return static_cast<int64_t>(H) * (Tq / kItemRows + B);

@@ -438,7 +438,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         const int c0 = j * kKvRows;
         const bool need_mask = (c0 + kKvRows > in.Lkv) || (p.causal && c0 + kKvRows - 1 > r);
         const int col_lim = p.causal ? min(in.Lkv, r + 1) : in.Lkv;  // valid cols: c < col_lim
-        const bool plain = !need_mask && !has_bias;  // scores need only the scale
+        // Scores need only the scale when no row of the warp needs a mask and there
+        // is no bias.  Decided per warp: the tcgen05.ld below is .sync.aligned, so
+        // the lanes of a warp must not split between the two paths.
+        const bool plain = !has_bias && __all_sync(0xffffffffu, !need_mask);
         // bwin[-cc] = bias(row, tile column cc) for this thread's row
         const float* bwin = bias_win + ((gj % C::kStages) * 2 + half) * 256 + row_in_half + 127;
         // x = score * c_s + bias * c_b - sub, with masked entries set to `fill`
@@ -458,26 +461,36 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
           }
         };
         if (kSoftmax) {
+          // The row's 128 scores stay in registers: TMEM and the bias window are
+          // read once.  Plain tiles keep raw scores (scale folded into the exponent).
+          float xs[kKvRows];
           float mt = -INFINITY;
           if (plain) {
-            // max(score * c_s) = c_s * max(score) for c_s > 0: no per-element scaling
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
+#pragma unroll
             for (int chunk = 0; chunk < 4; ++chunk) {
               uint32_t sr[32];
               tmem_ld32(t_s + chunk * 32, sr);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sr[i]));
+              for (int i = 0; i < 32; ++i) {
+                xs[chunk * 32 + i] = __uint_as_float(sr[i]);
+                m4[i & 3] = fmaxf(m4[i & 3], xs[chunk * 32 + i]);
+              }
             }
             mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c_s;
           } else {
-#pragma unroll 1
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
             for (int chunk = 0; chunk < 4; ++chunk) {
               float x[32];
               load_x(chunk, 0.0f, -INFINITY, x);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) mt = fmaxf(mt, x[i]);
+              for (int i = 0; i < 32; ++i) {
+                xs[chunk * 32 + i] = x[i];
+                m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+              }
             }
+            mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
           }
           const float m_new = fmaxf(m, mt);
           bool rescale = false;
@@ -501,16 +514,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
             }
           }
           const float m_ref = (m == -INFINITY) ? 0.0f : m;
+          // exponent = xs * xm - m_ref (plain: raw scores times the scale)
+          const float xm = plain ? c_s : 1.0f;
           float l2[2] = {0.0f, 0.0f};
-#pragma unroll 1
+#pragma unroll
           for (int chunk = 0; chunk < 4; ++chunk) {
-            float x[32];
-            load_x(chunk, m_ref, -INFINITY, x);
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float p0 = ex2_approx(x[2 * i]);
-              const float p1 = ex2_approx(x[2 * i + 1]);
+              const float p0 = ex2_approx(fmaf(xs[chunk * 32 + 2 * i], xm, -m_ref));
+              const float p1 = ex2_approx(fmaf(xs[chunk * 32 + 2 * i + 1], xm, -m_ref));
               l2[0] += p0;
               l2[1] += p1;
               pk[i] = pack_bf16x2(p0, p1);

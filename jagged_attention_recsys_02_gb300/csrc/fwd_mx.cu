@@ -1,0 +1,659 @@
+// MXFP8 forward kernel of jagged softmax attention (JFA), sm_103a.
+//
+// "GEM Training ..." low-precision paragraph: attention with end-to-end
+// MXFP8 block-scaled MMA.  Both products run on the block-scaled tensor
+// cores (tcgen05.mma kind::mxf8f6f4.block_scale): E4M3 operands, one E8M0
+// scale per 32 elements of the contraction, fp32 accumulation.
+//   S = Q K^T   Q, K quantised along channels (scales per 32 of d)
+//   O = P V     V quantised along tokens in 32-token blocks aligned to each
+//               sample's start; P quantised in registers per 32 keys (with a
+//               saturation-free block scale, see e8m0_nosat)
+// (gdpa_quantize_mxfp8 produces the Q, K and V operands.)
+//
+// Structure: the bf16 forward's (persistent CTAs over the cost-sorted work
+// list, two 128-row query halves per item, online softmax with lazy O
+// rescale), with 96-row key tiles (three 32-token scale blocks) so that the
+// scale factors fit in TMEM beside S and O:
+//   columns [0,96) S/P of half 0, [128,256) O of half 0,
+//           [256,352) S/P of half 1, [384,512) O of half 1,
+//   scale columns in the gaps [96,128) and [352,384).
+// A scale factor of row r (of A) or column r (of B^T) for the 32-element
+// block k of one MMA is byte k of a 32-bit word held in TMEM column
+// base + r/32, lane r%32 of every 32-lane quarter.
+//
+// Warp roles (448 threads):
+//   warps 0-3 / 4-7  activation groups of half 0 / half 1: scale, bias,
+//                    mask, online softmax, P -> E4M3 codes + block scales
+//   warps 8-11       scale group: writes the Q, K and V scale words to TMEM
+//   warp  12         producer: tickets, TMA copies of Q/K/V codes, bias windows
+//   warp  13         MMA issuer
+#include "common.cuh"
+
+namespace gdpa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 448;
+constexpr int kScaleWarp0 = 8;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kD = 128;
+constexpr int kTile = 96;        // key rows per tile
+constexpr int kStages = 2;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
+
+// TMEM columns: S/P and O of half h, Q and P scale words of half h, K and
+// V scale words of stage s.
+__device__ __forceinline__ uint32_t col_s(int h) { return 256u * h; }
+__device__ __forceinline__ uint32_t col_o(int h) { return 128u + 256u * h; }
+__device__ __forceinline__ uint32_t col_sfq(int h) { return 96u + 8u * h; }
+__device__ __forceinline__ uint32_t col_sfp(int h) { return 112u + 8u * h; }
+__device__ __forceinline__ uint32_t col_sfk(int s) { return 352u + 8u * s; }
+__device__ __forceinline__ uint32_t col_sfv(int s) { return 368u + 8u * s; }
+
+struct Cfg {
+  static constexpr int kQHalfBytes = kHalfRows * kD;   // 16 KB of E4M3 codes
+  static constexpr int kTileBytes = kTile * kD;        // 12 KB
+  static constexpr int kQ0 = 0, kQ1 = kQHalfBytes;
+  static constexpr int kKV = 2 * kQHalfBytes;          // K[s] = kKV + s*2*tile, V = K + tile
+  static constexpr int kBias = kKV + kStages * 2 * kTileBytes;  // [stage][half][256] floats
+  static constexpr int kSfp = kBias + kStages * 2 * 256 * 4;    // [half][buf][128] u32 P-scale words
+  static constexpr int kBar = kSfp + 2 * 2 * kHalfRows * 4;
+  static constexpr int kQFull = 0, kQEmpty = 1;
+  static constexpr int kKFull = 2;                      // + s
+  static constexpr int kVFull = kKFull + kStages;
+  static constexpr int kKEmpty = kVFull + kStages;
+  static constexpr int kVEmpty = kKEmpty + kStages;
+  static constexpr int kSfkvFull = kVEmpty + kStages;   // K and V scale words in TMEM
+  static constexpr int kSfqFull = kSfkvFull + kStages;  // Q scale words in TMEM
+  static constexpr int kSFull = kSfqFull + 1;           // + half
+  static constexpr int kPFull = kSFull + 2;
+  static constexpr int kODone = kPFull + 2;
+  static constexpr int kItemFull = kODone + 2;          // + slot
+  static constexpr int kItemEmpty = kItemFull + 2;
+  static constexpr int kDrain = kItemEmpty + 2;
+  static constexpr int kSfpBar = kDrain + 1;            // + half * 2 + buf: P-scale words staged
+  static constexpr int kNumBars = kSfpBar + 4;
+  static constexpr int kItemSlots = kBar + 8 * kNumBars;
+  static constexpr int kTmemSlot = kItemSlots + 16;
+  static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kUsed = kAbort + 4;
+  static constexpr int kSmemBytes = kUsed + 1024;
+};
+
+// Instruction descriptor of kind::mxf8f6f4 with E4M3 operands and E8M0
+// scales: B scale-factor id (bits 4-5), A/B major (15, 16), N>>3 (17-22),
+// E8M0 scale type (23), M = 128 (M>>4 in bits 24-28), A scale-factor id (29-30).
+__device__ __forceinline__ uint32_t idesc_mx(int N, bool b_mn, int sf_id) {
+  return (static_cast<uint32_t>(sf_id) << 4) | ((b_mn ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (8u << 24) |
+         (static_cast<uint32_t>(sf_id) << 29);
+}
+
+__device__ __forceinline__ void mma_mx_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
+      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_mx_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], p;\n}\n"
+      ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c,
+                                         uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(a),
+               "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// E8M0 code of the smallest power of two X with amax / X <= 448 (E4M3's
+// largest normal), clamped to [0, 254].  For the probabilities P this
+// saturation-free choice is used instead of 2^(floor(log2 amax) - 8), which
+// maps the block maximum into [256, 512) and would clip a dominant
+// probability by up to 12.5% whenever its mantissa exceeds 1.75.
+__device__ __forceinline__ int e8m0_nosat(float amax) {
+  const uint32_t u = __float_as_uint(amax) & 0x7FFFFFFFu;
+  if (u == 0) return 0;
+  int e = (u >> 23) != 0 ? static_cast<int>(u >> 23) - 127 : -127 - (__clz(u) - 9);
+  if ((u >> 23) != 0 && (u & 0x7FFFFFu) > 0x600000u) ++e;  // mantissa above 1.75
+  const int code = e - 8 + 127;
+  return code < 0 ? 0 : (code > 254 ? 254 : code);
+}
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+struct ItemInfo {
+  int b, head, blk;
+  int q0, k0, Lq, Lkv;
+  int n0, n1;
+};
+
+__device__ __forceinline__ ItemInfo decode_item(int2 it, const FwdParams& p) {
+  ItemInfo r;
+  r.b = it.x;
+  r.head = item_head(it);
+  r.blk = item_block(it);
+  r.q0 = p.qo[r.b];
+  r.Lq = p.qo[r.b + 1] - r.q0;
+  r.k0 = p.ko[r.b];
+  r.Lkv = p.ko[r.b + 1] - r.k0;
+  const int nkv = (r.Lkv + kTile - 1) / kTile;
+  const int r0 = r.blk * kItemRows;
+  const bool h1 = r0 + kHalfRows < r.Lq;
+  if (!p.causal) {
+    r.n0 = nkv;
+    r.n1 = h1 ? nkv : 0;
+  } else {
+    r.n0 = min(nkv, (min(r.Lq, r0 + kHalfRows) + kTile - 1) / kTile);
+    r.n1 = h1 ? min(nkv, (min(r.Lq, r0 + kItemRows) + kTile - 1) / kTile) : 0;
+  }
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+              const __grid_constant__ CUtensorMap tmap_v, const FwdParams p,
+              const uint8_t* __restrict__ q_sc, const uint8_t* __restrict__ k_sc,
+              const uint8_t* __restrict__ v_sc, long long v_sc_rows) {
+  using C = Cfg;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kBar + 8u * i; };
+  int2* item_slot = reinterpret_cast<int2*>(gbase + C::kItemSlots);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kAbort);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(C::kQFull), 1);
+    mbar_init(bar(C::kQEmpty), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(C::kKFull + s), 1);
+      mbar_init(bar(C::kVFull + s), 1);
+      mbar_init(bar(C::kKEmpty + s), 1);
+      mbar_init(bar(C::kVEmpty + s), 1);
+      mbar_init(bar(C::kSfkvFull + s), 128);
+    }
+    mbar_init(bar(C::kSfqFull), 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(C::kSFull + h), 1);
+      mbar_init(bar(C::kPFull + h), kHalfRows);
+      mbar_init(bar(C::kODone + h), 1);
+      mbar_init(bar(C::kItemFull + h), 1);
+      mbar_init(bar(C::kItemEmpty + h), 1 + 3 * 128);
+    }
+    mbar_init(bar(C::kDrain), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(C::kSfpBar + i), kHalfRows);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    set_status(p.status, GDPA_ERR_TIMEOUT);
+  };
+  const int rel_w = 2 * p.max_rel - 1;
+  constexpr int kWin = kHalfRows + kTile - 1;  // relative positions a (half, tile) pair spans
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer (whole warp)
+    const int n_items = *p.n_items;
+    float* bias_win = reinterpret_cast<float*>(gbase + C::kBias);
+    uint32_t it = 0, g = 0, qi = 0;
+    uint32_t inflight = 0, last_g[kStages] = {};
+    bool q_inflight = false, ok = true;
+    while (ok) {
+      int2 item = make_int2(-1, 0);
+      if (lane == 0) {
+        const int t = atomicAdd(p.ticket, 1);
+        if (t < n_items) item = p.items[t];
+      }
+      item.x = __shfl_sync(0xffffffffu, item.x, 0);
+      item.y = __shfl_sync(0xffffffffu, item.y, 0);
+      const uint32_t slot = it & 1u;
+      bool w = mbar_wait(bar(C::kItemEmpty + slot), ((it >> 1) & 1u) ^ 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+      if (lane == 0) {
+        item_slot[slot] = item;
+        mbar_arrive(bar(C::kItemFull + slot));
+      }
+      ++it;
+      if (item.x < 0) break;
+      const ItemInfo in = decode_item(item, p);
+      const int n = max(in.n0, in.n1);
+      if (n == 0) continue;
+      w = mbar_wait(bar(C::kQEmpty), (qi & 1u) ^ 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+      const int row0 = in.q0 + in.blk * kItemRows;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(C::kQFull), (in.n1 > 0 ? 2 : 1) * C::kQHalfBytes);
+        for (int half = 0; half < (in.n1 > 0 ? 2 : 1); ++half)
+          tma_load_3d(sbase + (half ? C::kQ1 : C::kQ0), &tmap_q, bar(C::kQFull), 0, in.head,
+                      row0 + half * kHalfRows);
+        q_inflight = true;
+      }
+      ++qi;
+      const float* brow =
+          p.bias_table ? p.bias_table + static_cast<long long>(in.head) * rel_w : nullptr;
+      for (int j = 0; j < n; ++j, ++g) {
+        const uint32_t s = g % kStages;
+        const uint32_t ph = (g / kStages) & 1u;
+        const uint32_t kdst = sbase + C::kKV + s * 2 * C::kTileBytes;
+        const int krow = in.k0 + j * kTile;
+        w = mbar_wait(bar(C::kKEmpty + s), ph ^ 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; if (lane == 0) fail(); break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(C::kKFull + s), C::kTileBytes);
+          tma_load_3d(kdst, &tmap_k, bar(C::kKFull + s), 0, in.head, krow);
+          inflight |= 1u << s;
+          last_g[s] = g;
+        }
+        w = mbar_wait(bar(C::kVEmpty + s), ph ^ 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; if (lane == 0) fail(); break; }
+        if (brow != nullptr) {
+          // entry e of half h: bias(i - j') with (i - r_h) - (j' - c0) = e - (kTile - 1)
+          for (int h = 0; h < 2; ++h) {
+            const int w0 = in.blk * kItemRows + h * kHalfRows - j * kTile - (kTile - 1) +
+                           p.max_rel - 1;
+            float* win = bias_win + (s * 2 + h) * 256;
+            for (int e = lane; e < kWin; e += 32)
+              win[e] = __ldg(brow + min(max(w0 + e, 0), rel_w - 1));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(C::kVFull + s), C::kTileBytes);
+          tma_load_3d(kdst + C::kTileBytes, &tmap_v, bar(C::kVFull + s), 0, in.head, krow);
+        }
+      }
+    }
+    if (lane == 0 && *abort_flag) {
+      for (int s = 0; s < kStages; ++s)
+        if (inflight & (1u << s)) {
+          const uint32_t ph = (last_g[s] / kStages) & 1u;
+          mbar_wait(bar(C::kKFull + s), ph, nullptr, 50000000ull);
+          mbar_wait(bar(C::kVFull + s), ph, nullptr, 50000000ull);
+        }
+      if (q_inflight) mbar_wait(bar(C::kQFull), (qi - 1) & 1u, nullptr, 50000000ull);
+    }
+  } else if (warp >= kScaleWarp0 && warp < kScaleWarp0 + 4) {
+    // ------------------------------------------------------------ scale group
+    // Lane L = 32q + i of this group writes, in scale column c, the word of
+    // row / column i + 32c (every quarter holds the same words).
+    const int wq = warp & 3;
+    const int i = lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const int H = p.H;
+    uint32_t it = 0, g = 0, qi = 0;
+    while (true) {
+      const uint32_t slot = it & 1u;
+      bool w = mbar_wait(bar(C::kItemFull + slot), (it >> 1) & 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+      const int2 item = item_slot[slot];
+      mbar_arrive(bar(C::kItemEmpty + slot));
+      ++it;
+      if (item.x < 0) break;
+      const ItemInfo in = decode_item(item, p);
+      const int n = max(in.n0, in.n1);
+      if (n == 0) continue;
+      // Q scale words of both halves: the previous item's score products must be done
+      w = mbar_wait(bar(C::kQEmpty), (qi & 1u) ^ 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+      ++qi;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const long long row = static_cast<long long>(in.q0) + in.blk * kItemRows + h * kHalfRows + i + 32 * c;
+          wv[c] = row < p.Tq ? __ldg(reinterpret_cast<const uint32_t*>(q_sc) + row * H + in.head)
+                             : 0x7F7F7F7Fu;
+        }
+        tmem_st4(tmem + lane_off + col_sfq(h), wv[0], wv[1], wv[2], wv[3]);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::kSfqFull));
+      const long long vrow0 = static_cast<long long>(in.b) + in.k0 / 32;  // first scale row of the sample
+      const int nblk = (in.Lkv + 31) / 32;
+      bool abort_now = false;
+      for (int j = 0; j < n; ++j, ++g) {
+        const uint32_t s = g % kStages;
+        const uint32_t ph = (g / kStages) & 1u;
+        // both scale columns of stage s are free once that stage's value products are done
+        w = mbar_wait(bar(C::kVEmpty + s), ph ^ 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); abort_now = true; break; }
+        uint32_t kw[4], vw[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int n_row = i + 32 * c;  // key row of the tile (c < 3) / channel (V)
+          const long long krow = static_cast<long long>(in.k0) + j * kTile + n_row;
+          kw[c] = (c < 3 && krow < p.Tkv)
+                      ? __ldg(reinterpret_cast<const uint32_t*>(k_sc) + krow * H + in.head)
+                      : 0x7F7F7F7Fu;
+          uint32_t v = 0;
+#pragma unroll
+          for (int kb = 0; kb < 3; ++kb) {
+            const int blk = 3 * j + kb;
+            uint32_t byte = 127u;
+            if (blk < nblk && vrow0 + blk < v_sc_rows)
+              byte = __ldg(v_sc + ((vrow0 + blk) * H + in.head) * kD + n_row);
+            v |= byte << (8 * kb);
+          }
+          vw[c] = v | (127u << 24);
+        }
+        tmem_st4(tmem + lane_off + col_sfk(s), kw[0], kw[1], kw[2], kw[3]);
+        tmem_st4(tmem + lane_off + col_sfv(s), vw[0], vw[1], vw[2], vw[3]);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::kSfkvFull + s));
+      }
+      if (abort_now) break;
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, g = 0, qi = 0;
+      uint32_t tcount[2] = {0, 0};
+      bool issued_any = false;
+      auto issue_s = [&](int half, uint32_t stage) {
+        const uint32_t qa = sbase + (half ? C::kQ1 : C::kQ0);
+        const uint32_t ka = sbase + C::kKV + stage * 2 * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kD / 32; ++ks) {
+          const uint64_t ad = sdesc(qa + ks * 32, 0, 1024, kSwizzle128B);
+          const uint64_t bd = sdesc(ka + ks * 32, 0, 1024, kSwizzle128B);
+          mma_mx_ss(tmem + col_s(half), ad, bd, idesc_mx(kTile, false, ks), tmem + col_sfq(half),
+                    tmem + col_sfk(stage), ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kSFull + half));
+        issued_any = true;
+      };
+      auto issue_pv = [&](int half, uint32_t stage, bool first) {
+        const uint32_t va = sbase + C::kKV + stage * 2 * C::kTileBytes + C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kTile / 32; ++ks) {
+          const uint64_t bd = sdesc(va + ks * 4096, 0, 1024, kSwizzle128B);
+          mma_mx_ts(tmem + col_o(half), tmem + col_s(half) + 8 * ks, bd, idesc_mx(kD, true, ks),
+                    tmem + col_sfp(half), tmem + col_sfv(stage), (first && ks == 0) ? 0u : 1u);
+        }
+        issued_any = true;
+      };
+      bool ok = true;
+      while (ok) {
+        const uint32_t slot = it & 1u;
+        if (!mbar_wait(bar(C::kItemFull + slot), (it >> 1) & 1u, abort_flag)) { fail(); break; }
+        const int2 item = item_slot[slot];
+        mbar_arrive(bar(C::kItemEmpty + slot));
+        ++it;
+        if (item.x < 0) break;
+        const ItemInfo in = decode_item(item, p);
+        const int n = max(in.n0, in.n1);
+        if (n == 0) continue;
+        if (!mbar_wait(bar(C::kQFull), qi & 1u, abort_flag)) { fail(); break; }
+        if (!mbar_wait(bar(C::kSfqFull), qi & 1u, abort_flag)) { fail(); break; }
+        ++qi;
+        tc_fence_after();
+        const int last_s_half = (in.n1 == n) ? 1 : 0;
+        {
+          const uint32_t s = g % kStages;
+          const uint32_t ph = (g / kStages) & 1u;
+          if (!mbar_wait(bar(C::kKFull + s), ph, abort_flag)) { fail(); break; }
+          if (!mbar_wait(bar(C::kSfkvFull + s), ph, abort_flag)) { fail(); break; }
+          tc_fence_after();
+          if (in.n0 > 0) issue_s(0, s);
+          if (in.n1 > 0) issue_s(1, s);
+          mma_commit(bar(C::kKEmpty + s));
+          if (n == 1) mma_commit(bar(C::kQEmpty));
+        }
+        for (int j = 0; j < n; ++j) {
+          const uint32_t gj = g + j;
+          const uint32_t s = gj % kStages;
+          const uint32_t s_next = (gj + 1) % kStages;
+          const uint32_t ph_next = ((gj + 1) / kStages) & 1u;
+          if (!mbar_wait(bar(C::kVFull + s), (gj / kStages) & 1u, abort_flag)) { ok = false; fail(); break; }
+          const int last_half_j = (j < in.n1) ? 1 : 0;
+          for (int half = 0; half < 2; ++half) {
+            const int nh = half ? in.n1 : in.n0;
+            if (j >= nh) continue;
+            if (!mbar_wait(bar(C::kPFull + half), tcount[half] & 1u, abort_flag)) { ok = false; fail(); break; }
+            ++tcount[half];
+            tc_fence_after();
+            issue_pv(half, s, j == 0);
+            if (j == nh - 1) mma_commit(bar(C::kODone + half));
+            if (half == last_half_j) mma_commit(bar(C::kVEmpty + s));
+            if (j + 1 < nh) {
+              if (!mbar_wait(bar(C::kKFull + s_next), ph_next, abort_flag) ||
+                  !mbar_wait(bar(C::kSfkvFull + s_next), ph_next, abort_flag)) { ok = false; fail(); break; }
+              tc_fence_after();
+              issue_s(half, s_next);
+              if (half == ((j + 1 < in.n1) ? 1 : 0)) mma_commit(bar(C::kKEmpty + s_next));
+              if (j + 1 == n - 1 && half == last_s_half) mma_commit(bar(C::kQEmpty));
+            }
+          }
+          if (!ok) break;
+        }
+        g += n;
+      }
+      if (issued_any) {
+        mma_commit(bar(C::kDrain));
+        mbar_wait(bar(C::kDrain), 0, nullptr, 100000000ull);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ activation groups
+    const int half = warp >> 2;
+    const int wq = warp & 3;
+    const int row_in_half = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + col_s(half);
+    const uint32_t t_o = tmem + lane_off + col_o(half);
+    const float c_s = p.scale * kLog2e;
+    const float* bias_win = reinterpret_cast<const float*>(gbase + C::kBias);
+    uint32_t* sfp_base = reinterpret_cast<uint32_t*>(gbase + C::kSfp) + half * 2 * kHalfRows;
+    uint32_t it = 0, tcount = 0, ocount = 0, g = 0, ptile = 0;
+    while (true) {
+      const uint32_t slot = it & 1u;
+      bool ok = mbar_wait(bar(C::kItemFull + slot), (it >> 1) & 1u, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) { if (lane == 0) fail(); break; }
+      const int2 item = item_slot[slot];
+      mbar_arrive(bar(C::kItemEmpty + slot));
+      ++it;
+      if (item.x < 0) break;
+      const ItemInfo in = decode_item(item, p);
+      const int nh = half ? in.n1 : in.n0;
+      const uint32_t g_item = g;
+      g += max(in.n0, in.n1);
+      const int r = in.blk * kItemRows + half * kHalfRows + row_in_half;
+      if (half == 1 && in.n1 == 0 && in.blk * kItemRows + kHalfRows >= in.Lq) continue;
+      const bool row_valid = r < in.Lq;
+      const bool has_bias = p.bias_table != nullptr;
+      float m = -INFINITY, l = 0.0f;
+      bool abort_now = false;
+      for (int j = 0; j < nh; ++j) {
+        const uint32_t gj = g_item + j;
+        bool okw = mbar_wait(bar(C::kSFull + half), tcount & 1u, abort_flag);
+        if (has_bias)
+          okw = okw && mbar_wait(bar(C::kVFull + gj % kStages), (gj / kStages) & 1u, abort_flag);
+        okw = __all_sync(0xffffffffu, okw);
+        if (!okw) { if (lane == 0) fail(); abort_now = true; break; }
+        ++tcount;
+        tc_fence_after();
+        const int c0 = j * kTile;
+        const bool need_mask = (c0 + kTile > in.Lkv) || (p.causal && c0 + kTile - 1 > r);
+        const int col_lim = p.causal ? min(in.Lkv, r + 1) : in.Lkv;
+        const float* bwin =
+            bias_win + ((gj % kStages) * 2 + half) * 256 + row_in_half + (kTile - 1);
+        auto load_x = [&](int chunk, float sub, float (&x)[32]) {
+          uint32_t sr[32];
+          tmem_ld32(t_s + chunk * 32, sr);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) x[q] = fmaf(__uint_as_float(sr[q]), c_s, -sub);
+          if (has_bias) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) x[q] = fmaf(bwin[-(chunk * 32 + q)], kLog2e, x[q]);
+          }
+          if (need_mask) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+              if (c0 + chunk * 32 + q >= col_lim) x[q] = -INFINITY;
+          }
+        };
+        float mt = -INFINITY;
+#pragma unroll 1
+        for (int chunk = 0; chunk < kTile / 32; ++chunk) {
+          float x[32];
+          load_x(chunk, 0.0f, x);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) mt = fmaxf(mt, x[q]);
+        }
+        const float m_new = fmaxf(m, mt);
+        bool rescale = false;
+        float factor = 1.0f;
+        if (m == -INFINITY) {
+          m = m_new;
+        } else if (m_new - m > kRescaleThreshold) {
+          factor = ex2_approx(m - m_new);
+          l *= factor;
+          m = m_new;
+          rescale = true;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int chunk = 0; chunk < kD / 32; ++chunk) {
+            uint32_t o[32];
+            tmem_ld32(t_o + chunk * 32, o);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * factor);
+            tmem_st32(t_o + chunk * 32, o);
+          }
+        }
+        const float m_ref = (m == -INFINITY) ? 0.0f : m;
+        uint32_t sfw = 127u << 24;  // byte kb = scale of keys [32kb, 32kb+32) of the tile
+#pragma unroll 1
+        for (int chunk = 0; chunk < kTile / 32; ++chunk) {
+          float x[32];
+          load_x(chunk, m_ref, x);
+          float amax = 0.0f;
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            x[q] = ex2_approx(x[q]);
+            l += x[q];
+            amax = fmaxf(amax, x[q]);
+          }
+          const int code = e8m0_nosat(amax);
+          const float inv = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
+          uint32_t pk[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            pk[q] = e4m3x4(x[4 * q] * inv, x[4 * q + 1] * inv, x[4 * q + 2] * inv,
+                           x[4 * q + 3] * inv);
+          tmem_st8(t_s + chunk * 8, pk);  // E4M3 codes: 4 keys per column
+          sfw |= static_cast<uint32_t>(code) << (8 * chunk);
+        }
+        // P scale words: row r of the half goes to column r/32, lane r%32 of every
+        // quarter, so the words are exchanged through shared memory (double
+        // buffered: a buffer is rewritten only after every thread has passed the
+        // next tile's exchange, i.e. finished reading it).
+        const uint32_t pbuf = ptile & 1u;
+        uint32_t* words = sfp_base + pbuf * kHalfRows;
+        words[row_in_half] = sfw;
+        mbar_arrive(bar(C::kSfpBar + half * 2 + pbuf));
+        okw = mbar_wait(bar(C::kSfpBar + half * 2 + pbuf), (ptile >> 1) & 1u, abort_flag);
+        okw = __all_sync(0xffffffffu, okw);
+        ++ptile;
+        if (!okw) { if (lane == 0) fail(); abort_now = true; break; }
+        tmem_st4(tmem + lane_off + col_sfp(half), words[lane], words[32 + lane], words[64 + lane],
+                 words[96 + lane]);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::kPFull + half));
+      }
+      if (abort_now) break;
+      const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+      __nv_bfloat16* orow = p.out + (static_cast<long long>(in.q0 + r) * p.H + in.head) * kD;
+      if (nh > 0) {
+        bool okw = mbar_wait(bar(C::kODone + half), ocount & 1u, abort_flag);
+        okw = __all_sync(0xffffffffu, okw);
+        if (!okw) { if (lane == 0) fail(); break; }
+        ++ocount;
+        tc_fence_after();
+#pragma unroll 1
+        for (int chunk = 0; chunk < kD / 32; ++chunk) {
+          uint32_t o[32];
+          tmem_ld32(t_o + chunk * 32, o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            pk[q] = pack_bf16x2(__uint_as_float(o[2 * q]) * inv_l, __uint_as_float(o[2 * q + 1]) * inv_l);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + chunk * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+        tc_fence_before();
+      } else if (row_valid) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+        for (int v = 0; v < kD / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+      }
+      if (row_valid && p.lse != nullptr) {
+        const float lse = (l > 0.0f) ? (m * kLn2 + __logf(l)) : -INFINITY;
+        p.lse[static_cast<long long>(in.head) * p.Tq + in.q0 + r] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+int fwd_mx_tile_rows() { return kTile; }
+
+cudaError_t launch_fwd_mx(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
+                          const uint8_t* v_sc, long long v_sc_rows, int grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(fwd_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  fwd_mx_kernel<<<grid, kThreads, Cfg::kSmemBytes, s>>>(tq, tk, tv, p, q_sc, k_sc, v_sc, v_sc_rows);
+  return cudaGetLastError();
+}
+
+}  // namespace gdpa

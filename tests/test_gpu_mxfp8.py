@@ -82,3 +82,146 @@ def test_quant_full_size_v_and_q():
         rc, rs = oracle.quant_rows(to_np(x[sl]))
         np.testing.assert_array_equal(qc[sl].cpu().numpy(), rc)
         np.testing.assert_array_equal(qs[sl].cpu().numpy(), rs)
+
+
+# ------------------------------------------------------------------ MXFP8 forward
+from gpu_common import MXFP8_TOL, assert_close, check_guards, guarded, oracle_fwd_samples, rand_bf16  # noqa: E402
+from jagged_attention_recsys_02_gb300.workloads import make_tensors, make_workload  # noqa: E402
+
+
+def _mx_fwd(q, qo, k, v, ko, causal, scale, bias=None, max_rel=0):
+    qc, qs = binding.quantize_mxfp8(q, mode=binding.MX_ALONG_CHANNELS)
+    kc, ks = binding.quantize_mxfp8(k, mode=binding.MX_ALONG_CHANNELS)
+    vc, vs = binding.quantize_mxfp8(v, ko, mode=binding.MX_ALONG_TOKENS)
+    Tq, H, d = q.shape
+    buf, out = guarded(Tq, H, d, q.device)
+    lse = torch.full((H, Tq), float("nan"), device=q.device)
+    binding.gdpa_fwd_mxfp8(qc, qs, qo, kc, ks, vc, vs, ko, causal=causal, scale=scale, bias=bias,
+                           max_rel=max_rel, out=out, lse=lse)
+    assert binding.device_status() == 0
+    check_guards(buf)
+    return out, lse
+
+
+def _dequant_rows(x):
+    """Oracle quantisation along channels, then back to float64 (E4M3 x 2^(s-127))."""
+    codes, scales = oracle.quant_rows(x)
+    dec = _DEC[codes]
+    return dec * np.exp2(scales.astype(np.float64) - 127).repeat(32, axis=2)
+
+
+def _dequant_tokens(x, offs):
+    codes, scales = oracle.quant_cols(x, offs)
+    dec = _DEC[codes]
+    out = np.zeros_like(dec)
+    k = 0
+    for b in range(len(offs) - 1):
+        for r in range((int(offs[b + 1]) - int(offs[b]) + 31) // 32):
+            t0 = int(offs[b]) + 32 * r
+            t1 = min(t0 + 32, int(offs[b + 1]))
+            out[t0:t1] = dec[t0:t1] * np.exp2(scales[k].astype(np.float64) - 127)[None]
+            k += 1
+    return out
+
+
+_DEC = np.array([oracle.e4m3_decode(c) for c in range(256)])
+
+
+def _mx_reference(q, k, v, qo, ko, samples, causal, scale, bias, max_rel, rows=None):
+    """fp64 oracle attention on the MXFP8 operands: the bf16 inputs quantised by the
+    oracle's own quantiser and decoded again (only P's rounding is left to the
+    kernel), plus the exact reference on the unquantised inputs for the report."""
+    qd = _dequant_rows(q)
+    kd = _dequant_rows(k)
+    vd = _dequant_tokens(v, ko)
+    mx = oracle_fwd_samples(qd, kd, vd, qo, ko, samples, "softmax", causal, scale, bias, max_rel,
+                            rows=rows)
+    exact = oracle_fwd_samples(q, k, v, qo, ko, samples, "softmax", causal, scale, bias, max_rel,
+                               rows=rows)
+    return mx, exact
+
+
+def _report_exact(got_all, exact, what):
+    worst = 0.0
+    for r_, o, _ in exact:
+        err = np.abs(got_all[r_] - o) / (MXFP8_TOL[0] + MXFP8_TOL[1] * np.abs(o))
+        worst = max(worst, float(err.max()) if err.size else 0.0)
+    print(f"{what}: worst err/bound against the unquantised inputs {worst:.3f}")
+
+
+def _mx_case(lq, lkv, H, causal=False, max_rel=0, seed=0):
+    d = 128
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    q = rand_bf16((sum(lq), H, d), g, DEV)
+    k = rand_bf16((sum(lkv), H, d), g, DEV)
+    v = rand_bf16((sum(lkv), H, d), g, DEV)
+    qo_np, ko_np = offsets(lq), offsets(lkv)
+    qo, ko = torch.from_numpy(qo_np).to(DEV), torch.from_numpy(ko_np).to(DEV)
+    bias = torch.randn(H, 2 * max_rel - 1, generator=g, device=DEV) * 0.5 if max_rel else None
+    scale = 1.0 / np.sqrt(d)
+    out, lse = _mx_fwd(q, qo, k, v, ko, causal, scale, bias, max_rel)
+    ref, exact = _mx_reference(to_np(q), to_np(k), to_np(v), qo_np, ko_np, range(len(lq)), causal,
+                               scale, None if bias is None else bias.cpu().double().numpy(),
+                               max_rel)
+    got = to_np(out)
+    got_lse = lse.cpu().double().numpy()
+    for rows, o, l in ref:
+        assert_close(got[rows], o, MXFP8_TOL, f"mxfp8 out rows {rows[0]}..{rows[-1]}")
+        assert_close(got_lse[:, rows], l, MXFP8_TOL, "mxfp8 lse")
+    _report_exact(got, exact, "mxfp8 case")
+
+
+def test_mxfp8_fwd_ragged():
+    # lengths crossing the 32-token scale blocks and the 96-row key tiles
+    _mx_case([1, 31, 32, 33, 95, 96, 97, 200, 0, 300, 513, 64],
+             [7, 32, 31, 96, 97, 1, 200, 3, 5, 191, 700, 64], 2)
+
+
+def test_mxfp8_fwd_causal_relpos():
+    L = [1, 96, 97, 128, 300, 0, 511, 257]
+    _mx_case(L, L, 2, causal=True, max_rel=300)
+
+
+def test_mxfp8_fwd_empty_keys():
+    _mx_case([3, 0, 130, 5], [0, 9, 0, 140], 2)
+
+
+def test_mxfp8_rejects_gdpa_and_d64():
+    lib = binding.load()
+    p = torch.zeros(64, device=DEV, dtype=torch.uint8).data_ptr()
+    o = torch.zeros(2, device=DEV, dtype=torch.int32).data_ptr()
+    common = (p, p, o, p, p, p, p, o, 1, 1)
+    assert lib.gdpa_fwd_mxfp8(*common, 128, 1, 1, None, 1, 0, 0.1, p, p, p, 1 << 20, None) == 2
+    assert lib.gdpa_fwd_mxfp8(*common, 64, 1, 1, None, 0, 0, 0.1, p, p, p, 1 << 20, None) == 2
+
+
+def test_mxfp8_fwd_full_heavy_tail():
+    """The production-like heavy-tailed mix (B=1024, log-normal lengths), softmax,
+    checked on the first, last and tile-boundary query rows of sampled samples."""
+    w = make_workload("heavy_tail", act="softmax")
+    t = make_tensors(w, device=DEV, with_dout=False)
+    out, lse = _mx_fwd(t["q"], t["qo"], t["k"], t["v"], t["ko"], False, w.scale)
+    qo, ko = w.offsets()
+    pairs = w.lq * w.lkv
+    rng = np.random.default_rng(5)
+    samples = sorted({int(np.argmin(pairs)), int(np.argmax(pairs)),
+                      *rng.choice(w.B, 12, replace=False).tolist()})
+    for b in samples:
+        q0, q1, k0, k1 = int(qo[b]), int(qo[b + 1]), int(ko[b]), int(ko[b + 1])
+        L = q1 - q0
+        rows = np.array(sorted({0, 1, L // 2, L - 1, *range(95, L, 96 * 5)}))
+        rows = rows[(rows >= 0) & (rows < L)]
+        ref, exact = _mx_reference(to_np(t["q"][q0:q1]), to_np(t["k"][k0:k1]),
+                                   to_np(t["v"][k0:k1]), np.array([0, L]),
+                                   np.array([0, k1 - k0]), [0], False, w.scale, None, 0,
+                                   rows={0: rows})
+        got_rows = {}
+        for r, o, l in ref:
+            sel = torch.from_numpy(q0 + r).to(DEV)
+            assert_close(to_np(out[sel]), o, MXFP8_TOL, f"heavy_tail mxfp8 sample {b}")
+            assert_close(lse[:, sel].cpu().double().numpy(), l, MXFP8_TOL, "heavy_tail mxfp8 lse")
+            got_rows[0] = to_np(out[sel])
+        for r, o, _ in exact:
+            err = np.abs(got_rows[0] - o) / (MXFP8_TOL[0] + MXFP8_TOL[1] * np.abs(o))
+            print(f"heavy_tail sample {b}: worst err/bound against the unquantised inputs "
+                  f"{float(err.max()):.3f}")

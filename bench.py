@@ -474,8 +474,7 @@ def run_gpu_mxfp8(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     if world > 1 and not dist.is_initialized():
         dist.init_process_group("nccl", device_id=dev)
-    w = make_workload(args.workload if args.workload != "jfa_causal_relpos" else "heavy_tail",
-                      act="softmax")
+    w = make_workload(args.workload or "heavy_tail", act="softmax")
     t = make_tensors(w, device=dev, seed=rank, with_dout=False)
     H, d, Tq, Tkv = w.H, w.d, w.Tq, w.Tkv
     out = torch.empty_like(t["q"])
@@ -557,7 +556,8 @@ def main():
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gdpa", choices=["gdpa", "reference"])
-    ap.add_argument("--workload", default="jfa_causal_relpos")
+    ap.add_argument("--workload", default=None,
+                    help="default: jfa_causal_relpos (heavy_tail with --mxfp8)")
     ap.add_argument("--act", default=None, help="override the workload's activation")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -571,9 +571,11 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
+        args.workload = args.workload or "jfa_causal_relpos"
         return run_reference(args, rank, world)
     if args.mxfp8:
         return run_gpu_mxfp8(args, rank, world, local_rank)
+    args.workload = args.workload or "jfa_causal_relpos"
     return run_gpu(args, rank, world, local_rank)
 
 

@@ -151,6 +151,79 @@ def workload_flops(w):
     return f, BWD_FLOP_FACTOR * f
 
 
+def measure_padded_sdpa(w, t, dev, iters=5, max_gb=40.0):
+    """torch's scaled_dot_product_attention, forward + backward, on zero-padded
+    [B, H, Lmax, d] copies of the same inputs, on the same GPU, timed with CUDA
+    events.  Its TFLOPS count the same non-padded FLOPs as the jagged path.
+
+    Softmax self-attention gets the exact mask (causal and rel-pos bias folded
+    into one additive [1, H, Lmax, Lmax] tensor; with equal lengths causality
+    also hides every padded key from every real query).  Other workloads run
+    mask-free softmax SDPA, a time-only lower bound on the padded cost (torch
+    has no fused SiLU/GELU attention and no cheap key-padding mask at Lmax)."""
+    import torch
+    import torch.nn.functional as F
+
+    B, H, d = w.B, w.H, w.d
+    lq_max, lkv_max = int(w.lq.max()), int(w.lkv.max())
+    exact = w.act == "softmax" and (w.causal or np.array_equal(w.lq, w.lkv))
+    gb = (4 * B * H * lq_max * d + 4 * B * H * lkv_max * d) * 2 / 1e9
+    if exact:
+        gb += H * lq_max * lkv_max * 2 / 1e9
+    if gb > max_gb:
+        return {"value": None, "skipped": f"padded copies would need {gb:.0f} GB"}
+    qo, ko = w.offsets()
+
+    def pad(x, offs, lmax):
+        y = torch.zeros((B, lmax, H, d), device=dev, dtype=x.dtype)
+        for b in range(B):
+            n = int(offs[b + 1] - offs[b])
+            if n:
+                y[b, :n] = x[int(offs[b]):int(offs[b + 1])]
+        return y.transpose(1, 2).contiguous()
+
+    q = pad(t["q"], qo, lq_max).requires_grad_(True)
+    k = pad(t["k"], ko, lkv_max).requires_grad_(True)
+    v = pad(t["v"], ko, lkv_max).requires_grad_(True)
+    do = pad(t["dout"], qo, lq_max)
+    mask = None
+    if exact and (w.causal or w.max_rel):
+        i = torch.arange(lq_max, device=dev)[:, None]
+        j = torch.arange(lkv_max, device=dev)[None, :]
+        if w.max_rel:
+            idx = (i - j + (w.max_rel - 1)).clamp(0, 2 * w.max_rel - 2)
+            mask = t["bias"][:, idx].to(torch.bfloat16)[None]
+        else:
+            mask = torch.zeros((1, H, lq_max, lkv_max), device=dev, dtype=torch.bfloat16)
+        if w.causal:
+            mask = mask.masked_fill((j > i)[None, None], float("-inf"))
+
+    def once():
+        o = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=w.scale)
+        o.backward(do)
+        q.grad = k.grad = v.grad = None
+
+    for _ in range(2):
+        once()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        once()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    fwd, bwd = workload_flops(w)
+    return {"value": (fwd + bwd) / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "inputs": f"zero-padded [B={B}, H={H}, Lmax, d={d}] bf16",
+            "mask": ("causal + rel-pos bias as one additive bf16 mask" if mask is not None and
+                     w.max_rel else "causal" if mask is not None else
+                     "none (exact for equal lengths without causal)" if exact else
+                     "none: mask-free softmax lower bound on padded cost"),
+            "steps": iters}
+
+
 def pick_cpu_sample(w, target_pairs, seed=0):
     """Deterministic subset of samples whose pair count is close to target_pairs."""
     order = np.random.default_rng(seed + 12345).permutation(w.B)
@@ -426,6 +499,12 @@ def run_gpu(args, rank, world, local_rank):
         cpu = {"value": tf, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": desc,
                "seconds": secs}
 
+    sdpa = None
+    if rank == 0 and world == 1 and not args.no_sdpa:
+        sdpa = measure_padded_sdpa(w, t, dev)
+        if sdpa.get("value"):
+            sdpa["jagged_over_padded"] = value / sdpa["value"]
+
     in_bytes = sum(x.numel() * x.element_size() for x in (t["q"], t["k"], t["v"], t["dout"]))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -449,6 +528,7 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "padded_sdpa": sdpa,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -561,6 +641,8 @@ def main():
     ap.add_argument("--act", default=None, help="override the workload's activation")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sdpa", action="store_true",
+                    help="skip the padded torch SDPA comparison")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--mxfp8", action="store_true",
                     help="time the MXFP8 forward path (quantise + block-scaled forward) instead")

@@ -368,7 +368,7 @@ gdpa_status gdpa_quantize_mxfp8(const void* x, const int32_t* offsets, int B, in
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = (mode == GDPA_MX_ALONG_CHANNELS)
                       ? launch_quant_rows(x, T * H, d, codes, scales, s)
-                      : launch_quant_tokens(x, offsets, B, H, d, codes, scales, s);
+                      : launch_quant_tokens(x, offsets, B, H, d, T, codes, scales, s);
   if (e != cudaSuccess) return GDPA_ERR_CUDA;
   ++t_launches;
   return GDPA_OK;

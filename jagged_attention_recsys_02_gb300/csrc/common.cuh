@@ -90,7 +90,7 @@ cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float sca
 cudaError_t launch_quant_rows(const void* x, long long rows, int d, void* codes, void* scales,
                               cudaStream_t s);
 cudaError_t launch_quant_tokens(const void* x, const int32_t* offsets, int B, int H, int d,
-                                void* codes, void* scales, cudaStream_t s);
+                                long long T, void* codes, void* scales, cudaStream_t s);
 
 int fwd_mx_tile_rows();
 cudaError_t launch_fwd_mx(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,

@@ -81,33 +81,65 @@ quant_rows_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ cod
   }
 }
 
-// One CTA per sample; threads cover (head, channel) pairs, one block of 32
-// tokens at a time (consecutive threads read consecutive channels).
-__global__ void __launch_bounds__(256)
+// One CTA per scale row s (32-token block r of sample b, s = b + floor(o_b/32) + r;
+// g(b) = b + floor(o_b/32) rises by at least 1 per sample, so the sample owning s is
+// the last b with g(b) <= s).  Rows in the gaps between samples own no tokens and are
+// left untouched.  Each thread takes 4 consecutive (head, channel) columns: 32 8-byte
+// loads in flight, a warp covers 256 contiguous bytes of each token row.
+__global__ void __launch_bounds__(128)
 quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ offsets,
-                    int H, int d, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
-  const int b = blockIdx.x;
+                    int B, int hd, long long T, uint8_t* __restrict__ codes,
+                    uint8_t* __restrict__ scales) {
+  const long long s = blockIdx.x;
+  int lo = 0, hi = B - 1;  // largest b with g(b) <= s; g(0) = 0 <= s
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (mid + offsets[mid] / 32 <= s) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
   const int t0 = offsets[b], L = offsets[b + 1] - t0;
-  const int hd = H * d;
-  const long long srow0 = static_cast<long long>(b) + t0 / 32;
-  for (int r = 0; 32 * r < L; ++r) {
-    const int n = min(32, L - 32 * r);
-    const long long tok = static_cast<long long>(t0) + 32 * r;
-    for (int c = threadIdx.x; c < hd; c += blockDim.x) {
-      float f[32];
-      float amax = 0.0f;
-#pragma unroll 8
-      for (int i = 0; i < 32; ++i) {
-        f[i] = i < n ? __bfloat162float(x[(tok + i) * hd + c]) : 0.0f;
-        amax = fmaxf(amax, fabsf(f[i]));
-      }
-      const int code = e8m0_code(amax);
-      const float inv = inv_scale(code);
-#pragma unroll 8
-      for (int i = 0; i < 32; ++i)
-        if (i < n) codes[(tok + i) * hd + c] = static_cast<uint8_t>(e4m3x2(f[i] * inv, 0.0f));
-      scales[(srow0 + r) * hd + c] = static_cast<uint8_t>(code);
+  if (t0 < 0 || L <= 0 || t0 + static_cast<long long>(L) > T) return;  // nothing valid to read
+  const int r = static_cast<int>(s - (b + t0 / 32));
+  if (r < 0 || 32 * r >= L) return;
+  const int n = min(32, L - 32 * r);
+  const long long tok = static_cast<long long>(t0) + 32 * r;
+  for (int g = threadIdx.x; 4 * g < hd; g += blockDim.x) {
+    const __nv_bfloat16* src = x + tok * hd + 4 * g;
+    uint2 v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      v[i] = i < n ? *reinterpret_cast<const uint2*>(src + static_cast<long long>(i) * hd)
+                   : make_uint2(0u, 0u);
+    float amax[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      amax[0] = fmaxf(amax[0], fabsf(__uint_as_float(v[i].x << 16)));
+      amax[1] = fmaxf(amax[1], fabsf(__uint_as_float(v[i].x & 0xFFFF0000u)));
+      amax[2] = fmaxf(amax[2], fabsf(__uint_as_float(v[i].y << 16)));
+      amax[3] = fmaxf(amax[3], fabsf(__uint_as_float(v[i].y & 0xFFFF0000u)));
     }
+    int code[4];
+    float inv[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      code[c] = e8m0_code(amax[c]);
+      inv[c] = inv_scale(code[c]);
+    }
+    uint8_t* dst = codes + tok * hd + 4 * g;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i < n) {
+        const uint32_t w =
+            e4m3x2(__uint_as_float(v[i].x << 16) * inv[0],
+                   __uint_as_float(v[i].x & 0xFFFF0000u) * inv[1]) |
+            (e4m3x2(__uint_as_float(v[i].y << 16) * inv[2],
+                    __uint_as_float(v[i].y & 0xFFFF0000u) * inv[3]) << 16);
+        *reinterpret_cast<uint32_t*>(dst + static_cast<long long>(i) * hd) = w;
+      }
+    }
+    *reinterpret_cast<uint32_t*>(scales + s * hd + 4 * g) =
+        static_cast<uint32_t>(code[0]) | (static_cast<uint32_t>(code[1]) << 8) |
+        (static_cast<uint32_t>(code[2]) << 16) | (static_cast<uint32_t>(code[3]) << 24);
   }
 }
 
@@ -126,11 +158,14 @@ cudaError_t launch_quant_rows(const void* x, long long rows, int d, void* codes,
 }
 
 cudaError_t launch_quant_tokens(const void* x, const int32_t* offsets, int B, int H, int d,
-                                void* codes, void* scales, cudaStream_t s) {
+                                long long T, void* codes, void* scales, cudaStream_t s) {
   if (B == 0) return cudaSuccess;
-  quant_tokens_kernel<<<B, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), offsets, H, d,
-                                        static_cast<uint8_t*>(codes),
-                                        static_cast<uint8_t*>(scales));
+  // Scale rows as counted by the buffer size: B + T/32 + 1 covers g(B-1) + ceil(L/32).
+  const long long rows = static_cast<long long>(B) + T / 32 + 1;
+  if (rows > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  quant_tokens_kernel<<<static_cast<unsigned>(rows), 128, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(x), offsets, B, H * d, T, static_cast<uint8_t*>(codes),
+      static_cast<uint8_t*>(scales));
   return cudaGetLastError();
 }
 

@@ -93,15 +93,16 @@ bool make_thd_map(CUtensorMap* m, const void* base, int64_t T, int H, int d, int
   return r == CUDA_SUCCESS;
 }
 
-// 3-D TMA map over the fp32 dQ accumulator [T][H][d]: box = 64 channels x
-// 1 head x 64 rows, no swizzle (the target of the backward's tile reduce-add).
-bool make_dq_map(CUtensorMap* m, void* base, int64_t T, int H, int d) {
+// 3-D TMA map over the fp32 dQ accumulator [T][H][d]: box = `box_ch` channels
+// x 1 head x `box_rows` rows, no swizzle (the target of the backward's tile
+// reduce-add).
+bool make_dq_map(CUtensorMap* m, void* base, int64_t T, int H, int d, int box_ch, int box_rows) {
   if (T <= 0) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(T)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
                            static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(d) * 4};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBwdQRows)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_ch), 1, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -284,8 +285,12 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
   const void* kb = Tkv > 0 ? k : q;
   const void* vb = Tkv > 0 ? v : q;
   const int64_t Tkm = Tkv > 0 ? Tkv : Tq;
+  // The softmax kernel streams 128-query tiles and reduces dQ in [16 x d]
+  // boxes; the general kernel uses 64-query tiles and [64 x 64] boxes.
+  const bool sm = act == GDPA_ACT_SOFTMAX;
+  const int q_rows = sm ? kBwdSmQRows : kBwdQRows;
   CUtensorMap tq, tk, tv, tdo;
-  if (!make_thd_map(&tq, qb, Tqm, H, d, kBwdQRows) || !make_thd_map(&tdo, dob, Tqm, H, d, kBwdQRows) ||
+  if (!make_thd_map(&tq, qb, Tqm, H, d, q_rows) || !make_thd_map(&tdo, dob, Tqm, H, d, q_rows) ||
       !make_thd_map(&tk, kb, Tkm, H, d, kBwdKvRows) || !make_thd_map(&tv, vb, Tkm, H, d, kBwdKvRows))
     return GDPA_ERR_INVALID_ARG;
 
@@ -300,7 +305,8 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
   float* delta = reinterpret_cast<float*>(ws + off);
   // Without query rows there is nothing to reduce into; any valid map will do.
   CUtensorMap tdq;
-  if (!make_dq_map(&tdq, Tq > 0 ? static_cast<void*>(dq_acc) : ws, Tq > 0 ? Tq : 1, H, d))
+  if (!make_dq_map(&tdq, Tq > 0 ? static_cast<void*>(dq_acc) : ws, Tq > 0 ? Tq : 1, H, d,
+                   sm ? d : 64, sm ? kBwdSmDqRows : kBwdQRows))
     return GDPA_ERR_INVALID_ARG;
 
   if (launch_build_worklist(kv_offsets, q_offsets, B, H, Tkv, Tq, causal, 1, items, n_items,

@@ -723,7 +723,6 @@ cudaError_t launch_main_d(const BwdParams& p, int act, const CUtensorMap& tq, co
                           const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                           int grid, cudaStream_t s) {
   switch (act) {
-    case GDPA_ACT_SOFTMAX: return launch_main<D, GDPA_ACT_SOFTMAX>(p, tq, tk, tv, tdo, tdq, grid, s);
     case GDPA_ACT_SILU: return launch_main<D, GDPA_ACT_SILU>(p, tq, tk, tv, tdo, tdq, grid, s);
     case GDPA_ACT_GELU_TANH:
       return launch_main<D, GDPA_ACT_GELU_TANH>(p, tq, tk, tv, tdo, tdq, grid, s);
@@ -752,8 +751,11 @@ cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const
   ++*launches;
   // 2) main kernel (optionally bracketed by timing events)
   if (ev_begin != nullptr && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess) return e;
-  e = (p.d == 64) ? launch_main_d<64>(p, act, tq, tk, tv, tdo, tdq, grid, stream)
-                  : launch_main_d<128>(p, act, tq, tk, tv, tdo, tdq, grid, stream);
+  if (act == GDPA_ACT_SOFTMAX)
+    e = launch_bwd_softmax_main(p, tq, tk, tv, tdo, tdq, grid, stream);
+  else
+    e = (p.d == 64) ? launch_main_d<64>(p, act, tq, tk, tv, tdo, tdq, grid, stream)
+                    : launch_main_d<128>(p, act, tq, tk, tv, tdo, tdq, grid, stream);
   if (e != cudaSuccess) return e;
   if (ev_end != nullptr && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess) return e;
   ++*launches;

@@ -20,6 +20,8 @@ constexpr int kKvRows = 128;
 // it in 64-row tiles.
 constexpr int kBwdKvRows = 128;
 constexpr int kBwdQRows = 64;
+constexpr int kBwdSmQRows = 128;  // query tile of the softmax backward
+constexpr int kBwdSmDqRows = 16;  // query rows per dQ reduce box of the softmax backward
 
 constexpr int kCostBuckets = 2048;
 
@@ -79,6 +81,9 @@ cudaError_t launch_build_worklist(const int32_t* outer_off, const int32_t* inner
 cudaError_t launch_fwd(const FwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, int grid, cudaStream_t stream);
 int fwd_smem_bytes(int d);
+cudaError_t launch_bwd_softmax_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                    const CUtensorMap& tv, const CUtensorMap& tdo,
+                                    const CUtensorMap& tdq, int grid, cudaStream_t s);
 cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                        int grid,

@@ -68,6 +68,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One arrival per warp: the warp's lanes converge (ordering their earlier
+// shared-memory and TMEM writes before lane 0's arrive) and lane 0 arrives.
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false once `limit_ns` of wall time has passed (or an iteration cap, as a
 // second guard), or as soon as *abort becomes non-zero.
@@ -209,6 +216,13 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, ui
 }
 constexpr uint32_t kSwizzle128B = 2;
 
+// The descriptor of an operand `bytes` further into shared memory: the start
+// address field holds address >> 4 in 14 bits, and shared-memory addresses
+// stay below 256 KB, so adding to the whole word never carries out of it.
+__device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor for kind::f16 with fp32 accumulation.
 // a_bf16/b_bf16 pick bf16 (else fp16); a_mn/b_mn mark an operand whose M (or
 // N) index is the contiguous one in shared memory.
@@ -271,6 +285,32 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 }
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Fire-and-forget add of four consecutive fp32 values into global memory
+// (performed in L2; the address must be 16-byte aligned).
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+// Register reallocation between warpgroups (every warp of the warpgroup runs
+// it): the block's register pool stays what it was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Elementwise product of two packed bf16 pairs, rounded to nearest.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // ---------------------------------------------------------------- math

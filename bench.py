@@ -51,7 +51,7 @@ def load_peaks():
 def load_traffic():
     """DRAM bytes per launch from the committed ncu summary, keyed
     "<workload>/<act>/<fwd|bwd>".  An entry is dropped (reported as null) when
-    the kernel's source has changed since the counters were taken."""
+    its kernel's source has changed since the counters were taken."""
     import hashlib
 
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
@@ -61,15 +61,18 @@ def load_traffic():
     except (OSError, ValueError):
         return {}
     csrc = os.path.join(ROOT, "jagged_attention_recsys_02_gb300", "csrc")
-    ok = {}
-    for key, src in (("fwd", "fwd.cu"), ("bwd", "bwd.cu")):
+    out = {}
+    for key, e in d.items():
+        if "/" not in key or not isinstance(e, dict):
+            continue
         try:
-            with open(os.path.join(csrc, src), "rb") as f:
+            with open(os.path.join(csrc, e["source"]), "rb") as f:
                 h = hashlib.sha256(f.read()).hexdigest()[:16]
-        except OSError:
-            h = None
-        ok[key] = h is not None and d.get("sources", {}).get(src) == h
-    return {k: v for k, v in d.items() if "/" in k and ok.get(k.rsplit("/", 1)[1], False)}
+        except (OSError, KeyError):
+            continue
+        if h == e.get("sha256_16"):
+            out[key] = e["bytes"]
+    return out
 
 
 # ------------------------------------------------------------------ clocks

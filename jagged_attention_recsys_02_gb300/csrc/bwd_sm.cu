@@ -73,7 +73,7 @@ struct SmCfg {
   static constexpr int kQ = 2 * kKvTileBytes;                   // + s * kQTileBytes
   static constexpr int kO = kQ + kQStages * kQTileBytes;        // dO: one stage
   static constexpr int kDs = kO + kQTileBytes;                  // [query atom][key row][64 queries]
-  // per Q stage: lse*log2e [128], D [128], then the bias window (255 entries,
+  // per Q stage: -lse*log2e [128], -D [128], then the bias window (255 entries,
   // times log2e) in four copies shifted by 0..3 entries, kBiasCopy floats apart
   // (so that every key row finds its 64 entries 16-byte aligned in one copy,
   // and the four copies start in different banks)
@@ -251,8 +251,8 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           float l2 = 0.0f, dd = 0.0f;
           if (ql < in.Lq) {
             const long long gi = static_cast<long long>(in.head) * p.Tq + in.q0 + ql;
-            l2 = __ldg(p.lse + gi) * kLog2e;
-            dd = __ldg(p.delta + gi);
+            l2 = -__ldg(p.lse + gi) * kLog2e;  // stored negated: added, not subtracted
+            dd = -__ldg(p.delta + gi);
           }
           v[2 * k] = l2;
           v[2 * k + 1] = dd;
@@ -523,13 +523,21 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
                 const float4 b4 = *reinterpret_cast<const float4*>(bwin + c0 + 4 * q4);
                 bv[0] = b4.x; bv[1] = b4.y; bv[2] = b4.z; bv[3] = b4.w;
               }
-              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-              float pv[4];
+              // exponent pairs: S * scale*log2e + (bias - lse)*log2e, two lanes per instruction
+              float2 off[2] = {make_float2(l4.x, l4.y), make_float2(l4.z, l4.w)};  // -lse*log2e
+              if (kBias) {
+                off[0] = add_f32x2(make_float2(bv[0], bv[1]), off[0]);
+                off[1] = add_f32x2(make_float2(bv[2], bv[3]), off[1]);
+              }
+              const uint32_t* sq = &sr[q4 / 8][4 * (q4 % 8)];
+              const float2 x01 = fma_f32x2(make_float2(__uint_as_float(sq[0]), __uint_as_float(sq[1])),
+                                           make_float2(c_s, c_s), off[0]);
+              const float2 x23 = fma_f32x2(make_float2(__uint_as_float(sq[2]), __uint_as_float(sq[3])),
+                                           make_float2(c_s, c_s), off[1]);
+              float pv[4] = {ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y)};
+              if (kMask) {
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float sv = __uint_as_float(sr[q4 / 8][4 * (q4 % 8) + e]);
-                pv[e] = ex2_approx(kBias ? fmaf(sv, c_s, bv[e] - lv[e]) : fmaf(sv, c_s, -lv[e]));
-                if (kMask) {
+                for (int e = 0; e < 4; ++e) {
                   const int c = c0 + 4 * q4 + e;
                   if (c < c_lo || c >= c_hi) pv[e] = 0.0f;
                 }
@@ -571,11 +579,12 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           for (int q4 = 0; q4 < 8; ++q4) {
             const float4 d4 = st4[((kQRows + c0) >> 2) + q4];
             const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-            float dv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) dv[e] = __uint_as_float(dr[4 * q4 + e]) - dd[e];
-            dh[2 * q4] = mul_bf16x2(pp[16 * half + 2 * q4], pack_bf16x2(dv[0], dv[1]));
-            dh[2 * q4 + 1] = mul_bf16x2(pp[16 * half + 2 * q4 + 1], pack_bf16x2(dv[2], dv[3]));
+            const float2 v01 = add_f32x2(make_float2(__uint_as_float(dr[4 * q4]), __uint_as_float(dr[4 * q4 + 1])),
+                                         make_float2(dd[0], dd[1]));  // -D
+            const float2 v23 = add_f32x2(make_float2(__uint_as_float(dr[4 * q4 + 2]), __uint_as_float(dr[4 * q4 + 3])),
+                                         make_float2(dd[2], dd[3]));
+            dh[2 * q4] = mul_bf16x2(pp[16 * half + 2 * q4], pack_bf16x2(v01.x, v01.y));
+            dh[2 * q4 + 1] = mul_bf16x2(pp[16 * half + 2 * q4 + 1], pack_bf16x2(v23.x, v23.y));
           }
 #pragma unroll
           for (int v = 0; v < 4; ++v) {

@@ -54,9 +54,14 @@ struct FwdCfg {
   static constexpr int kQ0 = 0;
   static constexpr int kQ1 = kQHalfBytes;
   static constexpr int kKV = 2 * kQHalfBytes;                          // K[s] = kKV + s*2*tile
-  // per stage and half: bias window of 256 floats (255 relative positions)
+  // per stage and half: the bias window (255 relative positions, in reverse
+  // order, times log2e for softmax) in four copies shifted by 0..3 entries,
+  // kBiasCopy floats apart, so that every query row finds its 128 entries of a
+  // key tile 16-byte aligned in one copy and the copies start in different banks
+  static constexpr int kBiasCopy = 260;
+  static constexpr int kBiasBlock = 4 * kBiasCopy;                     // floats per stage and half
   static constexpr int kBias = kKV + kStages * 2 * kTileBytes;
-  static constexpr int kBar = kBias + kStages * 2 * 256 * 4;          // barriers after tiles
+  static constexpr int kBar = kBias + kStages * 2 * kBiasBlock * 4;   // barriers after tiles
   // barrier block layout (8 bytes each)
   static constexpr int kQFull = 0, kQEmpty = 1;
   static constexpr int kKFull = 2;                                     // + s
@@ -230,6 +235,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       // tile's first local column).  Each lane holds entries lane + 32k of both
       // halves, fetched one tile ahead so the load latency overlaps the wait for
       // a free stage.
+      constexpr float kBiasMul = kSoftmax ? kLog2e : 1.0f;  // exponents are in log2 units
       auto fetch = [&](int j, float (&v)[16]) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -239,7 +245,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
           for (int k = 0; k < 8; ++k) {
             const int e = lane + 32 * k;
             v[8 * h + k] = (brow != nullptr && e < 255)
-                               ? __ldg(brow + min(max(w0 + e, 0), rel_w - 1))
+                               ? __ldg(brow + min(max(w0 + e, 0), rel_w - 1)) * kBiasMul
                                : 0.0f;
           }
         }
@@ -269,10 +275,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         if (brow != nullptr) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            float* win = bias_win + (s * 2 + h) * 256;
+            float* win = bias_win + (s * 2 + h) * C::kBiasBlock;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              if (lane + 32 * k < 255) win[lane + 32 * k] = cur[8 * h + k];
+            for (int k = 0; k < 8; ++k) {
+              const int e = lane + 32 * k;
+              if (e < 255) {
+#pragma unroll
+                for (int cp = 0; cp < 4; ++cp)  // entry e at position (254 - e) + cp of copy cp
+                  win[cp * C::kBiasCopy + cp + 254 - e] = cur[8 * h + k];
+              }
+            }
           }
           if (j + 1 < n) fetch(j + 1, nxt);
         }
@@ -402,7 +414,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
     const uint32_t t_s = tmem + lane_off + half * 256;
     const uint32_t t_o = t_s + 128;
     const float c_s = kSoftmax ? p.scale * kLog2e : p.scale;   // score multiplier
-    const float c_b = kSoftmax ? kLog2e : 1.0f;                 // bias multiplier
     const float* bias_win = reinterpret_cast<const float*>(gbase + C::kBias);
     uint32_t it = 0, tcount = 0, ocount = 0, g = 0;
     while (true) {
@@ -442,17 +453,29 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         // is no bias.  Decided per warp: the tcgen05.ld below is .sync.aligned, so
         // the lanes of a warp must not split between the two paths.
         const bool plain = !has_bias && __all_sync(0xffffffffu, !need_mask);
-        // bwin[-cc] = bias(row, tile column cc) for this thread's row
-        const float* bwin = bias_win + ((gj % C::kStages) * 2 + half) * 256 + row_in_half + 127;
-        // x = score * c_s + bias * c_b - sub, with masked entries set to `fill`
-        auto load_x = [&](int chunk, float sub, float fill, float (&x)[32]) {
+        // bwin[cc] = bias(row, tile column cc) (times log2e for softmax): the
+        // window copy shifted by (row + 1) % 4 holds this row's 128 entries in
+        // increasing column order from a 16-byte aligned position.
+        const int cp = (row_in_half + 1) & 3;
+        const float* bwin = bias_win + ((gj % C::kStages) * 2 + half) * C::kBiasBlock +
+                            cp * C::kBiasCopy + cp + (kKvRows - 1) - row_in_half;
+        // x = score * c_s + bias, with masked entries set to `fill` (pairs of
+        // columns per packed fp32 instruction)
+        auto load_x = [&](int chunk, float fill, float (&x)[32]) {
           uint32_t sr[32];
           tmem_ld32(t_s + chunk * 32, sr);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) x[i] = fmaf(__uint_as_float(sr[i]), c_s, -sub);
-          if (has_bias) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = fmaf(bwin[-(chunk * 32 + i)], c_b, x[i]);
+          for (int q4 = 0; q4 < 8; ++q4) {
+            float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (has_bias) b4 = *reinterpret_cast<const float4*>(bwin + chunk * 32 + 4 * q4);
+            const float2 x01 = fma_f32x2(make_float2(__uint_as_float(sr[4 * q4]), __uint_as_float(sr[4 * q4 + 1])),
+                                         make_float2(c_s, c_s), make_float2(b4.x, b4.y));
+            const float2 x23 = fma_f32x2(make_float2(__uint_as_float(sr[4 * q4 + 2]), __uint_as_float(sr[4 * q4 + 3])),
+                                         make_float2(c_s, c_s), make_float2(b4.z, b4.w));
+            x[4 * q4] = x01.x;
+            x[4 * q4 + 1] = x01.y;
+            x[4 * q4 + 2] = x23.x;
+            x[4 * q4 + 3] = x23.y;
           }
           if (need_mask) {
 #pragma unroll
@@ -483,7 +506,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
 #pragma unroll
             for (int chunk = 0; chunk < 4; ++chunk) {
               float x[32];
-              load_x(chunk, 0.0f, -INFINITY, x);
+              load_x(chunk, -INFINITY, x);
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 xs[chunk * 32 + i] = x[i];
@@ -516,26 +539,26 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
           const float m_ref = (m == -INFINITY) ? 0.0f : m;
           // exponent = xs * xm - m_ref (plain: raw scores times the scale)
           const float xm = plain ? c_s : 1.0f;
-          float l2[2] = {0.0f, 0.0f};
+          float2 l2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
           for (int chunk = 0; chunk < 4; ++chunk) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float p0 = ex2_approx(fmaf(xs[chunk * 32 + 2 * i], xm, -m_ref));
-              const float p1 = ex2_approx(fmaf(xs[chunk * 32 + 2 * i + 1], xm, -m_ref));
-              l2[0] += p0;
-              l2[1] += p1;
-              pk[i] = pack_bf16x2(p0, p1);
+              const float2 e = fma_f32x2(make_float2(xs[chunk * 32 + 2 * i], xs[chunk * 32 + 2 * i + 1]),
+                                         make_float2(xm, xm), make_float2(-m_ref, -m_ref));
+              const float2 pv = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+              l2[i & 1] = add_f32x2(l2[i & 1], pv);
+              pk[i] = pack_bf16x2(pv.x, pv.y);
             }
             tmem_st16(t_s + chunk * 32, pk);
           }
-          l += l2[0] + l2[1];
+          l += (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
         } else {
 #pragma unroll 1
           for (int chunk = 0; chunk < 4; ++chunk) {
             float x[32];
-            load_x(chunk, 0.0f, 0.0f, x);
+            load_x(chunk, 0.0f, x);
             uint32_t hi[16], lo[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {

@@ -74,11 +74,11 @@ struct SmCfg {
   static constexpr int kO = kQ + kQStages * kQTileBytes;        // dO: one stage
   static constexpr int kDs = kO + kQTileBytes;                  // [query atom][key row][64 queries]
   // per Q stage: -lse*log2e [128], -D [128], then the bias window (255 entries,
-  // times log2e) in four copies shifted by 0..3 entries, kBiasCopy floats apart
-  // (so that every key row finds its 64 entries 16-byte aligned in one copy,
-  // and the four copies start in different banks)
-  static constexpr int kBiasCopy = 260;
-  static constexpr int kStatFloats = 2 * kQRows + 4 * kBiasCopy;
+  // times log2e) in two copies shifted by 0 and 1 entries, kBiasCopy floats
+  // apart (every key row finds its 64 entries 8-byte aligned in one copy, and
+  // with this stride the 64-bit loads of a warp hit every bank once)
+  static constexpr int kBiasCopy = 270;
+  static constexpr int kStatFloats = 2 * kQRows + 2 * kBiasCopy + 4;  // (16-byte multiple)
   static constexpr int kStats = kDs + kDsBytes;
   static constexpr int kDqStageBytes = kDqChunk * D * 4;       // [16 queries][d] fp32
   static constexpr int kDqStage = kStats + kQStages * kStatFloats * 4;  // two buffers
@@ -287,7 +287,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           for (int k = 0; k < 8; ++k)
             if (lane + 32 * k < kWin) {
 #pragma unroll
-              for (int cp = 0; cp < 4; ++cp)  // copy cp holds entry e at position e + cp
+              for (int cp = 0; cp < 2; ++cp)  // copy cp holds entry e at position e + cp
                 st[2 * kQRows + cp * C::kBiasCopy + cp + lane + 32 * k] = cur[8 + k];
             }
         }
@@ -489,9 +489,9 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         const float* st = stats + s * C::kStatFloats;
         const float4* st4 = reinterpret_cast<const float4*>(st);  // 16-byte aligned
         // bias(query c, key j) * log2e is window entry c - j + 127; the copy
-        // shifted by (j + 1) % 4 holds entries c0 - j + 127 .. (c0 a multiple
-        // of 32) at a 16-byte aligned position.
-        const int cp = (j + 1) & 3;
+        // shifted by (j + 1) % 2 holds entries c0 - j + 127 .. (c0 even) at an
+        // 8-byte aligned position.
+        const int cp = (j + 1) & 1;
         const float* bwin = st + 2 * kQRows + cp * C::kBiasCopy + cp + (kKRows - 1) - j;
         const int qloc = (in.qt0 + t) * kQRows;
         // Tiles strictly inside the sample (and below the causal diagonal) need no mask.
@@ -520,8 +520,9 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
               const float4 l4 = st4[(c0 >> 2) + q4];
               float bv[4] = {0.f, 0.f, 0.f, 0.f};
               if (kBias) {
-                const float4 b4 = *reinterpret_cast<const float4*>(bwin + c0 + 4 * q4);
-                bv[0] = b4.x; bv[1] = b4.y; bv[2] = b4.z; bv[3] = b4.w;
+                const float2 b01 = *reinterpret_cast<const float2*>(bwin + c0 + 4 * q4);
+                const float2 b23 = *reinterpret_cast<const float2*>(bwin + c0 + 4 * q4 + 2);
+                bv[0] = b01.x; bv[1] = b01.y; bv[2] = b23.x; bv[3] = b23.y;
               }
               // exponent pairs: S * scale*log2e + (bias - lse)*log2e, two lanes per instruction
               float2 off[2] = {make_float2(l4.x, l4.y), make_float2(l4.z, l4.w)};  // -lse*log2e

@@ -55,11 +55,12 @@ struct FwdCfg {
   static constexpr int kQ1 = kQHalfBytes;
   static constexpr int kKV = 2 * kQHalfBytes;                          // K[s] = kKV + s*2*tile
   // per stage and half: the bias window (255 relative positions, in reverse
-  // order, times log2e for softmax) in four copies shifted by 0..3 entries,
-  // kBiasCopy floats apart, so that every query row finds its 128 entries of a
-  // key tile 16-byte aligned in one copy and the copies start in different banks
-  static constexpr int kBiasCopy = 260;
-  static constexpr int kBiasBlock = 4 * kBiasCopy;                     // floats per stage and half
+  // order, times log2e for softmax) in two copies shifted by 0 and 1 entries,
+  // kBiasCopy floats apart: every query row finds its 128 entries of a key
+  // tile 8-byte aligned in one copy, and with this stride the 64-bit loads of
+  // a warp hit every bank once
+  static constexpr int kBiasCopy = 270;
+  static constexpr int kBiasBlock = 2 * kBiasCopy;                     // floats per stage and half
   static constexpr int kBias = kKV + kStages * 2 * kTileBytes;
   static constexpr int kBar = kBias + kStages * 2 * kBiasBlock * 4;   // barriers after tiles
   // barrier block layout (8 bytes each)
@@ -281,7 +282,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
               const int e = lane + 32 * k;
               if (e < 255) {
 #pragma unroll
-                for (int cp = 0; cp < 4; ++cp)  // entry e at position (254 - e) + cp of copy cp
+                for (int cp = 0; cp < 2; ++cp)  // entry e at position (254 - e) + cp of copy cp
                   win[cp * C::kBiasCopy + cp + 254 - e] = cur[8 * h + k];
               }
             }
@@ -454,20 +455,24 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         // the lanes of a warp must not split between the two paths.
         const bool plain = !has_bias && __all_sync(0xffffffffu, !need_mask);
         // bwin[cc] = bias(row, tile column cc) (times log2e for softmax): the
-        // window copy shifted by (row + 1) % 4 holds this row's 128 entries in
-        // increasing column order from a 16-byte aligned position.
-        const int cp = (row_in_half + 1) & 3;
+        // window copy shifted by (row + 1) % 2 holds this row's 128 entries in
+        // increasing column order from an 8-byte aligned position.
+        const int cp = (row_in_half + 1) & 1;
         const float* bwin = bias_win + ((gj % C::kStages) * 2 + half) * C::kBiasBlock +
                             cp * C::kBiasCopy + cp + (kKvRows - 1) - row_in_half;
         // x = score * c_s + bias, with masked entries set to `fill` (pairs of
         // columns per packed fp32 instruction)
         auto load_x = [&](int chunk, float fill, float (&x)[32]) {
           uint32_t sr[32];
-          tmem_ld32(t_s + chunk * 32, sr);
+          tmem_ld32_nc(t_s + chunk * 32, sr);  // lets the bias loads overlap the TMEM load
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (has_bias) b4 = *reinterpret_cast<const float4*>(bwin + chunk * 32 + 4 * q4);
+            if (has_bias) {
+              const float2 b01 = *reinterpret_cast<const float2*>(bwin + chunk * 32 + 4 * q4);
+              const float2 b23 = *reinterpret_cast<const float2*>(bwin + chunk * 32 + 4 * q4 + 2);
+              b4 = make_float4(b01.x, b01.y, b23.x, b23.y);
+            }
             const float2 x01 = fma_f32x2(make_float2(__uint_as_float(sr[4 * q4]), __uint_as_float(sr[4 * q4 + 1])),
                                          make_float2(c_s, c_s), make_float2(b4.x, b4.y));
             const float2 x23 = fma_f32x2(make_float2(__uint_as_float(sr[4 * q4 + 2]), __uint_as_float(sr[4 * q4 + 3])),

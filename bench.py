@@ -453,48 +453,86 @@ def run_gpu(args, rank, world, local_rank):
     traffic = load_traffic().get(f"{w.name}/{w.act}/{dominant}")
 
     # ---------------- end to end through host buffers
+    # Every step copies its inputs from pinned host memory, runs forward and
+    # backward, and copies its outputs back.  Steps are pipelined over two
+    # buffer slots on three streams (host->device, compute, device->host), so
+    # the copies of one step overlap the compute of its neighbours.
     e2e = None
     if not args.no_e2e:
-        pin = {k_: t[k_].cpu().pin_memory() for k_ in ("q", "k", "v", "dout", "qo", "ko")}
+        names_in = ("q", "k", "v", "dout", "qo", "ko")
+        pin = {k_: t[k_].cpu().pin_memory() for k_ in names_in}
         hbias = t["bias"].cpu().pin_memory() if t["bias"] is not None else None
-        host_out = {k_: torch.empty(tuple(x.shape), dtype=x.dtype, pin_memory=True)
-                    for k_, x in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
-        dev_in = {k_: torch.empty_like(t[k_]) for k_ in pin}
-        dbias = torch.empty_like(t["bias"]) if hbias is not None else None
+        outs = [dict(out=torch.empty_like(out), lse=torch.empty_like(lse), dq=torch.empty_like(dq),
+                     dk=torch.empty_like(dk), dv=torch.empty_like(dv)) for _ in range(2)]
+        host_out = [{k_: torch.empty(tuple(x.shape), dtype=x.dtype, pin_memory=True)
+                     for k_, x in o.items()} for o in outs]
+        dev_in = [{k_: torch.empty_like(t[k_]) for k_ in names_in} for _ in range(2)]
+        dbias = [torch.empty_like(t["bias"]) if hbias is not None else None for _ in range(2)]
         h2d = sum(x.numel() * x.element_size() for x in pin.values())
         h2d += hbias.numel() * hbias.element_size() if hbias is not None else 0
-        d2h = sum(x.numel() * x.element_size() for x in host_out.values())
+        d2h = sum(x.numel() * x.element_size() for x in host_out[0].values())
+        s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_cmp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        for sl in range(2):  # nothing pending on either slot yet
+            for ev in (ev_cmp[sl], ev_out[sl]):
+                ev.record(torch.cuda.current_stream(dev))
 
-        def e2e_step():
-            for k_, x in pin.items():
-                dev_in[k_].copy_(x, non_blocking=True)
-            if hbias is not None:
-                dbias.copy_(hbias, non_blocking=True)
-            binding.gdpa_fwd(dev_in["q"], dev_in["qo"], dev_in["k"], dev_in["v"], dev_in["ko"],
-                             act=a, causal=w.causal, scale=w.scale, bias=dbias,
-                             max_rel=w.max_rel, out=out, lse=lse, workspace=ws_f)
-            binding.gdpa_bwd(dev_in["q"], dev_in["qo"], dev_in["k"], dev_in["v"], dev_in["ko"],
-                             out, lse, dev_in["dout"], act=a, causal=w.causal, scale=w.scale,
-                             bias=dbias, max_rel=w.max_rel, dq=dq, dk=dk, dv=dv, workspace=ws_b)
-            for k_, x in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
-                host_out[k_].copy_(x, non_blocking=True)
+        def e2e_step(k_step):
+            sl = k_step % 2
+            di, o, ho = dev_in[sl], outs[sl], host_out[sl]
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_cmp[sl])  # the compute two steps back read this slot
+                for k_, x in pin.items():
+                    di[k_].copy_(x, non_blocking=True)
+                if hbias is not None:
+                    dbias[sl].copy_(hbias, non_blocking=True)
+                ev_in[sl].record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(ev_in[sl])
+                s_cmp.wait_event(ev_out[sl])  # outputs of two steps back have been read
+                binding.gdpa_fwd(di["q"], di["qo"], di["k"], di["v"], di["ko"], act=a,
+                                 causal=w.causal, scale=w.scale, bias=dbias[sl], max_rel=w.max_rel,
+                                 out=o["out"], lse=o["lse"], workspace=ws_f, stream=s_cmp)
+                binding.gdpa_bwd(di["q"], di["qo"], di["k"], di["v"], di["ko"], o["out"], o["lse"],
+                                 di["dout"], act=a, causal=w.causal, scale=w.scale,
+                                 bias=dbias[sl], max_rel=w.max_rel, dq=o["dq"], dk=o["dk"],
+                                 dv=o["dv"], workspace=ws_b, stream=s_cmp)
+                ev_cmp[sl].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_cmp[sl])
+                for k_, x in o.items():
+                    ho[k_].copy_(x, non_blocking=True)
+                ev_out[sl].record(s_out)
 
-        for _ in range(2):
-            e2e_step()
+        for k_step in range(2):
+            e2e_step(k_step)
         torch.cuda.synchronize()
-        n_e2e = max(3, args.steps // 2)
+        n_e2e = max(4, args.steps // 2)
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
-        e0.record()
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record()
+        main = torch.cuda.current_stream(dev)
+        e0.record(main)
+        for st_ in (s_in, s_cmp, s_out):
+            st_.wait_event(e0)
+        for k_step in range(n_e2e):
+            e2e_step(k_step)
+        for st_ in (s_in, s_cmp, s_out):
+            done = torch.cuda.Event()
+            done.record(st_)
+            main.wait_event(done)
+        e1.record(main)
         torch.cuda.synchronize()
+        st = binding.device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} after the end-to-end steps")
         ms_e, _ = reduce_over_ranks(e0.elapsed_time(e1), 0.0, dev)
         e2e = {"value": tot_flops / args.steps * n_e2e / (ms_e * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": ms_e / n_e2e}
+               "ms_per_step": ms_e / n_e2e, "steps": n_e2e,
+               "pipeline": "2 buffer slots; host->device, compute and device->host streams"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

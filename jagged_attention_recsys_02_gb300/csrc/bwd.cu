@@ -665,30 +665,45 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
 }
 
 // Zero the fp32 dQ accumulator and (softmax) compute D = rowsum(dO * O).
-// One warp per (row, head); lanes cover the d channels.
+// A row of d bf16 values is d/8 16-byte vectors: each lane takes one vector of
+// O and of dO, and 16 (d = 128) or 8 (d = 64) lanes share a row, so a warp
+// covers 2 or 4 rows per step with full-width loads and stores.
 template <int D>
 __global__ void __launch_bounds__(256)
 bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
                       float* __restrict__ delta, float* __restrict__ dq_acc, long long Tq, int H,
                       int softmax) {
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const long long nrows = Tq * H;
   const int lane = threadIdx.x & 31;
+  const int sub = lane / kLanesPerRow;   // row of the warp's group
+  const int v = lane % kLanesPerRow;     // 16-byte vector within the row
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
-  for (long long row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; row < nrows; row += warps) {
-    float4* acc = reinterpret_cast<float4*>(dq_acc + row * D);
-    for (int v = lane; v < D / 4; v += 32) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long row0 = (blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * kRowsPerWarp;
+       row0 < nrows; row0 += warps * kRowsPerWarp) {
+    const long long row = row0 + sub;
+    const bool ok = row < nrows;
+    if (ok) {
+      float4* acc = reinterpret_cast<float4*>(dq_acc + row * D) + 2 * v;
+      acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (softmax) {
       float s = 0.f;
-      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(out + row * D);
-      const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(dout + row * D);
-      for (int c = lane; c < D / 2; c += 32) {
-        const float2 a = __bfloat1622float2(o2[c]);
-        const float2 b = __bfloat1622float2(d2[c]);
-        s = fmaf(a.x, b.x, fmaf(a.y, b.y, s));
+      if (ok) {
+        const uint4 a = reinterpret_cast<const uint4*>(out + row * D)[v];
+        const uint4 b = reinterpret_cast<const uint4*>(dout + row * D)[v];
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          s = fmaf(__uint_as_float(aw[k] << 16), __uint_as_float(bw[k] << 16), s);
+          s = fmaf(__uint_as_float(aw[k] & 0xFFFF0000u), __uint_as_float(bw[k] & 0xFFFF0000u), s);
+        }
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      if (lane == 0) {
+      for (int off = kLanesPerRow / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (ok && v == 0) {
         const long long t = row / H, h = row % H;
         delta[h * Tq + t] = s;
       }
@@ -696,13 +711,16 @@ bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16
   }
 }
 
-// dq = bf16(dq_acc * scale)
+// dq = bf16(dq_acc * scale), eight values (two 16-byte loads, one 16-byte
+// store) per thread and step.
 __global__ void __launch_bounds__(256)
-dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, long long n4, float scale) {
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long long n8, float scale) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float4 a = acc[i];
-    dq[i] = make_uint2(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale));
+    const float4 a = acc[2 * i];
+    const float4 b = acc[2 * i + 1];
+    dq[i] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                       pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
   }
 }
 
@@ -764,10 +782,10 @@ cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const
 
 cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale,
                               cudaStream_t stream) {
-  const long long n4 = n / 4;
-  const int blocks = static_cast<int>(n4 / 256 + 1 < 8192 ? n4 / 256 + 1 : 8192);
+  const long long n8 = n / 8;  // n = Tq * H * d with d in {64, 128}
+  const int blocks = static_cast<int>(n8 / 256 + 1 < 8192 ? n8 / 256 + 1 : 8192);
   dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(acc),
-                                                reinterpret_cast<uint2*>(dq), n4, scale);
+                                                reinterpret_cast<uint4*>(dq), n8, scale);
   return cudaGetLastError();
 }
 

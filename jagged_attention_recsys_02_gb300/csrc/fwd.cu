@@ -320,29 +320,34 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       uint32_t it = 0, g = 0, qi = 0;
       uint32_t tcount[2] = {0, 0};
       bool issued_any = false;
+      // Descriptors at each operand's first byte; stages, halves and k-steps
+      // are added to the start-address field (see dadd), keeping the issue
+      // loop short: this warp shares its sub-partition with busy warps.
+      const uint64_t dsc_q = sdesc(sbase + C::kQ0, 0, 1024, kSwizzle128B);   // A of S (K-major)
+      const uint64_t dsc_k = sdesc(sbase + C::kKV, 0, 1024, kSwizzle128B);   // B of S (K-major)
+      const uint64_t dsc_v = sdesc(sbase + C::kKV + C::kTileBytes, kKvRows * 128, 1024,
+                                   kSwizzle128B);                             // B of PV (MN-major)
       auto issue_s = [&](int half, uint32_t stage) {
-        const uint32_t qa = sbase + (half ? C::kQ1 : C::kQ0);
-        const uint32_t ka = sbase + C::kKV + stage * 2 * C::kTileBytes;
+        const uint64_t qb = dadd(dsc_q, half ? C::kQ1 - C::kQ0 : 0);
+        const uint64_t kb = dadd(dsc_k, stage * 2 * C::kTileBytes);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks / 4) * (kHalfRows * 128) + (ks % 4) * 32;
-          const uint64_t ad = sdesc(qa + off, 0, 1024, kSwizzle128B);
-          const uint64_t bd = sdesc(ka + off, 0, 1024, kSwizzle128B);
-          mma_f16_ss(tmem + half * 256, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
+          const uint32_t qoff = (ks / 4) * (kHalfRows * 128) + (ks % 4) * 32;
+          const uint32_t koff = (ks / 4) * (kKvRows * 128) + (ks % 4) * 32;
+          mma_f16_ss(tmem + half * 256, dadd(qb, qoff), dadd(kb, koff), idesc_s, ks > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kSFull + half));
         issued_any = true;
       };
       auto issue_pv = [&](int half, uint32_t stage, bool first) {
-        const uint32_t va = sbase + C::kKV + stage * 2 * C::kTileBytes + C::kTileBytes;
+        const uint64_t vb = dadd(dsc_v, stage * 2 * C::kTileBytes);
         const uint32_t tp = tmem + half * 256;
         const uint32_t to = tmem + half * 256 + 128;
 #pragma unroll
         for (int ks = 0; ks < kKvRows / 16; ++ks) {
-          const uint64_t bd = sdesc(va + ks * 2048, kKvRows * 128, 1024, kSwizzle128B);
           const uint32_t pcol = 32 * (ks / 2) + 8 * (ks % 2);
-          mma_f16_ts(to, tp + pcol, bd, idesc_pv, (first && ks == 0) ? 0u : 1u);
-          if (kSplit) mma_f16_ts(to, tp + pcol + 16, bd, idesc_pv, 1u);
+          mma_f16_ts(to, tp + pcol, dadd(vb, ks * 2048), idesc_pv, (first && ks == 0) ? 0u : 1u);
+          if (kSplit) mma_f16_ts(to, tp + pcol + 16, dadd(vb, ks * 2048), idesc_pv, 1u);
         }
         issued_any = true;
       };

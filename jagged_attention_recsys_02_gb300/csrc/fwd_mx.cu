@@ -59,8 +59,15 @@ struct Cfg {
   static constexpr int kTileBytes = kTile * kD;        // 12 KB
   static constexpr int kQ0 = 0, kQ1 = kQHalfBytes;
   static constexpr int kKV = 2 * kQHalfBytes;          // K[s] = kKV + s*2*tile, V = K + tile
-  static constexpr int kBias = kKV + kStages * 2 * kTileBytes;  // [stage][half][256] floats
-  static constexpr int kSfp = kBias + kStages * 2 * 256 * 4;    // [half][buf][128] u32 P-scale words
+  // per stage and half: the bias window (kTile + 127 relative positions, in
+  // reverse order, times log2e) in two copies shifted by 0 and 1 entries,
+  // kBiasCopy floats apart: every query row finds its entries of a key tile
+  // 8-byte aligned in one copy, and with this stride the 64-bit loads of a
+  // warp hit every bank once
+  static constexpr int kBiasCopy = 270;
+  static constexpr int kBiasBlock = 2 * kBiasCopy;
+  static constexpr int kBias = kKV + kStages * 2 * kTileBytes;
+  static constexpr int kSfp = kBias + kStages * 2 * kBiasBlock * 4;  // [half][buf][128] u32 P-scale words
   static constexpr int kBar = kSfp + 2 * 2 * kHalfRows * 4;
   static constexpr int kQFull = 0, kQEmpty = 1;
   static constexpr int kKFull = 2;                      // + s
@@ -201,7 +208,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       mbar_init(bar(C::kItemEmpty + h), 1 + 3 * 128);
     }
     mbar_init(bar(C::kDrain), 1);
-    for (int i = 0; i < 4; ++i) mbar_init(bar(C::kSfpBar + i), kHalfRows);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(C::kSfpBar + i), 4);  // one arrival per warp
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -284,9 +291,12 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           for (int h = 0; h < 2; ++h) {
             const int w0 = in.blk * kItemRows + h * kHalfRows - j * kTile - (kTile - 1) +
                            p.max_rel - 1;
-            float* win = bias_win + (s * 2 + h) * 256;
-            for (int e = lane; e < kWin; e += 32)
-              win[e] = __ldg(brow + min(max(w0 + e, 0), rel_w - 1));
+            float* win = bias_win + (s * 2 + h) * C::kBiasBlock;
+            for (int e = lane; e < kWin; e += 32) {
+              const float b = __ldg(brow + min(max(w0 + e, 0), rel_w - 1)) * kLog2e;
+              win[(kWin - 1) - e] = b;                  // copy 0: entry e at kWin - 1 - e
+              win[C::kBiasCopy + kWin - e] = b;         // copy 1: one position later
+            }
           }
         }
         __syncwarp();
@@ -385,24 +395,26 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       uint32_t it = 0, g = 0, qi = 0;
       uint32_t tcount[2] = {0, 0};
       bool issued_any = false;
+      // descriptors at each operand's first byte; offsets go into the
+      // start-address field (see dadd)
+      const uint64_t dsc_q = sdesc(sbase + C::kQ0, 0, 1024, kSwizzle128B);
+      const uint64_t dsc_kv = sdesc(sbase + C::kKV, 0, 1024, kSwizzle128B);
       auto issue_s = [&](int half, uint32_t stage) {
-        const uint32_t qa = sbase + (half ? C::kQ1 : C::kQ0);
-        const uint32_t ka = sbase + C::kKV + stage * 2 * C::kTileBytes;
+        const uint64_t qb = dadd(dsc_q, half ? C::kQ1 - C::kQ0 : 0);
+        const uint64_t kb = dadd(dsc_kv, stage * 2 * C::kTileBytes);
 #pragma unroll
         for (int ks = 0; ks < kD / 32; ++ks) {
-          const uint64_t ad = sdesc(qa + ks * 32, 0, 1024, kSwizzle128B);
-          const uint64_t bd = sdesc(ka + ks * 32, 0, 1024, kSwizzle128B);
-          mma_mx_ss(tmem + col_s(half), ad, bd, idesc_mx(kTile, false, ks), tmem + col_sfq(half),
-                    tmem + col_sfk(stage), ks > 0 ? 1u : 0u);
+          mma_mx_ss(tmem + col_s(half), dadd(qb, ks * 32), dadd(kb, ks * 32), idesc_mx(kTile, false, ks),
+                    tmem + col_sfq(half), tmem + col_sfk(stage), ks > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kSFull + half));
         issued_any = true;
       };
       auto issue_pv = [&](int half, uint32_t stage, bool first) {
-        const uint32_t va = sbase + C::kKV + stage * 2 * C::kTileBytes + C::kTileBytes;
+        const uint64_t vb = dadd(dsc_kv, stage * 2 * C::kTileBytes + C::kTileBytes);
 #pragma unroll
         for (int ks = 0; ks < kTile / 32; ++ks) {
-          const uint64_t bd = sdesc(va + ks * 4096, 0, 1024, kSwizzle128B);
+          const uint64_t bd = dadd(vb, ks * 4096);
           mma_mx_ts(tmem + col_o(half), tmem + col_s(half) + 8 * ks, bd, idesc_mx(kD, true, ks),
                     tmem + col_sfp(half), tmem + col_sfv(stage), (first && ks == 0) ? 0u : 1u);
         }
@@ -512,16 +524,26 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         const int c0 = j * kTile;
         const bool need_mask = (c0 + kTile > in.Lkv) || (p.causal && c0 + kTile - 1 > r);
         const int col_lim = p.causal ? min(in.Lkv, r + 1) : in.Lkv;
-        const float* bwin =
-            bias_win + ((gj % kStages) * 2 + half) * 256 + row_in_half + (kTile - 1);
+        // bwin[cc] = bias(row, tile column cc) * log2e, from the window copy in
+        // which this row's entries start 8-byte aligned
+        const int cp = (row_in_half + 1) & 1;
+        const float* bwin = bias_win + ((gj % kStages) * 2 + half) * C::kBiasBlock +
+                            cp * C::kBiasCopy + cp + 127 - row_in_half;
+        // x = score * c_s + bias - sub, two columns per packed instruction
         auto load_x = [&](int chunk, float sub, float (&x)[32]) {
           uint32_t sr[32];
-          tmem_ld32(t_s + chunk * 32, sr);
+          tmem_ld32_nc(t_s + chunk * 32, sr);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) x[q] = fmaf(__uint_as_float(sr[q]), c_s, -sub);
-          if (has_bias) {
-#pragma unroll
-            for (int q = 0; q < 32; ++q) x[q] = fmaf(bwin[-(chunk * 32 + q)], kLog2e, x[q]);
+          for (int q2 = 0; q2 < 16; ++q2) {
+            float2 b = make_float2(-sub, -sub);
+            if (has_bias) {
+              const float2 bb = *reinterpret_cast<const float2*>(bwin + chunk * 32 + 2 * q2);
+              b = make_float2(bb.x - sub, bb.y - sub);
+            }
+            const float2 v = fma_f32x2(make_float2(__uint_as_float(sr[2 * q2]), __uint_as_float(sr[2 * q2 + 1])),
+                                       make_float2(c_s, c_s), b);
+            x[2 * q2] = v.x;
+            x[2 * q2 + 1] = v.y;
           }
           if (need_mask) {
 #pragma unroll
@@ -565,12 +587,15 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           float x[32];
           load_x(chunk, m_ref, x);
           float amax = 0.0f;
+          float2 l2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
+          for (int q = 0; q < 32; q += 2) {
             x[q] = ex2_approx(x[q]);
-            l += x[q];
-            amax = fmaxf(amax, x[q]);
+            x[q + 1] = ex2_approx(x[q + 1]);
+            l2 = add_f32x2(l2, make_float2(x[q], x[q + 1]));
+            amax = fmaxf(amax, fmaxf(x[q], x[q + 1]));
           }
+          l += l2.x + l2.y;
           const int code = e8m0_nosat(amax);
           const float inv = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
           uint32_t pk[8];
@@ -588,7 +613,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         const uint32_t pbuf = ptile & 1u;
         uint32_t* words = sfp_base + pbuf * kHalfRows;
         words[row_in_half] = sfw;
-        mbar_arrive(bar(C::kSfpBar + half * 2 + pbuf));
+        warp_arrive(bar(C::kSfpBar + half * 2 + pbuf), lane);
         okw = mbar_wait(bar(C::kSfpBar + half * 2 + pbuf), (ptile >> 1) & 1u, abort_flag);
         okw = __all_sync(0xffffffffu, okw);
         ++ptile;

@@ -659,7 +659,7 @@ def run_gpu_mxfp8(args, rank, world, local_rank):
                        step="MXFP8 quantise Q,K,V + forward"),
         "roofline": {"bound": "tensor", "kernel": "MXFP8 forward kernel", "achieved": achieved,
                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
-                     "traffic": None,
+                     "traffic": load_traffic().get(f"{w.name}/mxfp8/fwd"),
                      "peak_source": f"2 x bf16_tflops of {src} (nominal FP8:BF16 = 2)"},
         "gpu_launches": launches, "clocks": clk,
     }

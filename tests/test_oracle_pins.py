@@ -418,3 +418,158 @@ def test_quant_cols_sample_aligned_blocks(oracle_mod):
     dec = np.vectorize(oracle_mod.e4m3_decode)(codes)
     # every element is +-2^b = +-2^8 * 2^(b-8): code 256 -> 0x78 with sign
     np.testing.assert_array_equal(np.abs(dec), 256.0)
+
+
+# --------------------------------------------------------------- sliding window
+def _band(L, window, causal):
+    i = np.arange(L)[:, None]
+    j = np.arange(L)[None, :]
+    keep = np.abs(i - j) < window
+    if causal:
+        keep &= j <= i
+    return keep
+
+
+@pytest.mark.parametrize("with_bias", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("window", [1, 3, 8])
+def test_window_softmax_matches_torch_sdpa(oracle_mod, window, causal, with_bias):
+    """The windowed softmax rows equal torch's fp64 SDPA under a band mask."""
+    H, d, max_rel = 2, 16, 6
+    lq = [5, 0, 17, 1, 12]
+    q = _bf16_randn((sum(lq), H, d), 41)
+    k = _bf16_randn((sum(lq), H, d), 42)
+    v = _bf16_randn((sum(lq), H, d), 43)
+    table = np.random.default_rng(44).normal(0, 0.5, size=(H, 2 * max_rel - 1)) if with_bias else None
+    qo = _offsets(lq)
+    scale = 1 / math.sqrt(d)
+    out, lse = oracle_mod.fwd(q, qo, k, v, qo, act=ACT_SOFTMAX, causal=causal, scale=scale,
+                              bias=table, max_rel=max_rel, window=window)
+    for b, L in enumerate(lq):
+        if L == 0:
+            continue
+        sl = slice(qo[b], qo[b + 1])
+        qb, kb, vb = (torch.from_numpy(x[sl]).permute(1, 0, 2)[None] for x in (q, k, v))
+        mask = np.where(_band(L, window, causal), 0.0, -np.inf)[None].repeat(H, 0)
+        if with_bias:
+            mask = mask + np.stack([_relpos_mask(table[h], L, L, max_rel) for h in range(H)])
+        m = torch.from_numpy(mask)[None]
+        ref = F.scaled_dot_product_attention(qb, kb, vb, attn_mask=m, scale=scale)
+        np.testing.assert_allclose(out[sl], ref[0].permute(1, 0, 2).numpy(), rtol=1e-11, atol=1e-12)
+        ref_lse = torch.logsumexp(scale * torch.einsum("bhqd,bhkd->bhqk", qb, kb) + m, dim=-1)
+        np.testing.assert_allclose(lse[:, sl], ref_lse[0].numpy(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("act", [ACT_SILU, ACT_GELU_TANH, ACT_IDENTITY])
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_gdpa_onehot_values(oracle_mod, act, causal):
+    """One-hot values: output row i is act(s_ij) on the band and exactly 0 off it."""
+    H, W, max_rel = 1, 4, 5
+    L = d = 13
+    q = _bf16_randn((L, H, d), 45)
+    k = _bf16_randn((L, H, d), 46)
+    v = np.eye(L)[:, None, :]
+    table = np.random.default_rng(47).normal(0, 0.5, size=(H, 2 * max_rel - 1))
+    out, _ = oracle_mod.fwd(q, _offsets([L]), k, v, _offsets([L]), act=act, causal=causal,
+                            scale=0.3, bias=table, max_rel=max_rel, window=W)
+    s = 0.3 * torch.einsum("qd,kd->qk", torch.from_numpy(q[:, 0]), torch.from_numpy(k[:, 0]))
+    s = s + torch.from_numpy(_relpos_mask(table[0], L, L, max_rel))
+    a = {ACT_SILU: F.silu, ACT_GELU_TANH: lambda x: F.gelu(x, approximate="tanh"),
+         ACT_IDENTITY: lambda x: x}[act](s).numpy()
+    ref = np.where(_band(L, W, causal), a, 0.0)
+    np.testing.assert_allclose(out[:, 0, :], ref, rtol=1e-13, atol=1e-14)
+
+
+def test_window_closed_forms(oracle_mod):
+    """K = 0 and one-hot V: the causal window averages the last min(i+1, W)
+    positions; window 1 returns v_i with lse = s_ii; a window at least as long
+    as the sample changes nothing."""
+    L, H, W = 11, 1, 4
+    d = L
+    q = _bf16_randn((L, H, d), 48)
+    k = np.zeros((L, H, d))
+    v = np.eye(L)[:, None, :]
+    o = _offsets([L])
+    out, lse = oracle_mod.fwd(q, o, k, v, o, act=ACT_SOFTMAX, causal=True, scale=1.0, window=W)
+    ref = np.zeros((L, L))
+    for i in range(L):
+        n = min(i + 1, W)
+        ref[i, i - n + 1:i + 1] = 1.0 / n
+    np.testing.assert_allclose(out[:, 0, :], ref, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(lse[0], np.log(np.minimum(np.arange(1, L + 1), W)), rtol=1e-14)
+    kk = _bf16_randn((L, H, d), 49)
+    vv = _bf16_randn((L, H, d), 50)
+    for causal in (False, True):
+        o1, l1 = oracle_mod.fwd(q, o, kk, vv, o, act=ACT_SOFTMAX, causal=causal, scale=0.7,
+                                window=1)
+        np.testing.assert_array_equal(o1, vv)
+        np.testing.assert_allclose(l1[0], 0.7 * np.einsum("id,id->i", q[:, 0], kk[:, 0]),
+                                   rtol=1e-14, atol=1e-14)
+        full, lf = oracle_mod.fwd(q, o, kk, vv, o, act=ACT_SOFTMAX, causal=causal, scale=0.7)
+        wide, lw = oracle_mod.fwd(q, o, kk, vv, o, act=ACT_SOFTMAX, causal=causal, scale=0.7,
+                                  window=L)
+        np.testing.assert_array_equal(wide, full)
+        np.testing.assert_array_equal(lw, lf)
+
+
+def test_window_row_equals_causal_attention_over_its_slice(oracle_mod):
+    """Row i of causal window W sees exactly keys i-W+1..i, so it equals the
+    last row of plain causal attention over that slice of the sample (the
+    relative-position bias depends on i - j only and is unchanged)."""
+    L, H, d, W, max_rel = 20, 2, 8, 6, 4
+    q = _bf16_randn((L, H, d), 51)
+    k = _bf16_randn((L, H, d), 52)
+    v = _bf16_randn((L, H, d), 53)
+    table = np.random.default_rng(54).normal(0, 0.5, size=(H, 2 * max_rel - 1))
+    o = _offsets([L])
+    kw = dict(scale=0.4, bias=table, max_rel=max_rel)
+    for act in (ACT_SOFTMAX, ACT_SILU):
+        out, lse = oracle_mod.fwd(q, o, k, v, o, act=act, causal=True, window=W, **kw)
+        for i in range(L):
+            a = max(0, i - W + 1)
+            n = i + 1 - a
+            os_, ls = oracle_mod.fwd(q[a:i + 1], _offsets([n]), k[a:i + 1], v[a:i + 1],
+                                     _offsets([n]), act=act, causal=True, **kw)
+            np.testing.assert_allclose(out[i], os_[-1], rtol=1e-13, atol=1e-14)
+            np.testing.assert_allclose(lse[:, i], ls[:, -1], rtol=1e-13, atol=1e-14)
+
+
+def test_window_rejects_bad_arguments(oracle_mod):
+    q = np.zeros((3, 1, 4))
+    with pytest.raises(ValueError):  # a window needs equal lengths
+        oracle_mod.fwd(q, np.array([0, 1, 3], dtype=np.int32), q, q,
+                       np.array([0, 2, 3], dtype=np.int32), act=0, scale=1.0, window=2)
+    with pytest.raises(ValueError):
+        oracle_mod.fwd(q, _offsets([3]), q, q, _offsets([3]), act=0, scale=1.0, window=-1)
+
+
+@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH])
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_backward_matches_central_differences(oracle_mod, act, causal):
+    H, d, max_rel, W = 2, 5, 3, 2
+    lq = [4, 5, 0]
+    rng = np.random.default_rng(200 + act + 10 * causal)
+    q = rng.normal(size=(sum(lq), H, d))
+    k = rng.normal(size=(sum(lq), H, d))
+    v = rng.normal(size=(sum(lq), H, d))
+    do = rng.normal(size=(sum(lq), H, d))
+    table = rng.normal(0, 0.5, size=(H, 2 * max_rel - 1))
+    qo = _offsets(lq)
+    kw = dict(act=act, causal=causal, scale=0.45, bias=table, max_rel=max_rel, window=W)
+    dq, dk, dv = oracle_mod.bwd(q, qo, k, v, qo, do, **kw)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle_mod.fwd(qq, qo, kk, vv, qo, **kw)
+        return float(np.sum(o * do))
+
+    h = 1e-5
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp = x.copy(); xp[idx] += h
+            xm = x.copy(); xm[idx] -= h
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        err = np.abs(num - g).max() / max(1.0, np.abs(num).max())
+        assert err < 1e-7, f"d{name}: {err}"

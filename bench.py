@@ -190,7 +190,7 @@ def measure_padded_sdpa(w, t, dev, iters=5, max_gb=40.0):
     v = pad(t["v"], ko, lkv_max).requires_grad_(True)
     do = pad(t["dout"], qo, lq_max)
     mask = None
-    if exact and (w.causal or w.max_rel):
+    if exact and (w.causal or w.max_rel or w.window):
         i = torch.arange(lq_max, device=dev)[:, None]
         j = torch.arange(lkv_max, device=dev)[None, :]
         if w.max_rel:
@@ -200,6 +200,8 @@ def measure_padded_sdpa(w, t, dev, iters=5, max_gb=40.0):
             mask = torch.zeros((1, H, lq_max, lkv_max), device=dev, dtype=torch.bfloat16)
         if w.causal:
             mask = mask.masked_fill((j > i)[None, None], float("-inf"))
+        if w.window:
+            mask = mask.masked_fill(((i - j).abs() >= w.window)[None, None], float("-inf"))
 
     def once():
         o = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=w.scale)
@@ -220,8 +222,10 @@ def measure_padded_sdpa(w, t, dev, iters=5, max_gb=40.0):
     fwd, bwd = workload_flops(w)
     return {"value": (fwd + bwd) / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
             "inputs": f"zero-padded [B={B}, H={H}, Lmax, d={d}] bf16",
-            "mask": ("causal + rel-pos bias as one additive bf16 mask" if mask is not None and
-                     w.max_rel else "causal" if mask is not None else
+            "mask": (" + ".join(x for x, on in (("causal", w.causal),
+                                                 (f"window {w.window}", w.window),
+                                                 ("rel-pos bias", w.max_rel)) if on)
+                     + " as one additive bf16 mask" if mask is not None else
                      "none (exact for equal lengths without causal)" if exact else
                      "none: mask-free softmax lower bound on padded cost"),
             "steps": iters}
@@ -230,7 +234,7 @@ def measure_padded_sdpa(w, t, dev, iters=5, max_gb=40.0):
 def pick_cpu_sample(w, target_pairs, seed=0):
     """Deterministic subset of samples whose pair count is close to target_pairs."""
     order = np.random.default_rng(seed + 12345).permutation(w.B)
-    pairs = (w.lq * (w.lq + 1) // 2) if w.causal else (w.lq * w.lkv)
+    pairs = w.sample_pairs()
     chosen, tot = [], 0
     for b in order:
         if pairs[b] == 0:
@@ -260,9 +264,9 @@ def oracle_step(w, tensors, samples):
         oq = np.array([0, q1 - q0], dtype=np.int32)
         ok = np.array([0, k1 - k0], dtype=np.int32)
         oracle.fwd(sq, oq, sk, sv, ok, act=a, causal=w.causal, scale=w.scale, bias=bias,
-                   max_rel=w.max_rel)
+                   max_rel=w.max_rel, window=w.window)
         oracle.bwd(sq, oq, sk, sv, ok, sd, act=a, causal=w.causal, scale=w.scale, bias=bias,
-                   max_rel=w.max_rel)
+                   max_rel=w.max_rel, window=w.window)
 
 
 def host_sample_tensors(w, samples, device_tensors=None, seed=0):
@@ -366,6 +370,7 @@ def run_reference(args, rank, world):
 
 def workload_config(w, l2_note):
     return {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "act": w.act, "causal": w.causal,
+            "window": w.window,
             "bias": (f"relpos table [{w.H},{2 * w.max_rel - 1}]" if w.max_rel else "none"),
             "Tq": w.Tq, "Tkv": w.Tkv, "pairs_non_padded": w.pairs(),
             "pairs_full_square": w.full_pairs(), "step": "forward + backward", "l2": l2_note}
@@ -395,7 +400,8 @@ def run_gpu(args, rank, world, local_rank):
     dv = torch.empty_like(t["v"])
     ws_f = torch.empty(binding.fwd_workspace_size(w.B, H, d, Tq, Tkv), device=dev, dtype=torch.uint8)
     ws_b = torch.empty(binding.bwd_workspace_size(w.B, H, d, Tq, Tkv), device=dev, dtype=torch.uint8)
-    kw = dict(act=a, causal=w.causal, scale=w.scale, bias=t["bias"], max_rel=w.max_rel)
+    kw = dict(act=a, causal=w.causal, scale=w.scale, bias=t["bias"], max_rel=w.max_rel,
+              window=w.window)
     fwd_flops, bwd_flops = workload_flops(w)
 
     def step(q, qo, k, v, ko, do):
@@ -492,13 +498,12 @@ def run_gpu(args, rank, world, local_rank):
             with torch.cuda.stream(s_cmp):
                 s_cmp.wait_event(ev_in[sl])
                 s_cmp.wait_event(ev_out[sl])  # outputs of two steps back have been read
-                binding.gdpa_fwd(di["q"], di["qo"], di["k"], di["v"], di["ko"], act=a,
-                                 causal=w.causal, scale=w.scale, bias=dbias[sl], max_rel=w.max_rel,
-                                 out=o["out"], lse=o["lse"], workspace=ws_f, stream=s_cmp)
+                kw_e = dict(kw, bias=dbias[sl])
+                binding.gdpa_fwd(di["q"], di["qo"], di["k"], di["v"], di["ko"], out=o["out"],
+                                 lse=o["lse"], workspace=ws_f, stream=s_cmp, **kw_e)
                 binding.gdpa_bwd(di["q"], di["qo"], di["k"], di["v"], di["ko"], o["out"], o["lse"],
-                                 di["dout"], act=a, causal=w.causal, scale=w.scale,
-                                 bias=dbias[sl], max_rel=w.max_rel, dq=o["dq"], dk=o["dk"],
-                                 dv=o["dv"], workspace=ws_b, stream=s_cmp)
+                                 di["dout"], dq=o["dq"], dk=o["dk"], dv=o["dv"], workspace=ws_b,
+                                 stream=s_cmp, **kw_e)
                 ev_cmp[sl].record(s_cmp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_cmp[sl])
@@ -540,6 +545,32 @@ def run_gpu(args, rank, world, local_rank):
         cpu = {"value": tf, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": desc,
                "seconds": secs}
 
+    # Sliding window: the same step without the window on the same inputs (the
+    # full causal attention the window replaces), for the latency reduction.
+    swa = None
+    if rank == 0 and world == 1 and w.window > 0:
+        kw_full = dict(kw, window=0)
+
+        def step_full():
+            binding.gdpa_fwd(*args_dev[:5], out=out, lse=lse, workspace=ws_f, **kw_full)
+            binding.gdpa_bwd(*args_dev, out, lse, dq=dq, dk=dk, dv=dv, workspace=ws_b, **kw_full)
+
+        for _ in range(2):
+            step_full()
+        n_full = max(3, args.steps // 4)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n_full):
+            step_full()
+        e1.record()
+        torch.cuda.synchronize()
+        if binding.device_status() != 0:
+            raise RuntimeError("device status after the full-attention comparison")
+        full_ms = e0.elapsed_time(e1) / n_full
+        swa = {"window": w.window, "swa_ms_per_step": ms / args.steps,
+               "full_causal_ms_per_step": full_ms,
+               "latency_reduction": 1.0 - (ms / args.steps) / full_ms, "full_steps": n_full}
+
     sdpa = None
     if rank == 0 and world == 1 and not args.no_sdpa:
         sdpa = measure_padded_sdpa(w, t, dev)
@@ -571,6 +602,8 @@ def run_gpu(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "padded_sdpa": sdpa,
     }
+    if swa is not None:
+        line["swa_vs_full"] = swa
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -614,8 +647,8 @@ def run_gpu_mxfp8(args, rank, world, local_rank):
         binding.quantize_mxfp8(t["v"], t["ko"], mode=binding.MX_ALONG_TOKENS, codes=vc, scales=vs)
         n += binding.last_launch_count()
         binding.gdpa_fwd_mxfp8(qc, qs, t["qo"], kc, ks, vc, vs, t["ko"], causal=w.causal,
-                               scale=w.scale, bias=t["bias"], max_rel=w.max_rel, out=out, lse=lse,
-                               workspace=ws)
+                               scale=w.scale, bias=t["bias"], max_rel=w.max_rel, window=w.window,
+                               out=out, lse=lse, workspace=ws)
         return n + binding.last_launch_count()
 
     for _ in range(args.warmup):

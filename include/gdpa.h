@@ -13,7 +13,8 @@
  *
  * For sample b with Lq_b = q_offsets[b+1]-q_offsets[b] query rows and
  * Lkv_b = kv_offsets[b+1]-kv_offsets[b] key/value rows, head h, local row i
- * and local key j (mask: j <= i when causal, else all):
+ * and local key j (mask: j <= i when causal, and |i - j| < window for the
+ * sliding-window entry points; else all):
  *     s_ij  = scale * <q_i, k_j> + bias_h(i - j)
  *     p_ij  = softmax_j(s_ij)       (GDPA_ACT_SOFTMAX, masked entries excluded)
  *           = act(s_ij)             (SiLU, GELU-tanh, identity; no normalisation)
@@ -77,7 +78,7 @@ typedef enum {
   GDPA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than the query says */
   GDPA_ERR_CUDA = 4,         /* a CUDA runtime call failed */
   GDPA_ERR_TIMEOUT = 5,      /* device: a pipeline wait ran past its limit */
-  GDPA_ERR_BAD_OFFSETS = 6   /* device: offsets malformed, or causal with Lq_b != Lkv_b */
+  GDPA_ERR_BAD_OFFSETS = 6   /* device: offsets malformed, or causal / window with Lq_b != Lkv_b */
 } gdpa_status;
 
 /* Bytes of workspace gdpa_fwd needs (the work list of the persistent
@@ -111,6 +112,30 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
                      const gdpa_bias* bias, int act, int causal, float scale, const void* out,
                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
                      void* workspace, size_t ws_bytes, void* stream);
+
+/* Sliding-window attention ("GEM Training ..." SWA paragraph: each token
+ * attends only to nearby events, O(L * window) work instead of O(L^2), and
+ * the kernel skips the tiles outside the window).  window > 0 keeps the
+ * pairs with |i - j| < window, intersected with j <= i when causal: a causal
+ * row sees its `window` most recent keys (itself included), a non-causal row
+ * also the window - 1 keys after it.  window == 0 is no window (the calls
+ * then equal gdpa_fwd / gdpa_bwd).  A window needs Lq_b == Lkv_b for every
+ * sample (device check, GDPA_ERR_BAD_OFFSETS); window < 0 returns
+ * GDPA_ERR_INVALID_ARG.  Key / query tiles outside the band are never
+ * loaded, and the scheduler's cost counts only the tiles inside it.  Every
+ * other argument, output, workspace and error is that of gdpa_fwd /
+ * gdpa_bwd; the backward must get the forward's window. */
+gdpa_status gdpa_fwd_window(const void* q, const int32_t* q_offsets, const void* k,
+                            const void* v, const int32_t* kv_offsets, int B, int H, int d,
+                            int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
+                            int window, float scale, void* out, float* lse, void* workspace,
+                            size_t ws_bytes, void* stream);
+gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void* k,
+                            const void* v, const int32_t* kv_offsets, int B, int H, int d,
+                            int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
+                            int window, float scale, const void* out, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                            size_t ws_bytes, void* stream);
 
 /* MXFP8 block quantisation (OCP Microscaling Formats v1.0; "GEM Training ..."
  * low-precision paragraph: attention with MXFP8 block-scaled MMA).  Elements
@@ -150,6 +175,15 @@ gdpa_status gdpa_fwd_mxfp8(const void* q_codes, const void* q_scales, const int3
                            int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
                            float scale, void* out, float* lse, void* workspace, size_t ws_bytes,
                            void* stream);
+
+/* gdpa_fwd_mxfp8 with a sliding window (semantics of gdpa_fwd_window). */
+gdpa_status gdpa_fwd_mxfp8_window(const void* q_codes, const void* q_scales,
+                                  const int32_t* q_offsets, const void* k_codes,
+                                  const void* k_scales, const void* v_codes, const void* v_scales,
+                                  const int32_t* kv_offsets, int B, int H, int d, int64_t Tq,
+                                  int64_t Tkv, const gdpa_bias* bias, int act, int causal,
+                                  int window, float scale, void* out, float* lse,
+                                  void* workspace, size_t ws_bytes, void* stream);
 
 /* Reads the device status word set by earlier calls on this device,
  * synchronising `stream` first, then clears it.  Returns GDPA_OK,

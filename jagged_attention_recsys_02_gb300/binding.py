@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "GDPA_OK", 1: "GDPA_ERR_INVALID_ARG", 2: "GDPA_ERR_UNSUPPORTE
 EXPORTS = ("gdpa_fwd_workspace_size", "gdpa_fwd", "gdpa_bwd_workspace_size", "gdpa_bwd",
            "gdpa_get_device_status", "gdpa_status_string", "gdpa_last_launch_count",
            "gdpa_timing_enable", "gdpa_timing_collect", "gdpa_fwd_noalloc",
-           "gdpa_mxfp8_scale_bytes", "gdpa_quantize_mxfp8", "gdpa_fwd_mxfp8")
+           "gdpa_mxfp8_scale_bytes", "gdpa_quantize_mxfp8", "gdpa_fwd_mxfp8",
+           "gdpa_fwd_window", "gdpa_bwd_window", "gdpa_fwd_mxfp8_window")
 MX_ALONG_CHANNELS, MX_ALONG_TOKENS = 0, 1
 
 
@@ -72,10 +73,17 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdpa_fwd.argtypes = [vp, vp, vp, vp, vp, I, I, I, i64, i64,
                                  ctypes.POINTER(gdpa_bias), I, I, F, vp, vp, vp, sz, vp]
         lib.gdpa_fwd.restype = I
+        lib.gdpa_fwd_window.argtypes = [vp, vp, vp, vp, vp, I, I, I, i64, i64,
+                                        ctypes.POINTER(gdpa_bias), I, I, I, F, vp, vp, vp, sz, vp]
+        lib.gdpa_fwd_window.restype = I
         lib.gdpa_bwd.argtypes = [vp, vp, vp, vp, vp, I, I, I, i64, i64,
                                  ctypes.POINTER(gdpa_bias), I, I, F, vp, vp, vp, vp, vp, vp,
                                  vp, sz, vp]
         lib.gdpa_bwd.restype = I
+        lib.gdpa_bwd_window.argtypes = [vp, vp, vp, vp, vp, I, I, I, i64, i64,
+                                        ctypes.POINTER(gdpa_bias), I, I, I, F, vp, vp, vp, vp, vp,
+                                        vp, vp, sz, vp]
+        lib.gdpa_bwd_window.restype = I
         lib.gdpa_get_device_status.argtypes = [vp]
         lib.gdpa_get_device_status.restype = I
         lib.gdpa_status_string.argtypes = [I]
@@ -94,6 +102,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdpa_fwd_mxfp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, i64, i64,
                                        ctypes.POINTER(gdpa_bias), I, I, F, vp, vp, vp, sz, vp]
         lib.gdpa_fwd_mxfp8.restype = I
+        lib.gdpa_fwd_mxfp8_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, i64, i64,
+                                              ctypes.POINTER(gdpa_bias), I, I, I, F, vp, vp, vp,
+                                              sz, vp]
+        lib.gdpa_fwd_mxfp8_window.restype = I
         _lib = lib
         return lib
 
@@ -134,8 +146,9 @@ def bwd_workspace_size(B, H, d, Tq, Tkv) -> int:
 
 
 def gdpa_fwd(q, q_offsets, k, v, kv_offsets, *, act, causal=False, scale, bias=None, max_rel=0,
-             out=None, lse=None, workspace=None, stream=None):
-    """Forward pass through the C ABI.  Returns (out, lse)."""
+             window=0, out=None, lse=None, workspace=None, stream=None):
+    """Forward pass through the C ABI (gdpa_fwd, or gdpa_fwd_window when
+    window > 0).  Returns (out, lse)."""
     lib = load()
     Tq, H, d = q.shape
     Tkv = k.shape[0]
@@ -148,16 +161,23 @@ def gdpa_fwd(q, q_offsets, k, v, kv_offsets, *, act, causal=False, scale, bias=N
     if workspace is None:
         workspace = torch.empty(fwd_workspace_size(B, H, d, Tq, Tkv), device=q.device,
                                 dtype=torch.uint8)
-    rc = lib.gdpa_fwd(_ptr(q), _ptr(q_offsets), _ptr(k), _ptr(v), _ptr(kv_offsets), B, H, d, Tq,
-                      Tkv, _bias(bias, max_rel), a, int(bool(causal)), float(scale), _ptr(out),
-                      _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream))
-    _check(rc, "gdpa_fwd")
+    head = (_ptr(q), _ptr(q_offsets), _ptr(k), _ptr(v), _ptr(kv_offsets), B, H, d, Tq, Tkv,
+            _bias(bias, max_rel), a, int(bool(causal)))
+    tail = (float(scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+            _stream(stream))
+    if window:
+        rc = lib.gdpa_fwd_window(*head, int(window), *tail)
+    else:
+        rc = lib.gdpa_fwd(*head, *tail)
+    _check(rc, "gdpa_fwd_window" if window else "gdpa_fwd")
     return out, lse
 
 
 def gdpa_bwd(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, act, causal=False, scale,
-             bias=None, max_rel=0, dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """Backward pass through the C ABI.  Returns (dq, dk, dv)."""
+             bias=None, max_rel=0, window=0, dq=None, dk=None, dv=None, workspace=None,
+             stream=None):
+    """Backward pass through the C ABI (gdpa_bwd, or gdpa_bwd_window when
+    window > 0).  Returns (dq, dk, dv)."""
     lib = load()
     Tq, H, d = q.shape
     Tkv = k.shape[0]
@@ -168,11 +188,15 @@ def gdpa_bwd(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, act, causal=Fals
     if workspace is None:
         workspace = torch.empty(bwd_workspace_size(B, H, d, Tq, Tkv), device=q.device,
                                 dtype=torch.uint8)
-    rc = lib.gdpa_bwd(_ptr(q), _ptr(q_offsets), _ptr(k), _ptr(v), _ptr(kv_offsets), B, H, d, Tq,
-                      Tkv, _bias(bias, max_rel), _act(act), int(bool(causal)), float(scale),
-                      _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
-                      _ptr(workspace), workspace.numel(), _stream(stream))
-    _check(rc, "gdpa_bwd")
+    head = (_ptr(q), _ptr(q_offsets), _ptr(k), _ptr(v), _ptr(kv_offsets), B, H, d, Tq, Tkv,
+            _bias(bias, max_rel), _act(act), int(bool(causal)))
+    tail = (float(scale), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+            _ptr(workspace), workspace.numel(), _stream(stream))
+    if window:
+        rc = lib.gdpa_bwd_window(*head, int(window), *tail)
+    else:
+        rc = lib.gdpa_bwd(*head, *tail)
+    _check(rc, "gdpa_bwd_window" if window else "gdpa_bwd")
     return dq, dk, dv
 
 
@@ -219,9 +243,10 @@ def quantize_mxfp8(x, offsets=None, *, mode, codes=None, scales=None, stream=Non
 
 
 def gdpa_fwd_mxfp8(q_codes, q_scales, q_offsets, k_codes, k_scales, v_codes, v_scales, kv_offsets,
-                   *, causal=False, scale, bias=None, max_rel=0, out=None, lse=None,
+                   *, causal=False, scale, bias=None, max_rel=0, window=0, out=None, lse=None,
                    workspace=None, stream=None):
-    """MXFP8 forward (softmax) through the C ABI.  Returns (out bf16, lse)."""
+    """MXFP8 forward (softmax) through the C ABI (gdpa_fwd_mxfp8, or
+    gdpa_fwd_mxfp8_window when window > 0).  Returns (out bf16, lse)."""
     lib = load()
     Tq, H, d = q_codes.shape
     Tkv = k_codes.shape[0]
@@ -233,10 +258,14 @@ def gdpa_fwd_mxfp8(q_codes, q_scales, q_offsets, k_codes, k_scales, v_codes, v_s
     if workspace is None:
         workspace = torch.empty(fwd_workspace_size(B, H, d, Tq, Tkv), device=q_codes.device,
                                 dtype=torch.uint8)
-    rc = lib.gdpa_fwd_mxfp8(_ptr(q_codes), _ptr(q_scales), _ptr(q_offsets), _ptr(k_codes),
-                            _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), _ptr(kv_offsets), B,
-                            H, d, Tq, Tkv, _bias(bias, max_rel), ACT_SOFTMAX, int(bool(causal)),
-                            float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
-                            workspace.numel(), _stream(stream))
-    _check(rc, "gdpa_fwd_mxfp8")
+    head = (_ptr(q_codes), _ptr(q_scales), _ptr(q_offsets), _ptr(k_codes), _ptr(k_scales),
+            _ptr(v_codes), _ptr(v_scales), _ptr(kv_offsets), B, H, d, Tq, Tkv,
+            _bias(bias, max_rel), ACT_SOFTMAX, int(bool(causal)))
+    tail = (float(scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+            _stream(stream))
+    if window:
+        rc = lib.gdpa_fwd_mxfp8_window(*head, int(window), *tail)
+    else:
+        rc = lib.gdpa_fwd_mxfp8(*head, *tail)
+    _check(rc, "gdpa_fwd_mxfp8_window" if window else "gdpa_fwd_mxfp8")
     return out, lse

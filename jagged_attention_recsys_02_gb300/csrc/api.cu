@@ -133,8 +133,9 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 gdpa_status check_common(const void* q, const int32_t* qo, const void* k, const void* v,
                          const int32_t* ko, int B, int H, int d, int64_t Tq, int64_t Tkv,
-                         const gdpa_bias* bias, int act, int causal) {
+                         const gdpa_bias* bias, int act, int causal, int window) {
   if (B < 0 || H <= 0 || Tq < 0 || Tkv < 0) return GDPA_ERR_INVALID_ARG;
+  if (window < 0) return GDPA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return GDPA_ERR_UNSUPPORTED;
   if (H > 256) return GDPA_ERR_UNSUPPORTED;
   if (act < GDPA_ACT_SOFTMAX || act > GDPA_ACT_IDENTITY) return GDPA_ERR_INVALID_ARG;
@@ -179,9 +180,18 @@ gdpa_status gdpa_fwd(const void* q, const int32_t* q_offsets, const void* k, con
                      const int32_t* kv_offsets, int B, int H, int d, int64_t Tq, int64_t Tkv,
                      const gdpa_bias* bias, int act, int causal, float scale, void* out,
                      float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  return gdpa_fwd_window(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act, causal, 0,
+                         scale, out, lse, workspace, ws_bytes, stream);
+}
+
+gdpa_status gdpa_fwd_window(const void* q, const int32_t* q_offsets, const void* k,
+                            const void* v, const int32_t* kv_offsets, int B, int H, int d,
+                            int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
+                            int window, float scale, void* out, float* lse, void* workspace,
+                            size_t ws_bytes, void* stream) {
   t_launches = 0;
   gdpa_status st = check_common(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act,
-                                causal);
+                                causal, window);
   if (st != GDPA_OK) return st;
   if (Tq > 0 && (out == nullptr || !aligned16(out))) return GDPA_ERR_INVALID_ARG;
   if (act == GDPA_ACT_SOFTMAX && Tq > 0 && lse == nullptr) return GDPA_ERR_INVALID_ARG;
@@ -209,8 +219,8 @@ gdpa_status gdpa_fwd(const void* q, const int32_t* q_offsets, const void* k, con
   int* ticket = reinterpret_cast<int*>(ws + 4);
   int2* items = reinterpret_cast<int2*>(ws + 256);
 
-  if (launch_build_worklist(q_offsets, kv_offsets, B, H, Tq, Tkv, causal, 0, items, n_items,
-                            ticket, dev->status, s) != cudaSuccess)
+  if (launch_build_worklist(q_offsets, kv_offsets, B, H, Tq, Tkv, causal, window, 0, items,
+                            n_items, ticket, dev->status, s) != cudaSuccess)
     return GDPA_ERR_CUDA;
   ++t_launches;
 
@@ -225,6 +235,7 @@ gdpa_status gdpa_fwd(const void* q, const int32_t* q_offsets, const void* k, con
   p.bias_table = table;
   p.max_rel = max_rel;
   p.causal = causal;
+  p.window = window;
   p.scale = scale;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
@@ -257,9 +268,19 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
                      const gdpa_bias* bias, int act, int causal, float scale, const void* out,
                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
                      void* workspace, size_t ws_bytes, void* stream) {
+  return gdpa_bwd_window(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act, causal, 0,
+                         scale, out, lse, dout, dq, dk, dv, workspace, ws_bytes, stream);
+}
+
+gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void* k,
+                            const void* v, const int32_t* kv_offsets, int B, int H, int d,
+                            int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
+                            int window, float scale, const void* out, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                            size_t ws_bytes, void* stream) {
   t_launches = 0;
   gdpa_status st = check_common(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act,
-                                causal);
+                                causal, window);
   if (st != GDPA_OK) return st;
   if (Tq > 0 && (dout == nullptr || dq == nullptr || !aligned16(dout) || !aligned16(dq)))
     return GDPA_ERR_INVALID_ARG;
@@ -309,8 +330,8 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
                    sm ? d : 64, sm ? kBwdSmDqRows : kBwdQRows))
     return GDPA_ERR_INVALID_ARG;
 
-  if (launch_build_worklist(kv_offsets, q_offsets, B, H, Tkv, Tq, causal, 1, items, n_items,
-                            ticket, dev->status, s) != cudaSuccess)
+  if (launch_build_worklist(kv_offsets, q_offsets, B, H, Tkv, Tq, causal, window, 1, items,
+                            n_items, ticket, dev->status, s) != cudaSuccess)
     return GDPA_ERR_CUDA;
   ++t_launches;
 
@@ -325,6 +346,7 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
   p.bias_table = table;
   p.max_rel = max_rel;
   p.causal = causal;
+  p.window = window;
   p.scale = scale;
   p.out = static_cast<const __nv_bfloat16*>(out);
   p.lse = lse;
@@ -386,9 +408,21 @@ gdpa_status gdpa_fwd_mxfp8(const void* q_codes, const void* q_scales, const int3
                            int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
                            float scale, void* out, float* lse, void* workspace, size_t ws_bytes,
                            void* stream) {
+  return gdpa_fwd_mxfp8_window(q_codes, q_scales, q_offsets, k_codes, k_scales, v_codes, v_scales,
+                               kv_offsets, B, H, d, Tq, Tkv, bias, act, causal, 0, scale, out,
+                               lse, workspace, ws_bytes, stream);
+}
+
+gdpa_status gdpa_fwd_mxfp8_window(const void* q_codes, const void* q_scales,
+                                  const int32_t* q_offsets, const void* k_codes,
+                                  const void* k_scales, const void* v_codes, const void* v_scales,
+                                  const int32_t* kv_offsets, int B, int H, int d, int64_t Tq,
+                                  int64_t Tkv, const gdpa_bias* bias, int act, int causal,
+                                  int window, float scale, void* out, float* lse,
+                                  void* workspace, size_t ws_bytes, void* stream) {
   t_launches = 0;
   gdpa_status st = check_common(q_codes, q_offsets, k_codes, v_codes, kv_offsets, B, H, d, Tq,
-                                Tkv, bias, act, causal);
+                                Tkv, bias, act, causal, window);
   if (st != GDPA_OK) return st;
   if (d != 128 || act != GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
   if (Tq > 0 && (q_scales == nullptr || out == nullptr || lse == nullptr || !aligned16(out)))
@@ -418,8 +452,8 @@ gdpa_status gdpa_fwd_mxfp8(const void* q_codes, const void* q_scales, const int3
   int* n_items = reinterpret_cast<int*>(ws);
   int* ticket = reinterpret_cast<int*>(ws + 4);
   int2* items = reinterpret_cast<int2*>(ws + 256);
-  if (launch_build_worklist(q_offsets, kv_offsets, B, H, Tq, Tkv, causal, 0, items, n_items,
-                            ticket, dev->status, s) != cudaSuccess)
+  if (launch_build_worklist(q_offsets, kv_offsets, B, H, Tq, Tkv, causal, window, 0, items,
+                            n_items, ticket, dev->status, s) != cudaSuccess)
     return GDPA_ERR_CUDA;
   ++t_launches;
   FwdParams p{};
@@ -433,6 +467,7 @@ gdpa_status gdpa_fwd_mxfp8(const void* q_codes, const void* q_scales, const int3
   p.bias_table = table;
   p.max_rel = max_rel;
   p.causal = causal;
+  p.window = window;
   p.scale = scale;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;

@@ -126,9 +126,14 @@ __device__ __forceinline__ SmItem decode_sm(int2 it, const BwdParams& p) {
   r.Lq = p.qo[r.b + 1] - r.q0;
   r.k0 = p.ko[r.b];
   r.Lkv = p.ko[r.b + 1] - r.k0;
-  r.qt0 = p.causal ? r.kb : 0;  // queries before the block's first key see none of it
-  const int rows = r.Lq - r.qt0 * kQRows;
-  r.nq = rows > 0 ? (rows + kQRows - 1) / kQRows : 0;
+  // query tiles that see some key of the block (causal / sliding-window band)
+  // (items exist only for blocks that start inside the sample, and every
+  // such key is seen by some query unless the sample has no query rows)
+  const int kb0 = r.kb * kKRows;
+  const int qb = band_query_begin(kb0, p.causal, p.window);
+  const int qe = band_query_end(min(r.Lkv, kb0 + kKRows) - 1, p.window, r.Lq);
+  r.qt0 = qb / kQRows;
+  r.nq = (qe + kQRows - 1) / kQRows - r.qt0;  // 0 when qe == qb == 0 (no query rows)
   return r;
 }
 
@@ -477,8 +482,14 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       const SmItem in = decode_sm(item, p);
       const int kb0 = in.kb * kKRows;   // first local key row of the block
       const int jl = kb0 + j;           // this thread's local key row
-      const bool key_ok = jl < in.Lkv;
-      const bool keys_full = kb0 + kKRows <= in.Lkv;
+      // queries that see this key: [vis_lo, vis_hi) (none for a key past the sample)
+      const int vis_lo = band_query_begin(jl, p.causal, p.window);
+      const int vis_hi = jl < in.Lkv ? band_query_end(jl, p.window, in.Lq) : 0;
+      // Query tiles inside [full_lo, full_hi) pair with every key of a full
+      // block and need no mask (the band's bounds grow with the key, so the
+      // block's last key bounds the first such query and its first key the last).
+      const int full_lo = band_query_begin(kb0 + kKRows - 1, p.causal, p.window);
+      const int full_hi = kb0 + kKRows <= in.Lkv ? band_query_end(kb0, p.window, in.Lq) : 0;
       bool abort_now = false;
       for (int t = 0; t < in.nq; ++t, ++g) {
         const uint32_t s = g % C::kQStages;
@@ -494,13 +505,11 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         const int cp = (j + 1) & 1;
         const float* bwin = st + 2 * kQRows + cp * C::kBiasCopy + cp + (kKRows - 1) - j;
         const int qloc = (in.qt0 + t) * kQRows;
-        // Tiles strictly inside the sample (and below the causal diagonal) need no mask.
-        const bool full = keys_full && qloc + kQRows <= in.Lq &&
-                          (!p.causal || qloc >= kb0 + kKRows - 1);
+        const bool full = qloc >= full_lo && qloc + kQRows <= full_hi;
         int c_lo = 0, c_hi = kQRows;  // valid query columns: c_lo <= c < c_hi
         if (!full) {
-          c_hi = key_ok ? min(kQRows, in.Lq - qloc) : 0;
-          if (p.causal) c_lo = max(0, jl - qloc);
+          c_hi = min(kQRows, vis_hi - qloc);
+          c_lo = max(0, vis_lo - qloc);
         }
         // Phase 1: P^T = exp2(S^T scale log2e + bias log2e - lse log2e); bf16
         // pairs go back into the S columns (query pair k of the group's 64 at

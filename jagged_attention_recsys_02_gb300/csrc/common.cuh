@@ -29,6 +29,54 @@ constexpr int kCostBuckets = 2048;
 __host__ __device__ inline int item_head(int2 it) { return it.y & 0xFF; }
 __host__ __device__ inline int item_block(int2 it) { return it.y >> 8; }
 
+// Sliding-window band ("GEM Training ..." SWA paragraph: each token attends
+// only to nearby events).  Local key j is visible from local query i when
+// j <= i (causal) and |i - j| < window (window > 0); window 0 is no window.
+// Both bounds are monotone in i (and in j), so the keys visible from a run
+// of consecutive rows, and the queries that see a run of consecutive keys,
+// are contiguous ranges.
+__host__ __device__ __forceinline__ int band_key_begin(int i, int window) {
+  return window > 0 ? max(0, i - window + 1) : 0;
+}
+__host__ __device__ __forceinline__ int band_key_end(int i, int causal, int window, int Lkv) {
+  if (causal) return min(Lkv, i + 1);
+  return window > 0 ? min(Lkv, i + window) : Lkv;
+}
+__host__ __device__ __forceinline__ int band_query_begin(int j, int causal, int window) {
+  if (causal) return j;
+  return window > 0 ? max(0, j - window + 1) : 0;
+}
+__host__ __device__ __forceinline__ int band_query_end(int j, int window, int Lq) {
+  return window > 0 ? min(Lq, j + window) : Lq;
+}
+// Tiles of `tile` keys visited by the query rows [r_begin, r_end) (r_begin <
+// r_end): [*t_begin, *t_end), empty when no key is visible.
+__host__ __device__ __forceinline__ void band_key_tiles(int r_begin, int r_end, int causal,
+                                                        int window, int Lkv, int tile,
+                                                        int* t_begin, int* t_end) {
+  const int kb = band_key_begin(r_begin, window);
+  const int ke = band_key_end(r_end - 1, causal, window, Lkv);
+  if (ke <= kb) {
+    *t_begin = *t_end = 0;
+    return;
+  }
+  *t_begin = kb / tile;
+  *t_end = (ke + tile - 1) / tile;
+}
+// Tiles of `tile` queries that see some key of [c_begin, c_end) (c_begin < c_end).
+__host__ __device__ __forceinline__ void band_query_tiles(int c_begin, int c_end, int causal,
+                                                          int window, int Lq, int tile,
+                                                          int* t_begin, int* t_end) {
+  const int qb = band_query_begin(c_begin, causal, window);
+  const int qe = band_query_end(c_end - 1, window, Lq);
+  if (qe <= qb) {
+    *t_begin = *t_end = 0;
+    return;
+  }
+  *t_begin = qb / tile;
+  *t_end = (qe + tile - 1) / tile;
+}
+
 // Device status word values (same numbering as gdpa_status).
 __device__ __forceinline__ void set_status(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
@@ -42,6 +90,7 @@ struct FwdParams {
   const float* bias_table;  // nullptr: no bias
   int max_rel;
   int causal;
+  int window;               // 0: no sliding window
   float scale;
   __nv_bfloat16* out;
   float* lse;               // nullptr allowed for GDPA activations
@@ -59,6 +108,7 @@ struct BwdParams {
   const float* bias_table;
   int max_rel;
   int causal;
+  int window;
   float scale;
   const __nv_bfloat16* out;
   const float* lse;
@@ -75,7 +125,8 @@ struct BwdParams {
 
 // Host-side launchers (defined in the kernel translation units).
 cudaError_t launch_build_worklist(const int32_t* outer_off, const int32_t* inner_off, int B, int H,
-                                  int64_t T_outer, int64_t T_inner, int causal, int mode,
+                                  int64_t T_outer, int64_t T_inner, int causal, int window,
+                                  int mode,
                                   int2* items, int* n_items, int* ticket, int* status,
                                   cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,

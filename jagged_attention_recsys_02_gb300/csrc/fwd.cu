@@ -101,7 +101,15 @@ __device__ __forceinline__ float act_apply(int act, float x) {
 struct ItemInfo {
   int b, head, blk;
   int q0, k0, Lq, Lkv;
-  int n0, n1;  // kv tiles visited by half 0 / half 1 (0 = half inactive)
+  // Key tiles visited: half h covers [lo_h, hi_h) (empty when lo_h == hi_h);
+  // the item streams their union [jb, je), which is contiguous because the
+  // causal / window band of consecutive rows is.
+  int lo0, hi0, lo1, hi1;
+  int jb, je;
+  __device__ __forceinline__ int lo(int h) const { return h ? lo1 : lo0; }
+  __device__ __forceinline__ int hi(int h) const { return h ? hi1 : hi0; }
+  __device__ __forceinline__ bool visits(int h, int j) const { return j >= lo(h) && j < hi(h); }
+  __device__ __forceinline__ bool has_half1() const { return hi1 > lo1; }
 };
 
 __device__ __forceinline__ ItemInfo decode_item(int2 it, const FwdParams& p) {
@@ -113,16 +121,18 @@ __device__ __forceinline__ ItemInfo decode_item(int2 it, const FwdParams& p) {
   r.Lq = p.qo[r.b + 1] - r.q0;
   r.k0 = p.ko[r.b];
   r.Lkv = p.ko[r.b + 1] - r.k0;
-  const int nkv = (r.Lkv + kKvRows - 1) / kKvRows;
   const int r0 = r.blk * kItemRows;
-  const bool h1 = r0 + kHalfRows < r.Lq;
-  if (!p.causal) {
-    r.n0 = nkv;
-    r.n1 = h1 ? nkv : 0;
-  } else {
-    r.n0 = min(nkv, (min(r.Lq, r0 + kHalfRows) + kKvRows - 1) / kKvRows);
-    r.n1 = h1 ? min(nkv, (min(r.Lq, r0 + kItemRows) + kKvRows - 1) / kKvRows) : 0;
-  }
+  band_key_tiles(r0, min(r.Lq, r0 + kHalfRows), p.causal, p.window, r.Lkv, kKvRows, &r.lo0,
+                 &r.hi0);
+  if (r0 + kHalfRows < r.Lq)
+    band_key_tiles(r0 + kHalfRows, min(r.Lq, r0 + kItemRows), p.causal, p.window, r.Lkv, kKvRows,
+                   &r.lo1, &r.hi1);
+  else
+    r.lo1 = r.hi1 = r.hi0;
+  // Half 0 starts no later and half 1 ends no earlier; with half 0 empty
+  // (no key at all) both are.
+  r.jb = r.lo0;
+  r.je = max(r.hi0, r.hi1);
   return r;
 }
 
@@ -215,14 +225,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       ++it;
       if (item.x < 0) break;
       const ItemInfo in = decode_item(item, p);
-      const int n = max(in.n0, in.n1);
+      const int n = in.je - in.jb;
       if (n == 0) continue;
       w = mbar_wait(bar(C::kQEmpty), (qi & 1u) ^ 1u, abort_flag);
       if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
       const int row0 = in.q0 + in.blk * kItemRows;
+      const int n_halves = in.has_half1() ? 2 : 1;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(C::kQFull), (in.n1 > 0 ? 2 : 1) * C::kQHalfBytes);
-        for (int half = 0; half < (in.n1 > 0 ? 2 : 1); ++half)
+        mbar_arrive_expect_tx(bar(C::kQFull), n_halves * C::kQHalfBytes);
+        for (int half = 0; half < n_halves; ++half)
           for (int x = 0; x < D; x += 64)
             tma_load_3d(sbase + (half ? C::kQ1 : C::kQ0) + (x / 64) * (kHalfRows * 128),
                         &tmap_q, bar(C::kQFull), x, in.head, row0 + half * kHalfRows);
@@ -252,8 +263,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         }
       };
       float cur[16];
-      if (brow != nullptr) fetch(0, cur);
-      for (int j = 0; j < n; ++j, ++g) {
+      if (brow != nullptr) fetch(in.jb, cur);
+      for (int j = in.jb; j < in.je; ++j, ++g) {
         const uint32_t s = g % C::kStages;
         const uint32_t ph = (g / C::kStages) & 1u;
         const uint32_t kdst = sbase + C::kKV + s * 2 * C::kTileBytes;
@@ -287,7 +298,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
               }
             }
           }
-          if (j + 1 < n) fetch(j + 1, nxt);
+          if (j + 1 < in.je) fetch(j + 1, nxt);
         }
         __syncwarp();
         if (lane == 0) {
@@ -296,7 +307,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
             tma_load_3d(kdst + C::kTileBytes + (x / 64) * (kKvRows * 128), &tmap_v,
                         bar(C::kVFull + s), x, in.head, krow);
         }
-        if (brow != nullptr && j + 1 < n) {
+        if (brow != nullptr && j + 1 < in.je) {
 #pragma unroll
           for (int k = 0; k < 16; ++k) cur[k] = nxt[k];
         }
@@ -360,45 +371,48 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         ++it;
         if (item.x < 0) break;
         const ItemInfo in = decode_item(item, p);
-        const int n = max(in.n0, in.n1);
+        const int n = in.je - in.jb;
         if (n == 0) continue;
         if (!mbar_wait(bar(C::kQFull), qi & 1u, abort_flag)) { fail(); break; }
         ++qi;
         tc_fence_after();
-        // The half that visits the most key tiles issues the item's last S.
-        const int last_s_half = (in.n1 == n) ? 1 : 0;
+        // Key tile j's last score product is half 1's when half 1 visits j;
+        // the item's last score product is that of tile je - 1.
+        const int last_s_half = in.visits(1, in.je - 1) ? 1 : 0;
         {
           const uint32_t s = g % C::kStages;
           if (!mbar_wait(bar(C::kKFull + s), (g / C::kStages) & 1u, abort_flag)) { fail(); break; }
           tc_fence_after();
-          if (in.n0 > 0) issue_s(0, s);
-          if (in.n1 > 0) issue_s(1, s);
-          mma_commit(bar(C::kKEmpty + s));  // K tile 0 has all its readers
+          if (in.visits(0, in.jb)) issue_s(0, s);
+          if (in.visits(1, in.jb)) issue_s(1, s);
+          mma_commit(bar(C::kKEmpty + s));  // the first K tile has all its readers
           if (n == 1) mma_commit(bar(C::kQEmpty));
         }
-        for (int j = 0; j < n; ++j) {
-          const uint32_t gj = g + j;
+        for (int j = in.jb; j < in.je; ++j) {
+          const uint32_t gj = g + (j - in.jb);
           const uint32_t s = gj % C::kStages;
           const uint32_t s_next = (gj + 1) % C::kStages;
           const uint32_t ph_next = ((gj + 1) / C::kStages) & 1u;
           if (!mbar_wait(bar(C::kVFull + s), (gj / C::kStages) & 1u, abort_flag)) { ok = false; fail(); break; }
-          const int last_half_j = (j < in.n1) ? 1 : 0;  // last user of stage s
+          const int last_half_j = in.visits(1, j) ? 1 : 0;  // last user of stage s
+          const int last_half_next = in.visits(1, j + 1) ? 1 : 0;
           for (int half = 0; half < 2; ++half) {
-            const int nh = half ? in.n1 : in.n0;
-            if (j >= nh) continue;
-            if (!mbar_wait(bar(C::kPFull + half), tcount[half] & 1u, abort_flag)) { ok = false; fail(); break; }
-            ++tcount[half];
-            tc_fence_after();
-            issue_pv(half, s, j == 0);
-            if (j == nh - 1) mma_commit(bar(C::kODone + half));
-            if (half == last_half_j) mma_commit(bar(C::kVEmpty + s));
-            if (j + 1 < nh) {
+            if (in.visits(half, j)) {
+              if (!mbar_wait(bar(C::kPFull + half), tcount[half] & 1u, abort_flag)) { ok = false; fail(); break; }
+              ++tcount[half];
+              tc_fence_after();
+              issue_pv(half, s, j == in.lo(half));
+              if (j == in.hi(half) - 1) mma_commit(bar(C::kODone + half));
+              if (half == last_half_j) mma_commit(bar(C::kVEmpty + s));
+            }
+            // S of the next tile (a half may start there: a sliding window
+            // moves half 1's first tile past half 0's)
+            if (in.visits(half, j + 1)) {
               if (!mbar_wait(bar(C::kKFull + s_next), ph_next, abort_flag)) { ok = false; fail(); break; }
               tc_fence_after();
               issue_s(half, s_next);
-              // the last score product that reads K tile j+1
-              if (half == ((j + 1 < in.n1) ? 1 : 0)) mma_commit(bar(C::kKEmpty + s_next));
-              if (j + 1 == n - 1 && half == last_s_half) mma_commit(bar(C::kQEmpty));
+              if (half == last_half_next) mma_commit(bar(C::kKEmpty + s_next));
+              if (j + 1 == in.je - 1 && half == last_s_half) mma_commit(bar(C::kQEmpty));
             }
           }
           if (!ok) break;
@@ -432,18 +446,22 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       ++it;
       if (item.x < 0) break;
       const ItemInfo in = decode_item(item, p);
-      const int nh = half ? in.n1 : in.n0;
+      const int j_lo = in.lo(half), j_hi = in.hi(half);
+      const int nh = j_hi - j_lo;
       const uint32_t g_item = g;  // key-tile counter at this item's first tile
-      g += max(in.n0, in.n1);
+      g += in.je - in.jb;
       const int r = in.blk * kItemRows + half * kHalfRows + row_in_half;  // local row
-      if (half == 1 && in.n1 == 0 && in.blk * kItemRows + kHalfRows >= in.Lq) continue;
+      if (half == 1 && in.blk * kItemRows + kHalfRows >= in.Lq) continue;
       const bool row_valid = r < in.Lq;
+      // visible key columns of this row: [col_lo, col_lim)
+      const int col_lo = band_key_begin(r, p.window);
+      const int col_lim = band_key_end(r, p.causal, p.window, in.Lkv);
       const bool has_bias = p.bias_table != nullptr;
       float m = -INFINITY;  // running max (log2 units), possibly stale
       float l = 0.0f;       // running sum relative to m
       bool abort_now = false;
-      for (int j = 0; j < nh; ++j) {
-        const uint32_t gj = g_item + j;
+      for (int j = j_lo; j < j_hi; ++j) {
+        const uint32_t gj = g_item + (j - in.jb);
         bool okw = mbar_wait(bar(C::kSFull + half), tcount & 1u, abort_flag);
         // the value-tile stage also carries this tile's bias window
         if (has_bias)
@@ -453,8 +471,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         ++tcount;
         tc_fence_after();
         const int c0 = j * kKvRows;
-        const bool need_mask = (c0 + kKvRows > in.Lkv) || (p.causal && c0 + kKvRows - 1 > r);
-        const int col_lim = p.causal ? min(in.Lkv, r + 1) : in.Lkv;  // valid cols: c < col_lim
+        const bool need_mask = (c0 < col_lo) || (c0 + kKvRows > col_lim);
         // Scores need only the scale when no row of the warp needs a mask and there
         // is no bias.  Decided per warp: the tcgen05.ld below is .sync.aligned, so
         // the lanes of a warp must not split between the two paths.
@@ -489,8 +506,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
           }
           if (need_mask) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c0 + chunk * 32 + i >= col_lim) x[i] = fill;
+            for (int i = 0; i < 32; ++i) {
+              const int c = c0 + chunk * 32 + i;
+              if (c < col_lo || c >= col_lim) x[i] = fill;
+            }
           }
         };
         if (kSoftmax) {

@@ -146,7 +146,14 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
 struct ItemInfo {
   int b, head, blk;
   int q0, k0, Lq, Lkv;
-  int n0, n1;
+  // Key tiles visited: half h covers [lo_h, hi_h); the item streams their
+  // (contiguous) union [jb, je).
+  int lo0, hi0, lo1, hi1;
+  int jb, je;
+  __device__ __forceinline__ int lo(int h) const { return h ? lo1 : lo0; }
+  __device__ __forceinline__ int hi(int h) const { return h ? hi1 : hi0; }
+  __device__ __forceinline__ bool visits(int h, int j) const { return j >= lo(h) && j < hi(h); }
+  __device__ __forceinline__ bool has_half1() const { return hi1 > lo1; }
 };
 
 __device__ __forceinline__ ItemInfo decode_item(int2 it, const FwdParams& p) {
@@ -158,16 +165,15 @@ __device__ __forceinline__ ItemInfo decode_item(int2 it, const FwdParams& p) {
   r.Lq = p.qo[r.b + 1] - r.q0;
   r.k0 = p.ko[r.b];
   r.Lkv = p.ko[r.b + 1] - r.k0;
-  const int nkv = (r.Lkv + kTile - 1) / kTile;
   const int r0 = r.blk * kItemRows;
-  const bool h1 = r0 + kHalfRows < r.Lq;
-  if (!p.causal) {
-    r.n0 = nkv;
-    r.n1 = h1 ? nkv : 0;
-  } else {
-    r.n0 = min(nkv, (min(r.Lq, r0 + kHalfRows) + kTile - 1) / kTile);
-    r.n1 = h1 ? min(nkv, (min(r.Lq, r0 + kItemRows) + kTile - 1) / kTile) : 0;
-  }
+  band_key_tiles(r0, min(r.Lq, r0 + kHalfRows), p.causal, p.window, r.Lkv, kTile, &r.lo0, &r.hi0);
+  if (r0 + kHalfRows < r.Lq)
+    band_key_tiles(r0 + kHalfRows, min(r.Lq, r0 + kItemRows), p.causal, p.window, r.Lkv, kTile,
+                   &r.lo1, &r.hi1);
+  else
+    r.lo1 = r.hi1 = r.hi0;
+  r.jb = r.lo0;
+  r.je = max(r.hi0, r.hi1);
   return r;
 }
 
@@ -256,14 +262,15 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       ++it;
       if (item.x < 0) break;
       const ItemInfo in = decode_item(item, p);
-      const int n = max(in.n0, in.n1);
+      const int n = in.je - in.jb;
       if (n == 0) continue;
       w = mbar_wait(bar(C::kQEmpty), (qi & 1u) ^ 1u, abort_flag);
       if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
       const int row0 = in.q0 + in.blk * kItemRows;
+      const int n_halves = in.has_half1() ? 2 : 1;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(C::kQFull), (in.n1 > 0 ? 2 : 1) * C::kQHalfBytes);
-        for (int half = 0; half < (in.n1 > 0 ? 2 : 1); ++half)
+        mbar_arrive_expect_tx(bar(C::kQFull), n_halves * C::kQHalfBytes);
+        for (int half = 0; half < n_halves; ++half)
           tma_load_3d(sbase + (half ? C::kQ1 : C::kQ0), &tmap_q, bar(C::kQFull), 0, in.head,
                       row0 + half * kHalfRows);
         q_inflight = true;
@@ -271,7 +278,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       ++qi;
       const float* brow =
           p.bias_table ? p.bias_table + static_cast<long long>(in.head) * rel_w : nullptr;
-      for (int j = 0; j < n; ++j, ++g) {
+      for (int j = in.jb; j < in.je; ++j, ++g) {
         const uint32_t s = g % kStages;
         const uint32_t ph = (g / kStages) & 1u;
         const uint32_t kdst = sbase + C::kKV + s * 2 * C::kTileBytes;
@@ -333,7 +340,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       ++it;
       if (item.x < 0) break;
       const ItemInfo in = decode_item(item, p);
-      const int n = max(in.n0, in.n1);
+      const int n = in.je - in.jb;
       if (n == 0) continue;
       // Q scale words of both halves: the previous item's score products must be done
       w = mbar_wait(bar(C::kQEmpty), (qi & 1u) ^ 1u, abort_flag);
@@ -356,7 +363,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       const long long vrow0 = static_cast<long long>(in.b) + in.k0 / 32;  // first scale row of the sample
       const int nblk = (in.Lkv + 31) / 32;
       bool abort_now = false;
-      for (int j = 0; j < n; ++j, ++g) {
+      for (int j = in.jb; j < in.je; ++j, ++g) {
         const uint32_t s = g % kStages;
         const uint32_t ph = (g / kStages) & 1u;
         // both scale columns of stage s are free once that stage's value products are done
@@ -429,47 +436,48 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         ++it;
         if (item.x < 0) break;
         const ItemInfo in = decode_item(item, p);
-        const int n = max(in.n0, in.n1);
+        const int n = in.je - in.jb;
         if (n == 0) continue;
         if (!mbar_wait(bar(C::kQFull), qi & 1u, abort_flag)) { fail(); break; }
         if (!mbar_wait(bar(C::kSfqFull), qi & 1u, abort_flag)) { fail(); break; }
         ++qi;
         tc_fence_after();
-        const int last_s_half = (in.n1 == n) ? 1 : 0;
+        const int last_s_half = in.visits(1, in.je - 1) ? 1 : 0;
         {
           const uint32_t s = g % kStages;
           const uint32_t ph = (g / kStages) & 1u;
           if (!mbar_wait(bar(C::kKFull + s), ph, abort_flag)) { fail(); break; }
           if (!mbar_wait(bar(C::kSfkvFull + s), ph, abort_flag)) { fail(); break; }
           tc_fence_after();
-          if (in.n0 > 0) issue_s(0, s);
-          if (in.n1 > 0) issue_s(1, s);
+          if (in.visits(0, in.jb)) issue_s(0, s);
+          if (in.visits(1, in.jb)) issue_s(1, s);
           mma_commit(bar(C::kKEmpty + s));
           if (n == 1) mma_commit(bar(C::kQEmpty));
         }
-        for (int j = 0; j < n; ++j) {
-          const uint32_t gj = g + j;
+        for (int j = in.jb; j < in.je; ++j) {
+          const uint32_t gj = g + (j - in.jb);
           const uint32_t s = gj % kStages;
           const uint32_t s_next = (gj + 1) % kStages;
           const uint32_t ph_next = ((gj + 1) / kStages) & 1u;
           if (!mbar_wait(bar(C::kVFull + s), (gj / kStages) & 1u, abort_flag)) { ok = false; fail(); break; }
-          const int last_half_j = (j < in.n1) ? 1 : 0;
+          const int last_half_j = in.visits(1, j) ? 1 : 0;
+          const int last_half_next = in.visits(1, j + 1) ? 1 : 0;
           for (int half = 0; half < 2; ++half) {
-            const int nh = half ? in.n1 : in.n0;
-            if (j >= nh) continue;
-            if (!mbar_wait(bar(C::kPFull + half), tcount[half] & 1u, abort_flag)) { ok = false; fail(); break; }
-            ++tcount[half];
-            tc_fence_after();
-            issue_pv(half, s, j == 0);
-            if (j == nh - 1) mma_commit(bar(C::kODone + half));
-            if (half == last_half_j) mma_commit(bar(C::kVEmpty + s));
-            if (j + 1 < nh) {
+            if (in.visits(half, j)) {
+              if (!mbar_wait(bar(C::kPFull + half), tcount[half] & 1u, abort_flag)) { ok = false; fail(); break; }
+              ++tcount[half];
+              tc_fence_after();
+              issue_pv(half, s, j == in.lo(half));
+              if (j == in.hi(half) - 1) mma_commit(bar(C::kODone + half));
+              if (half == last_half_j) mma_commit(bar(C::kVEmpty + s));
+            }
+            if (in.visits(half, j + 1)) {
               if (!mbar_wait(bar(C::kKFull + s_next), ph_next, abort_flag) ||
                   !mbar_wait(bar(C::kSfkvFull + s_next), ph_next, abort_flag)) { ok = false; fail(); break; }
               tc_fence_after();
               issue_s(half, s_next);
-              if (half == ((j + 1 < in.n1) ? 1 : 0)) mma_commit(bar(C::kKEmpty + s_next));
-              if (j + 1 == n - 1 && half == last_s_half) mma_commit(bar(C::kQEmpty));
+              if (half == last_half_next) mma_commit(bar(C::kKEmpty + s_next));
+              if (j + 1 == in.je - 1 && half == last_s_half) mma_commit(bar(C::kQEmpty));
             }
           }
           if (!ok) break;
@@ -503,17 +511,21 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       ++it;
       if (item.x < 0) break;
       const ItemInfo in = decode_item(item, p);
-      const int nh = half ? in.n1 : in.n0;
+      const int j_lo = in.lo(half), j_hi = in.hi(half);
+      const int nh = j_hi - j_lo;
       const uint32_t g_item = g;
-      g += max(in.n0, in.n1);
+      g += in.je - in.jb;
       const int r = in.blk * kItemRows + half * kHalfRows + row_in_half;
-      if (half == 1 && in.n1 == 0 && in.blk * kItemRows + kHalfRows >= in.Lq) continue;
+      if (half == 1 && in.blk * kItemRows + kHalfRows >= in.Lq) continue;
       const bool row_valid = r < in.Lq;
+      // visible key columns of this row: [col_lo, col_lim)
+      const int col_lo = band_key_begin(r, p.window);
+      const int col_lim = band_key_end(r, p.causal, p.window, in.Lkv);
       const bool has_bias = p.bias_table != nullptr;
       float m = -INFINITY, l = 0.0f;
       bool abort_now = false;
-      for (int j = 0; j < nh; ++j) {
-        const uint32_t gj = g_item + j;
+      for (int j = j_lo; j < j_hi; ++j) {
+        const uint32_t gj = g_item + (j - in.jb);
         bool okw = mbar_wait(bar(C::kSFull + half), tcount & 1u, abort_flag);
         if (has_bias)
           okw = okw && mbar_wait(bar(C::kVFull + gj % kStages), (gj / kStages) & 1u, abort_flag);
@@ -522,8 +534,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         ++tcount;
         tc_fence_after();
         const int c0 = j * kTile;
-        const bool need_mask = (c0 + kTile > in.Lkv) || (p.causal && c0 + kTile - 1 > r);
-        const int col_lim = p.causal ? min(in.Lkv, r + 1) : in.Lkv;
+        const bool need_mask = (c0 < col_lo) || (c0 + kTile > col_lim);
         // bwin[cc] = bias(row, tile column cc) * log2e, from the window copy in
         // which this row's entries start 8-byte aligned
         const int cp = (row_in_half + 1) & 1;
@@ -547,8 +558,10 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           }
           if (need_mask) {
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
-              if (c0 + chunk * 32 + q >= col_lim) x[q] = -INFINITY;
+            for (int q = 0; q < 32; ++q) {
+              const int c = c0 + chunk * 32 + q;
+              if (c < col_lo || c >= col_lim) x[q] = -INFINITY;
+            }
           }
         };
         float mt = -INFINITY;

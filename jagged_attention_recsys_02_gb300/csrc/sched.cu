@@ -23,31 +23,37 @@ constexpr int kThreads = 1024;
 
 // mode 0 (forward): outer = queries in 256-row blocks, inner = key tiles of 128.
 // mode 1 (backward): outer = keys in 128-row blocks, inner = query tiles of 64.
-__device__ __forceinline__ int block_cost(int mode, int causal, int Lo, int Li, int blk) {
+// The cost counts only the inner tiles inside the causal / sliding-window
+// band (tiles outside it are skipped by the kernels), plus one for the
+// block's fixed work.
+__device__ __forceinline__ int block_cost(int mode, int causal, int window, int Lo, int Li,
+                                          int blk) {
+  int tb, te;
   if (mode == 0) {
-    const int nkv = (Li + kKvRows - 1) / kKvRows;
-    if (!causal) return nkv + 1;
-    const int row_end = min(Lo, (blk + 1) * kItemRows);
-    return min(nkv, (row_end + kKvRows - 1) / kKvRows) + 1;
+    band_key_tiles(blk * kItemRows, min(Lo, (blk + 1) * kItemRows), causal, window, Li, kKvRows,
+                   &tb, &te);
+  } else {
+    band_query_tiles(blk * kBwdKvRows, min(Lo, (blk + 1) * kBwdKvRows), causal, window, Li,
+                     kBwdQRows, &tb, &te);
   }
-  const int first_q = causal ? blk * kBwdKvRows : 0;
-  const int nq = (Li - first_q + kBwdQRows - 1) / kBwdQRows;
-  return max(nq, 0) + 1;
+  return te - tb + 1;
 }
 
 // Histogram bucket of a sample's total cost: exact below 1024 inner tiles,
 // then 64-tile steps (coarser ordering among very long samples is enough for
 // the longest-first schedule).
-__device__ __forceinline__ int sample_bucket(int mode, int causal, int Lo, int Li, int nblk) {
+__device__ __forceinline__ int sample_bucket(int mode, int causal, int window, int Lo, int Li,
+                                             int nblk) {
   long long total = 0;
-  for (int blk = 0; blk < nblk; ++blk) total += block_cost(mode, causal, Lo, Li, blk);
+  for (int blk = 0; blk < nblk; ++blk) total += block_cost(mode, causal, window, Lo, Li, blk);
   const long long b = total < 1024 ? total : 1024 + (total - 1024) / 64;
   return static_cast<int>(b < kCostBuckets - 1 ? b : kCostBuckets - 1);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __restrict__ inner_off,
-                      int B, int H, long long T_outer, long long T_inner, int causal, int mode,
+                      int B, int H, long long T_outer, long long T_inner, int causal, int window,
+                      int mode,
                       int2* __restrict__ items, int* __restrict__ n_items,
                       int* __restrict__ ticket, int* __restrict__ status) {
   __shared__ int hist[kCostBuckets];
@@ -65,12 +71,12 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
   for (int b = tid; b < B; b += kThreads) {
     const int Lo = outer_off[b + 1] - outer_off[b];
     const int Li = inner_off[b + 1] - inner_off[b];
-    if (Lo < 0 || Li < 0 || (causal && Lo != Li)) {
+    if (Lo < 0 || Li < 0 || ((causal || window > 0) && Lo != Li)) {
       bad = 1;
       continue;
     }
     const int nblk = (Lo + block_rows - 1) / block_rows;
-    if (nblk > 0) atomicAdd(&hist[sample_bucket(mode, causal, Lo, Li, nblk)], nblk);
+    if (nblk > 0) atomicAdd(&hist[sample_bucket(mode, causal, window, Lo, Li, nblk)], nblk);
   }
   __syncthreads();
   if (bad) {
@@ -114,9 +120,10 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
     const int Li = inner_off[b + 1] - inner_off[b];
     const int nblk = (Lo + block_rows - 1) / block_rows;
     if (nblk == 0) continue;
-    const int pos = atomicAdd(&base[sample_bucket(mode, causal, Lo, Li, nblk)], nblk);
+    const int pos = atomicAdd(&base[sample_bucket(mode, causal, window, Lo, Li, nblk)], nblk);
     // Blocks in descending cost: under the causal mask the forward's last
-    // query blocks and the backward's first key blocks visit the most tiles.
+    // query blocks and the backward's first key blocks visit the most tiles
+    // (a sliding window makes the costs nearly flat; the order stays).
     for (int r = 0; r < nblk; ++r) {
       const int blk = (causal && mode == 0) ? nblk - 1 - r : r;
       for (int h = 0; h < H; ++h)
@@ -132,11 +139,12 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
 }  // namespace
 
 cudaError_t launch_build_worklist(const int32_t* outer_off, const int32_t* inner_off, int B, int H,
-                                  int64_t T_outer, int64_t T_inner, int causal, int mode,
-                                  int2* items, int* n_items, int* ticket, int* status,
+                                  int64_t T_outer, int64_t T_inner, int causal, int window,
+                                  int mode, int2* items, int* n_items, int* ticket, int* status,
                                   cudaStream_t stream) {
   build_worklist_kernel<<<1, kThreads, 0, stream>>>(outer_off, inner_off, B, H, T_outer, T_inner,
-                                                    causal, mode, items, n_items, ticket, status);
+                                                    causal, window, mode, items, n_items, ticket,
+                                                    status);
   return cudaGetLastError();
 }
 

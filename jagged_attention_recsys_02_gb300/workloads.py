@@ -18,6 +18,10 @@ sparsity 0.5; these workloads stand in for that traffic:
                      d=128, SiLU (queries expanded to [B*32, H, d])
   heavy_tail         B=1024, L=round(exp(N(ln 1024, 1))) clipped to [16,16384],
                      H=4, d=128, softmax or SiLU
+  swa_causal_relpos  sliding-window self-attention over long sequences ("GEM
+                     Training ..." SWA paragraph): B=64, L~U[1,16384], H=4,
+                     d=128, softmax, causal, window 1024, relative-position
+                     bias table [H, 2047] ~ N(0, 0.02)
 """
 from __future__ import annotations
 
@@ -30,6 +34,7 @@ import torch
 ACTS = {"softmax": 0, "silu": 1, "gelu_tanh": 2, "identity": 3}
 
 CONFIG_NAMES = ("tiny_silu", "jfa_causal_relpos", "gdpa_cross_gelu", "gdpa_pma_silu", "heavy_tail")
+EXTRA_NAMES = ("swa_causal_relpos",)
 
 
 @dataclass
@@ -44,6 +49,7 @@ class Workload:
     lkv: np.ndarray           # int64 [B]
     max_rel: int = 0          # >0: relative-position bias table [H, 2*max_rel-1]
     pma_seeds: int = 0        # >0: queries are this many seeds shared by all samples
+    window: int = 0           # >0: sliding window, pairs with |i - j| < window
     scale: float = 0.0
     extra: dict = field(default_factory=dict)
 
@@ -62,11 +68,22 @@ class Workload:
         ko[1:] = np.cumsum(self.lkv)
         return qo, ko
 
+    def sample_pairs(self) -> np.ndarray:
+        """Per-sample query-key pairs that are not masked (int64 [B])."""
+        L, W = self.lq, self.window
+        if W <= 0:
+            return self.lq * (self.lq + 1) // 2 if self.causal else self.lq * self.lkv
+        # causal window: row i sees min(i + 1, W) keys
+        m = np.minimum(L, W)
+        causal = m * (m + 1) // 2 + (L - m) * W
+        if self.causal:
+            return causal
+        # symmetric window: add the keys ahead of each row, min(L - 1 - i, W - 1)
+        return causal + causal - L
+
     def pairs(self) -> int:
         """Query-key pairs that are not masked (the non-padded work)."""
-        if self.causal:
-            return int(np.sum(self.lq * (self.lq + 1) // 2))
-        return int(np.sum(self.lq * self.lkv))
+        return int(np.sum(self.sample_pairs()))
 
     def full_pairs(self) -> int:
         return int(np.sum(self.lq * self.lkv))
@@ -95,6 +112,10 @@ def make_workload(name: str, seed: int = 0, act: str | None = None) -> Workload:
         x = np.exp(rng.normal(math.log(1024.0), 1.0, size=1024))
         L = np.clip(np.round(x), 16, 16384).astype(np.int64)
         w = Workload(name, 1024, 4, 128, "softmax", False, L.copy(), L.copy())
+    elif name == "swa_causal_relpos":
+        L = rng.integers(1, 16384, size=64, endpoint=True).astype(np.int64)
+        w = Workload(name, 64, 4, 128, "softmax", True, L.copy(), L.copy(), max_rel=1024,
+                     window=1024)
     else:
         raise KeyError(name)
     if act is not None:
@@ -103,10 +124,11 @@ def make_workload(name: str, seed: int = 0, act: str | None = None) -> Workload:
     return w
 
 
-def custom_workload(lq, lkv, H, d, act="softmax", causal=False, max_rel=0, name="custom"):
+def custom_workload(lq, lkv, H, d, act="softmax", causal=False, max_rel=0, name="custom",
+                    window=0):
     lq = np.asarray(lq, dtype=np.int64)
     lkv = np.asarray(lkv, dtype=np.int64)
-    w = Workload(name, len(lq), H, d, act, causal, lq, lkv, max_rel=max_rel)
+    w = Workload(name, len(lq), H, d, act, causal, lq, lkv, max_rel=max_rel, window=window)
     w.scale = 1.0 / math.sqrt(d)
     return w
 

@@ -63,13 +63,13 @@ def assert_close(got, ref, tol, what):
     return float((err / bound).max()) if err.size else 0.0
 
 
-def run_fwd(q, qo, k, v, ko, act, causal, scale, bias=None, max_rel=0, guard=3):
+def run_fwd(q, qo, k, v, ko, act, causal, scale, bias=None, max_rel=0, guard=3, window=0):
     Tq, H, d = q.shape
     buf, out = guarded(Tq, H, d, q.device, guard)
     a = ACTS[act] if isinstance(act, str) else act
     lse = torch.full((H, Tq), float("nan"), device=q.device) if a == 0 else None
     binding.gdpa_fwd(q, qo, k, v, ko, act=a, causal=causal, scale=scale, bias=bias,
-                     max_rel=max_rel, out=out, lse=lse)
+                     max_rel=max_rel, window=window, out=out, lse=lse)
     st = binding.device_status()
     assert st == 0, f"device status {st}"
     check_guards(buf, guard)
@@ -77,7 +77,7 @@ def run_fwd(q, qo, k, v, ko, act, causal, scale, bias=None, max_rel=0, guard=3):
 
 
 def oracle_fwd_samples(q, k, v, qo, ko, samples, act, causal, scale, bias=None, max_rel=0,
-                       rows=None):
+                       rows=None, window=0):
     """Oracle forward on a subset of samples (and optionally a subset of query
     rows per sample: rows[b] = array of local row indices; only for
     non-causal, bias-free problems, where rows are position-independent).
@@ -99,7 +99,7 @@ def oracle_fwd_samples(q, k, v, qo, ko, samples, act, causal, scale, bias=None, 
             glob = np.arange(q0, q1)
         o, l = oracle.fwd(qs, np.array([0, len(qs)], dtype=np.int32), k[k0:k1], v[k0:k1],
                           np.array([0, k1 - k0], dtype=np.int32), act=a, causal=causal,
-                          scale=scale, bias=bias, max_rel=max_rel)
+                          scale=scale, bias=bias, max_rel=max_rel, window=window)
         res.append((glob, o, l))
     return res
 

@@ -123,3 +123,29 @@ def test_empty_problem_is_a_no_op(lib):
     assert _fwd(lib, B=0, Tq=0, Tkv=0) == OK
     assert _fwd(lib, Tq=0) == OK
     assert _bwd(lib, B=0, Tq=0, Tkv=0) == OK
+
+
+def test_window_entry_points_reject_on_host(lib):
+    """gdpa_fwd_window / gdpa_bwd_window: a negative window is an argument
+    error; the other checks are those of gdpa_fwd / gdpa_bwd."""
+    def fwd_w(window, **kw):
+        a = dict(q=FAKE, qo=FAKE, k=FAKE, v=FAKE, ko=FAKE, d=64, ws=FAKE)
+        a.update(kw)
+        return lib.gdpa_fwd_window(a["q"], a["qo"], a["k"], a["v"], a["ko"], 2, 2, a["d"], 10, 10,
+                                   None, 0, 1, window, 0.125, FAKE, FAKE, a["ws"], 1 << 20, None)
+
+    def bwd_w(window, **kw):
+        a = dict(d=64)
+        a.update(kw)
+        return lib.gdpa_bwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, a["d"], 10, 10, None, 0, 1,
+                                   window, 0.125, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                   1 << 20, None)
+
+    for call in (fwd_w, bwd_w):
+        assert call(-1) == INVALID
+        assert call(5, d=96) == UNSUPPORTED
+    assert fwd_w(5, q=None) == INVALID
+    assert fwd_w(5, ws=None) == WORKSPACE
+    mx = lib.gdpa_fwd_mxfp8_window(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 10,
+                                   10, None, 0, 1, -3, 0.125, FAKE, FAKE, FAKE, 1 << 20, None)
+    assert mx == INVALID

@@ -9,9 +9,29 @@ import numpy as np
 import pytest
 import torch
 
-from jagged_attention_recsys_02_gb300.workloads import CONFIG_NAMES, make_tensors, make_workload
+from jagged_attention_recsys_02_gb300.workloads import (CONFIG_NAMES, custom_workload, make_tensors,
+                                                        make_workload)
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_pair_counts_match_the_mask(causal):
+    """Non-padded pair counts of sliding-window workloads (the FLOP count of
+    every windowed measurement) equal the number of kept entries of the band
+    mask |i - j| < W (and j <= i when causal), counted by brute force."""
+    lengths = [0, 1, 2, 5, 64, 129, 300]
+    for W in (1, 2, 7, 128, 400):
+        w = custom_workload(lengths, lengths, 1, 64, causal=causal, window=W)
+        for L, got in zip(lengths, w.sample_pairs()):
+            i, j = np.arange(L)[:, None], np.arange(L)[None, :]
+            keep = np.abs(i - j) < W
+            if causal:
+                keep &= j <= i
+            assert got == keep.sum(), (L, W, causal)
+    w = make_workload("swa_causal_relpos")
+    assert w.window == 1024 and w.causal and w.max_rel == 1024 and w.B == 64
+    assert w.pairs() < int(np.sum(w.lq * (w.lq + 1) // 2))
 
 
 def test_workload_recipes():

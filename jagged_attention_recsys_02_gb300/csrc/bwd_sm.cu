@@ -117,6 +117,9 @@ struct SmItem {
   int nq;   // number of query tiles visited
 };
 
+// kBand: a sliding window is set; without one the query range is the
+// plain causal / full one.
+template <bool kBand>
 __device__ __forceinline__ SmItem decode_sm(int2 it, const BwdParams& p) {
   SmItem r;
   r.b = it.x;
@@ -129,15 +132,21 @@ __device__ __forceinline__ SmItem decode_sm(int2 it, const BwdParams& p) {
   // query tiles that see some key of the block (causal / sliding-window band)
   // (items exist only for blocks that start inside the sample, and every
   // such key is seen by some query unless the sample has no query rows)
-  const int kb0 = r.kb * kKRows;
-  const int qb = band_query_begin(kb0, p.causal, p.window);
-  const int qe = band_query_end(min(r.Lkv, kb0 + kKRows) - 1, p.window, r.Lq);
-  r.qt0 = qb / kQRows;
-  r.nq = (qe + kQRows - 1) / kQRows - r.qt0;  // 0 when qe == qb == 0 (no query rows)
+  if (kBand) {
+    const int kb0 = r.kb * kKRows;
+    const int qb = band_query_begin(kb0, p.causal, p.window);
+    const int qe = band_query_end(min(r.Lkv, kb0 + kKRows) - 1, p.window, r.Lq);
+    r.qt0 = qb / kQRows;
+    r.nq = (qe + kQRows - 1) / kQRows - r.qt0;  // 0 when qe == qb == 0 (no query rows)
+  } else {
+    r.qt0 = p.causal ? r.kb : 0;  // queries before the block's first key see none of it
+    const int rows = r.Lq - r.qt0 * kQRows;
+    r.nq = rows > 0 ? (rows + kQRows - 1) / kQRows : 0;
+  }
   return r;
 }
 
-template <int D>
+template <int D, bool kBand>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
               const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
@@ -228,7 +237,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       }
       ++it;
       if (item.x < 0) break;
-      const SmItem in = decode_sm(item, p);
+      const SmItem in = decode_sm<kBand>(item, p);
       if (in.nq == 0) continue;
       w = mbar_wait(bar(C::kKvEmpty), (kvi & 1u) ^ 1u, abort_flag);
       if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
@@ -395,7 +404,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         mbar_arrive(bar(C::kItemEmpty + slot));
         ++it;
         if (item.x < 0) break;
-        const SmItem in = decode_sm(item, p);
+        const SmItem in = decode_sm<kBand>(item, p);
         if (in.nq == 0) continue;
         if (!mbar_wait(bar(C::kKvFull), kvi & 1u, abort_flag)) { fail(); break; }
         ++kvi;
@@ -479,7 +488,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       warp_arrive(bar(C::kItemEmpty + slot), lane);
       ++it;
       if (item.x < 0) break;
-      const SmItem in = decode_sm(item, p);
+      const SmItem in = decode_sm<kBand>(item, p);
       const int kb0 = in.kb * kKRows;   // first local key row of the block
       const int jl = kb0 + j;           // this thread's local key row
       // queries that see this key: [vis_lo, vis_hi) (none for a key past the sample)
@@ -625,7 +634,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       warp_arrive(bar(C::kItemEmpty + slot), lane);
       ++it;
       if (item.x < 0) break;
-      const SmItem in = decode_sm(item, p);
+      const SmItem in = decode_sm<kBand>(item, p);
       bool abort_now = false;
       for (int t = 0; t < in.nq; ++t) {
         w = mbar_wait(bar(C::kDqFull), dqc & 1u, abort_flag);
@@ -727,16 +736,16 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   }
 }
 
-template <int D>
+template <int D, bool kBand>
 cudaError_t launch_sm(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                       int grid, cudaStream_t s) {
   using C = SmCfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(bwd_sm_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(bwd_sm_kernel<D, kBand>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  bwd_sm_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, tdq, p);
+  bwd_sm_kernel<D, kBand><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
 
@@ -745,8 +754,11 @@ cudaError_t launch_sm(const BwdParams& p, const CUtensorMap& tq, const CUtensorM
 cudaError_t launch_bwd_softmax_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                                     const CUtensorMap& tv, const CUtensorMap& tdo,
                                     const CUtensorMap& tdq, int grid, cudaStream_t s) {
-  return p.d == 64 ? launch_sm<64>(p, tq, tk, tv, tdo, tdq, grid, s)
-                   : launch_sm<128>(p, tq, tk, tv, tdo, tdq, grid, s);
+  if (p.window > 0)
+    return p.d == 64 ? launch_sm<64, true>(p, tq, tk, tv, tdo, tdq, grid, s)
+                     : launch_sm<128, true>(p, tq, tk, tv, tdo, tdq, grid, s);
+  return p.d == 64 ? launch_sm<64, false>(p, tq, tk, tv, tdo, tdq, grid, s)
+                   : launch_sm<128, false>(p, tq, tk, tv, tdo, tdq, grid, s);
 }
 
 }  // namespace gdpa

@@ -112,6 +112,9 @@ struct ItemInfo {
   __device__ __forceinline__ bool has_half1() const { return hi1 > lo1; }
 };
 
+// kBand: a sliding window is set (p.window > 0).  Without one every half
+// starts at key tile 0, which keeps the common path's arithmetic minimal.
+template <bool kBand>
 __device__ __forceinline__ ItemInfo decode_item(int2 it, const FwdParams& p) {
   ItemInfo r;
   r.b = it.x;
@@ -122,13 +125,26 @@ __device__ __forceinline__ ItemInfo decode_item(int2 it, const FwdParams& p) {
   r.k0 = p.ko[r.b];
   r.Lkv = p.ko[r.b + 1] - r.k0;
   const int r0 = r.blk * kItemRows;
-  band_key_tiles(r0, min(r.Lq, r0 + kHalfRows), p.causal, p.window, r.Lkv, kKvRows, &r.lo0,
-                 &r.hi0);
-  if (r0 + kHalfRows < r.Lq)
-    band_key_tiles(r0 + kHalfRows, min(r.Lq, r0 + kItemRows), p.causal, p.window, r.Lkv, kKvRows,
-                   &r.lo1, &r.hi1);
-  else
-    r.lo1 = r.hi1 = r.hi0;
+  if (kBand) {
+    band_key_tiles(r0, min(r.Lq, r0 + kHalfRows), p.causal, p.window, r.Lkv, kKvRows, &r.lo0,
+                   &r.hi0);
+    if (r0 + kHalfRows < r.Lq)
+      band_key_tiles(r0 + kHalfRows, min(r.Lq, r0 + kItemRows), p.causal, p.window, r.Lkv,
+                     kKvRows, &r.lo1, &r.hi1);
+    else
+      r.lo1 = r.hi1 = r.hi0;
+  } else {
+    const int nkv = (r.Lkv + kKvRows - 1) / kKvRows;
+    const bool h1 = r0 + kHalfRows < r.Lq;
+    r.lo0 = r.lo1 = 0;
+    if (!p.causal) {
+      r.hi0 = nkv;
+      r.hi1 = h1 ? nkv : 0;
+    } else {
+      r.hi0 = min(nkv, (min(r.Lq, r0 + kHalfRows) + kKvRows - 1) / kKvRows);
+      r.hi1 = h1 ? min(nkv, (min(r.Lq, r0 + kItemRows) + kKvRows - 1) / kKvRows) : 0;
+    }
+  }
   // Half 0 starts no later and half 1 ends no earlier; with half 0 empty
   // (no key at all) both are.
   r.jb = r.lo0;
@@ -136,7 +152,7 @@ __device__ __forceinline__ ItemInfo decode_item(int2 it, const FwdParams& p) {
   return r;
 }
 
-template <int D, int ACT>
+template <int D, int ACT, bool kBand>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
            const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
@@ -224,7 +240,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       }
       ++it;
       if (item.x < 0) break;
-      const ItemInfo in = decode_item(item, p);
+      const ItemInfo in = decode_item<kBand>(item, p);
       const int n = in.je - in.jb;
       if (n == 0) continue;
       w = mbar_wait(bar(C::kQEmpty), (qi & 1u) ^ 1u, abort_flag);
@@ -370,7 +386,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         mbar_arrive(bar(C::kItemEmpty + slot));
         ++it;
         if (item.x < 0) break;
-        const ItemInfo in = decode_item(item, p);
+        const ItemInfo in = decode_item<kBand>(item, p);
         const int n = in.je - in.jb;
         if (n == 0) continue;
         if (!mbar_wait(bar(C::kQFull), qi & 1u, abort_flag)) { fail(); break; }
@@ -445,7 +461,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       mbar_arrive(bar(C::kItemEmpty + slot));
       ++it;
       if (item.x < 0) break;
-      const ItemInfo in = decode_item(item, p);
+      const ItemInfo in = decode_item<kBand>(item, p);
       const int j_lo = in.lo(half), j_hi = in.hi(half);
       const int nh = j_hi - j_lo;
       const uint32_t g_item = g;  // key-tile counter at this item's first tile
@@ -454,8 +470,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       if (half == 1 && in.blk * kItemRows + kHalfRows >= in.Lq) continue;
       const bool row_valid = r < in.Lq;
       // visible key columns of this row: [col_lo, col_lim)
-      const int col_lo = band_key_begin(r, p.window);
-      const int col_lim = band_key_end(r, p.causal, p.window, in.Lkv);
+      const int col_lo = kBand ? band_key_begin(r, p.window) : 0;
+      const int col_lim = kBand ? band_key_end(r, p.causal, p.window, in.Lkv)
+                                : (p.causal ? min(in.Lkv, r + 1) : in.Lkv);
       const bool has_bias = p.bias_table != nullptr;
       float m = -INFINITY;  // running max (log2 units), possibly stale
       float l = 0.0f;       // running sum relative to m
@@ -471,7 +488,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         ++tcount;
         tc_fence_after();
         const int c0 = j * kKvRows;
-        const bool need_mask = (c0 < col_lo) || (c0 + kKvRows > col_lim);
+        const bool need_mask = (kBand && c0 < col_lo) || (c0 + kKvRows > col_lim);
         // Scores need only the scale when no row of the warp needs a mask and there
         // is no bias.  Decided per warp: the tcgen05.ld below is .sync.aligned, so
         // the lanes of a warp must not split between the two paths.
@@ -508,7 +525,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int c = c0 + chunk * 32 + i;
-              if (c < col_lo || c >= col_lim) x[i] = fill;
+              if ((kBand && c < col_lo) || c >= col_lim) x[i] = fill;
             }
           }
         };
@@ -652,25 +669,27 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
   }
 }
 
-template <int D, int ACT>
+template <int D, int ACT, bool kBand>
 cudaError_t launch_one(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, int grid, cudaStream_t stream) {
   const int smem = FwdCfg<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, ACT>,
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, ACT, kBand>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  fwd_kernel<D, ACT><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  fwd_kernel<D, ACT, kBand><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool kBand>
 cudaError_t launch_d(const FwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, int grid, cudaStream_t stream) {
   switch (act) {
-    case GDPA_ACT_SOFTMAX: return launch_one<D, GDPA_ACT_SOFTMAX>(p, tq, tk, tv, grid, stream);
-    case GDPA_ACT_SILU: return launch_one<D, GDPA_ACT_SILU>(p, tq, tk, tv, grid, stream);
-    case GDPA_ACT_GELU_TANH: return launch_one<D, GDPA_ACT_GELU_TANH>(p, tq, tk, tv, grid, stream);
-    default: return launch_one<D, GDPA_ACT_IDENTITY>(p, tq, tk, tv, grid, stream);
+    case GDPA_ACT_SOFTMAX:
+      return launch_one<D, GDPA_ACT_SOFTMAX, kBand>(p, tq, tk, tv, grid, stream);
+    case GDPA_ACT_SILU: return launch_one<D, GDPA_ACT_SILU, kBand>(p, tq, tk, tv, grid, stream);
+    case GDPA_ACT_GELU_TANH:
+      return launch_one<D, GDPA_ACT_GELU_TANH, kBand>(p, tq, tk, tv, grid, stream);
+    default: return launch_one<D, GDPA_ACT_IDENTITY, kBand>(p, tq, tk, tv, grid, stream);
   }
 }
 
@@ -680,8 +699,12 @@ int fwd_smem_bytes(int d) { return d == 64 ? FwdCfg<64>::kSmemBytes : FwdCfg<128
 
 cudaError_t launch_fwd(const FwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, int grid, cudaStream_t stream) {
-  if (p.d == 64) return launch_d<64>(p, act, tq, tk, tv, grid, stream);
-  return launch_d<128>(p, act, tq, tk, tv, grid, stream);
+  const bool band = p.window > 0;
+  if (p.d == 64)
+    return band ? launch_d<64, true>(p, act, tq, tk, tv, grid, stream)
+                : launch_d<64, false>(p, act, tq, tk, tv, grid, stream);
+  return band ? launch_d<128, true>(p, act, tq, tk, tv, grid, stream)
+              : launch_d<128, false>(p, act, tq, tk, tv, grid, stream);
 }
 
 }  // namespace gdpa

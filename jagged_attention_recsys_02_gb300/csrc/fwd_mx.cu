@@ -156,6 +156,8 @@ struct ItemInfo {
   __device__ __forceinline__ bool has_half1() const { return hi1 > lo1; }
 };
 
+// kBand: a sliding window is set (p.window > 0).
+template <bool kBand>
 __device__ __forceinline__ ItemInfo decode_item(int2 it, const FwdParams& p) {
   ItemInfo r;
   r.b = it.x;
@@ -166,17 +168,32 @@ __device__ __forceinline__ ItemInfo decode_item(int2 it, const FwdParams& p) {
   r.k0 = p.ko[r.b];
   r.Lkv = p.ko[r.b + 1] - r.k0;
   const int r0 = r.blk * kItemRows;
-  band_key_tiles(r0, min(r.Lq, r0 + kHalfRows), p.causal, p.window, r.Lkv, kTile, &r.lo0, &r.hi0);
-  if (r0 + kHalfRows < r.Lq)
-    band_key_tiles(r0 + kHalfRows, min(r.Lq, r0 + kItemRows), p.causal, p.window, r.Lkv, kTile,
-                   &r.lo1, &r.hi1);
-  else
-    r.lo1 = r.hi1 = r.hi0;
+  if (kBand) {
+    band_key_tiles(r0, min(r.Lq, r0 + kHalfRows), p.causal, p.window, r.Lkv, kTile, &r.lo0,
+                   &r.hi0);
+    if (r0 + kHalfRows < r.Lq)
+      band_key_tiles(r0 + kHalfRows, min(r.Lq, r0 + kItemRows), p.causal, p.window, r.Lkv, kTile,
+                     &r.lo1, &r.hi1);
+    else
+      r.lo1 = r.hi1 = r.hi0;
+  } else {
+    const int nkv = (r.Lkv + kTile - 1) / kTile;
+    const bool h1 = r0 + kHalfRows < r.Lq;
+    r.lo0 = r.lo1 = 0;
+    if (!p.causal) {
+      r.hi0 = nkv;
+      r.hi1 = h1 ? nkv : 0;
+    } else {
+      r.hi0 = min(nkv, (min(r.Lq, r0 + kHalfRows) + kTile - 1) / kTile);
+      r.hi1 = h1 ? min(nkv, (min(r.Lq, r0 + kItemRows) + kTile - 1) / kTile) : 0;
+    }
+  }
   r.jb = r.lo0;
   r.je = max(r.hi0, r.hi1);
   return r;
 }
 
+template <bool kBand>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
               const __grid_constant__ CUtensorMap tmap_v, const FwdParams p,
@@ -261,7 +278,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       }
       ++it;
       if (item.x < 0) break;
-      const ItemInfo in = decode_item(item, p);
+      const ItemInfo in = decode_item<kBand>(item, p);
       const int n = in.je - in.jb;
       if (n == 0) continue;
       w = mbar_wait(bar(C::kQEmpty), (qi & 1u) ^ 1u, abort_flag);
@@ -339,7 +356,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       mbar_arrive(bar(C::kItemEmpty + slot));
       ++it;
       if (item.x < 0) break;
-      const ItemInfo in = decode_item(item, p);
+      const ItemInfo in = decode_item<kBand>(item, p);
       const int n = in.je - in.jb;
       if (n == 0) continue;
       // Q scale words of both halves: the previous item's score products must be done
@@ -435,7 +452,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         mbar_arrive(bar(C::kItemEmpty + slot));
         ++it;
         if (item.x < 0) break;
-        const ItemInfo in = decode_item(item, p);
+        const ItemInfo in = decode_item<kBand>(item, p);
         const int n = in.je - in.jb;
         if (n == 0) continue;
         if (!mbar_wait(bar(C::kQFull), qi & 1u, abort_flag)) { fail(); break; }
@@ -510,7 +527,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       mbar_arrive(bar(C::kItemEmpty + slot));
       ++it;
       if (item.x < 0) break;
-      const ItemInfo in = decode_item(item, p);
+      const ItemInfo in = decode_item<kBand>(item, p);
       const int j_lo = in.lo(half), j_hi = in.hi(half);
       const int nh = j_hi - j_lo;
       const uint32_t g_item = g;
@@ -519,8 +536,9 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       if (half == 1 && in.blk * kItemRows + kHalfRows >= in.Lq) continue;
       const bool row_valid = r < in.Lq;
       // visible key columns of this row: [col_lo, col_lim)
-      const int col_lo = band_key_begin(r, p.window);
-      const int col_lim = band_key_end(r, p.causal, p.window, in.Lkv);
+      const int col_lo = kBand ? band_key_begin(r, p.window) : 0;
+      const int col_lim = kBand ? band_key_end(r, p.causal, p.window, in.Lkv)
+                                : (p.causal ? min(in.Lkv, r + 1) : in.Lkv);
       const bool has_bias = p.bias_table != nullptr;
       float m = -INFINITY, l = 0.0f;
       bool abort_now = false;
@@ -534,7 +552,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         ++tcount;
         tc_fence_after();
         const int c0 = j * kTile;
-        const bool need_mask = (c0 < col_lo) || (c0 + kTile > col_lim);
+        const bool need_mask = (kBand && c0 < col_lo) || (c0 + kTile > col_lim);
         // bwin[cc] = bias(row, tile column cc) * log2e, from the window copy in
         // which this row's entries start 8-byte aligned
         const int cp = (row_in_half + 1) & 1;
@@ -560,7 +578,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
               const int c = c0 + chunk * 32 + q;
-              if (c < col_lo || c >= col_lim) x[q] = -INFINITY;
+              if ((kBand && c < col_lo) || c >= col_lim) x[q] = -INFINITY;
             }
           }
         };
@@ -687,10 +705,11 @@ int fwd_mx_tile_rows() { return kTile; }
 cudaError_t launch_fwd_mx(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
                           const uint8_t* v_sc, long long v_sc_rows, int grid, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(fwd_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kernel = p.window > 0 ? fwd_mx_kernel<true> : fwd_mx_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
-  fwd_mx_kernel<<<grid, kThreads, Cfg::kSmemBytes, s>>>(tq, tk, tv, p, q_sc, k_sc, v_sc, v_sc_rows);
+  kernel<<<grid, kThreads, Cfg::kSmemBytes, s>>>(tq, tk, tv, p, q_sc, k_sc, v_sc, v_sc_rows);
   return cudaGetLastError();
 }
 

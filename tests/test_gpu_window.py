@@ -100,7 +100,11 @@ def test_window_bwd_parity(d, act, causal, window):
 @pytest.mark.parametrize("causal", [True, False])
 def test_window_as_long_as_the_samples_is_bit_identical(act, causal):
     """A window no shorter than every sample masks nothing: the kernels must
-    visit the same tiles with the same masks and give bit-identical results."""
+    visit the same tiles with the same masks and give bit-identical out, lse,
+    dK and dV.  dQ sums the key blocks' contributions in whatever order the
+    CTAs reach the fp32 accumulator, so two runs agree only up to that order:
+    within a bf16 rounding step of the value plus fp32 rounding of partial
+    sums that cancel (bounded here by 1e-4 of the tensor's largest entry)."""
     H, d = 2, 128
     q, k, v, do, o, od, bias = _inputs(LENGTHS, H, d, 0, seed=3)
     a, scale = ACTS[act], 1.0 / math.sqrt(d)
@@ -112,10 +116,17 @@ def test_window_as_long_as_the_samples_is_bit_identical(act, causal):
         grads = binding.gdpa_bwd(q, od, k, v, od, out, lse, do, act=a, causal=causal, scale=scale,
                                  window=window)
         assert binding.device_status() == 0
-        res.append([out, *grads] + ([lse] if lse is not None else []))
-    for x, y in zip(*res):
-        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x,
-                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y)
+        res.append(dict(out=out, lse=lse, dq=grads[0], dk=grads[1], dv=grads[2]))
+    for name in ("out", "lse", "dk", "dv"):
+        x, y = res[0][name], res[1][name]
+        if x is None:
+            continue
+        if x.dtype == torch.bfloat16:
+            x, y = x.view(torch.int16), y.view(torch.int16)
+        assert torch.equal(x, y), name
+    x, y = res[0]["dq"].float(), res[1]["dq"].float()
+    tol = 2.0 ** -7 * torch.maximum(x.abs(), y.abs()) + 1e-4 * x.abs().max()
+    assert torch.all((x - y).abs() <= tol), "dq"
 
 
 def test_window_needs_equal_lengths():

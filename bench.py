@@ -382,7 +382,8 @@ def run_gpu(args, rank, world, local_rank):
     import torch.distributed as dist
 
     from jagged_attention_recsys_02_gb300 import binding
-    from jagged_attention_recsys_02_gb300.workloads import ACTS, make_tensors, make_workload
+    from jagged_attention_recsys_02_gb300.workloads import (ACTS, first_samples, make_tensors,
+                                                            make_workload)
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -390,6 +391,8 @@ def run_gpu(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
     binding.load()
     w = make_workload(args.workload, act=args.act)
+    if args.samples:
+        w = first_samples(w, args.samples)
     t = make_tensors(w, device=dev, seed=rank)
     a = ACTS[w.act]
     H, d, Tq, Tkv = w.H, w.d, w.Tq, w.Tkv
@@ -713,6 +716,9 @@ def main():
     ap.add_argument("--workload", default=None,
                     help="default: jfa_causal_relpos (heavy_tail with --mxfp8)")
     ap.add_argument("--act", default=None, help="override the workload's activation")
+    ap.add_argument("--samples", type=int, default=0,
+                    help="keep only the workload's first N samples (small profiler captures; "
+                         "not a benchmark configuration)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sdpa", action="store_true",

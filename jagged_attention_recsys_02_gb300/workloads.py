@@ -124,6 +124,15 @@ def make_workload(name: str, seed: int = 0, act: str | None = None) -> Workload:
     return w
 
 
+def first_samples(w: Workload, n: int) -> Workload:
+    """The workload restricted to its first n samples (same lengths and
+    settings; small cases of a recipe for profiler captures)."""
+    n = max(1, min(int(n), w.B))
+    return Workload(f"{w.name}[:{n}]", n, w.H, w.d, w.act, w.causal, w.lq[:n].copy(),
+                    w.lkv[:n].copy(), max_rel=w.max_rel, pma_seeds=w.pma_seeds, window=w.window,
+                    scale=w.scale, extra=dict(w.extra))
+
+
 def custom_workload(lq, lkv, H, d, act="softmax", causal=False, max_rel=0, name="custom",
                     window=0):
     lq = np.asarray(lq, dtype=np.int64)

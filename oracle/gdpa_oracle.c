@@ -18,6 +18,7 @@
  *
  *   s_ij = scale * <q_i, k_j> + bias_h(i - j)        (i < Lq_b, j < Lkv_b)
  *   mask_ij = (j <= i if causal) and (|i - j| < W if W > 0)
+ *             and (floor(i / K) == floor(j / K) if K > 0)
  *   softmax: p_ij = exp(s_ij - M_i) / sum_{j' masked-in} exp(s_ij' - M_i)
  *            lse_i = M_i + log sum_j exp(s_ij - M_i)   (natural log)
  *   GDPA:    p_ij = act(s_ij)   (no row normalisation)
@@ -43,6 +44,12 @@
  *     with |i - j| < W, so with causal a row sees its W most recent keys
  *     (itself included) and without causal the W - 1 on either side too.
  *     W = 0 means no window.  A window needs Lq_b == Lkv_b (self-attention).
+ *   - Block-aligned attention (the same paragraph: fixed 64-token blocks,
+ *     each query block attends only to its own key/value block, independent
+ *     64 x 64 problems): with a block size K > 0 the tokens of each sample
+ *     are cut into blocks of K starting at the sample's first token (the last
+ *     block may be shorter) and a pair is kept only inside one block.  K = 0
+ *     means no blocks.  Blocks need Lq_b == Lkv_b.
  *   - A softmax row with no masked-in key gets o = 0 and lse = -inf.
  *
  * Layouts: q/out/dq [Tq][H][d], k/v/dk/dv [Tkv][H][d], lse [H][Tq], bias
@@ -111,12 +118,14 @@ static double dot(const double* a, const double* b, int d) {
  * masked-in pairs. */
 static double row_probs(const double* q, const double* k, long qrow, long kbase, long Lkv, int H,
                         int d, int h, long i, const double* bias, int max_rel, int act, int causal,
-                        int window, double scale, double* s, double* p, unsigned char* live) {
+                        int window, int block, double scale, double* s, double* p,
+                        unsigned char* live) {
   const double* qi = q + (qrow * H + h) * (long)d;
   long n_live = 0;
   for (long j = 0; j < Lkv; ++j) {
     int in = causal ? (j <= i) : 1;
     if (window > 0 && (j <= i - window || j >= i + window)) in = 0;
+    if (block > 0 && i / block != j / block) in = 0;
     live[j] = (unsigned char)in;
     if (!live[j]) { s[j] = 0.0; p[j] = 0.0; continue; }
     ++n_live;
@@ -153,11 +162,11 @@ static int check_offsets(const int32_t* o, int B) {
 /* Forward.  Returns 0 on success, -1 on bad arguments. */
 int oracle_fwd(const double* q, const int32_t* qo, const double* k, const double* v,
                const int32_t* ko, int B, int H, int d, const double* bias, int max_rel, int act,
-               int causal, int window, double scale, double* out, double* lse) {
+               int causal, int window, int block, double scale, double* out, double* lse) {
   if (B < 0 || H <= 0 || d <= 0 || act < 0 || act > 3) return -1;
   if (!check_offsets(qo, B) || !check_offsets(ko, B)) return -1;
-  if (window < 0) return -1;
-  if (causal || window > 0)
+  if (window < 0 || block < 0) return -1;
+  if (causal || window > 0 || block > 0)
     for (int b = 0; b < B; ++b)
       if (qo[b + 1] - qo[b] != ko[b + 1] - ko[b]) return -1;
   const long Tq = qo[B];
@@ -172,7 +181,7 @@ int oracle_fwd(const double* q, const int32_t* qo, const double* k, const double
     unsigned char* live = (unsigned char*)malloc((size_t)(Lkv > 0 ? Lkv : 1));
     for (long i = 0; i < Lq; ++i) {
       const double l = row_probs(q, k, q0 + i, k0, Lkv, H, d, h, i, bias, max_rel, act, causal,
-                                 window, scale, s, p, live);
+                                 window, block, scale, s, p, live);
       double* oi = out + ((q0 + i) * H + h) * (long)d;
       for (int c = 0; c < d; ++c) oi[c] = 0.0;
       for (long j = 0; j < Lkv; ++j) {
@@ -193,12 +202,12 @@ int oracle_fwd(const double* q, const int32_t* qo, const double* k, const double
  * overwritten.  Returns 0 on success, -1 on bad arguments. */
 int oracle_bwd(const double* q, const int32_t* qo, const double* k, const double* v,
                const int32_t* ko, int B, int H, int d, const double* bias, int max_rel, int act,
-               int causal, int window, double scale, const double* dout, double* dq, double* dk,
-               double* dv) {
+               int causal, int window, int block, double scale, const double* dout, double* dq,
+               double* dk, double* dv) {
   if (B < 0 || H <= 0 || d <= 0 || act < 0 || act > 3) return -1;
   if (!check_offsets(qo, B) || !check_offsets(ko, B)) return -1;
-  if (window < 0) return -1;
-  if (causal || window > 0)
+  if (window < 0 || block < 0) return -1;
+  if (causal || window > 0 || block > 0)
     for (int b = 0; b < B; ++b)
       if (qo[b + 1] - qo[b] != ko[b + 1] - ko[b]) return -1;
   const long nwork = (long)B * H;
@@ -222,8 +231,8 @@ int oracle_bwd(const double* q, const int32_t* qo, const double* k, const double
       const double* doi = dout + ((q0 + i) * H + h) * (long)d;
       double* dqi = dq + ((q0 + i) * H + h) * (long)d;
       for (int c = 0; c < d; ++c) dqi[c] = 0.0;
-      row_probs(q, k, q0 + i, k0, Lkv, H, d, h, i, bias, max_rel, act, causal, window, scale, s, p,
-                live);
+      row_probs(q, k, q0 + i, k0, Lkv, H, d, h, i, bias, max_rel, act, causal, window, block, scale,
+                s, p, live);
       double row_dot = 0.0; /* sum_j p_ij dp_ij (softmax only) */
       for (long j = 0; j < Lkv; ++j) {
         const double* vj = v + ((k0 + j) * H + h) * (long)d;

@@ -46,9 +46,9 @@ def _load():
         ip = ctypes.POINTER(ctypes.c_int32)
         up = ctypes.POINTER(ctypes.c_uint8)
         I, D = ctypes.c_int, ctypes.c_double
-        lib.oracle_fwd.argtypes = [dp, ip, dp, dp, ip, I, I, I, dp, I, I, I, I, D, dp, dp]
+        lib.oracle_fwd.argtypes = [dp, ip, dp, dp, ip, I, I, I, dp, I, I, I, I, I, D, dp, dp]
         lib.oracle_fwd.restype = I
-        lib.oracle_bwd.argtypes = [dp, ip, dp, dp, ip, I, I, I, dp, I, I, I, I, D, dp, dp, dp, dp]
+        lib.oracle_bwd.argtypes = [dp, ip, dp, dp, ip, I, I, I, dp, I, I, I, I, I, D, dp, dp, dp, dp]
         lib.oracle_bwd.restype = I
         lib.oracle_e4m3_encode.argtypes = [D]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
@@ -89,12 +89,15 @@ def _bias_arg(bias, H, max_rel):
 
 
 def fwd(q, q_offsets, k, v, kv_offsets, *, act: int, causal: bool = False, scale: float,
-        bias=None, max_rel: int = 0, window: int = 0):
+        bias=None, max_rel: int = 0, window: int = 0, block: int = 0):
     """Forward pass.  Returns (out [Tq,H,d] float64, lse [H,Tq] float64).
 
     lse is the natural-log row logsumexp for softmax (-inf for a row with no
     key) and 0 for the GDPA activations.  window > 0 keeps only the pairs
-    with |i - j| < window (sliding-window attention; needs Lq == Lkv)."""
+    with |i - j| < window (sliding-window attention; needs Lq == Lkv).
+    block > 0 keeps only the pairs inside one block of `block` tokens, the
+    blocks starting at each sample's first token (block-aligned attention;
+    needs Lq == Lkv)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     qo, ko = _i32(q_offsets), _i32(kv_offsets)
     Tq, H, d = q.shape
@@ -107,7 +110,7 @@ def fwd(q, q_offsets, k, v, kv_offsets, *, act: int, causal: bool = False, scale
     rc = _load().oracle_fwd(_p(q, ctypes.c_double), _p(qo, ctypes.c_int32),
                             _p(k, ctypes.c_double), _p(v, ctypes.c_double),
                             _p(ko, ctypes.c_int32), B, H, d, bp, int(max_rel), int(act),
-                            int(bool(causal)), int(window), float(scale),
+                            int(bool(causal)), int(window), int(block), float(scale),
                             _p(out, ctypes.c_double), _p(lse, ctypes.c_double))
     if rc != 0:
         raise ValueError("oracle_fwd rejected its arguments")
@@ -116,7 +119,7 @@ def fwd(q, q_offsets, k, v, kv_offsets, *, act: int, causal: bool = False, scale
 
 
 def bwd(q, q_offsets, k, v, kv_offsets, dout, *, act: int, causal: bool = False, scale: float,
-        bias=None, max_rel: int = 0, window: int = 0):
+        bias=None, max_rel: int = 0, window: int = 0, block: int = 0):
     """Backward pass.  Returns (dq, dk, dv) as float64 arrays."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
     qo, ko = _i32(q_offsets), _i32(kv_offsets)
@@ -130,7 +133,7 @@ def bwd(q, q_offsets, k, v, kv_offsets, dout, *, act: int, causal: bool = False,
     rc = _load().oracle_bwd(_p(q, ctypes.c_double), _p(qo, ctypes.c_int32),
                             _p(k, ctypes.c_double), _p(v, ctypes.c_double),
                             _p(ko, ctypes.c_int32), B, H, d, bp, int(max_rel), int(act),
-                            int(bool(causal)), int(window), float(scale),
+                            int(bool(causal)), int(window), int(block), float(scale),
                             _p(do, ctypes.c_double), _p(dq, ctypes.c_double),
                             _p(dk, ctypes.c_double), _p(dv, ctypes.c_double))
     if rc != 0:

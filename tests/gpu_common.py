@@ -77,7 +77,7 @@ def run_fwd(q, qo, k, v, ko, act, causal, scale, bias=None, max_rel=0, guard=3, 
 
 
 def oracle_fwd_samples(q, k, v, qo, ko, samples, act, causal, scale, bias=None, max_rel=0,
-                       rows=None, window=0):
+                       rows=None, window=0, block=0):
     """Oracle forward on a subset of samples (and optionally a subset of query
     rows per sample: rows[b] = array of local row indices; only for
     non-causal, bias-free problems, where rows are position-independent).
@@ -99,7 +99,7 @@ def oracle_fwd_samples(q, k, v, qo, ko, samples, act, causal, scale, bias=None, 
             glob = np.arange(q0, q1)
         o, l = oracle.fwd(qs, np.array([0, len(qs)], dtype=np.int32), k[k0:k1], v[k0:k1],
                           np.array([0, k1 - k0], dtype=np.int32), act=a, causal=causal,
-                          scale=scale, bias=bias, max_rel=max_rel, window=window)
+                          scale=scale, bias=bias, max_rel=max_rel, window=window, block=block)
         res.append((glob, o, l))
     return res
 

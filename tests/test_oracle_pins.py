@@ -573,3 +573,113 @@ def test_window_backward_matches_central_differences(oracle_mod, act, causal):
             num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
         err = np.abs(num - g).max() / max(1.0, np.abs(num).max())
         assert err < 1e-7, f"d{name}: {err}"
+
+
+# --------------------------------------------------------------- block-aligned attention
+@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_SILU])
+@pytest.mark.parametrize("causal", [False, True])
+def test_blocks_equal_separate_samples(oracle_mod, act, causal):
+    """Cutting every sample into blocks of K tokens from its first token and
+    attending inside each block is the same as running each block as a sample
+    of its own (the relative-position bias depends on i - j only)."""
+    H, d, K, max_rel = 2, 8, 5, 4
+    lq = [12, 0, 5, 1, 9]
+    q = _bf16_randn((sum(lq), H, d), 61)
+    k = _bf16_randn((sum(lq), H, d), 62)
+    v = _bf16_randn((sum(lq), H, d), 63)
+    table = np.random.default_rng(64).normal(0, 0.5, size=(H, 2 * max_rel - 1))
+    o = _offsets(lq)
+    kw = dict(act=act, causal=causal, scale=0.3, bias=table, max_rel=max_rel)
+    out, lse = oracle_mod.fwd(q, o, k, v, o, block=K, **kw)
+    pieces = [min(K, L - s) for L in lq for s in range(0, L, K)]
+    ob = _offsets(pieces)
+    ref, rl = oracle_mod.fwd(q, ob, k, v, ob, **kw)
+    np.testing.assert_array_equal(out, ref)
+    np.testing.assert_array_equal(lse, rl)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_blocks_softmax_matches_torch_sdpa(oracle_mod, causal):
+    """Torch fp64 SDPA under a block-diagonal mask (blocks of 4 from the start)."""
+    H, d, K, L = 2, 16, 4, 14
+    q = _bf16_randn((L, H, d), 65)
+    k = _bf16_randn((L, H, d), 66)
+    v = _bf16_randn((L, H, d), 67)
+    o = _offsets([L])
+    out, lse = oracle_mod.fwd(q, o, k, v, o, act=ACT_SOFTMAX, causal=causal, scale=0.25, block=K)
+    i, j = np.arange(L)[:, None], np.arange(L)[None, :]
+    keep = (i // K) == (j // K)
+    if causal:
+        keep &= j <= i
+    m = torch.from_numpy(np.where(keep, 0.0, -np.inf))[None, None].expand(1, H, L, L)
+    qb, kb, vb = (torch.from_numpy(x).permute(1, 0, 2)[None] for x in (q, k, v))
+    ref = F.scaled_dot_product_attention(qb, kb, vb, attn_mask=m, scale=0.25)
+    np.testing.assert_allclose(out, ref[0].permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-13)
+    ref_lse = torch.logsumexp(0.25 * torch.einsum("bhqd,bhkd->bhqk", qb, kb) + m, dim=-1)
+    np.testing.assert_allclose(lse, ref_lse[0].numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_blocks_closed_forms(oracle_mod):
+    """K = 0 and one-hot V: row i averages its block's keys (1/len of the block,
+    the last block shorter); block 1 returns v_i; a block as long as the sample
+    changes nothing; blocks of 64 on a 150-token sample end at 64, 128, 150."""
+    L = 150
+    H = 1
+    q = _bf16_randn((L, H, L), 68)
+    k = np.zeros((L, H, L))
+    v = np.eye(L)[:, None, :]
+    o = _offsets([L])
+    out, lse = oracle_mod.fwd(q, o, k, v, o, act=ACT_SOFTMAX, scale=1.0, block=64)
+    ref = np.zeros((L, L))
+    for s, e in ((0, 64), (64, 128), (128, 150)):
+        ref[s:e, s:e] = 1.0 / (e - s)
+    np.testing.assert_allclose(out[:, 0, :], ref, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(lse[0], np.log(np.repeat([64, 64, 22], [64, 64, 22])), rtol=1e-14)
+    kk = _bf16_randn((L, H, L), 69)
+    vv = _bf16_randn((L, H, L), 70)
+    o1, _ = oracle_mod.fwd(q, o, kk, vv, o, act=ACT_SOFTMAX, scale=0.1, block=1)
+    np.testing.assert_array_equal(o1, vv)
+    full, lf = oracle_mod.fwd(q, o, kk, vv, o, act=ACT_SILU, scale=0.1)
+    wide, lw = oracle_mod.fwd(q, o, kk, vv, o, act=ACT_SILU, scale=0.1, block=L)
+    np.testing.assert_array_equal(wide, full)
+
+
+def test_blocks_reject_bad_arguments(oracle_mod):
+    q = np.zeros((3, 1, 4))
+    with pytest.raises(ValueError):
+        oracle_mod.fwd(q, np.array([0, 1, 3], dtype=np.int32), q, q,
+                       np.array([0, 2, 3], dtype=np.int32), act=0, scale=1.0, block=2)
+    with pytest.raises(ValueError):
+        oracle_mod.fwd(q, _offsets([3]), q, q, _offsets([3]), act=0, scale=1.0, block=-2)
+
+
+@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_GELU_TANH])
+@pytest.mark.parametrize("causal", [False, True])
+def test_blocks_backward_matches_central_differences(oracle_mod, act, causal):
+    H, d, max_rel, K = 2, 4, 3, 3
+    lq = [7, 2]
+    rng = np.random.default_rng(300 + act + 10 * causal)
+    q = rng.normal(size=(sum(lq), H, d))
+    k = rng.normal(size=(sum(lq), H, d))
+    v = rng.normal(size=(sum(lq), H, d))
+    do = rng.normal(size=(sum(lq), H, d))
+    table = rng.normal(0, 0.5, size=(H, 2 * max_rel - 1))
+    qo = _offsets(lq)
+    kw = dict(act=act, causal=causal, scale=0.45, bias=table, max_rel=max_rel, block=K)
+    dq, dk, dv = oracle_mod.bwd(q, qo, k, v, qo, do, **kw)
+
+    def loss(qq, kk, vv):
+        o_, _ = oracle_mod.fwd(qq, qo, kk, vv, qo, **kw)
+        return float(np.sum(o_ * do))
+
+    h = 1e-5
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp = x.copy(); xp[idx] += h
+            xm = x.copy(); xm[idx] -= h
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        err = np.abs(num - g).max() / max(1.0, np.abs(num).max())
+        assert err < 1e-7, f"d{name}: {err}"

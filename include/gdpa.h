@@ -137,6 +137,35 @@ gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void*
                             const void* dout, void* dq, void* dk, void* dv, void* workspace,
                             size_t ws_bytes, void* stream);
 
+/* Block-aligned attention ("GEM Training ..." SWA paragraph: with fixed
+ * 64-token blocks each query block attends only to its own key/value block,
+ * giving independent 64 x 64 problems without online softmax correction,
+ * logsumexp traffic or a separate D pass).  Self-attention: q, k, v share
+ * `offsets` (T rows).  The tokens of each sample are cut into blocks of 64
+ * from the sample's first token (the last block may be shorter); row i sees
+ * the keys of its own block (and only j <= i when causal).  Scores, bias,
+ * activations and layouts are those of gdpa_fwd.  The forward writes `out`
+ * only: no logsumexp (the backward recomputes each row's exact softmax from
+ * its block).  workspace: gdpa_block_workspace_size() bytes of device memory
+ * (the tile list), shared by gdpa_block_fwd and gdpa_block_bwd.  Malformed
+ * offsets raise GDPA_ERR_BAD_OFFSETS on the device. */
+size_t gdpa_block_workspace_size(int B, int H, int d, int64_t T);
+gdpa_status gdpa_block_fwd(const void* q, const int32_t* offsets, const void* k, const void* v,
+                           int B, int H, int d, int64_t T, const gdpa_bias* bias, int act,
+                           int causal, float scale, void* out, void* workspace, size_t ws_bytes,
+                           void* stream);
+
+/* Backward of gdpa_block_fwd: writes dq, dk, dv [T][H][d] (bf16) from q, k,
+ * v and dout alone.  Each 64-token block is one independent problem, so the
+ * kernel recomputes the block's scores and exact softmax, forms D = sum_j P
+ * dP inside the tile and writes every gradient row once (no atomics, no
+ * logsumexp or forward output needed).  Rows of a sample never see another
+ * sample's tokens.  Arguments, workspace and errors as gdpa_block_fwd. */
+gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k, const void* v,
+                           int B, int H, int d, int64_t T, const gdpa_bias* bias, int act,
+                           int causal, float scale, const void* dout, void* dq, void* dk, void* dv,
+                           void* workspace, size_t ws_bytes, void* stream);
+
 /* MXFP8 block quantisation (OCP Microscaling Formats v1.0; "GEM Training ..."
  * low-precision paragraph: attention with MXFP8 block-scaled MMA).  Elements
  * become E4M3 codes (round to nearest even, saturated at +-448); each block of

@@ -30,7 +30,8 @@ EXPORTS = ("gdpa_fwd_workspace_size", "gdpa_fwd", "gdpa_bwd_workspace_size", "gd
            "gdpa_get_device_status", "gdpa_status_string", "gdpa_last_launch_count",
            "gdpa_timing_enable", "gdpa_timing_collect", "gdpa_fwd_noalloc",
            "gdpa_mxfp8_scale_bytes", "gdpa_quantize_mxfp8", "gdpa_fwd_mxfp8",
-           "gdpa_fwd_window", "gdpa_bwd_window", "gdpa_fwd_mxfp8_window")
+           "gdpa_fwd_window", "gdpa_bwd_window", "gdpa_fwd_mxfp8_window",
+           "gdpa_block_workspace_size", "gdpa_block_fwd", "gdpa_block_bwd")
 MX_ALONG_CHANNELS, MX_ALONG_TOKENS = 0, 1
 
 
@@ -106,6 +107,14 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                               ctypes.POINTER(gdpa_bias), I, I, I, F, vp, vp, vp,
                                               sz, vp]
         lib.gdpa_fwd_mxfp8_window.restype = I
+        lib.gdpa_block_workspace_size.argtypes = [I, I, I, i64]
+        lib.gdpa_block_workspace_size.restype = sz
+        lib.gdpa_block_fwd.argtypes = [vp, vp, vp, vp, I, I, I, i64, ctypes.POINTER(gdpa_bias), I,
+                                       I, F, vp, vp, sz, vp]
+        lib.gdpa_block_fwd.restype = I
+        lib.gdpa_block_bwd.argtypes = [vp, vp, vp, vp, I, I, I, i64, ctypes.POINTER(gdpa_bias), I,
+                                       I, F, vp, vp, vp, vp, vp, sz, vp]
+        lib.gdpa_block_bwd.restype = I
         _lib = lib
         return lib
 
@@ -197,6 +206,49 @@ def gdpa_bwd(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, act, causal=Fals
     else:
         rc = lib.gdpa_bwd(*head, *tail)
     _check(rc, "gdpa_bwd_window" if window else "gdpa_bwd")
+    return dq, dk, dv
+
+
+def block_workspace_size(B, H, d, T) -> int:
+    return int(load().gdpa_block_workspace_size(B, H, d, T))
+
+
+def gdpa_block_fwd(q, offsets, k, v, *, act, causal=False, scale, bias=None, max_rel=0, out=None,
+                   workspace=None, stream=None):
+    """Block-aligned attention forward (64-token blocks) through the C ABI.
+    Returns out."""
+    lib = load()
+    T, H, d = q.shape
+    B = offsets.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = torch.empty(block_workspace_size(B, H, d, T), device=q.device,
+                                dtype=torch.uint8)
+    rc = lib.gdpa_block_fwd(_ptr(q), _ptr(offsets), _ptr(k), _ptr(v), B, H, d, T,
+                            _bias(bias, max_rel), _act(act), int(bool(causal)), float(scale),
+                            _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "gdpa_block_fwd")
+    return out
+
+
+def gdpa_block_bwd(q, offsets, k, v, dout, *, act, causal=False, scale, bias=None, max_rel=0,
+                   dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Block-aligned attention backward through the C ABI.  Returns (dq, dk, dv)."""
+    lib = load()
+    T, H, d = q.shape
+    B = offsets.numel() - 1
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(block_workspace_size(B, H, d, T), device=q.device,
+                                dtype=torch.uint8)
+    rc = lib.gdpa_block_bwd(_ptr(q), _ptr(offsets), _ptr(k), _ptr(v), B, H, d, T,
+                            _bias(bias, max_rel), _act(act), int(bool(causal)), float(scale),
+                            _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                            workspace.numel(), _stream(stream))
+    _check(rc, "gdpa_block_bwd")
     return dq, dk, dv
 
 

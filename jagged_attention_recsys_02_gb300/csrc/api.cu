@@ -376,6 +376,119 @@ gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void*
   return GDPA_OK;
 }
 
+size_t gdpa_block_workspace_size(int B, int H, int d, int64_t T) {
+  (void)H;
+  (void)d;
+  if (B < 0 || T < 0) return 0;
+  return 256 + align_up(static_cast<size_t>(max_block_tiles(B, T)) * sizeof(int4), 256);
+}
+
+gdpa_status gdpa_block_fwd(const void* q, const int32_t* offsets, const void* k, const void* v,
+                           int B, int H, int d, int64_t T, const gdpa_bias* bias, int act,
+                           int causal, float scale, void* out, void* workspace, size_t ws_bytes,
+                           void* stream) {
+  t_launches = 0;
+  gdpa_status st = check_common(q, offsets, k, v, offsets, B, H, d, T, T, bias, act, causal, 0);
+  if (st != GDPA_OK) return st;
+  if (T > 0 && (out == nullptr || !aligned16(out))) return GDPA_ERR_INVALID_ARG;
+  const size_t need = gdpa_block_workspace_size(B, H, d, T);
+  if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return GDPA_ERR_WORKSPACE;
+  if (T == 0 || B == 0) return GDPA_OK;
+  DeviceInfo* dev = nullptr;
+  if (device_info(&dev) != cudaSuccess) return GDPA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int max_rel = 1;
+  const float* table = bias_table(bias, &max_rel);
+  CUtensorMap tq, tk, tv;
+  if (!make_thd_map(&tq, q, T, H, d, 2 * kBlockRows) ||
+      !make_thd_map(&tk, k, T, H, d, 2 * kBlockRows) ||
+      !make_thd_map(&tv, v, T, H, d, 2 * kBlockRows))
+    return GDPA_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* n_tiles = reinterpret_cast<int*>(ws);
+  int4* tiles = reinterpret_cast<int4*>(ws + 256);
+  if (launch_block_list(offsets, B, T, tiles, n_tiles, dev->status, s) != cudaSuccess)
+    return GDPA_ERR_CUDA;
+  ++t_launches;
+  BlockParams p{};
+  p.tiles = tiles;
+  p.n_tiles = n_tiles;
+  p.H = H;
+  p.d = d;
+  p.T = T;
+  p.bias_table = table;
+  p.max_rel = max_rel;
+  p.causal = causal;
+  p.scale = scale;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.status = dev->status;
+  const int64_t max_items = max_block_tiles(B, T) * H;
+  const int grid = static_cast<int>(max_items < dev->sms ? max_items : dev->sms);
+  cudaEvent_t ea = nullptr, eb = nullptr;
+  const bool timed = timing_slot(0, &ea, &eb);
+  if (timed && cudaEventRecord(ea, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (launch_block_fwd(p, act, tq, tk, tv, grid, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (timed && cudaEventRecord(eb, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  ++t_launches;
+  return GDPA_OK;
+}
+
+gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k, const void* v,
+                           int B, int H, int d, int64_t T, const gdpa_bias* bias, int act,
+                           int causal, float scale, const void* dout, void* dq, void* dk, void* dv,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  t_launches = 0;
+  gdpa_status st = check_common(q, offsets, k, v, offsets, B, H, d, T, T, bias, act, causal, 0);
+  if (st != GDPA_OK) return st;
+  if (T > 0 && (dout == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
+                !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)))
+    return GDPA_ERR_INVALID_ARG;
+  const size_t need = gdpa_block_workspace_size(B, H, d, T);
+  if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return GDPA_ERR_WORKSPACE;
+  if (T == 0 || B == 0) return GDPA_OK;
+  DeviceInfo* dev = nullptr;
+  if (device_info(&dev) != cudaSuccess) return GDPA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int max_rel = 1;
+  const float* table = bias_table(bias, &max_rel);
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_thd_map(&tq, q, T, H, d, 2 * kBlockRows) ||
+      !make_thd_map(&tk, k, T, H, d, 2 * kBlockRows) ||
+      !make_thd_map(&tv, v, T, H, d, 2 * kBlockRows) ||
+      !make_thd_map(&tdo, dout, T, H, d, 2 * kBlockRows))
+    return GDPA_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* n_tiles = reinterpret_cast<int*>(ws);
+  int4* tiles = reinterpret_cast<int4*>(ws + 256);
+  if (launch_block_list(offsets, B, T, tiles, n_tiles, dev->status, s) != cudaSuccess)
+    return GDPA_ERR_CUDA;
+  ++t_launches;
+  BlockParams p{};
+  p.tiles = tiles;
+  p.n_tiles = n_tiles;
+  p.H = H;
+  p.d = d;
+  p.T = T;
+  p.bias_table = table;
+  p.max_rel = max_rel;
+  p.causal = causal;
+  p.scale = scale;
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.status = dev->status;
+  const int64_t max_items = max_block_tiles(B, T) * H;
+  const int grid = static_cast<int>(max_items < dev->sms ? max_items : dev->sms);
+  cudaEvent_t ea = nullptr, eb = nullptr;
+  const bool timed = timing_slot(1, &ea, &eb);
+  if (timed && cudaEventRecord(ea, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (launch_block_bwd(p, act, tq, tk, tv, tdo, grid, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (timed && cudaEventRecord(eb, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  ++t_launches;
+  return GDPA_OK;
+}
+
 size_t gdpa_mxfp8_scale_bytes(int B, int H, int d, int64_t T, int mode) {
   if (B < 0 || H <= 0 || T < 0 || (d != 64 && d != 128)) return 0;
   if (mode == GDPA_MX_ALONG_CHANNELS) return static_cast<size_t>(T) * H * (d / 32);

@@ -115,29 +115,6 @@ __device__ __forceinline__ BwdItem decode_bwd(int2 it, const BwdParams& p) {
   return r;
 }
 
-// act(x) and act'(x) for the GDPA activations (tanh forms).
-template <int ACT>
-__device__ __forceinline__ void act_and_grad(float x, float& a, float& g) {
-  if (ACT == GDPA_ACT_SILU) {
-    const float h = 0.5f * x;
-    const float t = tanh_approx(h);
-    const float sg = fmaf(0.5f, t, 0.5f);           // sigmoid(x)
-    a = x * sg;
-    g = sg * fmaf(x, 1.0f - sg, 1.0f);               // sigmoid * (1 + x (1 - sigmoid))
-  } else if (ACT == GDPA_ACT_GELU_TANH) {
-    const float k0 = 0.7978845608028654f, k1 = 0.7978845608028654f * 0.044715f;
-    const float x2 = x * x;
-    const float t = tanh_approx(x * fmaf(k1, x2, k0));
-    const float h = 0.5f * x;
-    a = fmaf(h, t, h);
-    // 0.5 (1 + t) + 0.5 x (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 x^2)
-    g = fmaf(0.5f, t, 0.5f) + h * (1.0f - t * t) * fmaf(3.0f * k1, x2, k0);
-  } else {
-    a = x;
-    g = 1.0f;
-  }
-}
-
 template <int D, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,

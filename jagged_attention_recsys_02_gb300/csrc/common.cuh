@@ -25,6 +25,10 @@ constexpr int kBwdSmDqRows = 16;  // query rows per dQ reduce box of the softmax
 
 constexpr int kCostBuckets = 2048;
 
+// Block-aligned attention: tokens per block (fixed; blocks start at each
+// sample's first token).
+constexpr int kBlockRows = 64;
+
 // Work item: x = sample b (or -1 = end of list), y = (block << 8) | head.
 __host__ __device__ inline int item_head(int2 it) { return it.y & 0xFF; }
 __host__ __device__ inline int item_block(int2 it) { return it.y >> 8; }
@@ -77,6 +81,31 @@ __host__ __device__ __forceinline__ void band_query_tiles(int c_begin, int c_end
   *t_end = (qe + tile - 1) / tile;
 }
 
+// GDPA activation and its derivative: SiLU x sigmoid(x) and GELU-tanh
+// 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) through tanh.approx (for
+// SiLU via sigmoid(x) = 0.5 + 0.5 tanh(x / 2)); identity otherwise.
+template <int ACT>
+__device__ __forceinline__ void act_and_grad(float x, float& a, float& g) {
+  if (ACT == GDPA_ACT_SILU) {
+    const float h = 0.5f * x;
+    const float t = ptx::tanh_approx(h);
+    const float sg = fmaf(0.5f, t, 0.5f);           // sigmoid(x)
+    a = x * sg;
+    g = sg * fmaf(x, 1.0f - sg, 1.0f);               // sigmoid * (1 + x (1 - sigmoid))
+  } else if (ACT == GDPA_ACT_GELU_TANH) {
+    const float k0 = 0.7978845608028654f, k1 = 0.7978845608028654f * 0.044715f;
+    const float x2 = x * x;
+    const float t = ptx::tanh_approx(x * fmaf(k1, x2, k0));
+    const float h = 0.5f * x;
+    a = fmaf(h, t, h);
+    // 0.5 (1 + t) + 0.5 x (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 x^2)
+    g = fmaf(0.5f, t, 0.5f) + h * (1.0f - t * t) * fmaf(3.0f * k1, x2, k0);
+  } else {
+    a = x;
+    g = 1.0f;
+  }
+}
+
 // Device status word values (same numbering as gdpa_status).
 __device__ __forceinline__ void set_status(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
@@ -123,6 +152,23 @@ struct BwdParams {
   int* status;
 };
 
+struct BlockParams {
+  const int4* tiles;        // {first row, rows of block A, rows of block B, 0} per tile
+  const int* n_tiles;
+  int H, d;
+  int64_t T;
+  const float* bias_table;  // nullptr: no bias
+  int max_rel;
+  int causal;
+  float scale;
+  __nv_bfloat16* out;             // forward output
+  const __nv_bfloat16* dout;      // backward inputs / outputs
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* status;
+};
+
 // Host-side launchers (defined in the kernel translation units).
 cudaError_t launch_build_worklist(const int32_t* outer_off, const int32_t* inner_off, int B, int H,
                                   int64_t T_outer, int64_t T_inner, int causal, int window,
@@ -153,6 +199,15 @@ cudaError_t launch_fwd_mx(const FwdParams& p, const CUtensorMap& tq, const CUten
                           const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
                           const uint8_t* v_sc, long long v_sc_rows, int grid, cudaStream_t s);
 
+cudaError_t launch_block_list(const int32_t* offsets, int B, int64_t T, int4* tiles, int* n_tiles,
+                              int* status, cudaStream_t s);
+cudaError_t launch_block_fwd(const BlockParams& p, int act, const CUtensorMap& tq,
+                             const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                             cudaStream_t s);
+cudaError_t launch_block_bwd(const BlockParams& p, int act, const CUtensorMap& tq,
+                             const CUtensorMap& tk, const CUtensorMap& tv,
+                             const CUtensorMap& tdo, int grid, cudaStream_t s);
+
 // Upper bound on the number of work items (host-side sizing).
 inline int64_t max_fwd_items(int B, int H, int64_t Tq) {
   return static_cast<int64_t>(H) * (Tq / kItemRows + B);
@@ -160,5 +215,7 @@ inline int64_t max_fwd_items(int B, int H, int64_t Tq) {
 inline int64_t max_bwd_items(int B, int H, int64_t Tkv) {
   return static_cast<int64_t>(H) * (Tkv / kBwdKvRows + B);
 }
+// Tiles of two 64-token blocks: at most (T/64 + B + 1) / 2.
+inline int64_t max_block_tiles(int B, int64_t T) { return (T / kBlockRows + B + 2) / 2; }
 
 }  // namespace gdpa

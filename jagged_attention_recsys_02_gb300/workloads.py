@@ -22,6 +22,10 @@ sparsity 0.5; these workloads stand in for that traffic:
                      Training ..." SWA paragraph): B=64, L~U[1,16384], H=4,
                      d=128, softmax, causal, window 1024, relative-position
                      bias table [H, 2047] ~ N(0, 0.02)
+  block_relpos       block-aligned attention over the same long sequences
+                     (same paragraph): B=64, L~U[1,16384], H=4, d=128,
+                     softmax, 64-token blocks, relative-position bias table
+                     [H, 127] ~ N(0, 0.02)
 """
 from __future__ import annotations
 
@@ -34,7 +38,7 @@ import torch
 ACTS = {"softmax": 0, "silu": 1, "gelu_tanh": 2, "identity": 3}
 
 CONFIG_NAMES = ("tiny_silu", "jfa_causal_relpos", "gdpa_cross_gelu", "gdpa_pma_silu", "heavy_tail")
-EXTRA_NAMES = ("swa_causal_relpos",)
+EXTRA_NAMES = ("swa_causal_relpos", "block_relpos")
 
 
 @dataclass
@@ -50,6 +54,7 @@ class Workload:
     max_rel: int = 0          # >0: relative-position bias table [H, 2*max_rel-1]
     pma_seeds: int = 0        # >0: queries are this many seeds shared by all samples
     window: int = 0           # >0: sliding window, pairs with |i - j| < window
+    block: int = 0            # >0: block-aligned attention in blocks of this many tokens
     scale: float = 0.0
     extra: dict = field(default_factory=dict)
 
@@ -71,6 +76,11 @@ class Workload:
     def sample_pairs(self) -> np.ndarray:
         """Per-sample query-key pairs that are not masked (int64 [B])."""
         L, W = self.lq, self.window
+        if self.block > 0:
+            K = self.block
+            full, rest = L // K, L % K
+            per = (lambda n: n * (n + 1) // 2) if self.causal else (lambda n: n * n)
+            return full * per(K) + per(rest)
         if W <= 0:
             return self.lq * (self.lq + 1) // 2 if self.causal else self.lq * self.lkv
         # causal window: row i sees min(i + 1, W) keys
@@ -116,6 +126,10 @@ def make_workload(name: str, seed: int = 0, act: str | None = None) -> Workload:
         L = rng.integers(1, 16384, size=64, endpoint=True).astype(np.int64)
         w = Workload(name, 64, 4, 128, "softmax", True, L.copy(), L.copy(), max_rel=1024,
                      window=1024)
+    elif name == "block_relpos":
+        L = rng.integers(1, 16384, size=64, endpoint=True).astype(np.int64)
+        w = Workload(name, 64, 4, 128, "softmax", False, L.copy(), L.copy(), max_rel=64,
+                     block=64)
     else:
         raise KeyError(name)
     if act is not None:
@@ -130,14 +144,15 @@ def first_samples(w: Workload, n: int) -> Workload:
     n = max(1, min(int(n), w.B))
     return Workload(f"{w.name}[:{n}]", n, w.H, w.d, w.act, w.causal, w.lq[:n].copy(),
                     w.lkv[:n].copy(), max_rel=w.max_rel, pma_seeds=w.pma_seeds, window=w.window,
-                    scale=w.scale, extra=dict(w.extra))
+                    block=w.block, scale=w.scale, extra=dict(w.extra))
 
 
 def custom_workload(lq, lkv, H, d, act="softmax", causal=False, max_rel=0, name="custom",
-                    window=0):
+                    window=0, block=0):
     lq = np.asarray(lq, dtype=np.int64)
     lkv = np.asarray(lkv, dtype=np.int64)
-    w = Workload(name, len(lq), H, d, act, causal, lq, lkv, max_rel=max_rel, window=window)
+    w = Workload(name, len(lq), H, d, act, causal, lq, lkv, max_rel=max_rel, window=window,
+                 block=block)
     w.scale = 1.0 / math.sqrt(d)
     return w
 

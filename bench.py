@@ -190,7 +190,7 @@ def measure_padded_sdpa(w, t, dev, iters=5, max_gb=40.0):
     v = pad(t["v"], ko, lkv_max).requires_grad_(True)
     do = pad(t["dout"], qo, lq_max)
     mask = None
-    if exact and (w.causal or w.max_rel or w.window):
+    if exact and (w.causal or w.max_rel or w.window or w.block):
         i = torch.arange(lq_max, device=dev)[:, None]
         j = torch.arange(lkv_max, device=dev)[None, :]
         if w.max_rel:
@@ -202,6 +202,8 @@ def measure_padded_sdpa(w, t, dev, iters=5, max_gb=40.0):
             mask = mask.masked_fill((j > i)[None, None], float("-inf"))
         if w.window:
             mask = mask.masked_fill(((i - j).abs() >= w.window)[None, None], float("-inf"))
+        if w.block:
+            mask = mask.masked_fill((i // w.block != j // w.block)[None, None], float("-inf"))
 
     def once():
         o = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=w.scale)
@@ -224,6 +226,7 @@ def measure_padded_sdpa(w, t, dev, iters=5, max_gb=40.0):
             "inputs": f"zero-padded [B={B}, H={H}, Lmax, d={d}] bf16",
             "mask": (" + ".join(x for x, on in (("causal", w.causal),
                                                  (f"window {w.window}", w.window),
+                                                 (f"blocks of {w.block}", w.block),
                                                  ("rel-pos bias", w.max_rel)) if on)
                      + " as one additive bf16 mask" if mask is not None else
                      "none (exact for equal lengths without causal)" if exact else
@@ -264,9 +267,9 @@ def oracle_step(w, tensors, samples):
         oq = np.array([0, q1 - q0], dtype=np.int32)
         ok = np.array([0, k1 - k0], dtype=np.int32)
         oracle.fwd(sq, oq, sk, sv, ok, act=a, causal=w.causal, scale=w.scale, bias=bias,
-                   max_rel=w.max_rel, window=w.window)
+                   max_rel=w.max_rel, window=w.window, block=w.block)
         oracle.bwd(sq, oq, sk, sv, ok, sd, act=a, causal=w.causal, scale=w.scale, bias=bias,
-                   max_rel=w.max_rel, window=w.window)
+                   max_rel=w.max_rel, window=w.window, block=w.block)
 
 
 def host_sample_tensors(w, samples, device_tensors=None, seed=0):
@@ -370,7 +373,7 @@ def run_reference(args, rank, world):
 
 def workload_config(w, l2_note):
     return {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "act": w.act, "causal": w.causal,
-            "window": w.window,
+            "window": w.window, "block": w.block,
             "bias": (f"relpos table [{w.H},{2 * w.max_rel - 1}]" if w.max_rel else "none"),
             "Tq": w.Tq, "Tkv": w.Tkv, "pairs_non_padded": w.pairs(),
             "pairs_full_square": w.full_pairs(), "step": "forward + backward", "l2": l2_note}
@@ -406,11 +409,29 @@ def run_gpu(args, rank, world, local_rank):
     kw = dict(act=a, causal=w.causal, scale=w.scale, bias=t["bias"], max_rel=w.max_rel,
               window=w.window)
     fwd_flops, bwd_flops = workload_flops(w)
+    if w.block:
+        # block-aligned attention: its own entry points (no lse, no D pass)
+        ws_k = torch.empty(binding.block_workspace_size(w.B, H, d, Tq), device=dev,
+                           dtype=torch.uint8)
+        kw.pop("window")
+
+    def run_fwd(q, qo, k, v, ko, out_, lse_, **kw_):
+        if w.block:
+            binding.gdpa_block_fwd(q, qo, k, v, out=out_, workspace=ws_k, **kw_)
+        else:
+            binding.gdpa_fwd(q, qo, k, v, ko, out=out_, lse=lse_, workspace=ws_f, **kw_)
+
+    def run_bwd(q, qo, k, v, ko, out_, lse_, do, dq_, dk_, dv_, **kw_):
+        if w.block:
+            binding.gdpa_block_bwd(q, qo, k, v, do, dq=dq_, dk=dk_, dv=dv_, workspace=ws_k, **kw_)
+        else:
+            binding.gdpa_bwd(q, qo, k, v, ko, out_, lse_, do, dq=dq_, dk=dk_, dv=dv_,
+                             workspace=ws_b, **kw_)
 
     def step(q, qo, k, v, ko, do):
-        binding.gdpa_fwd(q, qo, k, v, ko, out=out, lse=lse, workspace=ws_f, **kw)
+        run_fwd(q, qo, k, v, ko, out, lse, **kw)
         n = binding.last_launch_count()
-        binding.gdpa_bwd(q, qo, k, v, ko, out, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws_b, **kw)
+        run_bwd(q, qo, k, v, ko, out, lse, do, dq, dk, dv, **kw)
         return n + binding.last_launch_count()
 
     args_dev = (t["q"], t["qo"], t["k"], t["v"], t["ko"], t["dout"])
@@ -460,6 +481,15 @@ def run_gpu(args, rank, world, local_rank):
     dominant = "bwd" if sum(bwd_ms) >= sum(fwd_ms) else "fwd"
     achieved = b_tf if dominant == "bwd" else f_tf
     traffic = load_traffic().get(f"{w.name}/{w.act}/{dominant}")
+    hbm = None
+    if w.block:
+        # 64 x 64 problems are bound by HBM traffic: algorithmic bytes are q, k, v
+        # read and out written once (forward), q, k, v, dO read and dq, dk, dv
+        # written once (backward), bf16
+        row_bytes = H * d * 2
+        f_bytes, b_bytes = 4 * Tq * row_bytes, 7 * Tq * row_bytes
+        hbm = {"fwd_gbs": f_bytes / (f_avg * 1e-3) / 1e9, "bwd_gbs": b_bytes / (b_avg * 1e-3) / 1e9,
+               "fwd_bytes": f_bytes, "bwd_bytes": b_bytes}
 
     # ---------------- end to end through host buffers
     # Every step copies its inputs from pinned host memory, runs forward and
@@ -473,6 +503,9 @@ def run_gpu(args, rank, world, local_rank):
         hbias = t["bias"].cpu().pin_memory() if t["bias"] is not None else None
         outs = [dict(out=torch.empty_like(out), lse=torch.empty_like(lse), dq=torch.empty_like(dq),
                      dk=torch.empty_like(dk), dv=torch.empty_like(dv)) for _ in range(2)]
+        if w.block:  # the block forward writes no logsumexp
+            for o_ in outs:
+                del o_["lse"]
         host_out = [{k_: torch.empty(tuple(x.shape), dtype=x.dtype, pin_memory=True)
                      for k_, x in o.items()} for o in outs]
         dev_in = [{k_: torch.empty_like(t[k_]) for k_ in names_in} for _ in range(2)]
@@ -501,12 +534,11 @@ def run_gpu(args, rank, world, local_rank):
             with torch.cuda.stream(s_cmp):
                 s_cmp.wait_event(ev_in[sl])
                 s_cmp.wait_event(ev_out[sl])  # outputs of two steps back have been read
-                kw_e = dict(kw, bias=dbias[sl])
-                binding.gdpa_fwd(di["q"], di["qo"], di["k"], di["v"], di["ko"], out=o["out"],
-                                 lse=o["lse"], workspace=ws_f, stream=s_cmp, **kw_e)
-                binding.gdpa_bwd(di["q"], di["qo"], di["k"], di["v"], di["ko"], o["out"], o["lse"],
-                                 di["dout"], dq=o["dq"], dk=o["dk"], dv=o["dv"], workspace=ws_b,
-                                 stream=s_cmp, **kw_e)
+                kw_e = dict(kw, bias=dbias[sl], stream=s_cmp)
+                run_fwd(di["q"], di["qo"], di["k"], di["v"], di["ko"], o["out"], o.get("lse"),
+                        **kw_e)
+                run_bwd(di["q"], di["qo"], di["k"], di["v"], di["ko"], o["out"], o.get("lse"),
+                        di["dout"], o["dq"], o["dk"], o["dv"], **kw_e)
                 ev_cmp[sl].record(s_cmp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_cmp[sl])
@@ -594,14 +626,20 @@ def run_gpu(args, rank, world, local_rank):
                         + f" of {peak_src}"},
         "fwd": {"tflops": f_tf, "kernel_ms": f_avg, "flops_per_launch": fwd_flops},
         "bwd": {"tflops": b_tf, "kernel_ms": b_avg, "flops_per_launch": bwd_flops},
-        "roofline": {"bound": "tensor", "kernel": f"{dominant} main kernel",
-                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": ("bf16_tflops_sustained" if sustained else "bf16_tflops")
-                     + f" of {peak_src}"},
+        "roofline": ({"bound": "tensor", "kernel": f"{dominant} main kernel",
+                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                      "frac": achieved / peak, "traffic": traffic,
+                      "peak_source": ("bf16_tflops_sustained" if sustained else "bf16_tflops")
+                      + f" of {peak_src}"} if hbm is None else
+                     {"bound": "hbm", "kernel": f"block {dominant} kernel",
+                      "achieved": hbm[f"{dominant}_gbs"], "peak": float(peaks["hbm_gbs"]),
+                      "unit": "GB/s", "frac": hbm[f"{dominant}_gbs"] / float(peaks["hbm_gbs"]),
+                      "traffic": traffic, "algorithmic_bytes": hbm[f"{dominant}_bytes"],
+                      "peak_source": f"hbm_gbs of {peak_src}"}),
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": e2e,
+        "hbm": hbm,
         "cpu_baseline": cpu,
         "padded_sdpa": sdpa,
     }

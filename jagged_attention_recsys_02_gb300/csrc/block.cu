@@ -177,9 +177,13 @@ struct BfCfg {
   static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte alignment");
   static constexpr int kQ = 0, kK = kTileBytes, kV = 2 * kTileBytes, kBias = 3 * kTileBytes;
   static constexpr int kBar = kStages * kStageBytes;
-  static constexpr int kFull = 0;                 // + stage
-  static constexpr int kEmpty = kStages;          // + stage
-  static constexpr int kSFull = 2 * kStages;      // + buffer
+  // Q and K of a stage free up after its score product, V and the bias window
+  // after the value product: the next loads start as early as they can.
+  static constexpr int kQKFull = 0;               // + stage
+  static constexpr int kQKEmpty = kStages;        // + stage
+  static constexpr int kVFull = 2 * kStages;      // + stage (V and the bias window)
+  static constexpr int kVEmpty = 3 * kStages;     // + stage
+  static constexpr int kSFull = 4 * kStages;      // + buffer
   static constexpr int kPFull = kSFull + 2;       // + buffer
   static constexpr int kODone = kPFull + 2;       // + buffer
   static constexpr int kDrain = kODone + 2;
@@ -209,8 +213,10 @@ block_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(C::kFull + s), 1);
-      mbar_init(bar(C::kEmpty + s), 1);
+      mbar_init(bar(C::kQKFull + s), 1);
+      mbar_init(bar(C::kQKEmpty + s), 1);
+      mbar_init(bar(C::kVFull + s), 1);
+      mbar_init(bar(C::kVEmpty + s), 1);
     }
     for (int u = 0; u < 2; ++u) {
       mbar_init(bar(C::kSFull + u), 1);
@@ -250,30 +256,40 @@ block_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       const int head = item % p.H;
       const TileInfo ti = load_tile(p.tiles, item / p.H);
       const uint32_t s = k % C::kStages, ph = (k / C::kStages) & 1u;
-      bool w = mbar_wait(bar(C::kEmpty + s), ph ^ 1u, abort_flag);
-      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
       const uint32_t st = sbase + s * C::kStageBytes;
+      bool w = mbar_wait(bar(C::kQKEmpty + s), ph ^ 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(C::kQKFull + s), 2 * C::kTileBytes);
+#pragma unroll
+        for (int x = 0; x < D; x += 64) {
+          const uint32_t off = (x / 64) * (kTileRows * 128);
+          tma_load_3d(st + C::kQ + off, &tmap_q, bar(C::kQKFull + s), x, head, ti.row0);
+          tma_load_3d(st + C::kK + off, &tmap_k, bar(C::kQKFull + s), x, head, ti.row0);
+        }
+        inflight |= 1u << s;
+        last_k[s] = k;
+      }
+      w = mbar_wait(bar(C::kVEmpty + s), ph ^ 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
       if (has_bias)
         stage_bias(reinterpret_cast<float*>(gbase + s * C::kStageBytes + C::kBias), p.bias_table,
                    head, p.max_rel, kSoftmax ? kLog2e : 1.0f, lane);
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(C::kFull + s), 3 * C::kTileBytes);
+        mbar_arrive_expect_tx(bar(C::kVFull + s), C::kTileBytes);
 #pragma unroll
-        for (int x = 0; x < D; x += 64) {
-          const uint32_t off = (x / 64) * (kTileRows * 128);
-          tma_load_3d(st + C::kQ + off, &tmap_q, bar(C::kFull + s), x, head, ti.row0);
-          tma_load_3d(st + C::kK + off, &tmap_k, bar(C::kFull + s), x, head, ti.row0);
-          tma_load_3d(st + C::kV + off, &tmap_v, bar(C::kFull + s), x, head, ti.row0);
-        }
-        inflight |= 1u << s;
-        last_k[s] = k;
+        for (int x = 0; x < D; x += 64)
+          tma_load_3d(st + C::kV + (x / 64) * (kTileRows * 128), &tmap_v, bar(C::kVFull + s), x,
+                      head, ti.row0);
       }
     }
     if (lane == 0 && *abort_flag) {
       for (int s = 0; s < C::kStages; ++s)
-        if (inflight & (1u << s))
-          mbar_wait(bar(C::kFull + s), (last_k[s] / C::kStages) & 1u, nullptr, 50000000ull);
+        if (inflight & (1u << s)) {
+          mbar_wait(bar(C::kQKFull + s), (last_k[s] / C::kStages) & 1u, nullptr, 50000000ull);
+          mbar_wait(bar(C::kVFull + s), (last_k[s] / C::kStages) & 1u, nullptr, 50000000ull);
+        }
     }
   } else if (warp == kFwdMma) {
     // ------------------------------------------------------------ MMA issuer
@@ -288,7 +304,7 @@ block_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
         const bool have = item_of(k) < n_items;
         if (have) {
           const uint32_t s = k % C::kStages;
-          if (!mbar_wait(bar(C::kFull + s), (k / C::kStages) & 1u, abort_flag)) { fail(); break; }
+          if (!mbar_wait(bar(C::kQKFull + s), (k / C::kStages) & 1u, abort_flag)) { fail(); break; }
           tc_fence_after();
           const uint32_t so = s * C::kStageBytes;
 #pragma unroll
@@ -298,12 +314,14 @@ block_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
                        ks > 0 ? 1u : 0u);
           }
           mma_commit(bar(C::kSFull + (k & 1)));
+          mma_commit(bar(C::kQKEmpty + s));
           issued_any = true;
         }
         if (k >= 1) {
           const int kk = k - 1;
           const uint32_t u = kk & 1, s = kk % C::kStages;
           if (!mbar_wait(bar(C::kPFull + u), (kk >> 1) & 1u, abort_flag)) { fail(); break; }
+          if (!mbar_wait(bar(C::kVFull + s), (kk / C::kStages) & 1u, abort_flag)) { fail(); break; }
           tc_fence_after();
           const uint64_t vb = dadd(dsc_v, s * C::kStageBytes);
           const uint32_t tp = tmem + u * 256, to = tp + 128;
@@ -314,7 +332,7 @@ block_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
             if (kSplit) mma_f16_ts(to, tp + pcol + 16, dadd(vb, ks * 2048), idesc_pv, 1u);
           }
           mma_commit(bar(C::kODone + u));
-          mma_commit(bar(C::kEmpty + s));
+          mma_commit(bar(C::kVEmpty + s));
         }
         if (!have) break;
       }
@@ -340,8 +358,8 @@ block_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       const TileInfo ti = load_tile(p.tiles, item / p.H);
       const uint32_t s = k % C::kStages;
       bool w = mbar_wait(bar(C::kSFull + u), (k >> 1) & 1u, abort_flag);
-      // the stage's bias window was written by the producer before this barrier phase
-      if (has_bias) w = w && mbar_wait(bar(C::kFull + s), (k / C::kStages) & 1u, abort_flag);
+      // the stage's bias window was written by the producer before V's barrier phase
+      if (has_bias) w = w && mbar_wait(bar(C::kVFull + s), (k / C::kStages) & 1u, abort_flag);
       if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
       tc_fence_after();
       int c_lo, c_hi;
@@ -518,12 +536,13 @@ struct BbCfg {
   static constexpr int kBias = kPS + kPSBytes;              // bias window of the current head
   static constexpr int kBar = kBias + 4 * (2 * kTileRows - 1) + 4;
   static constexpr int kQKFull = 0, kQKEmpty = 2;           // + slot
-  static constexpr int kVOFull = 4, kVOEmpty = 5;
+  static constexpr int kVOFull = 4, kVOEmpty = 5;            // V (free after dP)
   static constexpr int kSFull = 6, kDpFull = 7, kPFull = 8, kDvDone = 9, kDsFull = 10;
   static constexpr int kGradFull = 11, kEpiDone = 12, kDrain = 13;
   static constexpr int kWinFree = 14, kWinReady = 15;      // bias window restaging
   static constexpr int kDsDone = 16;                        // GDPA: dK, dQ of dS's hi part done
-  static constexpr int kNumBars = 17;
+  static constexpr int kOFull = 17, kOEmpty = 18;           // dO (V uses kVOFull / kVOEmpty)
+  static constexpr int kNumBars = 19;
   static constexpr int kTmemSlot = kBar + 8 * kNumBars;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kUsed = kAbort + 4;
@@ -551,8 +570,11 @@ __device__ __forceinline__ void ps_store_row(uint8_t* ps, int r, int cb, const u
 
 __device__ __forceinline__ void ps_zero_atom(uint8_t* ps, int r, int atom) {
   uint8_t* row = ps + atom * (kTileRows * 128) + r * 128;
+  // in swizzled order, so that each store instruction of a warp spreads over
+  // all banks (the row's chunks are all zero either way)
 #pragma unroll
-  for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(row + v * 16) = make_uint4(0, 0, 0, 0);
+  for (int v = 0; v < 8; ++v)
+    *reinterpret_cast<uint4*>(row + ((v ^ (r & 7)) * 16)) = make_uint4(0, 0, 0, 0);
 }
 
 template <int D, int ACT>
@@ -591,6 +613,8 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     mbar_init(bar(C::kWinFree), 4);
     mbar_init(bar(C::kWinReady), 4);
     mbar_init(bar(C::kDsDone), 1);
+    mbar_init(bar(C::kOFull), 1);
+    mbar_init(bar(C::kOEmpty), 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -617,7 +641,7 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   if (warp == kBwdProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int last_qk[2] = {-1, -1}, last_vo = -1;
+      int last_qk[2] = {-1, -1}, last_vo = -1, last_o = -1;
       for (int k = 0;; ++k) {
         const int item = item_of(k);
         if (item >= n_items) break;
@@ -634,22 +658,28 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
           tma_load_3d(qk + C::kTileBytes + off, &tmap_k, bar(C::kQKFull + slot), x, head, row0);
         }
         last_qk[slot] = k;
-        if (!mbar_wait(bar(C::kVOEmpty), (k & 1u) ^ 1u, abort_flag)) { fail(); break; }
+        // V frees up after dP, dO after dV: separate barriers let each load start early
         const uint32_t vo = sbase + C::kVO;
-        mbar_arrive_expect_tx(bar(C::kVOFull), 2 * C::kTileBytes);
+        if (!mbar_wait(bar(C::kVOEmpty), (k & 1u) ^ 1u, abort_flag)) { fail(); break; }
+        mbar_arrive_expect_tx(bar(C::kVOFull), C::kTileBytes);
 #pragma unroll
-        for (int x = 0; x < D; x += 64) {
-          const uint32_t off = (x / 64) * C::kAtom;
-          tma_load_3d(vo + off, &tmap_v, bar(C::kVOFull), x, head, row0);
-          tma_load_3d(vo + C::kTileBytes + off, &tmap_do, bar(C::kVOFull), x, head, row0);
-        }
+        for (int x = 0; x < D; x += 64)
+          tma_load_3d(vo + (x / 64) * C::kAtom, &tmap_v, bar(C::kVOFull), x, head, row0);
         last_vo = k;
+        if (!mbar_wait(bar(C::kOEmpty), (k & 1u) ^ 1u, abort_flag)) { fail(); break; }
+        mbar_arrive_expect_tx(bar(C::kOFull), C::kTileBytes);
+#pragma unroll
+        for (int x = 0; x < D; x += 64)
+          tma_load_3d(vo + C::kTileBytes + (x / 64) * C::kAtom, &tmap_do, bar(C::kOFull), x, head,
+                      row0);
+        last_o = k;
       }
       if (*abort_flag) {
         for (int i = 0; i < 2; ++i)
           if (last_qk[i] >= 0)
             mbar_wait(bar(C::kQKFull + i), (last_qk[i] >> 1) & 1u, nullptr, 50000000ull);
         if (last_vo >= 0) mbar_wait(bar(C::kVOFull), last_vo & 1u, nullptr, 50000000ull);
+        if (last_o >= 0) mbar_wait(bar(C::kOFull), last_o & 1u, nullptr, 50000000ull);
       }
     }
   } else if (warp == kBwdMma) {
@@ -681,12 +711,16 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
           tc_fence_after();
           issue_nt(kColS, dsc_qk, dadd(dsc_qk, C::kTileBytes));
           mma_commit(bar(C::kSFull));
-          if (!mbar_wait(bar(C::kVOFull), 0, abort_flag)) { fail(); ok = false; }
+          if (!mbar_wait(bar(C::kVOFull), 0, abort_flag) || !mbar_wait(bar(C::kOFull), 0, abort_flag)) {
+            fail();
+            ok = false;
+          }
         }
         if (ok) {
           tc_fence_after();
           issue_nt(kColDP, dadd(dsc_vo, C::kTileBytes), dsc_vo);
           mma_commit(bar(C::kDpFull));
+          mma_commit(bar(C::kVOEmpty));  // V(0) is read
         }
       }
       for (int k = 0; ok; ++k) {
@@ -704,7 +738,7 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
           mma_commit(bar(C::kDvDone));
         }
         if (!okp) { fail(); break; }
-        mma_commit(bar(C::kVOEmpty));
+        mma_commit(bar(C::kOEmpty));  // dO(k) is read
         // S(k+1): softmax is done reading S(k) once P(k) is out; the GDPA
         // activations read S(k) again for act'(S), so theirs waits for dS(k)'s
         // hi part
@@ -738,12 +772,14 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
         mma_commit(bar(C::kGradFull));
         mma_commit(bar(C::kQKEmpty + (k & 1)));
         if (!next) break;
-        // dP(k+1) once the epilogue has read dQ, dK and dV of tile k
+        // dP(k+1) into the dP columns once the epilogue has read dQ(k) out of them
         if (!mbar_wait(bar(C::kEpiDone), k & 1u, abort_flag)) { fail(); break; }
-        if (!mbar_wait(bar(C::kVOFull), (k + 1) & 1u, abort_flag)) { fail(); break; }
+        if (!mbar_wait(bar(C::kVOFull), (k + 1) & 1u, abort_flag) ||
+            !mbar_wait(bar(C::kOFull), (k + 1) & 1u, abort_flag)) { fail(); break; }
         tc_fence_after();
         issue_nt(kColDP, dadd(dsc_vo, C::kTileBytes), dsc_vo);
         mma_commit(bar(C::kDpFull));
+        mma_commit(bar(C::kVOEmpty));  // V(k+1) is read
       }
       if (issued_any) {
         mma_commit(bar(C::kDrain));

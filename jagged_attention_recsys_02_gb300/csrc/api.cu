@@ -451,12 +451,10 @@ gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int max_rel = 1;
   const float* table = bias_table(bias, &max_rel);
-  CUtensorMap tq, tk, tv, tdo;
-  if (!make_thd_map(&tq, q, T, H, d, 2 * kBlockRows) ||
-      !make_thd_map(&tk, k, T, H, d, 2 * kBlockRows) ||
-      !make_thd_map(&tv, v, T, H, d, 2 * kBlockRows) ||
-      !make_thd_map(&tdo, dout, T, H, d, 2 * kBlockRows))
-    return GDPA_ERR_INVALID_ARG;
+  CUtensorMap maps[7];
+  const void* bases[7] = {q, k, v, dout, dq, dk, dv};
+  for (int i = 0; i < 7; ++i)
+    if (!make_thd_map(&maps[i], bases[i], T, H, d, 2 * kBlockRows)) return GDPA_ERR_INVALID_ARG;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* n_tiles = reinterpret_cast<int*>(ws);
   int4* tiles = reinterpret_cast<int4*>(ws + 256);
@@ -483,7 +481,7 @@ gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k,
   cudaEvent_t ea = nullptr, eb = nullptr;
   const bool timed = timing_slot(1, &ea, &eb);
   if (timed && cudaEventRecord(ea, s) != cudaSuccess) return GDPA_ERR_CUDA;
-  if (launch_block_bwd(p, act, tq, tk, tv, tdo, grid, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (launch_block_bwd(p, act, maps, grid, s) != cudaSuccess) return GDPA_ERR_CUDA;
   if (timed && cudaEventRecord(eb, s) != cudaSuccess) return GDPA_ERR_CUDA;
   ++t_launches;
   return GDPA_OK;

@@ -542,7 +542,10 @@ struct BbCfg {
   static constexpr int kWinFree = 14, kWinReady = 15;      // bias window restaging
   static constexpr int kDsDone = 16;                        // GDPA: dK, dQ of dS's hi part done
   static constexpr int kOFull = 17, kOEmpty = 18;           // dO (V uses kVOFull / kVOEmpty)
-  static constexpr int kNumBars = 19;
+  // epilogue of a full tile: each gradient is staged in the P / dS buffer and
+  // leaves by TMA store; the buffer goes back to the activation warps after
+  static constexpr int kEpiStaged = 19, kEpiFree = 20, kPsFree = 21;
+  static constexpr int kNumBars = 22;
   static constexpr int kTmemSlot = kBar + 8 * kNumBars;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kUsed = kAbort + 4;
@@ -581,7 +584,8 @@ template <int D, int ACT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
-                 const BlockParams p) {
+                 const __grid_constant__ CUtensorMap tmap_dq, const __grid_constant__ CUtensorMap tmap_dk,
+                 const __grid_constant__ CUtensorMap tmap_dv, const BlockParams p) {
   using C = BbCfg<D>;
   constexpr bool kSoftmax = (ACT == GDPA_ACT_SOFTMAX);
   constexpr int kParts = kSoftmax ? 1 : 2;  // P / dS passes through the buffer per tile
@@ -615,6 +619,9 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     mbar_init(bar(C::kDsDone), 1);
     mbar_init(bar(C::kOFull), 1);
     mbar_init(bar(C::kOEmpty), 1);
+    mbar_init(bar(C::kEpiStaged), 4);
+    mbar_init(bar(C::kEpiFree), 1);
+    mbar_init(bar(C::kPsFree), 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -891,8 +898,8 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
               pw[16 * ch + i] = pack_bf16x2(ex2_approx(x[2 * i] - m_ref) * inv_l,
                                             ex2_approx(x[2 * i + 1] - m_ref) * inv_l);
           }
-          // P into the buffer once the previous tile's dK, dQ are done with it
-          if (k > 0 && !wait_all(C::kGradFull, (k - 1) & 1u)) return;
+          // P into the buffer once the previous tile's epilogue is done with it
+          if (k > 0 && !wait_all(C::kPsFree, (k - 1) & 1u)) return;
           ps_store_row<NCH>(ps, r, cb, pw);
           publish(C::kPFull);
           // dS = P (dP - D), D = sum P dP
@@ -931,7 +938,7 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
           // P = act(S) and dS = act'(S) dP, each as a bf16 hi part and a lo part,
           // formed chunk by chunk from TMEM (S stays there until dS is out)
           for (int part = 0; part < 2; ++part) {
-            if (part == 0 && k > 0 && !wait_all(C::kGradFull, (k - 1) & 1u)) return;
+            if (part == 0 && k > 0 && !wait_all(C::kPsFree, (k - 1) & 1u)) return;
             if (part == 1 && !wait_all(C::kDvDone, (2 * k) & 1u)) return;  // dV read the hi part
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) {
@@ -993,9 +1000,21 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     }
   } else if (warp < kBwdEpi0 + 4) {
     // ------------------------------------------------------------ epilogue warps
+    // A full softmax tile's gradients leave through the P / dS buffer (free once
+    // dK and dQ are done) and TMA stores, one gradient at a time: coalesced
+    // writes instead of one 256-byte row per thread, which saturate the SM's
+    // load/store pipe that the activation warps also use.  A partial tile's
+    // rows are stored directly (a tile store would write into the next tile's
+    // rows).
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // tile row: query (dQ) or key (dK, dV)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    uint8_t* ps = gbase + C::kPS;
+    const uint32_t col[3] = {kColDP, kColDK, kColDV};
+    const float mul[3] = {p.scale, p.scale, 1.0f};
+    const CUtensorMap* maps[3] = {&tmap_dq, &tmap_dk, &tmap_dv};
+    uint32_t n_round = 0;
+    bool stores_pending = false;
     for (int k = 0;; ++k) {
       const int item = item_of(k);
       if (item >= n_items) break;
@@ -1004,12 +1023,42 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       bool w = mbar_wait(bar(C::kGradFull), k & 1u, abort_flag);
       if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
       tc_fence_after();
-      const long long g = (static_cast<long long>(ti.row0 + r) * p.H + head) * D;
-      __nv_bfloat16* const dst[3] = {p.dq + g, p.dk + g, p.dv + g};
-      const uint32_t col[3] = {kColDP, kColDK, kColDV};
-      const float mul[3] = {p.scale, p.scale, 1.0f};
+      // (GDPA tiles pass P and dS through the buffer twice each: there the
+      // activation warps need it back sooner than a staged epilogue returns it)
+      if (!kSoftmax || ti.rows < kTileRows) {
+        if (r == 0) mbar_arrive(bar(C::kPsFree));  // the buffer is not needed here
+        const long long g = (static_cast<long long>(ti.row0 + r) * p.H + head) * D;
+        __nv_bfloat16* const dst[3] = {p.dq + g, p.dk + g, p.dv + g};
 #pragma unroll
-      for (int which = 0; which < 3; ++which) {
+        for (int which = 0; which < 3; ++which) {
+#pragma unroll 1
+          for (int chunk = 0; chunk < D / 32; ++chunk) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + col[which] + 32 * chunk, v);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul[which],
+                                  __uint_as_float(v[2 * i + 1]) * mul[which]);
+            if (r < ti.rows) {
+              uint4* out = reinterpret_cast<uint4*>(dst[which] + 32 * chunk);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) out[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
+          }
+        }
+        tc_fence_before();
+        warp_arrive(bar(C::kEpiDone), lane);
+        continue;
+      }
+      bool ok = true;
+#pragma unroll 1
+      for (int which = 0; which < 3 && ok; ++which) {
+        // the previous gradient's store has finished reading the buffer
+        if (n_round > 0) {
+          w = mbar_wait(bar(C::kEpiFree), (n_round - 1) & 1u, abort_flag);
+          if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); ok = false; break; }
+        }
 #pragma unroll 1
         for (int chunk = 0; chunk < D / 32; ++chunk) {
           uint32_t v[32];
@@ -1019,16 +1068,33 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
           for (int i = 0; i < 16; ++i)
             pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul[which],
                                 __uint_as_float(v[2 * i + 1]) * mul[which]);
-          if (r < ti.rows) {
-            uint4* out = reinterpret_cast<uint4*>(dst[which] + 32 * chunk);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) out[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-          }
+          ps_store_row<1>(ps, r, 32 * chunk, pk);  // [channel atom][row][64 channels], swizzled
         }
+        if (which == 2) {
+          tc_fence_before();
+          warp_arrive(bar(C::kEpiDone), lane);  // TMEM of this tile is read
+        }
+        fence_proxy_async_smem();
+        warp_arrive(bar(C::kEpiStaged), lane);
+        if (r == 0) {
+          if (!mbar_wait(bar(C::kEpiStaged), n_round & 1u, abort_flag)) {
+            fail();
+          } else {
+#pragma unroll
+            for (int x = 0; x < D; x += 64)
+              tma_store_3d(maps[which], smem_u32(ps) + (x / 64) * C::kAtom, x, head, ti.row0);
+            bulk_commit_group();
+            stores_pending = true;
+          }
+          bulk_wait_group_read<0>();
+          mbar_arrive(bar(C::kEpiFree));
+          if (which == 2) mbar_arrive(bar(C::kPsFree));
+        }
+        ++n_round;
       }
-      tc_fence_before();
-      warp_arrive(bar(C::kEpiDone), lane);
+      if (!ok) break;
     }
+    if (r == 0 && stores_pending) bulk_wait_group_all();  // global writes done before exit
   }
 
   tc_fence_before();
@@ -1041,26 +1107,31 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
 
 template <int D, int ACT>
 cudaError_t launch_bwd_one(const BlockParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const CUtensorMap& tdo, int grid, cudaStream_t s) {
+                           const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                           const CUtensorMap& tdk, const CUtensorMap& tdv, int grid, cudaStream_t s) {
   constexpr int smem = BbCfg<D>::kSmemBytes;
   static_assert(smem <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(block_bwd_kernel<D, ACT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  block_bwd_kernel<D, ACT><<<grid, kBwdThreads, smem, s>>>(tq, tk, tv, tdo, p);
+  block_bwd_kernel<D, ACT><<<grid, kBwdThreads, smem, s>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
   return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_bwd_d(const BlockParams& p, int act, const CUtensorMap& tq,
-                         const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                         int grid, cudaStream_t s) {
+cudaError_t launch_bwd_d(const BlockParams& p, int act, const CUtensorMap* m, int grid,
+                         cudaStream_t s) {
   switch (act) {
-    case GDPA_ACT_SOFTMAX: return launch_bwd_one<D, GDPA_ACT_SOFTMAX>(p, tq, tk, tv, tdo, grid, s);
-    case GDPA_ACT_SILU: return launch_bwd_one<D, GDPA_ACT_SILU>(p, tq, tk, tv, tdo, grid, s);
+    case GDPA_ACT_SOFTMAX:
+      return launch_bwd_one<D, GDPA_ACT_SOFTMAX>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6], grid, s);
+    case GDPA_ACT_SILU:
+      return launch_bwd_one<D, GDPA_ACT_SILU>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6], grid, s);
     case GDPA_ACT_GELU_TANH:
-      return launch_bwd_one<D, GDPA_ACT_GELU_TANH>(p, tq, tk, tv, tdo, grid, s);
-    default: return launch_bwd_one<D, GDPA_ACT_IDENTITY>(p, tq, tk, tv, tdo, grid, s);
+      return launch_bwd_one<D, GDPA_ACT_GELU_TANH>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6], grid,
+                                                   s);
+    default:
+      return launch_bwd_one<D, GDPA_ACT_IDENTITY>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6], grid,
+                                                  s);
   }
 }
 
@@ -1079,11 +1150,10 @@ cudaError_t launch_block_fwd(const BlockParams& p, int act, const CUtensorMap& t
                    : launch_fwd_d<128>(p, act, tq, tk, tv, grid, s);
 }
 
-cudaError_t launch_block_bwd(const BlockParams& p, int act, const CUtensorMap& tq,
-                             const CUtensorMap& tk, const CUtensorMap& tv,
-                             const CUtensorMap& tdo, int grid, cudaStream_t s) {
-  return p.d == 64 ? launch_bwd_d<64>(p, act, tq, tk, tv, tdo, grid, s)
-                   : launch_bwd_d<128>(p, act, tq, tk, tv, tdo, grid, s);
+cudaError_t launch_block_bwd(const BlockParams& p, int act, const CUtensorMap* maps, int grid,
+                             cudaStream_t s) {
+  return p.d == 64 ? launch_bwd_d<64>(p, act, maps, grid, s)
+                   : launch_bwd_d<128>(p, act, maps, grid, s);
 }
 
 }  // namespace gdpa

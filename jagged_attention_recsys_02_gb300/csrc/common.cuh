@@ -204,9 +204,9 @@ cudaError_t launch_block_list(const int32_t* offsets, int B, int64_t T, int4* ti
 cudaError_t launch_block_fwd(const BlockParams& p, int act, const CUtensorMap& tq,
                              const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                              cudaStream_t s);
-cudaError_t launch_block_bwd(const BlockParams& p, int act, const CUtensorMap& tq,
-                             const CUtensorMap& tk, const CUtensorMap& tv,
-                             const CUtensorMap& tdo, int grid, cudaStream_t s);
+// maps: q, k, v, dout, dq, dk, dv (bf16 [T][H][d], 128-row boxes)
+cudaError_t launch_block_bwd(const BlockParams& p, int act, const CUtensorMap* maps, int grid,
+                             cudaStream_t s);
 
 // Upper bound on the number of work items (host-side sizing).
 inline int64_t max_fwd_items(int B, int H, int64_t Tq) {

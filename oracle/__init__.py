@@ -14,6 +14,7 @@ two matmuls with an elementwise activation in between; low-precision
 paragraph: MXFP8 block scaling).
 """
 from .oracle import (  # noqa: F401
+    ACT_GELU_ERF,
     ACT_GELU_TANH,
     ACT_IDENTITY,
     ACT_SILU,

@@ -34,7 +34,8 @@
  *
  * Readings taken where the pages are silent:
  *   - SiLU(x) = x * sigmoid(x); GELU is the tanh form
- *     0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+ *     0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) or the exact (erf)
+ *     form 0.5 x (1 + erf(x / sqrt(2))), both selectable.
  *   - The bias is a per-head relative-position table of 2*max_rel-1 entries,
  *     indexed by (i - j) + (max_rel - 1) with per-sample local positions; an
  *     index outside the table is clamped to its first or last entry.
@@ -66,7 +67,13 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_ACT_SOFTMAX = 0, ORC_ACT_SILU = 1, ORC_ACT_GELU_TANH = 2, ORC_ACT_IDENTITY = 3 };
+enum {
+  ORC_ACT_SOFTMAX = 0,
+  ORC_ACT_SILU = 1,
+  ORC_ACT_GELU_TANH = 2,
+  ORC_ACT_IDENTITY = 3,
+  ORC_ACT_GELU_ERF = 4
+};
 
 static double act_value(int act, double x) {
   switch (act) {
@@ -76,6 +83,8 @@ static double act_value(int act, double x) {
       const double c = sqrt(2.0 / M_PI);
       return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
     }
+    case ORC_ACT_GELU_ERF:
+      return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
     default:
       return x;
   }
@@ -93,6 +102,8 @@ static double act_deriv(int act, double x) {
       const double t = tanh(u);
       return 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * c * (1.0 + 3.0 * 0.044715 * x * x);
     }
+    case ORC_ACT_GELU_ERF: /* Phi(x) + x phi(x), phi the standard normal density */
+      return 0.5 * (1.0 + erf(x / sqrt(2.0))) + x * exp(-0.5 * x * x) / sqrt(2.0 * M_PI);
     default:
       return 1.0;
   }
@@ -163,7 +174,7 @@ static int check_offsets(const int32_t* o, int B) {
 int oracle_fwd(const double* q, const int32_t* qo, const double* k, const double* v,
                const int32_t* ko, int B, int H, int d, const double* bias, int max_rel, int act,
                int causal, int window, int block, double scale, double* out, double* lse) {
-  if (B < 0 || H <= 0 || d <= 0 || act < 0 || act > 3) return -1;
+  if (B < 0 || H <= 0 || d <= 0 || act < 0 || act > 4) return -1;
   if (!check_offsets(qo, B) || !check_offsets(ko, B)) return -1;
   if (window < 0 || block < 0) return -1;
   if (causal || window > 0 || block > 0)
@@ -204,7 +215,7 @@ int oracle_bwd(const double* q, const int32_t* qo, const double* k, const double
                const int32_t* ko, int B, int H, int d, const double* bias, int max_rel, int act,
                int causal, int window, int block, double scale, const double* dout, double* dq,
                double* dk, double* dv) {
-  if (B < 0 || H <= 0 || d <= 0 || act < 0 || act > 3) return -1;
+  if (B < 0 || H <= 0 || d <= 0 || act < 0 || act > 4) return -1;
   if (!check_offsets(qo, B) || !check_offsets(ko, B)) return -1;
   if (window < 0 || block < 0) return -1;
   if (causal || window > 0 || block > 0)

@@ -14,7 +14,7 @@ import threading
 
 import numpy as np
 
-ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH, ACT_IDENTITY = 0, 1, 2, 3
+ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH, ACT_IDENTITY, ACT_GELU_ERF = 0, 1, 2, 3, 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gdpa_oracle.c")

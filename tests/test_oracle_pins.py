@@ -17,10 +17,11 @@ import pytest
 import torch
 import torch.nn.functional as F
 
-from oracle import ACT_GELU_TANH, ACT_IDENTITY, ACT_SILU, ACT_SOFTMAX
+from oracle import ACT_GELU_ERF, ACT_GELU_TANH, ACT_IDENTITY, ACT_SILU, ACT_SOFTMAX
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-ACT_NAMES = {ACT_SOFTMAX: "softmax", ACT_SILU: "silu", ACT_GELU_TANH: "gelu", ACT_IDENTITY: "identity"}
+ACT_NAMES = {ACT_SOFTMAX: "softmax", ACT_SILU: "silu", ACT_GELU_TANH: "gelu", ACT_IDENTITY: "identity",
+             ACT_GELU_ERF: "gelu_erf"}
 
 
 def _bf16_randn(shape, seed, scale=1.0):
@@ -108,7 +109,7 @@ def test_softmax_matches_torch_sdpa(oracle_mod, with_bias, causal):
         np.testing.assert_allclose(lse[:, qo[b]:qo[b + 1]], ref_lse, rtol=1e-12, atol=1e-12)
 
 
-@pytest.mark.parametrize("act", [ACT_SILU, ACT_GELU_TANH, ACT_IDENTITY])
+@pytest.mark.parametrize("act", [ACT_SILU, ACT_GELU_TANH, ACT_IDENTITY, ACT_GELU_ERF])
 @pytest.mark.parametrize("with_bias", [False, True])
 @pytest.mark.parametrize("causal", [False, True])
 def test_gdpa_activation_via_onehot_values(oracle_mod, act, with_bias, causal):
@@ -129,7 +130,7 @@ def test_gdpa_activation_via_onehot_values(oracle_mod, act, with_bias, causal):
     out, _ = oracle_mod.fwd(q, qo, k, v, ko, act=act, causal=causal, scale=scale, bias=table,
                             max_rel=max_rel)
     tact = {ACT_SILU: F.silu, ACT_GELU_TANH: lambda x: F.gelu(x, approximate="tanh"),
-            ACT_IDENTITY: lambda x: x}[act]
+            ACT_IDENTITY: lambda x: x, ACT_GELU_ERF: lambda x: F.gelu(x, approximate="none")}[act]
     for b in range(len(lq)):
         qb = torch.from_numpy(q[qo[b]:qo[b + 1]])
         kb = torch.from_numpy(k[ko[b]:ko[b + 1]])
@@ -298,7 +299,7 @@ def test_rejects_bad_offsets(oracle_mod):
 
 
 # --------------------------------------------------------------- backward (finite differences)
-@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH, ACT_IDENTITY])
+@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH, ACT_IDENTITY, ACT_GELU_ERF])
 @pytest.mark.parametrize("variant", ["plain", "bias", "causal_bias"])
 def test_backward_matches_central_differences(oracle_mod, act, variant):
     H, d, max_rel = 2, 6, 3
@@ -683,3 +684,25 @@ def test_blocks_backward_matches_central_differences(oracle_mod, act, causal):
             num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
         err = np.abs(num - g).max() / max(1.0, np.abs(num).max())
         assert err < 1e-7, f"d{name}: {err}"
+
+
+def test_gelu_forms_differ_and_match_their_definitions(oracle_mod):
+    """Single key, one-hot value: the output is act(s) for the scalar score s,
+    checked against math.erf / math.tanh directly; the two GELU forms differ by
+    up to about 1e-3 (so a swapped form fails)."""
+    xs = np.linspace(-6, 6, 49)
+    d = 4
+    q = np.zeros((len(xs), 1, d))
+    q[:, 0, 0] = xs
+    k = np.zeros((len(xs), 1, d))
+    k[:, 0, 0] = 1.0
+    v = np.zeros((len(xs), 1, d))
+    v[:, 0, 1] = 1.0
+    o = _offsets([1] * len(xs))
+    out_e, _ = oracle_mod.fwd(q, o, k, v, o, act=ACT_GELU_ERF, scale=1.0)
+    out_t, _ = oracle_mod.fwd(q, o, k, v, o, act=ACT_GELU_TANH, scale=1.0)
+    ref_e = [0.5 * x * (1 + math.erf(x / math.sqrt(2))) for x in xs]
+    ref_t = [0.5 * x * (1 + math.tanh(math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3))) for x in xs]
+    np.testing.assert_allclose(out_e[:, 0, 1], ref_e, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(out_t[:, 0, 1], ref_t, rtol=1e-14, atol=1e-15)
+    assert np.abs(out_e - out_t).max() > 1e-4

@@ -19,7 +19,8 @@
  *     p_ij  = softmax_j(s_ij)       (GDPA_ACT_SOFTMAX, masked entries excluded)
  *           = act(s_ij)             (SiLU, GELU-tanh, identity; no normalisation)
  *     out_i = sum_j p_ij v_j
- * SiLU(x) = x sigmoid(x); GELU-tanh(x) = 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))).
+ * SiLU(x) = x sigmoid(x); GELU-tanh(x) = 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3)));
+ * GELU-erf(x) = 0.5 x (1 + erf(x / sqrt(2))).
  * A softmax row with no key gets out = 0 and lse = -inf; GDPA rows with no
  * key get 0.  Samples with no query rows write nothing.
  *
@@ -56,7 +57,8 @@ typedef enum {
   GDPA_ACT_SOFTMAX = 0,   /* JFA */
   GDPA_ACT_SILU = 1,      /* GDPA */
   GDPA_ACT_GELU_TANH = 2, /* GDPA */
-  GDPA_ACT_IDENTITY = 3   /* GDPA, linear attention; useful for testing */
+  GDPA_ACT_IDENTITY = 3,  /* GDPA, linear attention; useful for testing */
+  GDPA_ACT_GELU_ERF = 4   /* GDPA, exact GELU 0.5 x (1 + erf(x / sqrt(2))) */
 } gdpa_act;
 
 typedef enum { GDPA_BIAS_NONE = 0, GDPA_BIAS_RELPOS = 1 } gdpa_bias_kind;

@@ -16,9 +16,9 @@ import torch
 
 from . import build as _build
 
-ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH, ACT_IDENTITY = 0, 1, 2, 3
+ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH, ACT_IDENTITY, ACT_GELU_ERF = 0, 1, 2, 3, 4
 ACT_BY_NAME = {"softmax": ACT_SOFTMAX, "silu": ACT_SILU, "gelu_tanh": ACT_GELU_TANH,
-               "identity": ACT_IDENTITY}
+               "identity": ACT_IDENTITY, "gelu_erf": ACT_GELU_ERF}
 BIAS_NONE, BIAS_RELPOS = 0, 1
 
 STATUS_NAMES = {0: "GDPA_OK", 1: "GDPA_ERR_INVALID_ARG", 2: "GDPA_ERR_UNSUPPORTED",

@@ -138,7 +138,7 @@ gdpa_status check_common(const void* q, const int32_t* qo, const void* k, const 
   if (window < 0) return GDPA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return GDPA_ERR_UNSUPPORTED;
   if (H > 256) return GDPA_ERR_UNSUPPORTED;
-  if (act < GDPA_ACT_SOFTMAX || act > GDPA_ACT_IDENTITY) return GDPA_ERR_INVALID_ARG;
+  if (act < GDPA_ACT_SOFTMAX || act > GDPA_ACT_GELU_ERF) return GDPA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return GDPA_ERR_INVALID_ARG;
   if (qo == nullptr || ko == nullptr) return GDPA_ERR_INVALID_ARG;
   if (Tq > 0 && q == nullptr) return GDPA_ERR_INVALID_ARG;

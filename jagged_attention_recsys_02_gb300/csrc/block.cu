@@ -141,6 +141,7 @@ __device__ __forceinline__ float act_fwd(int act, float x) {
     const float h = 0.5f * x;
     return fmaf(h, tanh_approx(u), h);
   }
+  if (act == GDPA_ACT_GELU_ERF) return 0.5f * x * (1.0f + erff(x * 0.7071067811865476f));
   return x;
 }
 
@@ -495,6 +496,7 @@ cudaError_t launch_fwd_d(const BlockParams& p, int act, const CUtensorMap& tq,
     case GDPA_ACT_SOFTMAX: return launch_fwd_one<D, GDPA_ACT_SOFTMAX>(p, tq, tk, tv, grid, s);
     case GDPA_ACT_SILU: return launch_fwd_one<D, GDPA_ACT_SILU>(p, tq, tk, tv, grid, s);
     case GDPA_ACT_GELU_TANH: return launch_fwd_one<D, GDPA_ACT_GELU_TANH>(p, tq, tk, tv, grid, s);
+    case GDPA_ACT_GELU_ERF: return launch_fwd_one<D, GDPA_ACT_GELU_ERF>(p, tq, tk, tv, grid, s);
     default: return launch_fwd_one<D, GDPA_ACT_IDENTITY>(p, tq, tk, tv, grid, s);
   }
 }
@@ -1129,6 +1131,9 @@ cudaError_t launch_bwd_d(const BlockParams& p, int act, const CUtensorMap* m, in
     case GDPA_ACT_GELU_TANH:
       return launch_bwd_one<D, GDPA_ACT_GELU_TANH>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6], grid,
                                                    s);
+    case GDPA_ACT_GELU_ERF:
+      return launch_bwd_one<D, GDPA_ACT_GELU_ERF>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6], grid,
+                                                  s);
     default:
       return launch_bwd_one<D, GDPA_ACT_IDENTITY>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6], grid,
                                                   s);

@@ -730,6 +730,7 @@ cudaError_t launch_main_d(const BwdParams& p, int act, const CUtensorMap& tq, co
     case GDPA_ACT_SILU: return launch_main<D, GDPA_ACT_SILU>(p, tq, tk, tv, tdo, tdq, grid, s);
     case GDPA_ACT_GELU_TANH:
       return launch_main<D, GDPA_ACT_GELU_TANH>(p, tq, tk, tv, tdo, tdq, grid, s);
+    case GDPA_ACT_GELU_ERF: return launch_main<D, GDPA_ACT_GELU_ERF>(p, tq, tk, tv, tdo, tdq, grid, s);
     default: return launch_main<D, GDPA_ACT_IDENTITY>(p, tq, tk, tv, tdo, tdq, grid, s);
   }
 }

@@ -83,7 +83,8 @@ __host__ __device__ __forceinline__ void band_query_tiles(int c_begin, int c_end
 
 // GDPA activation and its derivative: SiLU x sigmoid(x) and GELU-tanh
 // 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) through tanh.approx (for
-// SiLU via sigmoid(x) = 0.5 + 0.5 tanh(x / 2)); identity otherwise.
+// SiLU via sigmoid(x) = 0.5 + 0.5 tanh(x / 2)), GELU-erf x Phi(x) through
+// erff; identity otherwise.
 template <int ACT>
 __device__ __forceinline__ void act_and_grad(float x, float& a, float& g) {
   if (ACT == GDPA_ACT_SILU) {
@@ -100,6 +101,11 @@ __device__ __forceinline__ void act_and_grad(float x, float& a, float& g) {
     a = fmaf(h, t, h);
     // 0.5 (1 + t) + 0.5 x (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 x^2)
     g = fmaf(0.5f, t, 0.5f) + h * (1.0f - t * t) * fmaf(3.0f * k1, x2, k0);
+  } else if (ACT == GDPA_ACT_GELU_ERF) {
+    // Phi(x) = 0.5 (1 + erf(x / sqrt 2)); act = x Phi(x), act' = Phi(x) + x phi(x)
+    const float cdf = fmaf(0.5f, erff(x * 0.7071067811865476f), 0.5f);
+    a = x * cdf;
+    g = fmaf(x * 0.3989422804014327f, expf(-0.5f * x * x), cdf);
   } else {
     a = x;
     g = 1.0f;

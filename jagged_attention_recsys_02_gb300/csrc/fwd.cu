@@ -95,6 +95,7 @@ __device__ __forceinline__ float act_apply(int act, float x) {
     const float h = 0.5f * x;
     return fmaf(h, tanh_approx(u), h);
   }
+  if (act == GDPA_ACT_GELU_ERF) return 0.5f * x * (1.0f + erff(x * 0.7071067811865476f));
   return x;  // identity
 }
 
@@ -689,6 +690,8 @@ cudaError_t launch_d(const FwdParams& p, int act, const CUtensorMap& tq, const C
     case GDPA_ACT_SILU: return launch_one<D, GDPA_ACT_SILU, kBand>(p, tq, tk, tv, grid, stream);
     case GDPA_ACT_GELU_TANH:
       return launch_one<D, GDPA_ACT_GELU_TANH, kBand>(p, tq, tk, tv, grid, stream);
+    case GDPA_ACT_GELU_ERF:
+      return launch_one<D, GDPA_ACT_GELU_ERF, kBand>(p, tq, tk, tv, grid, stream);
     default: return launch_one<D, GDPA_ACT_IDENTITY, kBand>(p, tq, tk, tv, grid, stream);
   }
 }

@@ -35,7 +35,7 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-ACTS = {"softmax": 0, "silu": 1, "gelu_tanh": 2, "identity": 3}
+ACTS = {"softmax": 0, "silu": 1, "gelu_tanh": 2, "identity": 3, "gelu_erf": 4}
 
 CONFIG_NAMES = ("tiny_silu", "jfa_causal_relpos", "gdpa_cross_gelu", "gdpa_pma_silu", "heavy_tail")
 EXTRA_NAMES = ("swa_causal_relpos", "block_relpos")

@@ -48,7 +48,7 @@ def _oracle_fwd(q, k, v, o, act, causal, scale, bias, max_rel):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh", "identity"])
+@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh", "identity", "gelu_erf"])
 @pytest.mark.parametrize("causal", [False, True])
 def test_block_fwd_parity(d, act, causal):
     H = 2
@@ -123,7 +123,7 @@ def _run_bwd(q, od, k, v, do, act, causal, scale, bias, max_rel):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh"])
+@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh", "gelu_erf"])
 @pytest.mark.parametrize("causal", [False, True])
 def test_block_bwd_parity(d, act, causal):
     H = 2

@@ -77,7 +77,7 @@ RAGGED_Q = [1, 63, 64, 65, 127, 128, 129, 0, 300, 513, 7]
 RAGGED_KV = [5, 128, 0, 129, 200, 256, 384, 3, 1, 513, 700]
 
 
-@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh", "identity"])
+@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh", "identity", "gelu_erf"])
 @pytest.mark.parametrize("d", [64, 128])
 def test_bwd_ragged(act, d):
     _case(RAGGED_Q, RAGGED_KV, 2, d, act)

@@ -47,7 +47,7 @@ def _case(lq, lkv, H, d, act, causal=False, max_rel=0, seed=0):
     return out
 
 
-@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh", "identity"])
+@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh", "identity", "gelu_erf"])
 @pytest.mark.parametrize("d", [64, 128])
 def test_fwd_ragged(act, d):
     _case(RAGGED_Q, RAGGED_KV, 2, d, act)

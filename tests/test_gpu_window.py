@@ -41,7 +41,7 @@ def _np_bias(bias):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh"])
+@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh", "gelu_erf"])
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("window", [1, 77, 128, 200, 384])
 def test_window_fwd_parity(d, act, causal, window):

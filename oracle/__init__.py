@@ -11,7 +11,9 @@ Every function follows the definition written out at the top of
 Efficiency of Its LLM-Scale Ads Foundation Model" (JFA paragraph: jagged
 tensors, custom biases, asymmetric Q/KV lengths, backward; GDPA paragraph:
 two matmuls with an elementwise activation in between; low-precision
-paragraph: MXFP8 block scaling).
+paragraph: MXFP8 block scaling; SWA / block paragraph: sliding windows,
+64-token blocks and the rotary-embedding backward fused into the block
+kernel's epilogue).
 """
 from .oracle import (  # noqa: F401
     ACT_GELU_ERF,
@@ -27,4 +29,6 @@ from .oracle import (  # noqa: F401
     fwd,
     quant_cols,
     quant_rows,
+    rope_bwd,
+    rope_fwd,
 )

@@ -1,4 +1,5 @@
-"""ctypes front end of the fp64 oracle (test infrastructure only).
+"""ctypes front end of the fp64 oracle (test infrastructure only), plus the
+rotary embedding (RoPE) in numpy float64.
 
 All inputs are converted to float64 numpy arrays before the call; the bf16
 values the GPU sees convert to float64 exactly, so the oracle works on the
@@ -180,3 +181,35 @@ def quant_cols(x, offsets):
     _load().oracle_quant_cols(_p(x, ctypes.c_double), _p(o, ctypes.c_int32), B, H, d,
                               _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_uint8))
     return codes, scales
+
+
+# ------------------------------------------------------------------ rotary embedding
+def _rope_angles(offsets, d: int, base: float):
+    """Angle [T, d/2] of channel pair c at each token: pos * base^(-2c/d), pos the
+    token's position within its sample."""
+    o = _i32(offsets)
+    pos = np.concatenate([np.arange(int(o[b + 1]) - int(o[b]), dtype=np.float64)
+                          for b in range(len(o) - 1)] or [np.zeros(0)])
+    inv = float(base) ** (-2.0 * np.arange(d // 2, dtype=np.float64) / d)
+    return pos[:, None] * inv[None, :]
+
+
+def rope_fwd(x, offsets, base: float):
+    """Rotary position embedding (rotate-half form): channel pairs (c, c + d/2)
+    rotated by pos * base^(-2c/d).  x [T,H,d] -> float64 [T,H,d]."""
+    x = _f64(x)
+    d = x.shape[2]
+    a = _rope_angles(offsets, d, base)[:, None, :]
+    c, s = np.cos(a), np.sin(a)
+    x1, x2 = x[..., : d // 2], x[..., d // 2:]
+    return np.concatenate([x1 * c - x2 * s, x1 * s + x2 * c], axis=-1)
+
+
+def rope_bwd(g, offsets, base: float):
+    """Gradient through rope_fwd: the transposed rotation R(pos)^T applied to g."""
+    g = _f64(g)
+    d = g.shape[2]
+    a = _rope_angles(offsets, d, base)[:, None, :]
+    c, s = np.cos(a), np.sin(a)
+    g1, g2 = g[..., : d // 2], g[..., d // 2:]
+    return np.concatenate([g1 * c + g2 * s, -g1 * s + g2 * c], axis=-1)

@@ -706,3 +706,53 @@ def test_gelu_forms_differ_and_match_their_definitions(oracle_mod):
     np.testing.assert_allclose(out_e[:, 0, 1], ref_e, rtol=1e-14, atol=1e-15)
     np.testing.assert_allclose(out_t[:, 0, 1], ref_t, rtol=1e-14, atol=1e-15)
     assert np.abs(out_e - out_t).max() > 1e-4
+
+
+# --------------------------------------------------------------- rotary embedding
+def test_rope_closed_form_and_identities(oracle_mod):
+    """d = 2: one pair rotated by exactly pos radians (theta_0 = 1); position 0 is
+    the identity; the backward is the inverse (R is orthogonal), so it undoes the
+    forward and keeps norms."""
+    x = np.array([[[1.0, 0.0]], [[0.0, 1.0]], [[0.6, -0.8]], [[2.0, 3.0]]])
+    o = _offsets([4])
+    y = oracle_mod.rope_fwd(x, o, 10000.0)
+    for p_, (a, b) in enumerate(x[:, 0]):
+        np.testing.assert_allclose(y[p_, 0], [a * math.cos(p_) - b * math.sin(p_),
+                                              a * math.sin(p_) + b * math.cos(p_)], rtol=1e-15, atol=1e-15)
+    lengths = [5, 0, 9]
+    z = _bf16_randn((sum(lengths), 3, 16), 80)
+    oo = _offsets(lengths)
+    rz = oracle_mod.rope_fwd(z, oo, 500.0)
+    np.testing.assert_array_equal(rz[0], z[0])        # sample 0, position 0
+    np.testing.assert_array_equal(rz[5], z[5])        # sample 2 restarts at position 0
+    np.testing.assert_allclose(oracle_mod.rope_bwd(rz, oo, 500.0), z, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(np.linalg.norm(rz, axis=-1), np.linalg.norm(z, axis=-1), rtol=1e-13)
+
+
+def test_rope_scores_depend_on_relative_position(oracle_mod):
+    """RoPE's defining property: <R(m) q, R(n) k> depends on m - n only."""
+    d, L = 32, 12
+    q = _bf16_randn((1, 1, d), 81).repeat(L, 0)
+    k = _bf16_randn((1, 1, d), 82).repeat(L, 0)
+    o = _offsets([L])
+    rq, rk = oracle_mod.rope_fwd(q, o, 10000.0), oracle_mod.rope_fwd(k, o, 10000.0)
+    s = np.einsum("ic,jc->ij", rq[:, 0], rk[:, 0])
+    for delta in range(-L + 1, L):
+        diag = np.diagonal(s, offset=-delta)
+        np.testing.assert_allclose(diag, diag[0], rtol=1e-12, atol=1e-12)
+
+
+def test_rope_backward_is_the_gradient(oracle_mod):
+    """<rope_fwd(x), g> differentiated by central differences equals rope_bwd(g)."""
+    rng = np.random.default_rng(83)
+    x = rng.normal(size=(7, 2, 8))
+    g = rng.normal(size=(7, 2, 8))
+    o = _offsets([3, 4])
+    h = 1e-6
+    num = np.zeros_like(x)
+    for idx in np.ndindex(*x.shape):
+        xp = x.copy(); xp[idx] += h
+        xm = x.copy(); xm[idx] -= h
+        num[idx] = (np.sum(oracle_mod.rope_fwd(xp, o, 100.0) * g) -
+                    np.sum(oracle_mod.rope_fwd(xm, o, 100.0) * g)) / (2 * h)
+    np.testing.assert_allclose(oracle_mod.rope_bwd(g, o, 100.0), num, rtol=1e-8, atol=1e-8)

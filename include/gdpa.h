@@ -162,11 +162,19 @@ gdpa_status gdpa_block_fwd(const void* q, const int32_t* offsets, const void* k,
  * kernel recomputes the block's scores and exact softmax, forms D = sum_j P
  * dP inside the tile and writes every gradient row once (no atomics, no
  * logsumexp or forward output needed).  Rows of a sample never see another
- * sample's tokens.  Arguments, workspace and errors as gdpa_block_fwd. */
+ * sample's tokens.
+ * rope_base > 0 fuses the rotary-embedding backward into the epilogue (the
+ * same paragraph: "fusing RoPE backward into the attention epilogue"): q and
+ * k are taken to be rotary-embedded (rotate-half form: channels c and c + d/2
+ * rotated by pos * rope_base^(-2c/d), pos the token's position in its
+ * sample), and dq, dk are returned with respect to the un-rotated q and k
+ * (the transposed rotation applied to the fp32 gradients).  rope_base = 0:
+ * no rotary embedding; negative or non-finite: GDPA_ERR_INVALID_ARG.
+ * Other arguments, workspace and errors as gdpa_block_fwd. */
 gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k, const void* v,
                            int B, int H, int d, int64_t T, const gdpa_bias* bias, int act,
-                           int causal, float scale, const void* dout, void* dq, void* dk, void* dv,
-                           void* workspace, size_t ws_bytes, void* stream);
+                           int causal, float scale, float rope_base, const void* dout, void* dq,
+                           void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream);
 
 /* MXFP8 block quantisation (OCP Microscaling Formats v1.0; "GEM Training ..."
  * low-precision paragraph: attention with MXFP8 block-scaled MMA).  Elements

@@ -113,7 +113,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                        I, F, vp, vp, sz, vp]
         lib.gdpa_block_fwd.restype = I
         lib.gdpa_block_bwd.argtypes = [vp, vp, vp, vp, I, I, I, i64, ctypes.POINTER(gdpa_bias), I,
-                                       I, F, vp, vp, vp, vp, vp, sz, vp]
+                                       I, F, F, vp, vp, vp, vp, vp, sz, vp]
         lib.gdpa_block_bwd.restype = I
         _lib = lib
         return lib
@@ -233,8 +233,9 @@ def gdpa_block_fwd(q, offsets, k, v, *, act, causal=False, scale, bias=None, max
 
 
 def gdpa_block_bwd(q, offsets, k, v, dout, *, act, causal=False, scale, bias=None, max_rel=0,
-                   dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """Block-aligned attention backward through the C ABI.  Returns (dq, dk, dv)."""
+                   rope_base=0.0, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Block-aligned attention backward through the C ABI.  Returns (dq, dk, dv);
+    with rope_base > 0, dq and dk are gradients of the un-rotated q and k."""
     lib = load()
     T, H, d = q.shape
     B = offsets.numel() - 1
@@ -246,7 +247,7 @@ def gdpa_block_bwd(q, offsets, k, v, dout, *, act, causal=False, scale, bias=Non
                                 dtype=torch.uint8)
     rc = lib.gdpa_block_bwd(_ptr(q), _ptr(offsets), _ptr(k), _ptr(v), B, H, d, T,
                             _bias(bias, max_rel), _act(act), int(bool(causal)), float(scale),
-                            _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                            float(rope_base), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
                             workspace.numel(), _stream(stream))
     _check(rc, "gdpa_block_bwd")
     return dq, dk, dv

@@ -435,11 +435,12 @@ gdpa_status gdpa_block_fwd(const void* q, const int32_t* offsets, const void* k,
 
 gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k, const void* v,
                            int B, int H, int d, int64_t T, const gdpa_bias* bias, int act,
-                           int causal, float scale, const void* dout, void* dq, void* dk, void* dv,
-                           void* workspace, size_t ws_bytes, void* stream) {
+                           int causal, float scale, float rope_base, const void* dout, void* dq,
+                           void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream) {
   t_launches = 0;
   gdpa_status st = check_common(q, offsets, k, v, offsets, B, H, d, T, T, bias, act, causal, 0);
   if (st != GDPA_OK) return st;
+  if (!(rope_base >= 0.0f) || rope_base > 3.0e38f) return GDPA_ERR_INVALID_ARG;  // NaN, < 0, inf
   if (T > 0 && (dout == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
                 !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)))
     return GDPA_ERR_INVALID_ARG;
@@ -475,6 +476,7 @@ gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k,
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.rope_base = rope_base;
   p.status = dev->status;
   const int64_t max_items = max_block_tiles(B, T) * H;
   const int grid = static_cast<int>(max_items < dev->sms ? max_items : dev->sms);

@@ -37,7 +37,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kListThreads = 1024;
 
 // ---------------------------------------------------------------- tile list
-// tiles[t] = {first row, rows of block 2t, rows of block 2t+1 (0 if none), 0}.
+// tiles[t] = {first row, rows of block 2t, rows of block 2t+1 (0 if none) | 1 << 16 if
+// that block continues the first one's sample, position of the first row in its sample}.
 __global__ void __launch_bounds__(kListThreads, 1)
 block_list_kernel(const int32_t* __restrict__ offs, int B, long long T, int4* __restrict__ tiles,
                   int* __restrict__ n_tiles, int* __restrict__ status) {
@@ -91,9 +92,9 @@ block_list_kernel(const int32_t* __restrict__ offs, int B, long long T, int4* __
       if ((g & 1) == 0) {
         t[0] = offs[b] + kBlk * r;
         t[1] = len;
-        t[3] = 0;
+        t[3] = kBlk * r;
       } else {
-        t[2] = len;
+        t[2] = len | (r > 0 ? 1 << 16 : 0);  // block r > 0 follows block r - 1 of its sample
       }
     }
     __syncthreads();
@@ -111,11 +112,17 @@ struct TileInfo {
   int row0;       // first global row of the tile
   int len_a;      // rows of the first block
   int rows;       // rows of both blocks
+  int pos_a;      // position of the first row in its sample
+  bool cont;      // the second block belongs to the first one's sample
+  // position of tile row r in its sample
+  __device__ __forceinline__ int pos(int r) const {
+    return (r < len_a || cont) ? pos_a + r : r - len_a;
+  }
 };
 
 __device__ __forceinline__ TileInfo load_tile(const int4* tiles, int t) {
   const int4 v = tiles[t];
-  return TileInfo{v.x, v.y, v.y + v.z};
+  return TileInfo{v.x, v.y, v.y + (v.z & 0xFFFF), v.w, (v.z >> 16) != 0};
 }
 
 // Keys [*c_lo, *c_hi) of tile row r (tile-local columns): the row's own block,
@@ -1015,6 +1022,39 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     const uint32_t col[3] = {kColDP, kColDK, kColDV};
     const float mul[3] = {p.scale, p.scale, 1.0f};
     const CUtensorMap* maps[3] = {&tmap_dq, &tmap_dk, &tmap_dv};
+    // theta_c = base^(-2c/d) = exp2(c * rope_k)
+    const float rope_k = p.rope_base > 0.0f ? -2.0f * log2f(p.rope_base) / D : 0.0f;
+    // Gradient `which` (dQ, dK, dV) of this row, channels [32j, 32j+32) and the
+    // matching half [d/2 + 32j, ...), scaled, as bf16 pairs.  With a rotary
+    // embedding, dQ and dK go back through it here, in fp32: the pair (c, c+d/2)
+    // is rotated by -pos * theta_c (the rotary backward, fused).
+    auto grad_pair = [&](int which, int j, int pos, uint32_t (&pk)[2][16]) {
+      uint32_t v1[32], v2[32];
+      tmem_ld32(tmem + lane_off + col[which] + 32 * j, v1);
+      tmem_ld32(tmem + lane_off + col[which] + 32 * j + D / 2, v2);
+      const bool rot = p.rope_base > 0.0f && which < 2;
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        float a[2], b[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float g1 = __uint_as_float(v1[i + e]) * mul[which];
+          float g2 = __uint_as_float(v2[i + e]) * mul[which];
+          if (rot) {
+            float sn, cs;
+            sincosf(static_cast<float>(pos) * exp2f(static_cast<float>(32 * j + i + e) * rope_k), &sn, &cs);
+            const float r1 = fmaf(g1, cs, g2 * sn);
+            const float r2 = fmaf(g2, cs, -g1 * sn);
+            g1 = r1;
+            g2 = r2;
+          }
+          a[e] = g1;
+          b[e] = g2;
+        }
+        pk[0][i / 2] = pack_bf16x2(a[0], a[1]);
+        pk[1][i / 2] = pack_bf16x2(b[0], b[1]);
+      }
+    };
     uint32_t n_round = 0;
     bool stores_pending = false;
     for (int k = 0;; ++k) {
@@ -1025,6 +1065,7 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       bool w = mbar_wait(bar(C::kGradFull), k & 1u, abort_flag);
       if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
       tc_fence_after();
+      const int pos = ti.pos(r);
       // (GDPA tiles pass P and dS through the buffer twice each: there the
       // activation warps need it back sooner than a staged epilogue returns it)
       if (!kSoftmax || ti.rows < kTileRows) {
@@ -1034,18 +1075,17 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
 #pragma unroll
         for (int which = 0; which < 3; ++which) {
 #pragma unroll 1
-          for (int chunk = 0; chunk < D / 32; ++chunk) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_off + col[which] + 32 * chunk, v);
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul[which],
-                                  __uint_as_float(v[2 * i + 1]) * mul[which]);
+          for (int j = 0; j < D / 64; ++j) {
+            uint32_t pk[2][16];
+            grad_pair(which, j, pos, pk);
             if (r < ti.rows) {
-              uint4* out = reinterpret_cast<uint4*>(dst[which] + 32 * chunk);
 #pragma unroll
-              for (int q = 0; q < 4; ++q) out[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+              for (int h = 0; h < 2; ++h) {
+                uint4* out = reinterpret_cast<uint4*>(dst[which] + 32 * j + (D / 2) * h);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  out[q] = make_uint4(pk[h][4 * q], pk[h][4 * q + 1], pk[h][4 * q + 2], pk[h][4 * q + 3]);
+              }
             }
           }
         }
@@ -1062,15 +1102,11 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
           if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); ok = false; break; }
         }
 #pragma unroll 1
-        for (int chunk = 0; chunk < D / 32; ++chunk) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + col[which] + 32 * chunk, v);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul[which],
-                                __uint_as_float(v[2 * i + 1]) * mul[which]);
-          ps_store_row<1>(ps, r, 32 * chunk, pk);  // [channel atom][row][64 channels], swizzled
+        for (int j = 0; j < D / 64; ++j) {
+          uint32_t pk[2][16];
+          grad_pair(which, j, pos, pk);
+          ps_store_row<1>(ps, r, 32 * j, pk[0]);  // [channel atom][row][64 channels], swizzled
+          ps_store_row<1>(ps, r, 32 * j + D / 2, pk[1]);
         }
         if (which == 2) {
           tc_fence_before();

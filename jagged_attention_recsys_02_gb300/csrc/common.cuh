@@ -172,6 +172,7 @@ struct BlockParams {
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
+  float rope_base;                // > 0: dq, dk go back through the rotary embedding
   int* status;
 };
 

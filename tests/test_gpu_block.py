@@ -170,3 +170,51 @@ def test_block_bwd_long_sequence_workload_sampled():
                                 block=BLOCK)
         for got, ref, nm in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
             assert_close(to_np(got[sl]), ref, BWD_TOL, f"block_relpos sample {b} {nm}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("act", ["softmax", "silu"])
+def test_block_bwd_fused_rope(d, act):
+    """q and k arrive rotary-embedded; with rope_base the kernel returns dq, dk
+    for the un-rotated inputs: the oracle's attention backward on the rotated
+    inputs followed by its rotary backward.  dv is unchanged by the rotation."""
+    H, base = 2, 10000.0
+    q, k, v, do, o, od, _ = _inputs(LENGTHS, H, d, 0, seed=23 + d)
+    scale = 1.0 / math.sqrt(d)
+    bufs = [guarded(sum(LENGTHS), H, d, DEV) for _ in range(3)]
+    binding.gdpa_block_bwd(q, od, k, v, do, act=act, scale=scale, rope_base=base,
+                           dq=bufs[0][1], dk=bufs[1][1], dv=bufs[2][1])
+    assert binding.device_status() == 0
+    for b, _ in bufs:
+        check_guards(b)
+    rq, rk, rv = oracle.bwd(to_np(q), o, to_np(k), to_np(v), o, to_np(do), act=ACTS[act],
+                            scale=scale, block=BLOCK)
+    rq, rk = oracle.rope_bwd(rq, o, base), oracle.rope_bwd(rk, o, base)
+    what = f"block bwd rope {act} d={d}"
+    assert_close(to_np(bufs[0][1]), rq, BWD_TOL, what + " dq")
+    assert_close(to_np(bufs[1][1]), rk, BWD_TOL, what + " dk")
+    assert_close(to_np(bufs[2][1]), rv, BWD_TOL, what + " dv")
+
+
+def test_block_bwd_fused_rope_long_positions():
+    """Positions up to 16k (large rotation angles): rows [15360, 16000) of one
+    16,000-token sample, whose blocks depend on themselves only."""
+    H, d, L, a, base = 1, 128, 16000, 15360, 10000.0
+    q, k, v, do, o, od, _ = _inputs([L], H, d, 0, seed=99)
+    scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = binding.gdpa_block_bwd(q, od, k, v, do, act="softmax", scale=scale,
+                                        rope_base=base)
+    assert binding.device_status() == 0
+    ob = np.array([0, L - a], dtype=np.int32)
+    sl = slice(a, L)
+    rq, rk, rv = oracle.bwd(to_np(q[sl]), ob, to_np(k[sl]), to_np(v[sl]), ob, to_np(do[sl]), act=0,
+                            scale=scale, block=BLOCK)
+
+    def rope_at(g):  # rotary backward at positions a .. L-1
+        pad = np.zeros((L, H, d))
+        pad[a:] = g
+        return oracle.rope_bwd(pad, np.array([0, L], dtype=np.int32), base)[a:]
+
+    assert_close(to_np(dq[sl]), rope_at(rq), BWD_TOL, "rope dq at long positions")
+    assert_close(to_np(dk[sl]), rope_at(rk), BWD_TOL, "rope dk at long positions")
+    assert_close(to_np(dv[sl]), rv, BWD_TOL, "dv")

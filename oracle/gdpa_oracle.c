@@ -31,6 +31,9 @@
  *   softmax: ds_ij = p_ij (dp_ij - sum_j' p_ij' dp_ij')
  *   GDPA:    ds_ij = act'(s_ij) dp_ij
  *   dq_i  = scale * sum_j ds_ij k_j,   dk_j = scale * sum_i ds_ij q_i
+ *   dbias_h[t] = sum over unmasked (i, j) of sample b with table index
+ *                clamp(i - j + max_rel - 1) == t of ds_ij   (the bias enters s
+ *                with weight 1; a learnable table's gradient)
  *
  * Readings taken where the pages are silent:
  *   - SiLU(x) = x * sigmoid(x); GELU is the tanh form
@@ -210,11 +213,12 @@ int oracle_fwd(const double* q, const int32_t* qo, const double* k, const double
 }
 
 /* Backward.  dq must be [Tq][H][d]; dk, dv [Tkv][H][d].  All three are
- * overwritten.  Returns 0 on success, -1 on bad arguments. */
+ * overwritten.  dbias, if not NULL, is [H][2*max_rel-1] and overwritten with
+ * the bias table's gradient.  Returns 0 on success, -1 on bad arguments. */
 int oracle_bwd(const double* q, const int32_t* qo, const double* k, const double* v,
                const int32_t* ko, int B, int H, int d, const double* bias, int max_rel, int act,
                int causal, int window, int block, double scale, const double* dout, double* dq,
-               double* dk, double* dv) {
+               double* dk, double* dv, double* dbias) {
   if (B < 0 || H <= 0 || d <= 0 || act < 0 || act > 4) return -1;
   if (!check_offsets(qo, B) || !check_offsets(ko, B)) return -1;
   if (window < 0 || block < 0) return -1;
@@ -222,6 +226,14 @@ int oracle_bwd(const double* q, const int32_t* qo, const double* k, const double
     for (int b = 0; b < B; ++b)
       if (qo[b + 1] - qo[b] != ko[b + 1] - ko[b]) return -1;
   const long nwork = (long)B * H;
+  const long width = 2L * (max_rel > 0 ? max_rel : 1) - 1;
+  if (dbias != NULL)
+    for (long t = 0; t < (long)H * width; ++t) dbias[t] = 0.0;
+  /* per-(sample, head) partial sums of the bias gradient, added in a fixed
+   * order after the parallel loop */
+  double* part = dbias != NULL ? (double*)calloc((size_t)(nwork > 0 ? nwork : 1) * (size_t)width,
+                                                 sizeof(double))
+                               : NULL;
 #pragma omp parallel for schedule(dynamic, 1)
   for (long w = 0; w < nwork; ++w) {
     const int b = (int)(w / H), h = (int)(w % H);
@@ -265,12 +277,23 @@ int oracle_bwd(const double* q, const int32_t* qo, const double* k, const double
           dkj[c] += scale * ds * qi[c];
           dvj[c] += p[j] * doi[c];
         }
+        if (part != NULL) {
+          long t = (i - j) + (max_rel - 1);
+          if (t < 0) t = 0;
+          if (t > width - 1) t = width - 1;
+          part[w * width + t] += ds;
+        }
       }
     }
     free(s);
     free(p);
     free(dp);
     free(live);
+  }
+  if (part != NULL) {
+    for (long w = 0; w < nwork; ++w)
+      for (long t = 0; t < width; ++t) dbias[(w % H) * width + t] += part[w * width + t];
+    free(part);
   }
   return 0;
 }

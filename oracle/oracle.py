@@ -49,7 +49,7 @@ def _load():
         I, D = ctypes.c_int, ctypes.c_double
         lib.oracle_fwd.argtypes = [dp, ip, dp, dp, ip, I, I, I, dp, I, I, I, I, I, D, dp, dp]
         lib.oracle_fwd.restype = I
-        lib.oracle_bwd.argtypes = [dp, ip, dp, dp, ip, I, I, I, dp, I, I, I, I, I, D, dp, dp, dp, dp]
+        lib.oracle_bwd.argtypes = [dp, ip, dp, dp, ip, I, I, I, dp, I, I, I, I, I, D, dp, dp, dp, dp, dp]
         lib.oracle_bwd.restype = I
         lib.oracle_e4m3_encode.argtypes = [D]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
@@ -120,8 +120,10 @@ def fwd(q, q_offsets, k, v, kv_offsets, *, act: int, causal: bool = False, scale
 
 
 def bwd(q, q_offsets, k, v, kv_offsets, dout, *, act: int, causal: bool = False, scale: float,
-        bias=None, max_rel: int = 0, window: int = 0, block: int = 0):
-    """Backward pass.  Returns (dq, dk, dv) as float64 arrays."""
+        bias=None, max_rel: int = 0, window: int = 0, block: int = 0, want_dbias: bool = False):
+    """Backward pass.  Returns (dq, dk, dv) as float64 arrays, and with
+    want_dbias also the bias table's gradient [H, 2*max_rel-1]:
+    (dq, dk, dv, dbias)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
     qo, ko = _i32(q_offsets), _i32(kv_offsets)
     Tq, H, d = q.shape
@@ -130,17 +132,20 @@ def bwd(q, q_offsets, k, v, kv_offsets, dout, *, act: int, causal: bool = False,
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
+    dbias = np.zeros((H, 2 * max(int(max_rel), 1) - 1), dtype=np.float64) if want_dbias else None
     keep, bp = _bias_arg(bias, H, max_rel)
     rc = _load().oracle_bwd(_p(q, ctypes.c_double), _p(qo, ctypes.c_int32),
                             _p(k, ctypes.c_double), _p(v, ctypes.c_double),
                             _p(ko, ctypes.c_int32), B, H, d, bp, int(max_rel), int(act),
                             int(bool(causal)), int(window), int(block), float(scale),
                             _p(do, ctypes.c_double), _p(dq, ctypes.c_double),
-                            _p(dk, ctypes.c_double), _p(dv, ctypes.c_double))
+                            _p(dk, ctypes.c_double), _p(dv, ctypes.c_double),
+                            _p(dbias, ctypes.c_double) if dbias is not None
+                            else ctypes.POINTER(ctypes.c_double)())
     if rc != 0:
         raise ValueError("oracle_bwd rejected its arguments")
     del keep
-    return dq, dk, dv
+    return (dq, dk, dv, dbias) if want_dbias else (dq, dk, dv)
 
 
 def e4m3_encode(x: float) -> int:

@@ -756,3 +756,36 @@ def test_rope_backward_is_the_gradient(oracle_mod):
         num[idx] = (np.sum(oracle_mod.rope_fwd(xp, o, 100.0) * g) -
                     np.sum(oracle_mod.rope_fwd(xm, o, 100.0) * g)) / (2 * h)
     np.testing.assert_allclose(oracle_mod.rope_bwd(g, o, 100.0), num, rtol=1e-8, atol=1e-8)
+
+
+# --------------------------------------------------------------- bias table gradient
+@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH])
+@pytest.mark.parametrize("variant", ["plain", "causal", "window", "clamped"])
+def test_dbias_matches_central_differences(oracle_mod, act, variant):
+    """The bias table's gradient against central differences of the forward in
+    every table entry (a 'clamped' table is shorter than the samples, so its end
+    entries collect many offsets)."""
+    H, d = 2, 5
+    max_rel = 2 if variant == "clamped" else 6
+    lq = [4, 6, 0]
+    causal = variant == "causal"
+    window = 3 if variant == "window" else 0
+    lkv = lq if (causal or window) else [5, 3, 2]
+    rng = np.random.default_rng(400 + act)
+    q = rng.normal(size=(sum(lq), H, d))
+    k = rng.normal(size=(sum(lkv), H, d))
+    v = rng.normal(size=(sum(lkv), H, d))
+    do = rng.normal(size=(sum(lq), H, d))
+    table = rng.normal(0, 0.5, size=(H, 2 * max_rel - 1))
+    qo, ko = _offsets(lq), _offsets(lkv)
+    kw = dict(act=act, causal=causal, window=window, scale=0.45, max_rel=max_rel)
+    *_, db = oracle_mod.bwd(q, qo, k, v, ko, do, bias=table, want_dbias=True, **kw)
+    h = 1e-6
+    num = np.zeros_like(table)
+    for idx in np.ndindex(*table.shape):
+        tp = table.copy(); tp[idx] += h
+        tm = table.copy(); tm[idx] -= h
+        op, _ = oracle_mod.fwd(q, qo, k, v, ko, bias=tp, **kw)
+        om, _ = oracle_mod.fwd(q, qo, k, v, ko, bias=tm, **kw)
+        num[idx] = (np.sum(op * do) - np.sum(om * do)) / (2 * h)
+    np.testing.assert_allclose(db, num, rtol=1e-7, atol=1e-8)

@@ -126,7 +126,16 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
  * GDPA_ERR_INVALID_ARG.  Key / query tiles outside the band are never
  * loaded, and the scheduler's cost counts only the tiles inside it.  Every
  * other argument, output, workspace and error is that of gdpa_fwd /
- * gdpa_bwd; the backward must get the forward's window. */
+ * gdpa_bwd; the backward must get the forward's window.
+ * dbias (gdpa_bwd_window only; NULL = not computed): the gradient of a
+ * learnable relative-position table ("custom attention biases", JFA
+ * paragraph), fp32 device memory [H][2*max_rel-1], ADDED to (so gradients of
+ * several calls accumulate; zero it first for a fresh gradient): entry t
+ * receives the sum of dS_ij over the unmasked pairs whose clamped table
+ * index (i - j + max_rel - 1) is t.  Needs a GDPA_BIAS_RELPOS bias
+ * (GDPA_ERR_INVALID_ARG otherwise) and the softmax activation
+ * (GDPA_ERR_UNSUPPORTED otherwise).  Its atomics make the sums' order, and
+ * so their last bits, vary between runs. */
 gdpa_status gdpa_fwd_window(const void* q, const int32_t* q_offsets, const void* k,
                             const void* v, const int32_t* kv_offsets, int B, int H, int d,
                             int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
@@ -136,8 +145,8 @@ gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void*
                             const void* v, const int32_t* kv_offsets, int B, int H, int d,
                             int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
                             int window, float scale, const void* out, const float* lse,
-                            const void* dout, void* dq, void* dk, void* dv, void* workspace,
-                            size_t ws_bytes, void* stream);
+                            const void* dout, void* dq, void* dk, void* dv, float* dbias,
+                            void* workspace, size_t ws_bytes, void* stream);
 
 /* Block-aligned attention ("GEM Training ..." SWA paragraph: with fixed
  * 64-token blocks each query block attends only to its own key/value block,

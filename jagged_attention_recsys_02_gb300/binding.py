@@ -83,7 +83,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdpa_bwd.restype = I
         lib.gdpa_bwd_window.argtypes = [vp, vp, vp, vp, vp, I, I, I, i64, i64,
                                         ctypes.POINTER(gdpa_bias), I, I, I, F, vp, vp, vp, vp, vp,
-                                        vp, vp, sz, vp]
+                                        vp, vp, vp, sz, vp]
         lib.gdpa_bwd_window.restype = I
         lib.gdpa_get_device_status.argtypes = [vp]
         lib.gdpa_get_device_status.restype = I
@@ -183,10 +183,11 @@ def gdpa_fwd(q, q_offsets, k, v, kv_offsets, *, act, causal=False, scale, bias=N
 
 
 def gdpa_bwd(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, act, causal=False, scale,
-             bias=None, max_rel=0, window=0, dq=None, dk=None, dv=None, workspace=None,
-             stream=None):
+             bias=None, max_rel=0, window=0, dq=None, dk=None, dv=None, dbias=None,
+             workspace=None, stream=None):
     """Backward pass through the C ABI (gdpa_bwd, or gdpa_bwd_window when
-    window > 0).  Returns (dq, dk, dv)."""
+    window > 0 or a bias-table gradient `dbias` [H, 2*max_rel-1] fp32 is given,
+    which is added to).  Returns (dq, dk, dv)."""
     lib = load()
     Tq, H, d = q.shape
     Tkv = k.shape[0]
@@ -199,13 +200,13 @@ def gdpa_bwd(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, act, causal=Fals
                                 dtype=torch.uint8)
     head = (_ptr(q), _ptr(q_offsets), _ptr(k), _ptr(v), _ptr(kv_offsets), B, H, d, Tq, Tkv,
             _bias(bias, max_rel), _act(act), int(bool(causal)))
-    tail = (float(scale), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
-            _ptr(workspace), workspace.numel(), _stream(stream))
-    if window:
-        rc = lib.gdpa_bwd_window(*head, int(window), *tail)
+    tail = (float(scale), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv))
+    ws = (_ptr(workspace), workspace.numel(), _stream(stream))
+    if window or dbias is not None:
+        rc = lib.gdpa_bwd_window(*head, int(window), *tail, _ptr(dbias), *ws)
     else:
-        rc = lib.gdpa_bwd(*head, *tail)
-    _check(rc, "gdpa_bwd_window" if window else "gdpa_bwd")
+        rc = lib.gdpa_bwd(*head, *tail, *ws)
+    _check(rc, "gdpa_bwd_window" if (window or dbias is not None) else "gdpa_bwd")
     return dq, dk, dv
 
 

@@ -269,19 +269,25 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
                      void* workspace, size_t ws_bytes, void* stream) {
   return gdpa_bwd_window(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act, causal, 0,
-                         scale, out, lse, dout, dq, dk, dv, workspace, ws_bytes, stream);
+                         scale, out, lse, dout, dq, dk, dv, nullptr, workspace, ws_bytes, stream);
 }
 
 gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void* k,
                             const void* v, const int32_t* kv_offsets, int B, int H, int d,
                             int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
                             int window, float scale, const void* out, const float* lse,
-                            const void* dout, void* dq, void* dk, void* dv, void* workspace,
-                            size_t ws_bytes, void* stream) {
+                            const void* dout, void* dq, void* dk, void* dv, float* dbias,
+                            void* workspace, size_t ws_bytes, void* stream) {
   t_launches = 0;
   gdpa_status st = check_common(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act,
                                 causal, window);
   if (st != GDPA_OK) return st;
+  if (dbias != nullptr) {
+    // the gradient of a relative-position table needs that table
+    if (bias == nullptr || bias->kind != GDPA_BIAS_RELPOS) return GDPA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(dbias) & 3u) return GDPA_ERR_INVALID_ARG;
+    if (act != GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
+  }
   if (Tq > 0 && (dout == nullptr || dq == nullptr || !aligned16(dout) || !aligned16(dq)))
     return GDPA_ERR_INVALID_ARG;
   if (Tkv > 0 && (dk == nullptr || dv == nullptr || !aligned16(dk) || !aligned16(dv)))
@@ -353,6 +359,7 @@ gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void*
   p.dout = static_cast<const __nv_bfloat16*>(dout);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.dbias = dbias;
   p.dq_acc = dq_acc;
   p.delta = delta;
   p.items = items;

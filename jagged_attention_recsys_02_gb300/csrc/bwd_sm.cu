@@ -82,7 +82,11 @@ struct SmCfg {
   static constexpr int kStats = kDs + kDsBytes;
   static constexpr int kDqStageBytes = kDqChunk * D * 4;       // [16 queries][d] fp32
   static constexpr int kDqStage = kStats + kQStages * kStatFloats * 4;  // two buffers
-  static constexpr int kBar = kDqStage + 2 * kDqStageBytes;
+  // bias-table gradient: per tile, dS summed along its 255 diagonals (two
+  // buffers of 256 floats, then {first diagonal, head})
+  static constexpr int kDbBuf = 256 * 4 + 16;
+  static constexpr int kDb = kDqStage + 2 * kDqStageBytes;
+  static constexpr int kBar = kDb + 2 * kDbBuf;
   static constexpr int kKvFull = 0, kKvEmpty = 1;
   static constexpr int kQFull = 2;                    // + stage
   static constexpr int kQEmpty = kQFull + kQStages;   // + stage
@@ -99,7 +103,9 @@ struct SmCfg {
   static constexpr int kItemFull = kDkvEmpty + 1;     // + slot
   static constexpr int kItemEmpty = kItemFull + 2;
   static constexpr int kDrain = kItemEmpty + 2;
-  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kDbAcc = kDrain + 1;     // + buffer: the activation warps added a tile
+  static constexpr int kDbFree = kDbAcc + 2;    // + buffer: flushed to the table and zeroed
+  static constexpr int kNumBars = kDbFree + 2;
   static constexpr int kItemSlots = kBar + 8 * kNumBars;
   static constexpr int kTmemSlot = kItemSlots + 16;
   static constexpr int kAbort = kTmemSlot + 4;
@@ -146,7 +152,7 @@ __device__ __forceinline__ SmItem decode_sm(int2 it, const BwdParams& p) {
   return r;
 }
 
-template <int D, bool kBand>
+template <int D, bool kBand, bool kDBias>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
               const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
@@ -186,11 +192,18 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     mbar_init(bar(C::kDkvEmpty), 4);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kItemFull + s), 1);
-      mbar_init(bar(C::kItemEmpty + s), 1 + kActWarps + 4);
+      mbar_init(bar(C::kItemEmpty + s), 1 + kActWarps + 4 + (kDBias ? 1 : 0));
     }
     mbar_init(bar(C::kDrain), 1);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(bar(C::kDbAcc + u), kActWarps);
+      mbar_init(bar(C::kDbFree + u), 1);
+    }
     fence_mbar_init();
   }
+  if (kDBias)
+    for (int i = threadIdx.x; i < 2 * C::kDbBuf / 4; i += kThreads)
+      reinterpret_cast<float*>(gbase + C::kDb)[i] = 0.0f;
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
@@ -582,6 +595,8 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         // product is taken on bf16 pairs: dS goes to the MMAs as bf16 anyway,
         // and the extra rounding of dP - D adds at most 2^-9 relative error.
         w = mbar_wait(bar(C::kDpFull), g & 1u, abort_flag);
+        // the diagonal buffer of this tile was flushed two tiles ago
+        if (kDBias) w = w && mbar_wait(bar(C::kDbFree + (g & 1u)), ((g >> 1) & 1u) ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); abort_now = true; break; }
         tc_fence_after();
         // dS^T row j, query atom grp: 16-byte chunk cc (8 queries) at (cc ^ (j % 8))
@@ -611,10 +626,28 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
             *reinterpret_cast<uint4*>(dsrow + ((cc ^ (j & 7)) * 16)) =
                 make_uint4(dh[4 * v], dh[4 * v + 1], dh[4 * v + 2], dh[4 * v + 3]);
           }
+          if (kDBias) {
+            // dS(query c, key j) lies on diagonal c - j + 127 of the tile: a
+            // warp's lanes hit consecutive words (no bank conflicts)
+            float* win = reinterpret_cast<float*>(gbase + C::kDb + (g & 1u) * C::kDbBuf) + (127 - j);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              atomicAdd(win + c0 + 2 * e, __uint_as_float(dh[e] << 16));
+              atomicAdd(win + c0 + 2 * e + 1, __uint_as_float(dh[e] & 0xFFFF0000u));
+            }
+          }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         warp_arrive(bar(C::kDsFull), lane);
+        if (kDBias) {
+          if (j == 0 && grp == 0) {
+            int* meta = reinterpret_cast<int*>(gbase + C::kDb + (g & 1u) * C::kDbBuf + 256 * 4);
+            meta[0] = qloc - kb0 - 127;  // diagonal (query - key) of window entry 0
+            meta[1] = in.head;
+          }
+          warp_arrive(bar(C::kDbAcc + (g & 1u)), lane);
+        }
       }
       if (abort_now) break;
     }
@@ -726,6 +759,41 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     if (r == 0) bulk_wait_group_all();  // every dQ reduce issued by this thread has landed
   } else {
     setmaxnreg_dec<kRegsLow>();  // spare warps of the last warpgroup
+    if (kDBias && warp == kMmaWarp + 1) {
+      // ---------------------------------------------------------- bias-table gradient
+      // Per tile: wait for the activation warps' diagonal sums, add them to the
+      // table (entry = clamp(query - key + max_rel - 1)), zero the buffer.
+      const int width = 2 * p.max_rel - 1;
+      uint32_t it = 0, g = 0;
+      while (true) {
+        const uint32_t slot = it & 1u;
+        bool w = mbar_wait(bar(C::kItemFull + slot), (it >> 1) & 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+        const int2 item = item_slot[slot];
+        warp_arrive(bar(C::kItemEmpty + slot), lane);
+        ++it;
+        if (item.x < 0) break;
+        const SmItem in = decode_sm<kBand>(item, p);
+        bool abort_now = false;
+        for (int t = 0; t < in.nq; ++t, ++g) {
+          const uint32_t u = g & 1u;
+          w = mbar_wait(bar(C::kDbAcc + u), (g >> 1) & 1u, abort_flag);
+          if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); abort_now = true; break; }
+          float* win = reinterpret_cast<float*>(gbase + C::kDb + u * C::kDbBuf);
+          const int* meta = reinterpret_cast<const int*>(win + 256);
+          const int delta0 = meta[0];
+          float* row = p.dbias + static_cast<long long>(meta[1]) * width;
+          for (int e = lane; e < 255; e += 32) {
+            const float v = win[e];
+            if (v != 0.0f) atomicAdd(row + min(max(e + delta0 + p.max_rel - 1, 0), width - 1), v);
+            win[e] = 0.0f;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(C::kDbFree + u));
+        }
+        if (abort_now) break;
+      }
+    }
   }
 
   tc_fence_before();
@@ -736,16 +804,16 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   }
 }
 
-template <int D, bool kBand>
+template <int D, bool kBand, bool kDBias>
 cudaError_t launch_sm(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                       int grid, cudaStream_t s) {
   using C = SmCfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(bwd_sm_kernel<D, kBand>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_sm_kernel<D, kBand, kDBias>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  bwd_sm_kernel<D, kBand><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, tdq, p);
+  bwd_sm_kernel<D, kBand, kDBias><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
 
@@ -754,11 +822,20 @@ cudaError_t launch_sm(const BwdParams& p, const CUtensorMap& tq, const CUtensorM
 cudaError_t launch_bwd_softmax_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                                     const CUtensorMap& tv, const CUtensorMap& tdo,
                                     const CUtensorMap& tdq, int grid, cudaStream_t s) {
-  if (p.window > 0)
-    return p.d == 64 ? launch_sm<64, true>(p, tq, tk, tv, tdo, tdq, grid, s)
-                     : launch_sm<128, true>(p, tq, tk, tv, tdo, tdq, grid, s);
-  return p.d == 64 ? launch_sm<64, false>(p, tq, tk, tv, tdo, tdq, grid, s)
-                   : launch_sm<128, false>(p, tq, tk, tv, tdo, tdq, grid, s);
+  const bool band = p.window > 0, db = p.dbias != nullptr;
+#define GDPA_SM_LAUNCH(DD, BB, DBB) \
+  if (p.d == DD && band == BB && db == DBB) \
+    return launch_sm<DD, BB, DBB>(p, tq, tk, tv, tdo, tdq, grid, s);
+  GDPA_SM_LAUNCH(64, false, false)
+  GDPA_SM_LAUNCH(64, false, true)
+  GDPA_SM_LAUNCH(64, true, false)
+  GDPA_SM_LAUNCH(64, true, true)
+  GDPA_SM_LAUNCH(128, false, false)
+  GDPA_SM_LAUNCH(128, false, true)
+  GDPA_SM_LAUNCH(128, true, false)
+  GDPA_SM_LAUNCH(128, true, true)
+#undef GDPA_SM_LAUNCH
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace gdpa

@@ -150,6 +150,7 @@ struct BwdParams {
   const __nv_bfloat16* dout;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
+  float* dbias;             // fp32 [H][2*max_rel-1], added to (nullptr: not computed)
   float* dq_acc;            // fp32 [Tq][H][d] accumulator (zeroed by the preprocess kernel)
   float* delta;             // fp32 [H][Tq]: rowsum(dO * O) for softmax
   const int2* items;

@@ -135,17 +135,23 @@ def test_window_entry_points_reject_on_host(lib):
                                    None, 0, 1, window, 0.125, FAKE, FAKE, a["ws"], 1 << 20, None)
 
     def bwd_w(window, **kw):
-        a = dict(d=64)
+        a = dict(d=64, bias=None, act=0, dbias=None)
         a.update(kw)
-        return lib.gdpa_bwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, a["d"], 10, 10, None, 0, 1,
-                                   window, 0.125, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
-                                   1 << 20, None)
+        return lib.gdpa_bwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, a["d"], 10, 10, a["bias"],
+                                   a["act"], 1, window, 0.125, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                   a["dbias"], FAKE, 1 << 20, None)
 
     for call in (fwd_w, bwd_w):
         assert call(-1) == INVALID
         assert call(5, d=96) == UNSUPPORTED
     assert fwd_w(5, q=None) == INVALID
     assert fwd_w(5, ws=None) == WORKSPACE
+    # a bias-table gradient needs a relative-position table, 4-byte alignment
+    # and (for now) the softmax activation
+    table = ctypes.byref(binding.gdpa_bias(binding.BIAS_RELPOS, FAKE, 8))
+    assert bwd_w(0, dbias=FAKE) == INVALID
+    assert bwd_w(0, dbias=FAKE + 2, bias=table) == INVALID
+    assert bwd_w(0, dbias=FAKE, bias=table, act=1) == UNSUPPORTED
     mx = lib.gdpa_fwd_mxfp8_window(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 10,
                                    10, None, 0, 1, -3, 0.125, FAKE, FAKE, FAKE, 1 << 20, None)
     assert mx == INVALID

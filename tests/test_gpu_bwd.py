@@ -160,3 +160,73 @@ def test_bwd_full_gdpa_pma_silu():
 @pytest.mark.parametrize("act", ["softmax", "silu"])
 def test_bwd_full_heavy_tail(act):
     _full_config("heavy_tail", act=act, budget=1.5e6)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("variant", ["full", "causal", "window", "clamped"])
+def test_dbias_softmax(d, variant):
+    """Gradient of the relative-position table (softmax backward) against the
+    oracle's; it is added to, so a second call doubles it."""
+    H = 2
+    causal = variant in ("causal", "window")
+    window = 150 if variant == "window" else 0
+    max_rel = 40 if variant == "clamped" else 600
+    lq = [1, 129, 300, 0, 257, 64, 511]
+    lkv = lq if causal else [5, 200, 128, 3, 300, 64, 400]
+    g = torch.Generator(device=DEV).manual_seed(50 + d)
+    q = rand_bf16((sum(lq), H, d), g, DEV)
+    k = rand_bf16((sum(lkv), H, d), g, DEV)
+    v = rand_bf16((sum(lkv), H, d), g, DEV)
+    do = rand_bf16((sum(lq), H, d), g, DEV)
+    bias = torch.randn(H, 2 * max_rel - 1, generator=g, device=DEV) * 0.5
+    qo_np, ko_np = offsets(lq), offsets(lkv)
+    qo, ko = torch.from_numpy(qo_np).to(DEV), torch.from_numpy(ko_np).to(DEV)
+    scale = 1.0 / math.sqrt(d)
+    kw = dict(act=0, causal=causal, scale=scale, bias=bias, max_rel=max_rel, window=window)
+    out, lse = binding.gdpa_fwd(q, qo, k, v, ko, **kw)
+    dbias = torch.zeros_like(bias)
+    binding.gdpa_bwd(q, qo, k, v, ko, out, lse, do, dbias=dbias, **kw)
+    assert binding.device_status() == 0
+    tb = bias.cpu().double().numpy()
+    *_, ref = oracle.bwd(to_np(q), qo_np, to_np(k), to_np(v), ko_np, to_np(do), act=0, causal=causal,
+                         scale=scale, bias=tb, max_rel=max_rel, window=window, want_dbias=True)
+    # Each table entry sums dS over many pairs, so the per-pair rounding adds
+    # up: the kernel's D = rowsum(dO * O) uses the bf16-rounded O (relative
+    # error <= 2^-9 per element) and dS is formed from bf16 P and dP - D and
+    # rounded to bf16 (2^-9 each).  Tolerance: the elementwise bound plus
+    # 4 * sum over the entry's pairs of |P| 2^-8 (|dP - D| + sum_c |dO_c O_c|),
+    # from fp64 quantities of the same inputs.
+    o_ref, _ = oracle.fwd(to_np(q), qo_np, to_np(k), to_np(v), ko_np, act=0, causal=causal,
+                          scale=scale, bias=tb, max_rel=max_rel, window=window)
+    qn, kn, vn, don = to_np(q), to_np(k), to_np(v), to_np(do)
+    err = np.zeros_like(ref)
+    for b in range(len(lq)):
+        q0, q1, k0, k1 = int(qo_np[b]), int(qo_np[b + 1]), int(ko_np[b]), int(ko_np[b + 1])
+        if q1 == q0 or k1 == k0:
+            continue
+        i = np.arange(q1 - q0)[:, None]
+        j = np.arange(k1 - k0)[None, :]
+        live = np.ones((q1 - q0, k1 - k0), bool)
+        if causal:
+            live &= j <= i
+        if window:
+            live &= np.abs(i - j) < window
+        t = np.clip(i - j + max_rel - 1, 0, 2 * max_rel - 2)
+        for h in range(H):
+            s_ = scale * qn[q0:q1, h] @ kn[k0:k1, h].T + tb[h][t]
+            s_ = np.where(live, s_, -np.inf)
+            pm = np.exp(s_ - s_.max(1, keepdims=True))
+            pm /= pm.sum(1, keepdims=True)
+            dp = don[q0:q1, h] @ vn[k0:k1, h].T
+            dd = (don[q0:q1, h] * o_ref[q0:q1, h]).sum(1, keepdims=True)
+            od = np.abs(don[q0:q1, h] * o_ref[q0:q1, h]).sum(1, keepdims=True)
+            e = pm * 2.0 ** -8 * (np.abs(dp - dd) + od)
+            np.add.at(err[h], t[live], e[live])
+    got = dbias.cpu().double().numpy()
+    bound = BWD_TOL[0] + BWD_TOL[1] * np.abs(ref) + 4 * err
+    assert np.all(np.abs(got - ref) <= bound), \
+        f"dbias {variant} d={d}: worst err/bound {float((np.abs(got - ref) / bound).max()):.3f}"
+    first = dbias.clone()
+    binding.gdpa_bwd(q, qo, k, v, ko, out, lse, do, dbias=dbias, **kw)
+    assert binding.device_status() == 0
+    torch.testing.assert_close(dbias, 2 * first, rtol=1e-5, atol=1e-6)

@@ -133,9 +133,8 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
  * several calls accumulate; zero it first for a fresh gradient): entry t
  * receives the sum of dS_ij over the unmasked pairs whose clamped table
  * index (i - j + max_rel - 1) is t.  Needs a GDPA_BIAS_RELPOS bias
- * (GDPA_ERR_INVALID_ARG otherwise) and the softmax activation
- * (GDPA_ERR_UNSUPPORTED otherwise).  Its atomics make the sums' order, and
- * so their last bits, vary between runs. */
+ * (GDPA_ERR_INVALID_ARG otherwise); every activation.  Its atomics make the
+ * sums' order, and so their last bits, vary between runs. */
 gdpa_status gdpa_fwd_window(const void* q, const int32_t* q_offsets, const void* k,
                             const void* v, const int32_t* kv_offsets, int B, int H, int d,
                             int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,

@@ -286,7 +286,6 @@ gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void*
     // the gradient of a relative-position table needs that table
     if (bias == nullptr || bias->kind != GDPA_BIAS_RELPOS) return GDPA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(dbias) & 3u) return GDPA_ERR_INVALID_ARG;
-    if (act != GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
   }
   if (Tq > 0 && (dout == nullptr || dq == nullptr || !aligned16(dout) || !aligned16(dq)))
     return GDPA_ERR_INVALID_ARG;

@@ -63,7 +63,11 @@ struct BwdCfg {
   static constexpr int kDqStageBytes = kBwdQRows * 64 * 4;
   static constexpr int kDqBufs = 1;
   static constexpr int kDqStage = kStats + kStages * kStatFloats * 4;
-  static constexpr int kBar = kDqStage + kDqBufs * kDqStageBytes;
+  // bias-table gradient: per tile, dS summed along its 191 diagonals (two
+  // buffers of 192 floats, then {first diagonal, head})
+  static constexpr int kDbBuf = 192 * 4 + 16;
+  static constexpr int kDb = kDqStage + kDqBufs * kDqStageBytes;
+  static constexpr int kBar = kDb + 2 * kDbBuf;
   static constexpr int kKvFull = 0, kKvEmpty = 1;
   static constexpr int kQdFull = 2;                 // + s
   static constexpr int kQdEmpty = kQdFull + kStages;
@@ -76,7 +80,9 @@ struct BwdCfg {
   static constexpr int kItemFull = kDkvEmpty + 1;   // + slot
   static constexpr int kItemEmpty = kItemFull + 2;
   static constexpr int kDrain = kItemEmpty + 2;
-  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kDbAcc = kDrain + 1;     // + buffer: the activation threads added a tile
+  static constexpr int kDbFree = kDbAcc + 2;    // + buffer: flushed to the table and zeroed
+  static constexpr int kNumBars = kDbFree + 2;
   static constexpr int kItemSlots = kBar + 8 * kNumBars;
   static constexpr int kTmemSlot = kItemSlots + 16;
   static constexpr int kAbort = kTmemSlot + 4;
@@ -115,8 +121,10 @@ __device__ __forceinline__ BwdItem decode_bwd(int2 it, const BwdParams& p) {
   return r;
 }
 
-template <int D, int ACT>
-__global__ void __launch_bounds__(kThreads, 1)
+// With a bias-table gradient one more warp (14) adds each tile's diagonal
+// sums to the table.
+template <int D, int ACT, bool kDBias>
+__global__ void __launch_bounds__(kThreads + (kDBias ? 32 : 0), 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
            const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
            const __grid_constant__ CUtensorMap tmap_dq, const BwdParams p) {
@@ -154,11 +162,18 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
     mbar_init(bar(C::kDkvEmpty), 128);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kItemFull + s), 1);
-      mbar_init(bar(C::kItemEmpty + s), 1 + kActThreads + 128);
+      mbar_init(bar(C::kItemEmpty + s), 1 + kActThreads + 128 + (kDBias ? 1 : 0));
     }
     mbar_init(bar(C::kDrain), 1);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(bar(C::kDbAcc + u), kActThreads);
+      mbar_init(bar(C::kDbFree + u), 1);
+    }
     fence_mbar_init();
   }
+  if (kDBias)
+    for (int i = threadIdx.x; i < 2 * C::kDbBuf / 4; i += blockDim.x)
+      reinterpret_cast<float*>(gbase + C::kDb)[i] = 0.0f;
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
@@ -455,6 +470,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         const uint32_t buf = t & 1;
         w = mbar_wait(bar(C::kQdFull + s), (g / C::kStages) & 1u, abort_flag);
         w = w && mbar_wait(bar(C::kSFull + buf), suse[buf] & 1u, abort_flag);
+        // the diagonal buffer of this tile was flushed two tiles ago
+        if (kDBias) w = w && mbar_wait(bar(C::kDbFree + (g & 1u)), ((g >> 1) & 1u) ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); abort_now = true; break; }
         suse[buf]++;
         tc_fence_after();
@@ -501,6 +518,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
                 pv[e] = 0.0f;
                 dv[e] = 0.0f;
               }
+              // dS(query c, key j) lies on diagonal c - j + 127 of the tile
+              if (kDBias)
+                atomicAdd(reinterpret_cast<float*>(gbase + C::kDb + (g & 1u) * C::kDbBuf) + c - j + 127,
+                          dv[e]);
             }
             const uint32_t ph = pack_bf16x2(pv[0], pv[1]);
             const uint32_t dh = pack_bf16x2(dv[0], dv[1]);
@@ -534,6 +555,49 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(C::kPFull));
+        if (kDBias) {
+          if (j == 0 && cbase == 0) {
+            int* meta = reinterpret_cast<int*>(gbase + C::kDb + (g & 1u) * C::kDbBuf + 192 * 4);
+            meta[0] = qloc - kb0 - 127;  // diagonal (query - key) of window entry 0
+            meta[1] = in.head;
+          }
+          mbar_arrive(bar(C::kDbAcc + (g & 1u)));
+        }
+      }
+      if (abort_now) break;
+    }
+  } else if (kDBias && warp == kMmaWarp + 1) {
+    // ------------------------------------------------------------ bias-table gradient
+    // Per tile: wait for the activation threads' diagonal sums, add them to the
+    // table (entry = clamp(query - key + max_rel - 1)), zero the buffer.
+    const int width = 2 * p.max_rel - 1;
+    uint32_t it = 0, g = 0;
+    while (true) {
+      const uint32_t slot = it & 1u;
+      bool w = mbar_wait(bar(C::kItemFull + slot), (it >> 1) & 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+      const int2 item = item_slot[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kItemEmpty + slot));
+      ++it;
+      if (item.x < 0) break;
+      const BwdItem in = decode_bwd(item, p);
+      bool abort_now = false;
+      for (int t = 0; t < in.nq; ++t, ++g) {
+        const uint32_t u = g & 1u;
+        w = mbar_wait(bar(C::kDbAcc + u), (g >> 1) & 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); abort_now = true; break; }
+        float* win = reinterpret_cast<float*>(gbase + C::kDb + u * C::kDbBuf);
+        const int* meta = reinterpret_cast<const int*>(win + 192);
+        const int delta0 = meta[0];
+        float* row = p.dbias + static_cast<long long>(meta[1]) * width;
+        for (int e = lane; e < 191; e += 32) {
+          const float v = win[e];
+          if (v != 0.0f) atomicAdd(row + min(max(e + delta0 + p.max_rel - 1, 0), width - 1), v);
+          win[e] = 0.0f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::kDbFree + u));
       }
       if (abort_now) break;
     }
@@ -710,16 +774,25 @@ dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long l
   }
 }
 
+template <int D, int ACT, bool kDBias>
+cudaError_t launch_main_db(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                           int grid, cudaStream_t s) {
+  using C = BwdCfg<D, ACT != GDPA_ACT_SOFTMAX>;
+  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, ACT, kDBias>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  bwd_kernel<D, ACT, kDBias><<<grid, kThreads + (kDBias ? 32 : 0), C::kSmemBytes, s>>>(tq, tk, tv,
+                                                                                     tdo, tdq, p);
+  return cudaGetLastError();
+}
+
 template <int D, int ACT>
 cudaError_t launch_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                         int grid, cudaStream_t s) {
-  using C = BwdCfg<D, ACT != GDPA_ACT_SOFTMAX>;
-  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, ACT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  bwd_kernel<D, ACT><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, tdq, p);
-  return cudaGetLastError();
+  return p.dbias != nullptr ? launch_main_db<D, ACT, true>(p, tq, tk, tv, tdo, tdq, grid, s)
+                            : launch_main_db<D, ACT, false>(p, tq, tk, tv, tdo, tdq, grid, s);
 }
 
 template <int D>

@@ -146,12 +146,11 @@ def test_window_entry_points_reject_on_host(lib):
         assert call(5, d=96) == UNSUPPORTED
     assert fwd_w(5, q=None) == INVALID
     assert fwd_w(5, ws=None) == WORKSPACE
-    # a bias-table gradient needs a relative-position table, 4-byte alignment
-    # and (for now) the softmax activation
+    # a bias-table gradient needs a relative-position table and 4-byte alignment
     table = ctypes.byref(binding.gdpa_bias(binding.BIAS_RELPOS, FAKE, 8))
     assert bwd_w(0, dbias=FAKE) == INVALID
     assert bwd_w(0, dbias=FAKE + 2, bias=table) == INVALID
-    assert bwd_w(0, dbias=FAKE, bias=table, act=1) == UNSUPPORTED
+    assert bwd_w(0, dbias=FAKE + 2, bias=table, act=1) == INVALID
     mx = lib.gdpa_fwd_mxfp8_window(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 10,
                                    10, None, 0, 1, -3, 0.125, FAKE, FAKE, FAKE, 1 << 20, None)
     assert mx == INVALID

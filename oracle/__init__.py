@@ -23,12 +23,18 @@ from .oracle import (  # noqa: F401
     ACT_SOFTMAX,
     build,
     bwd,
+    bwd_mx_operands,
+    bwd_mxfp8,
+    dequant_cols,
+    dequant_rows,
     e4m3_decode,
     e4m3_encode,
+    e8m0_nosat,
     e8m0_scale,
     fwd,
     quant_cols,
     quant_rows,
     rope_bwd,
+    round_blocks_2d,
     rope_fwd,
 )

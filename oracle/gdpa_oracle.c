@@ -417,3 +417,138 @@ void oracle_quant_cols(const double* x, const int32_t* offs, int B, int H, int d
     }
   }
 }
+
+/* ------------------------------------------------------------ MXFP8 backward
+ *
+ * The low-precision paragraph runs the backward pass on block-scaled MXFP8
+ * products too.  The pages give no recipe, so this is the plain reading:
+ * every product of the softmax backward takes the E4M3 + E8M0 version of its
+ * operands quantised along that product's contraction axis, and the two
+ * matrices made inside the pass, P and dS, are rounded to E4M3 in blocks of
+ * 32 keys x 32 queries that share one scale (a 32 x 32 block holds a 32-
+ * element block along either axis, so one rounding serves the dK product,
+ * whose contraction runs over queries, and the dQ product, over keys).
+ *
+ *   s_ij  = scale <qd_i, kd_j> + bias(i - j)      qd, kd: along channels
+ *   p_ij  = exp(s_ij - lse_i)  (0 when masked)    lse: the forward's, given
+ *   dp_ij = <dOd_i, vd_j>                         dOd, vd: along channels
+ *   ds_ij = p_ij (dp_ij - delta_i)                delta_i = <dO_i, O_i>, given
+ *   dv_j  = sum_i P_ij dOt_i                      dOt: along tokens
+ *   dk_j  = scale sum_i DS_ij qt_i                qt: along tokens
+ *   dq_i  = scale sum_j DS_ij kt_j                kt: along tokens
+ *
+ * P and DS are p and ds rounded (round_ps = 1) or p and ds (round_ps = 0).
+ * The blocks start at the sample's first key and first query.  A block's
+ * scale is the smallest power of two X with amax / X <= 448 (no element
+ * saturates; see oracle_e8m0_nosat).  Inputs are the decoded operand values
+ * [T][H][d]; lse and delta are [H][Tq].
+ */
+
+/* E8M0 code of the smallest power of two X = 2^(code - 127) with
+ * amax / X <= 448, clamped to [0, 254]; 0 for amax == 0. */
+uint8_t oracle_e8m0_nosat(double amax) {
+  if (!(amax > 0.0)) return 0;
+  int e = (int)ceil(log2(amax / 448.0));
+  /* guard against log2 rounding: the result is the least e with 448 * 2^e >= amax */
+  while (ldexp(448.0, e) < amax) ++e;
+  while (ldexp(448.0, e - 1) >= amax) --e;
+  int code = e + 127;
+  if (code < 0) code = 0;
+  if (code > 254) code = 254;
+  return (uint8_t)code;
+}
+
+/* Rounds m [R][C] (row-major) to E4M3 in 32 x 32 blocks from (0, 0). */
+void oracle_round_blocks_2d(double* m, long R, long C) {
+  for (long r0 = 0; r0 < R; r0 += 32)
+    for (long c0 = 0; c0 < C; c0 += 32) {
+      const long r1 = r0 + 32 < R ? r0 + 32 : R, c1 = c0 + 32 < C ? c0 + 32 : C;
+      double amax = 0.0;
+      for (long r = r0; r < r1; ++r)
+        for (long c = c0; c < c1; ++c)
+          if (fabs(m[r * C + c]) > amax) amax = fabs(m[r * C + c]);
+      const int sc = oracle_e8m0_nosat(amax);
+      const double x = ldexp(1.0, sc - 127);
+      for (long r = r0; r < r1; ++r)
+        for (long c = c0; c < c1; ++c)
+          m[r * C + c] = oracle_e4m3_decode(oracle_e4m3_encode(m[r * C + c] / x)) * x;
+    }
+}
+
+int oracle_bwd_mx(const double* qd, const double* qt, const double* kd, const double* kt,
+                  const double* vd, const double* dod, const double* dot_t, const int32_t* qo,
+                  const int32_t* ko, int B, int H, int d, const double* bias, int max_rel,
+                  int causal, double scale, const double* lse, const double* delta,
+                  int round_ps, double* dq, double* dk, double* dv) {
+  if (B < 0 || H <= 0 || d <= 0) return -1;
+  if (!check_offsets(qo, B) || !check_offsets(ko, B)) return -1;
+  if (causal)
+    for (int b = 0; b < B; ++b)
+      if (qo[b + 1] - qo[b] != ko[b + 1] - ko[b]) return -1;
+  const long Tq = qo[B];
+  const long nwork = (long)B * H;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (long w = 0; w < nwork; ++w) {
+    const int b = (int)(w / H), h = (int)(w % H);
+    const long Lq = qo[b + 1] - qo[b], Lkv = ko[b + 1] - ko[b];
+    const long q0 = qo[b], k0 = ko[b];
+    /* P and dS as [key j][query i] */
+    const size_t n = (size_t)(Lq > 0 ? Lq : 1) * (size_t)(Lkv > 0 ? Lkv : 1);
+    double* P = (double*)calloc(n, sizeof(double));
+    double* DS = (double*)calloc(n, sizeof(double));
+    if (P == NULL || DS == NULL) {
+      free(P);
+      free(DS);
+      bad = 1;
+      continue;
+    }
+    for (long i = 0; i < Lq; ++i) {
+      const double* qi = qd + ((q0 + i) * H + h) * (long)d;
+      const double* doi = dod + ((q0 + i) * H + h) * (long)d;
+      const double l = lse[(long)h * Tq + q0 + i];
+      const double dl = delta[(long)h * Tq + q0 + i];
+      for (long j = 0; j < Lkv; ++j) {
+        if (causal && j > i) continue;
+        const double s = scale * dot(qi, kd + ((k0 + j) * H + h) * (long)d, d) +
+                         bias_at(bias, max_rel, h, i, j);
+        const double p = exp(s - l);
+        const double dp = dot(doi, vd + ((k0 + j) * H + h) * (long)d, d);
+        P[j * Lq + i] = p;
+        DS[j * Lq + i] = p * (dp - dl);
+      }
+    }
+    if (round_ps) {
+      oracle_round_blocks_2d(P, Lkv, Lq);
+      oracle_round_blocks_2d(DS, Lkv, Lq);
+    }
+    for (long j = 0; j < Lkv; ++j) {
+      double* dkj = dk + ((k0 + j) * H + h) * (long)d;
+      double* dvj = dv + ((k0 + j) * H + h) * (long)d;
+      for (int c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
+      for (long i = 0; i < Lq; ++i) {
+        const double pp = P[j * Lq + i], ds = DS[j * Lq + i];
+        if (pp == 0.0 && ds == 0.0) continue;
+        const double* qti = qt + ((q0 + i) * H + h) * (long)d;
+        const double* doi = dot_t + ((q0 + i) * H + h) * (long)d;
+        for (int c = 0; c < d; ++c) {
+          dvj[c] += pp * doi[c];
+          dkj[c] += scale * ds * qti[c];
+        }
+      }
+    }
+    for (long i = 0; i < Lq; ++i) {
+      double* dqi = dq + ((q0 + i) * H + h) * (long)d;
+      for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+      for (long j = 0; j < Lkv; ++j) {
+        const double ds = DS[j * Lq + i];
+        if (ds == 0.0) continue;
+        const double* ktj = kt + ((k0 + j) * H + h) * (long)d;
+        for (int c = 0; c < d; ++c) dqi[c] += scale * ds * ktj[c];
+      }
+    }
+    free(P);
+    free(DS);
+  }
+  return bad ? -2 : 0;
+}

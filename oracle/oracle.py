@@ -61,6 +61,13 @@ def _load():
         lib.oracle_quant_rows.restype = None
         lib.oracle_quant_cols.argtypes = [dp, ip, I, I, I, up, up]
         lib.oracle_quant_cols.restype = None
+        lib.oracle_e8m0_nosat.argtypes = [D]
+        lib.oracle_e8m0_nosat.restype = ctypes.c_uint8
+        lib.oracle_round_blocks_2d.argtypes = [dp, ctypes.c_long, ctypes.c_long]
+        lib.oracle_round_blocks_2d.restype = None
+        lib.oracle_bwd_mx.argtypes = [dp, dp, dp, dp, dp, dp, dp, ip, ip, I, I, I, dp, I, I, D,
+                                      dp, dp, I, dp, dp, dp]
+        lib.oracle_bwd_mx.restype = I
         _lib = lib
         return lib
 
@@ -186,6 +193,97 @@ def quant_cols(x, offsets):
     _load().oracle_quant_cols(_p(x, ctypes.c_double), _p(o, ctypes.c_int32), B, H, d,
                               _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_uint8))
     return codes, scales
+
+
+def e8m0_nosat(amax: float) -> int:
+    """E8M0 code of the smallest power of two X with amax / X <= 448."""
+    return int(_load().oracle_e8m0_nosat(float(amax)))
+
+
+def round_blocks_2d(m):
+    """m [R, C] rounded to E4M3 in 32 x 32 blocks from (0, 0), each block with
+    the scale e8m0_nosat(block amax); returns a new float64 array."""
+    m = np.array(_f64(m), dtype=np.float64, copy=True, order="C")
+    assert m.ndim == 2
+    _load().oracle_round_blocks_2d(_p(m, ctypes.c_double), m.shape[0], m.shape[1])
+    return m
+
+
+_E4M3 = None
+
+
+def _e4m3_table():
+    global _E4M3
+    if _E4M3 is None:
+        _E4M3 = np.array([e4m3_decode(c) for c in range(256)], dtype=np.float64)
+    return _E4M3
+
+
+def dequant_rows(x):
+    """x quantised along channels (quant_rows) and decoded back to float64."""
+    codes, scales = quant_rows(x)
+    return _e4m3_table()[codes] * np.exp2(scales.astype(np.float64) - 127).repeat(32, axis=2)
+
+
+def dequant_cols(x, offsets):
+    """x quantised along tokens (quant_cols) and decoded back to float64."""
+    o = _i32(offsets)
+    codes, scales = quant_cols(x, o)
+    dec = _e4m3_table()[codes]
+    out = np.zeros_like(dec)
+    k = 0
+    for b in range(len(o) - 1):
+        for r in range((int(o[b + 1]) - int(o[b]) + 31) // 32):
+            t0 = int(o[b]) + 32 * r
+            t1 = min(t0 + 32, int(o[b + 1]))
+            out[t0:t1] = dec[t0:t1] * np.exp2(scales[k].astype(np.float64) - 127)[None]
+            k += 1
+    return out
+
+
+def bwd_mx_operands(qd, qt, kd, kt, vd, dod, dot, q_offsets, kv_offsets, lse, delta, *,
+                    causal: bool = False, scale: float, bias=None, max_rel: int = 0,
+                    round_ps: bool = True):
+    """Softmax backward with each product on its own operand version (the
+    definition at the MXFP8 backward section of gdpa_oracle.c): qd, kd, vd, dod
+    feed the channel contractions (S, dP), qt, kt, dot the token contractions
+    (dK, dQ, dV); lse and delta [H, Tq] are given.  P and dS are rounded to
+    E4M3 in 32 x 32 blocks when round_ps.  Returns (dq, dk, dv) float64."""
+    arrs = [_f64(a) for a in (qd, qt, kd, kt, vd, dod, dot)]
+    qo, ko = _i32(q_offsets), _i32(kv_offsets)
+    Tq, H, d = arrs[0].shape
+    B = len(qo) - 1
+    lse_a, delta_a = _f64(lse), _f64(delta)
+    assert lse_a.shape == (H, Tq) and delta_a.shape == (H, Tq)
+    dq = np.zeros((Tq, H, d))
+    dk = np.zeros(arrs[2].shape)
+    dv = np.zeros(arrs[2].shape)
+    keep, bp = _bias_arg(bias, H, max_rel)
+    rc = _load().oracle_bwd_mx(*[_p(a, ctypes.c_double) for a in arrs], _p(qo, ctypes.c_int32),
+                               _p(ko, ctypes.c_int32), B, H, d, bp, int(max_rel),
+                               int(bool(causal)), float(scale), _p(lse_a, ctypes.c_double),
+                               _p(delta_a, ctypes.c_double), int(bool(round_ps)),
+                               _p(dq, ctypes.c_double), _p(dk, ctypes.c_double),
+                               _p(dv, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle_bwd_mx rejected its arguments")
+    del keep
+    return dq, dk, dv
+
+
+def bwd_mxfp8(q, q_offsets, k, v, kv_offsets, out, dout, lse, *, causal: bool = False,
+              scale: float, bias=None, max_rel: int = 0):
+    """The MXFP8 softmax backward on bf16 inputs: Q, K, dO quantised along
+    channels and along tokens, V along channels (quant_rows / quant_cols,
+    decoded), delta = rowsum(dO * O) of the given values, P and dS rounded in
+    32 x 32 blocks.  Returns (dq, dk, dv) float64."""
+    q, k, v, out, dout = (_f64(a) for a in (q, k, v, out, dout))
+    qo, ko = _i32(q_offsets), _i32(kv_offsets)
+    delta = np.einsum("thc,thc->ht", dout, out)
+    return bwd_mx_operands(dequant_rows(q), dequant_cols(q, qo), dequant_rows(k),
+                           dequant_cols(k, ko), dequant_rows(v), dequant_rows(dout),
+                           dequant_cols(dout, qo), qo, ko, lse, delta, causal=causal,
+                           scale=scale, bias=bias, max_rel=max_rel, round_ps=True)
 
 
 # ------------------------------------------------------------------ rotary embedding

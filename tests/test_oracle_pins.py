@@ -789,3 +789,185 @@ def test_dbias_matches_central_differences(oracle_mod, act, variant):
         om, _ = oracle_mod.fwd(q, qo, k, v, ko, bias=tm, **kw)
         num[idx] = (np.sum(op * do) - np.sum(om * do)) / (2 * h)
     np.testing.assert_allclose(db, num, rtol=1e-7, atol=1e-8)
+
+
+# --------------------------------------------------------------- MXFP8 backward
+def test_e8m0_nosat_closed_forms(oracle_mod):
+    """The saturation-free block scale: the smallest power of two X with
+    amax / X <= 448, against hand values and against the OCP rule, which it
+    exceeds by one step exactly when the mantissa of amax is above 1.75."""
+    s = oracle_mod.e8m0_nosat
+    assert s(0.0) == 0
+    assert s(448.0) == 127
+    assert s(np.nextafter(448.0, np.inf)) == 128
+    assert s(1.75) == 119                      # 1.75 / 2^-8 = 448
+    assert s(np.nextafter(1.75, np.inf)) == 120
+    assert s(1.0) == 119                       # 2^-9 would give 512 > 448
+    assert s(2.0 ** -140) == 0                 # below the smallest scale: clamped
+    assert s(2.0 ** 200) == 254
+    for e in range(-100, 100):
+        assert s(448.0 * 2.0 ** e) == 127 + e
+        assert s(449.0 * 2.0 ** e) == 128 + e
+    rng = np.random.default_rng(3)
+    for a in np.exp(rng.uniform(-40, 40, 2000)):
+        m = a / 2.0 ** math.floor(math.log2(a))
+        assert s(a) - oracle_mod.e8m0_scale(a) == (1 if m > 1.75 else 0), a
+
+
+def test_round_blocks_2d_against_torch_float8(oracle_mod):
+    """32 x 32 blocks from (0, 0), edge blocks partial; each block divided by
+    its own scale and rounded as torch's float8_e4m3fn conversion rounds."""
+    rng = np.random.default_rng(4)
+    R, C = 70, 45
+    m = rng.standard_normal((R, C)) * np.exp2(rng.integers(-12, 12, (R, C)))
+    m[40:64, 32:45] = 0.0                      # an all-zero block part
+    r = oracle_mod.round_blocks_2d(m)
+    for r0 in range(0, R, 32):
+        for c0 in range(0, C, 32):
+            blk = m[r0:r0 + 32, c0:c0 + 32]
+            X = 2.0 ** (oracle_mod.e8m0_nosat(np.abs(blk).max()) - 127)
+            assert np.abs(blk).max() / X <= 448.0
+            ref = torch.from_numpy(blk / X).to(torch.float8_e4m3fn).double().numpy() * X
+            np.testing.assert_array_equal(r[r0:r0 + 32, c0:c0 + 32], ref)
+    np.testing.assert_array_equal(oracle_mod.round_blocks_2d(-m), -r)
+
+
+def test_round_blocks_2d_block_independence(oracle_mod):
+    rng = np.random.default_rng(6)
+    m = rng.standard_normal((64, 64))
+    r = oracle_mod.round_blocks_2d(m)
+    m2 = m.copy()
+    m2[31, 31] = 1e4                           # last element of block (0, 0)
+    r2 = oracle_mod.round_blocks_2d(m2)
+    changed = r2 != r
+    assert changed[:32, :32].any()
+    assert not changed[32:, :].any() and not changed[:, 32:].any()
+    # values already on a block's grid stay exact (amax 448 X, X = 2^-3)
+    g = np.array([oracle_mod.e4m3_decode(c) for c in range(0x00, 0x7F)])
+    blk = rng.choice(g, size=(32, 32)) * rng.choice([-1.0, 1.0], size=(32, 32))
+    blk[0, 0] = 448.0
+    np.testing.assert_array_equal(oracle_mod.round_blocks_2d(blk * 2.0 ** -3), blk * 2.0 ** -3)
+
+
+def _mx_inputs(lq, lkv, H, d, seed, causal, with_bias, oracle_mod):
+    qo, ko = _offsets(lq), _offsets(lkv)
+    q = _bf16_randn((sum(lq), H, d), seed)
+    k = _bf16_randn((sum(lkv), H, d), seed + 1)
+    v = _bf16_randn((sum(lkv), H, d), seed + 2)
+    do = _bf16_randn((sum(lq), H, d), seed + 3)
+    max_rel = 20 if with_bias else 0
+    bias = np.random.default_rng(seed).normal(0, 0.5, (H, 2 * max_rel - 1)) if with_bias else None
+    scale = 1.0 / math.sqrt(d)
+    out, lse = oracle_mod.fwd(q, qo, k, v, ko, act=ACT_SOFTMAX, causal=causal, scale=scale,
+                              bias=bias, max_rel=max_rel)
+    delta = np.einsum("thc,thc->ht", do, out)
+    return q, k, v, do, qo, ko, bias, max_rel, scale, out, lse, delta
+
+
+@pytest.mark.parametrize("with_bias", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_mx_operands_reduce_to_the_backward(oracle_mod, causal, with_bias):
+    """With every operand version equal to the unquantised tensor, no rounding
+    of P and dS, and the forward's lse and rowsum(dO * O), the MXFP8 backward's
+    definition is the softmax backward (itself pinned by finite differences)."""
+    lq = [5, 0, 37, 70, 1] if causal else [5, 3, 37, 70, 0]
+    lkv = lq if causal else [9, 0, 33, 64, 4]
+    H, d = 2, 8
+    q, k, v, do, qo, ko, bias, max_rel, scale, out, lse, delta = _mx_inputs(
+        lq, lkv, H, d, 11, causal, with_bias, oracle_mod)
+    got = oracle_mod.bwd_mx_operands(q, q, k, k, v, do, do, qo, ko, lse, delta, causal=causal,
+                                     scale=scale, bias=bias, max_rel=max_rel, round_ps=False)
+    ref = oracle_mod.bwd(q, qo, k, v, ko, do, act=ACT_SOFTMAX, causal=causal, scale=scale,
+                         bias=bias, max_rel=max_rel)
+    for g, r in zip(got, ref):
+        np.testing.assert_allclose(g, r, rtol=1e-10, atol=1e-12)
+
+
+def test_bwd_mx_operands_wiring(oracle_mod):
+    """Each token-contraction operand feeds one gradient, linearly; the channel
+    operands of dP reach dQ and dK but not dV; and dV with distinct versions is
+    the plain backward's dV on (qd, kd) with dout = dOt."""
+    lq = [40, 7, 66]
+    H, d = 2, 16
+    q, k, v, do, qo, ko, bias, max_rel, scale, out, lse, delta = _mx_inputs(
+        lq, lq, H, d, 21, True, True, oracle_mod)
+    rng = np.random.default_rng(8)
+    alt = {n: x + 0.1 * rng.standard_normal(x.shape) for n, x in
+           (("qt", q), ("kt", k), ("dot", do), ("vd", v), ("dod", do))}
+    ops = dict(qd=q, qt=alt["qt"], kd=k, kt=alt["kt"], vd=alt["vd"], dod=alt["dod"], dot=alt["dot"])
+    kw = dict(causal=True, scale=scale, bias=bias, max_rel=max_rel, round_ps=False)
+    order = ["qd", "qt", "kd", "kt", "vd", "dod", "dot"]
+
+    def run(**over):
+        o = dict(ops, **over)
+        return oracle_mod.bwd_mx_operands(*[o[n] for n in order], qo, qo, lse, delta, **kw)
+
+    dq, dk, dv = run()
+    for name, which in (("qt", 1), ("kt", 0), ("dot", 2)):
+        res = run(**{name: 2.0 * ops[name]})
+        for i, (a, b) in enumerate(zip(res, (dq, dk, dv))):
+            np.testing.assert_allclose(a, 2.0 * b if i == which else b, rtol=1e-12, atol=1e-14)
+    for name in ("vd", "dod"):
+        res = run(**{name: ops[name] + 0.3})
+        np.testing.assert_array_equal(res[2], dv)
+        assert not np.allclose(res[0], dq) and not np.allclose(res[1], dk)
+    ref_dv = oracle_mod.bwd(q, qo, k, v, qo, alt["dot"], act=ACT_SOFTMAX, causal=True,
+                            scale=scale, bias=bias, max_rel=max_rel)[2]
+    np.testing.assert_allclose(dv, ref_dv, rtol=1e-10, atol=1e-12)
+
+
+def test_bwd_mx_rounding_bound(oracle_mod):
+    """Rounding P and dS moves each gradient by at most 2^-4 of the sum of the
+    magnitudes of its terms (E4M3 keeps 3 mantissa bits; no block saturates),
+    plus a subnormal allowance."""
+    lq = [64, 33]
+    H, d = 1, 16
+    q, k, v, do, qo, ko, bias, max_rel, scale, out, lse, delta = _mx_inputs(
+        lq, lq, H, d, 31, True, False, oracle_mod)
+    args = (q, q, k, k, v, do, do, qo, qo, lse, delta)
+    exact = oracle_mod.bwd_mx_operands(*args, causal=True, scale=scale, round_ps=False)
+    rounded = oracle_mod.bwd_mx_operands(*args, causal=True, scale=scale, round_ps=True)
+    # sum of |terms| of dv: sum_i |p_ij| |do_i|; of dq, dk through |ds|: recompute p, ds
+    for b in range(len(lq)):
+        s0, s1 = int(qo[b]), int(qo[b + 1])
+        L = s1 - s0
+        S = scale * q[s0:s1, 0] @ k[s0:s1, 0].T
+        P = np.where(np.tril(np.ones((L, L), bool)), np.exp(S - lse[0, s0:s1, None]), 0.0)
+        dS = P * (do[s0:s1, 0] @ v[s0:s1, 0].T - delta[0, s0:s1, None])
+        # an element in its block's subnormal range is off by at most 2^-10 X,
+        # and X < amax / 224 under the saturation-free scale
+        ep = 2.0 ** -4 * np.abs(P) + 2.0 ** -10 * np.abs(P).max() / 224
+        es = 2.0 ** -4 * np.abs(dS) + 2.0 ** -10 * np.abs(dS).max() / 224
+        bv = ep.T @ np.abs(do[s0:s1, 0])
+        bq = scale * es @ np.abs(k[s0:s1, 0])
+        bk = scale * es.T @ np.abs(q[s0:s1, 0])
+        for g, e, bd in ((rounded[0], exact[0], bq), (rounded[1], exact[1], bk),
+                         (rounded[2], exact[2], bv)):
+            assert np.all(np.abs(g[s0:s1, 0] - e[s0:s1, 0]) <= bd * (1 + 1e-9))
+        assert np.abs(rounded[2] - exact[2]).max() > 0   # the rounding does act
+
+
+def test_bwd_mxfp8_on_exactly_representable_inputs(oracle_mod):
+    """Inputs whose every 32-element block (along channels and along tokens)
+    already lies on the E4M3 grid with scale 1 (magnitudes 256..448) are left
+    unchanged by the operand quantisation, so the full MXFP8 backward equals
+    the operand form with one version per tensor."""
+    lq = [40, 64, 9]
+    H, d = 2, 32
+    rng = np.random.default_rng(12)
+    grid = 256.0 * (1.0 + np.arange(7) / 8.0)          # 256 .. 448
+    T = sum(lq)
+    mk = lambda: rng.choice(grid, size=(T, H, d)) * rng.choice([-1.0, 1.0], size=(T, H, d))
+    q, k, v, do = mk(), mk(), mk(), mk()
+    qo = _offsets(lq)
+    scale = 2.0 ** -22
+    out, lse = oracle_mod.fwd(q, qo, k, v, qo, act=ACT_SOFTMAX, causal=True, scale=scale)
+    for x in (q, k, v, do):
+        np.testing.assert_array_equal(oracle_mod.dequant_rows(x), x)
+        np.testing.assert_array_equal(oracle_mod.dequant_cols(x, qo), x)
+    got = oracle_mod.bwd_mxfp8(q, qo, k, v, qo, out, do, lse, causal=True, scale=scale)
+    delta = np.einsum("thc,thc->ht", do, out)
+    ref = oracle_mod.bwd_mx_operands(q, q, k, k, v, do, do, qo, qo, lse, delta, causal=True,
+                                     scale=scale, round_ps=True)
+    for g, r in zip(got, ref):
+        np.testing.assert_array_equal(g, r)

@@ -656,9 +656,11 @@ def run_gpu(args, rank, world, local_rank):
 # ------------------------------------------------------------------ MXFP8 forward
 def run_gpu_mxfp8(args, rank, world, local_rank):
     """Forward on MXFP8 operands: a step quantises Q, K, V (E4M3 + E8M0 block
-    scales) and runs the block-scaled forward (softmax).  FLOPs are the forward's
-    non-padded 4*H*d*pairs; the peak is the FP8 one (2x the measured bf16 peak,
-    the nominal FP8 : BF16 ratio of the part)."""
+    scales) and runs the block-scaled forward (softmax); with --mxfp8-bwd the
+    step also runs the MXFP8 backward (which quantises Q, K, V, dO itself).
+    FLOPs are the non-padded 4*H*d*pairs forward (2.5x that for the backward);
+    the peak is the FP8 one (2x the measured bf16 peak, the nominal FP8 : BF16
+    ratio of the part)."""
     import torch
     import torch.distributed as dist
 
@@ -670,11 +672,16 @@ def run_gpu_mxfp8(args, rank, world, local_rank):
     if world > 1 and not dist.is_initialized():
         dist.init_process_group("nccl", device_id=dev)
     w = make_workload(args.workload or "heavy_tail", act="softmax")
-    t = make_tensors(w, device=dev, seed=rank, with_dout=False)
+    train = args.mxfp8_bwd
+    t = make_tensors(w, device=dev, seed=rank, with_dout=train)
     H, d, Tq, Tkv = w.H, w.d, w.Tq, w.Tkv
     out = torch.empty_like(t["q"])
     lse = torch.empty((H, Tq), device=dev, dtype=torch.float32)
     ws = torch.empty(binding.fwd_workspace_size(w.B, H, d, Tq, Tkv), device=dev, dtype=torch.uint8)
+    if train:
+        ws_b = torch.empty(binding.bwd_mxfp8_workspace_size(w.B, H, d, Tq, Tkv), device=dev,
+                           dtype=torch.uint8)
+        dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
     qc, qs = binding.quantize_mxfp8(t["q"], mode=binding.MX_ALONG_CHANNELS)
     kc, ks = binding.quantize_mxfp8(t["k"], mode=binding.MX_ALONG_CHANNELS)
     vc, vs = binding.quantize_mxfp8(t["v"], t["ko"], mode=binding.MX_ALONG_TOKENS)
@@ -690,7 +697,14 @@ def run_gpu_mxfp8(args, rank, world, local_rank):
         binding.gdpa_fwd_mxfp8(qc, qs, t["qo"], kc, ks, vc, vs, t["ko"], causal=w.causal,
                                scale=w.scale, bias=t["bias"], max_rel=w.max_rel, window=w.window,
                                out=out, lse=lse, workspace=ws)
-        return n + binding.last_launch_count()
+        n += binding.last_launch_count()
+        if train:
+            binding.gdpa_bwd_mxfp8(t["q"], t["qo"], t["k"], t["v"], t["ko"], out, lse, t["dout"],
+                                   causal=w.causal, scale=w.scale, bias=t["bias"],
+                                   max_rel=w.max_rel, window=w.window, dq=dq, dk=dk, dv=dv,
+                                   workspace=ws_b)
+            n += binding.last_launch_count()
+        return n
 
     for _ in range(args.warmup):
         step()
@@ -715,25 +729,41 @@ def run_gpu_mxfp8(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    fwd_ms, _ = binding.timing_collect()
-    flops = w.fwd_flops()
+    fwd_ms, bwd_ms = binding.timing_collect()
+    fwd_flops = w.fwd_flops()
+    bwd_flops = 2.5 * fwd_flops if train else 0.0
+    flops = fwd_flops + bwd_flops
     ms, tot = reduce_over_ranks(e0.elapsed_time(e1), flops * args.steps, dev)
     value = tot / (ms * 1e-3) / 1e12
     peaks, src = load_peaks()
     fp8_peak = 2.0 * float(peaks["bf16_tflops"])
-    k_ms = float(np.mean(fwd_ms))
-    achieved = flops / (k_ms * 1e-3) / 1e12
+    f_ms = float(np.mean(fwd_ms))
+    kernels = {"fwd": {"tflops": fwd_flops / (f_ms * 1e-3) / 1e12, "kernel_ms": f_ms,
+                       "flops_per_launch": fwd_flops}}
+    if train:
+        b_ms = float(np.mean(bwd_ms))
+        kernels["bwd"] = {"tflops": bwd_flops / (b_ms * 1e-3) / 1e12, "kernel_ms": b_ms,
+                          "flops_per_launch": bwd_flops}
+    # the dominant kernel: the one with the larger share of the step
+    dom = "bwd" if train and kernels["bwd"]["kernel_ms"] > f_ms else "fwd"
+    achieved = kernels[dom]["tflops"]
     line = {
-        "metric": "jagged attn MXFP8 fwd TFLOPS (non-padded FLOPs) & % of GB300 FP8 tensor peak",
+        "metric": ("jagged attn MXFP8 fwd+bwd TFLOPS (non-padded FLOPs) & % of GB300 FP8 tensor peak"
+                   if train else
+                   "jagged attn MXFP8 fwd TFLOPS (non-padded FLOPs) & % of GB300 FP8 tensor peak"),
         "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 (E8M0 block scales), fp32 accumulate",
         "data": "synthetic (seeded N(0,1) bf16 inputs, quantised every step)",
         "config": dict(workload_config(w, "inputs larger than L2 (no flush)"),
-                       step="MXFP8 quantise Q,K,V + forward"),
-        "roofline": {"bound": "tensor", "kernel": "MXFP8 forward kernel", "achieved": achieved,
-                     "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
-                     "traffic": load_traffic().get(f"{w.name}/mxfp8/fwd"),
+                       step=("MXFP8 quantise Q,K,V + forward + backward (quantise Q,K,V,dO inside)"
+                             if train else "MXFP8 quantise Q,K,V + forward")),
+        **kernels,
+        "roofline": {"bound": "tensor",
+                     "kernel": "MXFP8 backward kernel" if dom == "bwd" else "MXFP8 forward kernel",
+                     "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": achieved / fp8_peak,
+                     "traffic": load_traffic().get(f"{w.name}/mxfp8/{dom}"),
                      "peak_source": f"2 x bf16_tflops of {src} (nominal FP8:BF16 = 2)"},
         "gpu_launches": launches, "clocks": clk,
     }
@@ -764,7 +794,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--mxfp8", action="store_true",
                     help="time the MXFP8 forward path (quantise + block-scaled forward) instead")
+    ap.add_argument("--mxfp8-bwd", action="store_true",
+                    help="time the MXFP8 training step (forward + backward, all block-scaled)")
     args = ap.parse_args()
+    args.mxfp8 = args.mxfp8 or args.mxfp8_bwd
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     rank = int(os.environ.get("RANK", "0"))

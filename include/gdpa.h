@@ -196,7 +196,9 @@ gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k,
  *     the last may be partial (for V, whose product contracts over keys).
  *     codes [T][H][d] u8; scales [B + T/32 + 1][H][d] u8 where block r of
  *     sample b is scale row b + floor(offsets[b]/32) + r (rows that belong to
- *     no block are not written).  offsets are needed only in this mode.
+ *     no block are not written).  Tokens outside every sample (before
+ *     offsets[0] or from offsets[B] on) get code 0.  offsets are needed only
+ *     in this mode.
  * x is [T][H][d] bf16, 16-byte aligned; all buffers are device memory. */
 enum { GDPA_MX_ALONG_CHANNELS = 0, GDPA_MX_ALONG_TOKENS = 1 };
 size_t gdpa_mxfp8_scale_bytes(int B, int H, int d, int64_t T, int mode);
@@ -230,6 +232,34 @@ gdpa_status gdpa_fwd_mxfp8_window(const void* q_codes, const void* q_scales,
                                   const int32_t* kv_offsets, int B, int H, int d, int64_t Tq,
                                   int64_t Tkv, const gdpa_bias* bias, int act, int causal,
                                   int window, float scale, void* out, float* lse,
+                                  void* workspace, size_t ws_bytes, void* stream);
+
+/* Backward pass with every product on MXFP8 operands ("GEM Training ..."
+ * low-precision paragraph: end-to-end MXFP8 block-scaled MMA in the forward
+ * and the backward pass).  Takes the bf16 tensors of gdpa_bwd and quantises
+ * them into the workspace first (gdpa_quantize_mxfp8's formats): Q, K and dO
+ * along channels (for S = Q K^T and dP = dO V^T) and along tokens (for
+ * dK = dS^T Q, dQ = dS K and dV = P^T dO), V along channels.  P and dS are
+ * made in the kernel from fp32 S and dP and rounded to E4M3 in blocks of 32
+ * keys x 32 queries (aligned to each sample's first key and first query)
+ * sharing one E8M0 scale, the smallest power of two X with amax / X <= 448.
+ * D = rowsum(dO * O) comes from the bf16 out and dout.  Products accumulate
+ * in fp32; dq is written as bf16(scale * sum), dk and dv as bf16.
+ * d must be 128 and act GDPA_ACT_SOFTMAX (else GDPA_ERR_UNSUPPORTED).  Every
+ * other argument, output and error is that of gdpa_bwd_window; the workspace
+ * is gdpa_bwd_mxfp8_workspace_size bytes (16-byte aligned). */
+size_t gdpa_bwd_mxfp8_workspace_size(int B, int H, int d, int64_t Tq, int64_t Tkv);
+gdpa_status gdpa_bwd_mxfp8(const void* q, const int32_t* q_offsets, const void* k, const void* v,
+                           const int32_t* kv_offsets, int B, int H, int d, int64_t Tq,
+                           int64_t Tkv, const gdpa_bias* bias, int act, int causal, float scale,
+                           const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                           void* dv, void* workspace, size_t ws_bytes, void* stream);
+/* gdpa_bwd_mxfp8 with a sliding window (semantics of gdpa_bwd_window). */
+gdpa_status gdpa_bwd_mxfp8_window(const void* q, const int32_t* q_offsets, const void* k,
+                                  const void* v, const int32_t* kv_offsets, int B, int H, int d,
+                                  int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act,
+                                  int causal, int window, float scale, const void* out,
+                                  const float* lse, const void* dout, void* dq, void* dk, void* dv,
                                   void* workspace, size_t ws_bytes, void* stream);
 
 /* Reads the device status word set by earlier calls on this device,

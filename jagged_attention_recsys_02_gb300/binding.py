@@ -31,7 +31,8 @@ EXPORTS = ("gdpa_fwd_workspace_size", "gdpa_fwd", "gdpa_bwd_workspace_size", "gd
            "gdpa_timing_enable", "gdpa_timing_collect", "gdpa_fwd_noalloc",
            "gdpa_mxfp8_scale_bytes", "gdpa_quantize_mxfp8", "gdpa_fwd_mxfp8",
            "gdpa_fwd_window", "gdpa_bwd_window", "gdpa_fwd_mxfp8_window",
-           "gdpa_block_workspace_size", "gdpa_block_fwd", "gdpa_block_bwd")
+           "gdpa_block_workspace_size", "gdpa_block_fwd", "gdpa_block_bwd",
+           "gdpa_bwd_mxfp8_workspace_size", "gdpa_bwd_mxfp8", "gdpa_bwd_mxfp8_window")
 MX_ALONG_CHANNELS, MX_ALONG_TOKENS = 0, 1
 
 
@@ -115,6 +116,14 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdpa_block_bwd.argtypes = [vp, vp, vp, vp, I, I, I, i64, ctypes.POINTER(gdpa_bias), I,
                                        I, F, F, vp, vp, vp, vp, vp, sz, vp]
         lib.gdpa_block_bwd.restype = I
+        lib.gdpa_bwd_mxfp8_workspace_size.argtypes = [I, I, I, i64, i64]
+        lib.gdpa_bwd_mxfp8_workspace_size.restype = sz
+        lib.gdpa_bwd_mxfp8.argtypes = list(lib.gdpa_bwd.argtypes)
+        lib.gdpa_bwd_mxfp8.restype = I
+        lib.gdpa_bwd_mxfp8_window.argtypes = [vp, vp, vp, vp, vp, I, I, I, i64, i64,
+                                              ctypes.POINTER(gdpa_bias), I, I, I, F, vp, vp, vp,
+                                              vp, vp, vp, vp, sz, vp]
+        lib.gdpa_bwd_mxfp8_window.restype = I
         _lib = lib
         return lib
 
@@ -207,6 +216,38 @@ def gdpa_bwd(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, act, causal=Fals
     else:
         rc = lib.gdpa_bwd(*head, *tail, *ws)
     _check(rc, "gdpa_bwd_window" if (window or dbias is not None) else "gdpa_bwd")
+    return dq, dk, dv
+
+
+def bwd_mxfp8_workspace_size(B, H, d, Tq, Tkv) -> int:
+    return int(load().gdpa_bwd_mxfp8_workspace_size(B, H, d, Tq, Tkv))
+
+
+def gdpa_bwd_mxfp8(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, causal=False, scale,
+                   bias=None, max_rel=0, window=0, dq=None, dk=None, dv=None, workspace=None,
+                   stream=None):
+    """MXFP8 backward through the C ABI (gdpa_bwd_mxfp8, or
+    gdpa_bwd_mxfp8_window when window > 0) on the bf16 tensors of gdpa_bwd,
+    softmax, d = 128.  Returns (dq, dk, dv)."""
+    lib = load()
+    Tq, H, d = q.shape
+    Tkv = k.shape[0]
+    B = q_offsets.numel() - 1
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(bwd_mxfp8_workspace_size(B, H, d, Tq, Tkv), device=q.device,
+                                dtype=torch.uint8)
+    head = (_ptr(q), _ptr(q_offsets), _ptr(k), _ptr(v), _ptr(kv_offsets), B, H, d, Tq, Tkv,
+            _bias(bias, max_rel), ACT_SOFTMAX, int(bool(causal)))
+    tail = (float(scale), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+            _ptr(workspace), workspace.numel(), _stream(stream))
+    if window:
+        rc = lib.gdpa_bwd_mxfp8_window(*head, int(window), *tail)
+    else:
+        rc = lib.gdpa_bwd_mxfp8(*head, *tail)
+    _check(rc, "gdpa_bwd_mxfp8_window" if window else "gdpa_bwd_mxfp8")
     return dq, dk, dv
 
 

@@ -609,6 +609,184 @@ gdpa_status gdpa_fwd_mxfp8_window(const void* q_codes, const void* q_scales,
   return GDPA_OK;
 }
 
+namespace {
+// Carves the MXFP8 backward's workspace; returns the bytes it needs.
+struct BwdMxLayout {
+  size_t items, dq_acc, delta, qd, qt, dod, dot, kd, kt, vd, qd_sc, dod_sc, kd_sc, vd_sc, qt_sc,
+      dot_sc, kt_sc, total;
+};
+BwdMxLayout bwd_mx_layout(int B, int H, int d, int64_t Tq, int64_t Tkv) {
+  BwdMxLayout l{};
+  size_t off = 256;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes, 256);
+    return at;
+  };
+  const size_t hd = static_cast<size_t>(H) * d;
+  l.items = take(static_cast<size_t>(max_bwd_items(B, H, Tkv)) * sizeof(int2));
+  l.dq_acc = take(static_cast<size_t>(Tq) * hd * sizeof(float));
+  l.delta = take(static_cast<size_t>(Tq) * H * sizeof(float));
+  l.qd = take(static_cast<size_t>(Tq) * hd);
+  l.qt = take(static_cast<size_t>(Tq) * hd);
+  l.dod = take(static_cast<size_t>(Tq) * hd);
+  l.dot = take(static_cast<size_t>(Tq) * hd);
+  l.kd = take(static_cast<size_t>(Tkv) * hd);
+  l.kt = take(static_cast<size_t>(Tkv) * hd);
+  l.vd = take(static_cast<size_t>(Tkv) * hd);
+  l.qd_sc = take(static_cast<size_t>(Tq) * H * (d / 32));
+  l.dod_sc = take(static_cast<size_t>(Tq) * H * (d / 32));
+  l.kd_sc = take(static_cast<size_t>(Tkv) * H * (d / 32));
+  l.vd_sc = take(static_cast<size_t>(Tkv) * H * (d / 32));
+  l.qt_sc = take((static_cast<size_t>(B) + Tq / 32 + 1) * hd);
+  l.dot_sc = take((static_cast<size_t>(B) + Tq / 32 + 1) * hd);
+  l.kt_sc = take((static_cast<size_t>(B) + Tkv / 32 + 1) * hd);
+  l.total = off;
+  return l;
+}
+}  // namespace
+
+size_t gdpa_bwd_mxfp8_workspace_size(int B, int H, int d, int64_t Tq, int64_t Tkv) {
+  if (B < 0 || H <= 0 || Tq < 0 || Tkv < 0 || (d != 64 && d != 128)) return 0;
+  return bwd_mx_layout(B, H, d, Tq, Tkv).total;
+}
+
+gdpa_status gdpa_bwd_mxfp8(const void* q, const int32_t* q_offsets, const void* k, const void* v,
+                           const int32_t* kv_offsets, int B, int H, int d, int64_t Tq,
+                           int64_t Tkv, const gdpa_bias* bias, int act, int causal, float scale,
+                           const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                           void* dv, void* workspace, size_t ws_bytes, void* stream) {
+  return gdpa_bwd_mxfp8_window(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act, causal,
+                               0, scale, out, lse, dout, dq, dk, dv, workspace, ws_bytes, stream);
+}
+
+gdpa_status gdpa_bwd_mxfp8_window(const void* q, const int32_t* q_offsets, const void* k,
+                                  const void* v, const int32_t* kv_offsets, int B, int H, int d,
+                                  int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act,
+                                  int causal, int window, float scale, const void* out,
+                                  const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                  void* workspace, size_t ws_bytes, void* stream) {
+  t_launches = 0;
+  gdpa_status st = check_common(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act,
+                                causal, window);
+  if (st != GDPA_OK) return st;
+  if (d != 128 || act != GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
+  if (Tq > 0 && (dout == nullptr || dq == nullptr || out == nullptr || lse == nullptr ||
+                 !aligned16(dout) || !aligned16(dq) || !aligned16(out)))
+    return GDPA_ERR_INVALID_ARG;
+  if (Tkv > 0 && (dk == nullptr || dv == nullptr || !aligned16(dk) || !aligned16(dv)))
+    return GDPA_ERR_INVALID_ARG;
+  const BwdMxLayout lay = bwd_mx_layout(B, H, d, Tq, Tkv);
+  if (workspace == nullptr || ws_bytes < lay.total || !aligned16(workspace)) return GDPA_ERR_WORKSPACE;
+  if (B == 0 || (Tq == 0 && Tkv == 0)) return GDPA_OK;
+
+  DeviceInfo* dev = nullptr;
+  if (device_info(&dev) != cudaSuccess) return GDPA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto at = [&](size_t off) { return static_cast<void*>(ws + off); };
+
+  // 1) operand codes and scales: Q, K, dO along channels and along tokens, V along channels
+  cudaError_t e = cudaSuccess;
+  if (Tq > 0) {
+    if ((e = launch_quant_rows(q, Tq * H, d, at(lay.qd), at(lay.qd_sc), s)) != cudaSuccess ||
+        (e = launch_quant_tokens(q, q_offsets, B, H, d, Tq, at(lay.qt), at(lay.qt_sc), s)) != cudaSuccess ||
+        (e = launch_quant_rows(dout, Tq * H, d, at(lay.dod), at(lay.dod_sc), s)) != cudaSuccess ||
+        (e = launch_quant_tokens(dout, q_offsets, B, H, d, Tq, at(lay.dot), at(lay.dot_sc), s)) != cudaSuccess)
+      return GDPA_ERR_CUDA;
+    t_launches += 4;
+  }
+  if (Tkv > 0) {
+    if ((e = launch_quant_rows(k, Tkv * H, d, at(lay.kd), at(lay.kd_sc), s)) != cudaSuccess ||
+        (e = launch_quant_tokens(k, kv_offsets, B, H, d, Tkv, at(lay.kt), at(lay.kt_sc), s)) != cudaSuccess ||
+        (e = launch_quant_rows(v, Tkv * H, d, at(lay.vd), at(lay.vd_sc), s)) != cudaSuccess)
+      return GDPA_ERR_CUDA;
+    t_launches += 3;
+  }
+
+  // 2) TMA maps over the codes (an empty side is never loaded; any valid tensor stands in)
+  const int64_t Tqm = Tq > 0 ? Tq : Tkv;
+  const int64_t Tkm = Tkv > 0 ? Tkv : Tq;
+  const size_t qsrc[4] = {lay.qd, lay.qt, lay.dod, lay.dot};
+  const size_t ksrc[3] = {lay.kd, lay.kt, lay.vd};
+  CUtensorMap maps[8];
+  for (int i = 0; i < 4; ++i)
+    if (!make_u8_map(&maps[i], at(Tq > 0 ? qsrc[i] : ksrc[0]), Tqm, H, d, kBwdMxQRows))
+      return GDPA_ERR_INVALID_ARG;
+  for (int i = 0; i < 3; ++i)
+    if (!make_u8_map(&maps[4 + i], at(Tkv > 0 ? ksrc[i] : qsrc[0]), Tkm, H, d, kBwdKvRows))
+      return GDPA_ERR_INVALID_ARG;
+  float* dq_acc = reinterpret_cast<float*>(ws + lay.dq_acc);
+  if (!make_dq_map(&maps[7], Tq > 0 ? static_cast<void*>(dq_acc) : ws, Tq > 0 ? Tq : 1, H, d, d,
+                   kBwdSmDqRows))
+    return GDPA_ERR_INVALID_ARG;
+
+  // 3) work list of 128-key blocks
+  int* n_items = reinterpret_cast<int*>(ws);
+  int* ticket = reinterpret_cast<int*>(ws + 4);
+  int2* items = reinterpret_cast<int2*>(ws + lay.items);
+  if (launch_build_worklist(kv_offsets, q_offsets, B, H, Tkv, Tq, causal, window, 1, items,
+                            n_items, ticket, dev->status, s) != cudaSuccess)
+    return GDPA_ERR_CUDA;
+  ++t_launches;
+
+  int max_rel = 1;
+  const float* table = bias_table(bias, &max_rel);
+  BwdParams p{};
+  p.qo = q_offsets;
+  p.ko = kv_offsets;
+  p.B = B;
+  p.H = H;
+  p.d = d;
+  p.Tq = Tq;
+  p.Tkv = Tkv;
+  p.bias_table = table;
+  p.max_rel = max_rel;
+  p.causal = causal;
+  p.window = window;
+  p.scale = scale;
+  p.out = static_cast<const __nv_bfloat16*>(out);
+  p.lse = lse;
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.dq_acc = dq_acc;
+  p.delta = reinterpret_cast<float*>(ws + lay.delta);
+  p.items = items;
+  p.n_items = n_items;
+  p.ticket = ticket;
+  p.status = dev->status;
+  // 4) zero the dQ accumulator, D = rowsum(dO * O) from the bf16 tensors
+  if (Tq > 0) {
+    if (launch_bwd_preprocess(p, true, s) != cudaSuccess) return GDPA_ERR_CUDA;
+    ++t_launches;
+  }
+  BwdMxOperands mx{};
+  mx.qd_sc = ws + lay.qd_sc;
+  mx.kd_sc = ws + lay.kd_sc;
+  mx.vd_sc = ws + lay.vd_sc;
+  mx.dod_sc = ws + lay.dod_sc;
+  mx.qt_sc = ws + lay.qt_sc;
+  mx.kt_sc = ws + lay.kt_sc;
+  mx.dot_sc = ws + lay.dot_sc;
+  const int64_t max_items = max_bwd_items(B, H, Tkv);
+  const int grid = static_cast<int>(max_items < dev->sms ? (max_items > 0 ? max_items : 1) : dev->sms);
+  cudaEvent_t ea = nullptr, eb = nullptr;
+  const bool timed = timing_slot(1, &ea, &eb);
+  if (timed && cudaEventRecord(ea, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (launch_bwd_mx(p, mx, maps, grid, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (timed && cudaEventRecord(eb, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  ++t_launches;
+  // 5) dQ = bf16(scale * accumulator)
+  if (Tq > 0) {
+    if (launch_dq_convert(dq_acc, dq, static_cast<long long>(Tq) * H * d, scale, s) != cudaSuccess)
+      return GDPA_ERR_CUDA;
+    ++t_launches;
+  }
+  (void)e;
+  return GDPA_OK;
+}
+
 gdpa_status gdpa_get_device_status(void* stream) {
   DeviceInfo* dev = nullptr;
   if (device_info(&dev) != cudaSuccess) return GDPA_ERR_CUDA;

@@ -816,15 +816,7 @@ cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const
                        cudaStream_t stream, int* launches, cudaEvent_t ev_begin,
                        cudaEvent_t ev_end) {
   // 1) zero dQ accumulator, D = rowsum(dO * O)
-  const long long rows = p.Tq * p.H;
-  const int pre_blocks = static_cast<int>(rows / 8 + 1 < 4096 ? rows / 8 + 1 : 4096);
-  if (p.d == 64)
-    bwd_preprocess_kernel<64><<<pre_blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
-                                                              p.Tq, p.H, act == GDPA_ACT_SOFTMAX);
-  else
-    bwd_preprocess_kernel<128><<<pre_blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
-                                                               p.Tq, p.H, act == GDPA_ACT_SOFTMAX);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_bwd_preprocess(p, act == GDPA_ACT_SOFTMAX, stream);
   if (e != cudaSuccess) return e;
   ++*launches;
   // 2) main kernel (optionally bracketed by timing events)
@@ -838,6 +830,18 @@ cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const
   if (ev_end != nullptr && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess) return e;
   ++*launches;
   return cudaSuccess;
+}
+
+cudaError_t launch_bwd_preprocess(const BwdParams& p, bool softmax, cudaStream_t stream) {
+  const long long rows = p.Tq * p.H;
+  const int pre_blocks = static_cast<int>(rows / 8 + 1 < 4096 ? rows / 8 + 1 : 4096);
+  if (p.d == 64)
+    bwd_preprocess_kernel<64><<<pre_blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
+                                                              p.Tq, p.H, softmax ? 1 : 0);
+  else
+    bwd_preprocess_kernel<128><<<pre_blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
+                                                               p.Tq, p.H, softmax ? 1 : 0);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale,

@@ -22,6 +22,7 @@ constexpr int kBwdKvRows = 128;
 constexpr int kBwdQRows = 64;
 constexpr int kBwdSmQRows = 128;  // query tile of the softmax backward
 constexpr int kBwdSmDqRows = 16;  // query rows per dQ reduce box of the softmax backward
+constexpr int kBwdMxQRows = 64;   // query tile of the MXFP8 backward
 
 constexpr int kCostBuckets = 2048;
 
@@ -196,6 +197,8 @@ cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const
                        cudaEvent_t ev_end);
 cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale,
                               cudaStream_t stream);
+// Zeroes p.dq_acc and, for softmax, writes p.delta = rowsum(dO * O).
+cudaError_t launch_bwd_preprocess(const BwdParams& p, bool softmax, cudaStream_t stream);
 
 cudaError_t launch_quant_rows(const void* x, long long rows, int d, void* codes, void* scales,
                               cudaStream_t s);
@@ -203,6 +206,19 @@ cudaError_t launch_quant_tokens(const void* x, const int32_t* offsets, int B, in
                                 long long T, void* codes, void* scales, cudaStream_t s);
 
 int fwd_mx_tile_rows();
+// MXFP8 softmax backward (d = 128): operand codes and scales of each product.
+struct BwdMxOperands {
+  const uint8_t* qd_sc;   // Q along channels: u32 word of 4 scales per (token, head)
+  const uint8_t* kd_sc;
+  const uint8_t* vd_sc;
+  const uint8_t* dod_sc;
+  const uint8_t* qt_sc;   // along tokens: [B + T/32 + 1][H][d] bytes
+  const uint8_t* kt_sc;
+  const uint8_t* dot_sc;
+};
+// maps: qd, qt, dod, dot (64-row boxes), kd, kt, vd (128-row boxes), dq (fp32, 16-row boxes)
+cudaError_t launch_bwd_mx(const BwdParams& p, const BwdMxOperands& mx, const CUtensorMap* maps,
+                          int grid, cudaStream_t s);
 cudaError_t launch_fwd_mx(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
                           const uint8_t* v_sc, long long v_sc_rows, int grid, cudaStream_t s);

@@ -84,13 +84,29 @@ quant_rows_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ cod
 // One CTA per scale row s (32-token block r of sample b, s = b + floor(o_b/32) + r;
 // g(b) = b + floor(o_b/32) rises by at least 1 per sample, so the sample owning s is
 // the last b with g(b) <= s).  Rows in the gaps between samples own no tokens and are
-// left untouched.  Each thread takes 4 consecutive (head, channel) columns: 32 8-byte
+// left untouched; a few CTAs after the last row zero the codes of tokens outside
+// every sample.  Each thread takes 4 consecutive (head, channel) columns: 32 8-byte
 // loads in flight, a warp covers 256 contiguous bytes of each token row.
 __global__ void __launch_bounds__(128)
 quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ offsets,
-                    int B, int hd, long long T, uint8_t* __restrict__ codes,
+                    int B, int hd, long long T, long long n_rows, uint8_t* __restrict__ codes,
                     uint8_t* __restrict__ scales) {
   const long long s = blockIdx.x;
+  if (s >= n_rows) {
+    // Tail blocks: tokens before the first sample or after the last one have no
+    // scale row; their codes are zeroed so that a tile running past a sample's
+    // end never reads stale bytes (an E4M3 NaN code times a zero weight is NaN).
+    const long long a = min(static_cast<long long>(max(offsets[0], 0)), T);
+    const long long b = max(a, min(static_cast<long long>(offsets[B]), T));
+    const long long nthreads = (gridDim.x - n_rows) * static_cast<long long>(blockDim.x);
+    const long long tid = (s - n_rows) * blockDim.x + threadIdx.x;
+    uint4* c4 = reinterpret_cast<uint4*>(codes);
+    const long long per_tok = hd / 16;
+    for (long long i = tid; i < a * per_tok; i += nthreads) c4[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (long long i = b * per_tok + tid; i < T * per_tok; i += nthreads)
+      c4[i] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
   int lo = 0, hi = B - 1;  // largest b with g(b) <= s; g(0) = 0 <= s
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -163,9 +179,10 @@ cudaError_t launch_quant_tokens(const void* x, const int32_t* offsets, int B, in
   // Scale rows as counted by the buffer size: B + T/32 + 1 covers g(B-1) + ceil(L/32).
   const long long rows = static_cast<long long>(B) + T / 32 + 1;
   if (rows > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  quant_tokens_kernel<<<static_cast<unsigned>(rows), 128, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(x), offsets, B, H * d, T, static_cast<uint8_t*>(codes),
-      static_cast<uint8_t*>(scales));
+  constexpr int kTailBlocks = 16;  // zero the codes of tokens outside every sample
+  quant_tokens_kernel<<<static_cast<unsigned>(rows + kTailBlocks), 128, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(x), offsets, B, H * d, T, rows,
+      static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales));
   return cudaGetLastError();
 }
 

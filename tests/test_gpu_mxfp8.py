@@ -225,3 +225,153 @@ def test_mxfp8_fwd_full_heavy_tail():
             err = np.abs(got_rows[0] - o) / (MXFP8_TOL[0] + MXFP8_TOL[1] * np.abs(o))
             print(f"heavy_tail sample {b}: worst err/bound against the unquantised inputs "
                   f"{float(err.max()):.3f}")
+
+
+def test_quant_tokens_zeroes_tokens_outside_samples():
+    """Codes of tokens before the first or after the last sample are 0, whatever
+    the buffer held (a tile that runs past a sample's end reads them)."""
+    H, d, T = 2, 128, 70
+    x = _inputs(T, H, d, 4)
+    o = offsets([5, 40])                       # samples cover tokens 0..44
+    off = torch.from_numpy(o).to(DEV)
+    codes = torch.full((T, H, d), 0x7F, device=DEV, dtype=torch.uint8)  # E4M3 NaN codes
+    codes, scales = binding.quantize_mxfp8(x, off, mode=binding.MX_ALONG_TOKENS, codes=codes)
+    got = codes.cpu().numpy()
+    assert np.all(got[45:] == 0)
+    rc, _ = oracle.quant_cols(to_np(x[:45]), o)
+    np.testing.assert_array_equal(got[:45], rc)
+
+
+# ------------------------------------------------------------------ MXFP8 backward
+# The reference is the oracle's MXFP8 backward: the operands quantised by the
+# oracle's own quantisers, P and dS rounded in 32 x 32 blocks the same way.
+# What is left differs only by fp32 accumulation order, ex2.approx in P, the
+# bf16 rounding of the outputs (2^-9) and, rarely, an element sitting within
+# fp32 rounding of an E4M3 rounding boundary: (2e-2, 2e-2) covers them.
+MXBWD_TOL = (2e-2, 2e-2)
+
+
+def _mx_bwd_run(q, qo, k, v, ko, out, lse, dout, causal, scale, bias, max_rel, window=0):
+    Tq, H, d = q.shape
+    Tkv = k.shape[0]
+    bq, dq = guarded(Tq, H, d, q.device)
+    bk, dk = guarded(Tkv, H, d, q.device)
+    bv, dv = guarded(Tkv, H, d, q.device)
+    ws = torch.full((binding.bwd_mxfp8_workspace_size(qo.numel() - 1, H, d, Tq, Tkv),), 0xFF,
+                    device=q.device, dtype=torch.uint8)  # stale bytes must not matter
+    binding.gdpa_bwd_mxfp8(q, qo, k, v, ko, out, lse, dout, causal=causal, scale=scale, bias=bias,
+                           max_rel=max_rel, window=window, dq=dq, dk=dk, dv=dv, workspace=ws)
+    assert binding.device_status() == 0
+    for b in (bq, bk, bv):
+        check_guards(b)
+    return dq, dk, dv
+
+
+def _mx_bwd_case(lq, lkv, H, causal=False, max_rel=0, seed=0):
+    """Random bf16 inputs; out and lse from the oracle's forward (the backward's
+    inputs, as a training step passes them); every gradient element checked."""
+    d = 128
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    Tq, Tkv = sum(lq), sum(lkv)
+    q = rand_bf16((Tq, H, d), g, DEV)
+    k = rand_bf16((Tkv, H, d), g, DEV)
+    v = rand_bf16((Tkv, H, d), g, DEV)
+    dout = rand_bf16((Tq, H, d), g, DEV)
+    qo_np, ko_np = offsets(lq), offsets(lkv)
+    qo, ko = torch.from_numpy(qo_np).to(DEV), torch.from_numpy(ko_np).to(DEV)
+    bias = torch.randn(H, 2 * max_rel - 1, generator=g, device=DEV) * 0.5 if max_rel else None
+    bias_np = None if bias is None else bias.cpu().double().numpy()
+    scale = 1.0 / np.sqrt(d)
+    nq, nk = sum(lq), sum(lkv)
+    o_ref, l_ref = oracle.fwd(to_np(q[:nq]), qo_np, to_np(k[:nk]), to_np(v[:nk]), ko_np,
+                              act=oracle.ACT_SOFTMAX, causal=causal, scale=scale, bias=bias_np,
+                              max_rel=max_rel)
+    out = torch.zeros((Tq, H, d), device=DEV, dtype=torch.bfloat16)
+    out[:nq] = torch.from_numpy(o_ref).to(DEV).to(torch.bfloat16)
+    lse = torch.zeros((H, Tq), device=DEV, dtype=torch.float32)
+    lse[:, :nq] = torch.from_numpy(np.where(np.isinf(l_ref), 0.0, l_ref)).to(DEV).float()
+    dq, dk, dv = _mx_bwd_run(q, qo, k, v, ko, out, lse, dout, causal, scale, bias, max_rel)
+    ref = oracle.bwd_mxfp8(to_np(q[:nq]), qo_np, to_np(k[:nk]), to_np(v[:nk]), ko_np,
+                           to_np(out[:nq]), to_np(dout[:nq]), lse[:, :nq].cpu().double().numpy(),
+                           causal=causal, scale=scale, bias=bias_np, max_rel=max_rel)
+    for name, got, r in (("dq", dq[:nq], ref[0]), ("dk", dk[:nk], ref[1]), ("dv", dv[:nk], ref[2])):
+        assert_close(to_np(got), r, MXBWD_TOL, f"mxfp8 bwd {name}")
+    exact = oracle.bwd(to_np(q[:nq]), qo_np, to_np(k[:nk]), to_np(v[:nk]), ko_np, to_np(dout[:nq]),
+                       act=oracle.ACT_SOFTMAX, causal=causal, scale=scale, bias=bias_np,
+                       max_rel=max_rel)
+    for name, got, r in (("dq", dq[:nq], exact[0]), ("dk", dk[:nk], exact[1]), ("dv", dv[:nk], exact[2])):
+        e = np.abs(to_np(got) - r)
+        print(f"mxfp8 bwd {name}: relative RMS error against the unquantised backward "
+              f"{np.sqrt((e ** 2).mean() / max((r ** 2).mean(), 1e-300)):.4f}")
+    return dq, dk, dv
+
+
+def test_mxfp8_bwd_ragged():
+    # lengths crossing the 32-token scale blocks, the 64-query tiles and the 128-key blocks
+    _mx_bwd_case([1, 31, 32, 33, 63, 64, 65, 200, 0, 300, 129, 7],
+                 [7, 32, 31, 96, 128, 1, 129, 3, 5, 191, 300, 64], 2)
+
+
+def test_mxfp8_bwd_causal_relpos():
+    L = [1, 64, 65, 128, 129, 300, 0, 511, 257]
+    _mx_bwd_case(L, L, 2, causal=True, max_rel=300)
+
+
+def test_mxfp8_bwd_empty_sides():
+    _mx_bwd_case([3, 0, 130, 5], [0, 9, 0, 140], 2)
+
+
+def test_mxfp8_bwd_rejects_offsets_short_of_the_tensor():
+    """Offsets must end at the tensor's last row: a mismatch is reported through
+    the device status word (and the kernels do no work)."""
+    H, d = 1, 128
+    g = torch.Generator(device=DEV).manual_seed(3)
+    q = rand_bf16((150, H, d), g, DEV)
+    qo = torch.from_numpy(offsets([70, 30])).to(DEV)
+    lse = torch.zeros((H, 150), device=DEV)
+    binding.gdpa_bwd_mxfp8(q, qo, q, q, qo, q, lse, q, causal=True, scale=0.1)
+    assert binding.device_status() == 6  # GDPA_ERR_BAD_OFFSETS
+
+
+def test_mxfp8_bwd_rejects_gdpa_and_d64():
+    lib = binding.load()
+    p = torch.zeros(64, device=DEV, dtype=torch.uint8).data_ptr()
+    o = torch.zeros(2, device=DEV, dtype=torch.int32).data_ptr()
+    common = (p, o, p, p, o, 1, 1)
+    tail = (p, p, p, p, p, p, p, 1 << 20, None)
+    assert lib.gdpa_bwd_mxfp8(*common, 128, 1, 1, None, 1, 0, 0.1, *tail) == 2
+    assert lib.gdpa_bwd_mxfp8(*common, 64, 1, 1, None, 0, 0, 0.1, *tail) == 2
+
+
+def test_mxfp8_bwd_full_jfa_causal_relpos():
+    """The full causal rel-pos workload (B=32, L~U[1,4096], H=4) in the launch
+    configuration the benchmark times, every gradient element of three samples
+    (the shortest, a middle one, the longest) against the oracle.  The other
+    samples get out = 0 and lse = 30 (finite, P tiny): samples are independent."""
+    w = make_workload("jfa_causal_relpos")
+    t = make_tensors(w, device=DEV, with_dout=True)
+    qo, ko = w.offsets()
+    order = np.argsort(w.lq)
+    samples = [int(order[0]), int(order[len(order) // 2]), int(order[-1])]
+    out = torch.zeros_like(t["q"])
+    lse = torch.full((w.H, w.Tq), 30.0, device=DEV, dtype=torch.float32)
+    bias_np = t["bias"].cpu().double().numpy()
+    for b in samples:
+        s0, s1 = int(qo[b]), int(qo[b + 1])
+        o_ref, l_ref = oracle.fwd(to_np(t["q"][s0:s1]), np.array([0, s1 - s0]),
+                                  to_np(t["k"][s0:s1]), to_np(t["v"][s0:s1]),
+                                  np.array([0, s1 - s0]), act=oracle.ACT_SOFTMAX, causal=True,
+                                  scale=w.scale, bias=bias_np, max_rel=w.max_rel)
+        out[s0:s1] = torch.from_numpy(o_ref).to(DEV).to(torch.bfloat16)
+        lse[:, s0:s1] = torch.from_numpy(l_ref).to(DEV).float()
+    dq, dk, dv = _mx_bwd_run(t["q"], t["qo"], t["k"], t["v"], t["ko"], out, lse, t["dout"], True,
+                             w.scale, t["bias"], w.max_rel)
+    for b in samples:
+        s0, s1 = int(qo[b]), int(qo[b + 1])
+        one = np.array([0, s1 - s0])
+        ref = oracle.bwd_mxfp8(to_np(t["q"][s0:s1]), one, to_np(t["k"][s0:s1]),
+                               to_np(t["v"][s0:s1]), one, to_np(out[s0:s1]),
+                               to_np(t["dout"][s0:s1]), lse[:, s0:s1].cpu().double().numpy(),
+                               causal=True, scale=w.scale, bias=bias_np, max_rel=w.max_rel)
+        for name, got, r in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
+            assert_close(to_np(got[s0:s1]), r, MXBWD_TOL, f"jfa mxfp8 bwd {name} sample {b}")

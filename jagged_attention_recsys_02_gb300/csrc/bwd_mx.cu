@@ -171,6 +171,36 @@ __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
   asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
   return r;
 }
+// Largest |x| of 32 values (pairwise tree).
+__device__ __forceinline__ float amax32(const float (&x)[32]) {
+  float m[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m[i] = fmaxf(fabsf(x[2 * i]), fabsf(x[2 * i + 1]));
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+  return m[0];
+}
+// E4M3 codes of x * inv, four per word (packed fp32x2 scaling).
+__device__ __forceinline__ void quant32(const float (&x)[32], float inv, uint32_t (&pk)[8]) {
+  const float2 s2 = make_float2(inv, inv), z2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float2 a = fma_f32x2(make_float2(x[4 * q], x[4 * q + 1]), s2, z2);
+    const float2 b = fma_f32x2(make_float2(x[4 * q + 2], x[4 * q + 3]), s2, z2);
+    pk[q] = e4m3x4(a.x, a.y, b.x, b.y);
+  }
+}
+// 4 x 4 byte transpose across the lanes of each aligned group of four: lane r
+// holds bytes (query c = 0..3) of key r in `x`; returns bytes (key 0..3) of
+// query r.
+__device__ __forceinline__ uint32_t transpose4x4_bytes(uint32_t x, int lane) {
+  uint32_t p = __shfl_xor_sync(0xffffffffu, x, 1);
+  uint32_t t = __byte_perm(x, p, (lane & 1) ? 0x3715u : 0x6240u);
+  p = __shfl_xor_sync(0xffffffffu, t, 2);
+  return __byte_perm(t, p, (lane & 2) ? 0x3276u : 0x5410u);
+}
 
 struct MxItem {
   int b, head, kb;
@@ -704,16 +734,11 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
           }
         }
         {
-          float amax = 0.0f;
-#pragma unroll
-          for (int q = 0; q < 32; ++q) amax = fmaxf(amax, pv[q]);
           // one scale per 32 keys (this warp's lanes) x 32 queries (this group)
-          const int code = e8m0_nosat(__uint_as_float(warp_max_u32(__float_as_uint(amax))));
+          const int code = e8m0_nosat(__uint_as_float(warp_max_u32(__float_as_uint(amax32(pv)))));
           const float inv = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
           uint32_t pk[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            pk[q] = e4m3x4(pv[4 * q] * inv, pv[4 * q + 1] * inv, pv[4 * q + 2] * inv, pv[4 * q + 3] * inv);
+          quant32(pv, inv, pk);
           tmem_st8(tmem + lane_off + kColS + c0, pk);
           // word of key row 32 wq + lane, byte grp (the k-step of these queries)
           sf_p[lane * 16 + wq * 4 + grp] = static_cast<uint8_t>(code);
@@ -729,7 +754,7 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
         {
           uint32_t dr[32];
           tmem_ld32(tmem + lane_off + kColDP + c0, dr);
-          float amax = 0.0f;
+          const float2 z2 = make_float2(0.0f, 0.0f);
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             const float4 d4 = st4[((kQRows + c0) >> 2) + q4];  // -D
@@ -737,30 +762,37 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
                                          make_float2(d4.x, d4.y));
             const float2 v23 = add_f32x2(make_float2(__uint_as_float(dr[4 * q4 + 2]), __uint_as_float(dr[4 * q4 + 3])),
                                          make_float2(d4.z, d4.w));
-            pv[4 * q4] *= v01.x;  // masked P is exactly 0, so masked dS is too
-            pv[4 * q4 + 1] *= v01.y;
-            pv[4 * q4 + 2] *= v23.x;
-            pv[4 * q4 + 3] *= v23.y;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(pv[4 * q4 + e]));
+            // masked P is exactly 0, so masked dS is too
+            const float2 a = fma_f32x2(make_float2(pv[4 * q4], pv[4 * q4 + 1]), v01, z2);
+            const float2 b = fma_f32x2(make_float2(pv[4 * q4 + 2], pv[4 * q4 + 3]), v23, z2);
+            pv[4 * q4] = a.x;
+            pv[4 * q4 + 1] = a.y;
+            pv[4 * q4 + 2] = b.x;
+            pv[4 * q4 + 3] = b.y;
           }
-          const int code = e8m0_nosat(__uint_as_float(warp_max_u32(__float_as_uint(amax))));
+          const int code = e8m0_nosat(__uint_as_float(warp_max_u32(__float_as_uint(amax32(pv)))));
           const float inv = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
           uint32_t pk[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            pk[q] = e4m3x4(pv[4 * q] * inv, pv[4 * q + 1] * inv, pv[4 * q + 2] * inv, pv[4 * q + 3] * inv);
+          quant32(pv, inv, pk);
           // dS^T row j (A of dK): queries c0..c0+31 are 16-byte chunks 2 grp,
           // 2 grp + 1, stored at (chunk ^ (j % 8))
           uint8_t* dsrow = gbase + C::kDsT + j * 128;
           *reinterpret_cast<uint4*>(dsrow + (((2 * grp) ^ (j & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           *reinterpret_cast<uint4*>(dsrow + (((2 * grp + 1) ^ (j & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          // dS (B of dQ^T): byte j of query row i, chunk (j / 16) ^ (i % 8)
-          uint8_t* dsq = gbase + C::kDsQ + (j & 15);
+          // dS (B of dQ^T): query row i holds key j at byte j of the row, in
+          // 16-byte chunk (j / 16) ^ (i % 8).  Each group of four lanes (keys
+          // j4..j4+3) transposes its bytes so that lane r writes one word:
+          // keys j4..j4+3 of query c0 + 4q + r.
+          {
+            const int j4 = j & ~3;
+            const int r4 = lane & 3;
+            uint8_t* dsq = gbase + C::kDsQ + (j4 & 15);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int i = c0 + q;
-            dsq[i * 128 + (((j >> 4) ^ (i & 7)) << 4)] = static_cast<uint8_t>(pk[q >> 2] >> (8 * (q & 3)));
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t word = transpose4x4_bytes(pk[q], lane);
+              const int i = c0 + 4 * q + r4;
+              *reinterpret_cast<uint32_t*>(dsq + i * 128 + (((j4 >> 4) ^ (i & 7)) << 4)) = word;
+            }
           }
           // row scales of dS^T (rows = keys, k-step = query block grp) and
           // column scales (rows = queries of block grp, k-step = key block wq)
@@ -792,20 +824,24 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
       bool abort_now = false;
       for (int t = 0; t < in.nq; ++t) {
         w = mbar_wait(bar(C::kDqFull), dqc & 1u, abort_flag);
+        w = __all_sync(0xffffffffu, w);
+        // Read dQ^T out and free the dP columns first (the next dP product
+        // waits for them); a warp whose wait failed reads nothing.
+        uint32_t v[2][32];
+        if (w) {
+          tc_fence_after();
+          tmem_ld32(tmem + lane_off + kColDP, v[0]);
+          tmem_ld32(tmem + lane_off + kColDP + 32, v[1]);
+          tc_fence_before();
+          warp_arrive(bar(C::kDqEmpty), lane);  // the dP columns are free again
+        }
         // The group syncs on named barriers below, so its four warps must agree
         // on whether the wait succeeded before any of them can leave.
-        w = __all_sync(0xffffffffu, w);
         if (lane == 0) group_ok[wq] = w ? 1 : 0;
         named_bar_sync(1, 128);
         const bool all_ok = group_ok[0] && group_ok[1] && group_ok[2] && group_ok[3];
         if (!all_ok) { if (lane == 0) fail(); abort_now = true; break; }
         ++dqc;
-        tc_fence_after();
-        uint32_t v[2][32];
-        tmem_ld32(tmem + lane_off + kColDP, v[0]);
-        tmem_ld32(tmem + lane_off + kColDP + 32, v[1]);
-        tc_fence_before();
-        warp_arrive(bar(C::kDqEmpty), lane);  // the dP columns are free again
         // Stage 16-query chunks as [query][channel] and add each into the fp32
         // dQ rows with one bulk tensor reduce.  Columns of queries outside the
         // sample carry exact zeros (their dS is 0), so a box that runs into the

@@ -437,6 +437,7 @@ void oracle_quant_cols(const double* x, const int32_t* offs, int B, int H, int d
  *   dk_j  = scale sum_i DS_ij qt_i                qt: along tokens
  *   dq_i  = scale sum_j DS_ij kt_j                kt: along tokens
  *
+ * Masked pairs (causal, sliding window W > 0: |i - j| >= W) have p = ds = 0.
  * P and DS are p and ds rounded (round_ps = 1) or p and ds (round_ps = 0).
  * The blocks start at the sample's first key and first query.  A block's
  * scale is the smallest power of two X with amax / X <= 448 (no element
@@ -478,11 +479,11 @@ void oracle_round_blocks_2d(double* m, long R, long C) {
 int oracle_bwd_mx(const double* qd, const double* qt, const double* kd, const double* kt,
                   const double* vd, const double* dod, const double* dot_t, const int32_t* qo,
                   const int32_t* ko, int B, int H, int d, const double* bias, int max_rel,
-                  int causal, double scale, const double* lse, const double* delta,
+                  int causal, int window, double scale, const double* lse, const double* delta,
                   int round_ps, double* dq, double* dk, double* dv) {
-  if (B < 0 || H <= 0 || d <= 0) return -1;
+  if (B < 0 || H <= 0 || d <= 0 || window < 0) return -1;
   if (!check_offsets(qo, B) || !check_offsets(ko, B)) return -1;
-  if (causal)
+  if (causal || window > 0)
     for (int b = 0; b < B; ++b)
       if (qo[b + 1] - qo[b] != ko[b + 1] - ko[b]) return -1;
   const long Tq = qo[B];
@@ -510,6 +511,7 @@ int oracle_bwd_mx(const double* qd, const double* qt, const double* kd, const do
       const double dl = delta[(long)h * Tq + q0 + i];
       for (long j = 0; j < Lkv; ++j) {
         if (causal && j > i) continue;
+        if (window > 0 && (j <= i - window || j >= i + window)) continue;
         const double s = scale * dot(qi, kd + ((k0 + j) * H + h) * (long)d, d) +
                          bias_at(bias, max_rel, h, i, j);
         const double p = exp(s - l);

@@ -65,7 +65,7 @@ def _load():
         lib.oracle_e8m0_nosat.restype = ctypes.c_uint8
         lib.oracle_round_blocks_2d.argtypes = [dp, ctypes.c_long, ctypes.c_long]
         lib.oracle_round_blocks_2d.restype = None
-        lib.oracle_bwd_mx.argtypes = [dp, dp, dp, dp, dp, dp, dp, ip, ip, I, I, I, dp, I, I, D,
+        lib.oracle_bwd_mx.argtypes = [dp, dp, dp, dp, dp, dp, dp, ip, ip, I, I, I, dp, I, I, I, D,
                                       dp, dp, I, dp, dp, dp]
         lib.oracle_bwd_mx.restype = I
         _lib = lib
@@ -243,7 +243,7 @@ def dequant_cols(x, offsets):
 
 def bwd_mx_operands(qd, qt, kd, kt, vd, dod, dot, q_offsets, kv_offsets, lse, delta, *,
                     causal: bool = False, scale: float, bias=None, max_rel: int = 0,
-                    round_ps: bool = True):
+                    window: int = 0, round_ps: bool = True):
     """Softmax backward with each product on its own operand version (the
     definition at the MXFP8 backward section of gdpa_oracle.c): qd, kd, vd, dod
     feed the channel contractions (S, dP), qt, kt, dot the token contractions
@@ -261,7 +261,8 @@ def bwd_mx_operands(qd, qt, kd, kt, vd, dod, dot, q_offsets, kv_offsets, lse, de
     keep, bp = _bias_arg(bias, H, max_rel)
     rc = _load().oracle_bwd_mx(*[_p(a, ctypes.c_double) for a in arrs], _p(qo, ctypes.c_int32),
                                _p(ko, ctypes.c_int32), B, H, d, bp, int(max_rel),
-                               int(bool(causal)), float(scale), _p(lse_a, ctypes.c_double),
+                               int(bool(causal)), int(window), float(scale),
+                               _p(lse_a, ctypes.c_double),
                                _p(delta_a, ctypes.c_double), int(bool(round_ps)),
                                _p(dq, ctypes.c_double), _p(dk, ctypes.c_double),
                                _p(dv, ctypes.c_double))
@@ -272,7 +273,7 @@ def bwd_mx_operands(qd, qt, kd, kt, vd, dod, dot, q_offsets, kv_offsets, lse, de
 
 
 def bwd_mxfp8(q, q_offsets, k, v, kv_offsets, out, dout, lse, *, causal: bool = False,
-              scale: float, bias=None, max_rel: int = 0):
+              scale: float, bias=None, max_rel: int = 0, window: int = 0):
     """The MXFP8 softmax backward on bf16 inputs: Q, K, dO quantised along
     channels and along tokens, V along channels (quant_rows / quant_cols,
     decoded), delta = rowsum(dO * O) of the given values, P and dS rounded in
@@ -283,7 +284,7 @@ def bwd_mxfp8(q, q_offsets, k, v, kv_offsets, out, dout, lse, *, causal: bool = 
     return bwd_mx_operands(dequant_rows(q), dequant_cols(q, qo), dequant_rows(k),
                            dequant_cols(k, ko), dequant_rows(v), dequant_rows(dout),
                            dequant_cols(dout, qo), qo, ko, lse, delta, causal=causal,
-                           scale=scale, bias=bias, max_rel=max_rel, round_ps=True)
+                           scale=scale, bias=bias, max_rel=max_rel, window=window, round_ps=True)
 
 
 # ------------------------------------------------------------------ rotary embedding

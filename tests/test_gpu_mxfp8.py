@@ -267,7 +267,7 @@ def _mx_bwd_run(q, qo, k, v, ko, out, lse, dout, causal, scale, bias, max_rel, w
     return dq, dk, dv
 
 
-def _mx_bwd_case(lq, lkv, H, causal=False, max_rel=0, seed=0):
+def _mx_bwd_case(lq, lkv, H, causal=False, max_rel=0, seed=0, window=0):
     """Random bf16 inputs; out and lse from the oracle's forward (the backward's
     inputs, as a training step passes them); every gradient element checked."""
     d = 128
@@ -285,20 +285,22 @@ def _mx_bwd_case(lq, lkv, H, causal=False, max_rel=0, seed=0):
     nq, nk = sum(lq), sum(lkv)
     o_ref, l_ref = oracle.fwd(to_np(q[:nq]), qo_np, to_np(k[:nk]), to_np(v[:nk]), ko_np,
                               act=oracle.ACT_SOFTMAX, causal=causal, scale=scale, bias=bias_np,
-                              max_rel=max_rel)
+                              max_rel=max_rel, window=window)
     out = torch.zeros((Tq, H, d), device=DEV, dtype=torch.bfloat16)
     out[:nq] = torch.from_numpy(o_ref).to(DEV).to(torch.bfloat16)
     lse = torch.zeros((H, Tq), device=DEV, dtype=torch.float32)
     lse[:, :nq] = torch.from_numpy(np.where(np.isinf(l_ref), 0.0, l_ref)).to(DEV).float()
-    dq, dk, dv = _mx_bwd_run(q, qo, k, v, ko, out, lse, dout, causal, scale, bias, max_rel)
+    dq, dk, dv = _mx_bwd_run(q, qo, k, v, ko, out, lse, dout, causal, scale, bias, max_rel,
+                             window=window)
     ref = oracle.bwd_mxfp8(to_np(q[:nq]), qo_np, to_np(k[:nk]), to_np(v[:nk]), ko_np,
                            to_np(out[:nq]), to_np(dout[:nq]), lse[:, :nq].cpu().double().numpy(),
-                           causal=causal, scale=scale, bias=bias_np, max_rel=max_rel)
+                           causal=causal, scale=scale, bias=bias_np, max_rel=max_rel,
+                           window=window)
     for name, got, r in (("dq", dq[:nq], ref[0]), ("dk", dk[:nk], ref[1]), ("dv", dv[:nk], ref[2])):
         assert_close(to_np(got), r, MXBWD_TOL, f"mxfp8 bwd {name}")
     exact = oracle.bwd(to_np(q[:nq]), qo_np, to_np(k[:nk]), to_np(v[:nk]), ko_np, to_np(dout[:nq]),
                        act=oracle.ACT_SOFTMAX, causal=causal, scale=scale, bias=bias_np,
-                       max_rel=max_rel)
+                       max_rel=max_rel, window=window)
     for name, got, r in (("dq", dq[:nq], exact[0]), ("dk", dk[:nk], exact[1]), ("dv", dv[:nk], exact[2])):
         e = np.abs(to_np(got) - r)
         print(f"mxfp8 bwd {name}: relative RMS error against the unquantised backward "
@@ -315,6 +317,14 @@ def test_mxfp8_bwd_ragged():
 def test_mxfp8_bwd_causal_relpos():
     L = [1, 64, 65, 128, 129, 300, 0, 511, 257]
     _mx_bwd_case(L, L, 2, causal=True, max_rel=300)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_mxfp8_bwd_sliding_window(causal):
+    # windows shorter and longer than a 64-query tile / 128-key block, band edges inside tiles
+    L = [1, 64, 65, 130, 300, 0, 511]
+    for window in (7, 100, 200):
+        _mx_bwd_case(L, L, 2, causal=causal, max_rel=64, window=window, seed=window)
 
 
 def test_mxfp8_bwd_empty_sides():

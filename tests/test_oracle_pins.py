@@ -883,6 +883,29 @@ def test_bwd_mx_operands_reduce_to_the_backward(oracle_mod, causal, with_bias):
         np.testing.assert_allclose(g, r, rtol=1e-10, atol=1e-12)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("window", [1, 5, 40])
+def test_bwd_mx_operands_window_reduces_to_the_windowed_backward(oracle_mod, window, causal):
+    """The same reduction with a sliding window: the mask matches the windowed
+    backward's (pinned against torch's banded SDPA and finite differences)."""
+    lq = [5, 37, 70, 1]
+    H, d = 2, 8
+    qo = _offsets(lq)
+    q = _bf16_randn((sum(lq), H, d), 41)
+    k = _bf16_randn((sum(lq), H, d), 42)
+    v = _bf16_randn((sum(lq), H, d), 43)
+    do = _bf16_randn((sum(lq), H, d), 44)
+    bias = np.random.default_rng(2).normal(0, 0.5, (H, 39))
+    scale = 1.0 / math.sqrt(d)
+    kw = dict(causal=causal, scale=scale, bias=bias, max_rel=20, window=window)
+    out, lse = oracle_mod.fwd(q, qo, k, v, qo, act=ACT_SOFTMAX, **kw)
+    delta = np.einsum("thc,thc->ht", do, out)
+    got = oracle_mod.bwd_mx_operands(q, q, k, k, v, do, do, qo, qo, lse, delta, round_ps=False, **kw)
+    ref = oracle_mod.bwd(q, qo, k, v, qo, do, act=ACT_SOFTMAX, **kw)
+    for g, r in zip(got, ref):
+        np.testing.assert_allclose(g, r, rtol=1e-10, atol=1e-12)
+
+
 def test_bwd_mx_operands_wiring(oracle_mod):
     """Each token-contraction operand feeds one gradient, linearly; the channel
     operands of dP reach dQ and dK but not dV; and dV with distinct versions is

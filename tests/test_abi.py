@@ -154,3 +154,48 @@ def test_window_entry_points_reject_on_host(lib):
     mx = lib.gdpa_fwd_mxfp8_window(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 10,
                                    10, None, 0, 1, -3, 0.125, FAKE, FAKE, FAKE, 1 << 20, None)
     assert mx == INVALID
+
+
+def _bwd_mx(lib, window=None, **kw):
+    a = dict(q=FAKE, qo=FAKE, k=FAKE, v=FAKE, ko=FAKE, B=2, H=2, d=128, Tq=10, Tkv=10, bias=None,
+             act=0, causal=0, scale=0.125, out=FAKE, lse=FAKE, do=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+             ws=FAKE, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    head = (a["q"], a["qo"], a["k"], a["v"], a["ko"], a["B"], a["H"], a["d"], a["Tq"], a["Tkv"],
+            a["bias"], a["act"], a["causal"])
+    tail = (a["scale"], a["out"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"], a["ws"],
+            a["ws_bytes"], a["stream"])
+    if window is None:
+        return lib.gdpa_bwd_mxfp8(*head, *tail)
+    return lib.gdpa_bwd_mxfp8_window(*head, window, *tail)
+
+
+def test_mxfp8_backward_rejects_on_host(lib):
+    """gdpa_bwd_mxfp8(_window): the checks of gdpa_bwd, then softmax and d = 128
+    only, then the workspace; nothing reaches the device."""
+    for w in (None, 0, 3):
+        assert _bwd_mx(lib, window=w, act=1) == UNSUPPORTED
+        assert _bwd_mx(lib, window=w, d=64) == UNSUPPORTED
+        assert _bwd_mx(lib, window=w, d=96) == UNSUPPORTED
+        assert _bwd_mx(lib, window=w, H=0) == INVALID
+        assert _bwd_mx(lib, window=w, causal=2) == INVALID
+        assert _bwd_mx(lib, window=w, q=FAKE + 8) == INVALID
+        assert _bwd_mx(lib, window=w, do=None) == INVALID
+        assert _bwd_mx(lib, window=w, lse=None) == INVALID
+        assert _bwd_mx(lib, window=w, out=FAKE + 4) == INVALID
+        assert _bwd_mx(lib, window=w, dk=None) == INVALID
+        assert _bwd_mx(lib, window=w, ws=None) == WORKSPACE
+        assert _bwd_mx(lib, window=w, ws_bytes=4096) == WORKSPACE
+        assert _bwd_mx(lib, window=w, B=0, Tq=0, Tkv=0) == OK
+    assert _bwd_mx(lib, window=-1) == INVALID
+
+
+def test_mxfp8_backward_workspace_size(lib):
+    """Seven E4M3 operand versions (Q, K, dO twice, V once), their scales, the
+    fp32 dQ accumulator, D and the work list."""
+    s = lib.gdpa_bwd_mxfp8_workspace_size
+    B, H, d, Tq, Tkv = 32, 4, 128, 69091, 69091
+    codes = (4 * Tq + 3 * Tkv) * H * d
+    assert s(B, H, d, Tq, Tkv) >= codes + Tq * H * d * 4 + Tq * H * 4
+    assert s(B, H, d, Tq, Tkv) < codes * 1.3 + Tq * H * d * 4 + (1 << 20)
+    assert s(-1, H, d, 1, 1) == 0 and s(B, 0, d, 1, 1) == 0 and s(B, H, 96, 1, 1) == 0

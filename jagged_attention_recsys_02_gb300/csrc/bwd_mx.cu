@@ -40,11 +40,14 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "mx.cuh"
 
 namespace gdpa {
 namespace {
 
 using namespace ptx;
+using mx::e4m3x4;
+using mx::e8m0_nosat;
 
 constexpr int kThreads = 512;
 constexpr int kProducerWarp = 12;
@@ -119,30 +122,6 @@ static_assert(Cfg::kDsT % 1024 == 0 && Cfg::kDsQ % 1024 == 0 && Cfg::kQd % 1024 
 static_assert((Cfg::kStatFloats * 4) % 16 == 0 && Cfg::kSf % 16 == 0, "alignment");
 static_assert(Cfg::kSmemBytes <= 232448, "shared memory budget");
 
-// Instruction descriptor of kind::mxf8f6f4, E4M3 x E4M3 with E8M0 scales,
-// M = 128: B scale-factor byte (bits 4-5), A / B MN-major (15 / 16), N >> 3
-// (17-22), E8M0 scale type (23), M >> 4 (24-28), A scale-factor byte (29-30).
-__device__ __forceinline__ uint32_t idesc_mx(int N, bool a_mn, bool b_mn, int sf_id) {
-  return (static_cast<uint32_t>(sf_id) << 4) | ((a_mn ? 1u : 0u) << 15) |
-         ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
-         (8u << 24) | (static_cast<uint32_t>(sf_id) << 29);
-}
-__device__ __forceinline__ void mma_mx_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t sfa, uint32_t sfb, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
-      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void mma_mx_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t sfa, uint32_t sfb, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], p;\n}\n"
-      ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
-      : "memory");
-}
 // Copies 32 rows x 16 bytes of shared memory (described by `desc`) into TMEM
 // lanes 0..31 of every lane quarter, columns taddr..taddr+3.
 __device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t desc) {
@@ -150,22 +129,6 @@ __device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t desc) {
                : "memory");
 }
 
-// E8M0 code of the smallest power of two X with amax / X <= 448 (E4M3's
-// largest normal), clamped to [0, 254]; amax is a non-negative float.
-__device__ __forceinline__ int e8m0_nosat(float amax) {
-  const uint32_t u = __float_as_uint(amax) & 0x7FFFFFFFu;
-  if (u == 0) return 0;
-  int e = (u >> 23) != 0 ? static_cast<int>(u >> 23) - 127 : -127 - (__clz(u) - 9);
-  if ((u >> 23) != 0 && (u & 0x7FFFFFu) > 0x600000u) ++e;  // mantissa above 1.75
-  const int code = e - 8 + 127;
-  return code < 0 ? 0 : (code > 254 ? 254 : code);
-}
-__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
-  uint16_t lo, hi;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
-  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-}
 __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
   uint32_t r;
   asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
@@ -530,8 +493,8 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
         const uint64_t qb = dadd(dsc_qd, s * C::kQBytes);
 #pragma unroll
         for (int ks = 0; ks < kD / 32; ++ks)
-          mma_mx_ss(tmem + kColS, dadd(dsc_kd, ks * 32), dadd(qb, ks * 32),
-                    idesc_mx(kQRows, false, false, ks), tmem + col_sf(kTmKd), tmem + col_sf(kTmQd),
+          mx::mma_ss(tmem + kColS, dadd(dsc_kd, ks * 32), dadd(qb, ks * 32),
+                    mx::idesc(kQRows, false, false, ks), tmem + col_sf(kTmKd), tmem + col_sf(kTmQd),
                     ks > 0 ? 1u : 0u);
         mma_commit(bar(C::kSFull));
         issued_any = true;
@@ -550,8 +513,8 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
         cp_sf(kSmOd, kTmOd);
 #pragma unroll
         for (int ks = 0; ks < kD / 32; ++ks)
-          mma_mx_ss(tmem + kColDP, dadd(dsc_vd, ks * 32), dadd(dsc_od, ks * 32),
-                    idesc_mx(kQRows, false, false, ks), tmem + col_sf(kTmVd), tmem + col_sf(kTmOd),
+          mx::mma_ss(tmem + kColDP, dadd(dsc_vd, ks * 32), dadd(dsc_od, ks * 32),
+                    mx::idesc(kQRows, false, false, ks), tmem + col_sf(kTmVd), tmem + col_sf(kTmOd),
                     ks > 0 ? 1u : 0u);
         mma_commit(bar(C::kDpFull));
         return true;
@@ -593,8 +556,8 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
           cp_sf(kSmOt, kTmOt);
 #pragma unroll
           for (int ks = 0; ks < kQRows / 32; ++ks)
-            mma_mx_ts(tmem + kColDV, tmem + kColS + 32 * ks, dadd(dsc_ot, ks * 4096),
-                      idesc_mx(kD, false, true, ks), tmem + col_sf(kTmP), tmem + col_sf(kTmOt),
+            mx::mma_ts(tmem + kColDV, tmem + kColS + 32 * ks, dadd(dsc_ot, ks * 4096),
+                      mx::idesc(kD, false, true, ks), tmem + col_sf(kTmP), tmem + col_sf(kTmOt),
                       (t == 0 && ks == 0) ? 0u : 1u);
           mma_commit(bar(C::kOEmpty));
           // S(t+1) reuses the S columns: it follows dV(t) on the pipe
@@ -613,16 +576,16 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
           const uint64_t qtb = dadd(dsc_qt, s * C::kQBytes);
 #pragma unroll
           for (int ks = 0; ks < kQRows / 32; ++ks)
-            mma_mx_ss(tmem + kColDK, dadd(dsc_dst, ks * 32), dadd(qtb, ks * 4096),
-                      idesc_mx(kD, false, true, ks), tmem + col_sf(kTmDsR), tmem + col_sf(kTmQt),
+            mx::mma_ss(tmem + kColDK, dadd(dsc_dst, ks * 32), dadd(qtb, ks * 4096),
+                      mx::idesc(kD, false, true, ks), tmem + col_sf(kTmDsR), tmem + col_sf(kTmQt),
                       (t == 0 && ks == 0) ? 0u : 1u);
           mma_commit(bar(C::kQEmpty + s));
           // dQ^T = K^T dS^T into the dP columns (A = K MN-major, B = dS K-major)
           cp_sf(kSmDsC, kTmDsC);
 #pragma unroll
           for (int ks = 0; ks < kKRows / 32; ++ks)
-            mma_mx_ss(tmem + kColDP, dadd(dsc_kt, ks * 4096), dadd(dsc_dsq, ks * 32),
-                      idesc_mx(kQRows, true, false, ks), tmem + col_sf(kTmKt), tmem + col_sf(kTmDsC),
+            mx::mma_ss(tmem + kColDP, dadd(dsc_kt, ks * 4096), dadd(dsc_dsq, ks * 32),
+                      mx::idesc(kQRows, true, false, ks), tmem + col_sf(kTmKt), tmem + col_sf(kTmDsC),
                       ks > 0 ? 1u : 0u);
           mma_commit(bar(C::kDqFull));
           dq_pending = true;

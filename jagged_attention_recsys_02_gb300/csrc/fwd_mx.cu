@@ -28,11 +28,14 @@
 //   warp  12         producer: tickets, TMA copies of Q/K/V codes, bias windows
 //   warp  13         MMA issuer
 #include "common.cuh"
+#include "mx.cuh"
 
 namespace gdpa {
 namespace {
 
 using namespace ptx;
+using mx::e4m3x4;
+using mx::e8m0_nosat;
 
 constexpr int kThreads = 448;
 constexpr int kScaleWarp0 = 8;
@@ -91,56 +94,11 @@ struct Cfg {
   static constexpr int kSmemBytes = kUsed + 1024;
 };
 
-// Instruction descriptor of kind::mxf8f6f4 with E4M3 operands and E8M0
-// scales: B scale-factor id (bits 4-5), A/B major (15, 16), N>>3 (17-22),
-// E8M0 scale type (23), M = 128 (M>>4 in bits 24-28), A scale-factor id (29-30).
-__device__ __forceinline__ uint32_t idesc_mx(int N, bool b_mn, int sf_id) {
-  return (static_cast<uint32_t>(sf_id) << 4) | ((b_mn ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (8u << 24) |
-         (static_cast<uint32_t>(sf_id) << 29);
-}
-
-__device__ __forceinline__ void mma_mx_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t sfa, uint32_t sfb, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
-      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void mma_mx_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t sfa, uint32_t sfb, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], p;\n}\n"
-      ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
-      : "memory");
-}
 __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c,
                                          uint32_t d) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(a),
                "r"(b), "r"(c), "r"(d)
                : "memory");
-}
-
-// E8M0 code of the smallest power of two X with amax / X <= 448 (E4M3's
-// largest normal), clamped to [0, 254].  For the probabilities P this
-// saturation-free choice is used instead of 2^(floor(log2 amax) - 8), which
-// maps the block maximum into [256, 512) and would clip a dominant
-// probability by up to 12.5% whenever its mantissa exceeds 1.75.
-__device__ __forceinline__ int e8m0_nosat(float amax) {
-  const uint32_t u = __float_as_uint(amax) & 0x7FFFFFFFu;
-  if (u == 0) return 0;
-  int e = (u >> 23) != 0 ? static_cast<int>(u >> 23) - 127 : -127 - (__clz(u) - 9);
-  if ((u >> 23) != 0 && (u & 0x7FFFFFu) > 0x600000u) ++e;  // mantissa above 1.75
-  const int code = e - 8 + 127;
-  return code < 0 ? 0 : (code > 254 ? 254 : code);
-}
-__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
-  uint16_t lo, hi;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
-  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
 struct ItemInfo {
@@ -428,7 +386,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         const uint64_t kb = dadd(dsc_kv, stage * 2 * C::kTileBytes);
 #pragma unroll
         for (int ks = 0; ks < kD / 32; ++ks) {
-          mma_mx_ss(tmem + col_s(half), dadd(qb, ks * 32), dadd(kb, ks * 32), idesc_mx(kTile, false, ks),
+          mx::mma_ss(tmem + col_s(half), dadd(qb, ks * 32), dadd(kb, ks * 32), mx::idesc(kTile, false, false, ks),
                     tmem + col_sfq(half), tmem + col_sfk(stage), ks > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kSFull + half));
@@ -439,7 +397,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 #pragma unroll
         for (int ks = 0; ks < kTile / 32; ++ks) {
           const uint64_t bd = dadd(vb, ks * 4096);
-          mma_mx_ts(tmem + col_o(half), tmem + col_s(half) + 8 * ks, bd, idesc_mx(kD, true, ks),
+          mx::mma_ts(tmem + col_o(half), tmem + col_s(half) + 8 * ks, bd, mx::idesc(kD, false, true, ks),
                     tmem + col_sfp(half), tmem + col_sfv(stage), (first && ks == 0) ? 0u : 1u);
         }
         issued_any = true;

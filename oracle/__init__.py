@@ -26,6 +26,7 @@ from .oracle import (  # noqa: F401
     bwd_mx_operands,
     bwd_mxfp8,
     dequant_cols,
+    dense_bias_offsets,
     dequant_rows,
     e4m3_decode,
     e4m3_encode,

@@ -17,6 +17,7 @@
  * The pages give no formula, so each step below is the plain definition:
  *
  *   s_ij = scale * <q_i, k_j> + bias_h(i - j)        (i < Lq_b, j < Lkv_b)
+ *          (or + B_b[h][i][j] with a dense jagged bias, see bias_value)
  *   mask_ij = (j <= i if causal) and (|i - j| < W if W > 0)
  *             and (floor(i / K) == floor(j / K) if K > 0)
  *   softmax: p_ij = exp(s_ij - M_i) / sum_{j' masked-in} exp(s_ij' - M_i)
@@ -121,6 +122,25 @@ static double bias_at(const double* table, int max_rel, int h, long i, long j) {
   return table[(long)h * width + idx];
 }
 
+/* Dense jagged bias (the JFA paragraph's custom biases in their general
+ * form): one value per (head, query, key) of each sample, sample b's
+ * [H][Lq_b][Lkv_b] block starting at element doff[b] (doff[0] = 0,
+ * doff[b+1] - doff[b] = H Lq_b Lkv_b).  NULL: the relative-position table. */
+static double bias_value(const double* table, int max_rel, const double* dense,
+                         const int64_t* doff, int b, int h, long Lq, long Lkv, long i, long j) {
+  if (dense != NULL) return dense[doff[b] + ((long)h * Lq + i) * Lkv + j];
+  return bias_at(table, max_rel, h, i, j);
+}
+
+static int check_dense(const double* dense, const int64_t* doff, const int32_t* qo,
+                       const int32_t* ko, int B, int H) {
+  if (dense == NULL) return 1;
+  if (doff == NULL || doff[0] != 0) return 0;
+  for (int b = 0; b < B; ++b)
+    if (doff[b + 1] - doff[b] != (int64_t)H * (qo[b + 1] - qo[b]) * (ko[b + 1] - ko[b])) return 0;
+  return 1;
+}
+
 static double dot(const double* a, const double* b, int d) {
   double s = 0.0;
   for (int c = 0; c < d; ++c) s += a[c] * b[c];
@@ -131,9 +151,9 @@ static double dot(const double* a, const double* b, int d) {
  * masked) and returns the row's lse (softmax) or 0.  `live[j]` marks
  * masked-in pairs. */
 static double row_probs(const double* q, const double* k, long qrow, long kbase, long Lkv, int H,
-                        int d, int h, long i, const double* bias, int max_rel, int act, int causal,
-                        int window, int block, double scale, double* s, double* p,
-                        unsigned char* live) {
+                        int d, int h, long i, const double* bias, int max_rel, const double* dense,
+                        const int64_t* doff, int b, long Lq, int act, int causal, int window,
+                        int block, double scale, double* s, double* p, unsigned char* live) {
   const double* qi = q + (qrow * H + h) * (long)d;
   long n_live = 0;
   for (long j = 0; j < Lkv; ++j) {
@@ -144,7 +164,7 @@ static double row_probs(const double* q, const double* k, long qrow, long kbase,
     if (!live[j]) { s[j] = 0.0; p[j] = 0.0; continue; }
     ++n_live;
     const double* kj = k + ((kbase + j) * H + h) * (long)d;
-    s[j] = scale * dot(qi, kj, d) + bias_at(bias, max_rel, h, i, j);
+    s[j] = scale * dot(qi, kj, d) + bias_value(bias, max_rel, dense, doff, b, h, Lq, Lkv, i, j);
   }
   if (act != ORC_ACT_SOFTMAX) {
     for (long j = 0; j < Lkv; ++j) p[j] = live[j] ? act_value(act, s[j]) : 0.0;
@@ -176,9 +196,11 @@ static int check_offsets(const int32_t* o, int B) {
 /* Forward.  Returns 0 on success, -1 on bad arguments. */
 int oracle_fwd(const double* q, const int32_t* qo, const double* k, const double* v,
                const int32_t* ko, int B, int H, int d, const double* bias, int max_rel, int act,
-               int causal, int window, int block, double scale, double* out, double* lse) {
+               int causal, int window, int block, double scale, double* out, double* lse,
+               const double* dense, const int64_t* doff) {
   if (B < 0 || H <= 0 || d <= 0 || act < 0 || act > 4) return -1;
   if (!check_offsets(qo, B) || !check_offsets(ko, B)) return -1;
+  if (!check_dense(dense, doff, qo, ko, B, H)) return -1;
   if (window < 0 || block < 0) return -1;
   if (causal || window > 0 || block > 0)
     for (int b = 0; b < B; ++b)
@@ -194,8 +216,8 @@ int oracle_fwd(const double* q, const int32_t* qo, const double* k, const double
     double* p = (double*)malloc(sizeof(double) * (size_t)(Lkv > 0 ? Lkv : 1));
     unsigned char* live = (unsigned char*)malloc((size_t)(Lkv > 0 ? Lkv : 1));
     for (long i = 0; i < Lq; ++i) {
-      const double l = row_probs(q, k, q0 + i, k0, Lkv, H, d, h, i, bias, max_rel, act, causal,
-                                 window, block, scale, s, p, live);
+      const double l = row_probs(q, k, q0 + i, k0, Lkv, H, d, h, i, bias, max_rel, dense, doff,
+                                 b, Lq, act, causal, window, block, scale, s, p, live);
       double* oi = out + ((q0 + i) * H + h) * (long)d;
       for (int c = 0; c < d; ++c) oi[c] = 0.0;
       for (long j = 0; j < Lkv; ++j) {
@@ -218,9 +240,10 @@ int oracle_fwd(const double* q, const int32_t* qo, const double* k, const double
 int oracle_bwd(const double* q, const int32_t* qo, const double* k, const double* v,
                const int32_t* ko, int B, int H, int d, const double* bias, int max_rel, int act,
                int causal, int window, int block, double scale, const double* dout, double* dq,
-               double* dk, double* dv, double* dbias) {
+               double* dk, double* dv, double* dbias, const double* dense, const int64_t* doff) {
   if (B < 0 || H <= 0 || d <= 0 || act < 0 || act > 4) return -1;
   if (!check_offsets(qo, B) || !check_offsets(ko, B)) return -1;
+  if (!check_dense(dense, doff, qo, ko, B, H) || (dense != NULL && dbias != NULL)) return -1;
   if (window < 0 || block < 0) return -1;
   if (causal || window > 0 || block > 0)
     for (int b = 0; b < B; ++b)
@@ -254,8 +277,8 @@ int oracle_bwd(const double* q, const int32_t* qo, const double* k, const double
       const double* doi = dout + ((q0 + i) * H + h) * (long)d;
       double* dqi = dq + ((q0 + i) * H + h) * (long)d;
       for (int c = 0; c < d; ++c) dqi[c] = 0.0;
-      row_probs(q, k, q0 + i, k0, Lkv, H, d, h, i, bias, max_rel, act, causal, window, block, scale,
-                s, p, live);
+      row_probs(q, k, q0 + i, k0, Lkv, H, d, h, i, bias, max_rel, dense, doff, b, Lq, act, causal,
+                window, block, scale, s, p, live);
       double row_dot = 0.0; /* sum_j p_ij dp_ij (softmax only) */
       for (long j = 0; j < Lkv; ++j) {
         const double* vj = v + ((k0 + j) * H + h) * (long)d;

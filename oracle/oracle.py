@@ -47,9 +47,11 @@ def _load():
         ip = ctypes.POINTER(ctypes.c_int32)
         up = ctypes.POINTER(ctypes.c_uint8)
         I, D = ctypes.c_int, ctypes.c_double
-        lib.oracle_fwd.argtypes = [dp, ip, dp, dp, ip, I, I, I, dp, I, I, I, I, I, D, dp, dp]
+        lp = ctypes.POINTER(ctypes.c_int64)
+        lib.oracle_fwd.argtypes = [dp, ip, dp, dp, ip, I, I, I, dp, I, I, I, I, I, D, dp, dp, dp, lp]
         lib.oracle_fwd.restype = I
-        lib.oracle_bwd.argtypes = [dp, ip, dp, dp, ip, I, I, I, dp, I, I, I, I, I, D, dp, dp, dp, dp, dp]
+        lib.oracle_bwd.argtypes = [dp, ip, dp, dp, ip, I, I, I, dp, I, I, I, I, I, D, dp, dp, dp, dp, dp,
+                                   dp, lp]
         lib.oracle_bwd.restype = I
         lib.oracle_e4m3_encode.argtypes = [D]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
@@ -96,8 +98,26 @@ def _bias_arg(bias, H, max_rel):
     return b, _p(b, ctypes.c_double)
 
 
+def dense_bias_offsets(q_offsets, kv_offsets, H: int) -> np.ndarray:
+    """Element offset of each sample's [H][Lq][Lkv] block in a dense jagged
+    bias: H * prefix sums of Lq_b * Lkv_b (int64 [B+1])."""
+    qo, ko = _i32(q_offsets).astype(np.int64), _i32(kv_offsets).astype(np.int64)
+    o = np.zeros(len(qo), dtype=np.int64)
+    o[1:] = np.cumsum(H * np.diff(qo) * np.diff(ko))
+    return o
+
+
+def _dense_arg(dense_bias, qo, ko, H):
+    if dense_bias is None:
+        return None, ctypes.POINTER(ctypes.c_double)(), ctypes.POINTER(ctypes.c_int64)()
+    dv = _f64(dense_bias).reshape(-1)
+    off = np.ascontiguousarray(dense_bias_offsets(qo, ko, H))
+    assert dv.size == off[-1], (dv.size, off[-1])
+    return (dv, off), _p(dv, ctypes.c_double), _p(off, ctypes.c_int64)
+
+
 def fwd(q, q_offsets, k, v, kv_offsets, *, act: int, causal: bool = False, scale: float,
-        bias=None, max_rel: int = 0, window: int = 0, block: int = 0):
+        bias=None, max_rel: int = 0, window: int = 0, block: int = 0, dense_bias=None):
     """Forward pass.  Returns (out [Tq,H,d] float64, lse [H,Tq] float64).
 
     lse is the natural-log row logsumexp for softmax (-inf for a row with no
@@ -105,7 +125,9 @@ def fwd(q, q_offsets, k, v, kv_offsets, *, act: int, causal: bool = False, scale
     with |i - j| < window (sliding-window attention; needs Lq == Lkv).
     block > 0 keeps only the pairs inside one block of `block` tokens, the
     blocks starting at each sample's first token (block-aligned attention;
-    needs Lq == Lkv)."""
+    needs Lq == Lkv).  dense_bias, instead of the table, gives one bias value
+    per (head, query, key): the samples' [H][Lq_b][Lkv_b] blocks one after
+    another (dense_bias_offsets)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     qo, ko = _i32(q_offsets), _i32(kv_offsets)
     Tq, H, d = q.shape
@@ -115,11 +137,12 @@ def fwd(q, q_offsets, k, v, kv_offsets, *, act: int, causal: bool = False, scale
     out = np.zeros((Tq, H, d), dtype=np.float64)
     lse = np.zeros((H, Tq), dtype=np.float64)
     keep, bp = _bias_arg(bias, H, max_rel)
+    keep_d, dp_, op_ = _dense_arg(dense_bias, qo, ko, H)
     rc = _load().oracle_fwd(_p(q, ctypes.c_double), _p(qo, ctypes.c_int32),
                             _p(k, ctypes.c_double), _p(v, ctypes.c_double),
                             _p(ko, ctypes.c_int32), B, H, d, bp, int(max_rel), int(act),
                             int(bool(causal)), int(window), int(block), float(scale),
-                            _p(out, ctypes.c_double), _p(lse, ctypes.c_double))
+                            _p(out, ctypes.c_double), _p(lse, ctypes.c_double), dp_, op_)
     if rc != 0:
         raise ValueError("oracle_fwd rejected its arguments")
     del keep
@@ -127,7 +150,8 @@ def fwd(q, q_offsets, k, v, kv_offsets, *, act: int, causal: bool = False, scale
 
 
 def bwd(q, q_offsets, k, v, kv_offsets, dout, *, act: int, causal: bool = False, scale: float,
-        bias=None, max_rel: int = 0, window: int = 0, block: int = 0, want_dbias: bool = False):
+        bias=None, max_rel: int = 0, window: int = 0, block: int = 0, want_dbias: bool = False,
+        dense_bias=None):
     """Backward pass.  Returns (dq, dk, dv) as float64 arrays, and with
     want_dbias also the bias table's gradient [H, 2*max_rel-1]:
     (dq, dk, dv, dbias)."""
@@ -141,6 +165,7 @@ def bwd(q, q_offsets, k, v, kv_offsets, dout, *, act: int, causal: bool = False,
     dv = np.zeros_like(v)
     dbias = np.zeros((H, 2 * max(int(max_rel), 1) - 1), dtype=np.float64) if want_dbias else None
     keep, bp = _bias_arg(bias, H, max_rel)
+    keep_d, dp_, op_ = _dense_arg(dense_bias, qo, ko, H)
     rc = _load().oracle_bwd(_p(q, ctypes.c_double), _p(qo, ctypes.c_int32),
                             _p(k, ctypes.c_double), _p(v, ctypes.c_double),
                             _p(ko, ctypes.c_int32), B, H, d, bp, int(max_rel), int(act),
@@ -148,7 +173,7 @@ def bwd(q, q_offsets, k, v, kv_offsets, dout, *, act: int, causal: bool = False,
                             _p(do, ctypes.c_double), _p(dq, ctypes.c_double),
                             _p(dk, ctypes.c_double), _p(dv, ctypes.c_double),
                             _p(dbias, ctypes.c_double) if dbias is not None
-                            else ctypes.POINTER(ctypes.c_double)())
+                            else ctypes.POINTER(ctypes.c_double)(), dp_, op_)
     if rc != 0:
         raise ValueError("oracle_bwd rejected its arguments")
     del keep

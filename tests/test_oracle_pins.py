@@ -994,3 +994,109 @@ def test_bwd_mxfp8_on_exactly_representable_inputs(oracle_mod):
                                      scale=scale, round_ps=True)
     for g, r in zip(got, ref):
         np.testing.assert_array_equal(g, r)
+
+
+# --------------------------------------------------------------- dense jagged bias
+def _dense_from_table(table, lq, lkv, max_rel):
+    """The relative-position table written out as a dense jagged bias."""
+    parts = []
+    for Lq, Lkv in zip(lq, lkv):
+        for h in range(table.shape[0]):
+            parts.append(_relpos_mask(table[h], Lq, Lkv, max_rel).reshape(-1))
+    return np.concatenate(parts) if parts else np.zeros(0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dense_bias_matches_torch_sdpa(oracle_mod, causal):
+    """Softmax forward with a random dense bias against torch's fp64 SDPA with
+    that bias as the additive mask, sample by sample and head by head."""
+    lq = [5, 1, 33, 17]
+    lkv = lq if causal else [9, 4, 20, 1]
+    H, d = 3, 8
+    qo, ko = _offsets(lq), _offsets(lkv)
+    q = _bf16_randn((sum(lq), H, d), 51)
+    k = _bf16_randn((sum(lkv), H, d), 52)
+    v = _bf16_randn((sum(lkv), H, d), 53)
+    off = oracle_mod.dense_bias_offsets(qo, ko, H)
+    dense = np.random.default_rng(9).normal(0, 1.0, int(off[-1]))
+    scale = 1.0 / math.sqrt(d)
+    out, lse = oracle_mod.fwd(q, qo, k, v, ko, act=ACT_SOFTMAX, causal=causal, scale=scale,
+                              dense_bias=dense)
+    for b in range(len(lq)):
+        Lq, Lkv = lq[b], lkv[b]
+        blk = dense[off[b]:off[b + 1]].reshape(H, Lq, Lkv)
+        for h in range(H):
+            mask = torch.from_numpy(blk[h].copy())
+            if causal:
+                mask = mask.masked_fill(torch.ones(Lq, Lkv).triu(1).bool(), float("-inf"))
+            qs = torch.from_numpy(q[qo[b]:qo[b + 1], h].copy())[None, None]
+            ks = torch.from_numpy(k[ko[b]:ko[b + 1], h].copy())[None, None]
+            vs = torch.from_numpy(v[ko[b]:ko[b + 1], h].copy())[None, None]
+            ref = F.scaled_dot_product_attention(qs, ks, vs, attn_mask=mask, scale=scale)[0, 0]
+            np.testing.assert_allclose(out[qo[b]:qo[b + 1], h], ref.numpy(), rtol=1e-12, atol=1e-12)
+            s_ = scale * (qs[0, 0] @ ks[0, 0].T) + mask
+            np.testing.assert_allclose(lse[h, qo[b]:qo[b + 1]], torch.logsumexp(s_, -1).numpy(),
+                                       rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH])
+@pytest.mark.parametrize("causal", [False, True])
+def test_dense_bias_written_from_the_table_equals_the_table(oracle_mod, act, causal):
+    """A dense bias holding the relative-position table's values gives the
+    table's forward and backward (each pinned on its own): catches a swapped
+    query / key index, a wrong head or a wrong sample offset."""
+    lq = [6, 0, 40, 13]
+    lkv = lq if causal else [3, 7, 21, 13]
+    H, d, max_rel = 2, 8, 9
+    qo, ko = _offsets(lq), _offsets(lkv)
+    q = _bf16_randn((sum(lq), H, d), 61)
+    k = _bf16_randn((sum(lkv), H, d), 62)
+    v = _bf16_randn((sum(lkv), H, d), 63)
+    do = _bf16_randn((sum(lq), H, d), 64)
+    table = np.random.default_rng(4).normal(0, 0.7, (H, 2 * max_rel - 1))
+    dense = _dense_from_table(table, lq, lkv, max_rel)
+    kw = dict(act=act, causal=causal, scale=1.0 / math.sqrt(d))
+    a = oracle_mod.fwd(q, qo, k, v, ko, bias=table, max_rel=max_rel, **kw)
+    b = oracle_mod.fwd(q, qo, k, v, ko, dense_bias=dense, **kw)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    a = oracle_mod.bwd(q, qo, k, v, ko, do, bias=table, max_rel=max_rel, **kw)
+    b = oracle_mod.bwd(q, qo, k, v, ko, do, dense_bias=dense, **kw)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_dense_bias_backward_matches_central_differences(oracle_mod):
+    """The backward under a random (non-Toeplitz) dense bias against central
+    differences of the forward."""
+    lq, lkv = [4, 3], [5, 2]
+    H, d = 2, 4
+    qo, ko = _offsets(lq), _offsets(lkv)
+    rng = np.random.default_rng(7)
+    q, k, v = (rng.standard_normal((sum(n), H, d)) for n in (lq, lkv, lkv))
+    do = rng.standard_normal((sum(lq), H, d))
+    dense = rng.normal(0, 1.0, int(oracle_mod.dense_bias_offsets(qo, ko, H)[-1]))
+    for act in (ACT_SOFTMAX, ACT_SILU):
+        kw = dict(act=act, scale=0.7, dense_bias=dense)
+        dq, dk, dv = oracle_mod.bwd(q, qo, k, v, ko, do, **kw)
+        loss = lambda q_, k_, v_: float((oracle_mod.fwd(q_, qo, k_, v_, ko, **kw)[0] * do).sum())
+        h = 1e-6
+        for x, g, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(*x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args_p = [q, k, v]
+                args_m = [q, k, v]
+                args_p[which], args_m[which] = xp, xm
+                num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-7)
+
+
+def test_dense_bias_rejects_a_wrong_size(oracle_mod):
+    lq = [3, 2]
+    qo = _offsets(lq)
+    x = np.zeros((5, 1, 4))
+    with pytest.raises(AssertionError):
+        oracle_mod.fwd(x, qo, x, x, qo, act=ACT_SOFTMAX, scale=1.0, dense_bias=np.zeros(12))

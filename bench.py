@@ -255,9 +255,12 @@ def oracle_step(w, tensors, samples):
     """One oracle forward + backward over the given samples (host float64)."""
     import oracle
 
+    from jagged_attention_recsys_02_gb300.workloads import ACTS
+
     qo, ko = w.offsets()
-    a = {"softmax": 0, "silu": 1, "gelu_tanh": 2, "identity": 3}[w.act]
+    a = ACTS[w.act]
     bias = tensors.get("bias_np")
+    dense = tensors.get("dense_np", {})
     for b in samples:
         q0, q1, k0, k1 = int(qo[b]), int(qo[b + 1]), int(ko[b]), int(ko[b + 1])
         sq = tensors["q_np"][q0:q1]
@@ -266,10 +269,10 @@ def oracle_step(w, tensors, samples):
         sd = tensors["do_np"][q0:q1]
         oq = np.array([0, q1 - q0], dtype=np.int32)
         ok = np.array([0, k1 - k0], dtype=np.int32)
-        oracle.fwd(sq, oq, sk, sv, ok, act=a, causal=w.causal, scale=w.scale, bias=bias,
-                   max_rel=w.max_rel, window=w.window, block=w.block)
-        oracle.bwd(sq, oq, sk, sv, ok, sd, act=a, causal=w.causal, scale=w.scale, bias=bias,
-                   max_rel=w.max_rel, window=w.window, block=w.block)
+        kw = dict(act=a, causal=w.causal, scale=w.scale, bias=bias, max_rel=w.max_rel,
+                  window=w.window, block=w.block, dense_bias=dense.get(b))
+        oracle.fwd(sq, oq, sk, sv, ok, **kw)
+        oracle.bwd(sq, oq, sk, sv, ok, sd, **kw)
 
 
 def host_sample_tensors(w, samples, device_tensors=None, seed=0):
@@ -292,7 +295,12 @@ def host_sample_tensors(w, samples, device_tensors=None, seed=0):
             a0, a1 = int(offs[b]), int(offs[b + 1])
             arr[a0:a1] = t[a0:a1].float().cpu().double().numpy()
         out[name] = arr
-    if src.get("bias") is not None:
+    if w.dense:  # the chosen samples' [H][Lq][Lkv] blocks of the dense bias
+        vals, off = src["bias"]
+        off = off.cpu().numpy()
+        out["dense_np"] = {b: vals[int(off[b]):int(off[b + 1])].cpu().double().numpy()
+                           for b in samples}
+    elif src.get("bias") is not None:
         out["bias_np"] = src["bias"].cpu().double().numpy()
     del torch
     return out
@@ -374,7 +382,9 @@ def run_reference(args, rank, world):
 def workload_config(w, l2_note):
     return {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "act": w.act, "causal": w.causal,
             "window": w.window, "block": w.block,
-            "bias": (f"relpos table [{w.H},{2 * w.max_rel - 1}]" if w.max_rel else "none"),
+            "bias": (f"relpos table [{w.H},{2 * w.max_rel - 1}]" if w.max_rel else
+                     (f"dense jagged fp32 [{w.H * int((w.lq * w.lkv).sum())}]" if w.dense
+                      else "none")),
             "Tq": w.Tq, "Tkv": w.Tkv, "pairs_non_padded": w.pairs(),
             "pairs_full_square": w.full_pairs(), "step": "forward + backward", "l2": l2_note}
 
@@ -396,6 +406,12 @@ def run_gpu(args, rank, world, local_rank):
     w = make_workload(args.workload, act=args.act)
     if args.samples:
         w = first_samples(w, args.samples)
+    skipped = None
+    if w.dense:
+        # the dense bias (GBs) is an input: an end-to-end step would mostly time its
+        # host copy, and the padded SDPA comparison has no mask builder for it
+        args.no_e2e = args.no_sdpa = True
+        skipped = "dense bias: e2e and padded SDPA not run for this workload"
     t = make_tensors(w, device=dev, seed=rank)
     a = ACTS[w.act]
     H, d, Tq, Tkv = w.H, w.d, w.Tq, w.Tkv
@@ -482,6 +498,16 @@ def run_gpu(args, rank, world, local_rank):
     achieved = b_tf if dominant == "bwd" else f_tf
     traffic = load_traffic().get(f"{w.name}/{w.act}/{dominant}")
     hbm = None
+    if w.dense:
+        # bound by reading the dense bias: algorithmic bytes are the bias (fp32,
+        # once per pass) plus q, k, v read and out written (forward) or q, k, v,
+        # out, dO read and dq, dk, dv written (backward), bf16
+        row_bytes = H * d * 2
+        bias_bytes = int(t["bias"][0].numel()) * 4
+        f_bytes = bias_bytes + 4 * Tq * row_bytes
+        b_bytes = bias_bytes + 8 * Tq * row_bytes
+        hbm = {"fwd_gbs": f_bytes / (f_avg * 1e-3) / 1e9, "bwd_gbs": b_bytes / (b_avg * 1e-3) / 1e9,
+               "fwd_bytes": f_bytes, "bwd_bytes": b_bytes}
     if w.block:
         # 64 x 64 problems are bound by HBM traffic: algorithmic bytes are q, k, v
         # read and out written once (forward), q, k, v, dO read and dq, dk, dv
@@ -631,7 +657,8 @@ def run_gpu(args, rank, world, local_rank):
                       "frac": achieved / peak, "traffic": traffic,
                       "peak_source": ("bf16_tflops_sustained" if sustained else "bf16_tflops")
                       + f" of {peak_src}"} if hbm is None else
-                     {"bound": "hbm", "kernel": f"block {dominant} kernel",
+                     {"bound": "hbm",
+                      "kernel": f"{'dense-bias' if w.dense else 'block'} {dominant} kernel",
                       "achieved": hbm[f"{dominant}_gbs"], "peak": float(peaks["hbm_gbs"]),
                       "unit": "GB/s", "frac": hbm[f"{dominant}_gbs"] / float(peaks["hbm_gbs"]),
                       "traffic": traffic, "algorithmic_bytes": hbm[f"{dominant}_bytes"],
@@ -640,6 +667,7 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": e2e,
         "hbm": hbm,
+        **({"skipped": skipped} if skipped else {}),
         "cpu_baseline": cpu,
         "padded_sdpa": sdpa,
     }

@@ -61,16 +61,26 @@ typedef enum {
   GDPA_ACT_GELU_ERF = 4   /* GDPA, exact GELU 0.5 x (1 + erf(x / sqrt(2))) */
 } gdpa_act;
 
-typedef enum { GDPA_BIAS_NONE = 0, GDPA_BIAS_RELPOS = 1 } gdpa_bias_kind;
+typedef enum { GDPA_BIAS_NONE = 0, GDPA_BIAS_RELPOS = 1, GDPA_BIAS_DENSE = 2 } gdpa_bias_kind;
 
 /* Additive attention bias ("custom attention biases", JFA paragraph).
  * GDPA_BIAS_RELPOS: per-head relative-position table, fp32 device memory
  * [H][2*max_rel-1]; bias_h(i-j) = table[h][clamp(i-j+max_rel-1, 0, 2*max_rel-2)]
- * with per-sample local positions i, j.  1 <= max_rel <= 65536. */
+ * with per-sample local positions i, j.  1 <= max_rel <= 65536.
+ * GDPA_BIAS_DENSE: a dense jagged bias, one fp32 value per (head, query, key)
+ * of each sample: `table` holds the samples' [H][Lq_b][Lkv_b] blocks one after
+ * another, sample b's block starting at element offsets[b] (int64 device
+ * array [B+1], offsets[0] = 0, offsets[b+1] - offsets[b] = H Lq_b Lkv_b;
+ * a mismatch is reported as GDPA_ERR_BAD_OFFSETS through the device status).
+ * max_rel is ignored.  The dense bias is read from global memory by the
+ * kernels' activation warps; it is supported by gdpa_fwd, gdpa_bwd and
+ * gdpa_fwd_noalloc (no window, no bias gradient); the other entry points
+ * return GDPA_ERR_UNSUPPORTED. */
 typedef struct {
-  int kind;            /* gdpa_bias_kind */
-  const float* table;  /* device pointer, ignored for GDPA_BIAS_NONE */
+  int kind;                /* gdpa_bias_kind */
+  const float* table;      /* device pointer, ignored for GDPA_BIAS_NONE */
   int max_rel;
+  const int64_t* offsets;  /* GDPA_BIAS_DENSE only (device pointer), else ignored */
 } gdpa_bias;
 
 typedef enum {

@@ -19,7 +19,7 @@ from . import build as _build
 ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH, ACT_IDENTITY, ACT_GELU_ERF = 0, 1, 2, 3, 4
 ACT_BY_NAME = {"softmax": ACT_SOFTMAX, "silu": ACT_SILU, "gelu_tanh": ACT_GELU_TANH,
                "identity": ACT_IDENTITY, "gelu_erf": ACT_GELU_ERF}
-BIAS_NONE, BIAS_RELPOS = 0, 1
+BIAS_NONE, BIAS_RELPOS, BIAS_DENSE = 0, 1, 2
 
 STATUS_NAMES = {0: "GDPA_OK", 1: "GDPA_ERR_INVALID_ARG", 2: "GDPA_ERR_UNSUPPORTED",
                 3: "GDPA_ERR_WORKSPACE", 4: "GDPA_ERR_CUDA", 5: "GDPA_ERR_TIMEOUT",
@@ -43,7 +43,8 @@ class GdpaError(RuntimeError):
 
 
 class gdpa_bias(ctypes.Structure):
-    _fields_ = [("kind", ctypes.c_int), ("table", ctypes.c_void_p), ("max_rel", ctypes.c_int)]
+    _fields_ = [("kind", ctypes.c_int), ("table", ctypes.c_void_p), ("max_rel", ctypes.c_int),
+                ("offsets", ctypes.c_void_p)]
 
 
 _lib = None
@@ -140,10 +141,15 @@ def _stream(stream) -> int:
     return stream.cuda_stream
 
 
-def _bias(table, max_rel):
-    if table is None:
+def _bias(bias, max_rel):
+    """bias: None, a relative-position table [H, 2*max_rel-1] fp32, or a dense
+    jagged bias given as (values fp32 [sum_b H*Lq_b*Lkv_b], offsets int64 [B+1])."""
+    if bias is None:
         return None
-    return ctypes.byref(gdpa_bias(BIAS_RELPOS, table.data_ptr(), int(max_rel)))
+    if isinstance(bias, tuple):
+        values, offsets = bias
+        return ctypes.byref(gdpa_bias(BIAS_DENSE, values.data_ptr(), 0, offsets.data_ptr()))
+    return ctypes.byref(gdpa_bias(BIAS_RELPOS, bias.data_ptr(), int(max_rel), None))
 
 
 def _act(act) -> int:

@@ -146,6 +146,14 @@ gdpa_status check_common(const void* q, const int32_t* qo, const void* k, const 
   if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return GDPA_ERR_INVALID_ARG;
   if (Tq > (int64_t(1) << 31) - 1 || Tkv > (int64_t(1) << 31) - 1) return GDPA_ERR_UNSUPPORTED;
   if (bias != nullptr && bias->kind != GDPA_BIAS_NONE) {
+    if (bias->kind == GDPA_BIAS_DENSE) {
+      if (bias->table == nullptr || bias->offsets == nullptr ||
+          (reinterpret_cast<uintptr_t>(bias->table) & 3u) ||
+          (reinterpret_cast<uintptr_t>(bias->offsets) & 7u))
+        return GDPA_ERR_INVALID_ARG;
+      if (window > 0) return GDPA_ERR_UNSUPPORTED;  // built without the window
+      return GDPA_OK;
+    }
     if (bias->kind != GDPA_BIAS_RELPOS) return GDPA_ERR_INVALID_ARG;
     if (bias->table == nullptr || bias->max_rel < 1 || bias->max_rel > 65536)
       return GDPA_ERR_INVALID_ARG;
@@ -153,8 +161,11 @@ gdpa_status check_common(const void* q, const int32_t* qo, const void* k, const 
   return GDPA_OK;
 }
 
+bool is_dense(const gdpa_bias* bias) { return bias != nullptr && bias->kind == GDPA_BIAS_DENSE; }
+
+// The relative-position table (nullptr for no bias or a dense bias).
 const float* bias_table(const gdpa_bias* bias, int* max_rel) {
-  if (bias == nullptr || bias->kind == GDPA_BIAS_NONE) {
+  if (bias == nullptr || bias->kind != GDPA_BIAS_RELPOS) {
     *max_rel = 1;
     return nullptr;
   }
@@ -205,6 +216,7 @@ gdpa_status gdpa_fwd_window(const void* q, const int32_t* q_offsets, const void*
 
   int max_rel = 1;
   const float* table = bias_table(bias, &max_rel);
+  const int64_t* dense_off = is_dense(bias) ? bias->offsets : nullptr;
   CUtensorMap tq, tk, tv;
   if (!make_thd_map(&tq, q, Tq, H, d, kHalfRows)) return GDPA_ERR_INVALID_ARG;
   // With no key rows at all there is nothing to load; any valid map will do.
@@ -220,7 +232,7 @@ gdpa_status gdpa_fwd_window(const void* q, const int32_t* q_offsets, const void*
   int2* items = reinterpret_cast<int2*>(ws + 256);
 
   if (launch_build_worklist(q_offsets, kv_offsets, B, H, Tq, Tkv, causal, window, 0, items,
-                            n_items, ticket, dev->status, s) != cudaSuccess)
+                            n_items, ticket, dev->status, s, dense_off) != cudaSuccess)
     return GDPA_ERR_CUDA;
   ++t_launches;
 
@@ -237,6 +249,8 @@ gdpa_status gdpa_fwd_window(const void* q, const int32_t* q_offsets, const void*
   p.causal = causal;
   p.window = window;
   p.scale = scale;
+  p.bias_dense = dense_off != nullptr ? bias->table : nullptr;
+  p.bias_off = dense_off;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.items = items;
@@ -303,6 +317,7 @@ gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void*
 
   int max_rel = 1;
   const float* table = bias_table(bias, &max_rel);
+  const int64_t* dense_off = is_dense(bias) ? bias->offsets : nullptr;
   // Maps need at least one row; an empty side is never loaded, so any
   // valid tensor stands in for it.
   const void* qb = Tq > 0 ? q : k;
@@ -336,7 +351,7 @@ gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void*
     return GDPA_ERR_INVALID_ARG;
 
   if (launch_build_worklist(kv_offsets, q_offsets, B, H, Tkv, Tq, causal, window, 1, items,
-                            n_items, ticket, dev->status, s) != cudaSuccess)
+                            n_items, ticket, dev->status, s, dense_off) != cudaSuccess)
     return GDPA_ERR_CUDA;
   ++t_launches;
 
@@ -353,6 +368,8 @@ gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void*
   p.causal = causal;
   p.window = window;
   p.scale = scale;
+  p.bias_dense = dense_off != nullptr ? bias->table : nullptr;
+  p.bias_off = dense_off;
   p.out = static_cast<const __nv_bfloat16*>(out);
   p.lse = lse;
   p.dout = static_cast<const __nv_bfloat16*>(dout);
@@ -396,6 +413,7 @@ gdpa_status gdpa_block_fwd(const void* q, const int32_t* offsets, const void* k,
   t_launches = 0;
   gdpa_status st = check_common(q, offsets, k, v, offsets, B, H, d, T, T, bias, act, causal, 0);
   if (st != GDPA_OK) return st;
+  if (is_dense(bias)) return GDPA_ERR_UNSUPPORTED;
   if (T > 0 && (out == nullptr || !aligned16(out))) return GDPA_ERR_INVALID_ARG;
   const size_t need = gdpa_block_workspace_size(B, H, d, T);
   if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return GDPA_ERR_WORKSPACE;
@@ -446,6 +464,7 @@ gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k,
   t_launches = 0;
   gdpa_status st = check_common(q, offsets, k, v, offsets, B, H, d, T, T, bias, act, causal, 0);
   if (st != GDPA_OK) return st;
+  if (is_dense(bias)) return GDPA_ERR_UNSUPPORTED;
   if (!(rope_base >= 0.0f) || rope_base > 3.0e38f) return GDPA_ERR_INVALID_ARG;  // NaN, < 0, inf
   if (T > 0 && (dout == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
                 !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)))
@@ -543,6 +562,7 @@ gdpa_status gdpa_fwd_mxfp8_window(const void* q_codes, const void* q_scales,
   gdpa_status st = check_common(q_codes, q_offsets, k_codes, v_codes, kv_offsets, B, H, d, Tq,
                                 Tkv, bias, act, causal, window);
   if (st != GDPA_OK) return st;
+  if (is_dense(bias)) return GDPA_ERR_UNSUPPORTED;
   if (d != 128 || act != GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
   if (Tq > 0 && (q_scales == nullptr || out == nullptr || lse == nullptr || !aligned16(out)))
     return GDPA_ERR_INVALID_ARG;
@@ -670,7 +690,7 @@ gdpa_status gdpa_bwd_mxfp8_window(const void* q, const int32_t* q_offsets, const
   gdpa_status st = check_common(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act,
                                 causal, window);
   if (st != GDPA_OK) return st;
-  if (d != 128 || act != GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
+  if (d != 128 || act != GDPA_ACT_SOFTMAX || is_dense(bias)) return GDPA_ERR_UNSUPPORTED;
   if (Tq > 0 && (dout == nullptr || dq == nullptr || out == nullptr || lse == nullptr ||
                  !aligned16(dout) || !aligned16(dq) || !aligned16(out)))
     return GDPA_ERR_INVALID_ARG;

@@ -122,8 +122,10 @@ __device__ __forceinline__ BwdItem decode_bwd(int2 it, const BwdParams& p) {
 }
 
 // With a bias-table gradient one more warp (14) adds each tile's diagonal
-// sums to the table.
-template <int D, int ACT, bool kDBias>
+// sums to the table.  kDense: a dense jagged bias (p.bias_dense) instead of
+// the relative-position table, read from global memory by the activation
+// warps (the warp's lanes are consecutive keys: coalesced row segments).
+template <int D, int ACT, bool kDBias, bool kDense>
 __global__ void __launch_bounds__(kThreads + (kDBias ? 32 : 0), 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
            const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
@@ -464,6 +466,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       // block's last key bounds the first such query and its first key the last).
       const int full_lo = band_query_begin(kb0 + kBwdKvRows - 1, p.causal, p.window);
       const int full_hi = kb0 + kBwdKvRows <= in.Lkv ? band_query_end(kb0, p.window, in.Lq) : 0;
+      // dense bias of this key for query i: dcol[i * Lkv] (a key past the sample reads none)
+      const float* dcol = (kDense && jl < in.Lkv)
+                              ? p.bias_dense + p.bias_off[in.b] +
+                                    static_cast<long long>(in.head) * in.Lq * in.Lkv + jl
+                              : nullptr;
       bool abort_now = false;
       for (int t = 0; t < in.nq; ++t, ++g) {
         const uint32_t s = g % C::kStages;
@@ -503,7 +510,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
               const int c = c0 + i + e;
               const float sv = __uint_as_float(sr[half * 16 + i + e]);
               const float dp = __uint_as_float(dr[i + e]);
-              const float bv = has_bias ? bwin[c] : 0.0f;
+              float bv = 0.0f;
+              if (kDense) {
+                if (dcol != nullptr && c >= c_lo && c < c_hi)
+                  bv = __ldg(dcol + static_cast<long long>(qloc + c) * in.Lkv);
+              } else if (has_bias) {
+                bv = bwin[c];
+              }
               if (kSoftmax) {
                 const float pp = ex2_approx(fmaf(bv, c_b, fmaf(sv, c_s, -st[c])));
                 pv[e] = pp;
@@ -774,16 +787,16 @@ dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long l
   }
 }
 
-template <int D, int ACT, bool kDBias>
+template <int D, int ACT, bool kDBias, bool kDense>
 cudaError_t launch_main_db(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                            int grid, cudaStream_t s) {
   using C = BwdCfg<D, ACT != GDPA_ACT_SOFTMAX>;
-  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, ACT, kDBias>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, ACT, kDBias, kDense>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  bwd_kernel<D, ACT, kDBias><<<grid, kThreads + (kDBias ? 32 : 0), C::kSmemBytes, s>>>(tq, tk, tv,
-                                                                                     tdo, tdq, p);
+  bwd_kernel<D, ACT, kDBias, kDense><<<grid, kThreads + (kDBias ? 32 : 0), C::kSmemBytes, s>>>(
+      tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
 
@@ -791,8 +804,12 @@ template <int D, int ACT>
 cudaError_t launch_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                         int grid, cudaStream_t s) {
-  return p.dbias != nullptr ? launch_main_db<D, ACT, true>(p, tq, tk, tv, tdo, tdq, grid, s)
-                            : launch_main_db<D, ACT, false>(p, tq, tk, tv, tdo, tdq, grid, s);
+  if (p.bias_dense != nullptr)  // built without a window or a table gradient
+    return (p.window > 0 || p.dbias != nullptr)
+               ? cudaErrorInvalidValue
+               : launch_main_db<D, ACT, false, true>(p, tq, tk, tv, tdo, tdq, grid, s);
+  return p.dbias != nullptr ? launch_main_db<D, ACT, true, false>(p, tq, tk, tv, tdo, tdq, grid, s)
+                            : launch_main_db<D, ACT, false, false>(p, tq, tk, tv, tdo, tdq, grid, s);
 }
 
 template <int D>

@@ -152,7 +152,10 @@ __device__ __forceinline__ SmItem decode_sm(int2 it, const BwdParams& p) {
   return r;
 }
 
-template <int D, bool kBand, bool kDBias>
+// kDense: a dense jagged bias (p.bias_dense) instead of the relative-position
+// table, read from global memory by the activation warps (the warp's lanes
+// are consecutive keys, so each load is one coalesced 128-byte row segment).
+template <int D, bool kBand, bool kDBias, bool kDense>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
               const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
@@ -512,6 +515,11 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       // block's last key bounds the first such query and its first key the last).
       const int full_lo = band_query_begin(kb0 + kKRows - 1, p.causal, p.window);
       const int full_hi = kb0 + kKRows <= in.Lkv ? band_query_end(kb0, p.window, in.Lq) : 0;
+      // dense bias of this key for query i: dcol[i * Lkv] (a key past the sample reads none)
+      const float* dcol = (kDense && jl < in.Lkv)
+                              ? p.bias_dense + p.bias_off[in.b] +
+                                    static_cast<long long>(in.head) * in.Lq * in.Lkv + jl
+                              : nullptr;
       bool abort_now = false;
       for (int t = 0; t < in.nq; ++t, ++g) {
         const uint32_t s = g % C::kQStages;
@@ -550,7 +558,15 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
             for (int q4 = 0; q4 < 16; ++q4) {
               const float4 l4 = st4[(c0 >> 2) + q4];
               float bv[4] = {0.f, 0.f, 0.f, 0.f};
-              if (kBias) {
+              if (kDense) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int c = c0 + 4 * q4 + e;
+                  bv[e] = (dcol != nullptr && c >= c_lo && c < c_hi)
+                              ? __ldg(dcol + static_cast<long long>(qloc + c) * in.Lkv) * kLog2e
+                              : 0.0f;
+                }
+              } else if (kBias) {
                 const float2 b01 = *reinterpret_cast<const float2*>(bwin + c0 + 4 * q4);
                 const float2 b23 = *reinterpret_cast<const float2*>(bwin + c0 + 4 * q4 + 2);
                 bv[0] = b01.x; bv[1] = b01.y; bv[2] = b23.x; bv[3] = b23.y;
@@ -581,9 +597,9 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           using F = std::false_type;
           using T = std::true_type;
           if (full) {
-            if (has_bias) body(F{}, T{}); else body(F{}, F{});
+            if (has_bias || kDense) body(F{}, T{}); else body(F{}, F{});
           } else {
-            if (has_bias) body(T{}, T{}); else body(T{}, F{});
+            if (has_bias || kDense) body(T{}, T{}); else body(T{}, F{});
           }
           tmem_st16(tmem + lane_off + kColS + c0, *reinterpret_cast<uint32_t(*)[16]>(&pp[0]));
           tmem_st16(tmem + lane_off + kColS + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pp[16]));
@@ -804,16 +820,16 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   }
 }
 
-template <int D, bool kBand, bool kDBias>
+template <int D, bool kBand, bool kDBias, bool kDense>
 cudaError_t launch_sm(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                       int grid, cudaStream_t s) {
   using C = SmCfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(bwd_sm_kernel<D, kBand, kDBias>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_sm_kernel<D, kBand, kDBias, kDense>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  bwd_sm_kernel<D, kBand, kDBias><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, tdq, p);
+  bwd_sm_kernel<D, kBand, kDBias, kDense><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
 
@@ -823,9 +839,14 @@ cudaError_t launch_bwd_softmax_main(const BwdParams& p, const CUtensorMap& tq, c
                                     const CUtensorMap& tv, const CUtensorMap& tdo,
                                     const CUtensorMap& tdq, int grid, cudaStream_t s) {
   const bool band = p.window > 0, db = p.dbias != nullptr;
+  if (p.bias_dense != nullptr) {  // the dense bias is built without a window or table gradient
+    if (band || db) return cudaErrorInvalidValue;
+    return p.d == 64 ? launch_sm<64, false, false, true>(p, tq, tk, tv, tdo, tdq, grid, s)
+                     : launch_sm<128, false, false, true>(p, tq, tk, tv, tdo, tdq, grid, s);
+  }
 #define GDPA_SM_LAUNCH(DD, BB, DBB) \
   if (p.d == DD && band == BB && db == DBB) \
-    return launch_sm<DD, BB, DBB>(p, tq, tk, tv, tdo, tdq, grid, s);
+    return launch_sm<DD, BB, DBB, false>(p, tq, tk, tv, tdo, tdq, grid, s);
   GDPA_SM_LAUNCH(64, false, false)
   GDPA_SM_LAUNCH(64, false, true)
   GDPA_SM_LAUNCH(64, true, false)

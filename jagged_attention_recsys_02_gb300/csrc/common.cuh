@@ -128,6 +128,8 @@ struct FwdParams {
   int causal;
   int window;               // 0: no sliding window
   float scale;
+  const float* bias_dense;  // dense jagged bias (nullptr: none); sample b's [H][Lq][Lkv]
+  const int64_t* bias_off;  //   block starts at element bias_off[b]
   __nv_bfloat16* out;
   float* lse;               // nullptr allowed for GDPA activations
   const int2* items;
@@ -146,6 +148,8 @@ struct BwdParams {
   int causal;
   int window;
   float scale;
+  const float* bias_dense;  // dense jagged bias (nullptr: none), as in FwdParams
+  const int64_t* bias_off;
   const __nv_bfloat16* out;
   const float* lse;
   const __nv_bfloat16* dout;
@@ -179,11 +183,13 @@ struct BlockParams {
 };
 
 // Host-side launchers (defined in the kernel translation units).
+// bias_off (optional): element offsets of a dense jagged bias, checked against
+// H * Lq_b * Lkv_b (a mismatch is reported as GDPA_ERR_BAD_OFFSETS).
 cudaError_t launch_build_worklist(const int32_t* outer_off, const int32_t* inner_off, int B, int H,
                                   int64_t T_outer, int64_t T_inner, int causal, int window,
                                   int mode,
                                   int2* items, int* n_items, int* ticket, int* status,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, const int64_t* bias_off = nullptr);
 cudaError_t launch_fwd(const FwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, int grid, cudaStream_t stream);
 int fwd_smem_bytes(int d);

@@ -153,7 +153,9 @@ __device__ __forceinline__ ItemInfo decode_item(int2 it, const FwdParams& p) {
   return r;
 }
 
-template <int D, int ACT, bool kBand>
+// kDense: a dense jagged bias (p.bias_dense) instead of the relative-position
+// table; its rows are read from global memory by the activation warps.
+template <int D, int ACT, bool kBand, bool kDense>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
            const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
@@ -475,11 +477,29 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       const int col_lim = kBand ? band_key_end(r, p.causal, p.window, in.Lkv)
                                 : (p.causal ? min(in.Lkv, r + 1) : in.Lkv);
       const bool has_bias = p.bias_table != nullptr;
+      // dense bias row of this query: one value per key (none past the sample)
+      const float* drow = nullptr;
+      if (kDense && row_valid)
+        drow = p.bias_dense + p.bias_off[in.b] +
+               (static_cast<long long>(in.head) * in.Lq + r) * in.Lkv;
       float m = -INFINITY;  // running max (log2 units), possibly stale
       float l = 0.0f;       // running sum relative to m
       bool abort_now = false;
+      // dense bias: the row segment of key tile j is pulled into L2 one tile
+      // ahead (4 lines of 32 values; only columns the row sees)
+      auto prefetch_dense = [&](int jt) {
+        if (kDense && drow != nullptr && jt < j_hi) {
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int c = jt * kKvRows + 32 * k4;
+            if (c < col_lim) prefetch_l2(drow + c);
+          }
+        }
+      };
+      prefetch_dense(j_lo);
       for (int j = j_lo; j < j_hi; ++j) {
         const uint32_t gj = g_item + (j - in.jb);
+        prefetch_dense(j + 1);
         bool okw = mbar_wait(bar(C::kSFull + half), tcount & 1u, abort_flag);
         // the value-tile stage also carries this tile's bias window
         if (has_bias)
@@ -493,7 +513,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         // Scores need only the scale when no row of the warp needs a mask and there
         // is no bias.  Decided per warp: the tcgen05.ld below is .sync.aligned, so
         // the lanes of a warp must not split between the two paths.
-        const bool plain = !has_bias && __all_sync(0xffffffffu, !need_mask);
+        const bool plain = !has_bias && !kDense && __all_sync(0xffffffffu, !need_mask);
         // bwin[cc] = bias(row, tile column cc) (times log2e for softmax): the
         // window copy shifted by (row + 1) % 2 holds this row's 128 entries in
         // increasing column order from an 8-byte aligned position.
@@ -503,12 +523,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         // x = score * c_s + bias, with masked entries set to `fill` (pairs of
         // columns per packed fp32 instruction)
         auto load_x = [&](int chunk, float fill, float (&x)[32]) {
+          float db[32];  // dense bias of the chunk's visible columns (times log2e for softmax)
+          if (kDense) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int c = c0 + chunk * 32 + i;
+              db[i] = (drow != nullptr && c < col_lim) ? __ldg(drow + c) * (kSoftmax ? kLog2e : 1.0f)
+                                                        : 0.0f;
+            }
+          }
           uint32_t sr[32];
           tmem_ld32_nc(t_s + chunk * 32, sr);  // lets the bias loads overlap the TMEM load
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (has_bias) {
+            if (kDense) {
+              b4 = make_float4(db[4 * q4], db[4 * q4 + 1], db[4 * q4 + 2], db[4 * q4 + 3]);
+            } else if (has_bias) {
               const float2 b01 = *reinterpret_cast<const float2*>(bwin + chunk * 32 + 4 * q4);
               const float2 b23 = *reinterpret_cast<const float2*>(bwin + chunk * 32 + 4 * q4 + 2);
               b4 = make_float4(b01.x, b01.y, b23.x, b23.y);
@@ -670,29 +701,30 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
   }
 }
 
-template <int D, int ACT, bool kBand>
+template <int D, int ACT, bool kBand, bool kDense>
 cudaError_t launch_one(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, int grid, cudaStream_t stream) {
   const int smem = FwdCfg<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, ACT, kBand>,
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, ACT, kBand, kDense>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  fwd_kernel<D, ACT, kBand><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  fwd_kernel<D, ACT, kBand, kDense><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
-template <int D, bool kBand>
+template <int D, bool kBand, bool kDense>
 cudaError_t launch_d(const FwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, int grid, cudaStream_t stream) {
   switch (act) {
     case GDPA_ACT_SOFTMAX:
-      return launch_one<D, GDPA_ACT_SOFTMAX, kBand>(p, tq, tk, tv, grid, stream);
-    case GDPA_ACT_SILU: return launch_one<D, GDPA_ACT_SILU, kBand>(p, tq, tk, tv, grid, stream);
+      return launch_one<D, GDPA_ACT_SOFTMAX, kBand, kDense>(p, tq, tk, tv, grid, stream);
+    case GDPA_ACT_SILU:
+      return launch_one<D, GDPA_ACT_SILU, kBand, kDense>(p, tq, tk, tv, grid, stream);
     case GDPA_ACT_GELU_TANH:
-      return launch_one<D, GDPA_ACT_GELU_TANH, kBand>(p, tq, tk, tv, grid, stream);
+      return launch_one<D, GDPA_ACT_GELU_TANH, kBand, kDense>(p, tq, tk, tv, grid, stream);
     case GDPA_ACT_GELU_ERF:
-      return launch_one<D, GDPA_ACT_GELU_ERF, kBand>(p, tq, tk, tv, grid, stream);
-    default: return launch_one<D, GDPA_ACT_IDENTITY, kBand>(p, tq, tk, tv, grid, stream);
+      return launch_one<D, GDPA_ACT_GELU_ERF, kBand, kDense>(p, tq, tk, tv, grid, stream);
+    default: return launch_one<D, GDPA_ACT_IDENTITY, kBand, kDense>(p, tq, tk, tv, grid, stream);
   }
 }
 
@@ -703,11 +735,16 @@ int fwd_smem_bytes(int d) { return d == 64 ? FwdCfg<64>::kSmemBytes : FwdCfg<128
 cudaError_t launch_fwd(const FwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, int grid, cudaStream_t stream) {
   const bool band = p.window > 0;
+  if (p.bias_dense != nullptr) {  // the dense bias is built without a window
+    if (band) return cudaErrorInvalidValue;
+    return p.d == 64 ? launch_d<64, false, true>(p, act, tq, tk, tv, grid, stream)
+                     : launch_d<128, false, true>(p, act, tq, tk, tv, grid, stream);
+  }
   if (p.d == 64)
-    return band ? launch_d<64, true>(p, act, tq, tk, tv, grid, stream)
-                : launch_d<64, false>(p, act, tq, tk, tv, grid, stream);
-  return band ? launch_d<128, true>(p, act, tq, tk, tv, grid, stream)
-              : launch_d<128, false>(p, act, tq, tk, tv, grid, stream);
+    return band ? launch_d<64, true, false>(p, act, tq, tk, tv, grid, stream)
+                : launch_d<64, false, false>(p, act, tq, tk, tv, grid, stream);
+  return band ? launch_d<128, true, false>(p, act, tq, tk, tv, grid, stream)
+              : launch_d<128, false, false>(p, act, tq, tk, tv, grid, stream);
 }
 
 }  // namespace gdpa

@@ -55,7 +55,8 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
                       int B, int H, long long T_outer, long long T_inner, int causal, int window,
                       int mode,
                       int2* __restrict__ items, int* __restrict__ n_items,
-                      int* __restrict__ ticket, int* __restrict__ status) {
+                      int* __restrict__ ticket, int* __restrict__ status,
+                      const int64_t* __restrict__ bias_off) {
   __shared__ int hist[kCostBuckets];
   __shared__ int base[kCostBuckets];
   __shared__ int warp_tot[kThreads / 32];
@@ -65,13 +66,15 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
   for (int i = tid; i < kCostBuckets; i += kThreads) hist[i] = 0;
   if (tid == 0) {
     bad = (outer_off[0] != 0 || inner_off[0] != 0 || outer_off[B] != T_outer ||
-           inner_off[B] != T_inner) ? 1 : 0;
+           inner_off[B] != T_inner || (bias_off != nullptr && bias_off[0] != 0)) ? 1 : 0;
   }
   __syncthreads();
   for (int b = tid; b < B; b += kThreads) {
     const int Lo = outer_off[b + 1] - outer_off[b];
     const int Li = inner_off[b + 1] - inner_off[b];
-    if (Lo < 0 || Li < 0 || ((causal || window > 0) && Lo != Li)) {
+    if (Lo < 0 || Li < 0 || ((causal || window > 0) && Lo != Li) ||
+        (bias_off != nullptr &&
+         bias_off[b + 1] - bias_off[b] != static_cast<int64_t>(H) * Lo * Li)) {
       bad = 1;
       continue;
     }
@@ -141,10 +144,10 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
 cudaError_t launch_build_worklist(const int32_t* outer_off, const int32_t* inner_off, int B, int H,
                                   int64_t T_outer, int64_t T_inner, int causal, int window,
                                   int mode, int2* items, int* n_items, int* ticket, int* status,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, const int64_t* bias_off) {
   build_worklist_kernel<<<1, kThreads, 0, stream>>>(outer_off, inner_off, B, H, T_outer, T_inner,
                                                     causal, window, mode, items, n_items, ticket,
-                                                    status);
+                                                    status, bias_off);
   return cudaGetLastError();
 }
 

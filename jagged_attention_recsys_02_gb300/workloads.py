@@ -26,6 +26,10 @@ sparsity 0.5; these workloads stand in for that traffic:
                      (same paragraph): B=64, L~U[1,16384], H=4, d=128,
                      softmax, 64-token blocks, relative-position bias table
                      [H, 127] ~ N(0, 0.02)
+  jfa_causal_dense   jfa_causal_relpos's lengths and settings with a dense
+                     jagged bias instead of the table: one fp32 value
+                     ~ N(0, 0.02) per (head, query, key) of each sample
+                     (the JFA paragraph's custom biases in general form)
 """
 from __future__ import annotations
 
@@ -38,7 +42,7 @@ import torch
 ACTS = {"softmax": 0, "silu": 1, "gelu_tanh": 2, "identity": 3, "gelu_erf": 4}
 
 CONFIG_NAMES = ("tiny_silu", "jfa_causal_relpos", "gdpa_cross_gelu", "gdpa_pma_silu", "heavy_tail")
-EXTRA_NAMES = ("swa_causal_relpos", "block_relpos")
+EXTRA_NAMES = ("swa_causal_relpos", "block_relpos", "jfa_causal_dense")
 
 
 @dataclass
@@ -55,6 +59,7 @@ class Workload:
     pma_seeds: int = 0        # >0: queries are this many seeds shared by all samples
     window: int = 0           # >0: sliding window, pairs with |i - j| < window
     block: int = 0            # >0: block-aligned attention in blocks of this many tokens
+    dense: bool = False       # dense jagged bias [sum_b H*Lq_b*Lkv_b] instead of a table
     scale: float = 0.0
     extra: dict = field(default_factory=dict)
 
@@ -107,9 +112,11 @@ def make_workload(name: str, seed: int = 0, act: str | None = None) -> Workload:
     if name == "tiny_silu":
         L = np.array([1, 7, 33, 64], dtype=np.int64)
         w = Workload(name, 4, 2, 64, "silu", False, L.copy(), L.copy())
-    elif name == "jfa_causal_relpos":
+    elif name in ("jfa_causal_relpos", "jfa_causal_dense"):
         L = rng.integers(1, 4096, size=32, endpoint=True).astype(np.int64)
-        w = Workload(name, 32, 4, 128, "softmax", True, L.copy(), L.copy(), max_rel=4096)
+        dense = name == "jfa_causal_dense"
+        w = Workload(name, 32, 4, 128, "softmax", True, L.copy(), L.copy(),
+                     max_rel=0 if dense else 4096, dense=dense)
     elif name == "gdpa_cross_gelu":
         lq = rng.integers(64, 8192, size=256, endpoint=True).astype(np.int64)
         lkv = rng.integers(32, 256, size=256, endpoint=True).astype(np.int64)
@@ -144,7 +151,7 @@ def first_samples(w: Workload, n: int) -> Workload:
     n = max(1, min(int(n), w.B))
     return Workload(f"{w.name}[:{n}]", n, w.H, w.d, w.act, w.causal, w.lq[:n].copy(),
                     w.lkv[:n].copy(), max_rel=w.max_rel, pma_seeds=w.pma_seeds, window=w.window,
-                    block=w.block, scale=w.scale, extra=dict(w.extra))
+                    block=w.block, dense=w.dense, scale=w.scale, extra=dict(w.extra))
 
 
 def custom_workload(lq, lkv, H, d, act="softmax", causal=False, max_rel=0, name="custom",
@@ -179,6 +186,12 @@ def make_tensors(w: Workload, device="cpu", seed: int = 0, with_dout: bool = Tru
     if w.max_rel:
         bias = (torch.randn(H, 2 * w.max_rel - 1, generator=g, device=device,
                             dtype=torch.float32) * 0.02)
+    elif w.dense:
+        # sample b's [H][Lq_b][Lkv_b] block starts at element off[b]
+        off = np.zeros(w.B + 1, dtype=np.int64)
+        off[1:] = np.cumsum(H * w.lq.astype(np.int64) * w.lkv.astype(np.int64))
+        vals = torch.randn(int(off[-1]), generator=g, device=device, dtype=torch.float32) * 0.02
+        bias = (vals, torch.from_numpy(off).to(device))
     qo, ko = w.offsets()
     return dict(q=q, k=k, v=v, dout=dout, bias=bias,
                 qo=torch.from_numpy(qo).to(device), ko=torch.from_numpy(ko).to(device))

@@ -199,3 +199,26 @@ def test_mxfp8_backward_workspace_size(lib):
     assert s(B, H, d, Tq, Tkv) >= codes + Tq * H * d * 4 + Tq * H * 4
     assert s(B, H, d, Tq, Tkv) < codes * 1.3 + Tq * H * d * 4 + (1 << 20)
     assert s(-1, H, d, 1, 1) == 0 and s(B, 0, d, 1, 1) == 0 and s(B, H, 96, 1, 1) == 0
+
+
+def test_dense_bias_rejections_on_host(lib):
+    """A dense bias needs its values and its int64 offsets (4- and 8-byte
+    aligned); it has no window, no table gradient, no block or MXFP8 path."""
+    D = binding.BIAS_DENSE
+    dense = lambda table=FAKE, off=FAKE + 64: ctypes.byref(binding.gdpa_bias(D, table, 0, off))
+    assert _fwd(lib, bias=dense(off=None)) == INVALID
+    assert _fwd(lib, bias=dense(table=None)) == INVALID
+    assert _fwd(lib, bias=dense(table=FAKE + 2)) == INVALID
+    assert _fwd(lib, bias=dense(off=FAKE + 4)) == INVALID
+    assert _bwd(lib, bias=dense(off=None)) == INVALID
+    assert _fwd(lib, bias=dense(), ws=None) == WORKSPACE      # valid bias: the next check fires
+    assert lib.gdpa_fwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense(), 0, 0, 4,
+                               0.125, FAKE, FAKE, FAKE, 1 << 20, None) == UNSUPPORTED
+    assert lib.gdpa_bwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense(), 0, 0, 0,
+                               0.125, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20,
+                               None) == INVALID              # a table gradient needs a table
+    assert lib.gdpa_block_fwd(FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, dense(), 0, 0, 0.125, FAKE,
+                              FAKE, 1 << 20, None) == UNSUPPORTED
+    assert lib.gdpa_fwd_mxfp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 10, 10,
+                              dense(), 0, 0, 0.125, FAKE, FAKE, FAKE, 1 << 20, None) == UNSUPPORTED
+    assert _bwd_mx(lib, bias=dense()) == UNSUPPORTED

@@ -1,0 +1,104 @@
+"""GPU parity of the dense jagged bias (one fp32 value per head, query and key
+of each sample) against the oracle: forward for every activation, the softmax
+and GDPA backward, causal and not, ragged lengths, malformed bias offsets."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_common import (BWD_TOL, FWD_TOL, assert_close, check_guards, guarded, offsets,
+                        rand_bf16, to_np)
+from jagged_attention_recsys_02_gb300 import binding
+from jagged_attention_recsys_02_gb300.workloads import ACTS
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _case(lq, lkv, H, d, act, causal, seed, std=1.0):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    q = rand_bf16((sum(lq), H, d), g, DEV)
+    k = rand_bf16((sum(lkv), H, d), g, DEV)
+    v = rand_bf16((sum(lkv), H, d), g, DEV)
+    do = rand_bf16((sum(lq), H, d), g, DEV)
+    qo_np, ko_np = offsets(lq), offsets(lkv)
+    off_np = oracle.dense_bias_offsets(qo_np, ko_np, H)
+    vals = torch.randn(int(off_np[-1]), generator=g, device=DEV) * std
+    qo, ko = torch.from_numpy(qo_np).to(DEV), torch.from_numpy(ko_np).to(DEV)
+    off = torch.from_numpy(off_np).to(DEV)
+    return dict(q=q, k=k, v=v, do=do, qo=qo, ko=ko, qo_np=qo_np, ko_np=ko_np, vals=vals, off=off,
+                act=ACTS[act], causal=causal, scale=1.0 / np.sqrt(d))
+
+
+def _fwd(c):
+    Tq, H, d = c["q"].shape
+    buf, out = guarded(Tq, H, d, DEV)
+    lse = torch.full((H, Tq), float("nan"), device=DEV) if c["act"] == 0 else None
+    binding.gdpa_fwd(c["q"], c["qo"], c["k"], c["v"], c["ko"], act=c["act"], causal=c["causal"],
+                     scale=c["scale"], bias=(c["vals"], c["off"]), out=out, lse=lse)
+    assert binding.device_status() == 0
+    check_guards(buf)
+    return out, lse
+
+
+def _ref_kw(c):
+    return dict(act=c["act"], causal=c["causal"], scale=c["scale"],
+                dense_bias=c["vals"].double().cpu().numpy())
+
+
+CASES = [
+    ([1, 31, 64, 65, 200, 0, 300, 129], [7, 32, 1, 96, 128, 5, 191, 300], False),
+    ([1, 64, 65, 128, 129, 300, 0, 257], None, True),
+]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh", "gelu_erf"])
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_dense_bias_forward(case, act, d):
+    lq, lkv, causal = CASES[case]
+    c = _case(lq, lkv or lq, 2, d, act, causal, seed=10 + case)
+    out, lse = _fwd(c)
+    ro, rl = oracle.fwd(to_np(c["q"]), c["qo_np"], to_np(c["k"]), to_np(c["v"]), c["ko_np"],
+                        **_ref_kw(c))
+    assert_close(to_np(out), ro, FWD_TOL, f"dense {act} out")
+    if lse is not None:
+        assert_close(lse.cpu().double().numpy(), rl, FWD_TOL, f"dense {act} lse")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh"])
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_dense_bias_backward(case, act, d):
+    lq, lkv, causal = CASES[case]
+    c = _case(lq, lkv or lq, 2, d, act, causal, seed=20 + case)
+    out, lse = _fwd(c)
+    Tq, H, _ = c["q"].shape
+    Tkv = c["k"].shape[0]
+    bq, dq = guarded(Tq, H, d, DEV)
+    bk, dk = guarded(Tkv, H, d, DEV)
+    bv, dv = guarded(Tkv, H, d, DEV)
+    binding.gdpa_bwd(c["q"], c["qo"], c["k"], c["v"], c["ko"], out, lse, c["do"], act=c["act"],
+                     causal=c["causal"], scale=c["scale"], bias=(c["vals"], c["off"]), dq=dq, dk=dk,
+                     dv=dv)
+    assert binding.device_status() == 0
+    for b_ in (bq, bk, bv):
+        check_guards(b_)
+    ref = oracle.bwd(to_np(c["q"]), c["qo_np"], to_np(c["k"]), to_np(c["v"]), c["ko_np"],
+                     to_np(c["do"]), **_ref_kw(c))
+    for name, got, r in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
+        assert_close(to_np(got), r, BWD_TOL, f"dense {act} {name}")
+
+
+def test_dense_bias_bad_offsets_are_reported():
+    """Offsets that do not step by H * Lq * Lkv are reported through the device
+    status word, and nothing is computed."""
+    c = _case([5, 40], [9, 3], 2, 64, "softmax", False, seed=3)
+    bad = c["off"].clone()
+    bad[1] += 1
+    out = torch.zeros_like(c["q"])
+    lse = torch.zeros((2, c["q"].shape[0]), device=DEV)
+    binding.gdpa_fwd(c["q"], c["qo"], c["k"], c["v"], c["ko"], act=0, scale=c["scale"],
+                     bias=(c["vals"], bad), out=out, lse=lse)
+    assert binding.device_status() == 6   # GDPA_ERR_BAD_OFFSETS

@@ -194,6 +194,26 @@ gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k,
                            int causal, float scale, float rope_base, const void* dout, void* dq,
                            void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream);
 
+/* gdpa_bwd_window with the rotary-embedding backward fused into the epilogue
+ * ("GEM Training ..." SWA / block paragraph: RoPE backward in the attention
+ * epilogue, gradients kept in fp32).  q and k are taken as already
+ * rotary-embedded in the rotate-half form (channels c and c + d/2 rotated by
+ * pos * rope_base^(-2c/d), pos = the token's position in its sample, queries
+ * and keys each by their own offsets); dq and dk are returned for the
+ * un-rotated q and k: the transposed rotation is applied to the fp32
+ * gradients before rounding (dK in the kernel's epilogue, dQ in the
+ * accumulator's conversion).  rope_base = 0: no rotary embedding (this is
+ * gdpa_bwd_window); negative, infinite or NaN: GDPA_ERR_INVALID_ARG; with a
+ * bias-table gradient or a dense bias: GDPA_ERR_UNSUPPORTED.  Every
+ * other argument, output and error is that of gdpa_bwd_window; not available
+ * for the MXFP8 backward. */
+gdpa_status gdpa_bwd_rope(const void* q, const int32_t* q_offsets, const void* k, const void* v,
+                          const int32_t* kv_offsets, int B, int H, int d, int64_t Tq,
+                          int64_t Tkv, const gdpa_bias* bias, int act, int causal, int window,
+                          float scale, float rope_base, const void* out, const float* lse,
+                          const void* dout, void* dq, void* dk, void* dv, float* dbias,
+                          void* workspace, size_t ws_bytes, void* stream);
+
 /* MXFP8 block quantisation (OCP Microscaling Formats v1.0; "GEM Training ..."
  * low-precision paragraph: attention with MXFP8 block-scaled MMA).  Elements
  * become E4M3 codes (round to nearest even, saturated at +-448); each block of

@@ -32,7 +32,8 @@ EXPORTS = ("gdpa_fwd_workspace_size", "gdpa_fwd", "gdpa_bwd_workspace_size", "gd
            "gdpa_mxfp8_scale_bytes", "gdpa_quantize_mxfp8", "gdpa_fwd_mxfp8",
            "gdpa_fwd_window", "gdpa_bwd_window", "gdpa_fwd_mxfp8_window",
            "gdpa_block_workspace_size", "gdpa_block_fwd", "gdpa_block_bwd",
-           "gdpa_bwd_mxfp8_workspace_size", "gdpa_bwd_mxfp8", "gdpa_bwd_mxfp8_window")
+           "gdpa_bwd_mxfp8_workspace_size", "gdpa_bwd_mxfp8", "gdpa_bwd_mxfp8_window",
+           "gdpa_bwd_rope")
 MX_ALONG_CHANNELS, MX_ALONG_TOKENS = 0, 1
 
 
@@ -87,6 +88,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                         ctypes.POINTER(gdpa_bias), I, I, I, F, vp, vp, vp, vp, vp,
                                         vp, vp, vp, sz, vp]
         lib.gdpa_bwd_window.restype = I
+        lib.gdpa_bwd_rope.argtypes = [vp, vp, vp, vp, vp, I, I, I, i64, i64,
+                                      ctypes.POINTER(gdpa_bias), I, I, I, F, F, vp, vp, vp, vp, vp,
+                                      vp, vp, vp, sz, vp]
+        lib.gdpa_bwd_rope.restype = I
         lib.gdpa_get_device_status.argtypes = [vp]
         lib.gdpa_get_device_status.restype = I
         lib.gdpa_status_string.argtypes = [I]
@@ -199,10 +204,11 @@ def gdpa_fwd(q, q_offsets, k, v, kv_offsets, *, act, causal=False, scale, bias=N
 
 def gdpa_bwd(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, act, causal=False, scale,
              bias=None, max_rel=0, window=0, dq=None, dk=None, dv=None, dbias=None,
-             workspace=None, stream=None):
+             rope_base=0.0, workspace=None, stream=None):
     """Backward pass through the C ABI (gdpa_bwd, or gdpa_bwd_window when
     window > 0 or a bias-table gradient `dbias` [H, 2*max_rel-1] fp32 is given,
-    which is added to).  Returns (dq, dk, dv)."""
+    which is added to; gdpa_bwd_rope when rope_base > 0, dq and dk then going
+    back through the rotary embedding).  Returns (dq, dk, dv)."""
     lib = load()
     Tq, H, d = q.shape
     Tkv = k.shape[0]
@@ -217,11 +223,16 @@ def gdpa_bwd(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, act, causal=Fals
             _bias(bias, max_rel), _act(act), int(bool(causal)))
     tail = (float(scale), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv))
     ws = (_ptr(workspace), workspace.numel(), _stream(stream))
-    if window or dbias is not None:
+    if rope_base:
+        rc = lib.gdpa_bwd_rope(*head, int(window), float(scale), float(rope_base), *tail[1:],
+                               _ptr(dbias), *ws)
+        _check(rc, "gdpa_bwd_rope")
+    elif window or dbias is not None:
         rc = lib.gdpa_bwd_window(*head, int(window), *tail, _ptr(dbias), *ws)
+        _check(rc, "gdpa_bwd_window")
     else:
         rc = lib.gdpa_bwd(*head, *tail, *ws)
-    _check(rc, "gdpa_bwd_window" if (window or dbias is not None) else "gdpa_bwd")
+        _check(rc, "gdpa_bwd")
     return dq, dk, dv
 
 

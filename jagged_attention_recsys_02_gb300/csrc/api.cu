@@ -292,7 +292,20 @@ gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void*
                             int window, float scale, const void* out, const float* lse,
                             const void* dout, void* dq, void* dk, void* dv, float* dbias,
                             void* workspace, size_t ws_bytes, void* stream) {
+  return gdpa_bwd_rope(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act, causal, window,
+                       scale, 0.0f, out, lse, dout, dq, dk, dv, dbias, workspace, ws_bytes, stream);
+}
+
+gdpa_status gdpa_bwd_rope(const void* q, const int32_t* q_offsets, const void* k, const void* v,
+                          const int32_t* kv_offsets, int B, int H, int d, int64_t Tq,
+                          int64_t Tkv, const gdpa_bias* bias, int act, int causal, int window,
+                          float scale, float rope_base, const void* out, const float* lse,
+                          const void* dout, void* dq, void* dk, void* dv, float* dbias,
+                          void* workspace, size_t ws_bytes, void* stream) {
   t_launches = 0;
+  if (!(rope_base >= 0.0f) || rope_base == INFINITY) return GDPA_ERR_INVALID_ARG;  // NaN too
+  // the fused rotary backward is built without a table gradient or a dense bias
+  if (rope_base > 0.0f && (dbias != nullptr || is_dense(bias))) return GDPA_ERR_UNSUPPORTED;
   gdpa_status st = check_common(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act,
                                 causal, window);
   if (st != GDPA_OK) return st;
@@ -376,6 +389,7 @@ gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void*
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.dbias = dbias;
+  p.rope_base = rope_base;
   p.dq_acc = dq_acc;
   p.delta = delta;
   p.items = items;
@@ -392,8 +406,11 @@ gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void*
   t_launches += launches;
   if (e != cudaSuccess) return GDPA_ERR_CUDA;
   if (Tq > 0) {
-    if (launch_dq_convert(dq_acc, dq, static_cast<long long>(Tq) * H * d, scale, s) != cudaSuccess)
-      return GDPA_ERR_CUDA;
+    const cudaError_t ce =
+        rope_base > 0.0f
+            ? launch_dq_convert_rope(dq_acc, dq, q_offsets, B, Tq, H, d, scale, rope_base, s)
+            : launch_dq_convert(dq_acc, dq, static_cast<long long>(Tq) * H * d, scale, s);
+    if (ce != cudaSuccess) return GDPA_ERR_CUDA;
     ++t_launches;
   }
   return GDPA_OK;

@@ -690,6 +690,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
           const uint32_t col = which ? kColDK : kColDV;
           const float mul = which ? p.scale : 1.0f;
           __nv_bfloat16* dst = (which ? p.dk : p.dv) + grow;
+          if (which == 1 && p.rope_base > 0.0f) {  // dK back through the rotary embedding
+            rope_bwd_row<D>(tmem + lane_off + col, mul, jl, -2.0f * log2f(p.rope_base) / D, dst,
+                            row_ok);
+            continue;
+          }
 #pragma unroll 1
           for (int chunk = 0; chunk < D / 32; ++chunk) {
             uint32_t o[32];
@@ -787,6 +792,44 @@ dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long l
   }
 }
 
+// dq = bf16 of the rotary backward of scale * acc: each thread takes channels
+// c..c+3 of one (token, head) row and their partners c + d/2 .. c + d/2 + 3,
+// the token's position found by a binary search over the sample offsets.
+__global__ void __launch_bounds__(256)
+dq_convert_rope_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
+                       const int32_t* __restrict__ offsets, int B, long long T, int H, int d,
+                       float scale, float rope_k) {
+  const int per_row = d / 8;
+  const long long units = T * H * per_row;
+  for (long long u = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; u < units;
+       u += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = u / per_row;          // (token, head) row
+    const int c = 4 * static_cast<int>(u % per_row);
+    const long long t = row / H;
+    int lo = 0, hi = B - 1;  // last sample starting at or before t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (offsets[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int pos = static_cast<int>(t - offsets[lo]);
+    const float4 g1 = *reinterpret_cast<const float4*>(acc + row * d + c);
+    const float4 g2 = *reinterpret_cast<const float4*>(acc + row * d + d / 2 + c);
+    const float a1[4] = {g1.x * scale, g1.y * scale, g1.z * scale, g1.w * scale};
+    const float a2[4] = {g2.x * scale, g2.y * scale, g2.z * scale, g2.w * scale};
+    float r1[4], r2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float sn, cs;
+      sincosf(static_cast<float>(pos) * exp2f(static_cast<float>(c + e) * rope_k), &sn, &cs);
+      r1[e] = fmaf(a1[e], cs, a2[e] * sn);
+      r2[e] = fmaf(a2[e], cs, -a1[e] * sn);
+    }
+    *reinterpret_cast<uint2*>(dq + row * d + c) = make_uint2(pack_bf16x2(r1[0], r1[1]), pack_bf16x2(r1[2], r1[3]));
+    *reinterpret_cast<uint2*>(dq + row * d + d / 2 + c) =
+        make_uint2(pack_bf16x2(r2[0], r2[1]), pack_bf16x2(r2[2], r2[3]));
+  }
+}
+
 template <int D, int ACT, bool kDBias, bool kDense>
 cudaError_t launch_main_db(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
@@ -858,6 +901,17 @@ cudaError_t launch_bwd_preprocess(const BwdParams& p, bool softmax, cudaStream_t
   else
     bwd_preprocess_kernel<128><<<pre_blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
                                                                p.Tq, p.H, softmax ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert_rope(const float* acc, void* dq, const int32_t* offsets, int B,
+                                   long long T, int H, int d, float scale, float rope_base,
+                                   cudaStream_t stream) {
+  const long long units = T * H * (d / 8);  // 4 channels of the first half and their partners
+  const int blocks = static_cast<int>(units / 256 + 1 < 8192 ? units / 256 + 1 : 8192);
+  dq_convert_rope_kernel<<<blocks, 256, 0, stream>>>(acc, static_cast<__nv_bfloat16*>(dq), offsets,
+                                                     B, T, H, d, scale,
+                                                     -2.0f * log2f(rope_base) / d);
   return cudaGetLastError();
 }
 

@@ -155,7 +155,9 @@ __device__ __forceinline__ SmItem decode_sm(int2 it, const BwdParams& p) {
 // kDense: a dense jagged bias (p.bias_dense) instead of the relative-position
 // table, read from global memory by the activation warps (the warp's lanes
 // are consecutive keys, so each load is one coalesced 128-byte row segment).
-template <int D, bool kBand, bool kDBias, bool kDense>
+// kRope: dK (here) and dQ (in the accumulator's conversion) go back through
+// the rotary embedding.
+template <int D, bool kBand, bool kDBias, bool kDense, bool kRope>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
               const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
@@ -746,6 +748,11 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           const uint32_t col = which ? kColDK : kColDV;
           const float mul = which ? p.scale : 1.0f;
           __nv_bfloat16* dst = (which ? p.dk : p.dv) + grow;
+          if (kRope && which == 1) {  // dK back through the rotary embedding
+            rope_bwd_row<D>(tmem + lane_off + col, mul, jl, -2.0f * log2f(p.rope_base) / D, dst,
+                            row_ok);
+            continue;
+          }
 #pragma unroll 1
           for (int chunk = 0; chunk < D / 32; ++chunk) {
             uint32_t o[32];
@@ -820,16 +827,17 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   }
 }
 
-template <int D, bool kBand, bool kDBias, bool kDense>
+template <int D, bool kBand, bool kDBias, bool kDense, bool kRope = false>
 cudaError_t launch_sm(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                       int grid, cudaStream_t s) {
   using C = SmCfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(bwd_sm_kernel<D, kBand, kDBias, kDense>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_sm_kernel<D, kBand, kDBias, kDense, kRope>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  bwd_sm_kernel<D, kBand, kDBias, kDense><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, tdq, p);
+  bwd_sm_kernel<D, kBand, kDBias, kDense, kRope><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo,
+                                                                                   tdq, p);
   return cudaGetLastError();
 }
 
@@ -839,6 +847,14 @@ cudaError_t launch_bwd_softmax_main(const BwdParams& p, const CUtensorMap& tq, c
                                     const CUtensorMap& tv, const CUtensorMap& tdo,
                                     const CUtensorMap& tdq, int grid, cudaStream_t s) {
   const bool band = p.window > 0, db = p.dbias != nullptr;
+  if (p.rope_base > 0.0f) {  // built without a table gradient or a dense bias
+    if (db || p.bias_dense != nullptr) return cudaErrorInvalidValue;
+    if (p.d == 64)
+      return band ? launch_sm<64, true, false, false, true>(p, tq, tk, tv, tdo, tdq, grid, s)
+                  : launch_sm<64, false, false, false, true>(p, tq, tk, tv, tdo, tdq, grid, s);
+    return band ? launch_sm<128, true, false, false, true>(p, tq, tk, tv, tdo, tdq, grid, s)
+                : launch_sm<128, false, false, false, true>(p, tq, tk, tv, tdo, tdq, grid, s);
+  }
   if (p.bias_dense != nullptr) {  // the dense bias is built without a window or table gradient
     if (band || db) return cudaErrorInvalidValue;
     return p.d == 64 ? launch_sm<64, false, false, true>(p, tq, tk, tv, tdo, tdq, grid, s)

@@ -113,6 +113,49 @@ __device__ __forceinline__ void act_and_grad(float x, float& a, float& g) {
   }
 }
 
+// Rotary-embedding backward of one row ("GEM Training ..." SWA / block
+// paragraph: the RoPE backward fused into the attention epilogue, gradients
+// kept in fp32).  The row's D fp32 gradient values sit in TMEM columns
+// taddr..taddr+D; scaled by `mul`, each channel pair (c, c + D/2) is rotated
+// by -pos * theta_c with theta_c = base^(-2c/D) = exp2(c * rope_k), then
+// stored as bf16 to dst (when `store`; every lane must call this: the TMEM
+// loads are warp-collective).
+template <int D>
+__device__ __forceinline__ void rope_bwd_row(uint32_t taddr, float mul, int pos, float rope_k,
+                                             __nv_bfloat16* dst, bool store) {
+#pragma unroll 1
+  for (int j = 0; j < D / 64; ++j) {
+    uint32_t v1[32], v2[32];
+    ptx::tmem_ld32(taddr + 32 * j, v1);
+    ptx::tmem_ld32(taddr + 32 * j + D / 2, v2);
+    uint32_t pa[16], pb[16];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      float a[2], b[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float g1 = __uint_as_float(v1[i + e]) * mul;
+        const float g2 = __uint_as_float(v2[i + e]) * mul;
+        float sn, cs;
+        sincosf(static_cast<float>(pos) * exp2f(static_cast<float>(32 * j + i + e) * rope_k), &sn, &cs);
+        a[e] = fmaf(g1, cs, g2 * sn);
+        b[e] = fmaf(g2, cs, -g1 * sn);
+      }
+      pa[i / 2] = ptx::pack_bf16x2(a[0], a[1]);
+      pb[i / 2] = ptx::pack_bf16x2(b[0], b[1]);
+    }
+    if (store) {
+      uint4* d1 = reinterpret_cast<uint4*>(dst + 32 * j);
+      uint4* d2 = reinterpret_cast<uint4*>(dst + D / 2 + 32 * j);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        d1[v] = make_uint4(pa[4 * v], pa[4 * v + 1], pa[4 * v + 2], pa[4 * v + 3]);
+        d2[v] = make_uint4(pb[4 * v], pb[4 * v + 1], pb[4 * v + 2], pb[4 * v + 3]);
+      }
+    }
+  }
+}
+
 // Device status word values (same numbering as gdpa_status).
 __device__ __forceinline__ void set_status(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
@@ -156,6 +199,7 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   float* dbias;             // fp32 [H][2*max_rel-1], added to (nullptr: not computed)
+  float rope_base;          // > 0: dq, dk go back through the rotary embedding
   float* dq_acc;            // fp32 [Tq][H][d] accumulator (zeroed by the preprocess kernel)
   float* delta;             // fp32 [H][Tq]: rowsum(dO * O) for softmax
   const int2* items;
@@ -203,6 +247,11 @@ cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const
                        cudaEvent_t ev_end);
 cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale,
                               cudaStream_t stream);
+// dq = bf16 of the rotary backward of scale * acc ([T][H][d]); positions are
+// local to the samples of `offsets` (B + 1 entries).
+cudaError_t launch_dq_convert_rope(const float* acc, void* dq, const int32_t* offsets, int B,
+                                   long long T, int H, int d, float scale, float rope_base,
+                                   cudaStream_t stream);
 // Zeroes p.dq_acc and, for softmax, writes p.delta = rowsum(dO * O).
 cudaError_t launch_bwd_preprocess(const BwdParams& p, bool softmax, cudaStream_t stream);
 

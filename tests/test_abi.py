@@ -222,3 +222,22 @@ def test_dense_bias_rejections_on_host(lib):
     assert lib.gdpa_fwd_mxfp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 10, 10,
                               dense(), 0, 0, 0.125, FAKE, FAKE, FAKE, 1 << 20, None) == UNSUPPORTED
     assert _bwd_mx(lib, bias=dense()) == UNSUPPORTED
+
+
+def test_rope_backward_rejects_a_bad_base(lib):
+    def rope(base):
+        return lib.gdpa_bwd_rope(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, None, 0, 0, 0,
+                                 0.125, base, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE,
+                                 1 << 20, None)
+    assert rope(-1.0) == INVALID
+    assert rope(float("nan")) == INVALID
+    assert rope(float("inf")) == INVALID
+    # the fused rotary backward has no table-gradient or dense-bias variant
+    table = ctypes.byref(binding.gdpa_bias(binding.BIAS_RELPOS, FAKE, 8))
+    assert lib.gdpa_bwd_rope(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, table, 0, 0, 0, 0.125,
+                             1e4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20,
+                             None) == UNSUPPORTED
+    dense = ctypes.byref(binding.gdpa_bias(binding.BIAS_DENSE, FAKE, 0, FAKE + 64))
+    assert lib.gdpa_bwd_rope(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense, 0, 0, 0, 0.125,
+                             1e4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 20,
+                             None) == UNSUPPORTED

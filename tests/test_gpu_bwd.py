@@ -241,3 +241,39 @@ def test_dbias(act, d, variant):
     assert binding.device_status() == 0
     # (the fp32 atomics add in a different order each call: only the last bits differ)
     torch.testing.assert_close(dbias, 2 * first, rtol=1e-3, atol=1e-4 * float(first.abs().max()))
+
+
+@pytest.mark.parametrize("act", ["softmax", "silu"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_fused_rope(causal, d, act):
+    """gdpa_bwd_rope: q and k arrive rotary-embedded; dq and dk come back for
+    the un-rotated q, k (the oracle's rotary backward applied to its gradients,
+    queries and keys at their own positions), dv unchanged."""
+    lq = [1, 64, 65, 200, 0, 300, 129]
+    lkv = lq if causal else [7, 1, 130, 64, 5, 257, 3]
+    H, base = 2, 10000.0
+    g = torch.Generator(device="cuda").manual_seed(77 + d)
+    q = rand_bf16((sum(lq), H, d), g, "cuda")
+    k = rand_bf16((sum(lkv), H, d), g, "cuda")
+    v = rand_bf16((sum(lkv), H, d), g, "cuda")
+    do = rand_bf16((sum(lq), H, d), g, "cuda")
+    qo_np, ko_np = offsets(lq), offsets(lkv)
+    qo, ko = torch.from_numpy(qo_np).cuda(), torch.from_numpy(ko_np).cuda()
+    scale = 1.0 / math.sqrt(d)
+    a = ACTS[act]
+    out, lse = binding.gdpa_fwd(q, qo, k, v, ko, act=a, causal=causal, scale=scale)
+    bq, dq = guarded(sum(lq), H, d, q.device)
+    bk, dk = guarded(sum(lkv), H, d, q.device)
+    bv, dv = guarded(sum(lkv), H, d, q.device)
+    binding.gdpa_bwd(q, qo, k, v, ko, out, lse, do, act=a, causal=causal, scale=scale,
+                     rope_base=base, dq=dq, dk=dk, dv=dv)
+    assert binding.device_status() == 0
+    for b_ in (bq, bk, bv):
+        check_guards(b_)
+    rq, rk, rv = oracle.bwd(to_np(q), qo_np, to_np(k), to_np(v), ko_np, to_np(do), act=a,
+                            causal=causal, scale=scale)
+    what = f"rope bwd {act} d={d} causal={causal}"
+    assert_close(to_np(dq), oracle.rope_bwd(rq, qo_np, base), BWD_TOL, what + " dq")
+    assert_close(to_np(dk), oracle.rope_bwd(rk, ko_np, base), BWD_TOL, what + " dk")
+    assert_close(to_np(dv), rv, BWD_TOL, what + " dv")

@@ -74,6 +74,37 @@ def test_tensors_shapes_and_pma_sharing():
     assert torch.equal(q[0], q[-1])  # seed queries are shared by every sample
 
 
+def test_dense_bias_workload_layout():
+    """jfa_causal_dense: jfa_causal_relpos's lengths, no table, and a dense bias
+    whose per-sample blocks step by H * Lq * Lkv (checked on two samples)."""
+    from jagged_attention_recsys_02_gb300.workloads import first_samples
+
+    a, w = make_workload("jfa_causal_relpos"), make_workload("jfa_causal_dense")
+    assert np.array_equal(a.lq, w.lq) and w.dense and w.max_rel == 0 and w.causal
+    w2 = first_samples(w, 2)
+    w2.lq = w2.lkv = np.array([3, 5])
+    t = make_tensors(w2, device="cpu")
+    vals, off = t["bias"]
+    assert off.tolist() == [0, 4 * 9, 4 * 9 + 4 * 25] and vals.numel() == off[-1]
+    assert vals.dtype == torch.float32 and float(vals.std()) < 0.1
+
+
+def test_reference_arm_line_on_a_tiny_workload():
+    """bench.py --impl reference prints one JSON line with the contract's keys
+    (the oracle on the host cores; runs here, no GPU)."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_silu", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
 _WORKER = r'''
 import os, sys, json
 sys.path.insert(0, sys.argv[1])

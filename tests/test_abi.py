@@ -241,3 +241,35 @@ def test_rope_backward_rejects_a_bad_base(lib):
     assert lib.gdpa_bwd_rope(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense, 0, 0, 0, 0.125,
                              1e4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 20,
                              None) == UNSUPPORTED
+
+
+def test_binding_marshals_both_bias_forms():
+    """The binding's gdpa_bias: a table tensor gives the relative-position kind,
+    a (values, offsets) pair the dense kind with both pointers."""
+    import torch
+
+    table = torch.zeros(2, 15)
+    s = binding._bias(table, 8)._obj
+    assert (s.kind, s.table, s.max_rel, s.offsets) == (binding.BIAS_RELPOS, table.data_ptr(), 8, None)
+    vals, off = torch.zeros(12), torch.zeros(3, dtype=torch.int64)
+    s = binding._bias((vals, off), 0)._obj
+    assert (s.kind, s.table, s.offsets) == (binding.BIAS_DENSE, vals.data_ptr(), off.data_ptr())
+    assert binding._bias(None, 0) is None
+
+
+def test_bias_struct_layout_matches_the_header(tmp_path):
+    """The ctypes gdpa_bias has the C compiler's size and field offsets for the
+    struct declared in include/gdpa.h."""
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gdpa.h"\n'
+                   'int main(void) { printf("%zu %zu %zu %zu %zu", sizeof(gdpa_bias), '
+                   'offsetof(gdpa_bias, kind), offsetof(gdpa_bias, table), '
+                   'offsetof(gdpa_bias, max_rel), offsetof(gdpa_bias, offsets)); return 0; }\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    B = binding.gdpa_bias
+    assert got == [ctypes.sizeof(B), B.kind.offset, B.table.offset, B.max_rel.offset,
+                   B.offsets.offset]

@@ -1100,3 +1100,93 @@ def test_dense_bias_rejects_a_wrong_size(oracle_mod):
     x = np.zeros((5, 1, 4))
     with pytest.raises(AssertionError):
         oracle_mod.fwd(x, qo, x, x, qo, act=ACT_SOFTMAX, scale=1.0, dense_bias=np.zeros(12))
+
+
+# --------------------------------------------------------------- independent formulation
+def _torch_act(act):
+    return {ACT_SILU: F.silu, ACT_GELU_TANH: lambda x: F.gelu(x, approximate="tanh"),
+            ACT_GELU_ERF: lambda x: F.gelu(x, approximate="none"), ACT_IDENTITY: lambda x: x}[act]
+
+
+def _torch_reference(q, k, v, do, lq, lkv, act, causal, scale, table=None, max_rel=0, window=0,
+                     block=0, dense=None):
+    """Per-sample fp64 matrices (torch ops) and autograd: out, dq, dk, dv and the
+    table's gradient, with no code shared with the oracle's loops."""
+    H = q.shape[1]
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    tt = torch.tensor(table, dtype=torch.float64, requires_grad=True) if table is not None else None
+    outs, qo, ko, doff = [], 0, 0, 0
+    for Lq, Lkv in zip(lq, lkv):
+        i = torch.arange(Lq)[:, None]
+        j = torch.arange(Lkv)[None, :]
+        keep = torch.ones(Lq, Lkv, dtype=torch.bool)
+        if causal:
+            keep &= j <= i
+        if window:
+            keep &= (i - j).abs() < window
+        if block:
+            keep &= (i // block) == (j // block)
+        for h in range(H):
+            s = scale * tq[qo:qo + Lq, h] @ tk[ko:ko + Lkv, h].T
+            if tt is not None:
+                s = s + tt[h][(i - j + max_rel - 1).clamp(0, 2 * max_rel - 2)]
+            if dense is not None:
+                s = s + torch.tensor(dense[doff:doff + Lq * Lkv].reshape(Lq, Lkv))
+                doff += Lq * Lkv
+            if act == ACT_SOFTMAX:
+                p = torch.softmax(s.masked_fill(~keep, float("-inf")), dim=-1)
+                p = torch.nan_to_num(p, nan=0.0)      # a row with no key attends to nothing
+            else:
+                p = _torch_act(act)(s) * keep
+            outs.append((qo, h, p @ tv[ko:ko + Lkv, h]))
+        qo, ko = qo + Lq, ko + Lkv
+    out = torch.zeros_like(tq)
+    for q0, h, o in outs:
+        out[q0:q0 + o.shape[0], h] = o
+    (out * torch.tensor(do)).sum().backward()
+    return (out.detach().numpy(), tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy(),
+            tt.grad.numpy() if tt is not None else None)
+
+
+@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH, ACT_GELU_ERF, ACT_IDENTITY])
+@pytest.mark.parametrize("variant", ["tiny", "causal_bias", "window", "block", "dense"])
+def test_tiny_inputs_against_torch_autograd(oracle_mod, act, variant):
+    """Tiny inputs (B <= 4, L <= 64) against torch fp64 matrices differentiated by
+    autograd: the whole forward and every backward output, bias gradient too."""
+    rng = np.random.default_rng(100 + act)
+    H, d = 2, 8
+    if variant == "tiny":          # the four-sample tiny workload's lengths
+        lq = lkv = [1, 7, 33, 64]
+    elif variant == "causal_bias":
+        lq = lkv = [3, 5, 1]
+    else:
+        lq = lkv = [4, 5, 2] if variant != "block" else [9, 5, 12]
+    if variant == "tiny":
+        lkv = [2, 7, 5, 64]        # asymmetric lengths, no mask
+    causal = variant in ("causal_bias", "window")
+    max_rel = 4 if variant in ("causal_bias", "window", "block") else 0
+    table = rng.normal(0, 0.5, (H, 2 * max_rel - 1)) if max_rel else None
+    window = 2 if variant == "window" else 0
+    block = 4 if variant == "block" else 0
+    qo, ko = _offsets(lq), _offsets(lkv)
+    q, do = (rng.standard_normal((sum(lq), H, d)) for _ in range(2))
+    k, v = (rng.standard_normal((sum(lkv), H, d)) for _ in range(2))
+    dense = None
+    if variant == "dense":
+        dense = rng.normal(0, 0.7, int(oracle_mod.dense_bias_offsets(qo, ko, H)[-1]))
+        # the reference walks samples then heads: the oracle's layout is [b][h][i][j] too
+    scale = 0.6
+    kw = dict(act=act, causal=causal, scale=scale, window=window, block=block)
+    if table is not None:
+        kw.update(bias=table, max_rel=max_rel)
+    if dense is not None:
+        kw.update(dense_bias=dense)
+    ro, rdq, rdk, rdv, rdb = _torch_reference(q, k, v, do, lq, lkv, act, causal, scale, table,
+                                              max_rel, window, block, dense)
+    out, _ = oracle_mod.fwd(q, qo, k, v, ko, **kw)
+    np.testing.assert_allclose(out, ro, rtol=1e-11, atol=1e-12)
+    got = oracle_mod.bwd(q, qo, k, v, ko, do, want_dbias=table is not None, **kw)
+    for g, r in zip(got[:3], (rdq, rdk, rdv)):
+        np.testing.assert_allclose(g, r, rtol=1e-10, atol=1e-11)
+    if table is not None:
+        np.testing.assert_allclose(got[3], rdb, rtol=1e-10, atol=1e-11)

@@ -277,3 +277,26 @@ def test_bwd_fused_rope(causal, d, act):
     assert_close(to_np(dq), oracle.rope_bwd(rq, qo_np, base), BWD_TOL, what + " dq")
     assert_close(to_np(dk), oracle.rope_bwd(rk, ko_np, base), BWD_TOL, what + " dk")
     assert_close(to_np(dv), rv, BWD_TOL, what + " dv")
+
+
+@pytest.mark.parametrize("act", ["softmax", "silu"])
+def test_bwd_fused_rope_with_window(act):
+    """gdpa_bwd_rope with a sliding window (the windowed instantiation)."""
+    L = [1, 64, 65, 200, 300, 129]
+    H, d, base, window = 2, 128, 500.0, 100
+    g = torch.Generator(device="cuda").manual_seed(91)
+    q, k, v, do = (rand_bf16((sum(L), H, d), g, "cuda") for _ in range(4))
+    o_np = offsets(L)
+    o = torch.from_numpy(o_np).cuda()
+    scale = 1.0 / math.sqrt(d)
+    a = ACTS[act]
+    out, lse = binding.gdpa_fwd(q, o, k, v, o, act=a, causal=True, scale=scale, window=window)
+    dq, dk, dv = binding.gdpa_bwd(q, o, k, v, o, out, lse, do, act=a, causal=True, scale=scale,
+                                  window=window, rope_base=base)
+    assert binding.device_status() == 0
+    rq, rk, rv = oracle.bwd(to_np(q), o_np, to_np(k), to_np(v), o_np, to_np(do), act=a,
+                            causal=True, scale=scale, window=window)
+    what = f"rope+window bwd {act}"
+    assert_close(to_np(dq), oracle.rope_bwd(rq, o_np, base), BWD_TOL, what + " dq")
+    assert_close(to_np(dk), oracle.rope_bwd(rk, o_np, base), BWD_TOL, what + " dk")
+    assert_close(to_np(dv), rv, BWD_TOL, what + " dv")

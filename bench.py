@@ -693,13 +693,15 @@ def run_gpu_mxfp8(args, rank, world, local_rank):
     import torch.distributed as dist
 
     from jagged_attention_recsys_02_gb300 import binding
-    from jagged_attention_recsys_02_gb300.workloads import make_tensors, make_workload
+    from jagged_attention_recsys_02_gb300.workloads import first_samples, make_tensors, make_workload
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     if world > 1 and not dist.is_initialized():
         dist.init_process_group("nccl", device_id=dev)
     w = make_workload(args.workload or "heavy_tail", act="softmax")
+    if args.samples:
+        w = first_samples(w, args.samples)
     train = args.mxfp8_bwd
     t = make_tensors(w, device=dev, seed=rank, with_dout=train)
     H, d, Tq, Tkv = w.H, w.d, w.Tq, w.Tkv

@@ -35,6 +35,7 @@
  *   dbias_h[t] = sum over unmasked (i, j) of sample b with table index
  *                clamp(i - j + max_rel - 1) == t of ds_ij   (the bias enters s
  *                with weight 1; a learnable table's gradient)
+ *   dense bias: its gradient is ds_ij itself, in the bias's layout
  *
  * Readings taken where the pages are silent:
  *   - SiLU(x) = x * sigmoid(x); GELU is the tanh form
@@ -243,13 +244,20 @@ int oracle_bwd(const double* q, const int32_t* qo, const double* k, const double
                double* dk, double* dv, double* dbias, const double* dense, const int64_t* doff) {
   if (B < 0 || H <= 0 || d <= 0 || act < 0 || act > 4) return -1;
   if (!check_offsets(qo, B) || !check_offsets(ko, B)) return -1;
-  if (!check_dense(dense, doff, qo, ko, B, H) || (dense != NULL && dbias != NULL)) return -1;
+  if (!check_dense(dense, doff, qo, ko, B, H)) return -1;
   if (window < 0 || block < 0) return -1;
   if (causal || window > 0 || block > 0)
     for (int b = 0; b < B; ++b)
       if (qo[b + 1] - qo[b] != ko[b + 1] - ko[b]) return -1;
   const long nwork = (long)B * H;
   const long width = 2L * (max_rel > 0 ? max_rel : 1) - 1;
+  /* With a dense bias its gradient is ds itself, written in the bias's layout
+   * (0 for masked pairs); with a table, the per-entry sums below. */
+  double* ddense = (dense != NULL) ? dbias : NULL;
+  if (ddense != NULL) {
+    for (long t = 0; t < (long)doff[B]; ++t) ddense[t] = 0.0;
+    dbias = NULL;
+  }
   if (dbias != NULL)
     for (long t = 0; t < (long)H * width; ++t) dbias[t] = 0.0;
   /* per-(sample, head) partial sums of the bias gradient, added in a fixed
@@ -300,6 +308,7 @@ int oracle_bwd(const double* q, const int32_t* qo, const double* k, const double
           dkj[c] += scale * ds * qi[c];
           dvj[c] += p[j] * doi[c];
         }
+        if (ddense != NULL) ddense[doff[b] + ((long)h * Lq + i) * Lkv + j] = ds;
         if (part != NULL) {
           long t = (i - j) + (max_rel - 1);
           if (t < 0) t = 0;

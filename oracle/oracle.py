@@ -153,8 +153,8 @@ def bwd(q, q_offsets, k, v, kv_offsets, dout, *, act: int, causal: bool = False,
         bias=None, max_rel: int = 0, window: int = 0, block: int = 0, want_dbias: bool = False,
         dense_bias=None):
     """Backward pass.  Returns (dq, dk, dv) as float64 arrays, and with
-    want_dbias also the bias table's gradient [H, 2*max_rel-1]:
-    (dq, dk, dv, dbias)."""
+    want_dbias also the bias's gradient: the table's [H, 2*max_rel-1], or with
+    a dense bias one value per pair in its layout (dS): (dq, dk, dv, dbias)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
     qo, ko = _i32(q_offsets), _i32(kv_offsets)
     Tq, H, d = q.shape
@@ -163,7 +163,10 @@ def bwd(q, q_offsets, k, v, kv_offsets, dout, *, act: int, causal: bool = False,
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
-    dbias = np.zeros((H, 2 * max(int(max_rel), 1) - 1), dtype=np.float64) if want_dbias else None
+    if want_dbias and dense_bias is not None:  # the dense bias's gradient: ds, same layout
+        dbias = np.zeros(int(dense_bias_offsets(qo, ko, H)[-1]), dtype=np.float64)
+    else:
+        dbias = np.zeros((H, 2 * max(int(max_rel), 1) - 1), dtype=np.float64) if want_dbias else None
     keep, bp = _bias_arg(bias, H, max_rel)
     keep_d, dp_, op_ = _dense_arg(dense_bias, qo, ko, H)
     rc = _load().oracle_bwd(_p(q, ctypes.c_double), _p(qo, ctypes.c_int32),

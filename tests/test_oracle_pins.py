@@ -1190,3 +1190,44 @@ def test_tiny_inputs_against_torch_autograd(oracle_mod, act, variant):
         np.testing.assert_allclose(g, r, rtol=1e-10, atol=1e-11)
     if table is not None:
         np.testing.assert_allclose(got[3], rdb, rtol=1e-10, atol=1e-11)
+
+
+@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_SILU])
+@pytest.mark.parametrize("causal", [False, True])
+def test_dense_bias_gradient(oracle_mod, act, causal):
+    """The dense bias's gradient (dS, in the bias's layout): central differences
+    of the forward in sampled entries, zeros on masked pairs, and summed along
+    the clamped relative positions it equals the (pinned) table gradient when
+    the dense bias is the table written out."""
+    lq = [4, 6, 1] if causal else [4, 6, 2]
+    lkv = lq if causal else [3, 5, 4]
+    H, d, max_rel = 2, 4, 3
+    qo, ko = _offsets(lq), _offsets(lkv)
+    rng = np.random.default_rng(11)
+    q = rng.standard_normal((sum(lq), H, d))
+    k, v = (rng.standard_normal((sum(lkv), H, d)) for _ in range(2))
+    do = rng.standard_normal((sum(lq), H, d))
+    table = rng.normal(0, 0.5, (H, 2 * max_rel - 1))
+    dense = _dense_from_table(table, lq, lkv, max_rel)
+    kw = dict(act=act, causal=causal, scale=0.8)
+    *_, g = oracle_mod.bwd(q, qo, k, v, ko, do, want_dbias=True, dense_bias=dense, **kw)
+    assert g.shape == dense.shape
+    loss = lambda dn: float((oracle_mod.fwd(q, qo, k, v, ko, dense_bias=dn, **kw)[0] * do).sum())
+    h = 1e-6
+    for idx in rng.choice(dense.size, 25, replace=False):
+        e = np.zeros_like(dense)
+        e[idx] = h
+        np.testing.assert_allclose(g[idx], (loss(dense + e) - loss(dense - e)) / (2 * h),
+                                   rtol=1e-6, atol=1e-8)
+    off = oracle_mod.dense_bias_offsets(qo, ko, H)
+    table_grad = np.zeros_like(table)
+    for b, (Lq, Lkv) in enumerate(zip(lq, lkv)):
+        blk = g[off[b]:off[b + 1]].reshape(H, Lq, Lkv)
+        i, j = np.arange(Lq)[:, None], np.arange(Lkv)[None, :]
+        if causal:
+            assert np.all(blk[:, j > i] == 0.0)
+        idx = np.clip(i - j + max_rel - 1, 0, 2 * max_rel - 2)
+        for hh in range(H):
+            np.add.at(table_grad[hh], idx, blk[hh])
+    ref = oracle_mod.bwd(q, qo, k, v, ko, do, want_dbias=True, bias=table, max_rel=max_rel, **kw)[3]
+    np.testing.assert_allclose(table_grad, ref, rtol=1e-12, atol=1e-12)

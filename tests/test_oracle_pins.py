@@ -760,17 +760,18 @@ def test_rope_backward_is_the_gradient(oracle_mod):
 
 # --------------------------------------------------------------- bias table gradient
 @pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_SILU, ACT_GELU_TANH])
-@pytest.mark.parametrize("variant", ["plain", "causal", "window", "clamped"])
+@pytest.mark.parametrize("variant", ["plain", "causal", "window", "clamped", "block"])
 def test_dbias_matches_central_differences(oracle_mod, act, variant):
     """The bias table's gradient against central differences of the forward in
     every table entry (a 'clamped' table is shorter than the samples, so its end
-    entries collect many offsets)."""
+    entries collect many offsets; 'block' keeps pairs inside 3-token blocks)."""
     H, d = 2, 5
     max_rel = 2 if variant == "clamped" else 6
     lq = [4, 6, 0]
     causal = variant == "causal"
     window = 3 if variant == "window" else 0
-    lkv = lq if (causal or window) else [5, 3, 2]
+    block = 3 if variant == "block" else 0
+    lkv = lq if (causal or window or block) else [5, 3, 2]
     rng = np.random.default_rng(400 + act)
     q = rng.normal(size=(sum(lq), H, d))
     k = rng.normal(size=(sum(lkv), H, d))
@@ -778,7 +779,7 @@ def test_dbias_matches_central_differences(oracle_mod, act, variant):
     do = rng.normal(size=(sum(lq), H, d))
     table = rng.normal(0, 0.5, size=(H, 2 * max_rel - 1))
     qo, ko = _offsets(lq), _offsets(lkv)
-    kw = dict(act=act, causal=causal, window=window, scale=0.45, max_rel=max_rel)
+    kw = dict(act=act, causal=causal, window=window, block=block, scale=0.45, max_rel=max_rel)
     *_, db = oracle_mod.bwd(q, qo, k, v, ko, do, bias=table, want_dbias=True, **kw)
     h = 1e-6
     num = np.zeros_like(table)

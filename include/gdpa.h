@@ -15,9 +15,9 @@
  * Lkv_b = kv_offsets[b+1]-kv_offsets[b] key/value rows, head h, local row i
  * and local key j (mask: j <= i when causal, and |i - j| < window for the
  * sliding-window entry points; else all):
- *     s_ij  = scale * <q_i, k_j> + bias_h(i - j)
+ *     s_ij  = scale * <q_i, k_j> + bias_h(i - j)      (or + a dense bias B_b[h][i][j])
  *     p_ij  = softmax_j(s_ij)       (GDPA_ACT_SOFTMAX, masked entries excluded)
- *           = act(s_ij)             (SiLU, GELU-tanh, identity; no normalisation)
+ *           = act(s_ij)             (SiLU, GELU-tanh, GELU-erf, identity; no normalisation)
  *     out_i = sum_j p_ij v_j
  * SiLU(x) = x sigmoid(x); GELU-tanh(x) = 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3)));
  * GELU-erf(x) = 0.5 x (1 + erf(x / sqrt(2))).
@@ -42,6 +42,12 @@
  *    status word; gdpa_get_device_status() synchronises the stream, returns
  *    it and clears it.  After such an error the outputs are undefined, but
  *    every write stays inside the caller's buffers.
+ *
+ * Entry points: gdpa_fwd / gdpa_bwd (and their _window forms; gdpa_bwd_rope
+ * adds the fused rotary backward), gdpa_fwd_noalloc, the block-aligned
+ * gdpa_block_fwd / gdpa_block_bwd, the MXFP8 gdpa_quantize_mxfp8,
+ * gdpa_fwd_mxfp8(_window) and gdpa_bwd_mxfp8(_window), the workspace-size
+ * queries, and the status, launch-count and timing helpers.
  */
 #ifndef GDPA_H_
 #define GDPA_H_

@@ -724,19 +724,18 @@ gdpa_status gdpa_bwd_mxfp8_window(const void* q, const int32_t* q_offsets, const
   auto at = [&](size_t off) { return static_cast<void*>(ws + off); };
 
   // 1) operand codes and scales: Q, K, dO along channels and along tokens, V along channels
-  cudaError_t e = cudaSuccess;
   if (Tq > 0) {
-    if ((e = launch_quant_rows(q, Tq * H, d, at(lay.qd), at(lay.qd_sc), s)) != cudaSuccess ||
-        (e = launch_quant_tokens(q, q_offsets, B, H, d, Tq, at(lay.qt), at(lay.qt_sc), s)) != cudaSuccess ||
-        (e = launch_quant_rows(dout, Tq * H, d, at(lay.dod), at(lay.dod_sc), s)) != cudaSuccess ||
-        (e = launch_quant_tokens(dout, q_offsets, B, H, d, Tq, at(lay.dot), at(lay.dot_sc), s)) != cudaSuccess)
+    if (launch_quant_rows(q, Tq * H, d, at(lay.qd), at(lay.qd_sc), s) != cudaSuccess ||
+        launch_quant_tokens(q, q_offsets, B, H, d, Tq, at(lay.qt), at(lay.qt_sc), s) != cudaSuccess ||
+        launch_quant_rows(dout, Tq * H, d, at(lay.dod), at(lay.dod_sc), s) != cudaSuccess ||
+        launch_quant_tokens(dout, q_offsets, B, H, d, Tq, at(lay.dot), at(lay.dot_sc), s) != cudaSuccess)
       return GDPA_ERR_CUDA;
     t_launches += 4;
   }
   if (Tkv > 0) {
-    if ((e = launch_quant_rows(k, Tkv * H, d, at(lay.kd), at(lay.kd_sc), s)) != cudaSuccess ||
-        (e = launch_quant_tokens(k, kv_offsets, B, H, d, Tkv, at(lay.kt), at(lay.kt_sc), s)) != cudaSuccess ||
-        (e = launch_quant_rows(v, Tkv * H, d, at(lay.vd), at(lay.vd_sc), s)) != cudaSuccess)
+    if (launch_quant_rows(k, Tkv * H, d, at(lay.kd), at(lay.kd_sc), s) != cudaSuccess ||
+        launch_quant_tokens(k, kv_offsets, B, H, d, Tkv, at(lay.kt), at(lay.kt_sc), s) != cudaSuccess ||
+        launch_quant_rows(v, Tkv * H, d, at(lay.vd), at(lay.vd_sc), s) != cudaSuccess)
       return GDPA_ERR_CUDA;
     t_launches += 3;
   }
@@ -820,7 +819,6 @@ gdpa_status gdpa_bwd_mxfp8_window(const void* q, const int32_t* q_offsets, const
       return GDPA_ERR_CUDA;
     ++t_launches;
   }
-  (void)e;
   return GDPA_OK;
 }
 

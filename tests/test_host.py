@@ -34,6 +34,27 @@ def test_window_pair_counts_match_the_mask(causal):
     assert w.pairs() < int(np.sum(w.lq * (w.lq + 1) // 2))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_and_plain_pair_counts_match_the_mask(causal):
+    """Non-padded pair counts (the FLOP count of every measurement) for block
+    attention, plain causal and asymmetric non-causal workloads against brute
+    force over the mask; forward FLOPs are 4 H d per pair."""
+    lengths = [0, 1, 2, 5, 63, 64, 65, 200]
+    for K in (1, 3, 64):
+        w = custom_workload(lengths, lengths, 1, 64, causal=causal, block=K)
+        for L, got in zip(lengths, w.sample_pairs()):
+            i, j = np.arange(L)[:, None], np.arange(L)[None, :]
+            keep = (i // K) == (j // K)
+            if causal:
+                keep &= j <= i
+            assert got == keep.sum(), (L, K, causal)
+    lkv = lengths if causal else [3, 0, 9, 5, 1, 64, 2, 7]
+    w = custom_workload(lengths, lkv, 2, 128, causal=causal)
+    brute = sum(int(((np.arange(a)[:, None] >= np.arange(b)[None, :]) if causal
+                     else np.ones((a, b), bool)).sum()) for a, b in zip(lengths, lkv))
+    assert w.pairs() == brute and w.fwd_flops() == 4.0 * 2 * 128 * brute
+
+
 def test_workload_recipes():
     w = make_workload("tiny_silu")
     assert list(w.lq) == [1, 7, 33, 64] and (w.H, w.d, w.act) == (2, 64, "silu")

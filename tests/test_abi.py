@@ -273,3 +273,24 @@ def test_bias_struct_layout_matches_the_header(tmp_path):
     B = binding.gdpa_bias
     assert got == [ctypes.sizeof(B), B.kind.offset, B.table.offset, B.max_rel.offset,
                    B.offsets.offset]
+
+
+def test_header_compiles_as_c_and_links(tmp_path, lib):
+    """A C program that includes include/gdpa.h and takes the address of every
+    declared function compiles as C11 and links against the library."""
+    names = declared_functions()
+    src = tmp_path / "uses_abi.c"
+    src.write_text('#include <stdio.h>\n#include "gdpa.h"\n'
+                   "int main(void) {\n  void* fns[] = {\n"
+                   + "".join(f"    (void*){n},\n" for n in names)
+                   + "  };\n  int n = 0;\n"
+                   "  for (unsigned i = 0; i < sizeof(fns) / sizeof(fns[0]); ++i) n += fns[i] != 0;\n"
+                   '  printf("%d", n);\n  return 0;\n}\n')
+    exe = tmp_path / "uses_abi"
+    libdir = os.path.dirname(build.LIB)
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), f"-L{libdir}", "-l:" + os.path.basename(build.LIB),
+                    f"-Wl,-rpath,{libdir}", "-Wl,--unresolved-symbols=ignore-in-shared-libs"],
+                   check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, check=True)
+    assert int(r.stdout) == len(names)

@@ -47,7 +47,7 @@
  * adds the fused rotary backward), gdpa_fwd_noalloc, the block-aligned
  * gdpa_block_fwd / gdpa_block_bwd, the MXFP8 gdpa_quantize_mxfp8,
  * gdpa_fwd_mxfp8(_window) and gdpa_bwd_mxfp8(_window), the workspace-size
- * queries, and the status, launch-count and timing helpers.
+ * queries, and the status, launch-count, timing and self-test helpers.
  */
 #ifndef GDPA_H_
 #define GDPA_H_
@@ -302,6 +302,14 @@ gdpa_status gdpa_bwd_mxfp8_window(const void* q, const int32_t* q_offsets, const
  * synchronising `stream` first, then clears it.  Returns GDPA_OK,
  * GDPA_ERR_TIMEOUT, GDPA_ERR_BAD_OFFSETS or GDPA_ERR_CUDA. */
 gdpa_status gdpa_get_device_status(void* stream);
+
+/* Failure-detection self-test: launches one small kernel whose pipeline wait
+ * (an mbarrier nothing arrives at) cannot complete, waited on with the
+ * library's bounded wait for limit_us microseconds (1 .. 1e6).  The wait
+ * gives up, the kernel sets GDPA_ERR_TIMEOUT in the device status word and
+ * returns: the next gdpa_get_device_status() reports it, and the context
+ * stays usable.  No fault is raised. */
+gdpa_status gdpa_selftest_timeout(int limit_us, void* stream);
 
 /* Static, human-readable name of a status code. */
 const char* gdpa_status_string(int status);

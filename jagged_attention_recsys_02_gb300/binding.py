@@ -33,7 +33,7 @@ EXPORTS = ("gdpa_fwd_workspace_size", "gdpa_fwd", "gdpa_bwd_workspace_size", "gd
            "gdpa_fwd_window", "gdpa_bwd_window", "gdpa_fwd_mxfp8_window",
            "gdpa_block_workspace_size", "gdpa_block_fwd", "gdpa_block_bwd",
            "gdpa_bwd_mxfp8_workspace_size", "gdpa_bwd_mxfp8", "gdpa_bwd_mxfp8_window",
-           "gdpa_bwd_rope")
+           "gdpa_bwd_rope", "gdpa_selftest_timeout")
 MX_ALONG_CHANNELS, MX_ALONG_TOKENS = 0, 1
 
 
@@ -92,6 +92,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                       ctypes.POINTER(gdpa_bias), I, I, I, F, F, vp, vp, vp, vp, vp,
                                       vp, vp, vp, sz, vp]
         lib.gdpa_bwd_rope.restype = I
+        lib.gdpa_selftest_timeout.argtypes = [I, vp]
+        lib.gdpa_selftest_timeout.restype = I
         lib.gdpa_get_device_status.argtypes = [vp]
         lib.gdpa_get_device_status.restype = I
         lib.gdpa_status_string.argtypes = [I]
@@ -234,6 +236,12 @@ def gdpa_bwd(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, act, causal=Fals
         rc = lib.gdpa_bwd(*head, *tail, *ws)
         _check(rc, "gdpa_bwd")
     return dq, dk, dv
+
+
+def selftest_timeout(limit_us: int = 2000, stream=None) -> None:
+    """Launch the failure-detection self-test (a wait that times out after
+    limit_us and records GDPA_ERR_TIMEOUT in the device status word)."""
+    _check(load().gdpa_selftest_timeout(int(limit_us), _stream(stream)), "gdpa_selftest_timeout")
 
 
 def bwd_mxfp8_workspace_size(B, H, d, Tq, Tkv) -> int:

@@ -173,6 +173,22 @@ const float* bias_table(const gdpa_bias* bias, int* max_rel) {
   return bias->table;
 }
 
+// A pipeline wait that cannot complete: one mbarrier that nothing arrives
+// at, waited on with the kernels' own bounded wait (limit_ns of wall time).
+// When the wait gives up, the kernel records GDPA_ERR_TIMEOUT in the status
+// word and returns, as every kernel of the library does on a timeout.
+__global__ void selftest_timeout_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  const uint32_t b = ptx::smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(b, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !ptx::mbar_wait(b, 0, nullptr, limit_ns))
+    set_status(status, GDPA_ERR_TIMEOUT);
+}
+
 }  // namespace
 }  // namespace gdpa
 
@@ -819,6 +835,18 @@ gdpa_status gdpa_bwd_mxfp8_window(const void* q, const int32_t* q_offsets, const
       return GDPA_ERR_CUDA;
     ++t_launches;
   }
+  return GDPA_OK;
+}
+
+gdpa_status gdpa_selftest_timeout(int limit_us, void* stream) {
+  t_launches = 0;
+  if (limit_us < 1 || limit_us > 1000000) return GDPA_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if (device_info(&dev) != cudaSuccess) return GDPA_ERR_CUDA;
+  selftest_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      dev->status, static_cast<unsigned long long>(limit_us) * 1000ull);
+  if (cudaGetLastError() != cudaSuccess) return GDPA_ERR_CUDA;
+  ++t_launches;
   return GDPA_OK;
 }
 

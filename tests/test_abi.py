@@ -294,3 +294,8 @@ def test_header_compiles_as_c_and_links(tmp_path, lib):
                    check=True)
     r = subprocess.run([str(exe)], capture_output=True, text=True, check=True)
     assert int(r.stdout) == len(names)
+
+
+def test_selftest_rejects_a_bad_limit(lib):
+    assert lib.gdpa_selftest_timeout(0, None) == INVALID
+    assert lib.gdpa_selftest_timeout(2_000_000, None) == INVALID

@@ -164,3 +164,25 @@ def test_reduce_over_ranks_single_process():
     import bench
 
     assert bench.reduce_over_ranks(3.0, 7.0) == (3.0, 7.0)
+
+
+def test_traffic_table_is_well_formed():
+    """profiles/dram_traffic.json: every entry names an existing kernel source
+    and a 16-hex-digit hash prefix; the benchmark reports an entry only while
+    that source is unchanged (and the headline entries are current)."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+        table = json.load(f)
+    csrc = os.path.join(ROOT, "jagged_attention_recsys_02_gb300", "csrc")
+    for key, e in table.items():
+        if "/" not in key:
+            continue
+        assert os.path.exists(os.path.join(csrc, e["source"])), key
+        assert len(e["sha256_16"]) == 16 and int(e["sha256_16"], 16) >= 0, key
+        assert e["bytes"] > 0, key
+    valid = bench.load_traffic()
+    assert set(valid) <= set(table)
+    for key in ("jfa_causal_relpos/softmax/fwd", "jfa_causal_relpos/softmax/bwd"):
+        assert key in valid, f"{key} is stale: re-capture it"

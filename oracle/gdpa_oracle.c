@@ -399,14 +399,19 @@ uint8_t oracle_e8m0_scale(double amax) {
   return (uint8_t)code;
 }
 
+uint8_t oracle_e8m0_nosat(double amax);
+
+/* One block of n elements (stride apart): the shared scale is the OCP one,
+ * 2^(floor(log2 amax) - 8), or with nosat the smallest power of two X with
+ * amax / X <= 448 (no element saturates; see oracle_e8m0_nosat). */
 static void quant_block(const double* x, long stride, int n, uint8_t* codes, long cstride,
-                        uint8_t* scale) {
+                        uint8_t* scale, int nosat) {
   double amax = 0.0;
   for (int t = 0; t < n; ++t) {
     const double a = fabs(x[t * stride]);
     if (a > amax) amax = a;
   }
-  const uint8_t sc = oracle_e8m0_scale(amax);
+  const uint8_t sc = nosat ? oracle_e8m0_nosat(amax) : oracle_e8m0_scale(amax);
   *scale = sc;
   const double inv = ldexp(1.0, -(sc - 127));
   for (int t = 0; t < n; ++t) codes[t * cstride] = oracle_e4m3_encode(x[t * stride] * inv);
@@ -414,14 +419,15 @@ static void quant_block(const double* x, long stride, int n, uint8_t* codes, lon
 
 /* Q or K: blocks of 32 consecutive channels of each (token, head) row.
  * x [T][H][d] -> codes [T][H][d], scales [T][H][d/32].  d % 32 == 0. */
-void oracle_quant_rows(const double* x, long T, int H, int d, uint8_t* codes, uint8_t* scales) {
+void oracle_quant_rows(const double* x, long T, int H, int d, int nosat, uint8_t* codes,
+                       uint8_t* scales) {
   const int nb = d / 32;
 #pragma omp parallel for schedule(static)
   for (long t = 0; t < T; ++t)
     for (int h = 0; h < H; ++h)
       for (int g = 0; g < nb; ++g) {
         const long base = (t * H + h) * (long)d + 32L * g;
-        quant_block(x + base, 1, 32, codes + base, 1, scales + (t * H + h) * (long)nb + g);
+        quant_block(x + base, 1, 32, codes + base, 1, scales + (t * H + h) * (long)nb + g, nosat);
       }
 }
 
@@ -430,8 +436,8 @@ void oracle_quant_rows(const double* x, long T, int H, int d, uint8_t* codes, ui
  * channel.  x [T][H][d] -> codes [T][H][d]; scales [NB][H][d] where block
  * row r of sample b is NB-row blk_off[b] + r and blk_off[b] = sum over
  * b' < b of ceil(L_b' / 32). */
-void oracle_quant_cols(const double* x, const int32_t* offs, int B, int H, int d, uint8_t* codes,
-                       uint8_t* scales) {
+void oracle_quant_cols(const double* x, const int32_t* offs, int B, int H, int d, int nosat,
+                       uint8_t* codes, uint8_t* scales) {
 #pragma omp parallel for schedule(dynamic, 1)
   for (int b = 0; b < B; ++b) {
     long blk = 0;
@@ -444,7 +450,7 @@ void oracle_quant_cols(const double* x, const int32_t* offs, int B, int H, int d
         for (int c = 0; c < d; ++c) {
           const long base = (t0 * H + h) * (long)d + c;
           quant_block(x + base, (long)H * d, n, codes + base, (long)H * d,
-                      scales + ((blk + r) * H + h) * (long)d + c);
+                      scales + ((blk + r) * H + h) * (long)d + c, nosat);
         }
     }
   }

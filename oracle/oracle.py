@@ -59,9 +59,9 @@ def _load():
         lib.oracle_e4m3_decode.restype = D
         lib.oracle_e8m0_scale.argtypes = [D]
         lib.oracle_e8m0_scale.restype = ctypes.c_uint8
-        lib.oracle_quant_rows.argtypes = [dp, ctypes.c_long, I, I, up, up]
+        lib.oracle_quant_rows.argtypes = [dp, ctypes.c_long, I, I, I, up, up]
         lib.oracle_quant_rows.restype = None
-        lib.oracle_quant_cols.argtypes = [dp, ip, I, I, I, up, up]
+        lib.oracle_quant_cols.argtypes = [dp, ip, I, I, I, I, up, up]
         lib.oracle_quant_cols.restype = None
         lib.oracle_e8m0_nosat.argtypes = [D]
         lib.oracle_e8m0_nosat.restype = ctypes.c_uint8
@@ -195,20 +195,24 @@ def e8m0_scale(amax: float) -> int:
     return int(_load().oracle_e8m0_scale(float(amax)))
 
 
-def quant_rows(x):
-    """MXFP8 along the channel axis: x [T,H,d] -> (codes u8 [T,H,d], scales u8 [T,H,d/32])."""
+def quant_rows(x, nosat: bool = False):
+    """MXFP8 along the channel axis: x [T,H,d] -> (codes u8 [T,H,d], scales u8 [T,H,d/32]).
+
+    Block scale: the OCP one, 2^(floor(log2 amax) - 8), or with nosat the
+    saturation-free one (smallest power of two X with amax / X <= 448)."""
     x = _f64(x)
     T, H, d = x.shape
     assert d % 32 == 0
     codes = np.zeros((T, H, d), dtype=np.uint8)
     scales = np.zeros((T, H, d // 32), dtype=np.uint8)
-    _load().oracle_quant_rows(_p(x, ctypes.c_double), T, H, d, _p(codes, ctypes.c_uint8),
-                              _p(scales, ctypes.c_uint8))
+    _load().oracle_quant_rows(_p(x, ctypes.c_double), T, H, d, int(bool(nosat)),
+                              _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_uint8))
     return codes, scales
 
 
-def quant_cols(x, offsets):
-    """MXFP8 along tokens, in 32-token blocks aligned to each sample's start.
+def quant_cols(x, offsets, nosat: bool = False):
+    """MXFP8 along tokens, in 32-token blocks aligned to each sample's start
+    (block scale as in quant_rows).
 
     x [T,H,d] -> (codes u8 [T,H,d], scales u8 [NB,H,d]) with NB = sum ceil(L_b/32)."""
     x = _f64(x)
@@ -219,7 +223,8 @@ def quant_cols(x, offsets):
     codes = np.zeros((T, H, d), dtype=np.uint8)
     scales = np.zeros((max(nb, 0), H, d), dtype=np.uint8)
     _load().oracle_quant_cols(_p(x, ctypes.c_double), _p(o, ctypes.c_int32), B, H, d,
-                              _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_uint8))
+                              int(bool(nosat)), _p(codes, ctypes.c_uint8),
+                              _p(scales, ctypes.c_uint8))
     return codes, scales
 
 
@@ -247,16 +252,16 @@ def _e4m3_table():
     return _E4M3
 
 
-def dequant_rows(x):
+def dequant_rows(x, nosat: bool = False):
     """x quantised along channels (quant_rows) and decoded back to float64."""
-    codes, scales = quant_rows(x)
+    codes, scales = quant_rows(x, nosat)
     return _e4m3_table()[codes] * np.exp2(scales.astype(np.float64) - 127).repeat(32, axis=2)
 
 
-def dequant_cols(x, offsets):
+def dequant_cols(x, offsets, nosat: bool = False):
     """x quantised along tokens (quant_cols) and decoded back to float64."""
     o = _i32(offsets)
-    codes, scales = quant_cols(x, o)
+    codes, scales = quant_cols(x, o, nosat)
     dec = _e4m3_table()[codes]
     out = np.zeros_like(dec)
     k = 0

@@ -421,6 +421,60 @@ def test_quant_cols_sample_aligned_blocks(oracle_mod):
     np.testing.assert_array_equal(np.abs(dec), 256.0)
 
 
+def _nosat_exponent(amax):
+    """Least integer e with amax <= 448 * 2^e, from frexp (amax = f 2^k, f in
+    [0.5, 1)): 448 2^e = 0.875 2^(e+9), so e = k - 9 when f <= 0.875, else k - 8."""
+    f, k = np.frexp(amax)
+    return np.where(f <= 0.875, k - 9, k - 8)
+
+
+def test_quant_rows_nosat_against_torch_float8(oracle_mod):
+    """The saturation-free quantiser along channels: each 32-channel block is
+    divided by 2^e with e the least exponent keeping its maximum at or below
+    448, then rounded as torch's float8_e4m3fn conversion rounds; no element
+    saturates, and the scale is the OCP one or one step above it."""
+    T, H, d = 7, 3, 64
+    x = _bf16_randn((T, H, d), 31) * np.exp2(np.arange(d) // 32 * 3)[None, None, :]
+    x[0, 0, :32] = 1.875 * 2.0 ** 4                    # mantissa above 1.75: OCP would clip
+    x[1, 1, 32:] = 0.0                                 # all-zero block
+    codes, scales = oracle_mod.quant_rows(x, nosat=True)
+    blocks = x.reshape(T, H, 2, 32)
+    amax = np.abs(blocks).max(-1)
+    e = np.where(amax > 0, _nosat_exponent(np.where(amax > 0, amax, 1.0)), -127)
+    np.testing.assert_array_equal(scales.astype(int), e + 127)
+    X = np.exp2(e)[..., None]
+    ref = torch.from_numpy(blocks / X).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(codes, ref.reshape(T, H, d))
+    assert np.all(np.abs(blocks / X) <= 448.0)
+    _, ocp = oracle_mod.quant_rows(x)
+    step = scales.astype(int) - ocp.astype(int)
+    assert np.all((step == 0) | (step == 1)) and step[0, 0, 0] == 1
+    # the clipped block decodes exactly with the saturation-free scale
+    dec = np.vectorize(oracle_mod.e4m3_decode)(codes[0, 0, :32]) * 2.0 ** (int(scales[0, 0, 0]) - 127)
+    np.testing.assert_array_equal(dec, x[0, 0, :32])
+
+
+def test_quant_cols_nosat_against_torch_float8(oracle_mod):
+    """Saturation-free quantiser along tokens: the same rule on 32-token blocks
+    aligned to each sample's first token (the last block partial)."""
+    lengths = [5, 40, 33, 0, 64]
+    H, d = 2, 8
+    o = _offsets(lengths)
+    x = _bf16_randn((sum(lengths), H, d), 32) * 7.0
+    codes, scales = oracle_mod.quant_cols(x, o, nosat=True)
+    r = 0
+    for b, L in enumerate(lengths):
+        for t0 in range(int(o[b]), int(o[b + 1]), 32):
+            blk = x[t0:min(t0 + 32, int(o[b + 1]))]
+            amax = np.abs(blk).max(0)
+            e = _nosat_exponent(amax)
+            np.testing.assert_array_equal(scales[r].astype(int), e + 127)
+            ref = torch.from_numpy(blk / np.exp2(e)).to(torch.float8_e4m3fn).view(torch.uint8)
+            np.testing.assert_array_equal(codes[t0:t0 + len(blk)], ref.numpy())
+            r += 1
+    assert r == scales.shape[0]
+
+
 # --------------------------------------------------------------- sliding window
 def _band(L, window, causal):
     i = np.arange(L)[:, None]

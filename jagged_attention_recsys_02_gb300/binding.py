@@ -34,7 +34,7 @@ EXPORTS = ("gdpa_fwd_workspace_size", "gdpa_fwd", "gdpa_bwd_workspace_size", "gd
            "gdpa_block_workspace_size", "gdpa_block_fwd", "gdpa_block_bwd",
            "gdpa_bwd_mxfp8_workspace_size", "gdpa_bwd_mxfp8", "gdpa_bwd_mxfp8_window",
            "gdpa_bwd_rope", "gdpa_selftest_timeout")
-MX_ALONG_CHANNELS, MX_ALONG_TOKENS = 0, 1
+MX_ALONG_CHANNELS, MX_ALONG_TOKENS, MX_NOSAT = 0, 1, 2
 
 
 class GdpaError(RuntimeError):
@@ -345,18 +345,20 @@ def timing_collect(max_n: int = 4096):
     return f, b
 
 
-def quantize_mxfp8(x, offsets=None, *, mode, codes=None, scales=None, stream=None):
-    """MXFP8 block quantisation through the C ABI.  Returns (codes u8, scales u8)."""
+def quantize_mxfp8(x, offsets=None, *, mode, nosat=False, codes=None, scales=None, stream=None):
+    """MXFP8 block quantisation through the C ABI (nosat: the saturation-free
+    block scale, GDPA_MX_NOSAT).  Returns (codes u8, scales u8)."""
     lib = load()
     T, H, d = x.shape
     B = offsets.numel() - 1 if offsets is not None else 0
+    mode = int(mode) | (MX_NOSAT if nosat else 0)
     if codes is None:
         codes = torch.empty((T, H, d), device=x.device, dtype=torch.uint8)
     if scales is None:
         n = lib.gdpa_mxfp8_scale_bytes(max(B, 0), H, d, T, mode)
-        shape = (T, H, d // 32) if mode == MX_ALONG_CHANNELS else (n // (H * d), H, d)
+        shape = (T, H, d // 32) if not mode & MX_ALONG_TOKENS else (n // (H * d), H, d)
         scales = torch.empty(shape, device=x.device, dtype=torch.uint8)
-    rc = lib.gdpa_quantize_mxfp8(_ptr(x), _ptr(offsets), B, H, d, T, int(mode), _ptr(codes),
+    rc = lib.gdpa_quantize_mxfp8(_ptr(x), _ptr(offsets), B, H, d, T, mode, _ptr(codes),
                                  _ptr(scales), _stream(stream))
     _check(rc, "gdpa_quantize_mxfp8")
     return codes, scales

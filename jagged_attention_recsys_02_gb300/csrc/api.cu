@@ -549,9 +549,9 @@ gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k,
 
 size_t gdpa_mxfp8_scale_bytes(int B, int H, int d, int64_t T, int mode) {
   if (B < 0 || H <= 0 || T < 0 || (d != 64 && d != 128)) return 0;
-  if (mode == GDPA_MX_ALONG_CHANNELS) return static_cast<size_t>(T) * H * (d / 32);
-  if (mode == GDPA_MX_ALONG_TOKENS) return (static_cast<size_t>(B) + T / 32 + 1) * H * d;
-  return 0;
+  if ((mode & ~(GDPA_MX_ALONG_TOKENS | GDPA_MX_NOSAT)) != 0) return 0;
+  if ((mode & GDPA_MX_ALONG_TOKENS) == 0) return static_cast<size_t>(T) * H * (d / 32);
+  return (static_cast<size_t>(B) + T / 32 + 1) * H * d;
 }
 
 gdpa_status gdpa_quantize_mxfp8(const void* x, const int32_t* offsets, int B, int H, int d,
@@ -559,15 +559,16 @@ gdpa_status gdpa_quantize_mxfp8(const void* x, const int32_t* offsets, int B, in
   t_launches = 0;
   if (B < 0 || H <= 0 || T < 0) return GDPA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return GDPA_ERR_UNSUPPORTED;
-  if (mode != GDPA_MX_ALONG_CHANNELS && mode != GDPA_MX_ALONG_TOKENS) return GDPA_ERR_INVALID_ARG;
+  if ((mode & ~(GDPA_MX_ALONG_TOKENS | GDPA_MX_NOSAT)) != 0) return GDPA_ERR_INVALID_ARG;
+  const bool tokens = (mode & GDPA_MX_ALONG_TOKENS) != 0;
+  const bool nosat = (mode & GDPA_MX_NOSAT) != 0;
   if (T == 0) return GDPA_OK;
   if (x == nullptr || codes == nullptr || scales == nullptr || !aligned16(x) || !aligned16(codes))
     return GDPA_ERR_INVALID_ARG;
-  if (mode == GDPA_MX_ALONG_TOKENS && offsets == nullptr) return GDPA_ERR_INVALID_ARG;
+  if (tokens && offsets == nullptr) return GDPA_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = (mode == GDPA_MX_ALONG_CHANNELS)
-                      ? launch_quant_rows(x, T * H, d, codes, scales, s)
-                      : launch_quant_tokens(x, offsets, B, H, d, T, codes, scales, s);
+  cudaError_t e = !tokens ? launch_quant_rows(x, T * H, d, codes, scales, s, nosat)
+                          : launch_quant_tokens(x, offsets, B, H, d, T, codes, scales, s, nosat);
   if (e != cudaSuccess) return GDPA_ERR_CUDA;
   ++t_launches;
   return GDPA_OK;

@@ -255,10 +255,12 @@ cudaError_t launch_dq_convert_rope(const float* acc, void* dq, const int32_t* of
 // Zeroes p.dq_acc and, for softmax, writes p.delta = rowsum(dO * O).
 cudaError_t launch_bwd_preprocess(const BwdParams& p, bool softmax, cudaStream_t stream);
 
+// nosat: the saturation-free block scale (mx::e8m0_nosat) instead of the OCP one.
 cudaError_t launch_quant_rows(const void* x, long long rows, int d, void* codes, void* scales,
-                              cudaStream_t s);
+                              cudaStream_t s, bool nosat = false);
 cudaError_t launch_quant_tokens(const void* x, const int32_t* offsets, int B, int H, int d,
-                                long long T, void* codes, void* scales, cudaStream_t s);
+                                long long T, void* codes, void* scales, cudaStream_t s,
+                                bool nosat = false);
 
 int fwd_mx_tile_rows();
 // MXFP8 softmax backward (d = 128): operand codes and scales of each product.

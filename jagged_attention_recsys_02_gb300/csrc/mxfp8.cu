@@ -4,7 +4,9 @@
 // "GEM Training ..." low-precision paragraph: attention with end-to-end MXFP8
 // block-scaled MMA.  A block's shared scale is 2^(floor(log2 amax) - 8)
 // (8 = exponent of E4M3's largest normal, 448); elements are divided by it,
-// rounded to nearest even and saturated at +-448.
+// rounded to nearest even and saturated at +-448.  With `nosat` the scale is
+// instead the smallest power of two that keeps the block maximum at or below
+// 448 (mx::e8m0_nosat), so no element saturates.
 //
 // Two block shapes, matching the two products of attention:
 //   along channels (Q, K: the contraction of S = Q K^T runs over d): each
@@ -15,6 +17,7 @@
 //     channel).  Block r of sample b is scale row b + floor(offsets[b]/32) + r,
 //     an injective index that needs no prefix sum over samples.
 #include "common.cuh"
+#include "mx.cuh"
 
 namespace gdpa {
 namespace {
@@ -47,7 +50,7 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 // One thread per 32-channel block of one (token, head) row.
 __global__ void __launch_bounds__(256)
 quant_rows_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ codes,
-                  uint8_t* __restrict__ scales, long long nblocks) {
+                  uint8_t* __restrict__ scales, long long nblocks, bool nosat) {
   for (long long blk = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
        blk < nblocks; blk += static_cast<long long>(gridDim.x) * blockDim.x) {
     const uint4* src = reinterpret_cast<const uint4*>(x + blk * 32);
@@ -67,7 +70,7 @@ quant_rows_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ cod
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    const int code = e8m0_code(amax);
+    const int code = nosat ? mx::e8m0_nosat(amax) : e8m0_code(amax);
     const float inv = inv_scale(code);
     uint32_t out[8];
 #pragma unroll
@@ -90,7 +93,7 @@ quant_rows_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ cod
 __global__ void __launch_bounds__(128)
 quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ offsets,
                     int B, int hd, long long T, long long n_rows, uint8_t* __restrict__ codes,
-                    uint8_t* __restrict__ scales) {
+                    uint8_t* __restrict__ scales, bool nosat) {
   const long long s = blockIdx.x;
   if (s >= n_rows) {
     // Tail blocks: tokens before the first sample or after the last one have no
@@ -138,7 +141,7 @@ quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
     float inv[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      code[c] = e8m0_code(amax[c]);
+      code[c] = nosat ? mx::e8m0_nosat(amax[c]) : e8m0_code(amax[c]);
       inv[c] = inv_scale(code[c]);
     }
     uint8_t* dst = codes + tok * hd + 4 * g;
@@ -162,19 +165,20 @@ quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
 }  // namespace
 
 cudaError_t launch_quant_rows(const void* x, long long rows, int d, void* codes, void* scales,
-                              cudaStream_t s) {
+                              cudaStream_t s, bool nosat) {
   const long long nblocks = rows * (d / 32);
   if (nblocks == 0) return cudaSuccess;
   const long long want = (nblocks + 255) / 256;
   const int grid = static_cast<int>(want < 65536 ? want : 65536);
   quant_rows_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
                                          static_cast<uint8_t*>(codes),
-                                         static_cast<uint8_t*>(scales), nblocks);
+                                         static_cast<uint8_t*>(scales), nblocks, nosat);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_tokens(const void* x, const int32_t* offsets, int B, int H, int d,
-                                long long T, void* codes, void* scales, cudaStream_t s) {
+                                long long T, void* codes, void* scales, cudaStream_t s,
+                                bool nosat) {
   if (B == 0) return cudaSuccess;
   // Scale rows as counted by the buffer size: B + T/32 + 1 covers g(B-1) + ceil(L/32).
   const long long rows = static_cast<long long>(B) + T / 32 + 1;
@@ -182,7 +186,7 @@ cudaError_t launch_quant_tokens(const void* x, const int32_t* offsets, int B, in
   constexpr int kTailBlocks = 16;  // zero the codes of tokens outside every sample
   quant_tokens_kernel<<<static_cast<unsigned>(rows + kTailBlocks), 128, 0, s>>>(
       static_cast<const __nv_bfloat16*>(x), offsets, B, H * d, T, rows,
-      static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales));
+      static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales), nosat);
   return cudaGetLastError();
 }
 

@@ -190,6 +190,22 @@ def test_mxfp8_backward_rejects_on_host(lib):
     assert _bwd_mx(lib, window=-1) == INVALID
 
 
+def test_mxfp8_quantiser_modes_on_host(lib):
+    """GDPA_MX_NOSAT combines with either block shape and leaves the scale
+    buffer's size unchanged; any other mode bit is refused before a launch."""
+    sb = lib.gdpa_mxfp8_scale_bytes
+    B, H, d, T = 5, 3, 128, 1000
+    for shape in (binding.MX_ALONG_CHANNELS, binding.MX_ALONG_TOKENS):
+        assert sb(B, H, d, T, shape | binding.MX_NOSAT) == sb(B, H, d, T, shape) > 0
+    assert sb(B, H, d, T, 4) == 0 and sb(B, H, d, T, 7) == 0
+    q = lib.gdpa_quantize_mxfp8
+    assert q(FAKE, FAKE, B, H, d, T, 4, FAKE, FAKE, None) == INVALID
+    assert q(FAKE, FAKE, B, H, d, T, 8 | binding.MX_NOSAT, FAKE, FAKE, None) == INVALID
+    assert q(FAKE, None, B, H, d, T, binding.MX_ALONG_TOKENS | binding.MX_NOSAT, FAKE, FAKE,
+             None) == INVALID                       # along tokens needs the offsets
+    assert q(FAKE, FAKE, B, H, d, 0, binding.MX_NOSAT, FAKE, FAKE, None) == OK  # nothing to do
+
+
 def test_mxfp8_backward_workspace_size(lib):
     """Seven E4M3 operand versions (Q, K, dO twice, V once), their scales, the
     fp32 dQ accumulator, D and the work list."""

@@ -33,25 +33,27 @@ def _inputs(T, H, d, seed):
     return x
 
 
+@pytest.mark.parametrize("nosat", [False, True])
 @pytest.mark.parametrize("d", [64, 128])
-def test_quant_rows_bit_exact(d):
+def test_quant_rows_bit_exact(d, nosat):
     T, H = 300, 3
     x = _inputs(T, H, d, 1)
-    codes, scales = binding.quantize_mxfp8(x, mode=binding.MX_ALONG_CHANNELS)
-    rc, rs = oracle.quant_rows(to_np(x))
+    codes, scales = binding.quantize_mxfp8(x, mode=binding.MX_ALONG_CHANNELS, nosat=nosat)
+    rc, rs = oracle.quant_rows(to_np(x), nosat)
     np.testing.assert_array_equal(scales.cpu().numpy(), rs)
     np.testing.assert_array_equal(codes.cpu().numpy(), rc)
 
 
+@pytest.mark.parametrize("nosat", [False, True])
 @pytest.mark.parametrize("lengths", [[5, 40, 33, 0, 64, 1, 97], [300, 0, 31, 32, 33]])
-def test_quant_tokens_bit_exact(lengths):
+def test_quant_tokens_bit_exact(lengths, nosat):
     H, d = 2, 128
     T = sum(lengths)
     x = _inputs(T, H, d, 2)
     o = offsets(lengths)
     off = torch.from_numpy(o).to(DEV)
-    codes, scales = binding.quantize_mxfp8(x, off, mode=binding.MX_ALONG_TOKENS)
-    rc, rs = oracle.quant_cols(to_np(x), o)
+    codes, scales = binding.quantize_mxfp8(x, off, mode=binding.MX_ALONG_TOKENS, nosat=nosat)
+    rc, rs = oracle.quant_cols(to_np(x), o, nosat)
     np.testing.assert_array_equal(codes.cpu().numpy(), rc)
     # map the oracle's compact block rows onto the library's row index b + floor(o_b/32) + r
     got = scales.cpu().numpy()
@@ -90,9 +92,11 @@ from jagged_attention_recsys_02_gb300.workloads import make_tensors, make_worklo
 
 
 def _mx_fwd(q, qo, k, v, ko, causal, scale, bias=None, max_rel=0):
-    qc, qs = binding.quantize_mxfp8(q, mode=binding.MX_ALONG_CHANNELS)
-    kc, ks = binding.quantize_mxfp8(k, mode=binding.MX_ALONG_CHANNELS)
-    vc, vs = binding.quantize_mxfp8(v, ko, mode=binding.MX_ALONG_TOKENS)
+    """The MXFP8 forward on operands quantised with the saturation-free block
+    scale (GDPA_MX_NOSAT), the recipe the forward is specified with."""
+    qc, qs = binding.quantize_mxfp8(q, mode=binding.MX_ALONG_CHANNELS, nosat=True)
+    kc, ks = binding.quantize_mxfp8(k, mode=binding.MX_ALONG_CHANNELS, nosat=True)
+    vc, vs = binding.quantize_mxfp8(v, ko, mode=binding.MX_ALONG_TOKENS, nosat=True)
     Tq, H, d = q.shape
     buf, out = guarded(Tq, H, d, q.device)
     lse = torch.full((H, Tq), float("nan"), device=q.device)
@@ -103,37 +107,14 @@ def _mx_fwd(q, qo, k, v, ko, causal, scale, bias=None, max_rel=0):
     return out, lse
 
 
-def _dequant_rows(x):
-    """Oracle quantisation along channels, then back to float64 (E4M3 x 2^(s-127))."""
-    codes, scales = oracle.quant_rows(x)
-    dec = _DEC[codes]
-    return dec * np.exp2(scales.astype(np.float64) - 127).repeat(32, axis=2)
-
-
-def _dequant_tokens(x, offs):
-    codes, scales = oracle.quant_cols(x, offs)
-    dec = _DEC[codes]
-    out = np.zeros_like(dec)
-    k = 0
-    for b in range(len(offs) - 1):
-        for r in range((int(offs[b + 1]) - int(offs[b]) + 31) // 32):
-            t0 = int(offs[b]) + 32 * r
-            t1 = min(t0 + 32, int(offs[b + 1]))
-            out[t0:t1] = dec[t0:t1] * np.exp2(scales[k].astype(np.float64) - 127)[None]
-            k += 1
-    return out
-
-
-_DEC = np.array([oracle.e4m3_decode(c) for c in range(256)])
-
-
 def _mx_reference(q, k, v, qo, ko, samples, causal, scale, bias, max_rel, rows=None):
-    """fp64 oracle attention on the MXFP8 operands: the bf16 inputs quantised by the
-    oracle's own quantiser and decoded again (only P's rounding is left to the
-    kernel), plus the exact reference on the unquantised inputs for the report."""
-    qd = _dequant_rows(q)
-    kd = _dequant_rows(k)
-    vd = _dequant_tokens(v, ko)
+    """fp64 oracle attention twice: on the MXFP8 operands (the bf16 inputs
+    quantised by the oracle's own saturation-free quantiser and decoded again,
+    so only P's rounding is left to the kernel), and exactly, on the
+    unquantised inputs (the comparison the tolerance is stated for)."""
+    qd = oracle.dequant_rows(q, nosat=True)
+    kd = oracle.dequant_rows(k, nosat=True)
+    vd = oracle.dequant_cols(v, ko, nosat=True)
     mx = oracle_fwd_samples(qd, kd, vd, qo, ko, samples, "softmax", causal, scale, bias, max_rel,
                             rows=rows)
     exact = oracle_fwd_samples(q, k, v, qo, ko, samples, "softmax", causal, scale, bias, max_rel,
@@ -141,12 +122,34 @@ def _mx_reference(q, k, v, qo, ko, samples, causal, scale, bias, max_rel, rows=N
     return mx, exact
 
 
-def _report_exact(got_all, exact, what):
+def _assert_exact(pairs, what, max_frac, max_worst):
+    """The MXFP8 output against the exact fp64 forward on the unquantised bf16
+    inputs, at abs 6e-2 + rel 6e-2.  E4M3 keeps 3 mantissa bits, so at d = 128
+    the scores carry a rounding error of about 0.05 (one standard deviation);
+    on rows with a handful of keys the softmax turns that into output errors
+    near the bound, and a few elements pass it.  The assertion: at most
+    `max_frac` of the elements outside the bound and none beyond `max_worst`
+    times it.  Returns (fraction outside, worst err/bound)."""
+    bad = tot = 0
     worst = 0.0
-    for r_, o, _ in exact:
-        err = np.abs(got_all[r_] - o) / (MXFP8_TOL[0] + MXFP8_TOL[1] * np.abs(o))
-        worst = max(worst, float(err.max()) if err.size else 0.0)
-    print(f"{what}: worst err/bound against the unquantised inputs {worst:.3f}")
+    for got, ref in pairs:
+        r = np.abs(got - ref) / (MXFP8_TOL[0] + MXFP8_TOL[1] * np.abs(ref))
+        bad += int((r > 1.0).sum())
+        tot += r.size
+        worst = max(worst, float(r.max()) if r.size else 0.0)
+    frac = bad / max(tot, 1)
+    print(f"{what}: against the unquantised inputs {bad} of {tot} elements outside "
+          f"abs/rel 6e-2 (fraction {frac:.2e}), worst err/bound {worst:.3f}")
+    assert frac <= max_frac and worst <= max_worst, \
+        f"{what}: {bad} of {tot} elements outside the bound, worst {worst:.3f}"
+    return frac, worst
+
+
+# Short-key edge cases (1 to 3 keys, a bias of scale 0.5): at most 0.2% of the
+# elements may pass the bound, none by more than 3x.  The heavy-tailed
+# workload: at most 1e-5 of them, none by more than 1.5x.
+EDGE_BUDGET = (2e-3, 3.0)
+WORKLOAD_BUDGET = (1e-5, 1.5)
 
 
 def _mx_case(lq, lkv, H, causal=False, max_rel=0, seed=0):
@@ -168,7 +171,7 @@ def _mx_case(lq, lkv, H, causal=False, max_rel=0, seed=0):
     for rows, o, l in ref:
         assert_close(got[rows], o, MXFP8_TOL, f"mxfp8 out rows {rows[0]}..{rows[-1]}")
         assert_close(got_lse[:, rows], l, MXFP8_TOL, "mxfp8 lse")
-    _report_exact(got, exact, "mxfp8 case")
+    _assert_exact([(got[r_], o) for r_, o, _ in exact], "mxfp8 case", *EDGE_BUDGET)
 
 
 def test_mxfp8_fwd_ragged():
@@ -197,7 +200,10 @@ def test_mxfp8_rejects_gdpa_and_d64():
 
 def test_mxfp8_fwd_full_heavy_tail():
     """The production-like heavy-tailed mix (B=1024, log-normal lengths), softmax,
-    checked on the first, last and tile-boundary query rows of sampled samples."""
+    the workload the MXFP8 forward's tolerance is stated on.  Sampled samples:
+    every row of those up to 2048 tokens, the first, last and tile-boundary rows
+    of longer ones; against the quantisation-mirroring oracle elementwise, and
+    against the exact forward on the unquantised inputs."""
     w = make_workload("heavy_tail", act="softmax")
     t = make_tensors(w, device=DEV, with_dout=False)
     out, lse = _mx_fwd(t["q"], t["qo"], t["k"], t["v"], t["ko"], False, w.scale)
@@ -205,26 +211,27 @@ def test_mxfp8_fwd_full_heavy_tail():
     pairs = w.lq * w.lkv
     rng = np.random.default_rng(5)
     samples = sorted({int(np.argmin(pairs)), int(np.argmax(pairs)),
-                      *rng.choice(w.B, 12, replace=False).tolist()})
+                      *np.argsort(pairs)[:6].tolist(),
+                      *rng.choice(w.B, 24, replace=False).tolist()})
+    exact_pairs = []
     for b in samples:
         q0, q1, k0, k1 = int(qo[b]), int(qo[b + 1]), int(ko[b]), int(ko[b + 1])
         L = q1 - q0
-        rows = np.array(sorted({0, 1, L // 2, L - 1, *range(95, L, 96 * 5)}))
-        rows = rows[(rows >= 0) & (rows < L)]
+        if L <= 2048:
+            rows = np.arange(L)
+        else:
+            rows = np.array(sorted({0, 1, L // 2, L - 1, *range(95, L, 96 * 5)}))
         ref, exact = _mx_reference(to_np(t["q"][q0:q1]), to_np(t["k"][k0:k1]),
                                    to_np(t["v"][k0:k1]), np.array([0, L]),
                                    np.array([0, k1 - k0]), [0], False, w.scale, None, 0,
                                    rows={0: rows})
-        got_rows = {}
+        sel = torch.from_numpy(q0 + rows).to(DEV)
+        got = to_np(out[sel])
         for r, o, l in ref:
-            sel = torch.from_numpy(q0 + r).to(DEV)
-            assert_close(to_np(out[sel]), o, MXFP8_TOL, f"heavy_tail mxfp8 sample {b}")
+            assert_close(got, o, MXFP8_TOL, f"heavy_tail mxfp8 sample {b}")
             assert_close(lse[:, sel].cpu().double().numpy(), l, MXFP8_TOL, "heavy_tail mxfp8 lse")
-            got_rows[0] = to_np(out[sel])
-        for r, o, _ in exact:
-            err = np.abs(got_rows[0] - o) / (MXFP8_TOL[0] + MXFP8_TOL[1] * np.abs(o))
-            print(f"heavy_tail sample {b}: worst err/bound against the unquantised inputs "
-                  f"{float(err.max()):.3f}")
+        exact_pairs += [(got, o) for _, o, _ in exact]
+    _assert_exact(exact_pairs, "heavy_tail mxfp8", *WORKLOAD_BUDGET)
 
 
 def test_quant_tokens_zeroes_tokens_outside_samples():

@@ -42,6 +42,12 @@
  *    status word; gdpa_get_device_status() synchronises the stream, returns
  *    it and clears it.  After such an error the outputs are undefined, but
  *    every write stays inside the caller's buffers.
+ *  - Per-device state: on its first call on a device the library looks up
+ *    the device addresses of its status word and of the gdpa_fwd_noalloc
+ *    scratch array and keeps them for the life of the process.  A
+ *    cudaDeviceReset() in the caller's process unloads the library's device
+ *    code and makes those addresses stale: do not call the library on that
+ *    device after a reset.
  *
  * Entry points: gdpa_fwd / gdpa_bwd (and their _window forms; gdpa_bwd_rope
  * adds the fused rotary backward), gdpa_fwd_noalloc, the block-aligned
@@ -224,6 +230,10 @@ gdpa_status gdpa_bwd_rope(const void* q, const int32_t* q_offsets, const void* k
  * low-precision paragraph: attention with MXFP8 block-scaled MMA).  Elements
  * become E4M3 codes (round to nearest even, saturated at +-448); each block of
  * 32 elements shares an E8M0 scale 2^(floor(log2 amax) - 8), biased by 127.
+ * With GDPA_MX_NOSAT or-ed into `mode` the scale is instead the smallest power
+ * of two X with amax / X <= 448, so no element saturates (the OCP rule clips a
+ * block maximum whose mantissa is above 1.75 by up to 12.5%); this is the
+ * recipe the MXFP8 forward is specified and tested with.
  *   GDPA_MX_ALONG_CHANNELS: blocks of 32 consecutive channels of one (token,
  *     head) row (for Q and K, whose product contracts over d).
  *     codes [T][H][d] u8, scales [T][H][d/32] u8.
@@ -235,8 +245,9 @@ gdpa_status gdpa_bwd_rope(const void* q, const int32_t* q_offsets, const void* k
  *     no block are not written).  Tokens outside every sample (before
  *     offsets[0] or from offsets[B] on) get code 0.  offsets are needed only
  *     in this mode.
- * x is [T][H][d] bf16, 16-byte aligned; all buffers are device memory. */
-enum { GDPA_MX_ALONG_CHANNELS = 0, GDPA_MX_ALONG_TOKENS = 1 };
+ * x is [T][H][d] bf16, 16-byte aligned; all buffers are device memory.  Other
+ * mode bits return GDPA_ERR_INVALID_ARG (gdpa_mxfp8_scale_bytes returns 0). */
+enum { GDPA_MX_ALONG_CHANNELS = 0, GDPA_MX_ALONG_TOKENS = 1, GDPA_MX_NOSAT = 2 };
 size_t gdpa_mxfp8_scale_bytes(int B, int H, int d, int64_t T, int mode);
 gdpa_status gdpa_quantize_mxfp8(const void* x, const int32_t* offsets, int B, int H, int d,
                                 int64_t T, int mode, void* codes, void* scales, void* stream);
@@ -344,9 +355,11 @@ int gdpa_timing_collect(float* ms, int* kind, int max);
  * 131,000 work items) are refused with GDPA_ERR_WORKSPACE before anything is
  * launched.  The first call on each device looks up the array's device
  * address (cudaGetSymbolAddress); make that first call before any stream
- * capture.  All calls share the array: calls whose kernels may overlap on the
- * GPU (different streams or host threads) race and give undefined results,
- * so serialise them. */
+ * capture.  The address is kept for the life of the process: after a
+ * cudaDeviceReset() on the device it is stale, so do not call this entry
+ * point (or any other) on that device again.  All calls share the array:
+ * calls whose kernels may overlap on the GPU (different streams or host
+ * threads) race and give undefined results, so serialise them. */
 gdpa_status gdpa_fwd_noalloc(const void* q, const int32_t* q_offsets, const void* k,
                              const void* v, const int32_t* kv_offsets, int B, int H, int d,
                              int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,

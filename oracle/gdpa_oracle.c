@@ -207,16 +207,31 @@ int oracle_fwd(const double* q, const int32_t* qo, const double* k, const double
     for (int b = 0; b < B; ++b)
       if (qo[b + 1] - qo[b] != ko[b + 1] - ko[b]) return -1;
   const long Tq = qo[B];
-  const long nwork = (long)B * H;
+  /* Every output row is computed on its own, so the work is shared out in
+   * chunks of FWD_ROWS query rows of one (sample, head); the schedule does not
+   * change any row's arithmetic. */
+  enum { FWD_ROWS = 64 };
+  long nchunks = 0;
+  for (int b = 0; b < B; ++b) nchunks += (long)H * ((qo[b + 1] - qo[b] + FWD_ROWS - 1) / FWD_ROWS);
 #pragma omp parallel for schedule(dynamic, 1)
-  for (long w = 0; w < nwork; ++w) {
-    const int b = (int)(w / H), h = (int)(w % H);
+  for (long w = 0; w < nchunks; ++w) {
+    long rest = w;
+    int b = 0;
+    for (;; ++b) {
+      const long n = (long)H * ((qo[b + 1] - qo[b] + FWD_ROWS - 1) / FWD_ROWS);
+      if (rest < n) break;
+      rest -= n;
+    }
+    const long per_head = (qo[b + 1] - qo[b] + FWD_ROWS - 1) / FWD_ROWS;
+    const int h = (int)(rest / per_head);
+    const long i0 = (rest % per_head) * FWD_ROWS;
     const long Lq = qo[b + 1] - qo[b], Lkv = ko[b + 1] - ko[b];
+    const long i1 = i0 + FWD_ROWS < Lq ? i0 + FWD_ROWS : Lq;
     const long q0 = qo[b], k0 = ko[b];
     double* s = (double*)malloc(sizeof(double) * (size_t)(Lkv > 0 ? Lkv : 1));
     double* p = (double*)malloc(sizeof(double) * (size_t)(Lkv > 0 ? Lkv : 1));
     unsigned char* live = (unsigned char*)malloc((size_t)(Lkv > 0 ? Lkv : 1));
-    for (long i = 0; i < Lq; ++i) {
+    for (long i = i0; i < i1; ++i) {
       const double l = row_probs(q, k, q0 + i, k0, Lkv, H, d, h, i, bias, max_rel, dense, doff,
                                  b, Lq, act, causal, window, block, scale, s, p, live);
       double* oi = out + ((q0 + i) * H + h) * (long)d;

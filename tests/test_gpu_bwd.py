@@ -118,7 +118,47 @@ def test_bwd_tiny_config():
                    w.scale, None, 0, dq, dk, dv, "tiny")
 
 
-def _full_config(name, act=None, budget=3e6):
+def _key_rows(L):
+    """Key rows of a long sample on both sides of 64- and 128-row tile edges."""
+    rows = {0, 1, 63, 64, 127, 128, 129, 255, 256, L // 2, L // 2 + 1, L - 129, L - 128, L - 2,
+            L - 1}
+    return np.array(sorted(r for r in rows if 0 <= r < L))
+
+
+def _check_key_rows(t, w, b, dk, dv, what):
+    """dK and dV of a subset of key rows of sample b (non-causal, no bias) against
+    the oracle.  GDPA: a key's gradients depend on that key and every query only,
+    so the oracle backward on (all queries, the chosen keys) is exact for them.
+    Softmax: the oracle forward of the whole sample gives lse and D = rowsum(dO O);
+    the backward of the chosen keys is then the oracle's operand-form backward
+    on unquantised operands without rounding (the plain softmax backward)."""
+    qo, ko = w.offsets()
+    q0, q1, k0, k1 = int(qo[b]), int(qo[b + 1]), int(ko[b]), int(ko[b + 1])
+    keys = _key_rows(k1 - k0)
+    sel = torch.from_numpy(k0 + keys).to(DEV)
+    qn, don = to_np(t["q"][q0:q1]), to_np(t["dout"][q0:q1])
+    kn, vn = to_np(t["k"][sel]), to_np(t["v"][sel])
+    oq, ok = np.array([0, q1 - q0]), np.array([0, len(keys)])
+    if w.act == "softmax":
+        o_full, lse = oracle.fwd(qn, oq, to_np(t["k"][k0:k1]), to_np(t["v"][k0:k1]),
+                                 np.array([0, k1 - k0]), act=oracle.ACT_SOFTMAX, scale=w.scale)
+        delta = np.einsum("thc,thc->ht", don, o_full)
+        _, rk, rv = oracle.bwd_mx_operands(qn, qn, kn, kn, vn, don, don, oq, ok, lse, delta,
+                                           scale=w.scale, round_ps=False)
+    else:
+        _, rk, rv = oracle.bwd(qn, oq, kn, vn, ok, don, act=ACTS[w.act], scale=w.scale)
+    assert_close(to_np(dk[sel]), rk, BWD_TOL, f"{what} dk key rows of sample {b} (L={k1 - k0})")
+    assert_close(to_np(dv[sel]), rv, BWD_TOL, f"{what} dv key rows of sample {b} (L={k1 - k0})")
+
+
+def _full_config(name, act=None, budget=3e6, softmax_rows_max=8192):
+    """The full workload in the benchmark's launch configuration.  Every gradient
+    element of a deterministic subset of samples (up to `budget` query-key
+    pairs each); the longest sample in full when the workload is causal or has a
+    bias (the oracle backward of a 4096-token causal sample takes seconds);
+    otherwise dQ rows and dK / dV key rows of the longest sample (softmax: the
+    longest up to `softmax_rows_max` tokens, whose whole oracle forward is
+    needed for lse and D)."""
     w = make_workload(name, act=act)
     t = make_tensors(w, device=DEV)
     dq, dk, dv = run_bwd(t["q"], t["qo"], t["k"], t["v"], t["ko"], t["dout"], w.act, w.causal,
@@ -126,13 +166,17 @@ def _full_config(name, act=None, budget=3e6):
     qo, ko = w.offsets()
     pairs = w.lq * w.lkv
     samples = [b for b in pick_samples(w.lq, w.lkv, budget_pairs=budget) if pairs[b] <= budget]
+    longest = int(np.argmax(pairs))
+    plain = not w.causal and t["bias"] is None
+    if not plain:
+        samples.append(longest)
     if not samples:
         samples = [int(np.argmin(pairs))]
-    _check_samples(t["q"], t["k"], t["v"], t["dout"], qo, ko, samples, w.act, w.causal, w.scale,
-                   t["bias"], w.max_rel, dq, dk, dv, name)
-    if not w.causal and t["bias"] is None:
+    _check_samples(t["q"], t["k"], t["v"], t["dout"], qo, ko, sorted(set(samples)), w.act,
+                   w.causal, w.scale, t["bias"], w.max_rel, dq, dk, dv, name)
+    if plain:
         # longest sample: dQ rows are independent given all keys, so check a row subset
-        b = int(np.argmax(pairs))
+        b = longest
         q0, k0, k1 = int(qo[b]), int(ko[b]), int(ko[b + 1])
         L = int(w.lq[b])
         rows = np.array(sorted({0, 1, L // 3, L // 2, L - 2, L - 1}))
@@ -143,6 +187,12 @@ def _full_config(name, act=None, budget=3e6):
                               to_np(t["dout"][sel]), act=ACTS[w.act], causal=False,
                               scale=w.scale)
         assert_close(to_np(dq[sel]), rq, BWD_TOL, f"{name} dq rows of longest sample")
+        # dK / dV key rows of the longest sample (softmax: the longest that fits the cap)
+        if w.act == "softmax":
+            fit = np.flatnonzero(w.lq <= softmax_rows_max)
+            b = int(fit[np.argmax(pairs[fit])])
+        if pairs[b] > budget:
+            _check_key_rows(t, w, b, dk, dv, name)
 
 
 def test_bwd_full_jfa_causal_relpos():

@@ -147,6 +147,25 @@ def reduce_over_ranks(ms, flops, device=None):
     return float(t.item()), float(f.item())
 
 
+def resolve_steps(args, step, world, device, target_s=1.2, min_steps=20):
+    """--steps when given; otherwise enough steps for a timed region of about
+    target_s seconds (one warmed-up step timed with CUDA events, the slowest
+    rank's estimate shared by all)."""
+    if args.steps is not None:
+        return args.steps
+    import torch
+
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms, _ = reduce_over_ranks(e0.elapsed_time(e1), 0.0, device)
+    return max(min_steps, int(np.ceil(target_s * 1e3 / max(ms, 1e-3))))
+
+
 # ------------------------------------------------------------------ workload
 def workload_flops(w):
     f = w.fwd_flops()
@@ -209,19 +228,38 @@ def measure_padded_sdpa(w, t, dev, iters=5, max_gb=40.0):
         o.backward(do)
         q.grad = k.grad = v.grad = None
 
-    for _ in range(2):
-        once()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(iters):
-        once()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / iters
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / iters
+
+    ms = timed(once)
     fwd, bwd = workload_flops(w)
+    # The fastest padded call torch offers for this shape: no additive mask (so
+    # the flash / cuDNN kernels run), causal through is_causal, the bias dropped.
+    # It computes less than the jagged path (no bias), so it is a lower bound on
+    # the padded cost, and the speed-up against it the conservative one.
+    lb = None
+    if w.act == "softmax" and not w.window and not w.block:
+        def fast():
+            o = F.scaled_dot_product_attention(q, k, v, is_causal=bool(w.causal), scale=w.scale)
+            o.backward(do)
+            q.grad = k.grad = v.grad = None
+
+        ms_lb = timed(fast)
+        lb = {"value": (fwd + bwd) / (ms_lb * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms_lb,
+              "call": f"scaled_dot_product_attention(is_causal={bool(w.causal)}), no attn_mask",
+              "note": "lower bound on padded cost: the bias is omitted"}
     return {"value": (fwd + bwd) / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "lower_bound": lb,
             "inputs": f"zero-padded [B={B}, H={H}, Lmax, d={d}] bf16",
             "mask": (" + ".join(x for x, on in (("causal", w.causal),
                                                  (f"window {w.window}", w.window),
@@ -344,6 +382,8 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     w = make_workload(args.workload, act=args.act)
+    if args.steps is None:
+        args.steps = 20
     budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
     import oracle
 
@@ -386,6 +426,122 @@ def workload_config(w, l2_note):
                       else "none")),
             "Tq": w.Tq, "Tkv": w.Tkv, "pairs_non_padded": w.pairs(),
             "pairs_full_square": w.full_pairs(), "step": "forward + backward", "l2": l2_note}
+
+
+# ------------------------------------------------------------------ per-workload lines
+# (workload, activation, MXFP8 forward) measured beside the headline workload
+PER_WORKLOAD = (("gdpa_cross_gelu", None, False), ("gdpa_pma_silu", None, False),
+                ("heavy_tail", "softmax", False), ("heavy_tail", "silu", False),
+                ("heavy_tail", "softmax", True))
+
+
+def algorithmic_bytes(w, mx=False):
+    """Bytes a pass must move at least: forward reads q, k, v and writes out
+    (plus lse for softmax); backward reads q, k, v, out, dout (plus lse and D)
+    and writes dq, dk, dv.  bf16 rows of H*d elements; MXFP8 operands are one
+    byte per element plus one scale byte per 32."""
+    row = w.H * w.d * 2
+    stats = 4 * w.H * w.Tq if w.act == "softmax" else 0
+    op = (w.H * w.d * 33 // 32) if mx else row
+    fwd = op * (w.Tq + 2 * w.Tkv) + row * w.Tq + stats
+    bwd = row * (4 * w.Tq + 4 * w.Tkv) + 2 * stats
+    return fwd, bwd
+
+
+def roofline_for(flops, nbytes, ms, tensor_peak, hbm_gbs):
+    """min(tensor peak, arithmetic intensity x HBM bandwidth) and the fraction
+    of it reached."""
+    achieved = flops / (ms * 1e-3) / 1e12
+    bound_hbm = flops / nbytes * hbm_gbs / 1e3
+    peak = min(tensor_peak, bound_hbm)
+    return {"achieved_tflops": achieved, "roofline_tflops": peak,
+            "bound": "tensor" if tensor_peak <= bound_hbm else "hbm",
+            "ai_flop_per_byte": flops / nbytes, "algorithmic_bytes": nbytes,
+            "frac": achieved / peak}
+
+
+def measure_workload(name, act, mx, dev, gpu_index, steps, warmup):
+    """Forward and backward (MXFP8: quantise + forward) of one workload through
+    the C ABI: per-kernel CUDA-event times, TFLOPS on non-padded FLOPs and the
+    fraction of the workload's roofline; clocks sampled during the timing."""
+    import torch
+
+    from jagged_attention_recsys_02_gb300 import binding
+    from jagged_attention_recsys_02_gb300.workloads import ACTS, make_tensors, make_workload
+
+    w = make_workload(name, act=act)
+    t = make_tensors(w, device=dev, with_dout=not mx)
+    H, d, Tq, Tkv = w.H, w.d, w.Tq, w.Tkv
+    out = torch.empty_like(t["q"])
+    lse = torch.empty((H, Tq), device=dev, dtype=torch.float32)
+    ws_f = torch.empty(binding.fwd_workspace_size(w.B, H, d, Tq, Tkv), device=dev,
+                       dtype=torch.uint8)
+    kw = dict(act=ACTS[w.act], causal=w.causal, scale=w.scale, bias=t["bias"], max_rel=w.max_rel)
+    if mx:
+        qc, qs = binding.quantize_mxfp8(t["q"], mode=binding.MX_ALONG_CHANNELS, nosat=True)
+        kc, ks = binding.quantize_mxfp8(t["k"], mode=binding.MX_ALONG_CHANNELS, nosat=True)
+        vc, vs = binding.quantize_mxfp8(t["v"], t["ko"], mode=binding.MX_ALONG_TOKENS, nosat=True)
+
+        def step():
+            binding.quantize_mxfp8(t["q"], mode=binding.MX_ALONG_CHANNELS, nosat=True, codes=qc,
+                                   scales=qs)
+            binding.quantize_mxfp8(t["k"], mode=binding.MX_ALONG_CHANNELS, nosat=True, codes=kc,
+                                   scales=ks)
+            binding.quantize_mxfp8(t["v"], t["ko"], mode=binding.MX_ALONG_TOKENS, nosat=True,
+                                   codes=vc, scales=vs)
+            binding.gdpa_fwd_mxfp8(qc, qs, t["qo"], kc, ks, vc, vs, t["ko"], causal=w.causal,
+                                   scale=w.scale, out=out, lse=lse, workspace=ws_f)
+    else:
+        dq, dk, dv = (torch.empty_like(t[n_]) for n_ in ("q", "k", "v"))
+        ws_b = torch.empty(binding.bwd_workspace_size(w.B, H, d, Tq, Tkv), device=dev,
+                           dtype=torch.uint8)
+
+        def step():
+            binding.gdpa_fwd(t["q"], t["qo"], t["k"], t["v"], t["ko"], out=out, lse=lse,
+                             workspace=ws_f, **kw)
+            binding.gdpa_bwd(t["q"], t["qo"], t["k"], t["v"], t["ko"], out, lse, t["dout"],
+                             dq=dq, dk=dk, dv=dv, workspace=ws_b, **kw)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if binding.device_status() != 0:
+        raise RuntimeError(f"device status after warm-up of {name}")
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    binding.timing_enable(True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    binding.timing_enable(False)
+    clk = clocks.stop()
+    if binding.device_status() != 0:
+        raise RuntimeError(f"device status after timing {name}")
+    fwd_ms, bwd_ms = binding.timing_collect()
+    peaks, src = load_peaks()
+    bf16 = float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
+    fwd_flops, bwd_flops = workload_flops(w)
+    fb, bb = algorithmic_bytes(w, mx)
+    res = {"config": workload_config(w, "inputs larger than L2 (no flush)"),
+           "ms_per_step": e0.elapsed_time(e1) / steps, "steps": steps, "warmup": warmup,
+           "clocks": clk, "peaks": f"{src}: bf16 {bf16} TFLOP/s"
+                                   f"{' (x2 for FP8)' if mx else ''}, HBM {hbm} GB/s"}
+    f_avg = float(np.mean(fwd_ms))
+    res["fwd"] = dict(kernel_ms=f_avg, **roofline_for(fwd_flops, fb, f_avg,
+                                                      2 * bf16 if mx else bf16, hbm))
+    if not mx:
+        b_avg = float(np.mean(bwd_ms))
+        res["bwd"] = dict(kernel_ms=b_avg, **roofline_for(bwd_flops, bb, b_avg, bf16, hbm))
+        res["step_tflops"] = (fwd_flops + bwd_flops) / (res["ms_per_step"] * 1e-3) / 1e12
+    else:
+        res["step_tflops"] = fwd_flops / (res["ms_per_step"] * 1e-3) / 1e12
+        res["config"]["step"] = "MXFP8 quantise Q,K,V (saturation-free scales) + forward"
+    return res
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -456,6 +612,7 @@ def run_gpu(args, rank, world, local_rank):
     st = binding.device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
+    args.steps = resolve_steps(args, lambda: step(*args_dev), world, dev)
 
     clocks = ClockSampler(local_rank)
     clocks.start()
@@ -636,6 +793,20 @@ def run_gpu(args, rank, world, local_rank):
         sdpa = measure_padded_sdpa(w, t, dev)
         if sdpa.get("value"):
             sdpa["jagged_over_padded"] = value / sdpa["value"]
+        if sdpa.get("lower_bound"):
+            sdpa["jagged_over_padded_lower_bound"] = value / sdpa["lower_bound"]["value"]
+
+    # Every other configuration of the benchmark suite, timed on the same GPU
+    # in the same run (default workload only, one GPU).
+    per_workload = None
+    if rank == 0 and world == 1 and args.per_workload:
+        del t
+        torch.cuda.empty_cache()
+        per_workload = {}
+        for name, act, mx in PER_WORKLOAD:
+            per_workload[f"{name}/{'mxfp8' if mx else act}"] = measure_workload(
+                name, act, mx, dev, local_rank, steps=5, warmup=3)
+            torch.cuda.empty_cache()
 
     in_bytes = sum(x.numel() * x.element_size() for x in (t["q"], t["k"], t["v"], t["dout"]))
     line = {
@@ -670,6 +841,8 @@ def run_gpu(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "padded_sdpa": sdpa,
     }
+    if per_workload is not None:
+        line["per_workload"] = per_workload
     if swa is not None:
         line["swa_vs_full"] = swa
     if rank == 0:
@@ -711,17 +884,21 @@ def run_gpu_mxfp8(args, rank, world, local_rank):
         ws_b = torch.empty(binding.bwd_mxfp8_workspace_size(w.B, H, d, Tq, Tkv), device=dev,
                            dtype=torch.uint8)
         dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
-    qc, qs = binding.quantize_mxfp8(t["q"], mode=binding.MX_ALONG_CHANNELS)
-    kc, ks = binding.quantize_mxfp8(t["k"], mode=binding.MX_ALONG_CHANNELS)
-    vc, vs = binding.quantize_mxfp8(t["v"], t["ko"], mode=binding.MX_ALONG_TOKENS)
+    # the saturation-free block scale (GDPA_MX_NOSAT), the recipe the forward is tested with
+    qc, qs = binding.quantize_mxfp8(t["q"], mode=binding.MX_ALONG_CHANNELS, nosat=True)
+    kc, ks = binding.quantize_mxfp8(t["k"], mode=binding.MX_ALONG_CHANNELS, nosat=True)
+    vc, vs = binding.quantize_mxfp8(t["v"], t["ko"], mode=binding.MX_ALONG_TOKENS, nosat=True)
 
     def step():
         n = 0
-        binding.quantize_mxfp8(t["q"], mode=binding.MX_ALONG_CHANNELS, codes=qc, scales=qs)
+        binding.quantize_mxfp8(t["q"], mode=binding.MX_ALONG_CHANNELS, nosat=True, codes=qc,
+                               scales=qs)
         n += binding.last_launch_count()
-        binding.quantize_mxfp8(t["k"], mode=binding.MX_ALONG_CHANNELS, codes=kc, scales=ks)
+        binding.quantize_mxfp8(t["k"], mode=binding.MX_ALONG_CHANNELS, nosat=True, codes=kc,
+                               scales=ks)
         n += binding.last_launch_count()
-        binding.quantize_mxfp8(t["v"], t["ko"], mode=binding.MX_ALONG_TOKENS, codes=vc, scales=vs)
+        binding.quantize_mxfp8(t["v"], t["ko"], mode=binding.MX_ALONG_TOKENS, nosat=True, codes=vc,
+                               scales=vs)
         n += binding.last_launch_count()
         binding.gdpa_fwd_mxfp8(qc, qs, t["qo"], kc, ks, vc, vs, t["ko"], causal=w.causal,
                                scale=w.scale, bias=t["bias"], max_rel=w.max_rel, window=w.window,
@@ -740,6 +917,7 @@ def run_gpu_mxfp8(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if binding.device_status() != 0:
         raise RuntimeError("device status after warm-up")
+    args.steps = resolve_steps(args, step, world, dev)
     clocks = ClockSampler(local_rank)
     clocks.start()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -807,7 +985,8 @@ def run_gpu_mxfp8(args, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for a timed region of about 1.2 s)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gdpa", choices=["gdpa", "reference"])
     ap.add_argument("--workload", default=None,
@@ -821,12 +1000,16 @@ def main():
     ap.add_argument("--no-sdpa", action="store_true",
                     help="skip the padded torch SDPA comparison")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-per-workload", dest="per_workload", action="store_false",
+                    help="skip the other configurations' forward / backward lines")
     ap.add_argument("--mxfp8", action="store_true",
                     help="time the MXFP8 forward path (quantise + block-scaled forward) instead")
     ap.add_argument("--mxfp8-bwd", action="store_true",
                     help="time the MXFP8 training step (forward + backward, all block-scaled)")
     args = ap.parse_args()
     args.mxfp8 = args.mxfp8 or args.mxfp8_bwd
+    # the other configurations are measured beside the default workload only
+    args.per_workload = args.per_workload and args.workload is None and not args.samples
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     rank = int(os.environ.get("RANK", "0"))

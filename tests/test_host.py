@@ -185,3 +185,27 @@ def test_traffic_table_is_well_formed():
     valid = bench.load_traffic()
     assert set(valid) <= set(table)
     assert all(valid[k] == table[k]["bytes"] for k in valid)
+
+
+def test_roofline_arithmetic_of_the_per_workload_lines():
+    """The per-workload roofline: algorithmic bytes counted from the tensors a
+    pass must read and write, and min(tensor peak, intensity x HBM)."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    w = make_workload("gdpa_pma_silu")
+    row = w.H * w.d * 2
+    f, b = bench.algorithmic_bytes(w)
+    assert f == row * (2 * w.Tq + 2 * w.Tkv)               # q, k, v read; out written
+    assert b == row * (4 * w.Tq + 4 * w.Tkv)               # q, k, v, out, dout; dq, dk, dv
+    ws = make_workload("jfa_causal_relpos")
+    f2, b2 = bench.algorithmic_bytes(ws)
+    assert f2 == ws.H * ws.d * 2 * 4 * ws.Tq + 4 * ws.H * ws.Tq   # + lse
+    fm, _ = bench.algorithmic_bytes(ws, mx=True)
+    assert fm < f2                                          # one-byte operands
+    # HBM-bound: 1e12 FLOP over 1e10 bytes at 1000 GB/s -> 100 TFLOP/s ceiling
+    r = bench.roofline_for(1e12, 1e10, 20.0, tensor_peak=2000.0, hbm_gbs=1000.0)
+    assert r["bound"] == "hbm" and abs(r["roofline_tflops"] - 100.0) < 1e-9
+    assert abs(r["achieved_tflops"] - 50.0) < 1e-9 and abs(r["frac"] - 0.5) < 1e-12
+    r = bench.roofline_for(1e12, 1e8, 1.0, tensor_peak=2000.0, hbm_gbs=1000.0)
+    assert r["bound"] == "tensor" and r["roofline_tflops"] == 2000.0

@@ -796,17 +796,6 @@ def run_gpu(args, rank, world, local_rank):
         if sdpa.get("lower_bound"):
             sdpa["jagged_over_padded_lower_bound"] = value / sdpa["lower_bound"]["value"]
 
-    # Every other configuration of the benchmark suite, timed on the same GPU
-    # in the same run (default workload only, one GPU).
-    per_workload = None
-    if rank == 0 and world == 1 and args.per_workload:
-        del t
-        torch.cuda.empty_cache()
-        per_workload = {}
-        for name, act, mx in PER_WORKLOAD:
-            per_workload[f"{name}/{'mxfp8' if mx else act}"] = measure_workload(
-                name, act, mx, dev, local_rank, steps=5, warmup=3)
-            torch.cuda.empty_cache()
 
     in_bytes = sum(x.numel() * x.element_size() for x in (t["q"], t["k"], t["v"], t["dout"]))
     line = {
@@ -841,7 +830,16 @@ def run_gpu(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "padded_sdpa": sdpa,
     }
-    if per_workload is not None:
+    # Every other configuration of the benchmark suite, timed on the same GPU
+    # in the same run (default workload only, one GPU).
+    if rank == 0 and world == 1 and args.per_workload:
+        del t, args_dev
+        torch.cuda.empty_cache()
+        per_workload = {}
+        for name, act, mx in PER_WORKLOAD:
+            per_workload[f"{name}/{'mxfp8' if mx else act}"] = measure_workload(
+                name, act, mx, dev, local_rank, steps=5, warmup=3)
+            torch.cuda.empty_cache()
         line["per_workload"] = per_workload
     if swa is not None:
         line["swa_vs_full"] = swa

@@ -22,8 +22,8 @@
 //
 // Per tile t, on the tensor pipe (one issuing thread, in this order):
 //   P(t) ready   -> dV(t) += P^T dO,  S(t+1) = K Q(t+1)^T
-//   dS(t) ready  -> dK(t) += dS^T Q,  dQ^T(t) = K^T dS^T (into the dP columns)
-//   dQ^T read    -> dP(t+1) = V dO(t+1)^T
+//   dS(t) ready  -> dQ^T(t) = K^T dS^T (into the dP columns),  dK(t) += dS^T Q
+//   dQ^T read    -> dP(t+1) = V dO(t+1)^T  (the read overlaps dK(t))
 // The dQ group reads the whole dQ^T tile into registers (128 per thread, from
 // a register reallocation between warpgroups) so the dP columns free up at
 // once, then adds it into the fp32 dQ accumulator in 16-query boxes with bulk
@@ -462,6 +462,14 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           if (!mbar_wait(bar(C::kDsFull), pc & 1u, abort_flag)) { ok = false; fail(); break; }
           ++pc;
           tc_fence_after();
+          // dQ^T = K^T dS^T into the dP columns (dP(t) has been read by now).
+          // Issued before dK: the dQ group drains dQ^T while dK runs, so the
+          // columns are free again for dP(t+1) about when dK(t) completes.
+#pragma unroll
+          for (int ks = 0; ks < kKRows / 16; ++ks)
+            mma_f16_ss(tmem + kColDP, dadd(dsc_kt, ks * 2048), dadd(dsc_dsmn, ks * 2048), idesc_dq,
+                       ks > 0 ? 1u : 0u);
+          mma_commit(bar(C::kDqFull));
           // dK += dS^T Q   (A = dS^T K-major, B = Q MN-major)
           const uint64_t qmn = dadd(dsc_qmn, s * C::kQTileBytes);
 #pragma unroll
@@ -469,12 +477,6 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
             mma_f16_ss(tmem + kColDK, dadd(dsc_ds, (ks / 4) * C::kAtom + (ks % 4) * 32),
                        dadd(qmn, ks * 2048), idesc_acc, (t == 0 && ks == 0) ? 0u : 1u);
           mma_commit(bar(C::kQEmpty + s));
-          // dQ^T = K^T dS^T into the dP columns (dP(t) has been read by now)
-#pragma unroll
-          for (int ks = 0; ks < kKRows / 16; ++ks)
-            mma_f16_ss(tmem + kColDP, dadd(dsc_kt, ks * 2048), dadd(dsc_dsmn, ks * 2048), idesc_dq,
-                       ks > 0 ? 1u : 0u);
-          mma_commit(bar(C::kDqFull));
           dq_pending = true;
           if (t + 1 < in.nq && !issue_dp()) { ok = false; fail(); break; }
         }
@@ -549,9 +551,8 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         uint32_t pp[32];
         {
           const int c0 = 64 * grp;
-          uint32_t sr[2][32];  // both halves first: more independent work per warp
-          tmem_ld32(tmem + lane_off + kColS + c0, sr[0]);
-          tmem_ld32(tmem + lane_off + kColS + c0 + 32, sr[1]);
+          uint32_t sr[64];  // the group's 64 columns in one load and one wait
+          tmem_ld64(tmem + lane_off + kColS + c0, sr);
           // One straight-line body per (masked, bias) case.
           auto body = [&](auto masked, auto biased) {
             constexpr bool kMask = decltype(masked)::value;
@@ -579,7 +580,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
                 off[0] = add_f32x2(make_float2(bv[0], bv[1]), off[0]);
                 off[1] = add_f32x2(make_float2(bv[2], bv[3]), off[1]);
               }
-              const uint32_t* sq = &sr[q4 / 8][4 * (q4 % 8)];
+              const uint32_t* sq = &sr[4 * q4];
               const float2 x01 = fma_f32x2(make_float2(__uint_as_float(sq[0]), __uint_as_float(sq[1])),
                                            make_float2(c_s, c_s), off[0]);
               const float2 x23 = fma_f32x2(make_float2(__uint_as_float(sq[2]), __uint_as_float(sq[3])),
@@ -698,10 +699,11 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         if (!all_ok) { if (lane == 0) fail(); abort_now = true; break; }
         ++dqc;
         tc_fence_after();
-        // The whole dQ^T tile (channel r, 128 queries) into registers first.
-        uint32_t v[4][32];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) tmem_ld32(tmem + lane_off + kColDP + 32 * i, v[i]);
+        // The whole dQ^T tile (channel r, 128 queries) into registers first, in
+        // two loads of 64 columns (two waits).
+        uint32_t v[128];
+        tmem_ld64(tmem + lane_off + kColDP, *reinterpret_cast<uint32_t(*)[64]>(&v[0]));
+        tmem_ld64(tmem + lane_off + kColDP + 64, *reinterpret_cast<uint32_t(*)[64]>(&v[64]));
         tc_fence_before();
         warp_arrive(bar(C::kDqEmpty), lane);  // the dP columns are free again
         // Stage 16-query chunks as [query][channel] and add each into the fp32
@@ -721,7 +723,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
             float* stg = reinterpret_cast<float*>(gbase + C::kDqStage + buf * C::kDqStageBytes);
 #pragma unroll
             for (int c = 0; c < kDqChunk; ++c)
-              stg[c * D + r] = __uint_as_float(v[(ch * kDqChunk + c) / 32][(ch * kDqChunk + c) % 32]);
+              stg[c * D + r] = __uint_as_float(v[ch * kDqChunk + c]);
             fence_proxy_async_smem();
           }
           named_bar_sync(1, 128);
@@ -833,8 +835,14 @@ cudaError_t launch_sm(const BwdParams& p, const CUtensorMap& tq, const CUtensorM
                       int grid, cudaStream_t s) {
   using C = SmCfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(bwd_sm_kernel<D, kBand, kDBias, kDense, kRope>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  // The register split (setmaxnreg) hands out exactly the launch's pool of
+  // 128 per thread: refuse a build that launched with fewer.
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, bwd_sm_kernel<D, kBand, kDBias, kDense, kRope>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != 128) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(bwd_sm_kernel<D, kBand, kDBias, kDense, kRope>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   bwd_sm_kernel<D, kBand, kDBias, kDense, kRope><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo,
                                                                                    tdq, p);

@@ -284,6 +284,41 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr)
       : "memory");
 }
+// 64 and 128 consecutive columns in one instruction and one wait: a row's
+// whole score tile reaches the registers after a single TMEM round trip
+// instead of one per 32 columns.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : GDPA_R8(0), GDPA_R8(8), GDPA_R8(16), GDPA_R8(24), GDPA_R8(32), GDPA_R8(40),
+        GDPA_R8(48), GDPA_R8(56)
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,"
+      "%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+      "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,"
+      "%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+      "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127},"
+      " [%128];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : GDPA_R8(0), GDPA_R8(8), GDPA_R8(16), GDPA_R8(24), GDPA_R8(32), GDPA_R8(40),
+        GDPA_R8(48), GDPA_R8(56), GDPA_R8(64), GDPA_R8(72), GDPA_R8(80), GDPA_R8(88),
+        GDPA_R8(96), GDPA_R8(104), GDPA_R8(112), GDPA_R8(120)
+      : "r"(taddr)
+      : "memory");
+}
 #undef GDPA_R8
 
 #define GDPA_W8(b) "r"(r[b + 0]), "r"(r[b + 1]), "r"(r[b + 2]), "r"(r[b + 3]), \
@@ -351,6 +386,12 @@ __device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
 }
 
 // ---------------------------------------------------------------- math
+// Largest of three values in one instruction (three-input max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -10,7 +10,8 @@ tests run gdpa_fwd / gdpa_bwd (forward: blocks of 256 query rows over
 the list against a host count made row by row from the mask's definition:
 
   * every (sample, head, block) with rows appears exactly once, and nothing else;
-  * a sample's items are contiguous, blocks in descending cost, heads innermost;
+  * a sample's items are contiguous, heads innermost, and without a window
+    its blocks come in descending cost;
   * the samples' total costs do not increase along the list (exactly below
     1024 inner tiles, in 64-tile steps above, the scheduler's histogram);
   * a block's cost is 1 + the number of inner tiles holding a key (query)
@@ -90,7 +91,8 @@ def _check(lq, lkv, H, causal, window, mode, samples, blocks, heads):
     totals = []
     for b, blks in order:
         costs = [cost_fn(lq[b], lkv[b], blk, causal, window) for blk in blks]
-        assert all(x >= y for x, y in zip(costs, costs[1:])), f"sample {b}: blocks not by cost"
+        if not window:  # a window makes the costs nearly flat; the order is then the plain one
+            assert all(x >= y for x, y in zip(costs, costs[1:])), f"sample {b}: blocks not by cost"
         totals.append(sum(costs))
     buckets = [_bucket(t) for t in totals]
     assert all(x >= y for x, y in zip(buckets, buckets[1:])), "samples not longest first"

@@ -5,7 +5,8 @@
 // JFA paragraph: operate directly on jagged tensors with no padding, with
 // custom attention biases and asymmetric query / key lengths.
 //
-// Design (one persistent CTA per SM, warp-specialised, 320 threads):
+// Design (one persistent CTA per SM, warp-specialised, 384 threads = three
+// warpgroups):
 //   warps 0-3   "softmax group 0": query rows [0,128) of the item
 //   warps 4-7   "softmax group 1": query rows [128,256) of the item
 //   warp  8     TMA producer: pulls work items from the cost-sorted list
@@ -13,6 +14,11 @@
 //               ring of shared-memory stages
 //   warp  9     MMA issuer: tcgen05.mma S_h = Q_h K^T into TMEM, then
 //               O_h += P_h V with P_h read from TMEM
+//   warps 10-11 idle
+// Registers: each SM sub-partition holds 16384; the launch gives every thread
+// 168 (three warps per sub-partition), then the activation warpgroups rise to
+// 200 and the producer / MMA warpgroup drops to 104 (setmaxnreg), so a row's
+// 128 scores and their exponentials stay in registers without spilling.
 // TMEM (512 columns): half h owns S/P columns [256h, 256h+128) and O columns
 // [256h+128, 256h+128+d).  The activation group reads S row by row (TMEM lane
 // = query row), applies scale, bias, mask and the activation in registers
@@ -39,9 +45,13 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kActWarps = 8;
+constexpr int kRegsAct = 200;  // activation warpgroups
+constexpr int kRegsLow = 104;  // producer / MMA warpgroup
+static_assert(2 * kRegsAct + kRegsLow == 3 * 168, "register split must keep the launch total");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -216,6 +226,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer (whole warp)
+    setmaxnreg_dec<kRegsLow>();
     // Lane 0 takes tickets and issues the TMA copies; all lanes stage the
     // bias windows of each key tile (when there is a bias).
     const int n_items = *p.n_items;
@@ -344,6 +355,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    setmaxnreg_dec<kRegsLow>();
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_f16(128, 128, true, false, false);
       constexpr uint32_t idesc_pv = idesc_f16(128, D, true, false, true);
@@ -444,8 +456,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         mbar_wait(bar(C::kDrain), 0, nullptr, 100000000ull);
       }
     }
-  } else {
+  } else if (warp < kActWarps) {
     // ------------------------------------------------------------ activation groups
+    setmaxnreg_inc<kRegsAct>();
     const int half = warp >> 2;                 // 0 or 1
     const int wq = warp & 3;                    // TMEM lane quarter
     const int row_in_half = wq * 32 + lane;     // TMEM lane = query row of the half
@@ -510,10 +523,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         tc_fence_after();
         const int c0 = j * kKvRows;
         const bool need_mask = (kBand && c0 < col_lo) || (c0 + kKvRows > col_lim);
-        // Scores need only the scale when no row of the warp needs a mask and there
-        // is no bias.  Decided per warp: the tcgen05.ld below is .sync.aligned, so
-        // the lanes of a warp must not split between the two paths.
-        const bool plain = !has_bias && !kDense && __all_sync(0xffffffffu, !need_mask);
+        // Scores need only the scale when no row of the warp needs a mask, there
+        // is no bias and the scale is positive (the raw maximum times the scale is
+        // then the scaled maximum).  Decided per warp: the tcgen05.ld below is
+        // .sync.aligned, so the lanes of a warp must not split between the two paths.
+        const bool plain =
+            !has_bias && !kDense && c_s > 0.0f && __all_sync(0xffffffffu, !need_mask);
         // bwin[cc] = bias(row, tile column cc) (times log2e for softmax): the
         // window copy shifted by (row + 1) % 2 holds this row's 128 entries in
         // increasing column order from an 8-byte aligned position.
@@ -566,19 +581,48 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
           // read once.  Plain tiles keep raw scores (scale folded into the exponent).
           float xs[kKvRows];
           float mt = -INFINITY;
-          if (plain) {
+          if (!kDense) {
+            // One TMEM load of all 128 columns (one wait), scale and bias in
+            // place, then the row maximum with three-input max instructions in
+            // four independent chains.
+            uint32_t sr[kKvRows];
+            tmem_ld128(t_s, sr);
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (plain) {
 #pragma unroll
-            for (int chunk = 0; chunk < 4; ++chunk) {
-              uint32_t sr[32];
-              tmem_ld32(t_s + chunk * 32, sr);
+              for (int i = 0; i < kKvRows; ++i) xs[i] = __uint_as_float(sr[i]);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                xs[chunk * 32 + i] = __uint_as_float(sr[i]);
-                m4[i & 3] = fmaxf(m4[i & 3], xs[chunk * 32 + i]);
+              for (int i = 0; i < kKvRows; i += 2)
+                m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], xs[i], xs[i + 1]);
+              mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c_s;
+            } else {
+              const float2 cc = make_float2(c_s, c_s);
+#pragma unroll
+              for (int q4 = 0; q4 < kKvRows / 4; ++q4) {
+                float2 b01 = make_float2(0.f, 0.f), b23 = make_float2(0.f, 0.f);
+                if (has_bias) {
+                  b01 = *reinterpret_cast<const float2*>(bwin + 4 * q4);
+                  b23 = *reinterpret_cast<const float2*>(bwin + 4 * q4 + 2);
+                }
+                const float2 x01 = fma_f32x2(make_float2(__uint_as_float(sr[4 * q4]), __uint_as_float(sr[4 * q4 + 1])), cc, b01);
+                const float2 x23 = fma_f32x2(make_float2(__uint_as_float(sr[4 * q4 + 2]), __uint_as_float(sr[4 * q4 + 3])), cc, b23);
+                xs[4 * q4] = x01.x;
+                xs[4 * q4 + 1] = x01.y;
+                xs[4 * q4 + 2] = x23.x;
+                xs[4 * q4 + 3] = x23.y;
               }
+              if (need_mask) {
+#pragma unroll
+                for (int i = 0; i < kKvRows; ++i) {
+                  const int c = c0 + i;
+                  if ((kBand && c < col_lo) || c >= col_lim) xs[i] = -INFINITY;
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < kKvRows; i += 2)
+                m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], xs[i], xs[i + 1]);
+              mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             }
-            mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c_s;
           } else {
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -667,17 +711,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         ++ocount;
         tc_fence_after();
 #pragma unroll 1
-        for (int chunk = 0; chunk < D / 32; ++chunk) {
-          uint32_t o[32];
-          tmem_ld32(t_o + chunk * 32, o);
-          uint32_t pk[16];
+        for (int chunk = 0; chunk < D / 64; ++chunk) {
+          uint32_t o[64];
+          tmem_ld64(t_o + chunk * 64, o);
+          uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
+          for (int i = 0; i < 32; ++i)
             pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
           if (row_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + chunk * 32);
+            uint4* dst = reinterpret_cast<uint4*>(orow + chunk * 64);
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
+            for (int v = 0; v < 8; ++v)
               dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           }
         }
@@ -691,6 +735,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         p.lse[static_cast<long long>(in.head) * p.Tq + in.q0 + r] = lse;
       }
     }
+  } else {
+    setmaxnreg_dec<kRegsLow>();  // warps 10-11: no role
   }
 
   tc_fence_before();
@@ -705,8 +751,15 @@ template <int D, int ACT, bool kBand, bool kDense>
 cudaError_t launch_one(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, int grid, cudaStream_t stream) {
   const int smem = FwdCfg<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, ACT, kBand, kDense>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // The register split (setmaxnreg) hands out exactly the launch's pool of
+  // 168 per thread: a build that launched with fewer would leave the
+  // activation warps waiting for registers, so refuse to launch it.
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, fwd_kernel<D, ACT, kBand, kDense>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != (2 * kRegsAct + kRegsLow) / 3) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(fwd_kernel<D, ACT, kBand, kDense>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   fwd_kernel<D, ACT, kBand, kDense><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();

@@ -26,8 +26,10 @@
 //   dQ^T read    -> dP(t+1) = V dO(t+1)^T  (the read overlaps dK(t))
 // The dQ group reads the whole dQ^T tile into registers (128 per thread, from
 // a register reallocation between warpgroups) so the dP columns free up at
-// once, then adds it into the fp32 dQ accumulator in 16-query boxes with bulk
-// tensor reduce-adds from a small shared staging buffer.
+// once, then adds it into the fp32 dQ accumulator with bulk tensor
+// reduce-adds: each warp stages its own 32 channels of 16 queries in one of
+// three small shared buffers and issues its own reduce, so the four warps
+// never wait for each other.
 // The activation warps run two phases per tile: P from S (stored back into
 // TMEM for the dV product, kept in registers as bf16), then dS from dP
 // (stored to shared memory for the dK and dQ products).
@@ -80,12 +82,12 @@ struct SmCfg {
   static constexpr int kBiasCopy = 270;
   static constexpr int kStatFloats = 2 * kQRows + 2 * kBiasCopy + 4;  // (16-byte multiple)
   static constexpr int kStats = kDs + kDsBytes;
-  static constexpr int kDqStageBytes = kDqChunk * D * 4;       // [16 queries][d] fp32
-  static constexpr int kDqStage = kStats + kQStages * kStatFloats * 4;  // two buffers
+  static constexpr int kDqStage = kStats + kQStages * kStatFloats * 4;  // per-warp buffers
   // bias-table gradient: per tile, dS summed along its 255 diagonals (two
   // buffers of 256 floats, then {first diagonal, head})
   static constexpr int kDbBuf = 256 * 4 + 16;
-  static constexpr int kDb = kDqStage + 2 * kDqStageBytes;
+  static constexpr int kDqWarpBufs = 3;                    // per warp: [16 queries][32 channels]
+  static constexpr int kDb = kDqStage + 4 * kDqWarpBufs * kDqChunk * 32 * 4;
   static constexpr int kBar = kDb + 2 * kDbBuf;
   static constexpr int kKvFull = 0, kKvEmpty = 1;
   static constexpr int kQFull = 2;                    // + stage
@@ -713,22 +715,25 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         // past Tq are clipped by the copy.
         const int qloc = (in.qt0 + t) * kQRows;
         const int qrow = in.q0 + qloc;
+        // each warp reduces its own 32 channels: no group barrier
+        const uint32_t wstage = sbase + C::kDqStage + wq * C::kDqWarpBufs * (kDqChunk * 32 * 4);
+        float* wstg = reinterpret_cast<float*>(gbase + C::kDqStage) + wq * C::kDqWarpBufs * (kDqChunk * 32);
 #pragma unroll
         for (int ch = 0; ch < kQRows / kDqChunk; ++ch) {
           if (qloc + ch * kDqChunk >= in.Lq) break;  // uniform across the group
-          const int buf = dq_issue & 1;
-          if (r == 0) bulk_wait_group_read<1>();  // buffer `buf` is free again
-          named_bar_sync(1, 128);
-          if (r < D) {
-            float* stg = reinterpret_cast<float*>(gbase + C::kDqStage + buf * C::kDqStageBytes);
+          const int buf = dq_issue % C::kDqWarpBufs;
+          if (lane == 0) bulk_wait_group_read<C::kDqWarpBufs - 1>();
+          __syncwarp();
+          if (32 * wq < D) {
+            float* stg = wstg + buf * (kDqChunk * 32);
 #pragma unroll
             for (int c = 0; c < kDqChunk; ++c)
-              stg[c * D + r] = __uint_as_float(v[ch * kDqChunk + c]);
+              stg[c * 32 + lane] = __uint_as_float(v[ch * kDqChunk + c]);
             fence_proxy_async_smem();
           }
-          named_bar_sync(1, 128);
-          if (r == 0) {
-            tma_reduce_add_3d(&tmap_dq, sbase + C::kDqStage + buf * C::kDqStageBytes, 0, in.head,
+          __syncwarp();
+          if (lane == 0 && 32 * wq < D) {
+            tma_reduce_add_3d(&tmap_dq, wstage + buf * (kDqChunk * 32 * 4), 32 * wq, in.head,
                               qrow + ch * kDqChunk);
             bulk_commit_group();
           }
@@ -781,7 +786,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         }
       }
     }
-    if (r == 0) bulk_wait_group_all();  // every dQ reduce issued by this thread has landed
+    if (lane == 0) bulk_wait_group_all();  // every dQ reduce issued by this thread has landed
   } else {
     setmaxnreg_dec<kRegsLow>();  // spare warps of the last warpgroup
     if (kDBias && warp == kMmaWarp + 1) {

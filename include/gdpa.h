@@ -351,9 +351,9 @@ int gdpa_timing_collect(float* ms, int* kind, int max);
  * Arguments and results are those of gdpa_fwd without workspace/ws_bytes.
  * The scratch comes from one 1 MiB array compiled into the library (every
  * GPU that loads the library holds it until the process exits).  Problems
- * whose gdpa_fwd_workspace_size() exceeds 1 MiB (about H * (Tq/256 + B) >
- * 131,000 work items) are refused with GDPA_ERR_WORKSPACE before anything is
- * launched.  The first call on each device looks up the array's device
+ * whose gdpa_fwd_workspace_size() exceeds 1 MiB (about H * (Tq/256 + 2B) >
+ * 131,000 work-list entries) are refused with GDPA_ERR_WORKSPACE before
+ * anything is launched.  The first call on each device looks up the array's device
  * address (cudaGetSymbolAddress); make that first call before any stream
  * capture.  The address is kept for the life of the process: after a
  * cudaDeviceReset() on the device it is stale, so do not call this entry

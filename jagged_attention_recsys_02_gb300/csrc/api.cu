@@ -162,6 +162,7 @@ gdpa_status check_common(const void* q, const int32_t* qo, const void* k, const 
 }
 
 bool is_dense(const gdpa_bias* bias) { return bias != nullptr && bias->kind == GDPA_BIAS_DENSE; }
+int bias_kind(const gdpa_bias* bias) { return bias == nullptr ? GDPA_BIAS_NONE : bias->kind; }
 
 // The relative-position table (nullptr for no bias or a dense bias).
 const float* bias_table(const gdpa_bias* bias, int* max_rel) {
@@ -196,11 +197,15 @@ using namespace gdpa;
 
 extern "C" {
 
+// Workspace header (256 bytes): main-list count and ticket, short-query list
+// count and ticket, all-short flag.  The main list follows at byte 256, the
+// short-query list (one item per sample and head at most) after it.
 size_t gdpa_fwd_workspace_size(int B, int H, int d, int64_t Tq, int64_t Tkv) {
   (void)d;
   (void)Tkv;
   if (B < 0 || H <= 0 || Tq < 0) return 0;
-  return 256 + align_up(static_cast<size_t>(max_fwd_items(B, H, Tq)) * sizeof(int2), 256);
+  return 256 + align_up(static_cast<size_t>(max_fwd_items(B, H, Tq)) * sizeof(int2), 256) +
+         align_up(static_cast<size_t>(B) * H * sizeof(int2), 256);
 }
 
 gdpa_status gdpa_fwd(const void* q, const int32_t* q_offsets, const void* k, const void* v,
@@ -246,9 +251,22 @@ gdpa_status gdpa_fwd_window(const void* q, const int32_t* q_offsets, const void*
   int* n_items = reinterpret_cast<int*>(ws);
   int* ticket = reinterpret_cast<int*>(ws + 4);
   int2* items = reinterpret_cast<int2*>(ws + 256);
+  // Samples with at most kShortQ queries go to the short-query kernel (GDPA
+  // activations without mask or bias: the PMA shape).
+  ShortList sq;
+  CUtensorMap tq_short;
+  if (act != GDPA_ACT_SOFTMAX && !causal && window == 0 && bias_kind(bias) == GDPA_BIAS_NONE) {
+    if (!make_thd_map(&tq_short, q, Tq, H, d, kShortQ)) return GDPA_ERR_INVALID_ARG;
+    sq.max_q = kShortQ;
+    sq.items = reinterpret_cast<int2*>(
+        ws + 256 + align_up(static_cast<size_t>(max_fwd_items(B, H, Tq)) * sizeof(int2), 256));
+    sq.n_items = reinterpret_cast<int*>(ws + 8);
+    sq.ticket = reinterpret_cast<int*>(ws + 12);
+    sq.all_short = reinterpret_cast<int*>(ws + 16);
+  }
 
   if (launch_build_worklist(q_offsets, kv_offsets, B, H, Tq, Tkv, causal, window, 0, items,
-                            n_items, ticket, dev->status, s, dense_off) != cudaSuccess)
+                            n_items, ticket, dev->status, s, dense_off, sq) != cudaSuccess)
     return GDPA_ERR_CUDA;
   ++t_launches;
 
@@ -279,8 +297,20 @@ gdpa_status gdpa_fwd_window(const void* q, const int32_t* q_offsets, const void*
   const bool timed = timing_slot(0, &ea, &eb);
   if (timed && cudaEventRecord(ea, s) != cudaSuccess) return GDPA_ERR_CUDA;
   if (launch_fwd(p, act, tq, tk, tv, grid, s) != cudaSuccess) return GDPA_ERR_CUDA;
-  if (timed && cudaEventRecord(eb, s) != cudaSuccess) return GDPA_ERR_CUDA;
   ++t_launches;
+  if (sq.items != nullptr) {
+    // the short-query items (an empty list makes the kernel return at once)
+    FwdParams ps = p;
+    ps.items = sq.items;
+    ps.n_items = sq.n_items;
+    ps.ticket = sq.ticket;
+    const int64_t n_sq = static_cast<int64_t>(B) * H;
+    const int grid_sq = static_cast<int>(n_sq < dev->sms ? n_sq : dev->sms);
+    if (launch_fwd_short_q(ps, act, tq_short, tk, tv, grid_sq, s) != cudaSuccess)
+      return GDPA_ERR_CUDA;
+    ++t_launches;
+  }
+  if (timed && cudaEventRecord(eb, s) != cudaSuccess) return GDPA_ERR_CUDA;
   return GDPA_OK;
 }
 
@@ -290,6 +320,7 @@ size_t gdpa_bwd_workspace_size(int B, int H, int d, int64_t Tq, int64_t Tkv) {
   sz += align_up(static_cast<size_t>(max_bwd_items(B, H, Tkv)) * sizeof(int2), 256);
   sz += align_up(static_cast<size_t>(Tq) * H * d * sizeof(float), 256);  // dQ accumulator
   sz += align_up(static_cast<size_t>(Tq) * H * sizeof(float), 256);      // D = rowsum(dO*O)
+  sz += align_up(static_cast<size_t>(B) * H * sizeof(int2), 256);        // short-query list
   return sz;
 }
 
@@ -355,8 +386,9 @@ gdpa_status gdpa_bwd_rope(const void* q, const int32_t* q_offsets, const void* k
   const void* kb = Tkv > 0 ? k : q;
   const void* vb = Tkv > 0 ? v : q;
   const int64_t Tkm = Tkv > 0 ? Tkv : Tq;
-  // The softmax kernel streams 128-query tiles and reduces dQ in [16 x d]
-  // boxes; the general kernel uses 64-query tiles and [64 x 64] boxes.
+  // The softmax kernel streams 128-query tiles and reduces dQ in [16 x 32]
+  // boxes (one warp's channels); the general kernel uses 64-query tiles and
+  // [64 x 64] boxes.
   const bool sm = act == GDPA_ACT_SOFTMAX;
   const int q_rows = sm ? kBwdSmQRows : kBwdQRows;
   CUtensorMap tq, tk, tv, tdo;
@@ -373,14 +405,31 @@ gdpa_status gdpa_bwd_rope(const void* q, const int32_t* q_offsets, const void* k
   float* dq_acc = reinterpret_cast<float*>(ws + off);
   off += align_up(static_cast<size_t>(Tq) * H * d * sizeof(float), 256);
   float* delta = reinterpret_cast<float*>(ws + off);
+  off += align_up(static_cast<size_t>(Tq) * H * sizeof(float), 256);
   // Without query rows there is nothing to reduce into; any valid map will do.
   CUtensorMap tdq;
   if (!make_dq_map(&tdq, Tq > 0 ? static_cast<void*>(dq_acc) : ws, Tq > 0 ? Tq : 1, H, d,
-                   sm ? d : 64, sm ? kBwdSmDqRows : kBwdQRows))
+                   sm ? 32 : 64, sm ? kBwdSmDqRows : kBwdQRows))
     return GDPA_ERR_INVALID_ARG;
+  // Samples with at most kShortQ queries go to the short-query kernel (no
+  // mask, bias, bias gradient or rotary backward).
+  ShortList sql;
+  ShortBwd sqb;
+  const bool short_q = Tq > 0 && !causal && window == 0 && bias_kind(bias) == GDPA_BIAS_NONE &&
+                       dbias == nullptr && rope_base == 0.0f;
+  if (short_q) {
+    if (!make_thd_map(&sqb.tq, q, Tq, H, d, kShortQ) ||
+        !make_thd_map(&sqb.tdo, dout, Tq, H, d, kShortQ))
+      return GDPA_ERR_INVALID_ARG;
+    sql.max_q = kShortQ;
+    sql.items = reinterpret_cast<int2*>(ws + off);
+    sql.n_items = reinterpret_cast<int*>(ws + 8);
+    sql.ticket = reinterpret_cast<int*>(ws + 12);
+    sql.all_short = reinterpret_cast<int*>(ws + 16);
+  }
 
   if (launch_build_worklist(kv_offsets, q_offsets, B, H, Tkv, Tq, causal, window, 1, items,
-                            n_items, ticket, dev->status, s, dense_off) != cudaSuccess)
+                            n_items, ticket, dev->status, s, dense_off, sql) != cudaSuccess)
     return GDPA_ERR_CUDA;
   ++t_launches;
 
@@ -412,20 +461,31 @@ gdpa_status gdpa_bwd_rope(const void* q, const int32_t* q_offsets, const void* k
   p.n_items = n_items;
   p.ticket = ticket;
   p.status = dev->status;
+  p.all_short = sql.all_short;
+  if (short_q) {
+    sqb.p = p;
+    sqb.p.items = sql.items;
+    sqb.p.n_items = sql.n_items;
+    sqb.p.ticket = sql.ticket;
+    sqb.dq = dq;
+    const int64_t n_sq = static_cast<int64_t>(B) * H;
+    sqb.grid = static_cast<int>(n_sq < dev->sms ? n_sq : dev->sms);
+  }
   const int64_t max_items = max_bwd_items(B, H, Tkv);
   const int grid = static_cast<int>(max_items < dev->sms ? (max_items > 0 ? max_items : 1) : dev->sms);
   int launches = 0;
   cudaEvent_t ea = nullptr, eb = nullptr;
   const bool timed = timing_slot(1, &ea, &eb);
   cudaError_t e = launch_bwd(p, act, tq, tk, tv, tdo, tdq, grid, s, &launches,
-                             timed ? ea : nullptr, timed ? eb : nullptr);
+                             timed ? ea : nullptr, timed ? eb : nullptr, short_q ? &sqb : nullptr);
   t_launches += launches;
   if (e != cudaSuccess) return GDPA_ERR_CUDA;
   if (Tq > 0) {
     const cudaError_t ce =
         rope_base > 0.0f
             ? launch_dq_convert_rope(dq_acc, dq, q_offsets, B, Tq, H, d, scale, rope_base, s)
-            : launch_dq_convert(dq_acc, dq, static_cast<long long>(Tq) * H * d, scale, s);
+            : launch_dq_convert(dq_acc, dq, static_cast<long long>(Tq) * H * d, scale, s,
+                                p.all_short);
     if (ce != cudaSuccess) return GDPA_ERR_CUDA;
     ++t_launches;
   }

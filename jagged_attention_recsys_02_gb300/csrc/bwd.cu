@@ -740,8 +740,11 @@ template <int D>
 __global__ void __launch_bounds__(256)
 bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
                       float* __restrict__ delta, float* __restrict__ dq_acc, long long Tq, int H,
-                      int softmax) {
+                      int softmax, const int* __restrict__ all_short) {
   constexpr int kLanesPerRow = D / 8;
+  // no sample reduces into the accumulator: leave it alone
+  const bool zero_acc = all_short == nullptr || *all_short == 0;
+  if (!zero_acc && !softmax) return;
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const long long nrows = Tq * H;
   const int lane = threadIdx.x & 31;
@@ -752,7 +755,7 @@ bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16
        row0 < nrows; row0 += warps * kRowsPerWarp) {
     const long long row = row0 + sub;
     const bool ok = row < nrows;
-    if (ok) {
+    if (ok && zero_acc) {
       float4* acc = reinterpret_cast<float4*>(dq_acc + row * D) + 2 * v;
       acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -782,7 +785,9 @@ bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16
 // dq = bf16(dq_acc * scale), eight values (two 16-byte loads, one 16-byte
 // store) per thread and step.
 __global__ void __launch_bounds__(256)
-dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long long n8, float scale) {
+dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long long n8, float scale,
+                  const int* __restrict__ skip) {
+  if (skip != nullptr && *skip != 0) return;  // dq was written directly
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const float4 a = acc[2 * i];
@@ -874,7 +879,7 @@ cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const
                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                        int grid,
                        cudaStream_t stream, int* launches, cudaEvent_t ev_begin,
-                       cudaEvent_t ev_end) {
+                       cudaEvent_t ev_end, const ShortBwd* sq) {
   // 1) zero dQ accumulator, D = rowsum(dO * O)
   cudaError_t e = launch_bwd_preprocess(p, act == GDPA_ACT_SOFTMAX, stream);
   if (e != cudaSuccess) return e;
@@ -887,8 +892,14 @@ cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const
     e = (p.d == 64) ? launch_main_d<64>(p, act, tq, tk, tv, tdo, tdq, grid, stream)
                     : launch_main_d<128>(p, act, tq, tk, tv, tdo, tdq, grid, stream);
   if (e != cudaSuccess) return e;
-  if (ev_end != nullptr && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess) return e;
   ++*launches;
+  if (sq != nullptr) {
+    // the short-query items (an empty list makes the kernel return at once)
+    e = launch_bwd_short_q(sq->p, act, sq->tq, tk, tv, sq->tdo, sq->dq, sq->grid, stream);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+  }
+  if (ev_end != nullptr && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess) return e;
   return cudaSuccess;
 }
 
@@ -897,10 +908,12 @@ cudaError_t launch_bwd_preprocess(const BwdParams& p, bool softmax, cudaStream_t
   const int pre_blocks = static_cast<int>(rows / 8 + 1 < 4096 ? rows / 8 + 1 : 4096);
   if (p.d == 64)
     bwd_preprocess_kernel<64><<<pre_blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
-                                                              p.Tq, p.H, softmax ? 1 : 0);
+                                                              p.Tq, p.H, softmax ? 1 : 0,
+                                                              p.all_short);
   else
     bwd_preprocess_kernel<128><<<pre_blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
-                                                               p.Tq, p.H, softmax ? 1 : 0);
+                                                               p.Tq, p.H, softmax ? 1 : 0,
+                                                               p.all_short);
   return cudaGetLastError();
 }
 
@@ -916,11 +929,11 @@ cudaError_t launch_dq_convert_rope(const float* acc, void* dq, const int32_t* of
 }
 
 cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const int* skip) {
   const long long n8 = n / 8;  // n = Tq * H * d with d in {64, 128}
   const int blocks = static_cast<int>(n8 / 256 + 1 < 8192 ? n8 / 256 + 1 : 8192);
   dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(acc),
-                                                reinterpret_cast<uint4*>(dq), n8, scale);
+                                                reinterpret_cast<uint4*>(dq), n8, scale, skip);
   return cudaGetLastError();
 }
 

@@ -202,6 +202,9 @@ struct BwdParams {
   float rope_base;          // > 0: dq, dk go back through the rotary embedding
   float* dq_acc;            // fp32 [Tq][H][d] accumulator (zeroed by the preprocess kernel)
   float* delta;             // fp32 [H][Tq]: rowsum(dO * O) for softmax
+  const int* all_short;     // scheduler flag: every sample takes the short-query kernel, so
+                            //   the accumulator is neither zeroed nor converted (nullptr: no
+                            //   short-query list)
   const int2* items;
   const int* n_items;
   int* ticket;
@@ -226,6 +229,20 @@ struct BlockParams {
   int* status;
 };
 
+// The short-query list of the scheduler: samples with 1 <= Lq_b <= max_q get
+// one item {b, head} per head here instead of blocks in the main list
+// (max_q 0 or items null: no split).  all_short is set to 1 when every
+// sample with query rows went to this list.
+struct ShortList {
+  int max_q = 0;
+  int2* items = nullptr;
+  int* n_items = nullptr;
+  int* ticket = nullptr;
+  int* all_short = nullptr;
+};
+// Queries of a short-query item (the MMA width of the short-query kernels).
+constexpr int kShortQ = 32;
+
 // Host-side launchers (defined in the kernel translation units).
 // bias_off (optional): element offsets of a dense jagged bias, checked against
 // H * Lq_b * Lkv_b (a mismatch is reported as GDPA_ERR_BAD_OFFSETS).
@@ -233,20 +250,39 @@ cudaError_t launch_build_worklist(const int32_t* outer_off, const int32_t* inner
                                   int64_t T_outer, int64_t T_inner, int causal, int window,
                                   int mode,
                                   int2* items, int* n_items, int* ticket, int* status,
-                                  cudaStream_t stream, const int64_t* bias_off = nullptr);
+                                  cudaStream_t stream, const int64_t* bias_off = nullptr,
+                                  const ShortList& sq = ShortList{});
 cudaError_t launch_fwd(const FwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, int grid, cudaStream_t stream);
+// Short-query forward (GDPA activations, no mask or bias): p.items is the
+// scheduler's short-query list; tq has kShortQ-row boxes.
+cudaError_t launch_fwd_short_q(const FwdParams& p, int act, const CUtensorMap& tq,
+                               const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                               cudaStream_t stream);
 int fwd_smem_bytes(int d);
 cudaError_t launch_bwd_softmax_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                                     const CUtensorMap& tv, const CUtensorMap& tdo,
                                     const CUtensorMap& tdq, int grid, cudaStream_t s);
+// The short-query part of a backward call (its own list, maps and grid).
+struct ShortBwd {
+  BwdParams p;
+  CUtensorMap tq, tdo;
+  void* dq;
+  int grid;
+};
 cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                        int grid,
                        cudaStream_t stream, int* launches, cudaEvent_t ev_begin,
-                       cudaEvent_t ev_end);
+                       cudaEvent_t ev_end, const ShortBwd* sq = nullptr);
 cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale,
-                              cudaStream_t stream);
+                              cudaStream_t stream, const int* skip = nullptr);
+// Short-query backward (p.items: the scheduler's short-query list; tq, tdo
+// with kShortQ-row boxes).  dQ goes to dq as bf16 when *p.all_short, else
+// (unscaled) into the rows of p.dq_acc that the short samples own.
+cudaError_t launch_bwd_short_q(const BwdParams& p, int act, const CUtensorMap& tq,
+                               const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& tdo, void* dq, int grid, cudaStream_t stream);
 // dq = bf16 of the rotary backward of scale * acc ([T][H][d]); positions are
 // local to the samples of `offsets` (B + 1 entries).
 cudaError_t launch_dq_convert_rope(const float* acc, void* dq, const int32_t* offsets, int B,

@@ -14,6 +14,11 @@
 //
 // One CTA of 1024 threads builds the list; it also validates the offsets and
 // reports malformed ones through the device status word instead of trapping.
+//
+// Short-query samples (1 <= Lq_b <= short_q, when short_q > 0) go to a second
+// list of (sample, head) items, sorted the same way by their key-tile count,
+// for the kernels that stream a whole sample's keys past its few queries; the
+// scheduler then also records whether every sample with queries is short.
 #include "common.cuh"
 
 namespace gdpa {
@@ -50,48 +55,13 @@ __device__ __forceinline__ int sample_bucket(int mode, int causal, int window, i
   return static_cast<int>(b < kCostBuckets - 1 ? b : kCostBuckets - 1);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __restrict__ inner_off,
-                      int B, int H, long long T_outer, long long T_inner, int causal, int window,
-                      int mode,
-                      int2* __restrict__ items, int* __restrict__ n_items,
-                      int* __restrict__ ticket, int* __restrict__ status,
-                      const int64_t* __restrict__ bias_off) {
-  __shared__ int hist[kCostBuckets];
-  __shared__ int base[kCostBuckets];
-  __shared__ int warp_tot[kThreads / 32];
-  __shared__ int bad;
+// Query rows of sample b, for either mode.
+__device__ __forceinline__ int query_rows(int mode, int Lo, int Li) { return mode == 0 ? Lo : Li; }
+
+// Exclusive scan in descending bucket order: base[c] = sum of hist[c'] for
+// c' > c; returns the total.  Thread t owns reversed positions 2t and 2t+1.
+__device__ int scan_desc(const int* hist, int* base, int* warp_tot) {
   const int tid = threadIdx.x;
-  const int block_rows = (mode == 0) ? kItemRows : kBwdKvRows;
-  for (int i = tid; i < kCostBuckets; i += kThreads) hist[i] = 0;
-  if (tid == 0) {
-    bad = (outer_off[0] != 0 || inner_off[0] != 0 || outer_off[B] != T_outer ||
-           inner_off[B] != T_inner || (bias_off != nullptr && bias_off[0] != 0)) ? 1 : 0;
-  }
-  __syncthreads();
-  for (int b = tid; b < B; b += kThreads) {
-    const int Lo = outer_off[b + 1] - outer_off[b];
-    const int Li = inner_off[b + 1] - inner_off[b];
-    if (Lo < 0 || Li < 0 || ((causal || window > 0) && Lo != Li) ||
-        (bias_off != nullptr &&
-         bias_off[b + 1] - bias_off[b] != static_cast<int64_t>(H) * Lo * Li)) {
-      bad = 1;
-      continue;
-    }
-    const int nblk = (Lo + block_rows - 1) / block_rows;
-    if (nblk > 0) atomicAdd(&hist[sample_bucket(mode, causal, window, Lo, Li, nblk)], nblk);
-  }
-  __syncthreads();
-  if (bad) {
-    if (tid == 0) {
-      *n_items = 0;
-      *ticket = 0;
-      set_status(status, GDPA_ERR_BAD_OFFSETS);
-    }
-    return;
-  }
-  // Exclusive scan in descending cost order: base[c] = sum of hist[c'] for c' > c.
-  // Thread t owns reversed positions 2t and 2t+1.
   const int c0 = kCostBuckets - 1 - 2 * tid, c1 = c0 - 1;
   const int v0 = hist[c0], v1 = hist[c1];
   int incl = v0 + v1;
@@ -116,12 +86,82 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
   const int before = (warp > 0 ? warp_tot[warp - 1] : 0) + incl - (v0 + v1);
   base[c0] = before;
   base[c1] = before + v0;
-  __syncthreads();
   const int total = warp_tot[kThreads / 32 - 1];
+  __syncthreads();
+  return total;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __restrict__ inner_off,
+                      int B, int H, long long T_outer, long long T_inner, int causal, int window,
+                      int mode,
+                      int2* __restrict__ items, int* __restrict__ n_items,
+                      int* __restrict__ ticket, int* __restrict__ status,
+                      const int64_t* __restrict__ bias_off, ShortList sq) {
+  __shared__ int hist[kCostBuckets];
+  __shared__ int base[kCostBuckets];
+  __shared__ int shist[kCostBuckets];
+  __shared__ int sbase[kCostBuckets];
+  __shared__ int warp_tot[kThreads / 32];
+  __shared__ int bad;
+  const int tid = threadIdx.x;
+  const int block_rows = (mode == 0) ? kItemRows : kBwdKvRows;
+  const bool split = sq.items != nullptr && sq.max_q > 0;
+  for (int i = tid; i < kCostBuckets; i += kThreads) hist[i] = shist[i] = 0;
+  if (tid == 0) {
+    bad = (outer_off[0] != 0 || inner_off[0] != 0 || outer_off[B] != T_outer ||
+           inner_off[B] != T_inner || (bias_off != nullptr && bias_off[0] != 0)) ? 1 : 0;
+  }
+  __syncthreads();
+  for (int b = tid; b < B; b += kThreads) {
+    const int Lo = outer_off[b + 1] - outer_off[b];
+    const int Li = inner_off[b + 1] - inner_off[b];
+    if (Lo < 0 || Li < 0 || ((causal || window > 0) && Lo != Li) ||
+        (bias_off != nullptr &&
+         bias_off[b + 1] - bias_off[b] != static_cast<int64_t>(H) * Lo * Li)) {
+      bad = 1;
+      continue;
+    }
+    const int nblk = (Lo + block_rows - 1) / block_rows;
+    const int lq = query_rows(mode, Lo, Li);
+    if (split && lq >= 1 && lq <= sq.max_q) {
+      // one item per head; cost: the sample's key tiles
+      const int lk = mode == 0 ? Li : Lo;
+      const int c = 1 + (lk + kKvRows - 1) / kKvRows;
+      atomicAdd(&shist[c < 1024 ? c : min(kCostBuckets - 1, 1024 + (c - 1024) / 64)], 1);
+    } else if (nblk > 0) {
+      atomicAdd(&hist[sample_bucket(mode, causal, window, Lo, Li, nblk)], nblk);
+    }
+  }
+  __syncthreads();
+  if (bad) {
+    if (tid == 0) {
+      *n_items = 0;
+      *ticket = 0;
+      if (split) {
+        *sq.n_items = 0;
+        *sq.ticket = 0;
+        *sq.all_short = 0;
+      }
+      set_status(status, GDPA_ERR_BAD_OFFSETS);
+    }
+    return;
+  }
+  const int total = scan_desc(hist, base, warp_tot);
+  const int stotal = split ? scan_desc(shist, sbase, warp_tot) : 0;
   for (int b = tid; b < B; b += kThreads) {
     const int Lo = outer_off[b + 1] - outer_off[b];
     const int Li = inner_off[b + 1] - inner_off[b];
     const int nblk = (Lo + block_rows - 1) / block_rows;
+    const int lq = query_rows(mode, Lo, Li);
+    if (split && lq >= 1 && lq <= sq.max_q) {
+      const int lk = mode == 0 ? Li : Lo;
+      const int c = 1 + (lk + kKvRows - 1) / kKvRows;
+      const int pos = atomicAdd(&sbase[c < 1024 ? c : min(kCostBuckets - 1, 1024 + (c - 1024) / 64)], 1);
+      for (int h = 0; h < H; ++h)
+        sq.items[static_cast<long long>(pos) * H + h] = make_int2(b, h);
+      continue;
+    }
     if (nblk == 0) continue;
     const int pos = atomicAdd(&base[sample_bucket(mode, causal, window, Lo, Li, nblk)], nblk);
     // Blocks in descending cost: under the causal mask the forward's last
@@ -136,6 +176,11 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
   if (tid == 0) {
     *n_items = total * H;
     *ticket = 0;
+    if (split) {
+      *sq.n_items = stotal * H;
+      *sq.ticket = 0;
+      *sq.all_short = (total == 0 && stotal > 0) ? 1 : 0;
+    }
   }
 }
 
@@ -144,10 +189,11 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
 cudaError_t launch_build_worklist(const int32_t* outer_off, const int32_t* inner_off, int B, int H,
                                   int64_t T_outer, int64_t T_inner, int causal, int window,
                                   int mode, int2* items, int* n_items, int* ticket, int* status,
-                                  cudaStream_t stream, const int64_t* bias_off) {
+                                  cudaStream_t stream, const int64_t* bias_off,
+                                  const ShortList& sq) {
   build_worklist_kernel<<<1, kThreads, 0, stream>>>(outer_off, inner_off, B, H, T_outer, T_inner,
                                                     causal, window, mode, items, n_items, ticket,
-                                                    status, bias_off);
+                                                    status, bias_off, sq);
   return cudaGetLastError();
 }
 

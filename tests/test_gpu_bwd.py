@@ -101,6 +101,25 @@ def test_bwd_bias_noncausal(act):
     _case([5, 300, 129], [260, 7, 500], 3, 128, act, max_rel=64)
 
 
+# At most 32 queries: the short-query backward (keys as TMEM lanes, dQ kept in
+# TMEM across the sample's keys and stored once).  All-short batches write dq
+# directly in bf16; with a longer sample in the call, the short samples' dQ
+# rows pass through the fp32 accumulator and its conversion like the others.
+SHORTQ_Q = [32, 1, 31, 17, 32, 2, 5, 32]
+SHORTQ_KV = [700, 1, 128, 0, 129, 256, 513, 64]
+
+
+@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh", "identity", "gelu_erf"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mixed", [False, True])
+def test_bwd_short_queries(act, d, mixed):
+    lq = SHORTQ_Q + ([300] if mixed else [])
+    lkv = SHORTQ_KV + ([200] if mixed else [])
+    dq, dk, dv = _case(lq, lkv, 3, d, act)
+    z = sum(SHORTQ_Q[:3])
+    assert torch.all(dq[z:z + SHORTQ_Q[3]] == 0)  # the sample with no key
+
+
 def test_bwd_empty_sides():
     # no keys: dq rows are zero; no queries: dk/dv rows are zero
     dq, dk, dv = _case([3, 0, 130, 5], [0, 9, 0, 140], 2, 128, "softmax")

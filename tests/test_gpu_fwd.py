@@ -71,6 +71,20 @@ def test_fwd_bias_noncausal(act):
     _case([5, 300, 129], [260, 7, 500], 3, 128, act, max_rel=64)
 
 
+# At most 32 queries: the short-query kernel (keys as TMEM lanes, the queries
+# as the MMA's N); the 300-query sample of the same call takes the row-tile
+# kernel.  Key counts cross the 128-key tiles, and one short sample has none.
+SHORT_Q = [32, 1, 31, 0, 17, 32, 2, 5, 32, 300]
+SHORT_KV = [700, 1, 128, 9, 0, 129, 256, 513, 64, 200]
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu_tanh", "identity", "gelu_erf"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_fwd_short_queries(act, d):
+    out = _case(SHORT_Q, SHORT_KV, 3, d, act)
+    assert torch.all(out[sum(SHORT_Q[:4]):sum(SHORT_Q[:5])] == 0)  # the sample with no key
+
+
 def test_fwd_empty_keys_and_queries():
     # samples with no keys give zero rows (lse = -inf for softmax); empty query samples write nothing
     out = _case([3, 0, 130, 5], [0, 9, 0, 140], 2, 128, "softmax")

@@ -7,7 +7,9 @@ order; it writes the item count at byte 0 of the caller's workspace and the
 items, one int2 {sample, (block << 8) | head} each, from byte 256.  These
 tests run gdpa_fwd / gdpa_bwd (forward: blocks of 256 query rows over
 128-key tiles; backward: blocks of 128 keys over 64-query tiles) and check
-the list against a host count made row by row from the mask's definition:
+the list against a host count made row by row from the mask's definition
+(samples with at most 32 queries and no mask or bias go to a second list,
+one {sample, head} item each, for the short-query kernels):
 
   * every (sample, head, block) with rows appears exactly once, and nothing else;
   * a sample's items are contiguous, heads innermost, and without a window
@@ -60,21 +62,42 @@ def _bucket(total):
     return total if total < 1024 else 1024 + (total - 1024) // 64
 
 
-def _read_list(ws):
+def _align(n):
+    return (n + 255) // 256 * 256
+
+
+def _read_list(ws, short_at):
+    """Main list (count at byte 0, items from byte 256) and the short-query
+    list (count at byte 8, items from byte short_at, one {sample, head} each)."""
     raw = ws.cpu().numpy()
     n = int(raw[:4].view(np.int32)[0])
     items = raw[256:256 + 8 * n].view(np.int32).reshape(n, 2)
-    return items[:, 0].astype(np.int64), (items[:, 1] >> 8).astype(np.int64), \
-        (items[:, 1] & 0xFF).astype(np.int64)
+    main = (items[:, 0].astype(np.int64), (items[:, 1] >> 8).astype(np.int64),
+            (items[:, 1] & 0xFF).astype(np.int64))
+    ns = int(raw[8:12].view(np.int32)[0])
+    short = raw[short_at:short_at + 8 * ns].view(np.int32).reshape(ns, 2).astype(np.int64)
+    all_short = int(raw[16:20].view(np.int32)[0])
+    return main, short, all_short
 
 
-def _check(lq, lkv, H, causal, window, mode, samples, blocks, heads):
+def _check_short(lq, lkv, H, short_set, short, all_short, n_main):
+    """Short-query samples: one item per head, longest (most key tiles) first."""
+    got = [tuple(x) for x in short.tolist()]
+    assert len(got) == len(set(got)), "a short item appears twice"
+    assert set(got) == {(b, h) for b in short_set for h in range(H)}, "short items missing or extra"
+    costs = [_bucket(1 + math.ceil(lkv[b] / 128)) for b, _ in got]
+    assert all(x >= y for x, y in zip(costs, costs[1:])), "short items not longest first"
+    assert all_short == (1 if (n_main == 0 and len(got) > 0) else 0)
+
+
+def _check(lq, lkv, H, causal, window, mode, samples, blocks, heads, short_set=()):
     rows = lq if mode == "fwd" else lkv
     per = 256 if mode == "fwd" else 128
     cost_fn = _fwd_cost if mode == "fwd" else _bwd_cost
-    # every (sample, head, block) with rows exactly once, nothing else
-    want = {(b, blk, h) for b in range(len(lq)) for blk in range(math.ceil(rows[b] / per))
-            for h in range(H)}
+    # every (sample, head, block) with rows exactly once, nothing else (samples of
+    # the short-query list have no blocks here)
+    want = {(b, blk, h) for b in range(len(lq)) if b not in short_set
+            for blk in range(math.ceil(rows[b] / per)) for h in range(H)}
     got = list(zip(samples.tolist(), blocks.tolist(), heads.tolist()))
     assert len(got) == len(set(got)), "an item appears twice"
     assert set(got) == want, "items missing or extra"
@@ -118,19 +141,36 @@ def _run(lq, lkv, H, causal=False, window=0, act="softmax", seed=0):
                      window=window, workspace=ws_b)
     torch.cuda.synchronize()
     assert binding.device_status() == 0
-    f = _read_list(ws_f)
-    b = _read_list(ws_b)
+    B = len(lq)
+    # workspace layout: short list after the main list (forward), after the main
+    # list, the fp32 dQ accumulator and D (backward)
+    f_short_at = 256 + _align(H * (Tq // 256 + B) * 8)
+    b_short_at = 256 + _align(H * (Tkv // 128 + B) * 8) + _align(Tq * H * d * 4) + _align(Tq * H * 4)
+    (f, fs, fa), (b, bs, ba) = _read_list(ws_f, f_short_at), _read_list(ws_b, b_short_at)
     lq, lkv = np.asarray(lq), np.asarray(lkv)
-    return (_check(lq, lkv, H, causal, window, "fwd", *f),
-            _check(lq, lkv, H, causal, window, "bwd", *b))
+    # samples with 1..32 queries take the short-query kernels when there is no
+    # mask or bias (forward: GDPA activations only)
+    plain = not causal and not window
+    short = {i for i in range(B) if 1 <= lq[i] <= 32} if plain else set()
+    f_short = short if act != "softmax" else set()
+    _check_short(lq, lkv, H, f_short, fs, fa, len(f[0]))
+    _check_short(lq, lkv, H, short, bs, ba, len(b[0]))
+    return (_check(lq, lkv, H, causal, window, "fwd", *f, short_set=f_short),
+            _check(lq, lkv, H, causal, window, "bwd", *b, short_set=short))
 
 
 RAGGED_Q = [1, 300, 0, 129, 513, 64, 255, 256, 257, 1000, 7, 0, 2048]
 RAGGED_KV = [7, 256, 5, 0, 700, 64, 128, 129, 1, 300, 3000, 0, 200]
 
 
-def test_worklist_ragged_cross():
-    _run(RAGGED_Q, RAGGED_KV, 3, act="silu")
+@pytest.mark.parametrize("act", ["silu", "softmax"])
+def test_worklist_ragged_cross(act):
+    _run(RAGGED_Q, RAGGED_KV, 3, act=act)
+
+
+def test_worklist_all_short():
+    """Every sample short: the main lists are empty and the flag is set."""
+    _run([32, 1, 7, 20], [700, 0, 129, 5], 2, act="silu")
 
 
 def test_worklist_causal():

@@ -418,8 +418,10 @@ def run_reference(args, rank, world):
     return 0
 
 
-def workload_config(w, l2_note):
-    return {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "act": w.act, "causal": w.causal,
+def workload_config(w, l2_note, rope_base=0.0):
+    extra = {"rope_base": rope_base} if rope_base else {}
+    return {**extra, "workload": w.name, "B": w.B, "H": w.H, "d": w.d, "act": w.act,
+            "causal": w.causal,
             "window": w.window, "block": w.block,
             "bias": (f"relpos table [{w.H},{2 * w.max_rel - 1}]" if w.max_rel else
                      (f"dense jagged fp32 [{w.H * int((w.lq * w.lkv).sum())}]" if w.dense
@@ -593,6 +595,8 @@ def run_gpu(args, rank, world, local_rank):
             binding.gdpa_fwd(q, qo, k, v, ko, out=out_, lse=lse_, workspace=ws_f, **kw_)
 
     def run_bwd(q, qo, k, v, ko, out_, lse_, do, dq_, dk_, dv_, **kw_):
+        if args.rope_base:  # q and k taken as rotary-embedded: the fused rotary backward
+            kw_ = dict(kw_, rope_base=args.rope_base)
         if w.block:
             binding.gdpa_block_bwd(q, qo, k, v, do, dq=dq_, dk=dk_, dv=dv_, workspace=ws_k, **kw_)
         else:
@@ -805,7 +809,7 @@ def run_gpu(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1) bf16 inputs, lengths per workload recipe)",
         "config": workload_config(
             w, f"inputs larger than L2: {in_bytes / 2**20:.0f} MiB of q,k,v,dO per step "
-               f"(no flush)"),
+               f"(no flush)", args.rope_base),
         "pct_of_peak": {"value": 100.0 * value / peak, "peak_tflops": peak,
                         "peak": ("bf16_tflops_sustained" if sustained else "bf16_tflops")
                         + f" of {peak_src}"},
@@ -1000,6 +1004,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-per-workload", dest="per_workload", action="store_false",
                     help="skip the other configurations' forward / backward lines")
+    ap.add_argument("--rope-base", type=float, default=0.0,
+                    help="run the backward with the fused rotary-embedding backward (q, k taken "
+                         "as rotary-embedded with this base)")
     ap.add_argument("--mxfp8", action="store_true",
                     help="time the MXFP8 forward path (quantise + block-scaled forward) instead")
     ap.add_argument("--mxfp8-bwd", action="store_true",

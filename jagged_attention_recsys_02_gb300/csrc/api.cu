@@ -386,9 +386,9 @@ gdpa_status gdpa_bwd_rope(const void* q, const int32_t* q_offsets, const void* k
   const void* kb = Tkv > 0 ? k : q;
   const void* vb = Tkv > 0 ? v : q;
   const int64_t Tkm = Tkv > 0 ? Tkv : Tq;
-  // The softmax kernel streams 128-query tiles and reduces dQ in [16 x 32]
-  // boxes (one warp's channels); the general kernel uses 64-query tiles and
-  // [64 x 64] boxes.
+  // The softmax kernel streams 128-query tiles, the general kernel 64-query
+  // tiles; both reduce dQ in [16 queries x 32 channels] boxes, one warp's
+  // channels each.
   const bool sm = act == GDPA_ACT_SOFTMAX;
   const int q_rows = sm ? kBwdSmQRows : kBwdQRows;
   CUtensorMap tq, tk, tv, tdo;
@@ -409,7 +409,7 @@ gdpa_status gdpa_bwd_rope(const void* q, const int32_t* q_offsets, const void* k
   // Without query rows there is nothing to reduce into; any valid map will do.
   CUtensorMap tdq;
   if (!make_dq_map(&tdq, Tq > 0 ? static_cast<void*>(dq_acc) : ws, Tq > 0 ? Tq : 1, H, d,
-                   sm ? 32 : 64, sm ? kBwdSmDqRows : kBwdQRows))
+                   32, kBwdSmDqRows))
     return GDPA_ERR_INVALID_ARG;
   // Samples with at most kShortQ queries go to the short-query kernel (no
   // mask, bias, bias gradient or rotary backward).

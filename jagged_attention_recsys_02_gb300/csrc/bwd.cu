@@ -22,6 +22,7 @@
 //   warps 0-3  activation group A: P^T, dS^T for query columns [0,32) of a tile
 //   warps 4-7  activation group B: the same for query columns [32,64)
 //   warps 8-11 dQ group: dQ^T tile -> shared memory -> bulk tensor reduce-add
+//              (each warp its own 32 channels, no group barrier)
 //              into the fp32 dQ accumulator; dK/dV epilogue
 //   warp  12   producer: TMA loads of K/V, Q/dO tiles; lse, D and bias values
 //   warp  13   MMA issuer
@@ -59,14 +60,16 @@ struct BwdCfg {
   // per stage: float lse2[64], D[64], bias window[192]
   static constexpr int kStatFloats = 2 * kBwdQRows + kBwdQRows + kBwdKvRows;
   static constexpr int kStats = kDs + 2 * kDsParts * kDsBytes;
-  // dQ staging: one [64 query rows][64 channels] fp32 buffer
-  static constexpr int kDqStageBytes = kBwdQRows * 64 * 4;
-  static constexpr int kDqBufs = 1;
+  // dQ staging: per warp, three [16 queries][32 channels] fp32 buffers (each
+  // warp reduces its own channels)
+  static constexpr int kDqChunk = 16;
+  static constexpr int kDqWarpBufs = 3;
+  static constexpr int kDqStageBytes = 4 * kDqWarpBufs * kDqChunk * 32 * 4;
   static constexpr int kDqStage = kStats + kStages * kStatFloats * 4;
   // bias-table gradient: per tile, dS summed along its 191 diagonals (two
   // buffers of 192 floats, then {first diagonal, head})
   static constexpr int kDbBuf = 192 * 4 + 16;
-  static constexpr int kDb = kDqStage + kDqBufs * kDqStageBytes;
+  static constexpr int kDb = kDqStage + kDqStageBytes;
   static constexpr int kBar = kDb + 2 * kDbBuf;
   static constexpr int kKvFull = 0, kKvEmpty = 1;
   static constexpr int kQdFull = 2;                 // + s
@@ -648,28 +651,32 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         tc_fence_before();
         mbar_arrive(bar(C::kDqEmpty));
         // Stage the tile as [query][channel] and add it into the fp32 dQ rows with
-        // one bulk tensor reduce per 64 channels.  Columns of queries outside the
-        // sample carry exact zeros (their dS is masked to 0), so a box that runs
-        // into the next sample's rows adds nothing; rows past Tq are skipped.
+        // bulk tensor reduces: each warp its own 32 channels, 16 queries at a
+        // time, from three buffers of its own (no group barrier).  Columns of
+        // queries outside the sample carry exact zeros (their dS is masked to 0),
+        // so a box that runs into the next sample's rows adds nothing; rows past
+        // Tq are skipped.
         const int qrow = in.q0 + (in.qt0 + t) * kBwdQRows;
-#pragma unroll 1
-        for (int hcol = 0; hcol < D / 64; ++hcol) {
-          const int buf = dq_issue % C::kDqBufs;
-          if (r == 0) bulk_wait_group_read<C::kDqBufs - 1>();  // buffer `buf` is free again
-          named_bar_sync(1, 128);
-          if ((r >> 6) == hcol) {
-            float* stg = reinterpret_cast<float*>(gbase + C::kDqStage + buf * C::kDqStageBytes);
-            const int ch = r & 63;
+        const uint32_t wstage = sbase + C::kDqStage + wq * C::kDqWarpBufs * (C::kDqChunk * 32 * 4);
+        float* wstg = reinterpret_cast<float*>(gbase + C::kDqStage) + wq * C::kDqWarpBufs * (C::kDqChunk * 32);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) stg[c * 64 + ch] = __uint_as_float(v0[c]);
+        for (int ch = 0; ch < kBwdQRows / C::kDqChunk; ++ch) {
+          const int buf = dq_issue % C::kDqWarpBufs;
+          if (lane == 0) bulk_wait_group_read<C::kDqWarpBufs - 1>();  // buffer `buf` is free again
+          __syncwarp();
+          if (32 * wq < D) {
+            float* stg = wstg + buf * (C::kDqChunk * 32);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) stg[(c + 32) * 64 + ch] = __uint_as_float(v1[c]);
+            for (int c = 0; c < C::kDqChunk; ++c) {
+              const int q = ch * C::kDqChunk + c;
+              stg[c * 32 + lane] = __uint_as_float(q < 32 ? v0[q & 31] : v1[q & 31]);
+            }
             fence_proxy_async_smem();
           }
-          named_bar_sync(1, 128);
-          if (r == 0) {
-            tma_reduce_add_3d(&tmap_dq, sbase + C::kDqStage + buf * C::kDqStageBytes, hcol * 64,
-                              in.head, qrow);
+          __syncwarp();
+          if (lane == 0 && 32 * wq < D) {
+            tma_reduce_add_3d(&tmap_dq, wstage + buf * (C::kDqChunk * 32 * 4), 32 * wq, in.head,
+                              qrow + ch * C::kDqChunk);
             bulk_commit_group();
           }
           ++dq_issue;
@@ -721,7 +728,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         }
       }
     }
-    if (r == 0) bulk_wait_group_all();  // every dQ reduce issued by this thread has landed
+    if (lane == 0) bulk_wait_group_all();  // every dQ reduce issued by this thread has landed
   }
 
   tc_fence_before();

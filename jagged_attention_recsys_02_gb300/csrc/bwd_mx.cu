@@ -773,6 +773,7 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // TMEM lane: channel (dQ^T) or key row (dK, dV)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const bool out32 = aligned32(p.dk, p.dv);
     uint32_t it = 0, dqc = 0, dkvc = 0, dq_issue = 0;
     volatile int* group_ok = reinterpret_cast<volatile int*>(gbase + C::kGroupOk);
     while (true) {
@@ -855,11 +856,7 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
 #pragma unroll
             for (int i = 0; i < 16; ++i)
               pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * mul, __uint_as_float(o[2 * i + 1]) * mul);
-            if (row_ok) {
-              uint4* d4 = reinterpret_cast<uint4*>(dst + chunk * 32);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
+            if (row_ok) store_words(dst + chunk * 32, pk, out32);
           }
         }
         tc_fence_before();

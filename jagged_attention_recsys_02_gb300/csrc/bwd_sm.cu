@@ -680,6 +680,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     uint32_t it = 0, dqc = 0, dkvc = 0, dq_issue = 0;
     volatile int* group_ok = reinterpret_cast<volatile int*>(gbase + C::kGroupOk);
+    const bool out32 = aligned32(p.dk, p.dv);
     while (true) {
       const uint32_t slot = it & 1u;
       bool w = mbar_wait(bar(C::kItemFull + slot), (it >> 1) & 1u, abort_flag);
@@ -768,11 +769,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 #pragma unroll
             for (int i = 0; i < 16; ++i)
               pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * mul, __uint_as_float(o[2 * i + 1]) * mul);
-            if (row_ok) {
-              uint4* d4 = reinterpret_cast<uint4*>(dst + chunk * 32);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
+            if (row_ok) store_words(dst + chunk * 32, pk, out32);
           }
         }
         tc_fence_before();

@@ -394,6 +394,7 @@ bwd_sq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     // ------------------------------------------------------------ epilogue
     const int r = (warp & 3) * 32 + lane;  // TMEM lane: key (dK, dV) or channel (dQ^T)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const bool out32 = aligned32(p.dk, p.dv);
     // every sample is short: dq in bf16 (the accumulator is neither zeroed nor
     // converted); otherwise the item's finished rows go to the accumulator,
     // whose conversion follows
@@ -432,12 +433,7 @@ bwd_sq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * mul, __uint_as_float(o[2 * i + 1]) * mul);
-            if (key < Lkv) {
-              uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
-#pragma unroll
-              for (int v = 0; v < 8; ++v)
-                d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-            }
+            if (key < Lkv) store_words(dst + c0, pk, out32);
           }
         }
         tc_fence_before();

@@ -156,6 +156,30 @@ __device__ __forceinline__ void rope_bwd_row(uint32_t taddr, float mul, int pos,
   }
 }
 
+// One thread's run of N 32-bit words (N a multiple of 8) to global memory:
+// 32-byte stores when `v8` (the address is then 32-byte aligned), else
+// 16-byte ones.  Epilogues write one row per thread, so a warp's store
+// touches 32 rows: halving the store instructions halves that traffic.
+template <int N>
+__device__ __forceinline__ void store_words(void* dst, const uint32_t (&w)[N], bool v8) {
+  static_assert(N % 8 == 0, "whole 32-byte pieces");
+  if (v8) {
+#pragma unroll
+    for (int i = 0; i < N / 8; ++i)
+      ptx::st_global_v8(static_cast<uint8_t*>(dst) + 32 * i,
+                        *reinterpret_cast<const uint32_t(*)[8]>(&w[8 * i]));
+  } else {
+    uint4* d = static_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  }
+}
+// 32-byte stores are possible into rows of D bf16 (a multiple of 32 bytes)
+// when every base is 32-byte aligned.
+__device__ __forceinline__ bool aligned32(const void* a, const void* b = nullptr) {
+  return ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 31u) == 0;
+}
+
 // Device status word values (same numbering as gdpa_status).
 __device__ __forceinline__ void set_status(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);

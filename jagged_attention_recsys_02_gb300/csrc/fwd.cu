@@ -467,6 +467,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
     const uint32_t t_o = t_s + 128;
     const float c_s = kSoftmax ? p.scale * kLog2e : p.scale;   // score multiplier
     const float* bias_win = reinterpret_cast<const float*>(gbase + C::kBias);
+    const bool out32 = aligned32(p.out);
     uint32_t it = 0, tcount = 0, ocount = 0, g = 0;
     while (true) {
       const uint32_t slot = it & 1u;
@@ -718,12 +719,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          if (row_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + chunk * 64);
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          }
+          if (row_valid) store_words(orow + chunk * 64, pk, out32);
         }
         tc_fence_before();
       } else if (row_valid) {

@@ -469,6 +469,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     const int half = warp >> 2;
     const int wq = warp & 3;
     const int row_in_half = wq * 32 + lane;
+    const bool out32 = aligned32(p.out);
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t t_s = tmem + lane_off + col_s(half);
     const uint32_t t_o = tmem + lane_off + col_o(half);
@@ -630,11 +631,7 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 #pragma unroll
           for (int q = 0; q < 16; ++q)
             pk[q] = pack_bf16x2(__uint_as_float(o[2 * q]) * inv_l, __uint_as_float(o[2 * q + 1]) * inv_l);
-          if (row_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + chunk * 32);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          }
+          if (row_valid) store_words(orow + chunk * 32, pk, out32);
         }
         tc_fence_before();
       } else if (row_valid) {

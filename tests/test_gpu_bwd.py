@@ -369,3 +369,45 @@ def test_bwd_fused_rope_with_window(act):
     assert_close(to_np(dq), oracle.rope_bwd(rq, o_np, base), BWD_TOL, what + " dq")
     assert_close(to_np(dk), oracle.rope_bwd(rk, o_np, base), BWD_TOL, what + " dk")
     assert_close(to_np(dv), rv, BWD_TOL, what + " dv")
+
+
+# Epilogues store rows with 32-byte stores when every output base is 32-byte
+# aligned and with 16-byte stores otherwise: outputs that start 16 bytes into
+# an allocation must give the same results, for the forward and for every
+# backward kernel family (softmax, GDPA, short-query samples).
+@pytest.mark.parametrize("act", ["softmax", "silu"])
+def test_outputs_at_16_byte_offsets(act):
+    lq, lkv = [300, 20, 129, 1], [260, 700, 5, 129]
+    H, d = 2, 128
+    g = torch.Generator(device=DEV).manual_seed(3)
+    q = rand_bf16((sum(lq), H, d), g, DEV)
+    k = rand_bf16((sum(lkv), H, d), g, DEV)
+    v = rand_bf16((sum(lkv), H, d), g, DEV)
+    do = rand_bf16((sum(lq), H, d), g, DEV)
+    qo = torch.from_numpy(offsets(lq)).to(DEV)
+    ko = torch.from_numpy(offsets(lkv)).to(DEV)
+    a = ACTS[act]
+    scale = 1.0 / math.sqrt(d)
+
+    def shifted(like):  # a view that starts 16 bytes into its allocation
+        buf = torch.empty(like.numel() + 8, device=DEV, dtype=torch.bfloat16)
+        view = buf[8:].view(like.shape)
+        assert view.data_ptr() % 32 == 16
+        return view
+
+    out, lse = binding.gdpa_fwd(q, qo, k, v, ko, act=a, scale=scale)
+    out16 = shifted(out)
+    _, lse16 = binding.gdpa_fwd(q, qo, k, v, ko, act=a, scale=scale, out=out16)
+    assert torch.equal(out16, out)
+    if lse is not None:
+        assert torch.equal(lse16, lse)
+    grads = binding.gdpa_bwd(q, qo, k, v, ko, out, lse, do, act=a, scale=scale)
+    g16 = [shifted(t) for t in grads]
+    binding.gdpa_bwd(q, qo, k, v, ko, out, lse, do, act=a, scale=scale, dq=g16[0], dk=g16[1],
+                     dv=g16[2])
+    assert binding.device_status() == 0
+    # dK and dV rows are written once each: same bits.  dQ is summed by
+    # reduce-adds in whatever order the key blocks finish (its conversion
+    # always uses 16-byte stores): equal up to the last bf16 bit.
+    assert torch.equal(grads[1], g16[1]) and torch.equal(grads[2], g16[2])
+    torch.testing.assert_close(g16[0], grads[0], rtol=2 ** -7, atol=1e-3)

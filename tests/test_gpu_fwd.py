@@ -71,6 +71,31 @@ def test_fwd_bias_noncausal(act):
     _case([5, 300, 129], [260, 7, 500], 3, 128, act, max_rel=64)
 
 
+# Relative-position tables whose entries span 0.3, 40 and 100 (natural units)
+# against scores twice the usual size: the running maximum and the rescaling
+# of the softmax must keep every row exact when the bias, not the score,
+# decides which key dominates.
+@pytest.mark.parametrize("span", [0.3, 40.0, 100.0])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_bias_span(span, causal):
+    L = [1, 130, 300, 0, 511, 257]
+    H, d, max_rel = 2, 128, 300
+    g = torch.Generator(device=DEV).manual_seed(7)
+    q = rand_bf16((sum(L), H, d), g, DEV) * 2.0
+    k = rand_bf16((sum(L), H, d), g, DEV)
+    v = rand_bf16((sum(L), H, d), g, DEV)
+    o = torch.from_numpy(offsets(L)).to(DEV)
+    table = torch.rand(H, 2 * max_rel - 1, generator=g, device=DEV) * span - span / 2
+    scale = 1.0 / math.sqrt(d)
+    out, lse = run_fwd(q, o, k, v, o, "softmax", causal, scale, table, max_rel)
+    ref = oracle_fwd_samples(to_np(q), to_np(k), to_np(v), offsets(L), offsets(L), range(len(L)),
+                             "softmax", causal, scale, table.cpu().double().numpy(), max_rel)
+    got, got_lse = to_np(out), lse.cpu().double().numpy()
+    for rows, ro, rl in ref:
+        assert_close(got[rows], ro, FWD_TOL, f"out rows {rows[0]}..{rows[-1]}")
+        assert_close(got_lse[:, rows], rl, FWD_TOL, "lse")
+
+
 # At most 32 queries: the short-query kernel (keys as TMEM lanes, the queries
 # as the MMA's N); the 300-query sample of the same call takes the row-tile
 # kernel.  Key counts cross the 128-key tiles, and one short sample has none.

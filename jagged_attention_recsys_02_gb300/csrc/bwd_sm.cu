@@ -63,7 +63,7 @@ constexpr int kKRows = kBwdKvRows;   // 128 keys per item
 constexpr float kLog2e = 1.4426950408889634f;
 static_assert(kQRows == kKRows, "causal tile skipping assumes square tiles");
 
-template <int D>
+template <int D, bool kAug>
 struct SmCfg {
   static constexpr int kKvTileBytes = kKRows * D * 2;     // K or V block
   static constexpr int kQTileBytes = kQRows * D * 2;      // Q or dO tile
@@ -75,18 +75,33 @@ struct SmCfg {
   static constexpr int kQ = 2 * kKvTileBytes;                   // + s * kQTileBytes
   static constexpr int kO = kQ + kQStages * kQTileBytes;        // dO: one stage
   static constexpr int kDs = kO + kQTileBytes;                  // [query atom][key row][64 queries]
-  // per Q stage: -lse*log2e [128], -D [128], then the bias window (255 entries,
-  // times log2e) in two copies shifted by 0 and 1 entries, kBiasCopy floats
-  // apart (every key row finds its 64 entries 8-byte aligned in one copy, and
-  // with this stride the 64-bit loads of a warp hit every bank once)
+  // per Q stage: without the extra product step (below) -lse*log2e [128] and
+  // -D [128]; then the bias window (255 entries, times log2e) in two copies
+  // shifted by 0 and 1 entries, kBiasCopy floats apart (every key row finds
+  // its 64 entries 8-byte aligned in one copy, and with this stride the
+  // 64-bit loads of a warp hit every bank once)
   static constexpr int kBiasCopy = 270;
-  static constexpr int kStatFloats = 2 * kQRows + 2 * kBiasCopy + 4;  // (16-byte multiple)
+  static constexpr int kWinOff = kAug ? 0 : 2 * kQRows;                // floats
+  static constexpr int kStatFloats = kWinOff + 2 * kBiasCopy + 4;      // (16-byte multiple)
   static constexpr int kStats = kDs + kDsBytes;
-  static constexpr int kDqStage = kStats + kQStages * kStatFloats * 4;  // per-warp buffers
+  // kAug: an extra K = 16 step of the score and dP products, per Q stage: row i holds
+  // (a_hi, a_lo, d_hi, d_lo, 0, ...) in bf16, with a = -lse * log2e / c and
+  // d = -D split into two bf16 terms (canonical K-major layout without
+  // swizzle: core matrices of 8 rows x 16 bytes, the two k halves 128 bytes
+  // apart, row groups 256 bytes apart).  Two selector operands, whose rows are
+  // (1, 1, 0, ...) and (0, 0, 1, 1, 0, ...), pick a or d: the products come
+  // out of TMEM as S^T - lse log2e / c and dP^T - D.
+  // Taken with a relative-position table, whose window loads already fill the
+  // activation's shared-memory reads (without one, the extra tensor work
+  // costs more than the lse and D loads it saves).
+  static constexpr int kSel = kStats + kQStages * kStatFloats * 4;     // 2 x 256 bytes
+  static constexpr int kAugBytes = kQRows * 32;
+  static constexpr int kAugRows = kSel + (kAug ? 512 : 0);              // + s * kAugBytes
+  static constexpr int kDqStage = kAugRows + (kAug ? kQStages * kAugBytes : 0);  // per-warp buffers
   // bias-table gradient: per tile, dS summed along its 255 diagonals (two
   // buffers of 256 floats, then {first diagonal, head})
   static constexpr int kDbBuf = 256 * 4 + 16;
-  static constexpr int kDqWarpBufs = 3;                    // per warp: [16 queries][32 channels]
+  static constexpr int kDqWarpBufs = kAug ? 2 : 3;         // per warp: [16 queries][32 channels]
   static constexpr int kDb = kDqStage + 4 * kDqWarpBufs * kDqChunk * 32 * 4;
   static constexpr int kBar = kDb + 2 * kDbBuf;
   static constexpr int kKvFull = 0, kKvEmpty = 1;
@@ -117,6 +132,14 @@ struct SmCfg {
 };
 
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+
+// Score multiplier c = scale * log2e of the exponent, kept away from 0: the
+// extra product step carries -lse log2e / c, and a scale of 0 (scores that do
+// not count) then leaves S * c at 1e-30 * S, which rounds away against lse.
+__device__ __forceinline__ float score_mul(float scale) {
+  const float c = scale * 1.4426950408889634f;
+  return fabsf(c) < 1e-30f ? (c < 0.0f ? -1e-30f : 1e-30f) : c;
+}
 
 struct SmItem {
   int b, head, kb;
@@ -159,12 +182,12 @@ __device__ __forceinline__ SmItem decode_sm(int2 it, const BwdParams& p) {
 // are consecutive keys, so each load is one coalesced 128-byte row segment).
 // kRope: dK (here) and dQ (in the accumulator's conversion) go back through
 // the rotary embedding.
-template <int D, bool kBand, bool kDBias, bool kDense, bool kRope>
+template <int D, bool kBand, bool kDBias, bool kDense, bool kRope, bool kAug>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
               const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
               const __grid_constant__ CUtensorMap tmap_dq, const BwdParams p) {
-  using C = SmCfg<D>;
+  using C = SmCfg<D, kAug>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -211,6 +234,18 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   if (kDBias)
     for (int i = threadIdx.x; i < 2 * C::kDbBuf / 4; i += kThreads)
       reinterpret_cast<float*>(gbase + C::kDb)[i] = 0.0f;
+  // selectors and the zero columns of the extra product step (written once;
+  // the producer rewrites only the first 8 bytes of each row per tile)
+  if (kAug)
+  for (int i = threadIdx.x; i < (512 + C::kQStages * C::kAugBytes) / 4; i += kThreads) {
+    uint32_t v = 0;
+    if (i < 128) {  // selector words: 8 rows x 16 bytes per k half
+      const int sel = i / 64, kh = (i / 32) & 1, word = i & 3;  // 4 words per 16-byte row
+      if (kh == 0 && word == sel) v = 0x3F803F80u;            // bf16 pair (1, 1)
+    }
+    reinterpret_cast<uint32_t*>(gbase + C::kSel)[i] = v;
+  }
+  fence_proxy_async_smem();
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
@@ -274,6 +309,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       // Per-lane values of one query tile, fetched one tile ahead: lse*log2e
       // and D for columns lane + 32k, bias-window entries lane + 32k.
       const int rel_w = 2 * p.max_rel - 1;
+      const float inv_c = 1.0f / score_mul(p.scale);
       const float* brow =
           p.bias_table ? p.bias_table + static_cast<long long>(in.head) * rel_w : nullptr;
       constexpr int kWin = kQRows + kKRows - 1;  // 255 relative positions
@@ -311,10 +347,27 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         w = mbar_wait(bar(C::kQEmpty + s), ph ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, w)) { ok = false; if (lane == 0) fail(); break; }
         float* st = stats + s * C::kStatFloats;
+        if (!kAug) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            st[lane + 32 * k] = cur[2 * k];
+            st[kQRows + lane + 32 * k] = cur[2 * k + 1];
+          }
+        } else {
+        // extra product step: a = -lse log2e / c and d = -D as bf16 (hi, lo)
+        // pairs in the first 8 bytes of row i (queries past the sample get 0)
+        uint8_t* aug = gbase + C::kAugRows + s * C::kAugBytes;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          st[lane + 32 * k] = cur[2 * k];
-          st[kQRows + lane + 32 * k] = cur[2 * k + 1];
+          const int i = lane + 32 * k;
+          const float a = cur[2 * k] * inv_c, dd = cur[2 * k + 1];
+          const uint32_t ah = pack_bf16x2(a, 0.0f) & 0xFFFFu;
+          const uint32_t dh = pack_bf16x2(dd, 0.0f) & 0xFFFFu;
+          const float al = a - __uint_as_float(ah << 16), dl = dd - __uint_as_float(dh << 16);
+          *reinterpret_cast<uint2*>(aug + (i >> 3) * 256 + (i & 7) * 16) =
+              make_uint2(ah | (pack_bf16x2(al, 0.0f) << 16), dh | (pack_bf16x2(dl, 0.0f) << 16));
+        }
+        fence_proxy_async_smem();
         }
         if (brow != nullptr) {
 #pragma unroll
@@ -322,7 +375,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
             if (lane + 32 * k < kWin) {
 #pragma unroll
               for (int cp = 0; cp < 2; ++cp)  // copy cp holds entry e at position e + cp
-                st[2 * kQRows + cp * C::kBiasCopy + cp + lane + 32 * k] = cur[8 + k];
+                st[C::kWinOff + cp * C::kBiasCopy + cp + lane + 32 * k] = cur[8 + k];
             }
         }
         float nxt[16];
@@ -385,22 +438,29 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       const uint64_t dsc_omn = sdesc(sbase + C::kO, C::kAtom, 1024, kSwizzle128B);  // B of dV
       const uint64_t dsc_ds = sdesc(sbase + C::kDs, 0, 1024, kSwizzle128B);  // A of dK (K-major)
       const uint64_t dsc_dsmn = sdesc(sbase + C::kDs, C::kAtom, 1024, kSwizzle128B);  // B of dQ^T (MN-major)
+      // extra K = 16 step (no swizzle: k halves 128 bytes apart, row groups 256
+      // apart; the selectors repeat one 8-row group, stride 0)
+      const uint64_t dsc_aug = sdesc(sbase + C::kAugRows, 128, 256, 0);      // B
+      const uint64_t dsc_sel_a = sdesc(sbase + C::kSel, 128, 0, 0);          // A: picks a
+      const uint64_t dsc_sel_d = sdesc(sbase + C::kSel + 256, 128, 0, 0);    // A: picks d
       uint32_t it = 0, g = 0, kvi = 0, oc = 0, pc = 0, qe = 0, dkvc = 0;
       bool dq_pending = false, issued_any = false;
       bool ok = true;
-      auto issue_s = [&](uint32_t s) {  // S^T = K Q^T
+      auto issue_s = [&](uint32_t s) {  // S^T = K Q^T (kAug: - lse log2e / c)
         const uint64_t qb = dadd(dsc_q, s * C::kQTileBytes);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks / 4) * C::kAtom + (ks % 4) * 32;
           mma_f16_ss(tmem + kColS, dadd(dsc_k, off), dadd(qb, off), idesc_s, ks > 0 ? 1u : 0u);
         }
+        if (kAug) mma_f16_ss(tmem + kColS, dsc_sel_a, dadd(dsc_aug, s * C::kAugBytes), idesc_s, 1u);
         mma_commit(bar(C::kSFull));
         issued_any = true;
       };
-      // dP^T = V dO^T into the dP columns, once dO has landed and the dQ group
-      // has read the previous dQ^T out of the same columns.
-      auto issue_dp = [&]() -> bool {
+      // dP^T = V dO^T (kAug: - D of the tile in Q stage s) into the dP columns,
+      // once dO has landed and the dQ group has read the previous dQ^T out of
+      // the same columns.
+      auto issue_dp = [&](uint32_t s) -> bool {
         if (!mbar_wait(bar(C::kOFull), oc & 1u, abort_flag)) return false;
         ++oc;
         if (dq_pending) {
@@ -414,6 +474,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           const uint32_t off = (ks / 4) * C::kAtom + (ks % 4) * 32;
           mma_f16_ss(tmem + kColDP, dadd(dsc_v, off), dadd(dsc_o, off), idesc_s, ks > 0 ? 1u : 0u);
         }
+        if (kAug) mma_f16_ss(tmem + kColDP, dsc_sel_d, dadd(dsc_aug, s * C::kAugBytes), idesc_s, 1u);
         mma_commit(bar(C::kDpFull));
         return true;
       };
@@ -433,7 +494,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           if (!mbar_wait(bar(C::kQFull + s0), (g / C::kQStages) & 1u, abort_flag)) { fail(); break; }
           tc_fence_after();
           issue_s(s0);
-          if (!issue_dp()) { fail(); break; }
+          if (!issue_dp(s0)) { fail(); break; }
         }
         for (int t = 0; t < in.nq; ++t) {
           const uint32_t gt = g + t;
@@ -480,7 +541,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
                        dadd(qmn, ks * 2048), idesc_acc, (t == 0 && ks == 0) ? 0u : 1u);
           mma_commit(bar(C::kQEmpty + s));
           dq_pending = true;
-          if (t + 1 < in.nq && !issue_dp()) { ok = false; fail(); break; }
+          if (t + 1 < in.nq && !issue_dp((gt + 1) % C::kQStages)) { ok = false; fail(); break; }
         }
         if (!ok) break;
         mma_commit(bar(C::kDkvFull));
@@ -499,7 +560,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     const int grp = warp >> 2;           // query columns [64 grp, 64 grp + 64) of a tile
     const int j = wq * 32 + lane;        // key row within the block = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const float c_s = p.scale * kLog2e;
+    const float c_s = score_mul(p.scale);
     const bool has_bias = p.bias_table != nullptr;
     uint32_t it = 0, g = 0;
     while (true) {
@@ -534,12 +595,12 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); abort_now = true; break; }
         tc_fence_after();
         const float* st = stats + s * C::kStatFloats;
-        const float4* st4 = reinterpret_cast<const float4*>(st);  // 16-byte aligned
         // bias(query c, key j) * log2e is window entry c - j + 127; the copy
         // shifted by (j + 1) % 2 holds entries c0 - j + 127 .. (c0 even) at an
         // 8-byte aligned position.
         const int cp = (j + 1) & 1;
-        const float* bwin = st + 2 * kQRows + cp * C::kBiasCopy + cp + (kKRows - 1) - j;
+        const float4* st4 = reinterpret_cast<const float4*>(st);  // 16-byte aligned
+        const float* bwin = st + C::kWinOff + cp * C::kBiasCopy + cp + (kKRows - 1) - j;
         const int qloc = (in.qt0 + t) * kQRows;
         const bool full = qloc >= full_lo && qloc + kQRows <= full_hi;
         int c_lo = 0, c_hi = kQRows;  // valid query columns: c_lo <= c < c_hi
@@ -561,7 +622,6 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
             constexpr bool kBias = decltype(biased)::value;
 #pragma unroll
             for (int q4 = 0; q4 < 16; ++q4) {
-              const float4 l4 = st4[(c0 >> 2) + q4];
               float bv[4] = {0.f, 0.f, 0.f, 0.f};
               if (kDense) {
 #pragma unroll
@@ -576,11 +636,13 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
                 const float2 b23 = *reinterpret_cast<const float2*>(bwin + c0 + 4 * q4 + 2);
                 bv[0] = b01.x; bv[1] = b01.y; bv[2] = b23.x; bv[3] = b23.y;
               }
-              // exponent pairs: S * scale*log2e + (bias - lse)*log2e, two lanes per instruction
-              float2 off[2] = {make_float2(l4.x, l4.y), make_float2(l4.z, l4.w)};  // -lse*log2e
-              if (kBias) {
-                off[0] = add_f32x2(make_float2(bv[0], bv[1]), off[0]);
-                off[1] = add_f32x2(make_float2(bv[2], bv[3]), off[1]);
+              // exponent pairs: S * c + (bias - lse) log2e, two lanes per
+              // instruction (kAug: the product step already subtracted lse)
+              float2 off[2] = {make_float2(bv[0], bv[1]), make_float2(bv[2], bv[3])};
+              if (!kAug) {
+                const float4 l4 = st4[(c0 >> 2) + q4];  // -lse*log2e
+                off[0] = add_f32x2(make_float2(l4.x, l4.y), off[0]);
+                off[1] = add_f32x2(make_float2(l4.z, l4.w), off[1]);
               }
               const uint32_t* sq = &sr[4 * q4];
               const float2 x01 = fma_f32x2(make_float2(__uint_as_float(sq[0]), __uint_as_float(sq[1])),
@@ -612,9 +674,10 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         tmem_st_wait();
         tc_fence_before();
         warp_arrive(bar(C::kPFull), lane);
-        // Phase 2: dS^T = P^T (dP^T - D) once dP^T of this tile is in TMEM.  The
-        // product is taken on bf16 pairs: dS goes to the MMAs as bf16 anyway,
-        // and the extra rounding of dP - D adds at most 2^-9 relative error.
+        // Phase 2: dS^T = P^T (dP^T - D) once dP^T - D of this tile is in TMEM
+        // (the product step subtracted D).  The product is taken on bf16 pairs:
+        // dS goes to the MMAs as bf16 anyway, and the extra rounding of dP - D
+        // adds at most 2^-9 relative error.
         w = mbar_wait(bar(C::kDpFull), g & 1u, abort_flag);
         // the diagonal buffer of this tile was flushed two tiles ago
         if (kDBias) w = w && mbar_wait(bar(C::kDbFree + (g & 1u)), ((g >> 1) & 1u) ^ 1u, abort_flag);
@@ -628,16 +691,17 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           uint32_t dr[32];
           tmem_ld32(tmem + lane_off + kColDP + c0, dr);
           uint32_t dh[16];
-          // dP - D in fp32, rounded to bf16 pairs, times the bf16 P pairs (masked
-          // P is exactly 0, so masked dS is too).
+          // dP - D rounded to bf16 pairs, times the bf16 P pairs (masked P is
+          // exactly 0, so masked dS is too).
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
-            const float4 d4 = st4[((kQRows + c0) >> 2) + q4];
-            const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-            const float2 v01 = add_f32x2(make_float2(__uint_as_float(dr[4 * q4]), __uint_as_float(dr[4 * q4 + 1])),
-                                         make_float2(dd[0], dd[1]));  // -D
-            const float2 v23 = add_f32x2(make_float2(__uint_as_float(dr[4 * q4 + 2]), __uint_as_float(dr[4 * q4 + 3])),
-                                         make_float2(dd[2], dd[3]));
+            float2 v01 = make_float2(__uint_as_float(dr[4 * q4]), __uint_as_float(dr[4 * q4 + 1]));
+            float2 v23 = make_float2(__uint_as_float(dr[4 * q4 + 2]), __uint_as_float(dr[4 * q4 + 3]));
+            if (!kAug) {
+              const float4 d4 = st4[((kQRows + c0) >> 2) + q4];  // -D
+              v01 = add_f32x2(v01, make_float2(d4.x, d4.y));
+              v23 = add_f32x2(v23, make_float2(d4.z, d4.w));
+            }
             dh[2 * q4] = mul_bf16x2(pp[16 * half + 2 * q4], pack_bf16x2(v01.x, v01.y));
             dh[2 * q4 + 1] = mul_bf16x2(pp[16 * half + 2 * q4 + 1], pack_bf16x2(v23.x, v23.y));
           }
@@ -831,24 +895,41 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   }
 }
 
-template <int D, bool kBand, bool kDBias, bool kDense, bool kRope = false>
-cudaError_t launch_sm(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                      const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
-                      int grid, cudaStream_t s) {
-  using C = SmCfg<D>;
+template <int D, bool kBand, bool kDBias, bool kDense, bool kRope, bool kAug>
+cudaError_t launch_sm_cfg(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                          int grid, cudaStream_t s) {
+  using C = SmCfg<D, kAug>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   // The register split (setmaxnreg) hands out exactly the launch's pool of
   // 128 per thread: refuse a build that launched with fewer.
   cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, bwd_sm_kernel<D, kBand, kDBias, kDense, kRope>);
+  cudaError_t e = cudaFuncGetAttributes(&fa, bwd_sm_kernel<D, kBand, kDBias, kDense, kRope, kAug>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != 128) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(bwd_sm_kernel<D, kBand, kDBias, kDense, kRope>,
+  e = cudaFuncSetAttribute(bwd_sm_kernel<D, kBand, kDBias, kDense, kRope, kAug>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  bwd_sm_kernel<D, kBand, kDBias, kDense, kRope><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo,
-                                                                                   tdq, p);
+  bwd_sm_kernel<D, kBand, kDBias, kDense, kRope, kAug><<<grid, kThreads, C::kSmemBytes, s>>>(
+      tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
+}
+
+// The extra product step goes with a relative-position table (always present
+// with its gradient; never with a dense bias).
+template <int D, bool kBand, bool kDBias, bool kDense, bool kRope = false>
+cudaError_t launch_sm(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                      const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                      int grid, cudaStream_t s) {
+  if constexpr (kDBias) {
+    return launch_sm_cfg<D, kBand, true, kDense, kRope, true>(p, tq, tk, tv, tdo, tdq, grid, s);
+  } else if constexpr (kDense) {
+    return launch_sm_cfg<D, kBand, false, true, kRope, false>(p, tq, tk, tv, tdo, tdq, grid, s);
+  } else {
+    if (p.bias_table != nullptr)
+      return launch_sm_cfg<D, kBand, false, false, kRope, true>(p, tq, tk, tv, tdo, tdq, grid, s);
+    return launch_sm_cfg<D, kBand, false, false, kRope, false>(p, tq, tk, tv, tdo, tdq, grid, s);
+  }
 }
 
 }  // namespace

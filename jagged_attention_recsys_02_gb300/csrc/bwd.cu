@@ -499,12 +499,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         uint8_t* dsrow = gbase + C::kDs + buf * C::kDsParts * C::kDsBytes + j * 128;
         uint32_t sr[32];
         tmem_ld32(t_s + cbase, sr);  // all 32 scores first: P overwrites them in place
+        // bias-table gradient: this lane's sums along four diagonals of the tile
+        float diag[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int c0 = cbase + half * 16;
           uint32_t dr[16];
           tmem_ld16(t_dp + c0, dr);
           uint32_t phi[8], plo[8], dhi[8], dlo[8];
+          float xd[16];  // dS of the 16 columns (bias-table gradient only)
 #pragma unroll
           for (int i = 0; i < 16; i += 2) {
             float pv[2], dv[2];
@@ -534,10 +537,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
                 pv[e] = 0.0f;
                 dv[e] = 0.0f;
               }
-              // dS(query c, key j) lies on diagonal c - j + 127 of the tile
-              if (kDBias)
-                atomicAdd(reinterpret_cast<float*>(gbase + C::kDb + (g & 1u) * C::kDbBuf) + c - j + 127,
-                          dv[e]);
+              if (kDBias) xd[i + e] = dv[e];
             }
             const uint32_t ph = pack_bf16x2(pv[0], pv[1]);
             const uint32_t dh = pack_bf16x2(dv[0], dv[1]);
@@ -549,6 +549,20 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
               dlo[i / 2] = pack_bf16x2(dv[0] - __uint_as_float(dh << 16),
                                        dv[1] - __uint_as_float(dh & 0xFFFF0000u));
             }
+          }
+          if (kDBias) {
+            // dS(query c0 + i, key j = 32 wq + lane) lies on diagonal
+            // (c0 - 32 wq + 127) + (i - lane).  Lane l gathers the warp's values
+            // with i - src = l (mod 32): at step i it reads column i of lane
+            // (i - l) mod 32, whose offset is l when i >= l and l - 32 otherwise.
+            float up = 0.0f, down = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float v = __shfl_sync(0xffffffffu, xd[i], (i - lane) & 31);
+              if (i >= lane) up += v; else down += v;
+            }
+            diag[2 * half] += down;
+            diag[2 * half + 1] += up;
           }
           // P^T: query pair c/2 of the 32-column chunk lives at column chunk*32 + c/2 (hi)
           // and chunk*32 + 16 + c/2 (lo), where the dV MMA reads it.
@@ -565,6 +579,19 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
             if (kSplit)
               *reinterpret_cast<uint4*>(dsrow + C::kDsBytes + phys) =
                   make_uint4(dlo[4 * v], dlo[4 * v + 1], dlo[4 * v + 2], dlo[4 * v + 3]);
+          }
+        }
+        if (kDBias) {
+          // window entry (query - key + 127); a warp's lanes hit consecutive words
+          float* win = reinterpret_cast<float*>(gbase + C::kDb + (g & 1u) * C::kDbBuf) +
+                       (cbase - 32 * wq + 127 + lane);
+          if (lane > 0) {  // some column lies left of this lane's diagonal
+            atomicAdd(win - 32, diag[0]);
+            atomicAdd(win - 16, diag[2]);
+          }
+          if (lane < 16) {  // some column lies on or right of it
+            atomicAdd(win, diag[1]);
+            atomicAdd(win + 16, diag[3]);
           }
         }
         tmem_st_wait();

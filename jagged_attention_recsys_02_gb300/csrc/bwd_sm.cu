@@ -685,6 +685,9 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         tc_fence_after();
         // dS^T row j, query atom grp: 16-byte chunk cc (8 queries) at (cc ^ (j % 8))
         uint8_t* dsrow = gbase + C::kDs + grp * C::kAtom + j * 128;
+        // bias-table gradient: this lane's sums along six diagonals of the tile
+        // (see below), offsets -32, -31, 0, 1, 32, 33 from its own
+        float diag[6] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int c0 = 64 * grp + 32 * half;
@@ -712,15 +715,40 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
                 make_uint4(dh[4 * v], dh[4 * v + 1], dh[4 * v + 2], dh[4 * v + 3]);
           }
           if (kDBias) {
-            // dS(query c, key j) lies on diagonal c - j + 127 of the tile: a
-            // warp's lanes hit consecutive words (no bank conflicts)
-            float* win = reinterpret_cast<float*>(gbase + C::kDb + (g & 1u) * C::kDbBuf) + (127 - j);
+            // dS(query c0 + i, key 32 wq + lane) lies on diagonal
+            // (c0 - 32 wq + 127) + (i - lane) of the tile.  Lane l gathers the
+            // warp's bf16 pairs (columns 2e, 2e + 1) with 2e - src = l (mod
+            // 32): at step e it reads pair e of lane (2e - l) mod 32, whose
+            // columns sit at offsets l, l + 1 when 2e >= l and l - 32, l - 31
+            // otherwise.  The second half is 32 columns further on.
+            float up0 = 0.0f, up1 = 0.0f, dn0 = 0.0f, dn1 = 0.0f;
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              atomicAdd(win + c0 + 2 * e, __uint_as_float(dh[e] << 16));
-              atomicAdd(win + c0 + 2 * e + 1, __uint_as_float(dh[e] & 0xFFFF0000u));
+              const uint32_t v = __shfl_sync(0xffffffffu, dh[e], (2 * e - lane) & 31);
+              const float v0 = __uint_as_float(v << 16), v1 = __uint_as_float(v & 0xFFFF0000u);
+              if (2 * e >= lane) {
+                up0 += v0;
+                up1 += v1;
+              } else {
+                dn0 += v0;
+                dn1 += v1;
+              }
             }
+            diag[2 * half] += dn0;      // offset 32 half - 32
+            diag[2 * half + 1] += dn1;  // 32 half - 31
+            diag[2 * half + 2] += up0;  // 32 half
+            diag[2 * half + 3] += up1;  // 32 half + 1
           }
+        }
+        if (kDBias) {
+          // window entry (query - key + 127) of the tile; a warp's lanes hit
+          // consecutive words (the sums outside the window are zero)
+          const int e0 = 127 - 32 * wq + 64 * grp + lane;
+          float* win = reinterpret_cast<float*>(gbase + C::kDb + (g & 1u) * C::kDbBuf);
+          constexpr int kOff[6] = {-32, -31, 0, 1, 32, 33};
+#pragma unroll
+          for (int k = 0; k < 6; ++k)
+            if (e0 + kOff[k] >= 0 && e0 + kOff[k] < 255) atomicAdd(win + e0 + kOff[k], diag[k]);
         }
         fence_proxy_async_smem();
         tc_fence_before();

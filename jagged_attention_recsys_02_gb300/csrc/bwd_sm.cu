@@ -360,7 +360,12 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int i = lane + 32 * k;
-          const float a = cur[2 * k] * inv_c, dd = cur[2 * k + 1];
+          // finite values only: the selectors' zeros multiply them too (a row
+          // whose lse is -inf has no probability mass: a = 0 gives it P = 0
+          // wherever its bias is -inf)
+          float a = cur[2 * k] * inv_c, dd = cur[2 * k + 1];
+          a = (fabsf(a) <= 1e38f) ? a : 0.0f;
+          dd = (fabsf(dd) <= 1e38f) ? dd : 0.0f;
           const uint32_t ah = pack_bf16x2(a, 0.0f) & 0xFFFFu;
           const uint32_t dh = pack_bf16x2(dd, 0.0f) & 0xFFFFu;
           const float al = a - __uint_as_float(ah << 16), dl = dd - __uint_as_float(dh << 16);

@@ -85,9 +85,10 @@ typedef enum { GDPA_BIAS_NONE = 0, GDPA_BIAS_RELPOS = 1, GDPA_BIAS_DENSE = 2 } g
  * array [B+1], offsets[0] = 0, offsets[b+1] - offsets[b] = H Lq_b Lkv_b;
  * a mismatch is reported as GDPA_ERR_BAD_OFFSETS through the device status).
  * max_rel is ignored.  The dense bias is read from global memory by the
- * kernels' activation warps; it is supported by gdpa_fwd, gdpa_bwd and
- * gdpa_fwd_noalloc (no window, no bias gradient); the other entry points
- * return GDPA_ERR_UNSUPPORTED. */
+ * kernels' activation warps; it is supported without a window by gdpa_fwd,
+ * gdpa_bwd, gdpa_fwd_noalloc and gdpa_bwd_window / gdpa_bwd_rope (these two
+ * also return its gradient); the other entry points, and a window > 0, give
+ * GDPA_ERR_UNSUPPORTED. */
 typedef struct {
   int kind;                /* gdpa_bias_kind */
   const float* table;      /* device pointer, ignored for GDPA_BIAS_NONE */
@@ -149,14 +150,20 @@ gdpa_status gdpa_bwd(const void* q, const int32_t* q_offsets, const void* k, con
  * loaded, and the scheduler's cost counts only the tiles inside it.  Every
  * other argument, output, workspace and error is that of gdpa_fwd /
  * gdpa_bwd; the backward must get the forward's window.
- * dbias (gdpa_bwd_window only; NULL = not computed): the gradient of a
- * learnable relative-position table ("custom attention biases", JFA
- * paragraph), fp32 device memory [H][2*max_rel-1], ADDED to (so gradients of
- * several calls accumulate; zero it first for a fresh gradient): entry t
- * receives the sum of dS_ij over the unmasked pairs whose clamped table
- * index (i - j + max_rel - 1) is t.  Needs a GDPA_BIAS_RELPOS bias
- * (GDPA_ERR_INVALID_ARG otherwise); every activation.  Its atomics make the
- * sums' order, and so their last bits, vary between runs. */
+ * dbias (gdpa_bwd_window and gdpa_bwd_rope; NULL = not computed): the
+ * gradient of a learnable bias ("custom attention biases", JFA paragraph),
+ * fp32 device memory, ADDED to (so gradients of several calls accumulate;
+ * zero it first for a fresh gradient); every activation.
+ *   GDPA_BIAS_RELPOS: [H][2*max_rel-1]; entry t receives the sum of dS_ij
+ *   over the unmasked pairs whose clamped table index (i - j + max_rel - 1)
+ *   is t.  Its atomics make the sums' order, and so their last bits, vary
+ *   between runs.
+ *   GDPA_BIAS_DENSE: the dense bias's own layout (offsets[B] floats); the
+ *   entry of each unmasked pair receives that pair's dS_ij (the bf16 value
+ *   the softmax kernel feeds its products, the fp32 one for the other
+ *   activations); masked pairs' entries are left as they are.
+ * dS_ij is the gradient of the loss with respect to s_ij = scale q_i.k_j +
+ * bias_ij.  Without a bias: GDPA_ERR_INVALID_ARG. */
 gdpa_status gdpa_fwd_window(const void* q, const int32_t* q_offsets, const void* k,
                             const void* v, const int32_t* kv_offsets, int B, int H, int d,
                             int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
@@ -215,10 +222,9 @@ gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k,
  * un-rotated q and k: the transposed rotation is applied to the fp32
  * gradients before rounding (dK in the kernel's epilogue, dQ in the
  * accumulator's conversion).  rope_base = 0: no rotary embedding (this is
- * gdpa_bwd_window); negative, infinite or NaN: GDPA_ERR_INVALID_ARG; with a
- * bias-table gradient or a dense bias: GDPA_ERR_UNSUPPORTED.  Every
- * other argument, output and error is that of gdpa_bwd_window; not available
- * for the MXFP8 backward. */
+ * gdpa_bwd_window); negative, infinite or NaN: GDPA_ERR_INVALID_ARG.  Every
+ * other argument, output and error (biases and their gradients included) is
+ * that of gdpa_bwd_window; not available for the MXFP8 backward. */
 gdpa_status gdpa_bwd_rope(const void* q, const int32_t* q_offsets, const void* k, const void* v,
                           const int32_t* kv_offsets, int B, int H, int d, int64_t Tq,
                           int64_t Tkv, const gdpa_bias* bias, int act, int causal, int window,

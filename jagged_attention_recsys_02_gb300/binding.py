@@ -208,9 +208,10 @@ def gdpa_bwd(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, act, causal=Fals
              bias=None, max_rel=0, window=0, dq=None, dk=None, dv=None, dbias=None,
              rope_base=0.0, workspace=None, stream=None):
     """Backward pass through the C ABI (gdpa_bwd, or gdpa_bwd_window when
-    window > 0 or a bias-table gradient `dbias` [H, 2*max_rel-1] fp32 is given,
-    which is added to; gdpa_bwd_rope when rope_base > 0, dq and dk then going
-    back through the rotary embedding).  Returns (dq, dk, dv)."""
+    window > 0 or a bias gradient `dbias` fp32 is given, which is added to: the
+    table's [H, 2*max_rel-1], or a dense bias's values' layout; gdpa_bwd_rope
+    when rope_base > 0, dq and dk then going back through the rotary
+    embedding).  Returns (dq, dk, dv)."""
     lib = load()
     Tq, H, d = q.shape
     Tkv = k.shape[0]

@@ -351,14 +351,12 @@ gdpa_status gdpa_bwd_rope(const void* q, const int32_t* q_offsets, const void* k
                           void* workspace, size_t ws_bytes, void* stream) {
   t_launches = 0;
   if (!(rope_base >= 0.0f) || rope_base == INFINITY) return GDPA_ERR_INVALID_ARG;  // NaN too
-  // the fused rotary backward is built without a table gradient or a dense bias
-  if (rope_base > 0.0f && (dbias != nullptr || is_dense(bias))) return GDPA_ERR_UNSUPPORTED;
   gdpa_status st = check_common(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act,
                                 causal, window);
   if (st != GDPA_OK) return st;
   if (dbias != nullptr) {
-    // the gradient of a relative-position table needs that table
-    if (bias == nullptr || bias->kind != GDPA_BIAS_RELPOS) return GDPA_ERR_INVALID_ARG;
+    // the gradient of a bias needs that bias (a relative-position table or a dense bias)
+    if (bias_kind(bias) == GDPA_BIAS_NONE) return GDPA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(dbias) & 3u) return GDPA_ERR_INVALID_ARG;
   }
   if (Tq > 0 && (dout == nullptr || dq == nullptr || !aligned16(dout) || !aligned16(dq)))

@@ -127,15 +127,20 @@ __device__ __forceinline__ BwdItem decode_bwd(int2 it, const BwdParams& p) {
 // With a bias-table gradient one more warp (14) adds each tile's diagonal
 // sums to the table.  kDense: a dense jagged bias (p.bias_dense) instead of
 // the relative-position table, read from global memory by the activation
-// warps (the warp's lanes are consecutive keys: coalesced row segments).
+// warps (the warp's lanes are consecutive keys: coalesced row segments); with
+// p.dbias its gradient goes back the same way, one reduction per pair.
 template <int D, int ACT, bool kDBias, bool kDense>
-__global__ void __launch_bounds__(kThreads + (kDBias ? 32 : 0), 1)
+__global__ void __launch_bounds__(kThreads + (kDBias && !kDense ? 32 : 0), 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
            const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
            const __grid_constant__ CUtensorMap tmap_dq, const BwdParams p) {
   constexpr bool kSoftmax = (ACT == GDPA_ACT_SOFTMAX);
   constexpr bool kSplit = !kSoftmax;
   using C = BwdCfg<D, kSplit>;
+  // kDBias: the bias's gradient, of the table (diagonal sums in shared memory,
+  // flushed by warp 14) or of the dense bias (reduced straight to memory)
+  constexpr bool kTableGrad = kDBias && !kDense;
+  constexpr bool kDenseGrad = kDBias && kDense;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -167,7 +172,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
     mbar_init(bar(C::kDkvEmpty), 128);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kItemFull + s), 1);
-      mbar_init(bar(C::kItemEmpty + s), 1 + kActThreads + 128 + (kDBias ? 1 : 0));
+      mbar_init(bar(C::kItemEmpty + s), 1 + kActThreads + 128 + (kTableGrad ? 1 : 0));
     }
     mbar_init(bar(C::kDrain), 1);
     for (int u = 0; u < 2; ++u) {
@@ -176,7 +181,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
     }
     fence_mbar_init();
   }
-  if (kDBias)
+  if (kTableGrad)
     for (int i = threadIdx.x; i < 2 * C::kDbBuf / 4; i += blockDim.x)
       reinterpret_cast<float*>(gbase + C::kDb)[i] = 0.0f;
   if (warp == 0) {
@@ -474,6 +479,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
                               ? p.bias_dense + p.bias_off[in.b] +
                                     static_cast<long long>(in.head) * in.Lq * in.Lkv + jl
                               : nullptr;
+      // its gradient (p.dbias given with a dense bias), same layout: gcol[i * Lkv]
+      float* gcol = (kDenseGrad && dcol != nullptr)
+                        ? p.dbias + (dcol - p.bias_dense)
+                        : nullptr;
       bool abort_now = false;
       for (int t = 0; t < in.nq; ++t, ++g) {
         const uint32_t s = g % C::kStages;
@@ -481,7 +490,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         w = mbar_wait(bar(C::kQdFull + s), (g / C::kStages) & 1u, abort_flag);
         w = w && mbar_wait(bar(C::kSFull + buf), suse[buf] & 1u, abort_flag);
         // the diagonal buffer of this tile was flushed two tiles ago
-        if (kDBias) w = w && mbar_wait(bar(C::kDbFree + (g & 1u)), ((g >> 1) & 1u) ^ 1u, abort_flag);
+        if (kTableGrad) w = w && mbar_wait(bar(C::kDbFree + (g & 1u)), ((g >> 1) & 1u) ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); abort_now = true; break; }
         suse[buf]++;
         tc_fence_after();
@@ -537,7 +546,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
                 pv[e] = 0.0f;
                 dv[e] = 0.0f;
               }
-              if (kDBias) xd[i + e] = dv[e];
+              // dense-bias gradient: each pair is visited once, its dS added
+              // straight to its entry
+              if (kDenseGrad && gcol != nullptr && c >= c_lo && c < c_hi)
+                atomicAdd(gcol + static_cast<long long>(qloc + c) * in.Lkv, dv[e]);
+              if (kTableGrad) xd[i + e] = dv[e];
             }
             const uint32_t ph = pack_bf16x2(pv[0], pv[1]);
             const uint32_t dh = pack_bf16x2(dv[0], dv[1]);
@@ -550,7 +563,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
                                        dv[1] - __uint_as_float(dh & 0xFFFF0000u));
             }
           }
-          if (kDBias) {
+          if (kTableGrad) {
             // dS(query c0 + i, key j = 32 wq + lane) lies on diagonal
             // (c0 - 32 wq + 127) + (i - lane).  Lane l gathers the warp's values
             // with i - src = l (mod 32): at step i it reads column i of lane
@@ -581,7 +594,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
                   make_uint4(dlo[4 * v], dlo[4 * v + 1], dlo[4 * v + 2], dlo[4 * v + 3]);
           }
         }
-        if (kDBias) {
+        if (kTableGrad) {
           // window entry (query - key + 127); a warp's lanes hit consecutive words
           float* win = reinterpret_cast<float*>(gbase + C::kDb + (g & 1u) * C::kDbBuf) +
                        (cbase - 32 * wq + 127 + lane);
@@ -598,7 +611,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(C::kPFull));
-        if (kDBias) {
+        if (kTableGrad) {
           if (j == 0 && cbase == 0) {
             int* meta = reinterpret_cast<int*>(gbase + C::kDb + (g & 1u) * C::kDbBuf + 192 * 4);
             meta[0] = qloc - kb0 - 127;  // diagonal (query - key) of window entry 0
@@ -609,7 +622,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       }
       if (abort_now) break;
     }
-  } else if (kDBias && warp == kMmaWarp + 1) {
+  } else if (kTableGrad && warp == kMmaWarp + 1) {
     // ------------------------------------------------------------ bias-table gradient
     // Per tile: wait for the activation threads' diagonal sums, add them to the
     // table (entry = clamp(query - key + max_rel - 1)), zero the buffer.
@@ -874,7 +887,8 @@ cudaError_t launch_main_db(const BwdParams& p, const CUtensorMap& tq, const CUte
   cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, ACT, kDBias, kDense>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  bwd_kernel<D, ACT, kDBias, kDense><<<grid, kThreads + (kDBias ? 32 : 0), C::kSmemBytes, s>>>(
+  bwd_kernel<D, ACT, kDBias, kDense><<<grid, kThreads + (kDBias && !kDense ? 32 : 0),
+                                      C::kSmemBytes, s>>>(
       tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
@@ -883,10 +897,11 @@ template <int D, int ACT>
 cudaError_t launch_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                         int grid, cudaStream_t s) {
-  if (p.bias_dense != nullptr)  // built without a window or a table gradient
-    return (p.window > 0 || p.dbias != nullptr)
-               ? cudaErrorInvalidValue
-               : launch_main_db<D, ACT, false, true>(p, tq, tk, tv, tdo, tdq, grid, s);
+  if (p.bias_dense != nullptr) {  // no window
+    if (p.window > 0) return cudaErrorInvalidValue;
+    return p.dbias != nullptr ? launch_main_db<D, ACT, true, true>(p, tq, tk, tv, tdo, tdq, grid, s)
+                              : launch_main_db<D, ACT, false, true>(p, tq, tk, tv, tdo, tdq, grid, s);
+  }
   return p.dbias != nullptr ? launch_main_db<D, ACT, true, false>(p, tq, tk, tv, tdo, tdq, grid, s)
                             : launch_main_db<D, ACT, false, false>(p, tq, tk, tv, tdo, tdq, grid, s);
 }

@@ -179,7 +179,8 @@ __device__ __forceinline__ SmItem decode_sm(int2 it, const BwdParams& p) {
 
 // kDense: a dense jagged bias (p.bias_dense) instead of the relative-position
 // table, read from global memory by the activation warps (the warp's lanes
-// are consecutive keys, so each load is one coalesced 128-byte row segment).
+// are consecutive keys, so each load is one coalesced 128-byte row segment);
+// with p.dbias its gradient goes back the same way, one reduction per pair.
 // kRope: dK (here) and dQ (in the accumulator's conversion) go back through
 // the rotary embedding.
 template <int D, bool kBand, bool kDBias, bool kDense, bool kRope, bool kAug>
@@ -188,6 +189,10 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
               const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
               const __grid_constant__ CUtensorMap tmap_dq, const BwdParams p) {
   using C = SmCfg<D, kAug>;
+  // kDBias: the bias's gradient, of the table (diagonal sums in shared memory,
+  // flushed by warp 14) or of the dense bias (reduced straight to memory)
+  constexpr bool kTableGrad = kDBias && !kDense;
+  constexpr bool kDenseGrad = kDBias && kDense;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -222,7 +227,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     mbar_init(bar(C::kDkvEmpty), 4);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kItemFull + s), 1);
-      mbar_init(bar(C::kItemEmpty + s), 1 + kActWarps + 4 + (kDBias ? 1 : 0));
+      mbar_init(bar(C::kItemEmpty + s), 1 + kActWarps + 4 + (kTableGrad ? 1 : 0));
     }
     mbar_init(bar(C::kDrain), 1);
     for (int u = 0; u < 2; ++u) {
@@ -231,7 +236,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     }
     fence_mbar_init();
   }
-  if (kDBias)
+  if (kTableGrad)
     for (int i = threadIdx.x; i < 2 * C::kDbBuf / 4; i += kThreads)
       reinterpret_cast<float*>(gbase + C::kDb)[i] = 0.0f;
   // selectors and the zero columns of the extra product step (written once;
@@ -592,6 +597,10 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
                               ? p.bias_dense + p.bias_off[in.b] +
                                     static_cast<long long>(in.head) * in.Lq * in.Lkv + jl
                               : nullptr;
+      // its gradient (p.dbias given with a dense bias), same layout: gcol[i * Lkv]
+      float* gcol = (kDenseGrad && dcol != nullptr)
+                        ? p.dbias + (dcol - p.bias_dense)
+                        : nullptr;
       bool abort_now = false;
       for (int t = 0; t < in.nq; ++t, ++g) {
         const uint32_t s = g % C::kQStages;
@@ -685,7 +694,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         // adds at most 2^-9 relative error.
         w = mbar_wait(bar(C::kDpFull), g & 1u, abort_flag);
         // the diagonal buffer of this tile was flushed two tiles ago
-        if (kDBias) w = w && mbar_wait(bar(C::kDbFree + (g & 1u)), ((g >> 1) & 1u) ^ 1u, abort_flag);
+        if (kTableGrad) w = w && mbar_wait(bar(C::kDbFree + (g & 1u)), ((g >> 1) & 1u) ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); abort_now = true; break; }
         tc_fence_after();
         // dS^T row j, query atom grp: 16-byte chunk cc (8 queries) at (cc ^ (j % 8))
@@ -719,7 +728,21 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
             *reinterpret_cast<uint4*>(dsrow + ((cc ^ (j & 7)) * 16)) =
                 make_uint4(dh[4 * v], dh[4 * v + 1], dh[4 * v + 2], dh[4 * v + 3]);
           }
-          if (kDBias) {
+          if (kDenseGrad && gcol != nullptr) {
+            // dense-bias gradient: each pair of the tile is visited once, so
+            // its dS is added straight to its entry (a warp's lanes are
+            // consecutive keys: one 128-byte segment per query column)
+            float* gt = gcol + static_cast<long long>(qloc + c0) * in.Lkv;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int c = c0 + 2 * e;
+              if (c >= c_lo && c < c_hi) atomicAdd(gt, __uint_as_float(dh[e] << 16));
+              gt += in.Lkv;
+              if (c + 1 >= c_lo && c + 1 < c_hi) atomicAdd(gt, __uint_as_float(dh[e] & 0xFFFF0000u));
+              gt += in.Lkv;
+            }
+          }
+          if (kTableGrad) {
             // dS(query c0 + i, key 32 wq + lane) lies on diagonal
             // (c0 - 32 wq + 127) + (i - lane) of the tile.  Lane l gathers the
             // warp's bf16 pairs (columns 2e, 2e + 1) with 2e - src = l (mod
@@ -745,7 +768,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
             diag[2 * half + 3] += up1;  // 32 half + 1
           }
         }
-        if (kDBias) {
+        if (kTableGrad) {
           // window entry (query - key + 127) of the tile; a warp's lanes hit
           // consecutive words (the sums outside the window are zero)
           const int e0 = 127 - 32 * wq + 64 * grp + lane;
@@ -758,7 +781,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         fence_proxy_async_smem();
         tc_fence_before();
         warp_arrive(bar(C::kDsFull), lane);
-        if (kDBias) {
+        if (kTableGrad) {
           if (j == 0 && grp == 0) {
             int* meta = reinterpret_cast<int*>(gbase + C::kDb + (g & 1u) * C::kDbBuf + 256 * 4);
             meta[0] = qloc - kb0 - 127;  // diagonal (query - key) of window entry 0
@@ -883,7 +906,7 @@ bwd_sm_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     if (lane == 0) bulk_wait_group_all();  // every dQ reduce issued by this thread has landed
   } else {
     setmaxnreg_dec<kRegsLow>();  // spare warps of the last warpgroup
-    if (kDBias && warp == kMmaWarp + 1) {
+    if (kTableGrad && warp == kMmaWarp + 1) {
       // ---------------------------------------------------------- bias-table gradient
       // Per tile: wait for the activation warps' diagonal sums, add them to the
       // table (entry = clamp(query - key + max_rel - 1)), zero the buffer.
@@ -950,14 +973,14 @@ cudaError_t launch_sm_cfg(const BwdParams& p, const CUtensorMap& tq, const CUten
 
 // The extra product step goes with a relative-position table (always present
 // with its gradient; never with a dense bias).
-template <int D, bool kBand, bool kDBias, bool kDense, bool kRope = false>
+template <int D, bool kBand, bool kDBias, bool kDense, bool kRope>
 cudaError_t launch_sm(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                       int grid, cudaStream_t s) {
-  if constexpr (kDBias) {
-    return launch_sm_cfg<D, kBand, true, kDense, kRope, true>(p, tq, tk, tv, tdo, tdq, grid, s);
-  } else if constexpr (kDense) {
-    return launch_sm_cfg<D, kBand, false, true, kRope, false>(p, tq, tk, tv, tdo, tdq, grid, s);
+  if constexpr (kDense) {
+    return launch_sm_cfg<D, kBand, kDBias, true, kRope, false>(p, tq, tk, tv, tdo, tdq, grid, s);
+  } else if constexpr (kDBias) {
+    return launch_sm_cfg<D, kBand, true, false, kRope, true>(p, tq, tk, tv, tdo, tdq, grid, s);
   } else {
     if (p.bias_table != nullptr)
       return launch_sm_cfg<D, kBand, false, false, kRope, true>(p, tq, tk, tv, tdo, tdq, grid, s);
@@ -965,28 +988,23 @@ cudaError_t launch_sm(const BwdParams& p, const CUtensorMap& tq, const CUtensorM
   }
 }
 
-}  // namespace
-
-cudaError_t launch_bwd_softmax_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                                    const CUtensorMap& tv, const CUtensorMap& tdo,
-                                    const CUtensorMap& tdq, int grid, cudaStream_t s) {
-  const bool band = p.window > 0, db = p.dbias != nullptr;
-  if (p.rope_base > 0.0f) {  // built without a table gradient or a dense bias
-    if (db || p.bias_dense != nullptr) return cudaErrorInvalidValue;
+template <bool kRope>
+cudaError_t dispatch_sm(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                           int grid, cudaStream_t s) {
+  const bool band = p.window > 0;
+  const bool db = p.dbias != nullptr;
+  if (p.bias_dense != nullptr) {  // no window
+    if (band) return cudaErrorInvalidValue;
     if (p.d == 64)
-      return band ? launch_sm<64, true, false, false, true>(p, tq, tk, tv, tdo, tdq, grid, s)
-                  : launch_sm<64, false, false, false, true>(p, tq, tk, tv, tdo, tdq, grid, s);
-    return band ? launch_sm<128, true, false, false, true>(p, tq, tk, tv, tdo, tdq, grid, s)
-                : launch_sm<128, false, false, false, true>(p, tq, tk, tv, tdo, tdq, grid, s);
-  }
-  if (p.bias_dense != nullptr) {  // the dense bias is built without a window or table gradient
-    if (band || db) return cudaErrorInvalidValue;
-    return p.d == 64 ? launch_sm<64, false, false, true>(p, tq, tk, tv, tdo, tdq, grid, s)
-                     : launch_sm<128, false, false, true>(p, tq, tk, tv, tdo, tdq, grid, s);
+      return db ? launch_sm<64, false, true, true, kRope>(p, tq, tk, tv, tdo, tdq, grid, s)
+                : launch_sm<64, false, false, true, kRope>(p, tq, tk, tv, tdo, tdq, grid, s);
+    return db ? launch_sm<128, false, true, true, kRope>(p, tq, tk, tv, tdo, tdq, grid, s)
+              : launch_sm<128, false, false, true, kRope>(p, tq, tk, tv, tdo, tdq, grid, s);
   }
 #define GDPA_SM_LAUNCH(DD, BB, DBB) \
   if (p.d == DD && band == BB && db == DBB) \
-    return launch_sm<DD, BB, DBB, false>(p, tq, tk, tv, tdo, tdq, grid, s);
+    return launch_sm<DD, BB, DBB, false, kRope>(p, tq, tk, tv, tdo, tdq, grid, s);
   GDPA_SM_LAUNCH(64, false, false)
   GDPA_SM_LAUNCH(64, false, true)
   GDPA_SM_LAUNCH(64, true, false)
@@ -997,6 +1015,15 @@ cudaError_t launch_bwd_softmax_main(const BwdParams& p, const CUtensorMap& tq, c
   GDPA_SM_LAUNCH(128, true, true)
 #undef GDPA_SM_LAUNCH
   return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_softmax_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                    const CUtensorMap& tv, const CUtensorMap& tdo,
+                                    const CUtensorMap& tdq, int grid, cudaStream_t s) {
+  return p.rope_base > 0.0f ? dispatch_sm<true>(p, tq, tk, tv, tdo, tdq, grid, s)
+                            : dispatch_sm<false>(p, tq, tk, tv, tdo, tdq, grid, s);
 }
 
 }  // namespace gdpa

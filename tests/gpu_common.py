@@ -127,3 +127,45 @@ def to_np(t):
 
 def scale_for(d):
     return 1.0 / math.sqrt(d)
+
+
+def ds_pair_bounds(qn, qo, kn, vn, ko, don, o_ref, *, act, causal, scale, window=0,
+                   bias_of=None):
+    """Per (sample, head) of a backward problem: the unmasked pairs and a bound
+    on the kernels' rounding in each pair's dS, from fp64 quantities of the
+    same inputs.  Softmax: the kernel's D = rowsum(dO * O) uses the
+    bf16-rounded O (relative error <= 2^-9 per element) and dS is formed from
+    bf16 P and dP - D and rounded to bf16 (2^-9 each); per pair about
+    |P| 2^-8 (|dP - D| + sum_c |dO_c O_c|).  GDPA: dS = act'(s) dP in fp32
+    from fp32 scores; per pair at most 1.2 |dP| 2^-8 (|act'| <= 1.2 for SiLU
+    and GELU).  bias_of(b, h, i, j) returns the bias of sample b, head h at
+    local query / key grids i, j (None: no bias).  Yields (b, h, live, bound)
+    with [Lq_b, Lkv_b] arrays."""
+    a = ACTS[act] if isinstance(act, str) else act
+    H = qn.shape[1]
+    for b in range(len(qo) - 1):
+        q0, q1, k0, k1 = int(qo[b]), int(qo[b + 1]), int(ko[b]), int(ko[b + 1])
+        if q1 == q0 or k1 == k0:
+            continue
+        i = np.arange(q1 - q0)[:, None]
+        j = np.arange(k1 - k0)[None, :]
+        live = np.ones((q1 - q0, k1 - k0), bool)
+        if causal:
+            live &= j <= i
+        if window:
+            live &= np.abs(i - j) < window
+        for h in range(H):
+            s0 = scale * qn[q0:q1, h] @ kn[k0:k1, h].T
+            if bias_of is not None:
+                s0 = s0 + bias_of(b, h, i, j)
+            dp = don[q0:q1, h] @ vn[k0:k1, h].T
+            if a == 0:
+                s_ = np.where(live, s0, -np.inf)
+                pm = np.exp(s_ - s_.max(1, keepdims=True))
+                pm /= pm.sum(1, keepdims=True)
+                dd = (don[q0:q1, h] * o_ref[q0:q1, h]).sum(1, keepdims=True)
+                od = np.abs(don[q0:q1, h] * o_ref[q0:q1, h]).sum(1, keepdims=True)
+                e = pm * 2.0 ** -8 * (np.abs(dp - dd) + od)
+            else:
+                e = 1.2 * 2.0 ** -8 * np.abs(dp)
+            yield b, h, live, e

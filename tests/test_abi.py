@@ -219,7 +219,7 @@ def test_mxfp8_backward_workspace_size(lib):
 
 def test_dense_bias_rejections_on_host(lib):
     """A dense bias needs its values and its int64 offsets (4- and 8-byte
-    aligned); it has no window, no table gradient, no block or MXFP8 path."""
+    aligned); it has no window, no block or MXFP8 path."""
     D = binding.BIAS_DENSE
     dense = lambda table=FAKE, off=FAKE + 64: ctypes.byref(binding.gdpa_bias(D, table, 0, off))
     assert _fwd(lib, bias=dense(off=None)) == INVALID
@@ -230,9 +230,13 @@ def test_dense_bias_rejections_on_host(lib):
     assert _fwd(lib, bias=dense(), ws=None) == WORKSPACE      # valid bias: the next check fires
     assert lib.gdpa_fwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense(), 0, 0, 4,
                                0.125, FAKE, FAKE, FAKE, 1 << 20, None) == UNSUPPORTED
-    assert lib.gdpa_bwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense(), 0, 0, 0,
+    # its gradient: no window either; a misaligned gradient is refused
+    assert lib.gdpa_bwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense(), 0, 0, 4,
                                0.125, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20,
-                               None) == INVALID              # a table gradient needs a table
+                               None) == UNSUPPORTED
+    assert lib.gdpa_bwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense(), 0, 0, 0,
+                               0.125, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, FAKE, 1 << 20,
+                               None) == INVALID
     assert lib.gdpa_block_fwd(FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, dense(), 0, 0, 0.125, FAKE,
                               FAKE, 1 << 20, None) == UNSUPPORTED
     assert lib.gdpa_fwd_mxfp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 10, 10,
@@ -248,14 +252,15 @@ def test_rope_backward_rejects_a_bad_base(lib):
     assert rope(-1.0) == INVALID
     assert rope(float("nan")) == INVALID
     assert rope(float("inf")) == INVALID
-    # the fused rotary backward has no table-gradient or dense-bias variant
-    table = ctypes.byref(binding.gdpa_bias(binding.BIAS_RELPOS, FAKE, 8))
-    assert lib.gdpa_bwd_rope(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, table, 0, 0, 0, 0.125,
-                             1e4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20,
-                             None) == UNSUPPORTED
+    # a bias gradient needs a bias, with or without the rotary backward
+    for base in (0.0, 1e4):
+        assert lib.gdpa_bwd_rope(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, None, 0, 0, 0,
+                                 0.125, base, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                 1 << 20, None) == INVALID
+    # with a dense bias the window check still comes first
     dense = ctypes.byref(binding.gdpa_bias(binding.BIAS_DENSE, FAKE, 0, FAKE + 64))
-    assert lib.gdpa_bwd_rope(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense, 0, 0, 0, 0.125,
-                             1e4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 20,
+    assert lib.gdpa_bwd_rope(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense, 0, 0, 4, 0.125,
+                             1e4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20,
                              None) == UNSUPPORTED
 
 

@@ -12,8 +12,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_common import (BWD_TOL, assert_close, check_guards, guarded, offsets, pick_samples,
-                        rand_bf16, to_np)
+from gpu_common import (BWD_TOL, assert_close, check_guards, ds_pair_bounds, guarded, offsets,
+                        pick_samples, rand_bf16, to_np)
 from jagged_attention_recsys_02_gb300 import binding
 from jagged_attention_recsys_02_gb300.workloads import ACTS, make_tensors, make_workload
 
@@ -231,6 +231,32 @@ def test_bwd_full_heavy_tail(act):
     _full_config("heavy_tail", act=act, budget=1.5e6)
 
 
+def check_table_gradient(q, qo_np, k, v, ko_np, do, bias, dbias, *, act, causal, scale, max_rel,
+                         window, what):
+    """The relative-position table's gradient against the oracle's.  Each
+    table entry sums dS over many pairs, so the per-pair rounding
+    (ds_pair_bounds) adds up.  Tolerance: the elementwise bound plus 4 times
+    the per-pair bounds summed over the entry's pairs."""
+    tb = bias.cpu().double().numpy()
+    qn, kn, vn, don = to_np(q), to_np(k), to_np(v), to_np(do)
+    *_, ref = oracle.bwd(qn, qo_np, kn, vn, ko_np, don, act=act, causal=causal, scale=scale,
+                         bias=tb, max_rel=max_rel, window=window, want_dbias=True)
+    o_ref, _ = oracle.fwd(qn, qo_np, kn, vn, ko_np, act=0, causal=causal, scale=scale, bias=tb,
+                          max_rel=max_rel, window=window)
+    width = 2 * max_rel - 1
+    tab = lambda i, j: np.clip(i - j + max_rel - 1, 0, width - 1)
+    err = np.zeros_like(ref)
+    for b, h, live, e in ds_pair_bounds(qn, qo_np, kn, vn, ko_np, don, o_ref, act=act,
+                                        causal=causal, scale=scale, window=window,
+                                        bias_of=lambda b, h, i, j: tb[h][tab(i, j)]):
+        t = tab(np.arange(live.shape[0])[:, None], np.arange(live.shape[1])[None, :])
+        np.add.at(err[h], t[live], e[live])
+    got = dbias.cpu().double().numpy()
+    bound = BWD_TOL[0] + BWD_TOL[1] * np.abs(ref) + 4 * err
+    assert np.all(np.abs(got - ref) <= bound), \
+        f"{what}: worst err/bound {float((np.abs(got - ref) / bound).max()):.3f}"
+
+
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("variant", ["full", "causal", "window", "clamped"])
 @pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh"])
@@ -260,51 +286,9 @@ def test_dbias(act, d, variant):
     dbias = torch.zeros_like(bias)
     binding.gdpa_bwd(q, qo, k, v, ko, out, lse, do, dbias=dbias, **kw)
     assert binding.device_status() == 0
-    tb = bias.cpu().double().numpy()
-    *_, ref = oracle.bwd(to_np(q), qo_np, to_np(k), to_np(v), ko_np, to_np(do), act=a, causal=causal,
-                         scale=scale, bias=tb, max_rel=max_rel, window=window, want_dbias=True)
-    # Each table entry sums dS over many pairs, so the per-pair rounding adds
-    # up.  Softmax: the kernel's D = rowsum(dO * O) uses the bf16-rounded O
-    # (relative error <= 2^-9 per element) and dS is formed from bf16 P and
-    # dP - D and rounded to bf16 (2^-9 each); per pair at most
-    # |P| 2^-8 (|dP - D| + sum_c |dO_c O_c|).  GDPA: dS = act'(s) dP in fp32
-    # from fp32 scores; per pair at most 1.2 |dP| 2^-8 (|act'| <= 1.2 for SiLU
-    # and GELU).  Tolerance: the elementwise bound plus 4 times those per-pair
-    # bounds summed over the entry's pairs, from fp64 quantities of the same
-    # inputs.
-    o_ref, _ = oracle.fwd(to_np(q), qo_np, to_np(k), to_np(v), ko_np, act=0, causal=causal,
-                          scale=scale, bias=tb, max_rel=max_rel, window=window)
-    qn, kn, vn, don = to_np(q), to_np(k), to_np(v), to_np(do)
-    err = np.zeros_like(ref)
-    for b in range(len(lq)):
-        q0, q1, k0, k1 = int(qo_np[b]), int(qo_np[b + 1]), int(ko_np[b]), int(ko_np[b + 1])
-        if q1 == q0 or k1 == k0:
-            continue
-        i = np.arange(q1 - q0)[:, None]
-        j = np.arange(k1 - k0)[None, :]
-        live = np.ones((q1 - q0, k1 - k0), bool)
-        if causal:
-            live &= j <= i
-        if window:
-            live &= np.abs(i - j) < window
-        t = np.clip(i - j + max_rel - 1, 0, 2 * max_rel - 2)
-        for h in range(H):
-            s0 = scale * qn[q0:q1, h] @ kn[k0:k1, h].T + tb[h][t]
-            dp = don[q0:q1, h] @ vn[k0:k1, h].T
-            if act == "softmax":
-                s_ = np.where(live, s0, -np.inf)
-                pm = np.exp(s_ - s_.max(1, keepdims=True))
-                pm /= pm.sum(1, keepdims=True)
-                dd = (don[q0:q1, h] * o_ref[q0:q1, h]).sum(1, keepdims=True)
-                od = np.abs(don[q0:q1, h] * o_ref[q0:q1, h]).sum(1, keepdims=True)
-                e = pm * 2.0 ** -8 * (np.abs(dp - dd) + od)
-            else:  # |act'(s)| <= 1.2 for SiLU and GELU
-                e = 1.2 * 2.0 ** -8 * np.abs(dp)
-            np.add.at(err[h], t[live], e[live])
-    got = dbias.cpu().double().numpy()
-    bound = BWD_TOL[0] + BWD_TOL[1] * np.abs(ref) + 4 * err
-    assert np.all(np.abs(got - ref) <= bound), \
-        f"dbias {variant} d={d}: worst err/bound {float((np.abs(got - ref) / bound).max()):.3f}"
+    check_table_gradient(q, qo_np, k, v, ko_np, do, bias, dbias, act=a, causal=causal,
+                         scale=scale, max_rel=max_rel, window=window,
+                         what=f"dbias {variant} d={d}")
     first = dbias.clone()
     binding.gdpa_bwd(q, qo, k, v, ko, out, lse, do, dbias=dbias, **kw)
     assert binding.device_status() == 0
@@ -369,6 +353,36 @@ def test_bwd_fused_rope_with_window(act):
     assert_close(to_np(dq), oracle.rope_bwd(rq, o_np, base), BWD_TOL, what + " dq")
     assert_close(to_np(dk), oracle.rope_bwd(rk, o_np, base), BWD_TOL, what + " dk")
     assert_close(to_np(dv), rv, BWD_TOL, what + " dv")
+
+
+@pytest.mark.parametrize("act", ["softmax", "silu"])
+@pytest.mark.parametrize("window", [0, 100])
+def test_bwd_fused_rope_with_table_gradient(window, act):
+    """gdpa_bwd_rope with a relative-position table and its gradient: dq, dk
+    through the rotary backward, the table's gradient unchanged by it."""
+    lq = [1, 64, 65, 200, 0, 300, 129]
+    H, d, base, max_rel = 2, 128, 10000.0, 150
+    g = torch.Generator(device="cuda").manual_seed(93 + window)
+    q, k, v, do = (rand_bf16((sum(lq), H, d), g, "cuda") for _ in range(4))
+    bias = torch.randn(H, 2 * max_rel - 1, generator=g, device="cuda") * 0.5
+    o_np = offsets(lq)
+    o = torch.from_numpy(o_np).cuda()
+    scale = 1.0 / math.sqrt(d)
+    a = ACTS[act]
+    kw = dict(act=a, causal=True, scale=scale, bias=bias, max_rel=max_rel, window=window)
+    out, lse = binding.gdpa_fwd(q, o, k, v, o, **kw)
+    dbias = torch.zeros_like(bias)
+    dq, dk, dv = binding.gdpa_bwd(q, o, k, v, o, out, lse, do, rope_base=base, dbias=dbias, **kw)
+    assert binding.device_status() == 0
+    rq, rk, rv = oracle.bwd(to_np(q), o_np, to_np(k), to_np(v), o_np, to_np(do), act=a,
+                            causal=True, scale=scale, bias=bias.cpu().double().numpy(),
+                            max_rel=max_rel, window=window)
+    what = f"rope+table gradient {act} window={window}"
+    assert_close(to_np(dq), oracle.rope_bwd(rq, o_np, base), BWD_TOL, what + " dq")
+    assert_close(to_np(dk), oracle.rope_bwd(rk, o_np, base), BWD_TOL, what + " dk")
+    assert_close(to_np(dv), rv, BWD_TOL, what + " dv")
+    check_table_gradient(q, o_np, k, v, o_np, do, bias, dbias, act=a, causal=True, scale=scale,
+                         max_rel=max_rel, window=window, what=what + " dbias")
 
 
 # Epilogues store rows with 32-byte stores when every output base is 32-byte

@@ -1,13 +1,14 @@
 """GPU parity of the dense jagged bias (one fp32 value per head, query and key
 of each sample) against the oracle: forward for every activation, the softmax
-and GDPA backward, causal and not, ragged lengths, malformed bias offsets."""
+and GDPA backward, the bias's gradient, causal and not, ragged lengths,
+malformed bias offsets."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gpu_common import (BWD_TOL, FWD_TOL, assert_close, check_guards, guarded, offsets,
-                        rand_bf16, to_np)
+from gpu_common import (BWD_TOL, FWD_TOL, assert_close, check_guards, ds_pair_bounds, guarded,
+                        offsets, rand_bf16, to_np)
 from jagged_attention_recsys_02_gb300 import binding
 from jagged_attention_recsys_02_gb300.workloads import ACTS
 
@@ -89,6 +90,94 @@ def test_dense_bias_backward(case, act, d):
                      to_np(c["do"]), **_ref_kw(c))
     for name, got, r in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
         assert_close(to_np(got), r, BWD_TOL, f"dense {act} {name}")
+
+
+def check_dense_gradient(c, got, base, what):
+    """got = base + the kernel's dS of every unmasked pair, in the dense bias's
+    layout: against the oracle's gradient within the per-pair rounding bound
+    (times 4) plus the fp32 rounding of the addition to base; masked entries
+    keep base bit for bit."""
+    Tq, H, d = c["q"].shape
+    qn, kn, vn, don = to_np(c["q"]), to_np(c["k"]), to_np(c["v"]), to_np(c["do"])
+    *_, ref = oracle.bwd(qn, c["qo_np"], kn, vn, c["ko_np"], don, want_dbias=True, **_ref_kw(c))
+    o_ref, _ = oracle.fwd(qn, c["qo_np"], kn, vn, c["ko_np"], **_ref_kw(c))
+    vals = c["vals"].double().cpu().numpy()
+    off = oracle.dense_bias_offsets(c["qo_np"], c["ko_np"], H)
+    got = got.cpu()
+    base = base.cpu()
+    live_all = np.zeros(int(off[-1]), bool)
+    pair = np.zeros(int(off[-1]))
+    for b, h, live, e in ds_pair_bounds(qn, c["qo_np"], kn, vn, c["ko_np"], don, o_ref,
+                                        act=c["act"], causal=c["causal"], scale=c["scale"],
+                                        bias_of=lambda b, h, i, j: vals[
+                                            off[b] + (h * i.shape[0] + i) * j.shape[1] + j]):
+        n = live.size
+        s = slice(int(off[b]) + h * n, int(off[b]) + (h + 1) * n)
+        live_all[s] = live.reshape(-1)
+        pair[s] = e.reshape(-1)
+    assert torch.equal(got[~torch.from_numpy(live_all)], base[~torch.from_numpy(live_all)]), \
+        f"{what}: a masked entry changed"
+    g, b0 = got.double().numpy()[live_all], base.double().numpy()[live_all]
+    r = ref[live_all]
+    bound = 4 * pair[live_all] + 2.0 ** -23 * (np.abs(b0) + np.abs(r)) + 1e-7 * np.abs(r).max()
+    err = np.abs(g - b0 - r)
+    assert np.all(err <= bound), \
+        f"{what}: {int((err > bound).sum())} of {err.size} out, worst err/bound {(err / bound).max():.3f}"
+    # the softmax kernel rounds dS to bf16, the others keep it in fp32: both
+    # sit far inside the bound above; the bound itself is not vacuous
+    assert np.median(bound) < 1e-2 * np.abs(r).max()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh"])
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_dense_bias_gradient(case, act, d):
+    """The dense bias's gradient (dbias with a dense bias): each unmasked
+    pair's entry gets its dS added, the other entries are left as they are;
+    dq, dk, dv are those of the call without it."""
+    lq, lkv, causal = CASES[case]
+    c = _case(lq, lkv or lq, 2, d, act, causal, seed=30 + case)
+    out, lse = _fwd(c)
+    Tq, H, _ = c["q"].shape
+    g = torch.Generator(device=DEV).manual_seed(7)
+    base = torch.randn(c["vals"].numel(), generator=g, device=DEV)
+    dbias = base.clone()
+    kw = dict(act=c["act"], causal=c["causal"], scale=c["scale"], bias=(c["vals"], c["off"]))
+    dq, dk, dv = binding.gdpa_bwd(c["q"], c["qo"], c["k"], c["v"], c["ko"], out, lse, c["do"],
+                                  dbias=dbias, **kw)
+    assert binding.device_status() == 0
+    check_dense_gradient(c, dbias, base, f"dense {act} d={d} dbias")
+    dq0, dk0, dv0 = binding.gdpa_bwd(c["q"], c["qo"], c["k"], c["v"], c["ko"], out, lse, c["do"],
+                                     **kw)
+    assert binding.device_status() == 0
+    assert torch.equal(dk, dk0) and torch.equal(dv, dv0)
+    torch.testing.assert_close(dq, dq0, rtol=2 ** -7, atol=1e-3)  # (dQ reduce order)
+
+
+@pytest.mark.parametrize("act", ["softmax", "silu"])
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_dense_bias_with_fused_rope(case, act):
+    """gdpa_bwd_rope with a dense bias and its gradient: dq, dk through the
+    rotary backward (queries and keys at their own positions), dv and the
+    bias's gradient as without it."""
+    lq, lkv, causal = CASES[case]
+    d, base = 128, 10000.0
+    c = _case(lq, lkv or lq, 2, d, act, causal, seed=40 + case)
+    out, lse = _fwd(c)
+    g = torch.Generator(device=DEV).manual_seed(8)
+    bias0 = torch.randn(c["vals"].numel(), generator=g, device=DEV)
+    dbias = bias0.clone()
+    dq, dk, dv = binding.gdpa_bwd(c["q"], c["qo"], c["k"], c["v"], c["ko"], out, lse, c["do"],
+                                  act=c["act"], causal=c["causal"], scale=c["scale"],
+                                  bias=(c["vals"], c["off"]), dbias=dbias, rope_base=base)
+    assert binding.device_status() == 0
+    ref = oracle.bwd(to_np(c["q"]), c["qo_np"], to_np(c["k"]), to_np(c["v"]), c["ko_np"],
+                     to_np(c["do"]), **_ref_kw(c))
+    what = f"dense+rope {act}"
+    assert_close(to_np(dq), oracle.rope_bwd(ref[0], c["qo_np"], base), BWD_TOL, what + " dq")
+    assert_close(to_np(dk), oracle.rope_bwd(ref[1], c["ko_np"], base), BWD_TOL, what + " dk")
+    assert_close(to_np(dv), ref[2], BWD_TOL, what + " dv")
+    check_dense_gradient(c, dbias, bias0, what + " dbias")
 
 
 def test_dense_bias_bad_offsets_are_reported():

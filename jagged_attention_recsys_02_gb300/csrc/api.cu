@@ -198,14 +198,16 @@ using namespace gdpa;
 extern "C" {
 
 // Workspace header (256 bytes): main-list count and ticket, short-query list
-// count and ticket, all-short flag.  The main list follows at byte 256, the
-// short-query list (one item per sample and head at most) after it.
+// count and ticket, all-short flag, short-key list count and ticket.  The main
+// list follows at byte 256, the short-query list (one item per sample and
+// head at most) after it, then the forward's short-key list.
 size_t gdpa_fwd_workspace_size(int B, int H, int d, int64_t Tq, int64_t Tkv) {
   (void)d;
   (void)Tkv;
   if (B < 0 || H <= 0 || Tq < 0) return 0;
   return 256 + align_up(static_cast<size_t>(max_fwd_items(B, H, Tq)) * sizeof(int2), 256) +
-         align_up(static_cast<size_t>(B) * H * sizeof(int2), 256);
+         align_up(static_cast<size_t>(B) * H * sizeof(int2), 256) +
+         align_up(static_cast<size_t>(max_kv_items(B, H, Tq)) * sizeof(int2), 256);
 }
 
 gdpa_status gdpa_fwd(const void* q, const int32_t* q_offsets, const void* k, const void* v,
@@ -251,22 +253,28 @@ gdpa_status gdpa_fwd_window(const void* q, const int32_t* q_offsets, const void*
   int* n_items = reinterpret_cast<int*>(ws);
   int* ticket = reinterpret_cast<int*>(ws + 4);
   int2* items = reinterpret_cast<int2*>(ws + 256);
-  // Samples with at most kShortQ queries go to the short-query kernel (GDPA
-  // activations without mask or bias: the PMA shape).
+  // Samples with at most kShortQ queries go to the short-query kernel, samples
+  // with more queries and at most kShortKv keys to the short-key kernel (GDPA
+  // activations without mask or bias: the PMA and cross-attention shapes).
   ShortList sq;
+  KvList kvl;
   CUtensorMap tq_short;
   if (act != GDPA_ACT_SOFTMAX && !causal && window == 0 && bias_kind(bias) == GDPA_BIAS_NONE) {
     if (!make_thd_map(&tq_short, q, Tq, H, d, kShortQ)) return GDPA_ERR_INVALID_ARG;
+    const size_t sq_off = 256 + align_up(static_cast<size_t>(max_fwd_items(B, H, Tq)) * sizeof(int2), 256);
     sq.max_q = kShortQ;
-    sq.items = reinterpret_cast<int2*>(
-        ws + 256 + align_up(static_cast<size_t>(max_fwd_items(B, H, Tq)) * sizeof(int2), 256));
+    sq.items = reinterpret_cast<int2*>(ws + sq_off);
     sq.n_items = reinterpret_cast<int*>(ws + 8);
     sq.ticket = reinterpret_cast<int*>(ws + 12);
     sq.all_short = reinterpret_cast<int*>(ws + 16);
+    kvl.max_kv = kShortKv;
+    kvl.items = reinterpret_cast<int2*>(ws + sq_off + align_up(static_cast<size_t>(B) * H * sizeof(int2), 256));
+    kvl.n_items = reinterpret_cast<int*>(ws + 20);
+    kvl.ticket = reinterpret_cast<int*>(ws + 24);
   }
 
   if (launch_build_worklist(q_offsets, kv_offsets, B, H, Tq, Tkv, causal, window, 0, items,
-                            n_items, ticket, dev->status, s, dense_off, sq) != cudaSuccess)
+                            n_items, ticket, dev->status, s, dense_off, sq, kvl) != cudaSuccess)
     return GDPA_ERR_CUDA;
   ++t_launches;
 
@@ -308,6 +316,17 @@ gdpa_status gdpa_fwd_window(const void* q, const int32_t* q_offsets, const void*
     const int grid_sq = static_cast<int>(n_sq < dev->sms ? n_sq : dev->sms);
     if (launch_fwd_short_q(ps, act, tq_short, tk, tv, grid_sq, s) != cudaSuccess)
       return GDPA_ERR_CUDA;
+    ++t_launches;
+  }
+  if (kvl.items != nullptr) {
+    // the short-key items (an empty list makes the kernel return at once)
+    FwdParams pk = p;
+    pk.items = kvl.items;
+    pk.n_items = kvl.n_items;
+    pk.ticket = kvl.ticket;
+    const int64_t n_kv = max_kv_items(B, H, Tq);
+    const int grid_kv = static_cast<int>(n_kv < dev->sms ? (n_kv > 0 ? n_kv : 1) : dev->sms);
+    if (launch_fwd_short_kv(pk, act, tq, tk, tv, grid_kv, s) != cudaSuccess) return GDPA_ERR_CUDA;
     ++t_launches;
   }
   if (timed && cudaEventRecord(eb, s) != cudaSuccess) return GDPA_ERR_CUDA;

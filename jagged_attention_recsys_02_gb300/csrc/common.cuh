@@ -267,6 +267,25 @@ struct ShortList {
 // Queries of a short-query item (the MMA width of the short-query kernels).
 constexpr int kShortQ = 32;
 
+// The short-key list of the forward scheduler: samples with more than kShortQ
+// queries and 1 <= Lkv_b <= max_kv keys get items {b, (chunk << 8) | head},
+// one per head and chunk of kShortKvChunk queries, here instead of blocks in
+// the main list (max_kv 0 or items null: no split).  Items are sorted by
+// their own cost, longest first.
+struct KvList {
+  int max_kv = 0;
+  int2* items = nullptr;
+  int* n_items = nullptr;
+  int* ticket = nullptr;
+};
+// Keys a short-key sample may have (its K and V stay in shared memory) and
+// queries per short-key item.
+constexpr int kShortKv = 256;
+constexpr int kShortKvChunk = 2048;
+inline int64_t max_kv_items(int B, int H, int64_t Tq) {
+  return static_cast<int64_t>(H) * (Tq / kShortKvChunk + B);
+}
+
 // Host-side launchers (defined in the kernel translation units).
 // bias_off (optional): element offsets of a dense jagged bias, checked against
 // H * Lq_b * Lkv_b (a mismatch is reported as GDPA_ERR_BAD_OFFSETS).
@@ -275,7 +294,8 @@ cudaError_t launch_build_worklist(const int32_t* outer_off, const int32_t* inner
                                   int mode,
                                   int2* items, int* n_items, int* ticket, int* status,
                                   cudaStream_t stream, const int64_t* bias_off = nullptr,
-                                  const ShortList& sq = ShortList{});
+                                  const ShortList& sq = ShortList{},
+                                  const KvList& kv = KvList{});
 cudaError_t launch_fwd(const FwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, int grid, cudaStream_t stream);
 // Short-query forward (GDPA activations, no mask or bias): p.items is the
@@ -283,6 +303,11 @@ cudaError_t launch_fwd(const FwdParams& p, int act, const CUtensorMap& tq, const
 cudaError_t launch_fwd_short_q(const FwdParams& p, int act, const CUtensorMap& tq,
                                const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                                cudaStream_t stream);
+// Short-key forward (GDPA activations, no mask or bias): p.items is the
+// scheduler's short-key list; tq has kHalfRows-row boxes, tk and tv kKvRows.
+cudaError_t launch_fwd_short_kv(const FwdParams& p, int act, const CUtensorMap& tq,
+                                const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                                cudaStream_t stream);
 int fwd_smem_bytes(int d);
 cudaError_t launch_bwd_softmax_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                                     const CUtensorMap& tv, const CUtensorMap& tdo,

@@ -19,6 +19,11 @@
 // list of (sample, head) items, sorted the same way by their key-tile count,
 // for the kernels that stream a whole sample's keys past its few queries; the
 // scheduler then also records whether every sample with queries is short.
+// In the forward, samples with few keys (1 <= Lkv_b <= max_kv) and more
+// queries go to a third list for the kernel that keeps a sample's keys in
+// shared memory and streams its queries past them: one item per head and
+// chunk of kShortKvChunk queries, sorted by the item's own cost (query tiles
+// times 32-key columns), so the short last chunks of long samples come last.
 #include "common.cuh"
 
 namespace gdpa {
@@ -57,6 +62,14 @@ __device__ __forceinline__ int sample_bucket(int mode, int causal, int window, i
 
 // Query rows of sample b, for either mode.
 __device__ __forceinline__ int query_rows(int mode, int Lo, int Li) { return mode == 0 ? Lo : Li; }
+
+// Short-key items: cost of a chunk of `rows` queries against Li keys (at most
+// 16 tiles x 8 columns of 32 keys: below kKvBuckets).
+constexpr int kKvBuckets = 256;
+__device__ __forceinline__ int kv_cost(int rows, int Li) {
+  return ((rows + kHalfRows - 1) / kHalfRows) * ((Li + 31) / 32);
+}
+static_assert((kShortKvChunk / kHalfRows) * (kShortKv / 32) < kKvBuckets, "short-key cost range");
 
 // Exclusive scan in descending bucket order: base[c] = sum of hist[c'] for
 // c' > c; returns the total.  Thread t owns reversed positions 2t and 2t+1.
@@ -97,17 +110,27 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
                       int mode,
                       int2* __restrict__ items, int* __restrict__ n_items,
                       int* __restrict__ ticket, int* __restrict__ status,
-                      const int64_t* __restrict__ bias_off, ShortList sq) {
+                      const int64_t* __restrict__ bias_off, ShortList sq, KvList kv) {
   __shared__ int hist[kCostBuckets];
   __shared__ int base[kCostBuckets];
   __shared__ int shist[kCostBuckets];
   __shared__ int sbase[kCostBuckets];
+  __shared__ int khist[kKvBuckets];
+  __shared__ int kbase[kKvBuckets];
+  __shared__ int ktotal;
   __shared__ int warp_tot[kThreads / 32];
   __shared__ int bad;
   const int tid = threadIdx.x;
   const int block_rows = (mode == 0) ? kItemRows : kBwdKvRows;
   const bool split = sq.items != nullptr && sq.max_q > 0;
+  const bool kv_split = mode == 0 && kv.items != nullptr && kv.max_kv > 0;
+  // a short-key sample (forward): more queries than the short-query list
+  // takes, and 1..max_kv keys
+  auto short_kv = [&](int Lo, int Li) {
+    return kv_split && Li >= 1 && Li <= kv.max_kv && Lo >= 1 && !(split && Lo <= sq.max_q);
+  };
   for (int i = tid; i < kCostBuckets; i += kThreads) hist[i] = shist[i] = 0;
+  for (int i = tid; i < kKvBuckets; i += kThreads) khist[i] = 0;
   if (tid == 0) {
     bad = (outer_off[0] != 0 || inner_off[0] != 0 || outer_off[B] != T_outer ||
            inner_off[B] != T_inner || (bias_off != nullptr && bias_off[0] != 0)) ? 1 : 0;
@@ -129,6 +152,10 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
       const int lk = mode == 0 ? Li : Lo;
       const int c = 1 + (lk + kKvRows - 1) / kKvRows;
       atomicAdd(&shist[c < 1024 ? c : min(kCostBuckets - 1, 1024 + (c - 1024) / 64)], 1);
+    } else if (short_kv(Lo, Li)) {
+      const int nch = (Lo + kShortKvChunk - 1) / kShortKvChunk;
+      if (nch > 1) atomicAdd(&khist[kv_cost(kShortKvChunk, Li)], nch - 1);
+      atomicAdd(&khist[kv_cost(Lo - (nch - 1) * kShortKvChunk, Li)], 1);
     } else if (nblk > 0) {
       atomicAdd(&hist[sample_bucket(mode, causal, window, Lo, Li, nblk)], nblk);
     }
@@ -143,12 +170,25 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
         *sq.ticket = 0;
         *sq.all_short = 0;
       }
+      if (kv_split) {
+        *kv.n_items = 0;
+        *kv.ticket = 0;
+      }
       set_status(status, GDPA_ERR_BAD_OFFSETS);
     }
     return;
   }
   const int total = scan_desc(hist, base, warp_tot);
   const int stotal = split ? scan_desc(shist, sbase, warp_tot) : 0;
+  if (kv_split && tid == 0) {  // descending exclusive scan of the short-key costs
+    int acc = 0;
+    for (int c = kKvBuckets - 1; c >= 0; --c) {
+      kbase[c] = acc;
+      acc += khist[c];
+    }
+    ktotal = acc;
+  }
+  __syncthreads();
   for (int b = tid; b < B; b += kThreads) {
     const int Lo = outer_off[b + 1] - outer_off[b];
     const int Li = inner_off[b + 1] - inner_off[b];
@@ -160,6 +200,19 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
       const int pos = atomicAdd(&sbase[c < 1024 ? c : min(kCostBuckets - 1, 1024 + (c - 1024) / 64)], 1);
       for (int h = 0; h < H; ++h)
         sq.items[static_cast<long long>(pos) * H + h] = make_int2(b, h);
+      continue;
+    }
+    if (short_kv(Lo, Li)) {
+      const int nch = (Lo + kShortKvChunk - 1) / kShortKvChunk;
+      if (nch > 1) {
+        const int pos = atomicAdd(&kbase[kv_cost(kShortKvChunk, Li)], nch - 1);
+        for (int ch = 0; ch < nch - 1; ++ch)
+          for (int h = 0; h < H; ++h)
+            kv.items[static_cast<long long>(pos + ch) * H + h] = make_int2(b, (ch << 8) | h);
+      }
+      const int pos = atomicAdd(&kbase[kv_cost(Lo - (nch - 1) * kShortKvChunk, Li)], 1);
+      for (int h = 0; h < H; ++h)
+        kv.items[static_cast<long long>(pos) * H + h] = make_int2(b, ((nch - 1) << 8) | h);
       continue;
     }
     if (nblk == 0) continue;
@@ -181,6 +234,10 @@ build_worklist_kernel(const int32_t* __restrict__ outer_off, const int32_t* __re
       *sq.ticket = 0;
       *sq.all_short = (total == 0 && stotal > 0) ? 1 : 0;
     }
+    if (kv_split) {
+      *kv.n_items = ktotal * H;
+      *kv.ticket = 0;
+    }
   }
 }
 
@@ -190,10 +247,10 @@ cudaError_t launch_build_worklist(const int32_t* outer_off, const int32_t* inner
                                   int64_t T_outer, int64_t T_inner, int causal, int window,
                                   int mode, int2* items, int* n_items, int* ticket, int* status,
                                   cudaStream_t stream, const int64_t* bias_off,
-                                  const ShortList& sq) {
+                                  const ShortList& sq, const KvList& kv) {
   build_worklist_kernel<<<1, kThreads, 0, stream>>>(outer_off, inner_off, B, H, T_outer, T_inner,
                                                     causal, window, mode, items, n_items, ticket,
-                                                    status, bias_off, sq);
+                                                    status, bias_off, sq, kv);
   return cudaGetLastError();
 }
 

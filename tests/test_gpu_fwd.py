@@ -110,6 +110,24 @@ def test_fwd_short_queries(act, d):
     assert torch.all(out[sum(SHORT_Q[:4]):sum(SHORT_Q[:5])] == 0)  # the sample with no key
 
 
+# Short-key samples (more than 32 queries, 1..256 keys, GDPA without mask or
+# bias: the cross-attention shape) take the kernel that keeps a sample's K and
+# V in shared memory and streams its queries in 128-row tiles, in items of up
+# to 2048 queries.  Key counts cross the 16-key MMA steps, the 32-key
+# activation chunks and the 128-key boundary between two S buffers and one;
+# query counts cross the 128-row tiles and the 2048-query items.  One sample
+# has 257 keys (the general kernel), the last has none.
+SHORT_KV_Q = [33, 2049, 129, 40, 300, 128, 4100, 77, 2048, 500, 64, 1000, 35]
+SHORT_KV_KV = [1, 16, 17, 31, 33, 127, 128, 129, 200, 255, 256, 257, 0]
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu_tanh", "identity", "gelu_erf"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_fwd_short_keys(act, d):
+    out = _case(SHORT_KV_Q, SHORT_KV_KV, 3, d, act)
+    assert torch.all(out[-SHORT_KV_Q[-1]:] == 0)  # the sample with no key
+
+
 def test_fwd_empty_keys_and_queries():
     # samples with no keys give zero rows (lse = -inf for softmax); empty query samples write nothing
     out = _case([3, 0, 130, 5], [0, 9, 0, 140], 2, 128, "softmax")

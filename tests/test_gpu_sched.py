@@ -9,7 +9,10 @@ tests run gdpa_fwd / gdpa_bwd (forward: blocks of 256 query rows over
 128-key tiles; backward: blocks of 128 keys over 64-query tiles) and check
 the list against a host count made row by row from the mask's definition
 (samples with at most 32 queries and no mask or bias go to a second list,
-one {sample, head} item each, for the short-query kernels):
+one {sample, head} item each, for the short-query kernels; in the GDPA
+forward without mask or bias, samples with more queries and 1..256 keys go
+to a third list, one {sample, (chunk << 8) | head} item per 2048-query chunk,
+for the short-key kernel):
 
   * every (sample, head, block) with rows appears exactly once, and nothing else;
   * a sample's items are contiguous, heads innermost, and without a window
@@ -90,6 +93,31 @@ def _check_short(lq, lkv, H, short_set, short, all_short, n_main):
     assert all_short == (1 if (n_main == 0 and len(got) > 0) else 0)
 
 
+def _read_kv_list(ws, kv_at):
+    raw = ws.cpu().numpy()
+    n = int(raw[20:24].view(np.int32)[0])
+    items = raw[kv_at:kv_at + 8 * n].view(np.int32).reshape(n, 2).astype(np.int64)
+    return items[:, 0], items[:, 1] >> 8, items[:, 1] & 0xFF
+
+
+def _check_kv(lq, lkv, H, kv_set, samples, chunks, heads):
+    """Short-key samples: one item per head and 2048-query chunk, heads
+    innermost, items in non-increasing cost (query tiles x 32-key columns)."""
+    got = list(zip(samples.tolist(), chunks.tolist(), heads.tolist()))
+    assert len(got) == len(set(got)), "a short-key item appears twice"
+    want = {(b, ch, h) for b in kv_set for ch in range(math.ceil(lq[b] / 2048)) for h in range(H)}
+    assert set(got) == want, "short-key items missing or extra"
+    costs = []
+    for i in range(0, len(got), H):
+        unit = got[i:i + H]
+        assert [u[2] for u in unit] == list(range(H)), "heads not innermost"
+        assert all(u[:2] == unit[0][:2] for u in unit)
+        b, ch = unit[0][:2]
+        rows = min(2048, lq[b] - 2048 * ch)
+        costs.append(math.ceil(rows / 128) * math.ceil(lkv[b] / 32))
+    assert all(x >= y for x, y in zip(costs, costs[1:])), "short-key items not longest first"
+
+
 def _check(lq, lkv, H, causal, window, mode, samples, blocks, heads, short_set=()):
     rows = lq if mode == "fwd" else lkv
     per = 256 if mode == "fwd" else 128
@@ -145,6 +173,7 @@ def _run(lq, lkv, H, causal=False, window=0, act="softmax", seed=0):
     # workspace layout: short list after the main list (forward), after the main
     # list, the fp32 dQ accumulator and D (backward)
     f_short_at = 256 + _align(H * (Tq // 256 + B) * 8)
+    f_kv_at = f_short_at + _align(B * H * 8)
     b_short_at = 256 + _align(H * (Tkv // 128 + B) * 8) + _align(Tq * H * d * 4) + _align(Tq * H * 4)
     (f, fs, fa), (b, bs, ba) = _read_list(ws_f, f_short_at), _read_list(ws_b, b_short_at)
     lq, lkv = np.asarray(lq), np.asarray(lkv)
@@ -153,14 +182,18 @@ def _run(lq, lkv, H, causal=False, window=0, act="softmax", seed=0):
     plain = not causal and not window
     short = {i for i in range(B) if 1 <= lq[i] <= 32} if plain else set()
     f_short = short if act != "softmax" else set()
+    # GDPA forward without mask or bias: more than 32 queries and 1..256 keys
+    f_kv = ({i for i in range(B) if lq[i] > 32 and 1 <= lkv[i] <= 256}
+            if plain and act != "softmax" else set())
     _check_short(lq, lkv, H, f_short, fs, fa, len(f[0]))
     _check_short(lq, lkv, H, short, bs, ba, len(b[0]))
-    return (_check(lq, lkv, H, causal, window, "fwd", *f, short_set=f_short),
+    _check_kv(lq, lkv, H, f_kv, *_read_kv_list(ws_f, f_kv_at))
+    return (_check(lq, lkv, H, causal, window, "fwd", *f, short_set=f_short | f_kv),
             _check(lq, lkv, H, causal, window, "bwd", *b, short_set=short))
 
 
-RAGGED_Q = [1, 300, 0, 129, 513, 64, 255, 256, 257, 1000, 7, 0, 2048]
-RAGGED_KV = [7, 256, 5, 0, 700, 64, 128, 129, 1, 300, 3000, 0, 200]
+RAGGED_Q = [1, 300, 0, 129, 513, 64, 255, 256, 257, 1000, 7, 0, 2048, 5000, 4097]
+RAGGED_KV = [7, 256, 5, 0, 700, 64, 128, 129, 1, 300, 3000, 0, 200, 100, 31]
 
 
 @pytest.mark.parametrize("act", ["silu", "softmax"])

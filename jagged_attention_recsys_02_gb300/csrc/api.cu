@@ -479,6 +479,11 @@ gdpa_status gdpa_bwd_rope(const void* q, const int32_t* q_offsets, const void* k
   p.ticket = ticket;
   p.status = dev->status;
   p.all_short = sql.all_short;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  // GDPA without the rotary backward: samples whose keys fit one key block get
+  // their dQ written once, in bf16, by the main kernel
+  p.dq_direct_kv = (act != GDPA_ACT_SOFTMAX && rope_base == 0.0f) ? kBwdKvRows : 0;
+  p.short_q_max = short_q ? kShortQ : 0;
   if (short_q) {
     sqb.p = p;
     sqb.p.items = sql.items;
@@ -502,7 +507,7 @@ gdpa_status gdpa_bwd_rope(const void* q, const int32_t* q_offsets, const void* k
         rope_base > 0.0f
             ? launch_dq_convert_rope(dq_acc, dq, q_offsets, B, Tq, H, d, scale, rope_base, s)
             : launch_dq_convert(dq_acc, dq, static_cast<long long>(Tq) * H * d, scale, s,
-                                p.all_short);
+                                p.all_short, &p);
     if (ce != cudaSuccess) return GDPA_ERR_CUDA;
     ++t_launches;
   }

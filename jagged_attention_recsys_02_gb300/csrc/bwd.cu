@@ -674,6 +674,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       ++it;
       if (item.x < 0) break;
       const BwdItem in = decode_bwd(item, p);
+      // every key of the sample is in this block: dQ goes out once, in bf16
+      const bool direct = p.dq_direct_kv > 0 && in.Lkv <= p.dq_direct_kv;
       bool abort_now = false;
       for (int t = 0; t < in.nq; ++t) {
         w = mbar_wait(bar(C::kDqFull), dqc & 1u, abort_flag);
@@ -700,6 +702,37 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         const int qrow = in.q0 + (in.qt0 + t) * kBwdQRows;
         const uint32_t wstage = sbase + C::kDqStage + wq * C::kDqWarpBufs * (C::kDqChunk * 32 * 4);
         float* wstg = reinterpret_cast<float*>(gbase + C::kDqStage) + wq * C::kDqWarpBufs * (C::kDqChunk * 32);
+        if (direct) {
+          // A sample whose keys fit one block: this item saw every key, so the
+          // tile is dQ itself.  Each warp stages its 32 channels of 16 queries
+          // as bf16 (times the scale) and writes them back as 16-byte row
+          // pieces, only for the sample's own rows.
+          if (lane == 0) bulk_wait_group_read<0>();  // no earlier reduce still reads the buffers
+          __syncwarp();
+          uint16_t* sb = reinterpret_cast<uint16_t*>(wstg);
+#pragma unroll
+          for (int ch = 0; ch < kBwdQRows / C::kDqChunk; ++ch) {
+            if (32 * wq >= D) break;  // d = 64: warps 2 and 3 hold no channels
+#pragma unroll
+            for (int c = 0; c < C::kDqChunk; ++c) {
+              const int q = ch * C::kDqChunk + c;
+              sb[c * 32 + lane] = __bfloat16_as_ushort(
+                  __float2bfloat16_rn(__uint_as_float(q < 32 ? v0[q & 31] : v1[q & 31]) * p.scale));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int row = (lane >> 2) + 8 * k;  // query of the 16, 16-byte piece lane % 4
+              const int qloc = (in.qt0 + t) * kBwdQRows + ch * C::kDqChunk + row;
+              if (qloc < in.Lq)
+                *reinterpret_cast<uint4*>(p.dq + (static_cast<long long>(in.q0 + qloc) * p.H + in.head) * D +
+                                          32 * wq + 8 * (lane & 3)) =
+                    *reinterpret_cast<const uint4*>(sb + row * 32 + 8 * (lane & 3));
+            }
+            __syncwarp();
+          }
+          continue;
+        }
 #pragma unroll
         for (int ch = 0; ch < kBwdQRows / C::kDqChunk; ++ch) {
           const int buf = dq_issue % C::kDqWarpBufs;
@@ -784,7 +817,8 @@ template <int D>
 __global__ void __launch_bounds__(256)
 bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
                       float* __restrict__ delta, float* __restrict__ dq_acc, long long Tq, int H,
-                      int softmax, const int* __restrict__ all_short) {
+                      int softmax, const int* __restrict__ all_short, const int32_t* __restrict__ qo,
+                      const int32_t* __restrict__ ko, int B, int direct_kv, int short_q_max) {
   constexpr int kLanesPerRow = D / 8;
   // no sample reduces into the accumulator: leave it alone
   const bool zero_acc = all_short == nullptr || *all_short == 0;
@@ -799,7 +833,8 @@ bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16
        row0 < nrows; row0 += warps * kRowsPerWarp) {
     const long long row = row0 + sub;
     const bool ok = row < nrows;
-    if (ok && zero_acc) {
+    // (rows whose dQ the main kernel writes directly are left alone)
+    if (ok && zero_acc && !dq_row_direct(qo, ko, B, row / H, direct_kv, short_q_max)) {
       float4* acc = reinterpret_cast<float4*>(dq_acc + row * D) + 2 * v;
       acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -827,13 +862,18 @@ bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16
 }
 
 // dq = bf16(dq_acc * scale), eight values (two 16-byte loads, one 16-byte
-// store) per thread and step.
+// store) per thread and step; rows (token t, head h of row t * H + h, row
+// width d) whose dQ the main kernel wrote directly are skipped.
 __global__ void __launch_bounds__(256)
 dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long long n8, float scale,
-                  const int* __restrict__ skip) {
+                  const int* __restrict__ skip, const int32_t* __restrict__ qo,
+                  const int32_t* __restrict__ ko, int B, int H, int d, int direct_kv,
+                  int short_q_max) {
   if (skip != nullptr && *skip != 0) return;  // dq was written directly
+  const long long row8 = static_cast<long long>(H) * (d / 8);  // steps per token
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    if (direct_kv > 0 && dq_row_direct(qo, ko, B, i / row8, direct_kv, short_q_max)) continue;
     const float4 a = acc[2 * i];
     const float4 b = acc[2 * i + 1];
     dq[i] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
@@ -953,13 +993,13 @@ cudaError_t launch_bwd_preprocess(const BwdParams& p, bool softmax, cudaStream_t
   const long long rows = p.Tq * p.H;
   const int pre_blocks = static_cast<int>(rows / 8 + 1 < 4096 ? rows / 8 + 1 : 4096);
   if (p.d == 64)
-    bwd_preprocess_kernel<64><<<pre_blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
-                                                              p.Tq, p.H, softmax ? 1 : 0,
-                                                              p.all_short);
+    bwd_preprocess_kernel<64><<<pre_blocks, 256, 0, stream>>>(
+        p.out, p.dout, p.delta, p.dq_acc, p.Tq, p.H, softmax ? 1 : 0, p.all_short, p.qo, p.ko, p.B,
+        p.dq_direct_kv, p.short_q_max);
   else
-    bwd_preprocess_kernel<128><<<pre_blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
-                                                               p.Tq, p.H, softmax ? 1 : 0,
-                                                               p.all_short);
+    bwd_preprocess_kernel<128><<<pre_blocks, 256, 0, stream>>>(
+        p.out, p.dout, p.delta, p.dq_acc, p.Tq, p.H, softmax ? 1 : 0, p.all_short, p.qo, p.ko, p.B,
+        p.dq_direct_kv, p.short_q_max);
   return cudaGetLastError();
 }
 
@@ -975,11 +1015,15 @@ cudaError_t launch_dq_convert_rope(const float* acc, void* dq, const int32_t* of
 }
 
 cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale,
-                              cudaStream_t stream, const int* skip) {
+                              cudaStream_t stream, const int* skip, const BwdParams* direct) {
   const long long n8 = n / 8;  // n = Tq * H * d with d in {64, 128}
   const int blocks = static_cast<int>(n8 / 256 + 1 < 8192 ? n8 / 256 + 1 : 8192);
-  dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(acc),
-                                                reinterpret_cast<uint4*>(dq), n8, scale, skip);
+  const bool dir = direct != nullptr && direct->dq_direct_kv > 0;
+  dq_convert_kernel<<<blocks, 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(acc), reinterpret_cast<uint4*>(dq), n8, scale, skip,
+      dir ? direct->qo : nullptr, dir ? direct->ko : nullptr, dir ? direct->B : 0,
+      dir ? direct->H : 1, dir ? direct->d : 128, dir ? direct->dq_direct_kv : 0,
+      dir ? direct->short_q_max : 0);
   return cudaGetLastError();
 }
 

@@ -185,6 +185,23 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// Whether token t's dQ row is written directly in bf16 by the general backward
+// (see BwdParams::dq_direct_kv): the sample holding t is found by a binary
+// search over the query offsets (the last sample starting at or before t; an
+// empty sample shares its start with the next one, which then wins).
+__device__ __forceinline__ bool dq_row_direct(const int32_t* qo, const int32_t* ko, int B,
+                                              long long t, int direct_kv, int short_q_max) {
+  if (direct_kv <= 0) return false;
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(qo + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  const int Lq = __ldg(qo + lo + 1) - __ldg(qo + lo);
+  const int Lkv = __ldg(ko + lo + 1) - __ldg(ko + lo);
+  return Lkv >= 1 && Lkv <= direct_kv && Lq > short_q_max;
+}
+
 struct FwdParams {
   const int32_t* qo;
   const int32_t* ko;
@@ -229,6 +246,12 @@ struct BwdParams {
   const int* all_short;     // scheduler flag: every sample takes the short-query kernel, so
                             //   the accumulator is neither zeroed nor converted (nullptr: no
                             //   short-query list)
+  __nv_bfloat16* dq;        // bf16 dQ output
+  int dq_direct_kv;         // > 0: samples with 1..dq_direct_kv keys and more than short_q_max
+                            //   queries get dQ written once in bf16 by the main kernel (one key
+                            //   block sees every key); their accumulator rows are neither zeroed
+                            //   nor converted.  0: every row goes through the accumulator.
+  int short_q_max;          // queries of a short-query sample (0: no short-query list)
   const int2* items;
   const int* n_items;
   int* ticket;
@@ -325,7 +348,8 @@ cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const
                        cudaStream_t stream, int* launches, cudaEvent_t ev_begin,
                        cudaEvent_t ev_end, const ShortBwd* sq = nullptr);
 cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale,
-                              cudaStream_t stream, const int* skip = nullptr);
+                              cudaStream_t stream, const int* skip = nullptr,
+                              const BwdParams* direct = nullptr);
 // Short-query backward (p.items: the scheduler's short-query list; tq, tdo
 // with kShortQ-row boxes).  dQ goes to dq as bf16 when *p.all_short, else
 // (unscaled) into the rows of p.dq_acc that the short samples own.

@@ -120,6 +120,28 @@ def test_bwd_short_queries(act, d, mixed):
     assert torch.all(dq[z:z + SHORTQ_Q[3]] == 0)  # the sample with no key
 
 
+# GDPA samples whose keys fit one 128-key block get dQ written once in bf16 by
+# the main kernel (their accumulator rows are neither zeroed nor converted);
+# the others go through the fp32 accumulator.  One call mixes both with
+# short-query samples (their own kernel), samples without keys (zero dQ rows)
+# and without queries; query counts cross the 64-row tiles and the 16-row
+# store pieces, key counts the 128-key block.
+DIRECT_Q = [300, 65, 7, 129, 400, 33, 0, 250, 64, 1000, 20]
+DIRECT_KV = [128, 1, 90, 129, 0, 64, 50, 256, 127, 700, 40]
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu_tanh"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_direct_dq_rows(causal, d, act):
+    lq = DIRECT_Q
+    lkv = [x for x in lq] if causal else DIRECT_KV
+    dq, dk, dv = _case(lq, lkv, 3, d, act, causal=causal, seed=5)
+    if not causal:
+        z = sum(DIRECT_Q[:4])
+        assert torch.all(dq[z:z + DIRECT_Q[4]] == 0)  # the sample with no key
+
+
 def test_bwd_empty_sides():
     # no keys: dq rows are zero; no queries: dk/dv rows are zero
     dq, dk, dv = _case([3, 0, 130, 5], [0, 9, 0, 140], 2, 128, "softmax")

@@ -102,7 +102,8 @@ def test_window_as_long_as_the_samples_is_bit_identical(act, causal):
     """A window no shorter than every sample masks nothing: the kernels must
     visit the same tiles with the same masks and give bit-identical out, lse,
     dK and dV (rows of samples that the unwindowed call sends to the
-    short-query kernels agree within the parity tolerances).  dQ sums the key blocks' contributions in whatever order the
+    short-query kernels, or to the short-key forward, agree within the parity
+    tolerances).  dQ sums the key blocks' contributions in whatever order the
     CTAs reach the fp32 accumulator, so two runs agree only up to that order:
     within a bf16 rounding step of the value plus fp32 rounding of partial
     sums that cancel (bounded here by 1e-4 of the tensor's largest entry)."""
@@ -119,21 +120,29 @@ def test_window_as_long_as_the_samples_is_bit_identical(act, causal):
         assert binding.device_status() == 0
         res.append(dict(out=out, lse=lse, dq=grads[0], dk=grads[1], dv=grads[2]))
     # Without a window, samples of at most 32 queries take the short-query
-    # kernels (keys as TMEM lanes), whose sums run in another order: their rows
-    # agree within the parity tolerances, every other row bit for bit.
+    # kernels (keys as TMEM lanes), and in the GDPA forward samples with more
+    # queries and at most 256 keys the short-key kernel; their sums run in
+    # another order, so those rows agree within the parity tolerances, every
+    # other row bit for bit.
     o_np = offsets(LENGTHS)
     short = torch.zeros(sum(LENGTHS), dtype=torch.bool, device=DEV)
+    short_fwd = torch.zeros_like(short)
     if not causal:
         for b, L in enumerate(LENGTHS):
+            rows = slice(int(o_np[b]), int(o_np[b + 1]))
             if 1 <= L <= 32:
-                short[int(o_np[b]):int(o_np[b + 1])] = True
+                short[rows] = True
+                short_fwd[rows] = True
+            elif act != "softmax" and 32 < L <= 256:
+                short_fwd[rows] = True
     for name in ("out", "lse", "dk", "dv"):
         x, y = res[0][name], res[1][name]
         if x is None:
             continue
-        rows = short if name != "lse" else short[None, :].expand_as(x)
+        sel = short_fwd if name in ("out", "lse") else short
+        rows = sel if name != "lse" else sel[None, :].expand_as(x)
         tol = FWD_TOL if name in ("out", "lse") else BWD_TOL
-        assert_close(to_np(x[rows]), to_np(y[rows]), tol, name + " (short-query samples)")
+        assert_close(to_np(x[rows]), to_np(y[rows]), tol, name + " (short-query / short-key samples)")
         x, y = x[~rows], y[~rows]
         if x.dtype == torch.bfloat16:
             x, y = x.view(torch.int16), y.view(torch.int16)

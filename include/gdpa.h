@@ -85,10 +85,10 @@ typedef enum { GDPA_BIAS_NONE = 0, GDPA_BIAS_RELPOS = 1, GDPA_BIAS_DENSE = 2 } g
  * array [B+1], offsets[0] = 0, offsets[b+1] - offsets[b] = H Lq_b Lkv_b;
  * a mismatch is reported as GDPA_ERR_BAD_OFFSETS through the device status).
  * max_rel is ignored.  The dense bias is read from global memory by the
- * kernels' activation warps; it is supported without a window by gdpa_fwd,
- * gdpa_bwd, gdpa_fwd_noalloc and gdpa_bwd_window / gdpa_bwd_rope (these two
- * also return its gradient); the other entry points, and a window > 0, give
- * GDPA_ERR_UNSUPPORTED. */
+ * kernels' activation warps; it is supported by gdpa_fwd, gdpa_bwd,
+ * gdpa_fwd_noalloc, gdpa_fwd_window and gdpa_bwd_window / gdpa_bwd_rope
+ * (these two also return its gradient), with or without a sliding window;
+ * the block-aligned and MXFP8 entry points give GDPA_ERR_UNSUPPORTED. */
 typedef struct {
   int kind;                /* gdpa_bias_kind */
   const float* table;      /* device pointer, ignored for GDPA_BIAS_NONE */

@@ -151,7 +151,6 @@ gdpa_status check_common(const void* q, const int32_t* qo, const void* k, const 
           (reinterpret_cast<uintptr_t>(bias->table) & 3u) ||
           (reinterpret_cast<uintptr_t>(bias->offsets) & 7u))
         return GDPA_ERR_INVALID_ARG;
-      if (window > 0) return GDPA_ERR_UNSUPPORTED;  // built without the window
       return GDPA_OK;
     }
     if (bias->kind != GDPA_BIAS_RELPOS) return GDPA_ERR_INVALID_ARG;

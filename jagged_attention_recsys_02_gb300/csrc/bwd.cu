@@ -937,8 +937,7 @@ template <int D, int ACT>
 cudaError_t launch_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                         int grid, cudaStream_t s) {
-  if (p.bias_dense != nullptr) {  // no window
-    if (p.window > 0) return cudaErrorInvalidValue;
+  if (p.bias_dense != nullptr) {
     return p.dbias != nullptr ? launch_main_db<D, ACT, true, true>(p, tq, tk, tv, tdo, tdq, grid, s)
                               : launch_main_db<D, ACT, false, true>(p, tq, tk, tv, tdo, tdq, grid, s);
   }

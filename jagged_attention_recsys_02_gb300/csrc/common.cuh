@@ -335,6 +335,10 @@ int fwd_smem_bytes(int d);
 cudaError_t launch_bwd_softmax_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                                     const CUtensorMap& tv, const CUtensorMap& tdo,
                                     const CUtensorMap& tdq, int grid, cudaStream_t s);
+// The rotary-backward instantiations of the softmax backward (p.rope_base > 0).
+cudaError_t launch_bwd_softmax_rope(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                    const CUtensorMap& tv, const CUtensorMap& tdo,
+                                    const CUtensorMap& tdq, int grid, cudaStream_t s);
 // The short-query part of a backward call (its own list, maps and grid).
 struct ShortBwd {
   BwdParams p;

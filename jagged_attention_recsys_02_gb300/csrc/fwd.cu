@@ -544,8 +544,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int c = c0 + chunk * 32 + i;
-              db[i] = (drow != nullptr && c < col_lim) ? __ldg(drow + c) * (kSoftmax ? kLog2e : 1.0f)
-                                                        : 0.0f;
+              db[i] = (drow != nullptr && (!kBand || c >= col_lo) && c < col_lim)
+                          ? __ldg(drow + c) * (kSoftmax ? kLog2e : 1.0f)
+                          : 0.0f;
             }
           }
           uint32_t sr[32];
@@ -784,10 +785,12 @@ int fwd_smem_bytes(int d) { return d == 64 ? FwdCfg<64>::kSmemBytes : FwdCfg<128
 cudaError_t launch_fwd(const FwdParams& p, int act, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, int grid, cudaStream_t stream) {
   const bool band = p.window > 0;
-  if (p.bias_dense != nullptr) {  // the dense bias is built without a window
-    if (band) return cudaErrorInvalidValue;
-    return p.d == 64 ? launch_d<64, false, true>(p, act, tq, tk, tv, grid, stream)
-                     : launch_d<128, false, true>(p, act, tq, tk, tv, grid, stream);
+  if (p.bias_dense != nullptr) {
+    if (p.d == 64)
+      return band ? launch_d<64, true, true>(p, act, tq, tk, tv, grid, stream)
+                  : launch_d<64, false, true>(p, act, tq, tk, tv, grid, stream);
+    return band ? launch_d<128, true, true>(p, act, tq, tk, tv, grid, stream)
+                : launch_d<128, false, true>(p, act, tq, tk, tv, grid, stream);
   }
   if (p.d == 64)
     return band ? launch_d<64, true, false>(p, act, tq, tk, tv, grid, stream)

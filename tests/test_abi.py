@@ -219,7 +219,7 @@ def test_mxfp8_backward_workspace_size(lib):
 
 def test_dense_bias_rejections_on_host(lib):
     """A dense bias needs its values and its int64 offsets (4- and 8-byte
-    aligned); it has no window, no block or MXFP8 path."""
+    aligned); it has no block or MXFP8 path."""
     D = binding.BIAS_DENSE
     dense = lambda table=FAKE, off=FAKE + 64: ctypes.byref(binding.gdpa_bias(D, table, 0, off))
     assert _fwd(lib, bias=dense(off=None)) == INVALID
@@ -228,12 +228,13 @@ def test_dense_bias_rejections_on_host(lib):
     assert _fwd(lib, bias=dense(off=FAKE + 4)) == INVALID
     assert _bwd(lib, bias=dense(off=None)) == INVALID
     assert _fwd(lib, bias=dense(), ws=None) == WORKSPACE      # valid bias: the next check fires
+    # with a window it passes validation (the missing workspace is the next check)
     assert lib.gdpa_fwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense(), 0, 0, 4,
-                               0.125, FAKE, FAKE, FAKE, 1 << 20, None) == UNSUPPORTED
-    # its gradient: no window either; a misaligned gradient is refused
+                               0.125, FAKE, FAKE, None, 0, None) == WORKSPACE
     assert lib.gdpa_bwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense(), 0, 0, 4,
-                               0.125, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20,
-                               None) == UNSUPPORTED
+                               0.125, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0,
+                               None) == WORKSPACE
+    # a misaligned gradient is refused
     assert lib.gdpa_bwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense(), 0, 0, 0,
                                0.125, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, FAKE, 1 << 20,
                                None) == INVALID
@@ -257,11 +258,11 @@ def test_rope_backward_rejects_a_bad_base(lib):
         assert lib.gdpa_bwd_rope(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, None, 0, 0, 0,
                                  0.125, base, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                                  1 << 20, None) == INVALID
-    # with a dense bias the window check still comes first
+    # a dense bias with a window and the rotary backward passes validation
     dense = ctypes.byref(binding.gdpa_bias(binding.BIAS_DENSE, FAKE, 0, FAKE + 64))
     assert lib.gdpa_bwd_rope(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense, 0, 0, 4, 0.125,
-                             1e4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20,
-                             None) == UNSUPPORTED
+                             1e4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0,
+                             None) == WORKSPACE
 
 
 def test_binding_marshals_both_bias_forms():

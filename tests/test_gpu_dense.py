@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _case(lq, lkv, H, d, act, causal, seed, std=1.0):
+def _case(lq, lkv, H, d, act, causal, seed, std=1.0, window=0):
     g = torch.Generator(device=DEV).manual_seed(seed)
     q = rand_bf16((sum(lq), H, d), g, DEV)
     k = rand_bf16((sum(lkv), H, d), g, DEV)
@@ -29,7 +29,7 @@ def _case(lq, lkv, H, d, act, causal, seed, std=1.0):
     qo, ko = torch.from_numpy(qo_np).to(DEV), torch.from_numpy(ko_np).to(DEV)
     off = torch.from_numpy(off_np).to(DEV)
     return dict(q=q, k=k, v=v, do=do, qo=qo, ko=ko, qo_np=qo_np, ko_np=ko_np, vals=vals, off=off,
-                act=ACTS[act], causal=causal, scale=1.0 / np.sqrt(d))
+                act=ACTS[act], causal=causal, scale=1.0 / np.sqrt(d), window=window)
 
 
 def _fwd(c):
@@ -37,14 +37,15 @@ def _fwd(c):
     buf, out = guarded(Tq, H, d, DEV)
     lse = torch.full((H, Tq), float("nan"), device=DEV) if c["act"] == 0 else None
     binding.gdpa_fwd(c["q"], c["qo"], c["k"], c["v"], c["ko"], act=c["act"], causal=c["causal"],
-                     scale=c["scale"], bias=(c["vals"], c["off"]), out=out, lse=lse)
+                     scale=c["scale"], bias=(c["vals"], c["off"]), out=out, lse=lse,
+                     window=c["window"])
     assert binding.device_status() == 0
     check_guards(buf)
     return out, lse
 
 
 def _ref_kw(c):
-    return dict(act=c["act"], causal=c["causal"], scale=c["scale"],
+    return dict(act=c["act"], causal=c["causal"], scale=c["scale"], window=c["window"],
                 dense_bias=c["vals"].double().cpu().numpy())
 
 
@@ -109,6 +110,7 @@ def check_dense_gradient(c, got, base, what):
     pair = np.zeros(int(off[-1]))
     for b, h, live, e in ds_pair_bounds(qn, c["qo_np"], kn, vn, c["ko_np"], don, o_ref,
                                         act=c["act"], causal=c["causal"], scale=c["scale"],
+                                        window=c["window"],
                                         bias_of=lambda b, h, i, j: vals[
                                             off[b] + (h * i.shape[0] + i) * j.shape[1] + j]):
         n = live.size
@@ -142,7 +144,8 @@ def test_dense_bias_gradient(case, act, d):
     g = torch.Generator(device=DEV).manual_seed(7)
     base = torch.randn(c["vals"].numel(), generator=g, device=DEV)
     dbias = base.clone()
-    kw = dict(act=c["act"], causal=c["causal"], scale=c["scale"], bias=(c["vals"], c["off"]))
+    kw = dict(act=c["act"], causal=c["causal"], scale=c["scale"], bias=(c["vals"], c["off"]),
+              window=c["window"])
     dq, dk, dv = binding.gdpa_bwd(c["q"], c["qo"], c["k"], c["v"], c["ko"], out, lse, c["do"],
                                   dbias=dbias, **kw)
     assert binding.device_status() == 0
@@ -178,6 +181,36 @@ def test_dense_bias_with_fused_rope(case, act):
     assert_close(to_np(dk), oracle.rope_bwd(ref[1], c["ko_np"], base), BWD_TOL, what + " dk")
     assert_close(to_np(dv), ref[2], BWD_TOL, what + " dv")
     check_dense_gradient(c, dbias, bias0, what + " dbias")
+
+
+@pytest.mark.parametrize("act", ["softmax", "silu"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_dense_bias_with_window(causal, d, act):
+    """A dense bias under a sliding window (self-attention): forward, backward
+    and the bias's gradient against the oracle; entries outside the band keep
+    their value.  The window crosses the 128-key tiles."""
+    L = [1, 64, 130, 300, 0, 257, 129]
+    c = _case(L, L, 2, d, act, causal, seed=50 + d, window=100)
+    out, lse = _fwd(c)
+    ro, rl = oracle.fwd(to_np(c["q"]), c["qo_np"], to_np(c["k"]), to_np(c["v"]), c["ko_np"],
+                        **_ref_kw(c))
+    what = f"dense+window {act} d={d} causal={causal}"
+    assert_close(to_np(out), ro, FWD_TOL, what + " out")
+    if lse is not None:
+        assert_close(lse.cpu().double().numpy(), rl, FWD_TOL, what + " lse")
+    g = torch.Generator(device=DEV).manual_seed(9)
+    base = torch.randn(c["vals"].numel(), generator=g, device=DEV)
+    dbias = base.clone()
+    dq, dk, dv = binding.gdpa_bwd(c["q"], c["qo"], c["k"], c["v"], c["ko"], out, lse, c["do"],
+                                  act=c["act"], causal=c["causal"], scale=c["scale"],
+                                  bias=(c["vals"], c["off"]), window=c["window"], dbias=dbias)
+    assert binding.device_status() == 0
+    ref = oracle.bwd(to_np(c["q"]), c["qo_np"], to_np(c["k"]), to_np(c["v"]), c["ko_np"],
+                     to_np(c["do"]), **_ref_kw(c))
+    for name, got, r in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
+        assert_close(to_np(got), r, BWD_TOL, f"{what} {name}")
+    check_dense_gradient(c, dbias, base, what + " dbias")
 
 
 def test_dense_bias_bad_offsets_are_reported():

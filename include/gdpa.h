@@ -213,6 +213,20 @@ gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k,
                            int causal, float scale, float rope_base, const void* dout, void* dq,
                            void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream);
 
+/* gdpa_block_bwd with the gradient of a relative-position table: dbias (fp32
+ * device memory [H][2*max_rel-1], ADDED to, as in gdpa_bwd_window) receives,
+ * at entry clamp(i - j + max_rel - 1), the sum of dS_ij over the pairs each
+ * row sees in its block.  Each tile's sums are gathered in shared memory and
+ * added to the table with global atomics, so their order, and the sums' last
+ * bits, vary between runs.  dbias = NULL is gdpa_block_bwd; a dbias without a
+ * GDPA_BIAS_RELPOS bias, or not 4-byte aligned: GDPA_ERR_INVALID_ARG.  Every
+ * other argument, output and error is that of gdpa_block_bwd. */
+gdpa_status gdpa_block_bwd_dbias(const void* q, const int32_t* offsets, const void* k,
+                                 const void* v, int B, int H, int d, int64_t T,
+                                 const gdpa_bias* bias, int act, int causal, float scale,
+                                 float rope_base, const void* dout, void* dq, void* dk, void* dv,
+                                 float* dbias, void* workspace, size_t ws_bytes, void* stream);
+
 /* gdpa_bwd_window with the rotary-embedding backward fused into the epilogue
  * ("GEM Training ..." SWA / block paragraph: RoPE backward in the attention
  * epilogue, gradients kept in fp32).  q and k are taken as already

@@ -33,7 +33,7 @@ EXPORTS = ("gdpa_fwd_workspace_size", "gdpa_fwd", "gdpa_bwd_workspace_size", "gd
            "gdpa_fwd_window", "gdpa_bwd_window", "gdpa_fwd_mxfp8_window",
            "gdpa_block_workspace_size", "gdpa_block_fwd", "gdpa_block_bwd",
            "gdpa_bwd_mxfp8_workspace_size", "gdpa_bwd_mxfp8", "gdpa_bwd_mxfp8_window",
-           "gdpa_bwd_rope", "gdpa_selftest_timeout")
+           "gdpa_bwd_rope", "gdpa_selftest_timeout", "gdpa_block_bwd_dbias")
 MX_ALONG_CHANNELS, MX_ALONG_TOKENS, MX_NOSAT = 0, 1, 2
 
 
@@ -124,6 +124,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdpa_block_bwd.argtypes = [vp, vp, vp, vp, I, I, I, i64, ctypes.POINTER(gdpa_bias), I,
                                        I, F, F, vp, vp, vp, vp, vp, sz, vp]
         lib.gdpa_block_bwd.restype = I
+        lib.gdpa_block_bwd_dbias.argtypes = [vp, vp, vp, vp, I, I, I, i64,
+                                             ctypes.POINTER(gdpa_bias), I, I, F, F, vp, vp, vp, vp,
+                                             vp, vp, sz, vp]
+        lib.gdpa_block_bwd_dbias.restype = I
         lib.gdpa_bwd_mxfp8_workspace_size.argtypes = [I, I, I, i64, i64]
         lib.gdpa_bwd_mxfp8_workspace_size.restype = sz
         lib.gdpa_bwd_mxfp8.argtypes = list(lib.gdpa_bwd.argtypes)
@@ -301,9 +305,12 @@ def gdpa_block_fwd(q, offsets, k, v, *, act, causal=False, scale, bias=None, max
 
 
 def gdpa_block_bwd(q, offsets, k, v, dout, *, act, causal=False, scale, bias=None, max_rel=0,
-                   rope_base=0.0, dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """Block-aligned attention backward through the C ABI.  Returns (dq, dk, dv);
-    with rope_base > 0, dq and dk are gradients of the un-rotated q and k."""
+                   rope_base=0.0, dq=None, dk=None, dv=None, dbias=None, workspace=None,
+                   stream=None):
+    """Block-aligned attention backward through the C ABI (gdpa_block_bwd, or
+    gdpa_block_bwd_dbias when the bias table's gradient `dbias` [H, 2*max_rel-1]
+    fp32 is given, which is added to).  Returns (dq, dk, dv); with rope_base > 0,
+    dq and dk are gradients of the un-rotated q and k."""
     lib = load()
     T, H, d = q.shape
     B = offsets.numel() - 1
@@ -313,11 +320,16 @@ def gdpa_block_bwd(q, offsets, k, v, dout, *, act, causal=False, scale, bias=Non
     if workspace is None:
         workspace = torch.empty(block_workspace_size(B, H, d, T), device=q.device,
                                 dtype=torch.uint8)
-    rc = lib.gdpa_block_bwd(_ptr(q), _ptr(offsets), _ptr(k), _ptr(v), B, H, d, T,
-                            _bias(bias, max_rel), _act(act), int(bool(causal)), float(scale),
-                            float(rope_base), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
-                            workspace.numel(), _stream(stream))
-    _check(rc, "gdpa_block_bwd")
+    head = (_ptr(q), _ptr(offsets), _ptr(k), _ptr(v), B, H, d, T, _bias(bias, max_rel), _act(act),
+            int(bool(causal)), float(scale), float(rope_base), _ptr(dout), _ptr(dq), _ptr(dk),
+            _ptr(dv))
+    ws = (_ptr(workspace), workspace.numel(), _stream(stream))
+    if dbias is not None:
+        rc = lib.gdpa_block_bwd_dbias(*head, _ptr(dbias), *ws)
+        _check(rc, "gdpa_block_bwd_dbias")
+    else:
+        rc = lib.gdpa_block_bwd(*head, *ws)
+        _check(rc, "gdpa_block_bwd")
     return dq, dk, dv
 
 

@@ -575,10 +575,23 @@ gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k,
                            int B, int H, int d, int64_t T, const gdpa_bias* bias, int act,
                            int causal, float scale, float rope_base, const void* dout, void* dq,
                            void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream) {
+  return gdpa_block_bwd_dbias(q, offsets, k, v, B, H, d, T, bias, act, causal, scale, rope_base,
+                              dout, dq, dk, dv, nullptr, workspace, ws_bytes, stream);
+}
+
+gdpa_status gdpa_block_bwd_dbias(const void* q, const int32_t* offsets, const void* k,
+                                 const void* v, int B, int H, int d, int64_t T,
+                                 const gdpa_bias* bias, int act, int causal, float scale,
+                                 float rope_base, const void* dout, void* dq, void* dk, void* dv,
+                                 float* dbias, void* workspace, size_t ws_bytes, void* stream) {
   t_launches = 0;
   gdpa_status st = check_common(q, offsets, k, v, offsets, B, H, d, T, T, bias, act, causal, 0);
   if (st != GDPA_OK) return st;
   if (is_dense(bias)) return GDPA_ERR_UNSUPPORTED;
+  if (dbias != nullptr) {  // the gradient of a relative-position table needs that table
+    if (bias_kind(bias) != GDPA_BIAS_RELPOS) return GDPA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(dbias) & 3u) return GDPA_ERR_INVALID_ARG;
+  }
   if (!(rope_base >= 0.0f) || rope_base > 3.0e38f) return GDPA_ERR_INVALID_ARG;  // NaN, < 0, inf
   if (T > 0 && (dout == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
                 !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)))
@@ -616,6 +629,7 @@ gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k,
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.rope_base = rope_base;
+  p.dbias = dbias;
   p.status = dev->status;
   const int64_t max_items = max_block_tiles(B, T) * H;
   const int grid = static_cast<int>(max_items < dev->sms ? max_items : dev->sms);

@@ -273,6 +273,7 @@ struct BlockParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   float rope_base;                // > 0: dq, dk go back through the rotary embedding
+  float* dbias;                   // backward: the bias table's gradient, added to (nullptr: none)
   int* status;
 };
 
@@ -401,6 +402,9 @@ cudaError_t launch_block_fwd(const BlockParams& p, int act, const CUtensorMap& t
 // maps: q, k, v, dout, dq, dk, dv (bf16 [T][H][d], 128-row boxes)
 cudaError_t launch_block_bwd(const BlockParams& p, int act, const CUtensorMap* maps, int grid,
                              cudaStream_t s);
+// The bias-table gradient's instantiations of the block backward (p.dbias set).
+cudaError_t launch_block_bwd_dbias(const BlockParams& p, int act, const CUtensorMap* maps, int grid,
+                                   cudaStream_t s);
 
 // Upper bound on the number of work items (host-side sizing).
 inline int64_t max_fwd_items(int B, int H, int64_t Tq) {

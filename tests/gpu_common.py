@@ -130,7 +130,7 @@ def scale_for(d):
 
 
 def ds_pair_bounds(qn, qo, kn, vn, ko, don, o_ref, *, act, causal, scale, window=0,
-                   bias_of=None):
+                   bias_of=None, block=0):
     """Per (sample, head) of a backward problem: the unmasked pairs and a bound
     on the kernels' rounding in each pair's dS, from fp64 quantities of the
     same inputs.  Softmax: the kernel's D = rowsum(dO * O) uses the
@@ -139,7 +139,8 @@ def ds_pair_bounds(qn, qo, kn, vn, ko, don, o_ref, *, act, causal, scale, window
     |P| 2^-8 (|dP - D| + sum_c |dO_c O_c|).  GDPA: dS = act'(s) dP in fp32
     from fp32 scores; per pair at most 1.2 |dP| 2^-8 (|act'| <= 1.2 for SiLU
     and GELU).  bias_of(b, h, i, j) returns the bias of sample b, head h at
-    local query / key grids i, j (None: no bias).  Yields (b, h, live, bound)
+    local query / key grids i, j (None: no bias); block > 0 keeps only the
+    pairs inside one block of that many tokens.  Yields (b, h, live, bound)
     with [Lq_b, Lkv_b] arrays."""
     a = ACTS[act] if isinstance(act, str) else act
     H = qn.shape[1]
@@ -154,6 +155,8 @@ def ds_pair_bounds(qn, qo, kn, vn, ko, don, o_ref, *, act, causal, scale, window
             live &= j <= i
         if window:
             live &= np.abs(i - j) < window
+        if block:
+            live &= (i // block) == (j // block)
         for h in range(H):
             s0 = scale * qn[q0:q1, h] @ kn[k0:k1, h].T
             if bias_of is not None:

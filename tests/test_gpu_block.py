@@ -16,8 +16,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_common import (BWD_TOL, FWD_TOL, assert_close, check_guards, guarded, offsets, rand_bf16,
-                        to_np)
+from gpu_common import (BWD_TOL, FWD_TOL, assert_close, check_guards, ds_pair_bounds, guarded,
+                        offsets, rand_bf16, to_np)
 from jagged_attention_recsys_02_gb300 import binding
 from jagged_attention_recsys_02_gb300.workloads import ACTS, make_tensors, make_workload
 
@@ -138,6 +138,50 @@ def test_block_bwd_parity(d, act, causal):
     assert_close(to_np(dq), rq, BWD_TOL, what + " dq")
     assert_close(to_np(dk), rk, BWD_TOL, what + " dk")
     assert_close(to_np(dv), rv, BWD_TOL, what + " dv")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("act", ["softmax", "silu"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("max_rel", [100, 20])
+def test_block_bwd_table_gradient(max_rel, causal, act, d):
+    """gdpa_block_bwd_dbias: the relative-position table's gradient against the
+    oracle's (summed per entry over the in-block pairs; max_rel 20 clamps), dq,
+    dk, dv as without it, and the gradient added to what dbias held."""
+    H = 2
+    q, k, v, do, o, od, bias = _inputs(LENGTHS, H, d, max_rel, seed=40 + d + causal)
+    scale = 1.0 / math.sqrt(d)
+    base = torch.randn_like(bias)
+    dbias = base.clone()
+    kw = dict(act=act, causal=causal, scale=scale, bias=bias, max_rel=max_rel)
+    dq, dk, dv = binding.gdpa_block_bwd(q, od, k, v, do, dbias=dbias, **kw)
+    assert binding.device_status() == 0
+    dq0, dk0, dv0 = binding.gdpa_block_bwd(q, od, k, v, do, **kw)
+    assert binding.device_status() == 0
+    assert torch.equal(dq, dq0) and torch.equal(dk, dk0) and torch.equal(dv, dv0)
+    a = ACTS[act]
+    tb = _np_bias(bias)
+    qn, kn, vn, don = to_np(q), to_np(k), to_np(v), to_np(do)
+    *_, ref = oracle.bwd(qn, o, kn, vn, o, don, act=a, causal=causal, scale=scale, bias=tb,
+                         max_rel=max_rel, block=BLOCK, want_dbias=True)
+    o_ref, _ = oracle.fwd(qn, o, kn, vn, o, act=0, causal=causal, scale=scale, bias=tb,
+                          max_rel=max_rel, block=BLOCK)
+    width = 2 * max_rel - 1
+    tab = lambda i, j: np.clip(i - j + max_rel - 1, 0, width - 1)
+    err = np.zeros_like(ref)
+    for b, h, live, e in ds_pair_bounds(qn, o, kn, vn, o, don, o_ref, act=a, causal=causal,
+                                        scale=scale, block=BLOCK,
+                                        bias_of=lambda b, h, i, j: tb[h][tab(i, j)]):
+        t = tab(np.arange(live.shape[0])[:, None], np.arange(live.shape[1])[None, :])
+        np.add.at(err[h], t[live], e[live])
+    got = (dbias - base).cpu().double().numpy()
+    # the kernel's dS is fp32 (the per-pair bound covers the bf16 P it is formed
+    # from), plus the fp32 rounding of adding to base and a floor of 1e-3 of
+    # the largest entry
+    bound = (1e-3 * np.abs(ref).max() + 1e-3 * np.abs(ref) + 4 * err +
+             2.0 ** -23 * (np.abs(base.cpu().double().numpy()) + np.abs(ref)))
+    assert np.all(np.abs(got - ref) <= bound), \
+        f"block dbias {act}: worst err/bound {float((np.abs(got - ref) / bound).max()):.3f}"
 
 
 def test_block_bwd_single_sample_shapes():

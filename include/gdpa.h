@@ -52,7 +52,7 @@
  * Entry points: gdpa_fwd / gdpa_bwd (and their _window forms; gdpa_bwd_rope
  * adds the fused rotary backward), gdpa_fwd_noalloc, the block-aligned
  * gdpa_block_fwd / gdpa_block_bwd, the MXFP8 gdpa_quantize_mxfp8,
- * gdpa_fwd_mxfp8(_window) and gdpa_bwd_mxfp8(_window), the workspace-size
+ * gdpa_fwd_mxfp8(_window) and gdpa_bwd_mxfp8(_window, _rope), the workspace-size
  * queries, and the status, launch-count, timing and self-test helpers.
  */
 #ifndef GDPA_H_
@@ -328,6 +328,20 @@ gdpa_status gdpa_bwd_mxfp8_window(const void* q, const int32_t* q_offsets, const
                                   int causal, int window, float scale, const void* out,
                                   const float* lse, const void* dout, void* dq, void* dk, void* dv,
                                   void* workspace, size_t ws_bytes, void* stream);
+/* gdpa_bwd_mxfp8_window with the rotary-embedding backward (rope_base > 0:
+ * dq, dk returned for the un-rotated q, k, as in gdpa_bwd_rope: dK rotated in
+ * the kernel's epilogue, dQ in the accumulator's conversion; 0: none;
+ * negative, infinite or NaN: GDPA_ERR_INVALID_ARG) and the gradient of a
+ * relative-position table (dbias: fp32 [H][2*max_rel-1], added to, from the
+ * fp32 dS before its E4M3 rounding; NULL: not computed; without a
+ * GDPA_BIAS_RELPOS bias or not 4-byte aligned: GDPA_ERR_INVALID_ARG).  Every
+ * other argument, output and error is that of gdpa_bwd_mxfp8_window. */
+gdpa_status gdpa_bwd_mxfp8_rope(const void* q, const int32_t* q_offsets, const void* k,
+                                const void* v, const int32_t* kv_offsets, int B, int H, int d,
+                                int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
+                                int window, float scale, float rope_base, const void* out,
+                                const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                float* dbias, void* workspace, size_t ws_bytes, void* stream);
 
 /* Reads the device status word set by earlier calls on this device,
  * synchronising `stream` first, then clears it.  Returns GDPA_OK,

@@ -33,7 +33,8 @@ EXPORTS = ("gdpa_fwd_workspace_size", "gdpa_fwd", "gdpa_bwd_workspace_size", "gd
            "gdpa_fwd_window", "gdpa_bwd_window", "gdpa_fwd_mxfp8_window",
            "gdpa_block_workspace_size", "gdpa_block_fwd", "gdpa_block_bwd",
            "gdpa_bwd_mxfp8_workspace_size", "gdpa_bwd_mxfp8", "gdpa_bwd_mxfp8_window",
-           "gdpa_bwd_rope", "gdpa_selftest_timeout", "gdpa_block_bwd_dbias")
+           "gdpa_bwd_rope", "gdpa_selftest_timeout", "gdpa_block_bwd_dbias",
+           "gdpa_bwd_mxfp8_rope")
 MX_ALONG_CHANNELS, MX_ALONG_TOKENS, MX_NOSAT = 0, 1, 2
 
 
@@ -136,6 +137,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                               ctypes.POINTER(gdpa_bias), I, I, I, F, vp, vp, vp,
                                               vp, vp, vp, vp, sz, vp]
         lib.gdpa_bwd_mxfp8_window.restype = I
+        lib.gdpa_bwd_mxfp8_rope.argtypes = list(lib.gdpa_bwd_rope.argtypes)
+        lib.gdpa_bwd_mxfp8_rope.restype = I
         _lib = lib
         return lib
 
@@ -254,11 +257,12 @@ def bwd_mxfp8_workspace_size(B, H, d, Tq, Tkv) -> int:
 
 
 def gdpa_bwd_mxfp8(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, causal=False, scale,
-                   bias=None, max_rel=0, window=0, dq=None, dk=None, dv=None, workspace=None,
-                   stream=None):
-    """MXFP8 backward through the C ABI (gdpa_bwd_mxfp8, or
-    gdpa_bwd_mxfp8_window when window > 0) on the bf16 tensors of gdpa_bwd,
-    softmax, d = 128.  Returns (dq, dk, dv)."""
+                   bias=None, max_rel=0, window=0, dq=None, dk=None, dv=None, dbias=None,
+                   rope_base=0.0, workspace=None, stream=None):
+    """MXFP8 backward through the C ABI (gdpa_bwd_mxfp8, gdpa_bwd_mxfp8_window
+    when window > 0, gdpa_bwd_mxfp8_rope when rope_base > 0 or a bias-table
+    gradient `dbias` is given, which is added to) on the bf16 tensors of
+    gdpa_bwd, softmax, d = 128.  Returns (dq, dk, dv)."""
     lib = load()
     Tq, H, d = q.shape
     Tkv = k.shape[0]
@@ -273,11 +277,16 @@ def gdpa_bwd_mxfp8(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, causal=Fal
             _bias(bias, max_rel), ACT_SOFTMAX, int(bool(causal)))
     tail = (float(scale), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
             _ptr(workspace), workspace.numel(), _stream(stream))
-    if window:
+    if rope_base or dbias is not None:
+        rc = lib.gdpa_bwd_mxfp8_rope(*head, int(window), float(scale), float(rope_base), *tail[1:7],
+                                     _ptr(dbias), *tail[7:])
+        _check(rc, "gdpa_bwd_mxfp8_rope")
+    elif window:
         rc = lib.gdpa_bwd_mxfp8_window(*head, int(window), *tail)
+        _check(rc, "gdpa_bwd_mxfp8_window")
     else:
         rc = lib.gdpa_bwd_mxfp8(*head, *tail)
-    _check(rc, "gdpa_bwd_mxfp8_window" if window else "gdpa_bwd_mxfp8")
+        _check(rc, "gdpa_bwd_mxfp8")
     return dq, dk, dv
 
 

@@ -815,11 +815,27 @@ gdpa_status gdpa_bwd_mxfp8_window(const void* q, const int32_t* q_offsets, const
                                   int causal, int window, float scale, const void* out,
                                   const float* lse, const void* dout, void* dq, void* dk, void* dv,
                                   void* workspace, size_t ws_bytes, void* stream) {
+  return gdpa_bwd_mxfp8_rope(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act, causal,
+                             window, scale, 0.0f, out, lse, dout, dq, dk, dv, nullptr, workspace,
+                             ws_bytes, stream);
+}
+
+gdpa_status gdpa_bwd_mxfp8_rope(const void* q, const int32_t* q_offsets, const void* k,
+                                const void* v, const int32_t* kv_offsets, int B, int H, int d,
+                                int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,
+                                int window, float scale, float rope_base, const void* out,
+                                const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                float* dbias, void* workspace, size_t ws_bytes, void* stream) {
   t_launches = 0;
+  if (!(rope_base >= 0.0f) || rope_base == INFINITY) return GDPA_ERR_INVALID_ARG;  // NaN too
   gdpa_status st = check_common(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act,
                                 causal, window);
   if (st != GDPA_OK) return st;
   if (d != 128 || act != GDPA_ACT_SOFTMAX || is_dense(bias)) return GDPA_ERR_UNSUPPORTED;
+  if (dbias != nullptr) {  // the gradient of a relative-position table needs that table
+    if (bias_kind(bias) != GDPA_BIAS_RELPOS) return GDPA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(dbias) & 3u) return GDPA_ERR_INVALID_ARG;
+  }
   if (Tq > 0 && (dout == nullptr || dq == nullptr || out == nullptr || lse == nullptr ||
                  !aligned16(dout) || !aligned16(dq) || !aligned16(out)))
     return GDPA_ERR_INVALID_ARG;
@@ -899,6 +915,8 @@ gdpa_status gdpa_bwd_mxfp8_window(const void* q, const int32_t* q_offsets, const
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.dq_acc = dq_acc;
+  p.dbias = dbias;
+  p.rope_base = rope_base;
   p.delta = reinterpret_cast<float*>(ws + lay.delta);
   p.items = items;
   p.n_items = n_items;
@@ -925,10 +943,13 @@ gdpa_status gdpa_bwd_mxfp8_window(const void* q, const int32_t* q_offsets, const
   if (launch_bwd_mx(p, mx, maps, grid, s) != cudaSuccess) return GDPA_ERR_CUDA;
   if (timed && cudaEventRecord(eb, s) != cudaSuccess) return GDPA_ERR_CUDA;
   ++t_launches;
-  // 5) dQ = bf16(scale * accumulator)
+  // 5) dQ = bf16(scale * accumulator), rotated back through the rotary embedding if asked
   if (Tq > 0) {
-    if (launch_dq_convert(dq_acc, dq, static_cast<long long>(Tq) * H * d, scale, s) != cudaSuccess)
-      return GDPA_ERR_CUDA;
+    const cudaError_t ce =
+        rope_base > 0.0f
+            ? launch_dq_convert_rope(dq_acc, dq, q_offsets, B, Tq, H, d, scale, rope_base, s)
+            : launch_dq_convert(dq_acc, dq, static_cast<long long>(Tq) * H * d, scale, s);
+    if (ce != cudaSuccess) return GDPA_ERR_CUDA;
     ++t_launches;
   }
   return GDPA_OK;

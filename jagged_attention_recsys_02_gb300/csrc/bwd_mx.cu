@@ -36,7 +36,10 @@
 // [0,32) / [32,64) of a tile (P, dS, their codes and block scales); warps
 // 8-11 dQ group (dQ^T drain into the fp32 accumulator, dK/dV epilogue); warp
 // 12 producer (TMA of the E4M3 codes, the operands' scale words, lse, D and
-// bias values); warp 13 MMA issuer; warps 14-15 idle.
+// bias values); warp 13 MMA issuer; warp 14 adds each tile's bias-table
+// gradient (kDBias) to the table; warp 15 idle.  With rope_base > 0 the dK
+// epilogue rotates the rows back through the rotary embedding (dQ is rotated
+// in the accumulator's conversion).
 #include <type_traits>
 
 #include "common.cuh"
@@ -92,7 +95,11 @@ struct Cfg {
   static constexpr int kDqStage = kStats + kQStages * kStatFloats * 4;
   static constexpr int kSfBytes = 512;
   static constexpr int kSf = kDqStage + 2 * kDqStageBytes;
-  static constexpr int kBar = kSf + kNumSmSf * kSfBytes;
+  // bias-table gradient: per tile, dS summed along its 191 diagonals (two
+  // buffers of 192 floats, then {first diagonal, head})
+  static constexpr int kDbBuf = 192 * 4 + 16;
+  static constexpr int kDb = kSf + kNumSmSf * kSfBytes;
+  static constexpr int kBar = kDb + 2 * kDbBuf;
   static constexpr int kKvFull = 0, kKvEmpty = 1;
   static constexpr int kQFull = 2;                    // + stage
   static constexpr int kQEmpty = kQFull + kQStages;   // + stage
@@ -109,7 +116,9 @@ struct Cfg {
   static constexpr int kItemFull = kDkvEmpty + 1;     // + slot
   static constexpr int kItemEmpty = kItemFull + 2;
   static constexpr int kDrain = kItemEmpty + 2;
-  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kDbAcc = kDrain + 1;     // + buffer: the activation warps added a tile
+  static constexpr int kDbFree = kDbAcc + 2;    // + buffer: flushed to the table and zeroed
+  static constexpr int kNumBars = kDbFree + 2;
   static constexpr int kItemSlots = kBar + 8 * kNumBars;
   static constexpr int kTmemSlot = kItemSlots + 16;
   static constexpr int kAbort = kTmemSlot + 4;
@@ -196,7 +205,7 @@ __device__ __forceinline__ MxItem decode_mx(int2 it, const BwdParams& p) {
   return r;
 }
 
-template <bool kBand>
+template <bool kBand, bool kDBias, bool kRope>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant__ CUtensorMap tmap_qt,
               const __grid_constant__ CUtensorMap tmap_dod, const __grid_constant__ CUtensorMap tmap_dot,
@@ -238,11 +247,18 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
     mbar_init(bar(C::kDkvEmpty), 4);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kItemFull + s), 1);
-      mbar_init(bar(C::kItemEmpty + s), 1 + kActWarps + 4);
+      mbar_init(bar(C::kItemEmpty + s), 1 + kActWarps + 4 + (kDBias ? 1 : 0));
     }
     mbar_init(bar(C::kDrain), 1);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(bar(C::kDbAcc + u), kActWarps);
+      mbar_init(bar(C::kDbFree + u), 1);
+    }
     fence_mbar_init();
   }
+  if (kDBias)
+    for (int i = threadIdx.x; i < 2 * C::kDbBuf / 4; i += kThreads)
+      reinterpret_cast<float*>(gbase + C::kDb)[i] = 0.0f;
   // scale bytes that no product reads (k-steps past a tile) are still copied:
   // give them a defined value
   for (int i = threadIdx.x; i < kNumSmSf * C::kSfBytes / 4; i += kThreads)
@@ -636,6 +652,8 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
         const uint32_t s = g % C::kQStages;
         w = mbar_wait(bar(C::kQFull + s), (g / C::kQStages) & 1u, abort_flag);
         w = w && mbar_wait(bar(C::kSFull), g & 1u, abort_flag);
+        // the diagonal buffer of this tile was flushed two tiles ago
+        if (kDBias) w = w && mbar_wait(bar(C::kDbFree + (g & 1u)), ((g >> 1) & 1u) ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); abort_now = true; break; }
         tc_fence_after();
         const float* st = stats + s * C::kStatFloats;
@@ -733,6 +751,23 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
             pv[4 * q4 + 2] = b.x;
             pv[4 * q4 + 3] = b.y;
           }
+          if (kDBias) {
+            // dS(query c0 + i, key 32 wq + lane) lies on diagonal
+            // (c0 - 32 wq + 127) + (i - lane) of the tile.  Lane l gathers the
+            // warp's values with i - src = l (mod 32): at step i it reads
+            // column i of lane (i - l) mod 32, whose offset is l when i >= l
+            // and l - 32 otherwise; two shared atomics per lane and tile.
+            float up = 0.0f, down = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float v = __shfl_sync(0xffffffffu, pv[i], (i - lane) & 31);
+              if (i >= lane) up += v; else down += v;
+            }
+            float* win = reinterpret_cast<float*>(gbase + C::kDb + (g & 1u) * C::kDbBuf) +
+                         (c0 - 32 * wq + 127 + lane);
+            atomicAdd(win, up);
+            if (lane > 0) atomicAdd(win - 32, down);
+          }
           const int code = e8m0_nosat(__uint_as_float(warp_max_u32(__float_as_uint(amax32(pv)))));
           const float inv = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
           uint32_t pk[8];
@@ -765,6 +800,48 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
         fence_proxy_async_smem();
         tc_fence_before();
         warp_arrive(bar(C::kDsFull), lane);
+        if (kDBias) {
+          if (j == 0 && grp == 0) {
+            int* meta = reinterpret_cast<int*>(gbase + C::kDb + (g & 1u) * C::kDbBuf + 192 * 4);
+            meta[0] = qloc - kb0 - 127;  // diagonal (query - key) of window entry 0
+            meta[1] = in.head;
+          }
+          warp_arrive(bar(C::kDbAcc + (g & 1u)), lane);
+        }
+      }
+      if (abort_now) break;
+    }
+  } else if (kDBias && warp == kMmaWarp + 1) {
+    // ------------------------------------------------------------ bias-table gradient
+    // Per tile: wait for the activation warps' diagonal sums, add them to the
+    // table (entry = clamp(query - key + max_rel - 1)), zero the buffer.
+    const int width = 2 * p.max_rel - 1;
+    uint32_t it = 0, g = 0;
+    while (true) {
+      const uint32_t slot = it & 1u;
+      bool w = mbar_wait(bar(C::kItemFull + slot), (it >> 1) & 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
+      const int2 item = item_slot[slot];
+      warp_arrive(bar(C::kItemEmpty + slot), lane);
+      ++it;
+      if (item.x < 0) break;
+      const MxItem in = decode_mx<kBand>(item, p);
+      bool abort_now = false;
+      for (int t = 0; t < in.nq; ++t, ++g) {
+        const uint32_t u = g & 1u;
+        w = mbar_wait(bar(C::kDbAcc + u), (g >> 1) & 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); abort_now = true; break; }
+        float* win = reinterpret_cast<float*>(gbase + C::kDb + u * C::kDbBuf);
+        const int* meta = reinterpret_cast<const int*>(win + 192);
+        const int delta0 = meta[0];
+        float* row = p.dbias + static_cast<long long>(meta[1]) * width;
+        for (int e = lane; e < 191; e += 32) {
+          const float v = win[e];
+          if (v != 0.0f) atomicAdd(row + min(max(e + delta0 + p.max_rel - 1, 0), width - 1), v);
+          win[e] = 0.0f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::kDbFree + u));
       }
       if (abort_now) break;
     }
@@ -848,6 +925,11 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
           const uint32_t col = which ? kColDK : kColDV;
           const float mul = which ? p.scale : 1.0f;
           __nv_bfloat16* dst = (which ? p.dk : p.dv) + grow;
+          if (kRope && which == 1) {  // dK back through the rotary embedding
+            rope_bwd_row<kD>(tmem + lane_off + col, mul, jl, -2.0f * log2f(p.rope_base) / kD, dst,
+                             row_ok);
+            continue;
+          }
 #pragma unroll 1
           for (int chunk = 0; chunk < kD / 32; ++chunk) {
             uint32_t o[32];
@@ -881,15 +963,28 @@ bwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_qd, const __grid_constant
   }
 }
 
-template <bool kBand>
+template <bool kBand, bool kDBias, bool kRope>
 cudaError_t launch_mx(const BwdParams& p, const BwdMxOperands& mx, const CUtensorMap* m, int grid,
                       cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(bwd_mx_kernel<kBand>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_mx_kernel<kBand, kDBias, kRope>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
-  bwd_mx_kernel<kBand><<<grid, kThreads, Cfg::kSmemBytes, s>>>(m[0], m[1], m[2], m[3], m[4], m[5],
-                                                               m[6], m[7], p, mx);
+  bwd_mx_kernel<kBand, kDBias, kRope><<<grid, kThreads, Cfg::kSmemBytes, s>>>(
+      m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7], p, mx);
   return cudaGetLastError();
+}
+
+// The bias-table gradient and the rotary backward have instantiations of their
+// own, so calls without them run the unchanged kernels.
+template <bool kBand>
+cudaError_t launch_mx_band(const BwdParams& p, const BwdMxOperands& mx, const CUtensorMap* m,
+                           int grid, cudaStream_t s) {
+  const bool db = p.dbias != nullptr, rope = p.rope_base > 0.0f;
+  if (rope)
+    return db ? launch_mx<kBand, true, true>(p, mx, m, grid, s)
+              : launch_mx<kBand, false, true>(p, mx, m, grid, s);
+  return db ? launch_mx<kBand, true, false>(p, mx, m, grid, s)
+            : launch_mx<kBand, false, false>(p, mx, m, grid, s);
 }
 
 }  // namespace
@@ -897,7 +992,8 @@ cudaError_t launch_mx(const BwdParams& p, const BwdMxOperands& mx, const CUtenso
 cudaError_t launch_bwd_mx(const BwdParams& p, const BwdMxOperands& mx, const CUtensorMap* maps,
                           int grid, cudaStream_t s) {
   if (p.d != kD) return cudaErrorInvalidValue;
-  return p.window > 0 ? launch_mx<true>(p, mx, maps, grid, s) : launch_mx<false>(p, mx, maps, grid, s);
+  return p.window > 0 ? launch_mx_band<true>(p, mx, maps, grid, s)
+                      : launch_mx_band<false>(p, mx, maps, grid, s);
 }
 
 }  // namespace gdpa

@@ -172,3 +172,29 @@ def ds_pair_bounds(qn, qo, kn, vn, ko, don, o_ref, *, act, causal, scale, window
             else:
                 e = 1.2 * 2.0 ** -8 * np.abs(dp)
             yield b, h, live, e
+
+
+def check_table_gradient(q, qo_np, k, v, ko_np, do, bias, dbias, *, act, causal, scale, max_rel,
+                         window, what):
+    """The relative-position table's gradient against the oracle's.  Each
+    table entry sums dS over many pairs, so the per-pair rounding
+    (ds_pair_bounds) adds up.  Tolerance: the elementwise bound plus 4 times
+    the per-pair bounds summed over the entry's pairs."""
+    tb = bias.cpu().double().numpy()
+    qn, kn, vn, don = to_np(q), to_np(k), to_np(v), to_np(do)
+    *_, ref = oracle.bwd(qn, qo_np, kn, vn, ko_np, don, act=act, causal=causal, scale=scale,
+                         bias=tb, max_rel=max_rel, window=window, want_dbias=True)
+    o_ref, _ = oracle.fwd(qn, qo_np, kn, vn, ko_np, act=0, causal=causal, scale=scale, bias=tb,
+                          max_rel=max_rel, window=window)
+    width = 2 * max_rel - 1
+    tab = lambda i, j: np.clip(i - j + max_rel - 1, 0, width - 1)
+    err = np.zeros_like(ref)
+    for b, h, live, e in ds_pair_bounds(qn, qo_np, kn, vn, ko_np, don, o_ref, act=act,
+                                        causal=causal, scale=scale, window=window,
+                                        bias_of=lambda b, h, i, j: tb[h][tab(i, j)]):
+        t = tab(np.arange(live.shape[0])[:, None], np.arange(live.shape[1])[None, :])
+        np.add.at(err[h], t[live], e[live])
+    got = dbias.cpu().double().numpy()
+    bound = BWD_TOL[0] + BWD_TOL[1] * np.abs(ref) + 4 * err
+    assert np.all(np.abs(got - ref) <= bound), \
+        f"{what}: worst err/bound {float((np.abs(got - ref) / bound).max()):.3f}"

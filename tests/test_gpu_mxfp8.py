@@ -87,7 +87,8 @@ def test_quant_full_size_v_and_q():
 
 
 # ------------------------------------------------------------------ MXFP8 forward
-from gpu_common import MXFP8_TOL, assert_close, check_guards, guarded, oracle_fwd_samples, rand_bf16  # noqa: E402
+from gpu_common import (MXFP8_TOL, assert_close, check_guards, check_table_gradient, guarded,  # noqa: E402
+                        oracle_fwd_samples, rand_bf16)
 from jagged_attention_recsys_02_gb300.workloads import make_tensors, make_workload  # noqa: E402
 
 
@@ -332,6 +333,80 @@ def test_mxfp8_bwd_sliding_window(causal):
     L = [1, 64, 65, 130, 300, 0, 511]
     for window in (7, 100, 200):
         _mx_bwd_case(L, L, 2, causal=causal, max_rel=64, window=window, seed=window)
+
+
+def _e4m3_exact(shape, g):
+    """bf16 values that E4M3 holds exactly under any power-of-two block scale
+    the quantisers pick: k / 8 for integers |k| <= 12 (three significand bits),
+    so every product of the backward runs on exact operands."""
+    k = torch.randint(-12, 13, shape, generator=g, device=DEV)
+    return (k.float() / 8.0).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_mxfp8_bwd_table_gradient(causal):
+    """gdpa_bwd_mxfp8_rope with dbias: the gradient is summed from the fp32 dS
+    before its E4M3 rounding.  On inputs the quantisers hold exactly, the
+    scores and dP are exact, so the table gradient must match the unquantised
+    oracle's within the per-pair bounds of the bf16 backward (P from ex2.approx,
+    D from the bf16 forward output); dq, dk, dv still match the oracle's MXFP8
+    backward."""
+    L = [1, 64, 65, 130, 300, 0, 257]
+    lkv = L if causal else [7, 1, 128, 129, 200, 3, 300]
+    H, d, max_rel = 2, 128, 150
+    g = torch.Generator(device=DEV).manual_seed(17 + causal)
+    q, do = _e4m3_exact((sum(L), H, d), g), _e4m3_exact((sum(L), H, d), g)
+    k, v = _e4m3_exact((sum(lkv), H, d), g), _e4m3_exact((sum(lkv), H, d), g)
+    bias = torch.randn(H, 2 * max_rel - 1, generator=g, device=DEV) * 0.5
+    qo_np, ko_np = offsets(L), offsets(lkv)
+    qo, ko = torch.from_numpy(qo_np).to(DEV), torch.from_numpy(ko_np).to(DEV)
+    scale = 1.0 / np.sqrt(d)
+    bias_np = bias.cpu().double().numpy()
+    o_ref, l_ref = oracle.fwd(to_np(q), qo_np, to_np(k), to_np(v), ko_np, act=oracle.ACT_SOFTMAX,
+                              causal=causal, scale=scale, bias=bias_np, max_rel=max_rel)
+    out = torch.from_numpy(o_ref).to(DEV).to(torch.bfloat16)
+    lse = torch.from_numpy(np.where(np.isinf(l_ref), 0.0, l_ref)).to(DEV).float()
+    dbias = torch.zeros_like(bias)
+    dq, dk, dv = binding.gdpa_bwd_mxfp8(q, qo, k, v, ko, out, lse, do, causal=causal, scale=scale,
+                                        bias=bias, max_rel=max_rel, dbias=dbias)
+    assert binding.device_status() == 0
+    check_table_gradient(q, qo_np, k, v, ko_np, do, bias, dbias, act=oracle.ACT_SOFTMAX,
+                         causal=causal, scale=scale, max_rel=max_rel, window=0,
+                         what=f"mxfp8 dbias causal={causal}")
+    ref = oracle.bwd_mxfp8(to_np(q), qo_np, to_np(k), to_np(v), ko_np, to_np(out), to_np(do),
+                           lse.cpu().double().numpy(), causal=causal, scale=scale, bias=bias_np,
+                           max_rel=max_rel)
+    for name, got, r in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
+        assert_close(to_np(got), r, MXBWD_TOL, f"mxfp8 bwd with dbias {name}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_mxfp8_bwd_fused_rope(causal):
+    """gdpa_bwd_mxfp8_rope with rope_base > 0: dq, dk are the oracle's MXFP8
+    gradients sent back through the rotary embedding (queries and keys at
+    their own positions), dv unchanged."""
+    L = [1, 64, 65, 130, 300, 0, 257]
+    lkv = L if causal else [7, 1, 128, 129, 200, 3, 300]
+    H, d, base = 2, 128, 10000.0
+    g = torch.Generator(device=DEV).manual_seed(29 + causal)
+    q, do = rand_bf16((sum(L), H, d), g, DEV), rand_bf16((sum(L), H, d), g, DEV)
+    k, v = rand_bf16((sum(lkv), H, d), g, DEV), rand_bf16((sum(lkv), H, d), g, DEV)
+    qo_np, ko_np = offsets(L), offsets(lkv)
+    qo, ko = torch.from_numpy(qo_np).to(DEV), torch.from_numpy(ko_np).to(DEV)
+    scale = 1.0 / np.sqrt(d)
+    o_ref, l_ref = oracle.fwd(to_np(q), qo_np, to_np(k), to_np(v), ko_np, act=oracle.ACT_SOFTMAX,
+                              causal=causal, scale=scale)
+    out = torch.from_numpy(o_ref).to(DEV).to(torch.bfloat16)
+    lse = torch.from_numpy(np.where(np.isinf(l_ref), 0.0, l_ref)).to(DEV).float()
+    dq, dk, dv = binding.gdpa_bwd_mxfp8(q, qo, k, v, ko, out, lse, do, causal=causal, scale=scale,
+                                        rope_base=base)
+    assert binding.device_status() == 0
+    ref = oracle.bwd_mxfp8(to_np(q), qo_np, to_np(k), to_np(v), ko_np, to_np(out), to_np(do),
+                           lse.cpu().double().numpy(), causal=causal, scale=scale)
+    what = f"mxfp8 rope causal={causal}"
+    assert_close(to_np(dq), oracle.rope_bwd(ref[0], qo_np, base), MXBWD_TOL, what + " dq")
+    assert_close(to_np(dk), oracle.rope_bwd(ref[1], ko_np, base), MXBWD_TOL, what + " dk")
+    assert_close(to_np(dv), ref[2], MXBWD_TOL, what + " dv")
 
 
 def test_mxfp8_bwd_empty_sides():

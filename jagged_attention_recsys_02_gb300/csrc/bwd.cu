@@ -817,8 +817,7 @@ template <int D>
 __global__ void __launch_bounds__(256)
 bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
                       float* __restrict__ delta, float* __restrict__ dq_acc, long long Tq, int H,
-                      int softmax, const int* __restrict__ all_short, const int32_t* __restrict__ qo,
-                      const int32_t* __restrict__ ko, int B, int direct_kv, int short_q_max) {
+                      int softmax, const int* __restrict__ all_short) {
   constexpr int kLanesPerRow = D / 8;
   // no sample reduces into the accumulator: leave it alone
   const bool zero_acc = all_short == nullptr || *all_short == 0;
@@ -833,8 +832,7 @@ bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16
        row0 < nrows; row0 += warps * kRowsPerWarp) {
     const long long row = row0 + sub;
     const bool ok = row < nrows;
-    // (rows whose dQ the main kernel writes directly are left alone)
-    if (ok && zero_acc && !dq_row_direct(qo, ko, B, row / H, direct_kv, short_q_max)) {
+    if (ok && zero_acc) {
       float4* acc = reinterpret_cast<float4*>(dq_acc + row * D) + 2 * v;
       acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -862,23 +860,77 @@ bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16
 }
 
 // dq = bf16(dq_acc * scale), eight values (two 16-byte loads, one 16-byte
-// store) per thread and step; rows (token t, head h of row t * H + h, row
-// width d) whose dQ the main kernel wrote directly are skipped.
+// store) per thread and step.
 __global__ void __launch_bounds__(256)
 dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long long n8, float scale,
-                  const int* __restrict__ skip, const int32_t* __restrict__ qo,
-                  const int32_t* __restrict__ ko, int B, int H, int d, int direct_kv,
-                  int short_q_max) {
+                  const int* __restrict__ skip) {
   if (skip != nullptr && *skip != 0) return;  // dq was written directly
-  const long long row8 = static_cast<long long>(H) * (d / 8);  // steps per token
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    if (direct_kv > 0 && dq_row_direct(qo, ko, B, i / row8, direct_kv, short_q_max)) continue;
     const float4 a = acc[2 * i];
     const float4 b = acc[2 * i + 1];
     dq[i] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
                        pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
   }
+}
+
+// With dQ written directly for some samples (BwdParams::dq_direct_kv) the
+// accumulator is zeroed and converted only for the others.  Each block takes
+// kSegTokens consecutive tokens, finds the sample holding the first one (one
+// binary search over the offsets) and walks the samples of its range, handing
+// the accumulated pieces [a, b) of tokens to f: whole rows of H * d values,
+// contiguous in memory, so the block's stores stay coalesced.
+constexpr int kSegTokens = 64;
+template <typename F>
+__device__ __forceinline__ void acc_segments(const int32_t* __restrict__ qo,
+                                             const int32_t* __restrict__ ko, int B, long long Tq,
+                                             int direct_kv, int short_q_max, F&& f) {
+  const long long t0 = static_cast<long long>(blockIdx.x) * kSegTokens;
+  const long long t1 = min(Tq, t0 + kSegTokens);
+  if (t0 >= t1) return;
+  int lo = 0, hi = B - 1;  // the last sample starting at or before t0
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(qo + mid) <= t0) lo = mid; else hi = mid - 1;
+  }
+  long long t = t0;
+  for (int s = lo; s < B && t < t1; ++s) {
+    const long long e = min(t1, static_cast<long long>(__ldg(qo + s + 1)));
+    if (e <= t) continue;
+    const int Lq = __ldg(qo + s + 1) - __ldg(qo + s);
+    const int Lkv = __ldg(ko + s + 1) - __ldg(ko + s);
+    if (!(Lkv >= 1 && Lkv <= direct_kv && Lq > short_q_max)) f(t, e);
+    t = e;
+  }
+}
+
+__global__ void __launch_bounds__(256)
+dq_zero_segments_kernel(float4* __restrict__ acc, const int32_t* __restrict__ qo,
+                        const int32_t* __restrict__ ko, int B, long long Tq, int H, int d,
+                        int direct_kv, int short_q_max, const int* __restrict__ all_short) {
+  if (all_short != nullptr && *all_short != 0) return;  // nothing reduces into the accumulator
+  const long long row4 = static_cast<long long>(H) * d / 4;  // float4 per token
+  acc_segments(qo, ko, B, Tq, direct_kv, short_q_max, [&](long long a, long long b) {
+    for (long long i = a * row4 + threadIdx.x; i < b * row4; i += blockDim.x)
+      acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  });
+}
+
+__global__ void __launch_bounds__(256)
+dq_convert_segments_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, float scale,
+                           const int32_t* __restrict__ qo, const int32_t* __restrict__ ko, int B,
+                           long long Tq, int H, int d, int direct_kv, int short_q_max,
+                           const int* __restrict__ skip) {
+  if (skip != nullptr && *skip != 0) return;  // dq was written directly
+  const long long row8 = static_cast<long long>(H) * d / 8;  // 8-value groups per token
+  acc_segments(qo, ko, B, Tq, direct_kv, short_q_max, [&](long long a, long long b) {
+    for (long long i = a * row8 + threadIdx.x; i < b * row8; i += blockDim.x) {
+      const float4 x = acc[2 * i];
+      const float4 y = acc[2 * i + 1];
+      dq[i] = make_uint4(pack_bf16x2(x.x * scale, x.y * scale), pack_bf16x2(x.z * scale, x.w * scale),
+                         pack_bf16x2(y.x * scale, y.y * scale), pack_bf16x2(y.z * scale, y.w * scale));
+    }
+  });
 }
 
 // dq = bf16 of the rotary backward of scale * acc: each thread takes channels
@@ -989,16 +1041,24 @@ cudaError_t launch_bwd(const BwdParams& p, int act, const CUtensorMap& tq, const
 }
 
 cudaError_t launch_bwd_preprocess(const BwdParams& p, bool softmax, cudaStream_t stream) {
+  if (!softmax && p.dq_direct_kv > 0) {  // only the accumulated samples' rows need zeros
+    const long long blocks = (p.Tq + kSegTokens - 1) / kSegTokens;
+    if (blocks == 0) return cudaSuccess;
+    dq_zero_segments_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        reinterpret_cast<float4*>(p.dq_acc), p.qo, p.ko, p.B, p.Tq, p.H, p.d, p.dq_direct_kv,
+        p.short_q_max, p.all_short);
+    return cudaGetLastError();
+  }
   const long long rows = p.Tq * p.H;
   const int pre_blocks = static_cast<int>(rows / 8 + 1 < 4096 ? rows / 8 + 1 : 4096);
   if (p.d == 64)
-    bwd_preprocess_kernel<64><<<pre_blocks, 256, 0, stream>>>(
-        p.out, p.dout, p.delta, p.dq_acc, p.Tq, p.H, softmax ? 1 : 0, p.all_short, p.qo, p.ko, p.B,
-        p.dq_direct_kv, p.short_q_max);
+    bwd_preprocess_kernel<64><<<pre_blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
+                                                              p.Tq, p.H, softmax ? 1 : 0,
+                                                              p.all_short);
   else
-    bwd_preprocess_kernel<128><<<pre_blocks, 256, 0, stream>>>(
-        p.out, p.dout, p.delta, p.dq_acc, p.Tq, p.H, softmax ? 1 : 0, p.all_short, p.qo, p.ko, p.B,
-        p.dq_direct_kv, p.short_q_max);
+    bwd_preprocess_kernel<128><<<pre_blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
+                                                               p.Tq, p.H, softmax ? 1 : 0,
+                                                               p.all_short);
   return cudaGetLastError();
 }
 
@@ -1015,14 +1075,19 @@ cudaError_t launch_dq_convert_rope(const float* acc, void* dq, const int32_t* of
 
 cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale,
                               cudaStream_t stream, const int* skip, const BwdParams* direct) {
+  if (direct != nullptr && direct->dq_direct_kv > 0) {  // the accumulated samples' rows only
+    const long long blocks = (direct->Tq + kSegTokens - 1) / kSegTokens;
+    if (blocks == 0) return cudaSuccess;
+    dq_convert_segments_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        reinterpret_cast<const float4*>(acc), reinterpret_cast<uint4*>(dq), scale, direct->qo,
+        direct->ko, direct->B, direct->Tq, direct->H, direct->d, direct->dq_direct_kv,
+        direct->short_q_max, skip);
+    return cudaGetLastError();
+  }
   const long long n8 = n / 8;  // n = Tq * H * d with d in {64, 128}
   const int blocks = static_cast<int>(n8 / 256 + 1 < 8192 ? n8 / 256 + 1 : 8192);
-  const bool dir = direct != nullptr && direct->dq_direct_kv > 0;
-  dq_convert_kernel<<<blocks, 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(acc), reinterpret_cast<uint4*>(dq), n8, scale, skip,
-      dir ? direct->qo : nullptr, dir ? direct->ko : nullptr, dir ? direct->B : 0,
-      dir ? direct->H : 1, dir ? direct->d : 128, dir ? direct->dq_direct_kv : 0,
-      dir ? direct->short_q_max : 0);
+  dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(acc),
+                                                reinterpret_cast<uint4*>(dq), n8, scale, skip);
   return cudaGetLastError();
 }
 

@@ -185,22 +185,6 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
-// Whether token t's dQ row is written directly in bf16 by the general backward
-// (see BwdParams::dq_direct_kv): the sample holding t is found by a binary
-// search over the query offsets (the last sample starting at or before t; an
-// empty sample shares its start with the next one, which then wins).
-__device__ __forceinline__ bool dq_row_direct(const int32_t* qo, const int32_t* ko, int B,
-                                              long long t, int direct_kv, int short_q_max) {
-  if (direct_kv <= 0) return false;
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(qo + mid) <= t) lo = mid; else hi = mid - 1;
-  }
-  const int Lq = __ldg(qo + lo + 1) - __ldg(qo + lo);
-  const int Lkv = __ldg(ko + lo + 1) - __ldg(ko + lo);
-  return Lkv >= 1 && Lkv <= direct_kv && Lq > short_q_max;
-}
 
 struct FwdParams {
   const int32_t* qo;

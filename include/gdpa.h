@@ -87,8 +87,10 @@ typedef enum { GDPA_BIAS_NONE = 0, GDPA_BIAS_RELPOS = 1, GDPA_BIAS_DENSE = 2 } g
  * max_rel is ignored.  The dense bias is read from global memory by the
  * kernels' activation warps; it is supported by gdpa_fwd, gdpa_bwd,
  * gdpa_fwd_noalloc, gdpa_fwd_window and gdpa_bwd_window / gdpa_bwd_rope
- * (these two also return its gradient), with or without a sliding window;
- * the block-aligned and MXFP8 entry points give GDPA_ERR_UNSUPPORTED. */
+ * (these two also return its gradient), with or without a sliding window, by
+ * gdpa_block_fwd / gdpa_block_bwd / gdpa_block_bwd_dbias (the last with its
+ * gradient) and by gdpa_fwd_mxfp8(_window); the MXFP8 backward entry points
+ * give GDPA_ERR_UNSUPPORTED. */
 typedef struct {
   int kind;                /* gdpa_bias_kind */
   const float* table;      /* device pointer, ignored for GDPA_BIAS_NONE */
@@ -182,8 +184,11 @@ gdpa_status gdpa_bwd_window(const void* q, const int32_t* q_offsets, const void*
  * logsumexp traffic or a separate D pass).  Self-attention: q, k, v share
  * `offsets` (T rows).  The tokens of each sample are cut into blocks of 64
  * from the sample's first token (the last block may be shorter); row i sees
- * the keys of its own block (and only j <= i when causal).  Scores, bias,
- * activations and layouts are those of gdpa_fwd.  The forward writes `out`
+ * the keys of its own block (and only j <= i when causal).  Scores, bias
+ * (the relative-position table or a dense jagged bias, of which only the
+ * pairs inside a block are read), activations and layouts are those of
+ * gdpa_fwd; a dense bias's offsets are checked on the device like the
+ * offsets (GDPA_ERR_BAD_OFFSETS).  The forward writes `out`
  * only: no logsumexp (the backward recomputes each row's exact softmax from
  * its block).  workspace: gdpa_block_workspace_size() bytes of device memory
  * (the tile list), shared by gdpa_block_fwd and gdpa_block_bwd.  Malformed
@@ -213,14 +218,20 @@ gdpa_status gdpa_block_bwd(const void* q, const int32_t* offsets, const void* k,
                            int causal, float scale, float rope_base, const void* dout, void* dq,
                            void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream);
 
-/* gdpa_block_bwd with the gradient of a relative-position table: dbias (fp32
- * device memory [H][2*max_rel-1], ADDED to, as in gdpa_bwd_window) receives,
- * at entry clamp(i - j + max_rel - 1), the sum of dS_ij over the pairs each
- * row sees in its block.  Each tile's sums are gathered in shared memory and
- * added to the table with global atomics, so their order, and the sums' last
- * bits, vary between runs.  dbias = NULL is gdpa_block_bwd; a dbias without a
- * GDPA_BIAS_RELPOS bias, or not 4-byte aligned: GDPA_ERR_INVALID_ARG.  Every
- * other argument, output and error is that of gdpa_block_bwd. */
+/* gdpa_block_bwd with the gradient of the bias (fp32 device memory, ADDED to,
+ * as in gdpa_bwd_window):
+ *   GDPA_BIAS_RELPOS: dbias [H][2*max_rel-1] receives, at entry
+ *   clamp(i - j + max_rel - 1), the sum of dS_ij over the pairs each row sees
+ *   in its block.  Each tile's sums are gathered in shared memory and added
+ *   to the table with global atomics, so their order, and the sums' last
+ *   bits, vary between runs.
+ *   GDPA_BIAS_DENSE: dbias in the dense bias's own layout; the entry of each
+ *   pair a row sees in its block receives that pair's dS_ij (the bf16 value
+ *   the softmax products use, the fp32 one for the other activations); the
+ *   entries of other pairs are left as they are.
+ * dbias = NULL is gdpa_block_bwd; a dbias without a bias, or not 4-byte
+ * aligned: GDPA_ERR_INVALID_ARG.  Every other argument, output and error is
+ * that of gdpa_block_bwd. */
 gdpa_status gdpa_block_bwd_dbias(const void* q, const int32_t* offsets, const void* k,
                                  const void* v, int B, int H, int d, int64_t T,
                                  const gdpa_bias* bias, int act, int causal, float scale,
@@ -283,8 +294,10 @@ gdpa_status gdpa_quantize_mxfp8(const void* x, const int32_t* offsets, int B, in
  *     [B + Tkv/32 + 1][H][128] u8), quantised with the same kv_offsets.
  * d must be 128 and act GDPA_ACT_SOFTMAX (an unnormalised GDPA sum of
  * thousands of E4M3-rounded terms would not keep the output's precision);
- * other values return GDPA_ERR_UNSUPPORTED.  Every other argument, the
- * outputs and the workspace (gdpa_fwd_workspace_size) are those of gdpa_fwd. */
+ * other values return GDPA_ERR_UNSUPPORTED.  The bias (a relative-position
+ * table or a dense jagged bias) is added in fp32 to the fp32 scores.  Every
+ * other argument, the outputs and the workspace (gdpa_fwd_workspace_size)
+ * are those of gdpa_fwd. */
 gdpa_status gdpa_fwd_mxfp8(const void* q_codes, const void* q_scales, const int32_t* q_offsets,
                            const void* k_codes, const void* k_scales, const void* v_codes,
                            const void* v_scales, const int32_t* kv_offsets, int B, int H, int d,

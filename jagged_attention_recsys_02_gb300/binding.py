@@ -317,9 +317,10 @@ def gdpa_block_bwd(q, offsets, k, v, dout, *, act, causal=False, scale, bias=Non
                    rope_base=0.0, dq=None, dk=None, dv=None, dbias=None, workspace=None,
                    stream=None):
     """Block-aligned attention backward through the C ABI (gdpa_block_bwd, or
-    gdpa_block_bwd_dbias when the bias table's gradient `dbias` [H, 2*max_rel-1]
-    fp32 is given, which is added to).  Returns (dq, dk, dv); with rope_base > 0,
-    dq and dk are gradients of the un-rotated q and k."""
+    gdpa_block_bwd_dbias when the bias's gradient `dbias` fp32 is given, which
+    is added to: the table's [H, 2*max_rel-1], or a dense bias's values'
+    layout).  Returns (dq, dk, dv); with rope_base > 0, dq and dk are gradients
+    of the un-rotated q and k."""
     lib = load()
     T, H, d = q.shape
     B = offsets.numel() - 1

@@ -527,7 +527,6 @@ gdpa_status gdpa_block_fwd(const void* q, const int32_t* offsets, const void* k,
   t_launches = 0;
   gdpa_status st = check_common(q, offsets, k, v, offsets, B, H, d, T, T, bias, act, causal, 0);
   if (st != GDPA_OK) return st;
-  if (is_dense(bias)) return GDPA_ERR_UNSUPPORTED;
   if (T > 0 && (out == nullptr || !aligned16(out))) return GDPA_ERR_INVALID_ARG;
   const size_t need = gdpa_block_workspace_size(B, H, d, T);
   if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return GDPA_ERR_WORKSPACE;
@@ -545,7 +544,9 @@ gdpa_status gdpa_block_fwd(const void* q, const int32_t* offsets, const void* k,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* n_tiles = reinterpret_cast<int*>(ws);
   int4* tiles = reinterpret_cast<int4*>(ws + 256);
-  if (launch_block_list(offsets, B, T, tiles, n_tiles, dev->status, s) != cudaSuccess)
+  const int64_t* dense_off = is_dense(bias) ? bias->offsets : nullptr;
+  if (launch_block_list(offsets, B, T, tiles, n_tiles, dev->status, s, dense_off, H) !=
+      cudaSuccess)
     return GDPA_ERR_CUDA;
   ++t_launches;
   BlockParams p{};
@@ -558,6 +559,10 @@ gdpa_status gdpa_block_fwd(const void* q, const int32_t* offsets, const void* k,
   p.max_rel = max_rel;
   p.causal = causal;
   p.scale = scale;
+  p.bias_dense = dense_off != nullptr ? bias->table : nullptr;
+  p.bias_off = dense_off;
+  p.offsets = offsets;
+  p.B = B;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.status = dev->status;
   const int64_t max_items = max_block_tiles(B, T) * H;
@@ -587,9 +592,8 @@ gdpa_status gdpa_block_bwd_dbias(const void* q, const int32_t* offsets, const vo
   t_launches = 0;
   gdpa_status st = check_common(q, offsets, k, v, offsets, B, H, d, T, T, bias, act, causal, 0);
   if (st != GDPA_OK) return st;
-  if (is_dense(bias)) return GDPA_ERR_UNSUPPORTED;
-  if (dbias != nullptr) {  // the gradient of a relative-position table needs that table
-    if (bias_kind(bias) != GDPA_BIAS_RELPOS) return GDPA_ERR_INVALID_ARG;
+  if (dbias != nullptr) {  // the gradient of a bias needs that bias (a table or a dense bias)
+    if (bias_kind(bias) == GDPA_BIAS_NONE) return GDPA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(dbias) & 3u) return GDPA_ERR_INVALID_ARG;
   }
   if (!(rope_base >= 0.0f) || rope_base > 3.0e38f) return GDPA_ERR_INVALID_ARG;  // NaN, < 0, inf
@@ -611,7 +615,9 @@ gdpa_status gdpa_block_bwd_dbias(const void* q, const int32_t* offsets, const vo
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* n_tiles = reinterpret_cast<int*>(ws);
   int4* tiles = reinterpret_cast<int4*>(ws + 256);
-  if (launch_block_list(offsets, B, T, tiles, n_tiles, dev->status, s) != cudaSuccess)
+  const int64_t* dense_off = is_dense(bias) ? bias->offsets : nullptr;
+  if (launch_block_list(offsets, B, T, tiles, n_tiles, dev->status, s, dense_off, H) !=
+      cudaSuccess)
     return GDPA_ERR_CUDA;
   ++t_launches;
   BlockParams p{};
@@ -624,6 +630,10 @@ gdpa_status gdpa_block_bwd_dbias(const void* q, const int32_t* offsets, const vo
   p.max_rel = max_rel;
   p.causal = causal;
   p.scale = scale;
+  p.bias_dense = dense_off != nullptr ? bias->table : nullptr;
+  p.bias_off = dense_off;
+  p.offsets = offsets;
+  p.B = B;
   p.dout = static_cast<const __nv_bfloat16*>(dout);
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
@@ -691,7 +701,6 @@ gdpa_status gdpa_fwd_mxfp8_window(const void* q_codes, const void* q_scales,
   gdpa_status st = check_common(q_codes, q_offsets, k_codes, v_codes, kv_offsets, B, H, d, Tq,
                                 Tkv, bias, act, causal, window);
   if (st != GDPA_OK) return st;
-  if (is_dense(bias)) return GDPA_ERR_UNSUPPORTED;
   if (d != 128 || act != GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
   if (Tq > 0 && (q_scales == nullptr || out == nullptr || lse == nullptr || !aligned16(out)))
     return GDPA_ERR_INVALID_ARG;
@@ -720,8 +729,9 @@ gdpa_status gdpa_fwd_mxfp8_window(const void* q_codes, const void* q_scales,
   int* n_items = reinterpret_cast<int*>(ws);
   int* ticket = reinterpret_cast<int*>(ws + 4);
   int2* items = reinterpret_cast<int2*>(ws + 256);
+  const int64_t* dense_off = is_dense(bias) ? bias->offsets : nullptr;
   if (launch_build_worklist(q_offsets, kv_offsets, B, H, Tq, Tkv, causal, window, 0, items,
-                            n_items, ticket, dev->status, s) != cudaSuccess)
+                            n_items, ticket, dev->status, s, dense_off) != cudaSuccess)
     return GDPA_ERR_CUDA;
   ++t_launches;
   FwdParams p{};
@@ -734,6 +744,8 @@ gdpa_status gdpa_fwd_mxfp8_window(const void* q_codes, const void* q_scales,
   p.Tkv = Tkv;
   p.bias_table = table;
   p.max_rel = max_rel;
+  p.bias_dense = dense_off != nullptr ? bias->table : nullptr;
+  p.bias_off = dense_off;
   p.causal = causal;
   p.window = window;
   p.scale = scale;

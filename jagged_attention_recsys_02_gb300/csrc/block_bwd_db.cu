@@ -6,8 +6,8 @@ namespace gdpa {
 
 cudaError_t launch_block_bwd_dbias(const BlockParams& p, int act, const CUtensorMap* maps, int grid,
                                    cudaStream_t s) {
-  return p.d == 64 ? launch_bwd_d<64, true>(p, act, maps, grid, s)
-                   : launch_bwd_d<128, true>(p, act, maps, grid, s);
+  return p.d == 64 ? launch_bwd_d<64, true, false>(p, act, maps, grid, s)
+                   : launch_bwd_d<128, true, false>(p, act, maps, grid, s);
 }
 
 }  // namespace gdpa

@@ -1,6 +1,8 @@
 // Block-aligned attention: the backward kernel and its launch templates
 // (shared pieces in block_common.cuh), compiled from block_bwd.cu (without
-// the bias-table gradient) and block_bwd_db.cu (with it).
+// a bias gradient), block_bwd_db.cu (the bias-table gradient),
+// block_bwd_dense.cu (a dense jagged bias) and block_bwd_dense_db.cu (a dense
+// bias and its gradient).
 #pragma once
 #include "block_common.cuh"
 
@@ -93,7 +95,7 @@ __device__ __forceinline__ void ps_zero_atom(uint8_t* ps, int r, int atom) {
     *reinterpret_cast<uint4*>(row + ((v ^ (r & 7)) * 16)) = make_uint4(0, 0, 0, 0);
 }
 
-template <int D, int ACT, bool kDBias>
+template <int D, int ACT, bool kDBias, bool kDense>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
@@ -327,7 +329,11 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     // entry of its diagonal (a warp's 32 rows hit 32 different entries per
     // key), flushed to the table after every tile
     float* dwin = reinterpret_cast<float*>(gbase + C::kDbWin);
-    constexpr bool want_db = kDBias;
+    constexpr bool want_db = kDBias && !kDense;
+    // dense bias (kDense): row r's value of column c is drow[c]; its gradient
+    // (kDBias too) goes to the same place in p.dbias, each pair's dS added
+    // once by the thread that owns the pair
+    constexpr bool kDenseGrad = kDBias && kDense;
     uint32_t n_db = 0;
     for (int k = 0;; ++k) {
       const int item = item_of(k);
@@ -353,6 +359,19 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       }
       int c_lo, c_hi;
       row_keys(ti, r, p.causal, &c_lo, &c_hi);
+      const float* drow = nullptr;
+      float* grow = nullptr;
+      if (kDense) {
+        const long long base = dense_row_base(p, ti, r, head);
+        if (base >= 0) {
+          drow = p.bias_dense + base;
+          if (kDenseGrad) grow = p.dbias + base;
+        }
+      }
+      // dense-bias gradient of (row r, column c), keys the row sees only
+      auto add_dense = [&](int c, float v) {
+        if (c >= c_lo && c < c_hi) atomicAdd(grow + c, v);
+      };
       bool w = mbar_wait(bar(C::kSFull), k & 1u, abort_flag);
       if (!__all_sync(0xffffffffu, w)) { if (lane == 0) fail(); break; }
       tc_fence_after();
@@ -375,7 +394,11 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
           for (int i = 0; i < 32; ++i) {
             const int c = cb + 32 * ch + i;
             float v = __uint_as_float(sr[i]) * c_s;
-            if (has_bias) v += bwin[-c];
+            if (kDense) {
+              if (c >= c_lo && c < c_hi) v += __ldg(drow + c) * (kSoftmax ? kLog2e : 1.0f);
+            } else if (has_bias) {
+              v += bwin[-c];
+            }
             x[i] = (c >= c_lo && c < c_hi) ? v : (kSoftmax ? -INFINITY : __int_as_float(0x7fffffff));
           }
         };
@@ -461,6 +484,10 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
                 add_db(cb + 32 * ch + 2 * i, d0);
                 add_db(cb + 32 * ch + 2 * i + 1, d1);
               }
+              if (kDenseGrad) {  // the bf16 dS the products use
+                add_dense(cb + 32 * ch + 2 * i, __uint_as_float(dw[i] << 16));
+                add_dense(cb + 32 * ch + 2 * i + 1, __uint_as_float(dw[i] & 0xFFFF0000u));
+              }
             }
             ps_store_row<1>(ps, r, cb + 32 * ch, dw);
           }
@@ -513,6 +540,10 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
               if (want_db) {
                 add_db(cb + 32 * ch + 2 * i, d0);
                 add_db(cb + 32 * ch + 2 * i + 1, d1);
+              }
+              if (kDenseGrad) {
+                add_dense(cb + 32 * ch + 2 * i, d0);
+                add_dense(cb + 32 * ch + 2 * i + 1, d1);
               }
               const uint32_t h = pack_bf16x2(d0, d1);
               dw[i] = h;
@@ -689,38 +720,38 @@ block_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   }
 }
 
-template <int D, int ACT, bool kDBias>
+template <int D, int ACT, bool kDBias, bool kDense>
 cudaError_t launch_bwd_db(const BlockParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                           const CUtensorMap& tdk, const CUtensorMap& tdv, int grid, cudaStream_t s) {
   constexpr int smem = BbCfg<D>::kSmemBytes;
   static_assert(smem <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(block_bwd_kernel<D, ACT, kDBias>,
+  cudaError_t e = cudaFuncSetAttribute(block_bwd_kernel<D, ACT, kDBias, kDense>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  block_bwd_kernel<D, ACT, kDBias><<<grid, kBwdThreads, smem, s>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
+  block_bwd_kernel<D, ACT, kDBias, kDense><<<grid, kBwdThreads, smem, s>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
   return cudaGetLastError();
 }
 
 
-template <int D, bool kDBias>
+template <int D, bool kDBias, bool kDense>
 cudaError_t launch_bwd_d(const BlockParams& p, int act, const CUtensorMap* m, int grid,
                          cudaStream_t s) {
   switch (act) {
     case GDPA_ACT_SOFTMAX:
-      return launch_bwd_db<D, GDPA_ACT_SOFTMAX, kDBias>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
+      return launch_bwd_db<D, GDPA_ACT_SOFTMAX, kDBias, kDense>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
                                                  grid, s);
     case GDPA_ACT_SILU:
-      return launch_bwd_db<D, GDPA_ACT_SILU, kDBias>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
+      return launch_bwd_db<D, GDPA_ACT_SILU, kDBias, kDense>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
                                                  grid, s);
     case GDPA_ACT_GELU_TANH:
-      return launch_bwd_db<D, GDPA_ACT_GELU_TANH, kDBias>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
+      return launch_bwd_db<D, GDPA_ACT_GELU_TANH, kDBias, kDense>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
                                                  grid, s);
     case GDPA_ACT_GELU_ERF:
-      return launch_bwd_db<D, GDPA_ACT_GELU_ERF, kDBias>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
+      return launch_bwd_db<D, GDPA_ACT_GELU_ERF, kDBias, kDense>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
                                                  grid, s);
     default:
-      return launch_bwd_db<D, GDPA_ACT_IDENTITY, kDBias>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
+      return launch_bwd_db<D, GDPA_ACT_IDENTITY, kDBias, kDense>(p, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
                                                  grid, s);
   }
 }

@@ -23,9 +23,9 @@
 // the (tile, head) items with a static stride over a persistent grid (every
 // item costs the same).
 //
-// This header holds what the forward (block.cu) and backward (block_bwd.cu)
-// translation units share: the tile descriptor, the row's key range, the
-// activation and the bias window.
+// This header holds what the forward (block_fwd_kernel.cuh) and backward
+// (block_bwd_kernel.cuh) kernels share: the tile descriptor, the row's key
+// range, the activation, the bias window and the dense bias's row address.
 #pragma once
 #include <type_traits>
 
@@ -68,6 +68,24 @@ __device__ __forceinline__ void row_keys(const TileInfo& ti, int r, int causal, 
   if (causal) hi = min(hi, r + 1);
   *c_lo = lo;
   *c_hi = hi;
+}
+
+// Dense bias of tile row r for one head: the value for (row r, tile column c)
+// is p.bias_dense[base + c] for the keys the row sees (its own block, so its
+// own sample); -1 for rows past the tile.  The row's sample is the last b
+// with offsets[b] <= its global row (empty samples are skipped by that).
+__device__ __forceinline__ long long dense_row_base(const BlockParams& p, const TileInfo& ti,
+                                                    int r, int head) {
+  if (r >= ti.rows) return -1;
+  const int gr = ti.row0 + r;
+  int lo = 0, hi = p.B;  // offsets[lo] <= gr < offsets[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.offsets + mid) <= gr) lo = mid; else hi = mid;
+  }
+  const int s0 = __ldg(p.offsets + lo);
+  const long long L = __ldg(p.offsets + lo + 1) - s0;
+  return __ldg(p.bias_off + lo) + (head * L + (gr - s0)) * L + (ti.row0 - s0);
 }
 
 __device__ __forceinline__ float act_fwd(int act, float x) {

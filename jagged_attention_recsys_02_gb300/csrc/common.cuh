@@ -251,13 +251,20 @@ struct BlockParams {
   int max_rel;
   int causal;
   float scale;
+  // dense jagged bias instead of the table (nullptr: none): sample b's
+  // [H][L_b][L_b] values from bias_dense + bias_off[b]; offsets / B locate a
+  // row's sample
+  const float* bias_dense;
+  const int64_t* bias_off;
+  const int32_t* offsets;
+  int B;
   __nv_bfloat16* out;             // forward output
   const __nv_bfloat16* dout;      // backward inputs / outputs
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   float rope_base;                // > 0: dq, dk go back through the rotary embedding
-  float* dbias;                   // backward: the bias table's gradient, added to (nullptr: none)
+  float* dbias;                   // backward: the bias's gradient, added to (nullptr: none)
   int* status;
 };
 
@@ -378,17 +385,30 @@ cudaError_t launch_fwd_mx(const FwdParams& p, const CUtensorMap& tq, const CUten
                           const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
                           const uint8_t* v_sc, long long v_sc_rows, int grid, cudaStream_t s);
 
+// bias_off (a dense bias's per-sample offsets, H heads) is checked with the
+// offsets: GDPA_ERR_BAD_OFFSETS unless sample b holds H * L_b^2 values.
 cudaError_t launch_block_list(const int32_t* offsets, int B, int64_t T, int4* tiles, int* n_tiles,
-                              int* status, cudaStream_t s);
+                              int* status, cudaStream_t s, const int64_t* bias_off = nullptr,
+                              int H = 0);
 cudaError_t launch_block_fwd(const BlockParams& p, int act, const CUtensorMap& tq,
                              const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                              cudaStream_t s);
+// The dense-bias instantiations of the block forward (p.bias_dense set).
+cudaError_t launch_block_fwd_dense(const BlockParams& p, int act, const CUtensorMap& tq,
+                                   const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                                   cudaStream_t s);
 // maps: q, k, v, dout, dq, dk, dv (bf16 [T][H][d], 128-row boxes)
 cudaError_t launch_block_bwd(const BlockParams& p, int act, const CUtensorMap* maps, int grid,
                              cudaStream_t s);
 // The bias-table gradient's instantiations of the block backward (p.dbias set).
 cudaError_t launch_block_bwd_dbias(const BlockParams& p, int act, const CUtensorMap* maps, int grid,
                                    cudaStream_t s);
+// The dense-bias instantiations of the block backward, without and with the
+// dense bias's gradient (p.bias_dense set; p.dbias selects the gradient).
+cudaError_t launch_block_bwd_dense(const BlockParams& p, int act, const CUtensorMap* maps, int grid,
+                                   cudaStream_t s);
+cudaError_t launch_block_bwd_dense_db(const BlockParams& p, int act, const CUtensorMap* maps,
+                                      int grid, cudaStream_t s);
 
 // Upper bound on the number of work items (host-side sizing).
 inline int64_t max_fwd_items(int B, int H, int64_t Tq) {

@@ -151,7 +151,9 @@ __device__ __forceinline__ ItemInfo decode_item(int2 it, const FwdParams& p) {
   return r;
 }
 
-template <bool kBand>
+// kDense: a dense jagged bias (p.bias_dense) instead of the relative-position
+// table; each activation thread reads its row's values of the key tile.
+template <bool kBand, bool kDense>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
               const __grid_constant__ CUtensorMap tmap_v, const FwdParams p,
@@ -499,6 +501,11 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       const int col_lim = kBand ? band_key_end(r, p.causal, p.window, in.Lkv)
                                 : (p.causal ? min(in.Lkv, r + 1) : in.Lkv);
       const bool has_bias = p.bias_table != nullptr;
+      // dense bias row of this query: one value per key
+      const float* drow = nullptr;
+      if (kDense && row_valid)
+        drow = p.bias_dense + p.bias_off[in.b] +
+               (static_cast<long long>(in.head) * in.Lq + r) * in.Lkv;
       float m = -INFINITY, l = 0.0f;
       bool abort_now = false;
       for (int j = j_lo; j < j_hi; ++j) {
@@ -524,7 +531,13 @@ fwd_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 #pragma unroll
           for (int q2 = 0; q2 < 16; ++q2) {
             float2 b = make_float2(-sub, -sub);
-            if (has_bias) {
+            if (kDense) {  // the row's value of each visible column
+              const int c = c0 + chunk * 32 + 2 * q2;
+              if (drow != nullptr && (!kBand || c >= col_lo) && c < col_lim)
+                b.x = fmaf(__ldg(drow + c), kLog2e, -sub);
+              if (drow != nullptr && (!kBand || c + 1 >= col_lo) && c + 1 < col_lim)
+                b.y = fmaf(__ldg(drow + c + 1), kLog2e, -sub);
+            } else if (has_bias) {
               const float2 bb = *reinterpret_cast<const float2*>(bwin + chunk * 32 + 2 * q2);
               b = make_float2(bb.x - sub, bb.y - sub);
             }
@@ -660,7 +673,9 @@ int fwd_mx_tile_rows() { return kTile; }
 cudaError_t launch_fwd_mx(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
                           const uint8_t* v_sc, long long v_sc_rows, int grid, cudaStream_t s) {
-  auto kernel = p.window > 0 ? fwd_mx_kernel<true> : fwd_mx_kernel<false>;
+  const bool dense = p.bias_dense != nullptr;
+  auto kernel = p.window > 0 ? (dense ? fwd_mx_kernel<true, true> : fwd_mx_kernel<true, false>)
+                             : (dense ? fwd_mx_kernel<false, true> : fwd_mx_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;

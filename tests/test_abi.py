@@ -219,7 +219,7 @@ def test_mxfp8_backward_workspace_size(lib):
 
 def test_dense_bias_rejections_on_host(lib):
     """A dense bias needs its values and its int64 offsets (4- and 8-byte
-    aligned); it has no block or MXFP8 path."""
+    aligned); it has no MXFP8 backward."""
     D = binding.BIAS_DENSE
     dense = lambda table=FAKE, off=FAKE + 64: ctypes.byref(binding.gdpa_bias(D, table, 0, off))
     assert _fwd(lib, bias=dense(off=None)) == INVALID
@@ -238,10 +238,18 @@ def test_dense_bias_rejections_on_host(lib):
     assert lib.gdpa_bwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, 10, dense(), 0, 0, 0,
                                0.125, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, FAKE, 1 << 20,
                                None) == INVALID
+    # the block kernels take it (the missing workspace is the next check), and
+    # the block backward returns its gradient
     assert lib.gdpa_block_fwd(FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, dense(), 0, 0, 0.125, FAKE,
-                              FAKE, 1 << 20, None) == UNSUPPORTED
+                              None, 0, None) == WORKSPACE
+    blk_bwd = lambda dbias: lib.gdpa_block_bwd_dbias(FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 10, dense(),
+                                                     0, 0, 0.125, 0.0, FAKE, FAKE, FAKE, FAKE,
+                                                     dbias, None, 0, None)
+    assert blk_bwd(FAKE) == WORKSPACE
+    assert blk_bwd(FAKE + 2) == INVALID
+    # the MXFP8 forward takes it too, the MXFP8 backward does not
     assert lib.gdpa_fwd_mxfp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 10, 10,
-                              dense(), 0, 0, 0.125, FAKE, FAKE, FAKE, 1 << 20, None) == UNSUPPORTED
+                              dense(), 0, 0, 0.125, FAKE, FAKE, None, 0, None) == WORKSPACE
     assert _bwd_mx(lib, bias=dense()) == UNSUPPORTED
 
 

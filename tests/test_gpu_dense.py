@@ -1,7 +1,8 @@
 """GPU parity of the dense jagged bias (one fp32 value per head, query and key
 of each sample) against the oracle: forward for every activation, the softmax
 and GDPA backward, the bias's gradient, causal and not, ragged lengths,
-malformed bias offsets."""
+malformed bias offsets; with a sliding window, the fused rotary backward and
+the block-aligned kernels."""
 import numpy as np
 import pytest
 import torch
@@ -17,7 +18,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _case(lq, lkv, H, d, act, causal, seed, std=1.0, window=0):
+def _case(lq, lkv, H, d, act, causal, seed, std=1.0, window=0, block=0):
     g = torch.Generator(device=DEV).manual_seed(seed)
     q = rand_bf16((sum(lq), H, d), g, DEV)
     k = rand_bf16((sum(lkv), H, d), g, DEV)
@@ -29,7 +30,7 @@ def _case(lq, lkv, H, d, act, causal, seed, std=1.0, window=0):
     qo, ko = torch.from_numpy(qo_np).to(DEV), torch.from_numpy(ko_np).to(DEV)
     off = torch.from_numpy(off_np).to(DEV)
     return dict(q=q, k=k, v=v, do=do, qo=qo, ko=ko, qo_np=qo_np, ko_np=ko_np, vals=vals, off=off,
-                act=ACTS[act], causal=causal, scale=1.0 / np.sqrt(d), window=window)
+                act=ACTS[act], causal=causal, scale=1.0 / np.sqrt(d), window=window, block=block)
 
 
 def _fwd(c):
@@ -46,7 +47,7 @@ def _fwd(c):
 
 def _ref_kw(c):
     return dict(act=c["act"], causal=c["causal"], scale=c["scale"], window=c["window"],
-                dense_bias=c["vals"].double().cpu().numpy())
+                block=c["block"], dense_bias=c["vals"].double().cpu().numpy())
 
 
 CASES = [
@@ -110,7 +111,7 @@ def check_dense_gradient(c, got, base, what):
     pair = np.zeros(int(off[-1]))
     for b, h, live, e in ds_pair_bounds(qn, c["qo_np"], kn, vn, c["ko_np"], don, o_ref,
                                         act=c["act"], causal=c["causal"], scale=c["scale"],
-                                        window=c["window"],
+                                        window=c["window"], block=c["block"],
                                         bias_of=lambda b, h, i, j: vals[
                                             off[b] + (h * i.shape[0] + i) * j.shape[1] + j]):
         n = live.size
@@ -224,3 +225,75 @@ def test_dense_bias_bad_offsets_are_reported():
     binding.gdpa_fwd(c["q"], c["qo"], c["k"], c["v"], c["ko"], act=0, scale=c["scale"],
                      bias=(c["vals"], bad), out=out, lse=lse)
     assert binding.device_status() == 6   # GDPA_ERR_BAD_OFFSETS
+
+
+BLOCK = 64
+BLOCK_LENS = [1, 64, 65, 128, 129, 300, 0, 257, 200]  # blocks and tiles across samples
+
+
+def _block_fwd(c):
+    T, H, d = c["q"].shape
+    buf, out = guarded(T, H, d, DEV)
+    binding.gdpa_block_fwd(c["q"], c["qo"], c["k"], c["v"], act=c["act"], causal=c["causal"],
+                           scale=c["scale"], bias=(c["vals"], c["off"]), out=out)
+    assert binding.device_status() == 0
+    check_guards(buf)
+    return out
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh", "gelu_erf", "identity"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_dense_bias_block_forward(causal, act, d):
+    """The block-aligned forward with a dense bias: only the pairs inside a
+    64-token block are read; against the oracle with the same blocks."""
+    c = _case(BLOCK_LENS, BLOCK_LENS, 2, d, act, causal, seed=60 + d, block=BLOCK)
+    out = _block_fwd(c)
+    ro, _ = oracle.fwd(to_np(c["q"]), c["qo_np"], to_np(c["k"]), to_np(c["v"]), c["ko_np"],
+                       **_ref_kw(c))
+    assert_close(to_np(out), ro, FWD_TOL, f"dense+block {act} d={d} causal={causal} out")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("act", ["softmax", "silu", "gelu_tanh"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_dense_bias_block_backward_and_gradient(causal, act, d):
+    """The block-aligned backward with a dense bias: dq, dk, dv against the
+    oracle; with dbias the entry of every pair inside a block gets its dS
+    added (the other entries are left as they are) and dq, dk, dv are those
+    of the call without it, bit for bit (each tile writes its rows once)."""
+    c = _case(BLOCK_LENS, BLOCK_LENS, 2, d, act, causal, seed=70 + d, block=BLOCK)
+    T, H, _ = c["q"].shape
+    kw = dict(act=c["act"], causal=c["causal"], scale=c["scale"], bias=(c["vals"], c["off"]))
+    bufs = [guarded(T, H, d, DEV) for _ in range(3)]
+    binding.gdpa_block_bwd(c["q"], c["qo"], c["k"], c["v"], c["do"], dq=bufs[0][1],
+                           dk=bufs[1][1], dv=bufs[2][1], **kw)
+    assert binding.device_status() == 0
+    for b_, _ in bufs:
+        check_guards(b_)
+    ref = oracle.bwd(to_np(c["q"]), c["qo_np"], to_np(c["k"]), to_np(c["v"]), c["ko_np"],
+                     to_np(c["do"]), **_ref_kw(c))
+    what = f"dense+block {act} d={d} causal={causal}"
+    for name, (_, got), r in zip(("dq", "dk", "dv"), bufs, ref):
+        assert_close(to_np(got), r, BWD_TOL, f"{what} {name}")
+    g = torch.Generator(device=DEV).manual_seed(9)
+    base = torch.randn(c["vals"].numel(), generator=g, device=DEV)
+    dbias = base.clone()
+    dq, dk, dv = binding.gdpa_block_bwd(c["q"], c["qo"], c["k"], c["v"], c["do"], dbias=dbias, **kw)
+    assert binding.device_status() == 0
+    for got, (_, want) in zip((dq, dk, dv), bufs):
+        assert torch.equal(got, want), f"{what}: the gradient call changed dq / dk / dv"
+    check_dense_gradient(c, dbias, base, what + " dbias")
+
+
+def test_dense_bias_block_bad_offsets_are_reported():
+    """A dense bias whose per-sample sizes are not H * L_b^2 is refused on the
+    device by the block kernels too: GDPA_ERR_BAD_OFFSETS, nothing written."""
+    c = _case(BLOCK_LENS, BLOCK_LENS, 2, 64, "softmax", False, seed=80, block=BLOCK)
+    bad = c["off"].clone()
+    bad[3] += 1  # samples 2 and 3 no longer hold H * L^2 values
+    out = torch.zeros_like(c["q"])
+    binding.gdpa_block_fwd(c["q"], c["qo"], c["k"], c["v"], act=c["act"], scale=c["scale"],
+                           bias=(c["vals"], bad), out=out)
+    assert binding.device_status() == 6   # GDPA_ERR_BAD_OFFSETS
+    assert torch.all(out == 0)

@@ -190,6 +190,37 @@ def test_mxfp8_fwd_empty_keys():
     _mx_case([3, 0, 130, 5], [0, 9, 0, 140], 2)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_mxfp8_fwd_dense_bias(causal):
+    """The MXFP8 forward with a dense jagged bias (fp32 values added to the
+    fp32 scores): against the oracle on the decoded operands at the MXFP8
+    tolerance, and against the exact forward on the unquantised inputs within
+    the edge-case budget."""
+    lq = [1, 31, 96, 97, 200, 0, 300, 129]
+    lkv = lq if causal else [7, 32, 1, 96, 128, 5, 191, 300]
+    H, d = 2, 128
+    g = torch.Generator(device=DEV).manual_seed(11 + causal)
+    q = rand_bf16((sum(lq), H, d), g, DEV)
+    k = rand_bf16((sum(lkv), H, d), g, DEV)
+    v = rand_bf16((sum(lkv), H, d), g, DEV)
+    qo_np, ko_np = offsets(lq), offsets(lkv)
+    qo, ko = torch.from_numpy(qo_np).to(DEV), torch.from_numpy(ko_np).to(DEV)
+    off_np = oracle.dense_bias_offsets(qo_np, ko_np, H)
+    vals = torch.randn(int(off_np[-1]), generator=g, device=DEV) * 0.5
+    scale = 1.0 / np.sqrt(d)
+    out, lse = _mx_fwd(q, qo, k, v, ko, causal, scale, bias=(vals, torch.from_numpy(off_np).to(DEV)))
+    qn, kn, vn = to_np(q), to_np(k), to_np(v)
+    kw = dict(act=0, causal=causal, scale=scale, dense_bias=vals.double().cpu().numpy())
+    ro, rl = oracle.fwd(oracle.dequant_rows(qn, nosat=True), qo_np,
+                        oracle.dequant_rows(kn, nosat=True),
+                        oracle.dequant_cols(vn, ko_np, nosat=True), ko_np, **kw)
+    got = to_np(out)
+    assert_close(got, ro, MXFP8_TOL, f"mxfp8 dense causal={causal} out")
+    assert_close(lse.cpu().double().numpy(), rl, MXFP8_TOL, f"mxfp8 dense causal={causal} lse")
+    ex, _ = oracle.fwd(qn, qo_np, kn, vn, ko_np, **kw)
+    _assert_exact([(got, ex)], f"mxfp8 dense causal={causal}", *EDGE_BUDGET)
+
+
 def test_mxfp8_rejects_gdpa_and_d64():
     lib = binding.load()
     p = torch.zeros(64, device=DEV, dtype=torch.uint8).data_ptr()

@@ -482,7 +482,8 @@ void oracle_quant_cols(const double* x, const int32_t* offs, int B, int H, int d
  * element block along either axis, so one rounding serves the dK product,
  * whose contraction runs over queries, and the dQ product, over keys).
  *
- *   s_ij  = scale <qd_i, kd_j> + bias(i - j)      qd, kd: along channels
+ *   s_ij  = scale <qd_i, kd_j> + bias_ij          qd, kd: along channels
+ *           (bias_ij: the table's bias(i - j), or a dense bias's value)
  *   p_ij  = exp(s_ij - lse_i)  (0 when masked)    lse: the forward's, given
  *   dp_ij = <dOd_i, vd_j>                         dOd, vd: along channels
  *   ds_ij = p_ij (dp_ij - delta_i)                delta_i = <dO_i, O_i>, given
@@ -533,9 +534,11 @@ int oracle_bwd_mx(const double* qd, const double* qt, const double* kd, const do
                   const double* vd, const double* dod, const double* dot_t, const int32_t* qo,
                   const int32_t* ko, int B, int H, int d, const double* bias, int max_rel,
                   int causal, int window, double scale, const double* lse, const double* delta,
-                  int round_ps, double* dq, double* dk, double* dv) {
+                  int round_ps, double* dq, double* dk, double* dv, const double* dense,
+                  const int64_t* doff) {
   if (B < 0 || H <= 0 || d <= 0 || window < 0) return -1;
   if (!check_offsets(qo, B) || !check_offsets(ko, B)) return -1;
+  if (!check_dense(dense, doff, qo, ko, B, H)) return -1;
   if (causal || window > 0)
     for (int b = 0; b < B; ++b)
       if (qo[b + 1] - qo[b] != ko[b + 1] - ko[b]) return -1;
@@ -566,7 +569,7 @@ int oracle_bwd_mx(const double* qd, const double* qt, const double* kd, const do
         if (causal && j > i) continue;
         if (window > 0 && (j <= i - window || j >= i + window)) continue;
         const double s = scale * dot(qi, kd + ((k0 + j) * H + h) * (long)d, d) +
-                         bias_at(bias, max_rel, h, i, j);
+                         bias_value(bias, max_rel, dense, doff, b, h, Lq, Lkv, i, j);
         const double p = exp(s - l);
         const double dp = dot(doi, vd + ((k0 + j) * H + h) * (long)d, d);
         P[j * Lq + i] = p;

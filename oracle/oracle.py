@@ -68,7 +68,7 @@ def _load():
         lib.oracle_round_blocks_2d.argtypes = [dp, ctypes.c_long, ctypes.c_long]
         lib.oracle_round_blocks_2d.restype = None
         lib.oracle_bwd_mx.argtypes = [dp, dp, dp, dp, dp, dp, dp, ip, ip, I, I, I, dp, I, I, I, D,
-                                      dp, dp, I, dp, dp, dp]
+                                      dp, dp, I, dp, dp, dp, dp, lp]
         lib.oracle_bwd_mx.restype = I
         _lib = lib
         return lib
@@ -276,12 +276,13 @@ def dequant_cols(x, offsets, nosat: bool = False):
 
 def bwd_mx_operands(qd, qt, kd, kt, vd, dod, dot, q_offsets, kv_offsets, lse, delta, *,
                     causal: bool = False, scale: float, bias=None, max_rel: int = 0,
-                    window: int = 0, round_ps: bool = True):
+                    window: int = 0, round_ps: bool = True, dense_bias=None):
     """Softmax backward with each product on its own operand version (the
     definition at the MXFP8 backward section of gdpa_oracle.c): qd, kd, vd, dod
     feed the channel contractions (S, dP), qt, kt, dot the token contractions
     (dK, dQ, dV); lse and delta [H, Tq] are given.  P and dS are rounded to
-    E4M3 in 32 x 32 blocks when round_ps.  Returns (dq, dk, dv) float64."""
+    E4M3 in 32 x 32 blocks when round_ps.  dense_bias (in the layout of
+    dense_bias_offsets) replaces the table.  Returns (dq, dk, dv) float64."""
     arrs = [_f64(a) for a in (qd, qt, kd, kt, vd, dod, dot)]
     qo, ko = _i32(q_offsets), _i32(kv_offsets)
     Tq, H, d = arrs[0].shape
@@ -292,21 +293,22 @@ def bwd_mx_operands(qd, qt, kd, kt, vd, dod, dot, q_offsets, kv_offsets, lse, de
     dk = np.zeros(arrs[2].shape)
     dv = np.zeros(arrs[2].shape)
     keep, bp = _bias_arg(bias, H, max_rel)
+    keep_d, dp_, op_ = _dense_arg(dense_bias, qo, ko, H)
     rc = _load().oracle_bwd_mx(*[_p(a, ctypes.c_double) for a in arrs], _p(qo, ctypes.c_int32),
                                _p(ko, ctypes.c_int32), B, H, d, bp, int(max_rel),
                                int(bool(causal)), int(window), float(scale),
                                _p(lse_a, ctypes.c_double),
                                _p(delta_a, ctypes.c_double), int(bool(round_ps)),
                                _p(dq, ctypes.c_double), _p(dk, ctypes.c_double),
-                               _p(dv, ctypes.c_double))
+                               _p(dv, ctypes.c_double), dp_, op_)
     if rc != 0:
         raise ValueError("oracle_bwd_mx rejected its arguments")
-    del keep
+    del keep, keep_d
     return dq, dk, dv
 
 
 def bwd_mxfp8(q, q_offsets, k, v, kv_offsets, out, dout, lse, *, causal: bool = False,
-              scale: float, bias=None, max_rel: int = 0, window: int = 0):
+              scale: float, bias=None, max_rel: int = 0, window: int = 0, dense_bias=None):
     """The MXFP8 softmax backward on bf16 inputs: Q, K, dO quantised along
     channels and along tokens, V along channels (quant_rows / quant_cols,
     decoded), delta = rowsum(dO * O) of the given values, P and dS rounded in
@@ -317,7 +319,8 @@ def bwd_mxfp8(q, q_offsets, k, v, kv_offsets, out, dout, lse, *, causal: bool = 
     return bwd_mx_operands(dequant_rows(q), dequant_cols(q, qo), dequant_rows(k),
                            dequant_cols(k, ko), dequant_rows(v), dequant_rows(dout),
                            dequant_cols(dout, qo), qo, ko, lse, delta, causal=causal,
-                           scale=scale, bias=bias, max_rel=max_rel, window=window, round_ps=True)
+                           scale=scale, bias=bias, max_rel=max_rel, window=window, round_ps=True,
+                           dense_bias=dense_bias)
 
 
 # ------------------------------------------------------------------ rotary embedding

@@ -939,6 +939,36 @@ def test_bwd_mx_operands_reduce_to_the_backward(oracle_mod, causal, with_bias):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+def test_bwd_mx_operands_dense_bias_reduces_to_the_backward(oracle_mod, causal):
+    """The same reduction with a dense jagged bias: the MXFP8 backward's
+    definition reads the bias of each pair where the dense backward does (that
+    one pinned by finite differences and by torch's SDPA with the bias as a
+    mask); a transposed or shifted index fails it."""
+    lq = [5, 0, 37, 70, 1] if causal else [5, 3, 37, 70, 0]
+    lkv = lq if causal else [9, 0, 33, 64, 4]
+    H, d = 2, 8
+    qo, ko = _offsets(lq), _offsets(lkv)
+    q = _bf16_randn((sum(lq), H, d), 21)
+    k = _bf16_randn((sum(lkv), H, d), 22)
+    v = _bf16_randn((sum(lkv), H, d), 23)
+    do = _bf16_randn((sum(lq), H, d), 24)
+    off = oracle_mod.dense_bias_offsets(qo, ko, H)
+    dense = np.random.default_rng(5).normal(0, 1.0, int(off[-1]))
+    kw = dict(causal=causal, scale=1.0 / math.sqrt(d), dense_bias=dense)
+    out, lse = oracle_mod.fwd(q, qo, k, v, ko, act=ACT_SOFTMAX, **kw)
+    delta = np.einsum("thc,thc->ht", do, out)
+    got = oracle_mod.bwd_mx_operands(q, q, k, k, v, do, do, qo, ko, lse, delta, round_ps=False,
+                                     **kw)
+    ref = oracle_mod.bwd(q, qo, k, v, ko, do, act=ACT_SOFTMAX, **kw)
+    for g, r in zip(got, ref):
+        np.testing.assert_allclose(g, r, rtol=1e-10, atol=1e-12)
+    # the bias matters here: without it the result moves well past the tolerance
+    plain = oracle_mod.bwd(q, qo, k, v, ko, do, act=ACT_SOFTMAX, causal=causal,
+                           scale=1.0 / math.sqrt(d))
+    assert max(np.abs(g - r).max() for g, r in zip(got, plain)) > 1e-3
+
+
+@pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("window", [1, 5, 40])
 def test_bwd_mx_operands_window_reduces_to_the_windowed_backward(oracle_mod, window, causal):
     """The same reduction with a sliding window: the mask matches the windowed

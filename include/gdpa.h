@@ -89,8 +89,8 @@ typedef enum { GDPA_BIAS_NONE = 0, GDPA_BIAS_RELPOS = 1, GDPA_BIAS_DENSE = 2 } g
  * gdpa_fwd_noalloc, gdpa_fwd_window and gdpa_bwd_window / gdpa_bwd_rope
  * (these two also return its gradient), with or without a sliding window, by
  * gdpa_block_fwd / gdpa_block_bwd / gdpa_block_bwd_dbias (the last with its
- * gradient) and by gdpa_fwd_mxfp8(_window); the MXFP8 backward entry points
- * give GDPA_ERR_UNSUPPORTED. */
+ * gradient), by gdpa_fwd_mxfp8(_window) and by gdpa_bwd_mxfp8(_window,
+ * _rope) (the last with its gradient). */
 typedef struct {
   int kind;                /* gdpa_bias_kind */
   const float* table;      /* device pointer, ignored for GDPA_BIAS_NONE */
@@ -344,11 +344,13 @@ gdpa_status gdpa_bwd_mxfp8_window(const void* q, const int32_t* q_offsets, const
 /* gdpa_bwd_mxfp8_window with the rotary-embedding backward (rope_base > 0:
  * dq, dk returned for the un-rotated q, k, as in gdpa_bwd_rope: dK rotated in
  * the kernel's epilogue, dQ in the accumulator's conversion; 0: none;
- * negative, infinite or NaN: GDPA_ERR_INVALID_ARG) and the gradient of a
- * relative-position table (dbias: fp32 [H][2*max_rel-1], added to, from the
- * fp32 dS before its E4M3 rounding; NULL: not computed; without a
- * GDPA_BIAS_RELPOS bias or not 4-byte aligned: GDPA_ERR_INVALID_ARG).  Every
- * other argument, output and error is that of gdpa_bwd_mxfp8_window. */
+ * negative, infinite or NaN: GDPA_ERR_INVALID_ARG) and the gradient of the
+ * bias (dbias, fp32, added to, from the fp32 dS before its E4M3 rounding: a
+ * relative-position table's [H][2*max_rel-1] as in gdpa_bwd_window, or a
+ * dense bias's own layout, each unmasked pair's entry receiving its dS;
+ * NULL: not computed; without a bias or not 4-byte aligned:
+ * GDPA_ERR_INVALID_ARG).  Every other argument, output and error is that of
+ * gdpa_bwd_mxfp8_window. */
 gdpa_status gdpa_bwd_mxfp8_rope(const void* q, const int32_t* q_offsets, const void* k,
                                 const void* v, const int32_t* kv_offsets, int B, int H, int d,
                                 int64_t Tq, int64_t Tkv, const gdpa_bias* bias, int act, int causal,

@@ -260,9 +260,10 @@ def gdpa_bwd_mxfp8(q, q_offsets, k, v, kv_offsets, out, lse, dout, *, causal=Fal
                    bias=None, max_rel=0, window=0, dq=None, dk=None, dv=None, dbias=None,
                    rope_base=0.0, workspace=None, stream=None):
     """MXFP8 backward through the C ABI (gdpa_bwd_mxfp8, gdpa_bwd_mxfp8_window
-    when window > 0, gdpa_bwd_mxfp8_rope when rope_base > 0 or a bias-table
-    gradient `dbias` is given, which is added to) on the bf16 tensors of
-    gdpa_bwd, softmax, d = 128.  Returns (dq, dk, dv)."""
+    when window > 0, gdpa_bwd_mxfp8_rope when rope_base > 0 or the bias's
+    gradient `dbias` is given, which is added to: the table's layout or a
+    dense bias's) on the bf16 tensors of gdpa_bwd, softmax, d = 128.  Returns
+    (dq, dk, dv)."""
     lib = load()
     Tq, H, d = q.shape
     Tkv = k.shape[0]

@@ -843,9 +843,9 @@ gdpa_status gdpa_bwd_mxfp8_rope(const void* q, const int32_t* q_offsets, const v
   gdpa_status st = check_common(q, q_offsets, k, v, kv_offsets, B, H, d, Tq, Tkv, bias, act,
                                 causal, window);
   if (st != GDPA_OK) return st;
-  if (d != 128 || act != GDPA_ACT_SOFTMAX || is_dense(bias)) return GDPA_ERR_UNSUPPORTED;
-  if (dbias != nullptr) {  // the gradient of a relative-position table needs that table
-    if (bias_kind(bias) != GDPA_BIAS_RELPOS) return GDPA_ERR_INVALID_ARG;
+  if (d != 128 || act != GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
+  if (dbias != nullptr) {  // the gradient of a bias needs that bias (a table or a dense bias)
+    if (bias_kind(bias) == GDPA_BIAS_NONE) return GDPA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(dbias) & 3u) return GDPA_ERR_INVALID_ARG;
   }
   if (Tq > 0 && (dout == nullptr || dq == nullptr || out == nullptr || lse == nullptr ||
@@ -901,8 +901,9 @@ gdpa_status gdpa_bwd_mxfp8_rope(const void* q, const int32_t* q_offsets, const v
   int* n_items = reinterpret_cast<int*>(ws);
   int* ticket = reinterpret_cast<int*>(ws + 4);
   int2* items = reinterpret_cast<int2*>(ws + lay.items);
+  const int64_t* dense_off = is_dense(bias) ? bias->offsets : nullptr;
   if (launch_build_worklist(kv_offsets, q_offsets, B, H, Tkv, Tq, causal, window, 1, items,
-                            n_items, ticket, dev->status, s) != cudaSuccess)
+                            n_items, ticket, dev->status, s, dense_off) != cudaSuccess)
     return GDPA_ERR_CUDA;
   ++t_launches;
 
@@ -918,6 +919,8 @@ gdpa_status gdpa_bwd_mxfp8_rope(const void* q, const int32_t* q_offsets, const v
   p.Tkv = Tkv;
   p.bias_table = table;
   p.max_rel = max_rel;
+  p.bias_dense = dense_off != nullptr ? bias->table : nullptr;
+  p.bias_off = dense_off;
   p.causal = causal;
   p.window = window;
   p.scale = scale;

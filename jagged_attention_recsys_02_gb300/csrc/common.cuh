@@ -381,6 +381,9 @@ struct BwdMxOperands {
 // maps: qd, qt, dod, dot (64-row boxes), kd, kt, vd (128-row boxes), dq (fp32, 16-row boxes)
 cudaError_t launch_bwd_mx(const BwdParams& p, const BwdMxOperands& mx, const CUtensorMap* maps,
                           int grid, cudaStream_t s);
+// The dense-bias instantiations of the MXFP8 backward (p.bias_dense set).
+cudaError_t launch_bwd_mx_dense(const BwdParams& p, const BwdMxOperands& mx,
+                                const CUtensorMap* maps, int grid, cudaStream_t s);
 cudaError_t launch_fwd_mx(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
                           const uint8_t* v_sc, long long v_sc_rows, int grid, cudaStream_t s);

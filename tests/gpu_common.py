@@ -198,3 +198,47 @@ def check_table_gradient(q, qo_np, k, v, ko_np, do, bias, dbias, *, act, causal,
     bound = BWD_TOL[0] + BWD_TOL[1] * np.abs(ref) + 4 * err
     assert np.all(np.abs(got - ref) <= bound), \
         f"{what}: worst err/bound {float((np.abs(got - ref) / bound).max()):.3f}"
+
+
+def dense_ref_kw(c):
+    """Oracle keyword arguments of a dense-bias case: a dict with act, causal,
+    scale, window, block and the bias values vals (torch, on any device)."""
+    return dict(act=c["act"], causal=c["causal"], scale=c["scale"], window=c["window"],
+                block=c["block"], dense_bias=c["vals"].double().cpu().numpy())
+
+
+def check_dense_gradient(c, got, base, what):
+    """got = base + the kernel's dS of every unmasked pair, in the dense bias's
+    layout: against the oracle's gradient within the per-pair rounding bound
+    (times 4) plus the fp32 rounding of the addition to base; masked entries
+    keep base bit for bit."""
+    Tq, H, d = c["q"].shape
+    qn, kn, vn, don = to_np(c["q"]), to_np(c["k"]), to_np(c["v"]), to_np(c["do"])
+    *_, ref = oracle.bwd(qn, c["qo_np"], kn, vn, c["ko_np"], don, want_dbias=True, **dense_ref_kw(c))
+    o_ref, _ = oracle.fwd(qn, c["qo_np"], kn, vn, c["ko_np"], **dense_ref_kw(c))
+    vals = c["vals"].double().cpu().numpy()
+    off = oracle.dense_bias_offsets(c["qo_np"], c["ko_np"], H)
+    got = got.cpu()
+    base = base.cpu()
+    live_all = np.zeros(int(off[-1]), bool)
+    pair = np.zeros(int(off[-1]))
+    for b, h, live, e in ds_pair_bounds(qn, c["qo_np"], kn, vn, c["ko_np"], don, o_ref,
+                                        act=c["act"], causal=c["causal"], scale=c["scale"],
+                                        window=c["window"], block=c["block"],
+                                        bias_of=lambda b, h, i, j: vals[
+                                            off[b] + (h * i.shape[0] + i) * j.shape[1] + j]):
+        n = live.size
+        s = slice(int(off[b]) + h * n, int(off[b]) + (h + 1) * n)
+        live_all[s] = live.reshape(-1)
+        pair[s] = e.reshape(-1)
+    assert torch.equal(got[~torch.from_numpy(live_all)], base[~torch.from_numpy(live_all)]), \
+        f"{what}: a masked entry changed"
+    g, b0 = got.double().numpy()[live_all], base.double().numpy()[live_all]
+    r = ref[live_all]
+    bound = 4 * pair[live_all] + 2.0 ** -23 * (np.abs(b0) + np.abs(r)) + 1e-7 * np.abs(r).max()
+    err = np.abs(g - b0 - r)
+    assert np.all(err <= bound), \
+        f"{what}: {int((err > bound).sum())} of {err.size} out, worst err/bound {(err / bound).max():.3f}"
+    # the softmax kernel rounds dS to bf16, the others keep it in fp32: both
+    # sit far inside the bound above; the bound itself is not vacuous
+    assert np.median(bound) < 1e-2 * np.abs(r).max()

@@ -219,7 +219,7 @@ def test_mxfp8_backward_workspace_size(lib):
 
 def test_dense_bias_rejections_on_host(lib):
     """A dense bias needs its values and its int64 offsets (4- and 8-byte
-    aligned); it has no MXFP8 backward."""
+    aligned); every entry point takes it once those are valid."""
     D = binding.BIAS_DENSE
     dense = lambda table=FAKE, off=FAKE + 64: ctypes.byref(binding.gdpa_bias(D, table, 0, off))
     assert _fwd(lib, bias=dense(off=None)) == INVALID
@@ -247,10 +247,10 @@ def test_dense_bias_rejections_on_host(lib):
                                                      dbias, None, 0, None)
     assert blk_bwd(FAKE) == WORKSPACE
     assert blk_bwd(FAKE + 2) == INVALID
-    # the MXFP8 forward takes it too, the MXFP8 backward does not
+    # the MXFP8 forward and backward take it too
     assert lib.gdpa_fwd_mxfp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 10, 10,
                               dense(), 0, 0, 0.125, FAKE, FAKE, None, 0, None) == WORKSPACE
-    assert _bwd_mx(lib, bias=dense()) == UNSUPPORTED
+    assert _bwd_mx(lib, bias=dense(), ws=None) == WORKSPACE
 
 
 def test_rope_backward_rejects_a_bad_base(lib):

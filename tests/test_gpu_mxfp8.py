@@ -87,8 +87,9 @@ def test_quant_full_size_v_and_q():
 
 
 # ------------------------------------------------------------------ MXFP8 forward
-from gpu_common import (MXFP8_TOL, assert_close, check_guards, check_table_gradient, guarded,  # noqa: E402
-                        oracle_fwd_samples, rand_bf16)
+from gpu_common import (MXFP8_TOL, assert_close, check_dense_gradient, check_guards,  # noqa: E402
+                        check_table_gradient, dense_ref_kw, guarded, oracle_fwd_samples,
+                        rand_bf16)
 from jagged_attention_recsys_02_gb300.workloads import make_tensors, make_workload  # noqa: E402
 
 
@@ -409,6 +410,52 @@ def test_mxfp8_bwd_table_gradient(causal):
                            max_rel=max_rel)
     for name, got, r in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
         assert_close(to_np(got), r, MXBWD_TOL, f"mxfp8 bwd with dbias {name}")
+
+
+@pytest.mark.parametrize("window", [0, 100])
+@pytest.mark.parametrize("causal", [False, True])
+def test_mxfp8_bwd_dense_bias(causal, window):
+    """The MXFP8 backward with a dense jagged bias: dq, dk, dv against the
+    oracle's MXFP8 backward with that bias on random bf16 inputs (with and
+    without a sliding window); then on inputs the quantisers hold exactly, the
+    dense bias's gradient (dbias, from the fp32 dS) against the unquantised
+    oracle's within the per-pair bounds, masked entries untouched."""
+    L = [1, 64, 65, 130, 300, 0, 257]
+    lkv = L if (causal or window) else [7, 1, 128, 129, 200, 3, 300]
+    H, d = 2, 128
+    g = torch.Generator(device=DEV).manual_seed(29 + causal + window)
+    qo_np, ko_np = offsets(L), offsets(lkv)
+    qo, ko = torch.from_numpy(qo_np).to(DEV), torch.from_numpy(ko_np).to(DEV)
+    off_np = oracle.dense_bias_offsets(qo_np, ko_np, H)
+    off = torch.from_numpy(off_np).to(DEV)
+    vals = torch.randn(int(off_np[-1]), generator=g, device=DEV) * 0.5
+    scale = 1.0 / np.sqrt(d)
+    what = f"mxfp8 dense causal={causal} window={window}"
+    for exact_inputs in (False, True):
+        if exact_inputs:
+            q, do = _e4m3_exact((sum(L), H, d), g), _e4m3_exact((sum(L), H, d), g)
+            k, v = _e4m3_exact((sum(lkv), H, d), g), _e4m3_exact((sum(lkv), H, d), g)
+        else:
+            q, do = rand_bf16((sum(L), H, d), g, DEV), rand_bf16((sum(L), H, d), g, DEV)
+            k, v = rand_bf16((sum(lkv), H, d), g, DEV), rand_bf16((sum(lkv), H, d), g, DEV)
+        c = dict(q=q, k=k, v=v, do=do, qo_np=qo_np, ko_np=ko_np, vals=vals, act=oracle.ACT_SOFTMAX,
+                 causal=causal, scale=scale, window=window, block=0)
+        o_ref, l_ref = oracle.fwd(to_np(q), qo_np, to_np(k), to_np(v), ko_np, **dense_ref_kw(c))
+        out = torch.from_numpy(o_ref).to(DEV).to(torch.bfloat16)
+        lse = torch.from_numpy(np.where(np.isinf(l_ref), 0.0, l_ref)).to(DEV).float()
+        base = torch.randn(vals.numel(), generator=g, device=DEV) if exact_inputs else None
+        dbias = base.clone() if exact_inputs else None
+        dq, dk, dv = binding.gdpa_bwd_mxfp8(q, qo, k, v, ko, out, lse, do, causal=causal,
+                                            scale=scale, bias=(vals, off), window=window,
+                                            dbias=dbias)
+        assert binding.device_status() == 0
+        ref = oracle.bwd_mxfp8(to_np(q), qo_np, to_np(k), to_np(v), ko_np, to_np(out), to_np(do),
+                               lse.cpu().double().numpy(), causal=causal, scale=scale,
+                               window=window, dense_bias=vals.double().cpu().numpy())
+        for name, got, r in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
+            assert_close(to_np(got), r, MXBWD_TOL, f"{what} exact_inputs={exact_inputs} {name}")
+        if exact_inputs:
+            check_dense_gradient(c, dbias, base, what + " dbias")
 
 
 @pytest.mark.parametrize("causal", [False, True])

@@ -259,8 +259,6 @@ def test_bwd_full_heavy_tail(act):
 def test_dbias(act, d, variant):
     """Gradient of the relative-position table against the oracle's; it is
     added to, so a second call doubles it."""
-    if act != "softmax" and variant in ("causal", "clamped"):
-        pytest.skip("covered by the softmax cases and the GDPA full / window cases")
     H = 2
     a = ACTS[act]
     causal = variant in ("causal", "window")

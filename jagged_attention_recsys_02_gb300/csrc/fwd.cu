@@ -514,6 +514,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
       for (int j = j_lo; j < j_hi; ++j) {
         const uint32_t gj = g_item + (j - in.jb);
         prefetch_dense(j + 1);
+        // softmax with a dense bias: the row's 128 values of this key tile (times
+        // log2e; 0 where the row does not see the key) are requested before the
+        // score wait, so that one load latency overlaps the products instead of
+        // one per 32-column chunk
+        float dz[(kDense && kSoftmax) ? kKvRows : 1];
+        if constexpr (kDense && kSoftmax) {
+#pragma unroll
+          for (int i = 0; i < kKvRows; ++i) {
+            const int c = j * kKvRows + i;
+            dz[i] = (drow != nullptr && (!kBand || c >= col_lo) && c < col_lim)
+                        ? __ldg(drow + c) * kLog2e
+                        : 0.0f;
+          }
+        }
         bool okw = mbar_wait(bar(C::kSFull + half), tcount & 1u, abort_flag);
         // the value-tile stage also carries this tile's bias window
         if (has_bias)
@@ -626,15 +640,19 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
               mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             }
           } else {
+            // dense bias: scores plus the values requested before the wait
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int chunk = 0; chunk < 4; ++chunk) {
-              float x[32];
-              load_x(chunk, -INFINITY, x);
+              uint32_t sr[32];
+              tmem_ld32(t_s + chunk * 32, sr);
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
-                xs[chunk * 32 + i] = x[i];
-                m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+                const int c = c0 + chunk * 32 + i;
+                float x = fmaf(__uint_as_float(sr[i]), c_s, dz[chunk * 32 + i]);
+                if (need_mask && ((kBand && c < col_lo) || c >= col_lim)) x = -INFINITY;
+                xs[chunk * 32 + i] = x;
+                m4[i & 3] = fmaxf(m4[i & 3], x);
               }
             }
             mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));

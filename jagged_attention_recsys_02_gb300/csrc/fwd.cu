@@ -520,12 +520,37 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ C
         // one per 32-column chunk
         float dz[(kDense && kSoftmax) ? kKvRows : 1];
         if constexpr (kDense && kSoftmax) {
+          // 16-byte loads from the aligned position at or before the tile's first
+          // column (a load instruction costs one L1 wavefront per row either way,
+          // so four columns per load cut them fourfold), then each lane shifts
+          // its window by its own misalignment sh; a 16-byte group not wholly
+          // inside the row's visible columns is read element by element
+          const int cb = j * kKvRows;
+          const int lo = kBand ? max(col_lo, 0) : 0;
+          const int sh = drow != nullptr ? static_cast<int>((reinterpret_cast<uintptr_t>(drow + cb) >> 2) & 3u) : 0;
+          float w[kKvRows + 4];
+#pragma unroll
+          for (int q = 0; q < kKvRows / 4 + 1; ++q) {
+            const int ca = cb + 4 * q - sh;  // column of the group's first element
+            if (drow != nullptr && ca >= lo && ca + 4 <= col_lim) {
+              const float4 t = __ldg(reinterpret_cast<const float4*>(drow + ca));
+              w[4 * q] = t.x;
+              w[4 * q + 1] = t.y;
+              w[4 * q + 2] = t.z;
+              w[4 * q + 3] = t.w;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int c = ca + e;
+                w[4 * q + e] = (drow != nullptr && c >= lo && c < col_lim) ? __ldg(drow + c) : 0.0f;
+              }
+            }
+          }
 #pragma unroll
           for (int i = 0; i < kKvRows; ++i) {
-            const int c = j * kKvRows + i;
-            dz[i] = (drow != nullptr && (!kBand || c >= col_lo) && c < col_lim)
-                        ? __ldg(drow + c) * kLog2e
-                        : 0.0f;
+            const float t01 = (sh & 1) ? w[i + 1] : w[i];
+            const float t23 = (sh & 1) ? w[i + 3] : w[i + 2];
+            dz[i] = ((sh & 2) ? t23 : t01) * kLog2e;
           }
         }
         bool okw = mbar_wait(bar(C::kSFull + half), tcount & 1u, abort_flag);

@@ -142,6 +142,34 @@ def test_bwd_direct_dq_rows(causal, d, act):
         assert torch.all(dq[z:z + DIRECT_Q[4]] == 0)  # the sample with no key
 
 
+@pytest.mark.parametrize("act", ["silu", "gelu_tanh"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_direct_dq_ignores_a_stale_workspace(d, act):
+    """With the workspace filled with NaN bit patterns the gradients still match
+    the oracle: the direct dQ rows never read the accumulator, and the rows of
+    the samples that reduce into it (more than 128 keys) are zeroed by the
+    helper first."""
+    lq, lkv = DIRECT_Q, DIRECT_KV
+    H = 3
+    g = torch.Generator(device=DEV).manual_seed(9)
+    q = rand_bf16((sum(lq), H, d), g, DEV)
+    k = rand_bf16((sum(lkv), H, d), g, DEV)
+    v = rand_bf16((sum(lkv), H, d), g, DEV)
+    do = rand_bf16((sum(lq), H, d), g, DEV)
+    qo_np, ko_np = offsets(lq), offsets(lkv)
+    qo, ko = torch.from_numpy(qo_np).to(DEV), torch.from_numpy(ko_np).to(DEV)
+    scale = 1.0 / math.sqrt(d)
+    a = ACTS[act]
+    out, lse = binding.gdpa_fwd(q, qo, k, v, ko, act=a, scale=scale)
+    B = len(lq)
+    ws = torch.full((binding.bwd_workspace_size(B, H, d, sum(lq), sum(lkv)),), 0xFF,
+                    dtype=torch.uint8, device=DEV)
+    dq, dk, dv = binding.gdpa_bwd(q, qo, k, v, ko, out, lse, do, act=a, scale=scale, workspace=ws)
+    assert binding.device_status() == 0
+    _check_samples(q, k, v, do, qo_np, ko_np, range(B), act, False, scale, None, 0, dq, dk, dv,
+                   f"stale workspace {act} d={d}")
+
+
 def test_bwd_empty_sides():
     # no keys: dq rows are zero; no queries: dk/dv rows are zero
     dq, dk, dv = _case([3, 0, 130, 5], [0, 9, 0, 140], 2, 128, "softmax")
